@@ -1,0 +1,139 @@
+"""Seeded synthetic inputs for the chunkwise linear-attention forward pass.
+
+This module is shared by the float64 oracle's tests and by the CUDA path's
+tests and benchmark. It holds only input recipes -- shapes, dtypes, value
+distributions and draw order -- and none of the method's arithmetic.
+
+Five workloads stand in for the long-sequence training forward the pages on
+linear attention describe ("Talk Linear Attention", sections 3-6; "Linear
+Attention" glossary, applications list). No public dataset is involved:
+every tensor is drawn from one CPU ``torch.Generator`` seeded per workload,
+in the fixed order q, k, v, g, beta, S0, in float32, and then cast to the
+workload's input dtype. Consumers must use the cast values (the oracle
+upcasts them exactly to float64).
+
+Gate convention: ``g`` holds natural-log gates, so the decay factor applied
+to the state is ``alpha = exp(g)``.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field, replace
+
+import torch
+import torch.nn.functional as F
+
+__all__ = ["Workload", "WORKLOADS", "make_inputs", "MODES"]
+
+# Mode names used throughout the Python side. The C ABI has its own enum;
+# the binding maps these names onto it.
+MODES = ("linear", "elu1", "retnet", "gla", "scalar", "gdn")
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    mode: str
+    B: int
+    H: int
+    T: int
+    dk: int
+    dv: int
+    dtype: str            # "bf16" or "f32": dtype of q, k, v and o
+    C: int                # chunk length the workload is specified with
+    seed: int
+    qkv_scale: float = 1.0
+    l2norm_qk: bool = False
+    s0: bool = False      # random initial state
+    extra: dict = field(default_factory=dict)
+
+    def with_sizes(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+
+WORKLOADS = {
+    # Plain causal linear attention, fp32 inputs.
+    "linear_fp32": Workload("linear_fp32", "linear", 1, 1, 256, 64, 64, "f32", 64,
+                            seed=1, qkv_scale=1.0 / 8.0),
+    # elu(x)+1 kernelised attention with the causal normaliser.
+    "elu1": Workload("elu1", "elu1", 4, 8, 2048, 64, 64, "bf16", 64, seed=2),
+    # RetNet fixed per-head decay gamma_h = 1 - 2^(-5-h).
+    "retnet": Workload("retnet", "retnet", 8, 16, 4096, 128, 128, "bf16", 64, seed=3,
+                       qkv_scale=1.0 / math.sqrt(128.0)),
+    # GLA per-key-channel data-dependent gate, log alpha = logsigmoid(N(0,1))/16.
+    "gla": Workload("gla", "gla", 8, 16, 8192, 128, 128, "bf16", 64, seed=4,
+                    qkv_scale=1.0 / math.sqrt(128.0)),
+    # Gated DeltaNet: L2-normalised q,k; beta = sigmoid(N); alpha = exp(-softplus(N)/8).
+    "gdn": Workload("gdn", "gdn", 4, 16, 16384, 128, 128, "bf16", 64, seed=5,
+                    l2norm_qk=True, s0=True),
+    # Data-dependent scalar decay (the Mamba-2 style update, unit write).
+    # Not one of the five headline workloads; used by parity tests only.
+    "scalar": Workload("scalar", "scalar", 2, 4, 1024, 128, 128, "bf16", 64, seed=6,
+                       qkv_scale=1.0 / math.sqrt(128.0), s0=True),
+}
+
+
+def _normal(gen, shape, scale=1.0):
+    x = torch.randn(*shape, generator=gen, dtype=torch.float32)
+    if scale != 1.0:
+        x.mul_(scale)
+    return x
+
+
+def make_inputs(wl: Workload | str, **sizes) -> dict:
+    """Draw one workload's inputs on the CPU.
+
+    Returns a dict with q, k, v (workload dtype, [B,H,T,d] contiguous),
+    g (float32 or None), beta (float32 or None), S0 (float32 or None), plus
+    the workload itself under "wl". ``sizes`` overrides B, H, T, dk, dv
+    (and optionally seed) while keeping the value distributions.
+    """
+    if isinstance(wl, str):
+        wl = WORKLOADS[wl]
+    if sizes:
+        wl = wl.with_sizes(**sizes)
+    B, H, T, dk, dv = wl.B, wl.H, wl.T, wl.dk, wl.dv
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(wl.seed)
+
+    q = _normal(gen, (B, H, T, dk), wl.qkv_scale)
+    k = _normal(gen, (B, H, T, dk), wl.qkv_scale)
+    v = _normal(gen, (B, H, T, dv), wl.qkv_scale)
+    if wl.l2norm_qk:
+        q = q / q.norm(dim=-1, keepdim=True).clamp_min(1e-6)
+        k = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-6)
+
+    g = None
+    beta = None
+    if wl.mode == "retnet":
+        # gamma_h = 1 - 2^(-5-h), h = 0..H-1; stored as float32 log gamma_h.
+        g = torch.tensor([math.log1p(-(2.0 ** (-5 - h))) for h in range(H)],
+                         dtype=torch.float64).to(torch.float32)
+    elif wl.mode == "gla":
+        g = F.logsigmoid(_normal(gen, (B, H, T, dk))) / 16.0
+    elif wl.mode == "scalar":
+        g = -F.softplus(_normal(gen, (B, H, T))) / 8.0
+    elif wl.mode == "gdn":
+        g = -F.softplus(_normal(gen, (B, H, T))) / 8.0
+        beta = torch.sigmoid(_normal(gen, (B, H, T)))
+        # draw order is q,k,v,g,beta,S0: g above is drawn before beta
+    S0 = None
+    if wl.s0:
+        width = dv + 1 if wl.mode == "elu1" else dv
+        S0 = _normal(gen, (B, H, dk, width), 0.1)  # N(0, 0.01): variance 0.01
+
+    dt = wl.torch_dtype
+    return {
+        "wl": wl,
+        "q": q.to(dt).contiguous(),
+        "k": k.to(dt).contiguous(),
+        "v": v.to(dt).contiguous(),
+        "g": None if g is None else g.contiguous(),
+        "beta": None if beta is None else beta.contiguous(),
+        "S0": None if S0 is None else S0.contiguous(),
+    }
+
