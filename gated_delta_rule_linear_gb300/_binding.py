@@ -1,0 +1,170 @@
+"""ctypes binding of libla.so: the C ABI of include/la.h under the same names.
+
+Argument marshalling only. The raw entry points (``la_chunk_fwd``,
+``la_recurrent_step``, ...) take integers for device pointers exactly like the
+C functions; ``chunk_fwd`` / ``recurrent_step`` accept torch CUDA tensors,
+allocate the outputs and raise ``LAError`` on a non-zero status. Every step of
+the computation runs in the library's CUDA kernels; there is no fallback: if
+the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libla.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "la.h")
+
+
+def _read_constants(path):
+    consts = {}
+    with open(path) as f:
+        for line in f:
+            m = re.match(r"#define\s+(LA_[A-Z0-9_]+)\s+(0x[0-9a-fA-F]+|\d+)", line)
+            if m:
+                consts[m.group(1)] = int(m.group(2), 0)
+    return consts
+
+
+CONSTANTS = _read_constants(HEADER)
+globals().update(CONSTANTS)
+
+MODE_IDS = {
+    "linear": CONSTANTS["LA_LINEAR"],
+    "elu1": CONSTANTS["LA_ELU1_NORM"],
+    "retnet": CONSTANTS["LA_RETNET"],
+    "gla": CONSTANTS["LA_GLA"],
+    "scalar": CONSTANTS["LA_SCALAR_GATE"],
+    "gdn": CONSTANTS["LA_GDN"],
+}
+
+# Every function the header declares, with its ctypes signature.
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+SIGNATURES = {
+    "la_chunk_fwd": ([_P] * 8 + [_I] * 7 + [_P], _I),
+    "la_recurrent_step": ([_P] * 7 + [_I] * 5 + [_P], _I),
+    "la_stream_status": ([_P], _I),
+    "la_last_error": ([], ctypes.c_char_p),
+    "la_version": ([], _I),
+}
+
+
+class LAError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libla.so (once) and bind every declared symbol. Raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libla.so is not built ({path}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    for name, (args, res) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+# ---- raw C entry points (same names and argument order as la.h) -----------
+
+def la_chunk_fwd(q, k, v, g, beta, o, S0, S_final, B, H, T, dk, dv, C, mode, stream):
+    return load_library().la_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(o),
+                                       _ptr(S0), _ptr(S_final), B, H, T, dk, dv, C, mode, stream)
+
+
+def la_recurrent_step(q, k, v, g, beta, o, S, B, H, dk, dv, mode, stream):
+    return load_library().la_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                            _ptr(o), _ptr(S), B, H, dk, dv, mode, stream)
+
+
+def la_stream_status(stream):
+    return load_library().la_stream_status(stream)
+
+
+def la_last_error() -> str:
+    return load_library().la_last_error().decode()
+
+
+def la_version() -> int:
+    return load_library().la_version()
+
+
+# ---- torch-tensor convenience wrappers --------------------------------------
+
+def _mode_id(mode, dtype):
+    import torch
+    mid = MODE_IDS[mode] if isinstance(mode, str) else int(mode)
+    if dtype == torch.float32:
+        mid |= CONSTANTS["LA_F32"]
+    elif dtype != torch.bfloat16:
+        raise TypeError(f"q/k/v must be bfloat16 or float32, got {dtype}")
+    return mid
+
+
+def _check(t, name):
+    if t is not None and (not t.is_cuda or not t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+def _stream_handle(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def chunk_fwd(q, k, v, mode, g=None, beta=None, S0=None, C=0, with_state=True,
+              o=None, S_final=None, stream=None):
+    """Chunkwise causal forward. q, k [B,H,T,dk], v [B,H,T,dv] (bf16 or fp32,
+    CUDA, contiguous). Returns (o, S_final or None)."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("S0", S0)):
+        _check(t, name)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    mid = _mode_id(mode, q.dtype)
+    if o is None:
+        o = torch.empty((B, H, T, dv), dtype=q.dtype, device=q.device)
+    if with_state and S_final is None:
+        W = dv + 1 if (mid & 0xFF) == CONSTANTS["LA_ELU1_NORM"] else dv
+        S_final = torch.empty((B, H, dk, W), dtype=torch.float32, device=q.device)
+    rc = la_chunk_fwd(q, k, v, g, beta, o, S0, S_final if with_state else None,
+                      B, H, T, dk, dv, C, mid, _stream_handle(stream))
+    if rc != 0:
+        raise LAError(rc, la_last_error())
+    return o, (S_final if with_state else None)
+
+
+def recurrent_step(q, k, v, S, mode, g=None, beta=None, o=None, stream=None):
+    """One decode step. q, k [B,H,dk], v [B,H,dv]; S [B,H,dk,W] fp32 updated in place."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("S", S)):
+        _check(t, name)
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    mid = _mode_id(mode, q.dtype)
+    if o is None:
+        o = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
+    rc = la_recurrent_step(q, k, v, g, beta, o, S, B, H, dk, dv, mid, _stream_handle(stream))
+    if rc != 0:
+        raise LAError(rc, la_last_error())
+    return o

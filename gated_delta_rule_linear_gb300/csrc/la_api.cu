@@ -1,0 +1,209 @@
+// Host side of the C ABI declared in include/la.h: argument validation, the
+// per-shape choice of kernel, the thread-local error message and the device
+// status word. Every step of the computation runs in the CUDA kernels; this
+// file only checks arguments and launches them on the caller's stream.
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "la_internal.h"
+
+namespace la {
+
+namespace {
+thread_local char g_err[512] = "";
+
+// Written by kernels only when a bounded device-side wait gives up.
+__device__ unsigned g_status_word;
+
+constexpr int kMaxDevices = 64;
+unsigned *g_status_ptr[kMaxDevices] = {};
+std::mutex g_status_mu;
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+}  // namespace
+
+void set_error(const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
+unsigned *status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  if (!g_status_ptr[dev]) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<unsigned *>(ptr);
+  }
+  return g_status_ptr[dev];
+}
+
+// Host-side kernel choice. bf16 inputs go to the tensor-core kernel when it
+// supports the shape, float32 inputs to the CUDA-core kernel. LA_VARIANT
+// (auto | tc | simt) overrides the choice for measurement sweeps.
+int select_variant(const ChunkParams &p, int *chunk_out) {
+  const char *env = getenv("LA_VARIANT");
+  int want = -1;
+  if (env && strcmp(env, "tc") == 0) want = kVariantTc;
+  if (env && strcmp(env, "simt") == 0) want = kVariantSimt;
+  const int C = p.C == 0 ? 64 : p.C;
+  if (C != 64) {
+    set_error("la_chunk_fwd: chunk length C=%d is not implemented in this build (use 0 or 64)", p.C);
+    return -1;
+  }
+  *chunk_out = C;
+  if (p.f32) return want == kVariantTc ? -2 : kVariantSimt;
+  if (want >= 0) return want;
+  return kVariantSimt;
+}
+
+}  // namespace la
+
+using namespace la;
+
+extern "C" {
+
+const char *la_last_error(void) { return g_err; }
+
+int la_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+int la_stream_status(la_stream_t stream) {
+  g_err[0] = '\0';
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    set_error("la_stream_status: stream synchronisation failed: %s", cudaGetErrorString(e));
+    return LA_ERR_CUDA;
+  }
+  unsigned *w = status_word();
+  if (!w) {
+    set_error("la_stream_status: device status word unavailable");
+    return LA_ERR_CUDA;
+  }
+  unsigned v = 0;
+  if (cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(w, 0, sizeof(v)) != cudaSuccess) {
+    set_error("la_stream_status: reading the status word failed");
+    return LA_ERR_CUDA;
+  }
+  if (v & kStatusTimeout) {
+    set_error("a kernel gave up on a bounded device-side wait (status 0x%x)", v);
+    return LA_ERR_TIMEOUT;
+  }
+  return LA_OK;
+}
+
+static int check_mode(int mode, const float *g, const float *beta, const char *fn) {
+  const int kind = mode & 0xff;
+  if ((mode & ~(0xff | LA_F32)) != 0 || kind < LA_LINEAR || kind > LA_GDN) {
+    set_error("%s: unknown mode 0x%x", fn, mode);
+    return LA_ERR_INVALID_ARG;
+  }
+  const bool needs_g = kind == LA_RETNET || kind == LA_GLA || kind == LA_SCALAR_GATE;
+  const bool takes_g = needs_g || kind == LA_GDN;
+  if (needs_g && !g) {
+    set_error("%s: mode %d needs log-gates g", fn, kind);
+    return LA_ERR_INVALID_ARG;
+  }
+  if (!takes_g && g) {
+    set_error("%s: mode %d takes no gates (g must be NULL)", fn, kind);
+    return LA_ERR_INVALID_ARG;
+  }
+  if (kind != LA_GDN && beta) {
+    set_error("%s: beta is only used by LA_GDN (must be NULL for mode %d)", fn, kind);
+    return LA_ERR_INVALID_ARG;
+  }
+  return LA_OK;
+}
+
+int la_chunk_fwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                 void *o, const float *S0, float *S_final, int B, int H, int T, int dk, int dv,
+                 int C, int mode, la_stream_t stream) {
+  g_err[0] = '\0';
+  const char *fn = "la_chunk_fwd";
+  if (!q || !k || !v || !o) {
+    set_error("%s: q, k, v and o are required", fn);
+    return LA_ERR_INVALID_ARG;
+  }
+  if (B < 1 || H < 1 || T < 1) {
+    set_error("%s: B, H and T must be >= 1 (got %d, %d, %d)", fn, B, H, T);
+    return LA_ERR_INVALID_ARG;
+  }
+  if ((long long)B * H > 0x7fffffffLL) {
+    set_error("%s: B*H too large", fn);
+    return LA_ERR_INVALID_ARG;
+  }
+  if ((dk != 64 && dk != 128) || (dv != 64 && dv != 128)) {
+    set_error("%s: dk and dv must be 64 or 128 (got %d, %d)", fn, dk, dv);
+    return LA_ERR_UNSUPPORTED;
+  }
+  if (C != 0 && C != 64 && C != 128) {
+    set_error("%s: C must be 0, 64 or 128 (got %d)", fn, C);
+    return LA_ERR_INVALID_ARG;
+  }
+  int rc = check_mode(mode, g, beta, fn);
+  if (rc) return rc;
+  const int kind = mode & 0xff;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16)) {
+    set_error("%s: q, k, v and o must be 16-byte aligned", fn);
+    return LA_ERR_INVALID_ARG;
+  }
+  if ((g && !aligned(g, kind == LA_GLA ? 16 : 4)) || (beta && !aligned(beta, 4)) ||
+      (S0 && !aligned(S0, 4)) || (S_final && !aligned(S_final, 4))) {
+    set_error("%s: g (16 bytes for LA_GLA), beta, S0 and S_final must be aligned", fn);
+    return LA_ERR_INVALID_ARG;
+  }
+
+  ChunkParams p{q, k, v, g, beta, o, S0, S_final, B, H, T, dk, dv, C, kind,
+                (mode & LA_F32) ? 1 : 0, status_word()};
+  if (!p.status) {
+    set_error("%s: no CUDA device available (%s)", fn, cudaGetErrorString(cudaGetLastError()));
+    return LA_ERR_CUDA;
+  }
+  int chunk = 64;
+  const int variant = select_variant(p, &chunk);
+  if (variant == -2) {
+    set_error("%s: the tensor-core kernel takes bfloat16 inputs only", fn);
+    return LA_ERR_UNSUPPORTED;
+  }
+  if (variant < 0) return LA_ERR_UNSUPPORTED;
+  p.C = chunk;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return variant == kVariantTc ? launch_chunk_tc(p, s) : launch_chunk_simt(p, s);
+}
+
+int la_recurrent_step(const void *q, const void *k, const void *v, const float *g,
+                      const float *beta, void *o, float *S, int B, int H, int dk, int dv, int mode,
+                      la_stream_t stream) {
+  g_err[0] = '\0';
+  const char *fn = "la_recurrent_step";
+  if (!q || !k || !v || !o || !S) {
+    set_error("%s: q, k, v, o and S are required", fn);
+    return LA_ERR_INVALID_ARG;
+  }
+  if (B < 1 || H < 1 || (long long)B * H > 0x7fffffffLL) {
+    set_error("%s: B and H must be >= 1 (got %d, %d)", fn, B, H);
+    return LA_ERR_INVALID_ARG;
+  }
+  if ((dk != 64 && dk != 128) || (dv != 64 && dv != 128)) {
+    set_error("%s: dk and dv must be 64 or 128 (got %d, %d)", fn, dk, dv);
+    return LA_ERR_UNSUPPORTED;
+  }
+  int rc = check_mode(mode, g, beta, fn);
+  if (rc) return rc;
+  const size_t el = (mode & LA_F32) ? 4 : 2;
+  if (!aligned(q, el) || !aligned(k, el) || !aligned(v, el) || !aligned(o, el) ||
+      !aligned(S, 4) || (g && !aligned(g, 4)) || (beta && !aligned(beta, 4))) {
+    set_error("%s: pointers must be aligned to their element size", fn);
+    return LA_ERR_INVALID_ARG;
+  }
+  StepParams p{q, k, v, g, beta, o, S, B, H, dk, dv, mode & 0xff, (mode & LA_F32) ? 1 : 0};
+  return launch_step(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

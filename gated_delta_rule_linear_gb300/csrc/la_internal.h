@@ -1,0 +1,64 @@
+// Internal declarations shared by the host entry points and the kernels of
+// libla.so. Nothing here is part of the public ABI (include/la.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/la.h"
+
+namespace la {
+
+enum Kind : int {
+  kLinear = LA_LINEAR,
+  kElu1 = LA_ELU1_NORM,
+  kRetnet = LA_RETNET,
+  kGla = LA_GLA,
+  kScalar = LA_SCALAR_GATE,
+  kGdn = LA_GDN,
+};
+
+// Bits of the device status word (one per device, see la_status.cu).
+enum StatusBits : unsigned {
+  kStatusTimeout = 1u,
+};
+
+// Everything a chunk-forward kernel needs, by value.
+struct ChunkParams {
+  const void *q, *k, *v;
+  const float *g, *beta;
+  void *o;
+  const float *S0;
+  float *S_final;
+  int B, H, T, dk, dv, C;
+  int kind;
+  int f32;          // 1: q/k/v/o are float32, 0: bfloat16
+  unsigned *status; // device status word
+};
+
+struct StepParams {
+  const void *q, *k, *v;
+  const float *g, *beta;
+  void *o;
+  float *S;
+  int B, H, dk, dv;
+  int kind;
+  int f32;
+};
+
+// Thread-local error message for la_last_error().
+void set_error(const char *fmt, ...);
+
+// Device status word of the current device (a __device__ variable).
+unsigned *status_word();
+
+// Launchers: return LA_OK or an LA_ERR_* code (message already set).
+int launch_chunk_simt(const ChunkParams &p, cudaStream_t stream);
+int launch_chunk_tc(const ChunkParams &p, cudaStream_t stream);
+int launch_step(const StepParams &p, cudaStream_t stream);
+
+// Which chunk-forward kernel a shape goes to (host-side selection).
+enum Variant : int { kVariantSimt = 0, kVariantTc = 1 };
+int select_variant(const ChunkParams &p, int *chunk_out);
+
+}  // namespace la

@@ -1,0 +1,140 @@
+/*
+ * la.h -- C ABI of the chunkwise linear-attention forward library (libla.so)
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The library computes, for every batch entry b and head h independently,
+ * the causal forward pass of the matrix-state recurrence
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T ,
+ *     o_t = S_t^T q_t ,
+ *
+ * and its special cases, with S key-major ([dk][dv], float32). The pages this
+ * follows state the same recurrence value-major (S = sum v k^T, o = S q;
+ * "Talk Linear Attention" section 6; "LLM attention optimisation: linear
+ * attention", DeltaNet and Gated DeltaNet sections); the key-major state here
+ * is its transpose and gives the same o. The sequence is processed in chunks
+ * of C tokens ("Talk Linear Attention" section 3.2: local attention inside a
+ * chunk, state passing between chunks); the result equals the token-by-token
+ * recurrence up to floating-point rounding.
+ *
+ * Conventions for every entry point
+ *   - Tensors are dense row-major: q, k [B][H][T][dk], v, o [B][H][T][dv]
+ *     (d fastest). Decode steps drop the T axis.
+ *   - q, k, v and o share one dtype: bfloat16 by default, float32 when the
+ *     LA_F32 flag is set in `mode`. All arithmetic accumulates in float32.
+ *   - Gates g are natural logarithms: the decay applied is alpha = exp(g).
+ *   - The state is float32 [B][H][dk][W] with W = dv, except for
+ *     LA_ELU1_NORM where W = dv + 1 and column dv holds the normaliser z.
+ *   - All pointers are DEVICE pointers owned by the caller. The library never
+ *     frees or retains them and allocates no device memory of its own.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream);
+ *     nothing synchronises with the host.
+ *   - Return value: LA_OK, or an LA_ERR_* code with a message available from
+ *     la_last_error() (thread-local). Argument errors are detected on the host
+ *     before anything is launched; nothing is written in that case.
+ */
+#ifndef LA_H
+#define LA_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same underlying type as cudaStream_t / CUstream: pass either directly. */
+struct CUstream_st;
+typedef struct CUstream_st *la_stream_t;
+
+/* ---- status codes ------------------------------------------------------ */
+#define LA_OK                0
+#define LA_ERR_INVALID_ARG   1  /* null required pointer, bad size, misalignment, g/beta vs mode */
+#define LA_ERR_UNSUPPORTED   2  /* valid request this build does not implement (dims, C, dtype) */
+#define LA_ERR_CUDA          3  /* a CUDA runtime/driver call or launch failed */
+#define LA_ERR_TIMEOUT       4  /* a kernel gave up waiting on a device barrier (see la_stream_status) */
+
+/* ---- modes (low byte) and flags ---------------------------------------- */
+/* Plain causal linear attention: S_t = S_{t-1} + k_t v_t^T, o_t = S_t^T q_t.
+ * ("Talk Linear Attention", section 2.1.) g and beta must be NULL. */
+#define LA_LINEAR        0
+/* Kernelised attention phi(x) = elu(x) + 1 with the causal normaliser:
+ * S_t = S_{t-1} + phi(k_t) v_t^T, z_t = z_{t-1} + phi(k_t),
+ * o_t = S_t^T phi(q_t) / (z_t . phi(q_t)).  (Kernel-attention notes,
+ * sections 13-14; "Linear Attention" glossary.) g and beta must be NULL.
+ * The library applies phi; the state has dv + 1 columns (z in column dv). */
+#define LA_ELU1_NORM     1
+/* Fixed per-head decay (RetNet): S_t = gamma_h S_{t-1} + k_t v_t^T.
+ * g = float32 [H] holding log gamma_h. beta must be NULL. */
+#define LA_RETNET        2
+/* GLA diagonal gate on the key axis: S_t = Diag(alpha_t) S_{t-1} + k_t v_t^T
+ * ("Talk Linear Attention", section 5.1). g = float32 [B][H][T][dk]
+ * (per step [B][H][dk]), 16-byte aligned. beta must be NULL. Chunked
+ * evaluation factors exp(b_r - b_s) per channel around the chunk midpoint;
+ * a cumulative log-gate magnitude above ~80 within half a chunk underflows. */
+#define LA_GLA           3
+/* Data-dependent scalar decay (Mamba-2 form): S_t = alpha_t S_{t-1} + k_t v_t^T.
+ * g = float32 [B][H][T] (per step [B][H]). beta must be NULL. */
+#define LA_SCALAR_GATE   4
+/* Gated DeltaNet: decay, then the delta rule,
+ * S_t = (I - beta_t k_t k_t^T) alpha_t S_{t-1} + beta_t k_t v_t^T
+ * ("LLM attention optimisation", Gated DeltaNet section; "Talk Linear
+ * Attention" section 6.2). g = float32 [B][H][T] or NULL (alpha = 1, plain
+ * DeltaNet); beta = float32 [B][H][T] or NULL (beta = 1). */
+#define LA_GDN           5
+/* Flag: q, k, v and o are float32 instead of bfloat16. */
+#define LA_F32           0x100
+
+/*
+ * la_chunk_fwd -- causal forward pass over a whole sequence, chunkwise.
+ *
+ *   q, k    [B][H][T][dk]  input dtype, 16-byte aligned
+ *   v       [B][H][T][dv]  input dtype, 16-byte aligned
+ *   g       float32, shape per mode (see the mode list), or NULL
+ *   beta    float32 [B][H][T] (LA_GDN only) or NULL
+ *   o       [B][H][T][dv]  output, input dtype, 16-byte aligned; written
+ *   S0      float32 [B][H][dk][W] initial state, or NULL for zero
+ *   S_final float32 [B][H][dk][W] final state, or NULL to skip writing it
+ *           (may alias S0: every head reads its S0 before writing S_final)
+ *   B, H, T >= 1; dk, dv in {64, 128}
+ *   C       chunk length: 0 (pick per shape), 64 or 128
+ *   mode    one LA_* mode, optionally | LA_F32
+ *
+ * S_final of one call passed as S0 of the next continues the sequence
+ * (the recurrent state is the whole checkpoint).
+ */
+int la_chunk_fwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                 void *o, const float *S0, float *S_final,
+                 int B, int H, int T, int dk, int dv, int C, int mode, la_stream_t stream);
+
+/*
+ * la_recurrent_step -- one decode step (the recurrent form, "Talk Linear
+ * Attention" section 2.1; kernel-attention notes section 14): for every
+ * (b, h), apply the mode's update with this token and write o = S^T q
+ * (divided by z . phi(q) for LA_ELU1_NORM).
+ *
+ *   q, k [B][H][dk]; v, o [B][H][dv] (input dtype, 4-byte aligned)
+ *   g    LA_RETNET [H]; LA_GLA [B][H][dk]; LA_SCALAR_GATE / LA_GDN [B][H]
+ *   beta LA_GDN [B][H] or NULL
+ *   S    float32 [B][H][dk][W], updated in place
+ */
+int la_recurrent_step(const void *q, const void *k, const void *v, const float *g,
+                      const float *beta, void *o, float *S,
+                      int B, int H, int dk, int dv, int mode, la_stream_t stream);
+
+/*
+ * la_stream_status -- synchronise `stream`, then read and clear this
+ * library's device status word on the current device. Returns LA_OK, or
+ * LA_ERR_TIMEOUT if a kernel launched since the last call gave up on a
+ * bounded device-side wait (it then skipped its remaining work and released
+ * its resources; its outputs are undefined), or LA_ERR_CUDA.
+ */
+int la_stream_status(la_stream_t stream);
+
+/* Message for the last error on the calling thread ("" if none). */
+const char *la_last_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int la_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LA_H */

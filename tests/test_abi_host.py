@@ -1,0 +1,133 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must build, load, export every function include/la.h declares,
+and reject bad arguments on the host before touching a device.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import gated_delta_rule_linear_gb300 as la
+from gated_delta_rule_linear_gb300 import build as labuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "la.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    labuild.build()
+    return la.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(la_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    assert names == sorted(["la_chunk_fwd", "la_recurrent_step", "la_stream_status",
+                            "la_last_error", "la_version"])
+    assert set(names) == set(la.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", la.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (la_[a-z_]+)\b", out))
+    for name in _declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_version(lib):
+    assert la.la_version() == 10000
+
+
+# Fake but aligned device addresses: validation must reject the call on the
+# host before any of them is dereferenced or any CUDA call is made.
+A = 0x10000
+
+
+def _call(**kw):
+    args = dict(q=A, k=A, v=A, g=None, beta=None, o=A, S0=None, S_final=None,
+                B=1, H=1, T=64, dk=64, dv=64, C=0, mode=la.LA_LINEAR, stream=None)
+    args.update(kw)
+    rc = la.la_chunk_fwd(**args)
+    return rc, la.la_last_error()
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), "LA_ERR_INVALID_ARG"),
+    (dict(o=None), "LA_ERR_INVALID_ARG"),
+    (dict(T=0), "LA_ERR_INVALID_ARG"),
+    (dict(B=0), "LA_ERR_INVALID_ARG"),
+    (dict(H=-1), "LA_ERR_INVALID_ARG"),
+    (dict(dk=96), "LA_ERR_UNSUPPORTED"),
+    (dict(dv=32), "LA_ERR_UNSUPPORTED"),
+    (dict(C=32), "LA_ERR_INVALID_ARG"),
+    (dict(mode=9), "LA_ERR_INVALID_ARG"),
+    (dict(mode=0x200), "LA_ERR_INVALID_ARG"),
+    (dict(q=A + 8), "LA_ERR_INVALID_ARG"),            # 16-byte alignment
+    (dict(o=A + 2), "LA_ERR_INVALID_ARG"),
+    (dict(g=A), "LA_ERR_INVALID_ARG"),                # linear takes no gates
+    (dict(mode=2), "LA_ERR_INVALID_ARG"),             # retnet needs g
+    (dict(mode=3), "LA_ERR_INVALID_ARG"),             # gla needs g
+    (dict(mode=3, g=A + 4), "LA_ERR_INVALID_ARG"),    # gla g must be 16-byte aligned
+    (dict(mode=4), "LA_ERR_INVALID_ARG"),             # scalar needs g
+    (dict(mode=2, g=A, beta=A), "LA_ERR_INVALID_ARG"),  # beta only for gdn
+    (dict(mode=1, g=A), "LA_ERR_INVALID_ARG"),        # elu1 takes no gates
+    (dict(S0=A + 1), "LA_ERR_INVALID_ARG"),
+])
+def test_chunk_fwd_rejects_bad_arguments(lib, kw, code):
+    rc, msg = _call(**kw)
+    assert rc == la.CONSTANTS[code], (rc, msg)
+    assert msg.startswith("la_chunk_fwd:"), msg
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(S=None), "LA_ERR_INVALID_ARG"),
+    (dict(B=0), "LA_ERR_INVALID_ARG"),
+    (dict(dk=100), "LA_ERR_UNSUPPORTED"),
+    (dict(mode=5, beta=A, g=A + 1), "LA_ERR_INVALID_ARG"),
+    (dict(mode=0, beta=A), "LA_ERR_INVALID_ARG"),
+])
+def test_recurrent_step_rejects_bad_arguments(lib, kw, code):
+    args = dict(q=A, k=A, v=A, g=None, beta=None, o=A, S=A, B=1, H=1, dk=64, dv=64,
+                mode=la.LA_LINEAR, stream=None)
+    args.update(kw)
+    rc = la.la_recurrent_step(**args)
+    assert rc == la.CONSTANTS[code], (rc, la.la_last_error())
+    assert la.la_last_error().startswith("la_recurrent_step:")
+
+
+def test_error_message_is_thread_local(lib):
+    import threading
+    rc, _ = _call(T=0)
+    assert rc != 0
+    seen = []
+    t = threading.Thread(target=lambda: seen.append(la.la_last_error()))
+    t.start()
+    t.join()
+    assert seen == [""]
+    assert "T must be" in la.la_last_error()
+
+
+def test_binding_constants_match_header():
+    text = open(HEADER).read()
+    for name, val in la.CONSTANTS.items():
+        assert re.search(rf"#define\s+{name}\s+{hex(val) if val >= 0x100 else val}\b", text), name
+
+
+def test_product_does_not_reference_the_oracle():
+    root = os.path.dirname(la.__file__)
+    for dirpath, _, files in os.walk(root):
+        for f in files:
+            if f.endswith((".py", ".cu", ".h", ".cuh", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "la_oracle" not in text, f
