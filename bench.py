@@ -1,0 +1,435 @@
+#!/usr/bin/env python3
+"""Benchmark of the chunkwise linear-attention forward (libla.so) on GB300.
+
+One step = one la_chunk_fwd call over one batch of the workload: the whole
+hot path (staging, gate prefix, local scores, WY/UT solve, state-dependent
+values, output, state passing) in one fused kernel launch. Default workload:
+Gated DeltaNet, B=4, H=16, T=16384, dk=dv=128, bf16, C=64.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+on its own GPU (the path shards by (batch, head) with no exchange), timing is
+the max over ranks and `value` sums the tokens of all ranks.
+
+Prints ONE JSON line (rank 0). `--impl reference` times the float64 CPU
+oracle on this host's cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "tokens/sec and TFLOP/s of chunk fwd at 1 GB300; % of roofline"
+UNIT = "tokens/s"
+PROFILE_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+KERNEL_SOURCES = ["gated_delta_rule_linear_gb300/csrc/la_chunk_tc.cu",
+                  "gated_delta_rule_linear_gb300/csrc/la_sm100.cuh"]
+
+
+# ---------------------------------------------------------------- cost model
+
+def flops_per_token_head(mode: str, dk: int, dv: int, C: int = 64) -> float:
+    """Algorithmic FLOP per token and head of the chunk form, fixed at C=64.
+    Unit write: scores 2*C*dk, local output 2*C*dv, inter output 2*dk*dv,
+    state update 2*dk*dv. Delta rule adds K K^T (2*C*dk), the triangular solve
+    (C^2/3), the WY products (2*C*dk + 2*C*dv) and the S-dependent correction
+    (2*dk*dv). elu+1 carries one extra value column (the normaliser)."""
+    if mode == "elu1":
+        dv = dv + 1
+    if mode == "gdn":
+        return 2 * C * (3 * dk + 2 * dv) + C * C / 3.0 + 6 * dk * dv
+    return 2 * C * (dk + dv) + 4 * dk * dv
+
+
+def algorithmic_bytes(wl, has_s0: bool) -> float:
+    """Minimum HBM traffic of one call: read q, k, v, gates, beta once, write o
+    once, read S0 and write S_final once."""
+    B, H, T, dk, dv = wl.B, wl.H, wl.T, wl.dk, wl.dv
+    e = 2 if wl.dtype == "bf16" else 4
+    per_tok = e * (2 * dk + dv) + e * dv
+    if wl.mode in ("scalar", "gdn"):
+        per_tok += 4
+    if wl.mode == "gdn":
+        per_tok += 4
+    if wl.mode == "gla":
+        per_tok += 4 * dk
+    W = dv + 1 if wl.mode == "elu1" else dv
+    state = 4 * dk * W * (2 if has_s0 else 1)
+    return float(B * H * (T * per_tok + state))
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source for this workload; else None."""
+    if not os.path.exists(PROFILE_FILE):
+        return None
+    cur = kernel_hash()
+    with open(PROFILE_FILE) as f:
+        for line in f:
+            m = re.match(r"\s*traffic\s+workload=(\S+)\s+kernel_hash=(\S+)\s+bytes_per_launch=(\d+)", line)
+            if m and m.group(1) == workload and m.group(2) == cur:
+                return int(m.group(3))
+    return None
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() in ("active", "1"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def time_oracle(wl, inp, target_s: float = 12.0, max_heads: int | None = None):
+    """Time the float64 C oracle on this host on a sample of heads over the
+    full sequence. Returns (tokens/s scaled to the workload's unit, cores, sample)."""
+    import numpy as np
+    import oracle
+
+    cores = oracle.c_threads_default()
+    BH = wl.B * wl.H
+    nh = max(1, min(BH, max_heads or 4 * cores))
+    heads = [(i // wl.H, i % wl.H) for i in range(nh)]
+
+    def pick(x):
+        if x is None:
+            return None
+        return torch.stack([x[b, h] for b, h in heads])[None].float().numpy().astype(np.float64)
+
+    q, k, v = pick(inp["q"]), pick(inp["k"]), pick(inp["v"])
+    g = inp["g"]
+    if g is not None:
+        g = (torch.stack([g[h] for _, h in heads]).double().numpy() if wl.mode == "retnet"
+             else pick(g))
+    beta, S0 = pick(inp["beta"]), pick(inp["S0"])
+    t0 = time.perf_counter()
+    oracle.recurrence_c(q, k, v, wl.mode, g=g, beta=beta, S0=S0, nthreads=cores)
+    dt = time.perf_counter() - t0
+    # nh head-sequences of T tokens = nh/H of the workload's B*T tokens
+    tokens = nh * wl.T / wl.H
+    sample = f"{nh} of {BH} (batch, head) sequences, full T={wl.T}, float64, {cores} threads"
+    return tokens / dt, cores, sample, dt
+
+
+# ---------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="gdn", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--B", type=int, default=None, help="override batch (profiling of a smaller case)")
+    ap.add_argument("--H", type=int, default=None)
+    ap.add_argument("--T", type=int, default=None)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = workloads.WORKLOADS[args.workload]
+    over = {k: getattr(args, k) for k in ("B", "H", "T") if getattr(args, k) is not None}
+    if over:
+        wl = wl.with_sizes(**over)
+
+    if args.impl == "reference":
+        return run_reference(args, wl, rank, world)
+
+    import gated_delta_rule_linear_gb300 as la
+    from gated_delta_rule_linear_gb300 import build as labuild
+    labuild.build()
+    la.load_library()
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+
+    inp = workloads.make_inputs(wl)
+    d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in inp.items()}
+    B, H, T, dk, dv = wl.B, wl.H, wl.T, wl.dk, wl.dv
+    W = dv + 1 if wl.mode == "elu1" else dv
+    o = torch.empty((B, H, T, dv), dtype=wl.torch_dtype, device=dev)
+    S = torch.empty((B, H, dk, W), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    mode_id = la.MODE_IDS[wl.mode] | (la.CONSTANTS["LA_F32"] if wl.dtype == "f32" else 0)
+    ptr = lambda t: None if t is None else t.data_ptr()
+
+    def step():
+        rc = la.la_chunk_fwd(d["q"], d["k"], d["v"], ptr(d["g"]), ptr(d["beta"]), o,
+                             ptr(d["S0"]), S, B, H, T, dk, dv, wl.C, mode_id, sh)
+        if rc != 0:
+            raise RuntimeError(la.la_last_error())
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    rc = la.la_stream_status(sh)
+    if rc != 0:
+        raise RuntimeError(f"device status after warm-up: {la.la_last_error()}")
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[2 * i].record(stream)
+        step()
+        ev[2 * i + 1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    launch_ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    tokens_per_step = B * T
+    value = world * tokens_per_step * args.steps / (total_ms / 1e3)
+    flop_call = B * H * T * flops_per_token_head(wl.mode, dk, dv)
+    tflops = world * flop_call * args.steps / (total_ms / 1e3) / 1e12
+    avg_launch_s = statistics.mean(launch_ms) / 1e3
+    alg_bytes = algorithmic_bytes(wl, d["S0"] is not None)
+    hbm_peak, tc_peak, peak_src = read_peaks()
+    ai = flop_call / alg_bytes
+    ridge = tc_peak * 1e12 / (hbm_peak * 1e9)
+    if ai < ridge:
+        achieved = alg_bytes / avg_launch_s / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4)}
+    else:
+        achieved = flop_call / avg_launch_s / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": tc_peak,
+                "unit": "TFLOP/s", "frac": round(achieved / tc_peak, 4)}
+    traffic = recorded_traffic(args.workload)
+    roof["traffic"] = traffic
+    roof["peak_source"] = peak_src
+    roof["algorithmic_bytes"] = alg_bytes
+    roof["kernel"] = "chunk_tc_kernel" if wl.dtype == "bf16" else "chunk_simt_kernel"
+    roof["launch_ms_mean"] = round(statistics.mean(launch_ms), 4)
+
+    # ---- end to end through the C ABI with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(la, wl, inp, dev, stream, mode_id, args, world, dist)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v_cpu, cores, sample, dt = time_oracle(wl, inp)
+        cpu = {"value": round(v_cpu, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": sample, "seconds": round(dt, 2)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": wl.dtype, "data": "synthetic (seeded; shapes and distributions of the workload)",
+            "config": {"workload": wl.name, "mode": wl.mode, "B": B, "H": H, "T": T, "dk": dk,
+                       "dv": dv, "C": wl.C, "global_batch": B * world, "seq_len": T,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (no flush)" if alg_bytes > 129e6 else
+                             "inputs smaller than L2"},
+            "tflops": round(tflops, 2),
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "clocks": clk,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def run_e2e(la, wl, inp, dev, stream, mode_id, args, world, dist):
+    """Same metric through the C ABI with host buffers: every step copies the
+    inputs from pinned host memory, runs the forward, and copies o and the
+    final state back, all inside the timed region."""
+    B, H, T, dk, dv = wl.B, wl.H, wl.T, wl.dk, wl.dv
+    W = dv + 1 if wl.mode == "elu1" else dv
+    names = [n for n in ("q", "k", "v", "g", "beta", "S0") if inp[n] is not None]
+    host = {n: inp[n].pin_memory() for n in names}
+    devb = {n: torch.empty_like(inp[n], device=dev) for n in names}
+    o_h = torch.empty((B, H, T, dv), dtype=wl.torch_dtype).pin_memory()
+    S_h = torch.empty((B, H, dk, W), dtype=torch.float32).pin_memory()
+    o_d = torch.empty((B, H, T, dv), dtype=wl.torch_dtype, device=dev)
+    S_d = torch.empty((B, H, dk, W), dtype=torch.float32, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = o_h.numel() * o_h.element_size() + S_h.numel() * S_h.element_size()
+    sh = stream.cuda_stream
+
+    def step():
+        with torch.cuda.stream(stream):
+            for n in names:
+                devb[n].copy_(host[n], non_blocking=True)
+            rc = la.la_chunk_fwd(devb["q"], devb["k"], devb["v"], devb.get("g"), devb.get("beta"),
+                                 o_d, devb.get("S0"), S_d, B, H, T, dk, dv, wl.C, mode_id, sh)
+            if rc != 0:
+                raise RuntimeError(la.la_last_error())
+            o_h.copy_(o_d, non_blocking=True)
+            S_h.copy_(S_d, non_blocking=True)
+
+    steps = max(3, min(args.steps, 10))
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": round(world * B * T * steps / (ms / 1e3), 1), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
+            "ms_per_step": round(ms / steps, 4)}
+
+
+def run_reference(args, wl, rank, world):
+    """Reference arm: the float64 CPU oracle, timed as it stands on this
+    host's cores, each step a bounded sample of the same workload."""
+    if rank != 0:
+        return
+    inp = workloads.make_inputs(wl)
+    vals = []
+    cores = sample = None
+    for i in range(args.warmup + args.steps):
+        v, cores, sample, _ = time_oracle(wl, inp, max_heads=None)
+        if i >= args.warmup:
+            vals.append(v)
+    value = statistics.mean(vals)
+    B, T = wl.B, wl.T
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(B * T / value * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": {"workload": wl.name, "mode": wl.mode, "B": B, "H": wl.H, "T": T, "dk": wl.dk,
+                   "dv": wl.dv, "C": wl.C, "global_batch": B, "seq_len": T,
+                   "parallelism": "single"},
+        "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

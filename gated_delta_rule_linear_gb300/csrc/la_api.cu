@@ -60,7 +60,7 @@ int select_variant(const ChunkParams &p, int *chunk_out) {
   *chunk_out = C;
   if (p.f32) return want == kVariantTc ? -2 : kVariantSimt;
   if (want >= 0) return want;
-  return kVariantSimt;
+  return kVariantTc;
 }
 
 }  // namespace la

@@ -40,9 +40,10 @@ def _inputs(mode, dtype, B=2, H=2, T=200, dk=128, dv=128, s0=True, seed=None):
 
 
 @pytest.mark.parametrize("mode", MODES)
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype,variant", [("bf16", "tc"), ("bf16", "simt"), ("f32", "simt")])
 @pytest.mark.parametrize("dims", [(128, 128), (64, 64), (64, 128), (128, 64)])
-def test_small_parity(mode, dtype, dims):
+def test_small_parity(mode, dtype, variant, dims, monkeypatch):
+    monkeypatch.setenv("LA_VARIANT", variant)
     dk, dv = dims
     inp = _inputs(mode, dtype, dk=dk, dv=dv)
     o, S = run_cuda(inp)
