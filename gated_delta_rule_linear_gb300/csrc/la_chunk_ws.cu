@@ -1,0 +1,677 @@
+// Warp-specialised chunk forward for the unit-write modes (plain linear
+// attention, elu+1 with normaliser, RetNet decay, scalar decay, GLA gates) on
+// tcgen05 + TMEM + TMA, bf16 inputs, fp32 state.
+//
+// One CTA owns one (b, h) for the whole sequence and keeps S^T in TMEM
+// (lane = value column, columns = key axis). Per chunk of C = 64 tokens with
+// inclusive log-gate prefix b ("Talk Linear Attention" sections 3.2 and 5.2):
+//
+//   P    = (Q K^T) ⊙ exp(b_r - b_s) ⊙ M        (scores from D1 = [Q; K] K^T)
+//   S^T <- Diag(e^{b_last}) S^T + V^T Kt,   Kt = Diag(e^{b_last - b}) K
+//   O^T  = Diag(e^{b}) (S_prev^T Q^T) + V^T P^T
+//
+// GLA factors the per-channel exp(b_r - b_s) around the chunk midpoint m:
+// Q and K are scaled by e^{b - b_m} and e^{b_m - b}, the bf16 state copy by
+// e^{b_m}. elu+1 applies phi to q and k, splits phi(k) into bf16 high and low
+// halves for the state update, and divides o by q.z + P 1 (kernel-attention
+// notes, sections 13-14).
+//
+// Roles (384 threads):
+//   warp 0      TMA producer: q/k/v (and GLA gate) tiles into an ns-stage ring
+//   warp 1      issues the score MMA of each chunk
+//   warp 2      issues the state-update and output MMAs
+//   warp 3      owns the TMEM allocation
+//   warps 4-7   state group: per chunk, read S^T from TMEM once to build the
+//               bf16 operand copy and apply the decay; then the output
+//               epilogue of the previous chunk (overlapping the state MMA)
+//   warps 8-11  key group, one chunk ahead: gate prefix, q/k transforms,
+//               masked/decayed scores P, Kt in place, elu+1 normaliser
+// Every wait is a bounded mbarrier poll; on expiry the CTA raises the device
+// status word, every role leaves its loop, in-flight copies and MMAs are
+// drained and TMEM is released.
+#include "la_tc_common.cuh"
+
+namespace la {
+namespace {
+
+using namespace sm100;
+using namespace tc;
+
+constexpr int kThreads = 384;
+constexpr int kMid = kC / 2 - 1;
+constexpr uint32_t kSpin = 1u << 22;
+constexpr uint32_t kTmemCols = 512;
+// TMEM columns: state, scores, two O1 and two O2 buffers
+constexpr uint32_t kColS = 0, kColD1 = 128, kColO1 = 192, kColO2 = 320;
+constexpr int kSG = 128, kKG = 256;    // first thread of each group
+constexpr int kBarSG = 1, kBarKG = 2;  // named barriers of the groups
+constexpr float kLog2e = 1.4426950408889634f;
+
+// per-stage scalars (floats)
+constexpr int kMsB2 = 0, kMsEB = 64, kMsDen = 128, kMsDec = 192, kMsB2L = 193, kMsBM = 256,
+              kMsBL = 384, kMsLM = 512, kMsBytes = 3072;
+
+__host__ __device__ inline uint32_t up1k(uint32_t x) { return (x + 1023u) & ~1023u; }
+
+// Offsets inside one pipeline stage, and of the per-CTA buffers after the stages.
+struct WsLayout {
+  uint32_t qk, v, g, klo, p, misc, stage;  // inside a stage
+  uint32_t st, z, tmp, bar, total;         // after ns stages
+};
+
+__host__ __device__ inline WsLayout ws_layout(int dk, int kind, int ns) {
+  WsLayout L;
+  const bool gla = kind == kGla, elu = kind == kElu1;
+  const uint32_t qk_bytes = (uint32_t)(dk / 64) * 16384u;
+  uint32_t o = 0;
+  L.qk = o; o += qk_bytes;
+  L.v = o; o += 16384u;  // upper 8 KB is a zero pad when dv = 64
+  L.g = o; o += gla ? up1k((uint32_t)kC * dk * 4u) : 0u;
+  L.klo = o; o += elu ? (uint32_t)(dk / 64) * 8192u : 0u;
+  L.p = o; o += 8192u;
+  L.misc = o; o += kMsBytes;
+  L.stage = o;
+  o = L.stage * ns;
+  L.st = o; o += qk_bytes;
+  L.z = o; o += 512u;
+  L.tmp = o; o += 256u;
+  L.bar = o; o += 256u;
+  L.total = o;
+  return L;
+}
+
+__device__ __forceinline__ void group_sync(int id) {
+  asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
+}
+// All-reduce of a predicate over one 128-thread group (also a barrier).
+__device__ __forceinline__ bool group_all(bool v, int id) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id)
+      : "memory");
+  return r != 0;
+}
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                              unsigned *status) {
+  for (uint32_t i = 0; i < kSpin; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (i > 32) __nanosleep(64);
+  }
+  *abort_flag = 1;
+  atomicOr(status, kStatusTimeout);
+  return false;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// 32 consecutive fp32 values (columns c0..c0+31 of `row`, c0 % 32 == 0) as
+// bf16 into a K-major 128B-swizzled operand with atoms `atom_bytes` apart.
+__device__ __forceinline__ void store_row32_bf16(uint8_t *base, uint32_t atom_bytes, int row, int c0,
+                                                 const float *v) {
+  uint8_t *a = base + (uint32_t)(c0 >> 6) * atom_bytes;
+  const int cc = c0 & 63;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    uint4 u;
+    u.x = pack_bf16(v[8 * g + 0], v[8 * g + 1]);
+    u.y = pack_bf16(v[8 * g + 2], v[8 * g + 3]);
+    u.z = pack_bf16(v[8 * g + 4], v[8 * g + 5]);
+    u.w = pack_bf16(v[8 * g + 6], v[8 * g + 7]);
+    *reinterpret_cast<uint4 *>(a + sw128_off(row, cc + 8 * g)) = u;
+  }
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &u, float *f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ uint4 pack8(const float *f) {
+  uint4 u;
+  u.x = pack_bf16(f[0], f[1]);
+  u.y = pack_bf16(f[2], f[3]);
+  u.z = pack_bf16(f[4], f[5]);
+  u.w = pack_bf16(f[6], f[7]);
+  return u;
+}
+
+template <int DK, int DV, int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap tm_q,
+                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                const __grid_constant__ CUtensorMap tm_g) {
+  constexpr bool elu = KIND == kElu1, gla = KIND == kGla;
+  constexpr bool sgate = KIND == kRetnet || KIND == kScalar;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const WsLayout L = ws_layout(DK, KIND, ns);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x, h = bh % p.H;
+  const int T = p.T, nchunks = (T + kC - 1) / kC;
+  constexpr int Wmem = DV + (elu ? 1 : 0);
+
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bar);
+  uint64_t *full = bars, *empty = bars + 3, *qk_ready = bars + 6, *key_ready = bars + 9;
+  uint64_t *d1_done = bars + 12, *s_ready = bars + 13, *s_done = bars + 14, *o1_done = bars + 15;
+  uint64_t *o_done = bars + 16, *o_free = bars + 18, *drain = bars + 20;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 22);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  float *zs = reinterpret_cast<float *>(sm + L.z);
+  float *tmp = reinterpret_cast<float *>(sm + L.tmp);
+  auto stage = [&](int s) { return sm + (uint32_t)s * L.stage; };
+
+  if (warp == 3) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 3);  // key group + state-side MMA commit + state group
+      mbar_init(&qk_ready[s], 1);
+      mbar_init(&key_ready[s], 1);
+    }
+    mbar_init(d1_done, 1);
+    mbar_init(s_ready, 1);
+    mbar_init(s_done, 1);
+    mbar_init(o1_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&o_done[b], 1);
+      mbar_init(&o_free[b], 1);
+      mbar_init(&drain[b], 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (DV == 64) {  // zero rows 64..127 of the value operand in every stage
+    for (int i = tid; i < ns * 512; i += kThreads)
+      reinterpret_cast<uint4 *>(stage(i >> 9) + L.v + 8192)[i & 511] = make_uint4(0, 0, 0, 0);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint32_t tl = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      if (gla) prefetch_tmap(&tm_g);
+      constexpr uint32_t bytes = 2u * DK * kC * 2u + DV * kC * 2u + (gla ? DK * kC * 4u : 0u);
+      int issued = 0;
+      for (int j = 0; j < nchunks; ++j) {
+        const int s = j % ns;
+        if (!wait_or_abort(&empty[s], ((j / ns) & 1) ^ 1, abort_flag, p.status)) break;
+        const int t0 = j * kC;
+        uint8_t *st = stage(s);
+        mbar_arrive_expect_tx(&full[s], bytes);
+#pragma unroll
+        for (int a = 0; a < DK / 64; ++a) {
+          tma_load_3d(st + L.qk + a * 16384, &tm_q, &full[s], 64 * a, t0, bh);
+          tma_load_3d(st + L.qk + a * 16384 + 8192, &tm_k, &full[s], 64 * a, t0, bh);
+        }
+#pragma unroll
+        for (int a = 0; a < DV / 64; ++a)
+          tma_load_3d(st + L.v + a * 8192, &tm_v, &full[s], 64 * a, t0, bh);
+        if (gla) tma_load_3d(st + L.g, &tm_g, &full[s], 0, t0, bh);
+        issued = j + 1;
+      }
+      // copies still in flight must land before the CTA's memory is released
+      for (int j = (issued > ns ? issued - ns : 0); j < issued; ++j)
+        (void)mbar_wait_bounded(&full[j % ns], (j / ns) & 1, kSpin);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------- score MMA: D1 = [Q;K] K^T
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 64, false, false);
+      for (int j = 0; j < nchunks; ++j) {
+        const int s = j % ns;
+        if (!wait_or_abort(&qk_ready[s], (j / ns) & 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t a_qk = smem_u32(stage(s) + L.qk);
+#pragma unroll
+        for (int kk = 0; kk < DK / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_bf16(tbase + kColD1, desc_sw128(a_qk + ko, 16, 1024),
+                   desc_sw128(a_qk + ko + 8192, 16, 1024), idesc, kk > 0);
+        }
+        mma_commit(d1_done);
+      }
+      mma_commit(&drain[0]);
+      (void)mbar_wait_bounded(&drain[0], 0, kSpin);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------ state update and output MMAs
+    if (lane == 0) {
+      constexpr uint32_t id_su = idesc_bf16_f32(128, DK, true, true);
+      constexpr uint32_t id_o1 = idesc_bf16_f32(128, 64, false, false);
+      constexpr uint32_t id_o2 = idesc_bf16_f32(128, 64, true, false);
+      const uint32_t a_st = smem_u32(sm + L.st);
+      for (int i = 0; i < nchunks; ++i) {
+        const int s = i % ns;
+        if (!wait_or_abort(&key_ready[s], (i / ns) & 1, abort_flag, p.status)) break;
+        if (!wait_or_abort(s_ready, i & 1, abort_flag, p.status)) break;
+        if (!wait_or_abort(&o_free[i & 1], ((i >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        uint8_t *st = stage(s);
+        const uint32_t a_v = smem_u32(st + L.v), a_qk = smem_u32(st + L.qk), a_p = smem_u32(st + L.p);
+        // S^T += V^T Kt (V as MN-major A; Kt rows of the k tile as MN-major B)
+#pragma unroll
+        for (int kk = 0; kk < kC / 16; ++kk) {
+          const uint64_t dv_ = desc_sw128(a_v + kk * 2048, 8192, 1024);
+          mma_bf16(tbase + kColS, dv_, desc_sw128(a_qk + 8192 + kk * 2048, 16384, 1024), id_su, 1);
+          if (elu)
+            mma_bf16(tbase + kColS, dv_, desc_sw128(smem_u32(st + L.klo) + kk * 2048, 8192, 1024),
+                     id_su, 1);
+        }
+        mma_commit(s_done);
+        // O1^T = S_prev^T Q^T from the bf16 state copy
+        const uint32_t d_o1 = tbase + kColO1 + (uint32_t)(i & 1) * 64u;
+        const uint32_t d_o2 = tbase + kColO2 + (uint32_t)(i & 1) * 64u;
+#pragma unroll
+        for (int kk = 0; kk < DK / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_bf16(d_o1, desc_sw128(a_st + ko, 16, 1024), desc_sw128(a_qk + ko, 16, 1024), id_o1, kk > 0);
+        }
+        mma_commit(o1_done);
+        // O2^T = V^T P^T
+#pragma unroll
+        for (int kk = 0; kk < kC / 16; ++kk)
+          mma_bf16(d_o2, desc_sw128(a_v + kk * 2048, 8192, 1024), desc_sw128(a_p + kk * 32, 16, 1024),
+                   id_o2, kk > 0);
+        mma_commit(&o_done[i & 1]);
+        mma_commit(&empty[s]);
+      }
+      mma_commit(&drain[1]);
+      (void)mbar_wait_bounded(&drain[1], 0, kSpin);
+    }
+  } else if (tid >= kSG && tid < kKG) {
+    // ------------------------------------------------------------ state group
+    const int v = tid - kSG;
+    for (int c0 = 0; c0 < DK; c0 += 32) {
+      float vals[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        vals[e] = (p.S0 && v < DV) ? p.S0[((size_t)bh * DK + c0 + e) * Wmem + v] : 0.f;
+      tmem_st32(tl + kColS + c0, vals);
+    }
+    tmem_wait_st();
+    bool alive = true;
+    for (int i = 0; i <= nchunks && alive; ++i) {
+      if (i < nchunks) {
+        const int s = i % ns;
+        const float *ms = reinterpret_cast<const float *>(stage(s) + L.misc);
+        bool ok = wait_or_abort(&key_ready[s], (i / ns) & 1, abort_flag, p.status);
+        if (ok && i > 0)
+          ok = wait_or_abort(s_done, (i - 1) & 1, abort_flag, p.status) &&
+               wait_or_abort(o1_done, (i - 1) & 1, abort_flag, p.status);
+        if (!group_all(ok, kBarSG)) { alive = false; break; }
+        tc_fence_after();
+        // state round trip: bf16 operand copy of S_prev, decay in place
+#pragma unroll 1
+        for (int c0 = 0; c0 < DK; c0 += 32) {
+          float x[32];
+          tmem_ld32(tl + kColS + c0, x);
+          tmem_wait_ld();
+          if (gla) {
+            float cp[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) cp[e] = x[e] * ms[kMsBM + c0 + e];
+            store_row32_bf16(sm + L.st, 16384, v, c0, cp);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[e] *= ms[kMsBL + c0 + e];
+            tmem_st32(tl + kColS + c0, x);
+          } else {
+            store_row32_bf16(sm + L.st, 16384, v, c0, x);
+            if (sgate) {
+              const float dec = ms[kMsDec];
+#pragma unroll
+              for (int e = 0; e < 32; ++e) x[e] *= dec;
+              tmem_st32(tl + kColS + c0, x);
+            }
+          }
+        }
+        tmem_wait_st();
+        fence_proxy_async();
+        tc_fence_before();
+        group_sync(kBarSG);
+        if (v == 0) mbar_arrive(s_ready);
+      }
+      if (i > 0) {
+        // output epilogue of chunk c = i - 1 (overlaps the state MMA of chunk i)
+        const int c = i - 1, ob = c & 1, n = min(kC, T - c * kC), sc = c % ns;
+        const float *ms = reinterpret_cast<const float *>(stage(sc) + L.misc);
+        bool ok = wait_or_abort(&o_done[ob], (c >> 1) & 1, abort_flag, p.status);
+        if (!group_all(ok, kBarSG)) { alive = false; break; }
+        tc_fence_after();
+        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o) + ((size_t)bh * T + (size_t)c * kC) * DV;
+        const bool odd = lane & 1;
+#pragma unroll 1
+        for (int r0 = 0; r0 < kC; r0 += 32) {
+          float a[32], b[32];
+          tmem_ld32(tl + kColO1 + ob * 64 + r0, a);
+          tmem_ld32(tl + kColO2 + ob * 64 + r0, b);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int r = r0 + e;
+            float y = sgate ? fmaf(ms[kMsEB + r], a[e], b[e]) : a[e] + b[e];
+            if (elu) y = __fdividef(y, ms[kMsDen + r]);
+            a[e] = y;
+          }
+          // rows (r, r+1) of neighbouring lanes are exchanged so that each
+          // thread writes two adjacent bf16 of one row
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float send = odd ? a[e] : a[e + 1];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+            const int r = r0 + e + (odd ? 1 : 0);
+            const int col = v - (odd ? 1 : 0);
+            const uint32_t w = odd ? pack_bf16(recv, a[e + 1]) : pack_bf16(a[e], recv);
+            if (r < n && v < DV) *reinterpret_cast<uint32_t *>(o + (size_t)r * DV + col) = w;
+          }
+        }
+        tc_fence_before();
+        group_sync(kBarSG);
+        if (v == 0) {
+          mbar_arrive(&o_free[ob]);
+          mbar_arrive(&empty[sc]);
+        }
+      }
+    }
+    if (alive && p.S_final) {
+      bool ok = wait_or_abort(s_done, (nchunks - 1) & 1, abort_flag, p.status);
+      if (group_all(ok, kBarSG)) {
+        tc_fence_after();
+        for (int c0 = 0; c0 < DK; c0 += 32) {
+          float x[32];
+          tmem_ld32(tl + kColS + c0, x);
+          tmem_wait_ld();
+          if (v < DV) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) p.S_final[((size_t)bh * DK + c0 + e) * Wmem + v] = x[e];
+          }
+        }
+      }
+    }
+  } else if (tid >= kKG) {
+    // -------------------------------------------------------------- key group
+    const int kg = tid - kKG, kwarp = kg >> 5;
+    if (elu && kg < DK) zs[kg] = p.S0 ? p.S0[((size_t)bh * DK + kg) * Wmem + DV] : 0.f;
+    float lg0 = 0.f, lg1 = 0.f;  // scalar log-gates of the next chunk (warp 0 of the group)
+    auto load_gates = [&](int j) {
+      lg0 = lg1 = 0.f;
+      if (j >= nchunks) return;
+      const int t = j * kC + lane;
+      if (KIND == kRetnet) {
+        const float g = __ldg(p.g + h);
+        lg0 = (t < T) ? g : 0.f;
+        lg1 = (t + 32 < T) ? g : 0.f;
+      } else {
+        lg0 = (t < T) ? __ldg(p.g + (size_t)bh * T + t) : 0.f;
+        lg1 = (t + 32 < T) ? __ldg(p.g + (size_t)bh * T + t + 32) : 0.f;
+      }
+    };
+    if (sgate && kwarp == 0) load_gates(0);
+    for (int j = 0; j < nchunks; ++j) {
+      const int s = j % ns, n = min(kC, T - j * kC);
+      uint8_t *st = stage(s);
+      float *ms = reinterpret_cast<float *>(st + L.misc);
+      uint8_t *qk = st + L.qk;
+      float *gt = reinterpret_cast<float *>(st + L.g);
+      bool ok = wait_or_abort(&full[s], (j / ns) & 1, abort_flag, p.status);
+      if (!group_all(ok, kBarKG)) break;
+      // ---- inclusive log-gate prefix
+      if (gla) {
+        if (kg < DK) {
+          float acc = 0.f, bmid = 0.f;
+          for (int r = 0; r < kC; ++r) {
+            acc += gt[r * DK + kg];
+            gt[r * DK + kg] = acc;
+            if (r == kMid) bmid = acc;
+          }
+          ms[kMsBM + kg] = __expf(bmid);
+          ms[kMsBL + kg] = __expf(acc);
+          ms[kMsLM + kg] = __expf(acc - bmid);
+        }
+      } else if (sgate && kwarp == 0) {
+        float v0 = lg0 * kLog2e, v1 = lg1 * kLog2e;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const float a0 = __shfl_up_sync(0xffffffffu, v0, off);
+          const float a1 = __shfl_up_sync(0xffffffffu, v1, off);
+          if (lane >= off) { v0 += a0; v1 += a1; }
+        }
+        v1 += __shfl_sync(0xffffffffu, v0, 31);
+        const float blast = __shfl_sync(0xffffffffu, v1, 31);
+        ms[kMsB2 + lane] = v0;
+        ms[kMsB2 + lane + 32] = v1;
+        ms[kMsEB + lane] = exp2f(v0);
+        ms[kMsEB + lane + 32] = exp2f(v1);
+        if (lane == 0) {
+          ms[kMsDec] = exp2f(blast);
+          ms[kMsB2L] = blast;
+        }
+        load_gates(j + 1);
+      }
+      if (gla || sgate) group_sync(kBarKG);
+      // ---- elementwise transforms of the q/k tiles
+      if (elu || gla) {
+        constexpr int kPer = 2 * kC * DK / 8 / 128;  // 16-byte groups per thread
+        const int row = kg;                          // row of [Q; K]
+        const int r = row & (kC - 1);
+        const bool is_k = row >= kC;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int g8 = i;  // 8-column group within the row
+          uint8_t *ptr = qk + (g8 >> 3) * 16384 + sw128_off(row, (g8 & 7) * 8);
+          float f[8];
+          unpack8(*reinterpret_cast<uint4 *>(ptr), f);
+          if (elu) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = (r < n) ? (f[e] > 0.f ? f[e] + 1.f : __expf(f[e])) : 0.f;
+            const uint4 hi = pack8(f);
+            if (is_k) {
+              float fh[8];
+              unpack8(hi, fh);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) fh[e] = f[e] - fh[e];
+              *reinterpret_cast<uint4 *>(st + L.klo + (g8 >> 3) * 8192 + sw128_off(r, (g8 & 7) * 8)) =
+                  pack8(fh);
+            }
+            *reinterpret_cast<uint4 *>(ptr) = hi;
+          } else {
+            const float *brow = gt + r * DK + g8 * 8;
+            const float *bmid = gt + kMid * DK + g8 * 8;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float d = (brow[e] - bmid[e]) * kLog2e;
+              f[e] *= exp2f(is_k ? -d : d);
+            }
+            *reinterpret_cast<uint4 *>(ptr) = pack8(f);
+          }
+        }
+        fence_proxy_async();
+        group_sync(kBarKG);
+      }
+      if (kg == 0) mbar_arrive(&qk_ready[s]);
+      ok = wait_or_abort(d1_done, j & 1, abort_flag, p.status);
+      if (!group_all(ok, kBarKG)) break;
+      tc_fence_after();
+      // ---- masked, decayed scores P (TMEM lanes 0..63 hold the Q K^T rows)
+      if (kg < kC) {
+        const int r = kg;
+        const float b2r = sgate ? ms[kMsB2 + r] : 0.f;
+        float rowsum = 0.f;
+#pragma unroll 1
+        for (int s0 = 0; s0 < kC; s0 += 32) {
+          float d[32];
+          tmem_ld32(tl + kColD1 + s0, d);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int sc = s0 + e;
+            float x = (sc <= r && r < n) ? d[e] : 0.f;
+            if (sgate) x *= exp2f(sc <= r ? b2r - ms[kMsB2 + sc] : 0.f);
+            if (elu) {
+              x = __bfloat162float(__float2bfloat16_rn(x));
+              rowsum += x;
+            }
+            d[e] = x;
+          }
+          store_row32_bf16(st + L.p, 8192, r, s0, d);
+        }
+        if (elu) ms[kMsDen + r] = rowsum;
+      } else if (elu) {
+        const int r = kg - kC;  // phi(q_r) . z with the rounded phi(q) the MMA used
+        float acc = 0.f;
+#pragma unroll
+        for (int g8 = 0; g8 < DK / 8; ++g8) {
+          float f[8];
+          unpack8(*reinterpret_cast<const uint4 *>(qk + (g8 >> 3) * 16384 + sw128_off(r, (g8 & 7) * 8)), f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc = fmaf(f[e], zs[g8 * 8 + e], acc);
+        }
+        tmp[r] = acc;
+      }
+      tc_fence_before();
+      group_sync(kBarKG);
+      // ---- Kt in place; elu+1: denominators and z
+      if (sgate || gla) {
+        constexpr int kHalf = DK / 16;  // 16-byte groups per half row
+        const int r = kg >> 1, g0 = (kg & 1) * kHalf;
+        const float rs = sgate ? exp2f(ms[kMsB2L] - ms[kMsB2 + r]) : 1.f;
+        uint4 u[kHalf];
+#pragma unroll
+        for (int i = 0; i < kHalf; ++i) {
+          const int g8 = g0 + i;
+          u[i] = *reinterpret_cast<const uint4 *>(qk + 8192 + (g8 >> 3) * 16384 + sw128_off(r, (g8 & 7) * 8));
+        }
+#pragma unroll
+        for (int i = 0; i < kHalf; ++i) {
+          const int g8 = g0 + i;
+          float f[8];
+          unpack8(u[i], f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] *= gla ? ms[kMsLM + g8 * 8 + e] : rs;
+          *reinterpret_cast<uint4 *>(qk + 8192 + (g8 >> 3) * 16384 + sw128_off(r, (g8 & 7) * 8)) = pack8(f);
+        }
+      }
+      if (elu) {
+        if (kg < kC) ms[kMsDen + kg] += tmp[kg];
+        if (kg < DK) {
+          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+          const uint8_t *kh = qk + (kg >> 6) * 16384 + 8192;
+          const uint8_t *kl = st + L.klo + (kg >> 6) * 8192;
+#pragma unroll 4
+          for (int r = 0; r < kC; r += 2) {
+            a0 += bf16_at(kh, sw128_off(r, kg & 63));
+            a1 += bf16_at(kl, sw128_off(r, kg & 63));
+            a2 += bf16_at(kh, sw128_off(r + 1, kg & 63));
+            a3 += bf16_at(kl, sw128_off(r + 1, kg & 63));
+          }
+          zs[kg] += (a0 + a2) + (a1 + a3);
+        }
+      }
+      fence_proxy_async();
+      group_sync(kBarKG);
+      if (kg == 0) {
+        mbar_arrive(&key_ready[s]);
+        mbar_arrive(&empty[s]);
+      }
+    }
+    if (elu && p.S_final && kg < DK && !*abort_flag)
+      p.S_final[((size_t)bh * DK + kg) * Wmem + DV] = zs[kg];
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 3) tmem_dealloc(tbase, kTmemCols);
+}
+
+template <int DK, int DV, int KIND>
+int launch_typed(const ChunkParams &p, cudaStream_t stream) {
+  int ns = 3;
+  WsLayout L = ws_layout(DK, KIND, ns);
+  while (ns > 2 && L.total + 1024 > 232448) L = ws_layout(DK, KIND, --ns);
+  const size_t smem = L.total + 1024;
+  if (smem > 232448) {
+    set_error("la_chunk_fwd: pipelined kernel needs %zu bytes of shared memory", smem);
+    return LA_ERR_UNSUPPORTED;
+  }
+  const int BH = p.B * p.H;
+  CUtensorMap mq, mk, mv, mg;
+  bool ok = make_map(&mq, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DK, p.T, BH, 64,
+                     CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_map(&mk, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DK, p.T, BH, 64,
+                     CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_map(&mv, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DV, p.T, BH, 64,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+  if (ok && KIND == kGla)
+    ok = make_map(&mg, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, DK, p.T, BH, DK,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+  else
+    mg = mq;
+  if (!ok) {
+    set_error("la_chunk_fwd: cuTensorMapEncodeTiled rejected a tensor map");
+    return LA_ERR_CUDA;
+  }
+  auto kern = chunk_ws_kernel<DK, DV, KIND>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess) {
+    kern<<<BH, kThreads, smem, stream>>>(p, ns, mq, mk, mv, mg);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) {
+    set_error("la_chunk_fwd: pipelined kernel launch failed: %s", cudaGetErrorString(e));
+    return LA_ERR_CUDA;
+  }
+  return LA_OK;
+}
+
+template <int KIND>
+int launch_kind(const ChunkParams &p, cudaStream_t stream) {
+  if (p.dk == 128 && p.dv == 128) return launch_typed<128, 128, KIND>(p, stream);
+  if (p.dk == 128 && p.dv == 64) return launch_typed<128, 64, KIND>(p, stream);
+  if (p.dk == 64 && p.dv == 128) return launch_typed<64, 128, KIND>(p, stream);
+  return launch_typed<64, 64, KIND>(p, stream);
+}
+
+}  // namespace
+
+int launch_chunk_ws(const ChunkParams &p, cudaStream_t stream) {
+  if (!encode_fn()) {
+    set_error("la_chunk_fwd: cuTensorMapEncodeTiled is unavailable");
+    return LA_ERR_CUDA;
+  }
+  switch (p.kind) {
+    case kLinear: return launch_kind<kLinear>(p, stream);
+    case kElu1: return launch_kind<kElu1>(p, stream);
+    case kRetnet: return launch_kind<kRetnet>(p, stream);
+    case kScalar: return launch_kind<kScalar>(p, stream);
+    case kGla: return launch_kind<kGla>(p, stream);
+    default:
+      set_error("la_chunk_fwd: mode %d is not handled by the pipelined kernel", p.kind);
+      return LA_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace la

@@ -55,6 +55,7 @@ unsigned *status_word();
 // Launchers: return LA_OK or an LA_ERR_* code (message already set).
 int launch_chunk_simt(const ChunkParams &p, cudaStream_t stream);
 int launch_chunk_tc(const ChunkParams &p, cudaStream_t stream);
+int launch_chunk_ws(const ChunkParams &p, cudaStream_t stream);
 int launch_step(const StepParams &p, cudaStream_t stream);
 
 // Which chunk-forward kernel a shape goes to (host-side selection).
