@@ -39,24 +39,36 @@ using namespace tc;
 
 constexpr int kThreads = 384;
 constexpr int kMid = kC / 2 - 1;
-constexpr uint32_t kSpin = 1u << 22;
+constexpr uint32_t kSpin = 1u << 24;  // polls before a wait gives up (well over 100 ms)
+constexpr int kNM = 4;                // slots of the per-chunk scalar ring
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: state, scores, two O1 and two O2 buffers
-constexpr uint32_t kColS = 0, kColD1 = 128, kColO1 = 192, kColO2 = 320;
+// TMEM columns: state, two score buffers, two output buffers
+constexpr uint32_t kColS = 0, kColD1 = 128, kColO = 256;
 constexpr int kSG = 128, kKG = 256;    // first thread of each group
 constexpr int kBarSG = 1, kBarKG = 2;  // named barriers of the groups
 constexpr float kLog2e = 1.4426950408889634f;
 
-// per-stage scalars (floats)
-constexpr int kMsB2 = 0, kMsEB = 64, kMsDen = 128, kMsDec = 192, kMsB2L = 193, kMsBM = 256,
-              kMsBL = 384, kMsLM = 512, kMsBytes = 3072;
+// per-stage scalars (floats): log2-domain gate prefix b2, e^{b}, elu+1
+// denominators, chunk decay, fast-path flag, per-row factors e^{b - b_last}
+// (scores) and e^{b_last - b} (value or key rows), GLA per-channel factors
+constexpr int kMsB2 = 0, kMsEB = 64, kMsDen = 128, kMsDec = 192, kMsB2L = 193, kMsFast = 194,
+              kMsF = 256, kMsVS = 320, kMsBM = 384, kMsBL = 512, kMsLM = 640;
+// bytes of one scalar slot: the GLA per-channel factors need the upper part
+__host__ __device__ constexpr uint32_t ms_bytes(int kind) { return kind == kGla ? 3072u : 1536u; }
+// GLA's 32 KB gate tiles leave no room for an output staging tile: it stores o directly
+__host__ __device__ constexpr bool staged_out(int kind) { return kind != kGla; }
+// A chunk whose total decay is below 2^-kFastLimit takes the exact path.
+constexpr float kFastLimit = 100.f;
 
 __host__ __device__ inline uint32_t up1k(uint32_t x) { return (x + 1023u) & ~1023u; }
 
-// Offsets inside one pipeline stage, and of the per-CTA buffers after the stages.
+// Offsets inside one pipeline stage (released when the chunk's MMAs are
+// done), and of the per-CTA buffers after the stages: the bf16 state copy,
+// the output staging tile, the ring of per-chunk scalars (released after the
+// chunk's output epilogue), elu+1 normaliser, barriers.
 struct WsLayout {
-  uint32_t qk, v, g, klo, p, misc, stage;  // inside a stage
-  uint32_t st, z, tmp, bar, total;         // after ns stages
+  uint32_t qk, v, g, klo, p, stage;  // inside a stage
+  uint32_t st, ot, misc, z, tmp, bar, total;
 };
 
 __host__ __device__ inline WsLayout ws_layout(int dk, int kind, int ns) {
@@ -69,10 +81,11 @@ __host__ __device__ inline WsLayout ws_layout(int dk, int kind, int ns) {
   L.g = o; o += gla ? up1k((uint32_t)kC * dk * 4u) : 0u;
   L.klo = o; o += elu ? (uint32_t)(dk / 64) * 8192u : 0u;
   L.p = o; o += 8192u;
-  L.misc = o; o += kMsBytes;
   L.stage = o;
   o = L.stage * ns;
   L.st = o; o += qk_bytes;
+  L.ot = o; o += staged_out(kind) ? 16384u : 0u;
+  L.misc = o; o += kNM * ms_bytes(kind);
   L.z = o; o += 512u;
   L.tmp = o; o += 256u;
   L.bar = o; o += 256u;
@@ -103,7 +116,6 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
   for (uint32_t i = 0; i < kSpin; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (i > 32) __nanosleep(64);
   }
   *abort_flag = 1;
   atomicOr(status, kStatusTimeout);
@@ -153,7 +165,7 @@ template <int DK, int DV, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                const __grid_constant__ CUtensorMap tm_g) {
+                const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_o) {
   constexpr bool elu = KIND == kElu1, gla = KIND == kGla;
   constexpr bool sgate = KIND == kRetnet || KIND == kScalar;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -166,13 +178,17 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
 
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bar);
   uint64_t *full = bars, *empty = bars + 3, *qk_ready = bars + 6, *key_ready = bars + 9;
-  uint64_t *d1_done = bars + 12, *s_ready = bars + 13, *s_done = bars + 14, *o1_done = bars + 15;
+  uint64_t *s_ready = bars + 13, *s_done = bars + 14, *o1_done = bars + 15;
   uint64_t *o_done = bars + 16, *o_free = bars + 18, *drain = bars + 20;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 22);
+  uint64_t *d1_full = bars + 22, *d1_free = bars + 24, *mfree = bars + 26;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 26 + kNM);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   float *zs = reinterpret_cast<float *>(sm + L.z);
   float *tmp = reinterpret_cast<float *>(sm + L.tmp);
   auto stage = [&](int s) { return sm + (uint32_t)s * L.stage; };
+  auto mslot = [&](int j) {
+    return reinterpret_cast<float *>(sm + L.misc + (uint32_t)(j % kNM) * ms_bytes(KIND));
+  };
 
   if (warp == 3) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -180,16 +196,18 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
   }
   if (tid == 0) {
     for (int s = 0; s < 3; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 3);  // key group + state-side MMA commit + state group
+      mbar_init(&full[s], sgate ? 2 : 1);  // TMA bytes (+ the producer's gate prefix)
+      mbar_init(&empty[s], 2);  // key group + state-side MMA commit
       mbar_init(&qk_ready[s], 1);
       mbar_init(&key_ready[s], 1);
     }
-    mbar_init(d1_done, 1);
     mbar_init(s_ready, 1);
     mbar_init(s_done, 1);
     mbar_init(o1_done, 1);
+    for (int m = 0; m < kNM; ++m) mbar_init(&mfree[m], 1);
     for (int b = 0; b < 2; ++b) {
+      mbar_init(&d1_full[b], 1);
+      mbar_init(&d1_free[b], 1);
       mbar_init(&o_done[b], 1);
       mbar_init(&o_free[b], 1);
       mbar_init(&drain[b], 1);
@@ -209,18 +227,64 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Lane 0 streams the tiles; for the scalar-gate modes the whole warp
+    // then forms the chunk's log-gate prefix and per-row factors.
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
       if (gla) prefetch_tmap(&tm_g);
-      constexpr uint32_t bytes = 2u * DK * kC * 2u + DV * kC * 2u + (gla ? DK * kC * 4u : 0u);
-      int issued = 0;
-      for (int j = 0; j < nchunks; ++j) {
-        const int s = j % ns;
-        if (!wait_or_abort(&empty[s], ((j / ns) & 1) ^ 1, abort_flag, p.status)) break;
-        const int t0 = j * kC;
-        uint8_t *st = stage(s);
+    }
+    constexpr uint32_t bytes = 2u * DK * kC * 2u + DV * kC * 2u + (gla ? DK * kC * 4u : 0u);
+    int issued = 0;
+    for (int j = 0; j < nchunks; ++j) {
+      const int s = j % ns;
+      const int t0 = j * kC;
+      int ok = 1;
+      // per-chunk scalars first (their slot frees after the chunk kNM back has
+      // been written out), so the gate loads overlap the wait for a stage
+      if (lane == 0) ok = wait_or_abort(&mfree[j % kNM], ((j / kNM) & 1) ^ 1, abort_flag, p.status);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      if (sgate) {
+        float *ms = mslot(j);
+        const int t = t0 + lane;
+        float g0, g1;
+        if (KIND == kRetnet) {
+          const float g = __ldg(p.g + h);
+          g0 = (t < T) ? g : 0.f;
+          g1 = (t + 32 < T) ? g : 0.f;
+        } else {
+          g0 = (t < T) ? __ldg(p.g + (size_t)bh * T + t) : 0.f;
+          g1 = (t + 32 < T) ? __ldg(p.g + (size_t)bh * T + t + 32) : 0.f;
+        }
+        float v0 = g0 * kLog2e, v1 = g1 * kLog2e;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const float a0 = __shfl_up_sync(0xffffffffu, v0, off);
+          const float a1 = __shfl_up_sync(0xffffffffu, v1, off);
+          if (lane >= off) { v0 += a0; v1 += a1; }
+        }
+        v1 += __shfl_sync(0xffffffffu, v0, 31);
+        const float bl = __shfl_sync(0xffffffffu, v1, 31);
+        ms[kMsB2 + lane] = v0;
+        ms[kMsB2 + lane + 32] = v1;
+        ms[kMsEB + lane] = exp2f(v0);
+        ms[kMsEB + lane + 32] = exp2f(v1);
+        ms[kMsF + lane] = exp2f(v0 - bl);
+        ms[kMsF + lane + 32] = exp2f(v1 - bl);
+        ms[kMsVS + lane] = exp2f(bl - v0);
+        ms[kMsVS + lane + 32] = exp2f(bl - v1);
+        if (lane == 0) {
+          ms[kMsDec] = exp2f(bl);
+          ms[kMsB2L] = bl;
+          ms[kMsFast] = (-bl < kFastLimit) ? 1.f : 0.f;
+        }
+        __syncwarp();
+      }
+      if (lane == 0) ok = wait_or_abort(&empty[s], ((j / ns) & 1) ^ 1, abort_flag, p.status);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      uint8_t *st = stage(s);
+      if (lane == 0) {
         mbar_arrive_expect_tx(&full[s], bytes);
 #pragma unroll
         for (int a = 0; a < DK / 64; ++a) {
@@ -231,28 +295,33 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
         for (int a = 0; a < DV / 64; ++a)
           tma_load_3d(st + L.v + a * 8192, &tm_v, &full[s], 64 * a, t0, bh);
         if (gla) tma_load_3d(st + L.g, &tm_g, &full[s], 0, t0, bh);
-        issued = j + 1;
+        if (sgate) mbar_arrive(&full[s]);  // the gate prefix of this chunk is in place
       }
-      // copies still in flight must land before the CTA's memory is released
+      issued = j + 1;
+    }
+    // copies still in flight must land before the CTA's memory is released
+    if (lane == 0)
       for (int j = (issued > ns ? issued - ns : 0); j < issued; ++j)
         (void)mbar_wait_bounded(&full[j % ns], (j / ns) & 1, kSpin);
-    }
   } else if (warp == 1) {
     // ---------------------------------------------- score MMA: D1 = [Q;K] K^T
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, 64, false, false);
       for (int j = 0; j < nchunks; ++j) {
         const int s = j % ns;
-        if (!wait_or_abort(&qk_ready[s], (j / ns) & 1, abort_flag, p.status)) break;
+        // tiles that need no elementwise transform are used as soon as they land
+        if (!wait_or_abort((elu || gla) ? &qk_ready[s] : &full[s], (j / ns) & 1, abort_flag, p.status))
+          break;
+        if (!wait_or_abort(&d1_free[j & 1], ((j >> 1) & 1) ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t a_qk = smem_u32(stage(s) + L.qk);
 #pragma unroll
         for (int kk = 0; kk < DK / 16; ++kk) {
           const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16(tbase + kColD1, desc_sw128(a_qk + ko, 16, 1024),
+          mma_bf16(tbase + kColD1 + (uint32_t)(j & 1) * 64u, desc_sw128(a_qk + ko, 16, 1024),
                    desc_sw128(a_qk + ko + 8192, 16, 1024), idesc, kk > 0);
         }
-        mma_commit(d1_done);
+        mma_commit(&d1_full[j & 1]);
       }
       mma_commit(&drain[0]);
       (void)mbar_wait_bounded(&drain[0], 0, kSpin);
@@ -282,20 +351,19 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
                      id_su, 1);
         }
         mma_commit(s_done);
-        // O1^T = S_prev^T Q^T from the bf16 state copy
-        const uint32_t d_o1 = tbase + kColO1 + (uint32_t)(i & 1) * 64u;
-        const uint32_t d_o2 = tbase + kColO2 + (uint32_t)(i & 1) * 64u;
+        // O^T = S_prev^T Qt^T (bf16 state copy; Qt = Diag(e^b) Q) ...
+        const uint32_t d_o1 = tbase + kColO + (uint32_t)(i & 1) * 64u, d_o2 = d_o1;
 #pragma unroll
         for (int kk = 0; kk < DK / 16; ++kk) {
           const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
           mma_bf16(d_o1, desc_sw128(a_st + ko, 16, 1024), desc_sw128(a_qk + ko, 16, 1024), id_o1, kk > 0);
         }
         mma_commit(o1_done);
-        // O2^T = V^T P^T
+        // ... + V^T P^T
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)
           mma_bf16(d_o2, desc_sw128(a_v + kk * 2048, 8192, 1024), desc_sw128(a_p + kk * 32, 16, 1024),
-                   id_o2, kk > 0);
+                   id_o2, 1);
         mma_commit(&o_done[i & 1]);
         mma_commit(&empty[s]);
       }
@@ -317,7 +385,7 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
     for (int i = 0; i <= nchunks && alive; ++i) {
       if (i < nchunks) {
         const int s = i % ns;
-        const float *ms = reinterpret_cast<const float *>(stage(s) + L.misc);
+        const float *ms = mslot(i);
         bool ok = wait_or_abort(&key_ready[s], (i / ns) & 1, abort_flag, p.status);
         if (ok && i > 0)
           ok = wait_or_abort(s_done, (i - 1) & 1, abort_flag, p.status) &&
@@ -356,46 +424,57 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
       }
       if (i > 0) {
         // output epilogue of chunk c = i - 1 (overlaps the state MMA of chunk i)
-        const int c = i - 1, ob = c & 1, n = min(kC, T - c * kC), sc = c % ns;
-        const float *ms = reinterpret_cast<const float *>(stage(sc) + L.misc);
+        const int c = i - 1, ob = c & 1, n = min(kC, T - c * kC);
+        const float *ms = mslot(c);
         bool ok = wait_or_abort(&o_done[ob], (c >> 1) & 1, abort_flag, p.status);
+        if (v == 0) bulk_wait_read<0>();  // the previous tile has left the staging buffer
         if (!group_all(ok, kBarSG)) { alive = false; break; }
         tc_fence_after();
-        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o) + ((size_t)bh * T + (size_t)c * kC) * DV;
+        uint8_t *ot = sm + L.ot + (uint32_t)(v >> 6) * 8192u;
+        __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(p.o) + ((size_t)bh * T + (size_t)c * kC) * DV;
         const bool odd = lane & 1;
 #pragma unroll 1
         for (int r0 = 0; r0 < kC; r0 += 32) {
-          float a[32], b[32];
-          tmem_ld32(tl + kColO1 + ob * 64 + r0, a);
-          tmem_ld32(tl + kColO2 + ob * 64 + r0, b);
+          float a[32];
+          tmem_ld32(tl + kColO + ob * 64 + r0, a);
           tmem_wait_ld();
+          if (elu) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int r = r0 + e;
-            float y = sgate ? fmaf(ms[kMsEB + r], a[e], b[e]) : a[e] + b[e];
-            if (elu) y = __fdividef(y, ms[kMsDen + r]);
-            a[e] = y;
+            for (int e = 0; e < 32; ++e) a[e] = __fdividef(a[e], ms[kMsDen + r0 + e]);
           }
           // rows (r, r+1) of neighbouring lanes are exchanged so that each
           // thread writes two adjacent bf16 of one row
+          if (v < DV) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float send = odd ? a[e] : a[e + 1];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-            const int r = r0 + e + (odd ? 1 : 0);
-            const int col = v - (odd ? 1 : 0);
-            const uint32_t w = odd ? pack_bf16(recv, a[e + 1]) : pack_bf16(a[e], recv);
-            if (r < n && v < DV) *reinterpret_cast<uint32_t *>(o + (size_t)r * DV + col) = w;
+            for (int e = 0; e < 32; e += 2) {
+              const float send = odd ? a[e] : a[e + 1];
+              const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+              const int r = r0 + e + (odd ? 1 : 0);
+              const int col = v - (odd ? 1 : 0);
+              const uint32_t w = odd ? pack_bf16(recv, a[e + 1]) : pack_bf16(a[e], recv);
+              if (staged_out(KIND))
+                *reinterpret_cast<uint32_t *>(ot + sw128_off(r, col & 63)) = w;
+              else if (r < n)
+                *reinterpret_cast<uint32_t *>(og + (size_t)r * DV + col) = w;
+            }
           }
         }
+        if (staged_out(KIND)) fence_proxy_async();
         tc_fence_before();
         group_sync(kBarSG);
         if (v == 0) {
+          if (staged_out(KIND)) {
+#pragma unroll
+            for (int a = 0; a < DV / 64; ++a)
+              tma_store_3d(&tm_o, sm + L.ot + a * 8192, 64 * a, c * kC, bh);
+            bulk_commit();
+          }
           mbar_arrive(&o_free[ob]);
-          mbar_arrive(&empty[sc]);
+          mbar_arrive(&mfree[c % kNM]);
         }
       }
     }
+    if (v == 0) bulk_wait<0>();  // output tiles written before the CTA leaves
     if (alive && p.S_final) {
       bool ok = wait_or_abort(s_done, (nchunks - 1) & 1, abort_flag, p.status);
       if (group_all(ok, kBarSG)) {
@@ -413,27 +492,12 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
     }
   } else if (tid >= kKG) {
     // -------------------------------------------------------------- key group
-    const int kg = tid - kKG, kwarp = kg >> 5;
+    const int kg = tid - kKG;
     if (elu && kg < DK) zs[kg] = p.S0 ? p.S0[((size_t)bh * DK + kg) * Wmem + DV] : 0.f;
-    float lg0 = 0.f, lg1 = 0.f;  // scalar log-gates of the next chunk (warp 0 of the group)
-    auto load_gates = [&](int j) {
-      lg0 = lg1 = 0.f;
-      if (j >= nchunks) return;
-      const int t = j * kC + lane;
-      if (KIND == kRetnet) {
-        const float g = __ldg(p.g + h);
-        lg0 = (t < T) ? g : 0.f;
-        lg1 = (t + 32 < T) ? g : 0.f;
-      } else {
-        lg0 = (t < T) ? __ldg(p.g + (size_t)bh * T + t) : 0.f;
-        lg1 = (t + 32 < T) ? __ldg(p.g + (size_t)bh * T + t + 32) : 0.f;
-      }
-    };
-    if (sgate && kwarp == 0) load_gates(0);
     for (int j = 0; j < nchunks; ++j) {
       const int s = j % ns, n = min(kC, T - j * kC);
       uint8_t *st = stage(s);
-      float *ms = reinterpret_cast<float *>(st + L.misc);
+      float *ms = mslot(j);
       uint8_t *qk = st + L.qk;
       float *gt = reinterpret_cast<float *>(st + L.g);
       bool ok = wait_or_abort(&full[s], (j / ns) & 1, abort_flag, p.status);
@@ -451,27 +515,8 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
           ms[kMsBL + kg] = __expf(acc);
           ms[kMsLM + kg] = __expf(acc - bmid);
         }
-      } else if (sgate && kwarp == 0) {
-        float v0 = lg0 * kLog2e, v1 = lg1 * kLog2e;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const float a0 = __shfl_up_sync(0xffffffffu, v0, off);
-          const float a1 = __shfl_up_sync(0xffffffffu, v1, off);
-          if (lane >= off) { v0 += a0; v1 += a1; }
-        }
-        v1 += __shfl_sync(0xffffffffu, v0, 31);
-        const float blast = __shfl_sync(0xffffffffu, v1, 31);
-        ms[kMsB2 + lane] = v0;
-        ms[kMsB2 + lane + 32] = v1;
-        ms[kMsEB + lane] = exp2f(v0);
-        ms[kMsEB + lane + 32] = exp2f(v1);
-        if (lane == 0) {
-          ms[kMsDec] = exp2f(blast);
-          ms[kMsB2L] = blast;
-        }
-        load_gates(j + 1);
       }
-      if (gla || sgate) group_sync(kBarKG);
+      if (gla) group_sync(kBarKG);
       // ---- elementwise transforms of the q/k tiles
       if (elu || gla) {
         constexpr int kPer = 2 * kC * DK / 8 / 128;  // 16-byte groups per thread
@@ -511,25 +556,29 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
         fence_proxy_async();
         group_sync(kBarKG);
       }
-      if (kg == 0) mbar_arrive(&qk_ready[s]);
-      ok = wait_or_abort(d1_done, j & 1, abort_flag, p.status);
+      if ((elu || gla) && kg == 0) mbar_arrive(&qk_ready[s]);
+      ok = wait_or_abort(&d1_full[j & 1], (j >> 1) & 1, abort_flag, p.status);
       if (!group_all(ok, kBarKG)) break;
       tc_fence_after();
+      const bool fast = sgate && ms[kMsFast] != 0.f;
       // ---- masked, decayed scores P (TMEM lanes 0..63 hold the Q K^T rows)
       if (kg < kC) {
         const int r = kg;
         const float b2r = sgate ? ms[kMsB2 + r] : 0.f;
+        const float fr = fast ? ms[kMsF + r] : 1.f;
         float rowsum = 0.f;
 #pragma unroll 1
         for (int s0 = 0; s0 < kC; s0 += 32) {
           float d[32];
-          tmem_ld32(tl + kColD1 + s0, d);
+          tmem_ld32(tl + kColD1 + (uint32_t)(j & 1) * 64u + s0, d);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int sc = s0 + e;
             float x = (sc <= r && r < n) ? d[e] : 0.f;
-            if (sgate) x *= exp2f(sc <= r ? b2r - ms[kMsB2 + sc] : 0.f);
+            // fast path: P' = Q K^T e^{b_r - b_last} against e^{b_last - b_s} V;
+            // exact path: P = Q K^T e^{b_r - b_s} against Kt = e^{b_last - b_s} K
+            if (sgate) x *= fast ? fr : exp2f(sc <= r ? b2r - ms[kMsB2 + sc] : 0.f);
             if (elu) {
               x = __bfloat162float(__float2bfloat16_rn(x));
               rowsum += x;
@@ -553,11 +602,51 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
       }
       tc_fence_before();
       group_sync(kBarKG);
-      // ---- Kt in place; elu+1: denominators and z
-      if (sgate || gla) {
+      if (kg == 0) mbar_arrive(&d1_free[j & 1]);
+      if (sgate) {  // Qt = Diag(e^{b}) Q for the inter-chunk output
+        constexpr int kHalf = DK / 16;
+        const int r = kg >> 1, g0 = (kg & 1) * kHalf;
+        const float rs = ms[kMsEB + r];
+        uint4 u[kHalf];
+#pragma unroll
+        for (int i = 0; i < kHalf; ++i) {
+          const int g8 = g0 + i;
+          u[i] = *reinterpret_cast<const uint4 *>(qk + (g8 >> 3) * 16384 + sw128_off(r, (g8 & 7) * 8));
+        }
+#pragma unroll
+        for (int i = 0; i < kHalf; ++i) {
+          const int g8 = g0 + i;
+          float f[8];
+          unpack8(u[i], f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] *= rs;
+          *reinterpret_cast<uint4 *>(qk + (g8 >> 3) * 16384 + sw128_off(r, (g8 & 7) * 8)) = pack8(f);
+        }
+      }
+      // ---- row scaling in place: e^{b_last - b_s} V (fast) or Kt; elu+1: z, den
+      if (fast) {
+        constexpr int kHalf = DV / 16;
+        const int r = kg >> 1, g0 = (kg & 1) * kHalf;
+        const float rs = ms[kMsVS + r];
+        uint4 u[kHalf];
+#pragma unroll
+        for (int i = 0; i < kHalf; ++i) {
+          const int g8 = g0 + i;
+          u[i] = *reinterpret_cast<const uint4 *>(st + L.v + (g8 >> 3) * 8192 + sw128_off(r, (g8 & 7) * 8));
+        }
+#pragma unroll
+        for (int i = 0; i < kHalf; ++i) {
+          const int g8 = g0 + i;
+          float f[8];
+          unpack8(u[i], f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] *= rs;
+          *reinterpret_cast<uint4 *>(st + L.v + (g8 >> 3) * 8192 + sw128_off(r, (g8 & 7) * 8)) = pack8(f);
+        }
+      } else if (sgate || gla) {
         constexpr int kHalf = DK / 16;  // 16-byte groups per half row
         const int r = kg >> 1, g0 = (kg & 1) * kHalf;
-        const float rs = sgate ? exp2f(ms[kMsB2L] - ms[kMsB2 + r]) : 1.f;
+        const float rs = sgate ? ms[kMsVS + r] : 1.f;
         uint4 u[kHalf];
 #pragma unroll
         for (int i = 0; i < kHalf; ++i) {
@@ -618,8 +707,10 @@ int launch_typed(const ChunkParams &p, cudaStream_t stream) {
     return LA_ERR_UNSUPPORTED;
   }
   const int BH = p.B * p.H;
-  CUtensorMap mq, mk, mv, mg;
+  CUtensorMap mq, mk, mv, mg, mo;
   bool ok = make_map(&mq, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DK, p.T, BH, 64,
+                     CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_map(&mo, p.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DV, p.T, BH, 64,
                      CU_TENSOR_MAP_SWIZZLE_128B) &&
             make_map(&mk, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DK, p.T, BH, 64,
                      CU_TENSOR_MAP_SWIZZLE_128B) &&
@@ -637,7 +728,7 @@ int launch_typed(const ChunkParams &p, cudaStream_t stream) {
   auto kern = chunk_ws_kernel<DK, DV, KIND>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess) {
-    kern<<<BH, kThreads, smem, stream>>>(p, ns, mq, mk, mv, mg);
+    kern<<<BH, kThreads, smem, stream>>>(p, ns, mq, mk, mv, mg, mo);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) {
