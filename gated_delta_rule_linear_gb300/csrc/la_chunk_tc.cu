@@ -633,6 +633,7 @@ int launch_chunk_tc(const ChunkParams &p, cudaStream_t stream) {
     return LA_ERR_CUDA;
   }
   if (p.kind != kGdn) return launch_chunk_ws(p, stream);
+  if (p.dk == 128 && p.dv == 128) return launch_chunk_delta(p, stream);
   if (p.dk == 128 && p.dv == 128) return launch_typed<128, 128>(p, stream);
   if (p.dk == 128 && p.dv == 64) return launch_typed<128, 64>(p, stream);
   if (p.dk == 64 && p.dv == 128) return launch_typed<64, 128>(p, stream);

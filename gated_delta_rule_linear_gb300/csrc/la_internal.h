@@ -56,6 +56,7 @@ unsigned *status_word();
 int launch_chunk_simt(const ChunkParams &p, cudaStream_t stream);
 int launch_chunk_tc(const ChunkParams &p, cudaStream_t stream);
 int launch_chunk_ws(const ChunkParams &p, cudaStream_t stream);
+int launch_chunk_delta(const ChunkParams &p, cudaStream_t stream);
 int launch_step(const StepParams &p, cudaStream_t stream);
 
 // Which chunk-forward kernel a shape goes to (host-side selection).

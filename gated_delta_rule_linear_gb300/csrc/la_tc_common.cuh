@@ -50,6 +50,78 @@ __device__ __forceinline__ float bf16_at(const uint8_t *base, uint32_t off) {
 }
 
 
+// ---------------------------------------------------------- pipeline helpers
+
+__device__ __forceinline__ void group_sync(int id) {
+  asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
+}
+// All-reduce of a predicate over one 128-thread group (also a barrier).
+__device__ __forceinline__ bool group_all(bool v, int id) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id)
+      : "memory");
+  return r != 0;
+}
+
+// Bounded wait that also gives up as soon as another role has aborted.
+constexpr uint32_t kSpinLimit = 1u << 24;  // polls before a wait gives up (well over 100 ms)
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                              unsigned *status) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+  }
+  *abort_flag = 1;
+  atomicOr(status, kStatusTimeout);
+  return false;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// 32 consecutive fp32 values (columns c0..c0+31 of `row`, c0 % 32 == 0) as
+// bf16 into a K-major 128B-swizzled operand with atoms `atom_bytes` apart.
+__device__ __forceinline__ void store_row32_bf16(uint8_t *base, uint32_t atom_bytes, int row, int c0,
+                                                 const float *v) {
+  uint8_t *a = base + (uint32_t)(c0 >> 6) * atom_bytes;
+  const int cc = c0 & 63;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    uint4 u;
+    u.x = pack_bf16(v[8 * g + 0], v[8 * g + 1]);
+    u.y = pack_bf16(v[8 * g + 2], v[8 * g + 3]);
+    u.z = pack_bf16(v[8 * g + 4], v[8 * g + 5]);
+    u.w = pack_bf16(v[8 * g + 6], v[8 * g + 7]);
+    *reinterpret_cast<uint4 *>(a + sw128_off(row, cc + 8 * g)) = u;
+  }
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &u, float *f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ uint4 pack8(const float *f) {
+  uint4 u;
+  u.x = pack_bf16(f[0], f[1]);
+  u.y = pack_bf16(f[2], f[3]);
+  u.z = pack_bf16(f[4], f[5]);
+  u.w = pack_bf16(f[6], f[7]);
+  return u;
+}
+
+
 // ---------------------------------------------------------------- host side
 
 inline PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
