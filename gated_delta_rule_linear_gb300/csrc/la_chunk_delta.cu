@@ -76,6 +76,51 @@ __host__ __device__ inline DLayout d_layout() {
   return L;
 }
 
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+// Warp-level 16x8x8 tf32 MMA (register fragments), fp32 accumulate.
+__device__ __forceinline__ void mma_16x8x8_tf32(float *d, const uint32_t *a, const uint32_t *b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// acc (16x16, two 16x8 fragments) += Ab (16x16) * Bb (16x16), fp32 blocks of
+// pitch kAp in shared memory, one warp.
+__device__ __forceinline__ void block_mma_16(float (&acc)[2][4], const float *Ab, const float *Bb, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int ks = 0; ks < 2; ++ks) {
+    uint32_t a[4];
+    a[0] = to_tf32(Ab[g * kAp + 8 * ks + t]);
+    a[1] = to_tf32(Ab[(g + 8) * kAp + 8 * ks + t]);
+    a[2] = to_tf32(Ab[g * kAp + 8 * ks + t + 4]);
+    a[3] = to_tf32(Ab[(g + 8) * kAp + 8 * ks + t + 4]);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      uint32_t b[2];
+      b[0] = to_tf32(Bb[(8 * ks + t) * kAp + 8 * nt + g]);
+      b[1] = to_tf32(Bb[(8 * ks + t + 4) * kAp + 8 * nt + g]);
+      mma_16x8x8_tf32(acc[nt], a, b);
+    }
+  }
+}
+// Store a 16x16 accumulator (scaled by sgn) into an fp32 block of pitch kAp.
+__device__ __forceinline__ void block_store_16(float *Cb, const float (&acc)[2][4], float sgn, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    Cb[g * kAp + 8 * nt + 2 * t] = sgn * acc[nt][0];
+    Cb[g * kAp + 8 * nt + 2 * t + 1] = sgn * acc[nt][1];
+    Cb[(g + 8) * kAp + 8 * nt + 2 * t] = sgn * acc[nt][2];
+    Cb[(g + 8) * kAp + 8 * nt + 2 * t + 1] = sgn * acc[nt][3];
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -416,13 +461,14 @@ chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q
         const float b2r = ms[kMsB2 + r], fr = ms[kMsF + r];
 #pragma unroll 1
         for (int s0 = 0; s0 < kC; s0 += 32) {
-          float d[32];
+          float d[32], fs[32];
+          load32(ms + (fast ? kMsVS : kMsB2) + s0, fs);
           tmem_ld32(tl + kColD1 + s0, d);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int sc = s0 + e;
-            const float g = fast ? fr * ms[kMsVS + sc] : exp2f(sc <= r ? b2r - ms[kMsB2 + sc] : 0.f);
+            const float g = fast ? fr * fs[e] : exp2f(sc <= r ? b2r - fs[e] : 0.f);
             d[e] = (sc <= r && r < n) ? d[e] * g : 0.f;
           }
           store_row32_bf16(sm + L.p + (uint32_t)(j & 1) * 8192u, 8192, r, s0, d);
@@ -432,15 +478,18 @@ chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q
         const float b2r = ms[kMsB2 + r], ar = ms[kMsAR + r], br = ms[kMsBeta + r];
 #pragma unroll 1
         for (int s0 = 0; s0 < kC; s0 += 32) {
-          float d[32];
+          float d[32], fs[32];
+          load32(ms + (fast ? kMsVS : kMsB2) + s0, fs);
           tmem_ld32(tl + kColD1 + s0, d);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int sc = s0 + e;
-            const float g = fast ? ar * ms[kMsVS + sc] : br * exp2f(sc < r ? b2r - ms[kMsB2 + sc] : 0.f);
-            Af[r * kAp + sc] = (sc < r && r < n) ? d[e] * g : 0.f;
+            const float g = fast ? ar * fs[e] : br * exp2f(sc < r ? b2r - fs[e] : 0.f);
+            d[e] = (sc < r && r < n) ? d[e] * g : 0.f;
           }
+#pragma unroll
+          for (int e = 0; e < 32; ++e) Af[r * kAp + s0 + e] = d[e];
         }
       }
       tc_fence_before();
@@ -462,64 +511,46 @@ chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q
         for (int r = 0; r < 16; ++r) Tf[(base + r) * kAp + base + jc] = x[r];
       }
       group_sync(kBarKG);
+      // off-diagonal blocks level by level: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj,
+      // one warp per 16x16 output block (tf32 warp MMAs)
+      {
+        const int kw = kg >> 5;
 #pragma unroll
-      for (int lvl = 1; lvl < 4; ++lvl) {
-        const int nit = 2 * (4 - lvl);  // output elements per thread at this level
-        float xv[6];
-        // X = sum_{k=j}^{i-1} A_ik T_kj for blocks (i, j = i - lvl), into registers
-#pragma unroll
-        for (int it = 0; it < nit; ++it) {
-          const int e = kg + it * 128;
-          const int bi = e >> 8, a = (e >> 4) & 15, bc = e & 15, ib = bi + lvl, jb = bi;
-          float acc = 0.f;
-          for (int kb = jb; kb < ib; ++kb)
-#pragma unroll
-            for (int m = 0; m < 16; ++m)
-              acc = fmaf(Af[(ib * 16 + a) * kAp + kb * 16 + m], Tf[(kb * 16 + m) * kAp + jb * 16 + bc], acc);
-          xv[it] = acc;
+        for (int lvl = 1; lvl < 4; ++lvl) {
+          if (kw < 4 - lvl) {
+            const int ib = kw + lvl, jb = kw;
+            float acc[2][4] = {};
+            for (int kb = jb; kb < ib; ++kb)
+              block_mma_16(acc, Af + ib * 16 * kAp + kb * 16, Tf + kb * 16 * kAp + jb * 16, lane);
+            float *Tij = Tf + ib * 16 * kAp + jb * 16;
+            block_store_16(Tij, acc, 1.f, lane);  // X parked in its output block
+            __syncwarp();
+            float acc2[2][4] = {};
+            block_mma_16(acc2, Tf + ib * 16 * kAp + ib * 16, Tij, lane);
+            __syncwarp();
+            block_store_16(Tij, acc2, -1.f, lane);
+          }
+          group_sync(kBarKG);
         }
-        group_sync(kBarKG);
-#pragma unroll
-        for (int it = 0; it < nit; ++it) {  // X parked in its output block
-          const int e = kg + it * 128;
-          const int bi = e >> 8, a = (e >> 4) & 15, bc = e & 15, ib = bi + lvl, jb = bi;
-          Tf[(ib * 16 + a) * kAp + jb * 16 + bc] = xv[it];
-        }
-        group_sync(kBarKG);
-#pragma unroll
-        for (int it = 0; it < nit; ++it) {  // T_ij = -T_ii X
-          const int e = kg + it * 128;
-          const int bi = e >> 8, a = (e >> 4) & 15, bc = e & 15, ib = bi + lvl, jb = bi;
-          float acc = 0.f;
-#pragma unroll
-          for (int m = 0; m < 16; ++m)
-            if (m <= a) acc = fmaf(Tf[(ib * 16 + a) * kAp + ib * 16 + m], Tf[(ib * 16 + m) * kAp + jb * 16 + bc], acc);
-          xv[it] = -acc;
-        }
-        group_sync(kBarKG);
-#pragma unroll
-        for (int it = 0; it < nit; ++it) {
-          const int e = kg + it * 128;
-          const int bi = e >> 8, a = (e >> 4) & 15, bc = e & 15, ib = bi + lvl, jb = bi;
-          Tf[(ib * 16 + a) * kAp + jb * 16 + bc] = xv[it];
-        }
-        group_sync(kBarKG);
       }
       // ---- T' and T'' (bf16) once chunk j-1 has finished with the buffers
       ok = wait_or_abort(kfree, (j & 1) ^ 1, abort_flag, p.status);
       if (!group_all(ok, kBarKG)) break;
       {
         const int r = kg >> 1, g0 = (kg & 1) * 4;
+        float tv[32], bt[32], bb[32];
+        load32(ms + kMsBeta + g0 * 8, bt);
+        load32(ms + kMsBEB + g0 * 8, bb);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) tv[e] = (g0 * 8 + e <= r) ? Tf[r * kAp + g0 * 8 + e] : 0.f;
 #pragma unroll
         for (int gi = 0; gi < 4; ++gi) {
           const int g8 = g0 + gi;
           float f1[8], f2[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const int sc = g8 * 8 + e;
-            const float t = (sc <= r) ? Tf[r * kAp + sc] : 0.f;
-            f1[e] = t * ms[kMsBeta + sc];
-            f2[e] = t * ms[kMsBEB + sc];
+            f1[e] = tv[gi * 8 + e] * bt[gi * 8 + e];
+            f2[e] = tv[gi * 8 + e] * bb[gi * 8 + e];
           }
           *reinterpret_cast<uint4 *>(sm + L.tp + sw128_off(r, g8 * 8)) = pack8(f1);
           *reinterpret_cast<uint4 *>(sm + L.tpp + sw128_off(r, g8 * 8)) = pack8(f2);

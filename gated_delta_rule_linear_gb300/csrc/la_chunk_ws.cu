@@ -331,12 +331,14 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
           tmem_ld32(tl + kColS + c0, x);
           tmem_wait_ld();
           if (gla) {
-            float cp[32];
+            float cp[32], fm[32], fl[32];
+            load32(ms + kMsBM + c0, fm);
+            load32(ms + kMsBL + c0, fl);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) cp[e] = x[e] * ms[kMsBM + c0 + e];
+            for (int e = 0; e < 32; ++e) cp[e] = x[e] * fm[e];
             store_row32_bf16(sm + L.st, 16384, v, c0, cp);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) x[e] *= ms[kMsBL + c0 + e];
+            for (int e = 0; e < 32; ++e) x[e] *= fl[e];
             tmem_st32(tl + kColS + c0, x);
           } else {
             store_row32_bf16(sm + L.st, 16384, v, c0, x);
@@ -371,8 +373,10 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
           tmem_ld32(tl + kColO + ob * 64 + r0, a);
           tmem_wait_ld();
           if (elu) {
+            float den[32];
+            load32(ms + kMsDen + r0, den);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) a[e] = __fdividef(a[e], ms[kMsDen + r0 + e]);
+            for (int e = 0; e < 32; ++e) a[e] = __fdividef(a[e], den[e]);
           }
           // rows (r, r+1) of neighbouring lanes are exchanged so that each
           // thread writes two adjacent bf16 of one row
@@ -501,7 +505,8 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
         float rowsum = 0.f;
 #pragma unroll 1
         for (int s0 = 0; s0 < kC; s0 += 32) {
-          float d[32];
+          float d[32], b2s[32];
+          if (sgate) load32(ms + kMsB2 + s0, b2s);
           tmem_ld32(tl + kColD1 + (uint32_t)(j & 1) * 64u + s0, d);
           tmem_wait_ld();
 #pragma unroll
@@ -510,7 +515,7 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
             float x = (sc <= r && r < n) ? d[e] : 0.f;
             // fast path: P' = Q K^T e^{b_r - b_last} against e^{b_last - b_s} V;
             // exact path: P = Q K^T e^{b_r - b_s} against Kt = e^{b_last - b_s} K
-            if (sgate) x *= fast ? fr : exp2f(sc <= r ? b2r - ms[kMsB2 + sc] : 0.f);
+            if (sgate) x *= fast ? fr : exp2f(sc <= r ? b2r - b2s[e] : 0.f);
             if (elu) {
               x = __bfloat162float(__float2bfloat16_rn(x));
               rowsum += x;
@@ -579,6 +584,11 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
         constexpr int kHalf = DK / 16;  // 16-byte groups per half row
         const int r = kg >> 1, g0 = (kg & 1) * kHalf;
         const float rs = sgate ? ms[kMsVS + r] : 1.f;
+        float lm[gla ? 8 * kHalf : 1];
+        if (gla) {
+#pragma unroll
+          for (int q = 0; q < kHalf / 4; ++q) load32(ms + kMsLM + g0 * 8 + 32 * q, lm + 32 * q);
+        }
         uint4 u[kHalf];
 #pragma unroll
         for (int i = 0; i < kHalf; ++i) {
@@ -591,7 +601,7 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
           float f[8];
           unpack8(u[i], f);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] *= gla ? ms[kMsLM + g8 * 8 + e] : rs;
+          for (int e = 0; e < 8; ++e) f[e] *= gla ? lm[(gla ? i * 8 + e : 0)] : rs;
           *reinterpret_cast<uint4 *>(qk + 8192 + (g8 >> 3) * 16384 + sw128_off(r, (g8 & 7) * 8)) = pack8(f);
         }
       }

@@ -82,6 +82,31 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
   return false;
 }
 
+// Group-wide wait: one elected thread polls the mbarrier while the rest of
+// the 128-thread group sleeps on the group's named barrier (no issue slots
+// used); the outcome is shared by the barrier reduction, which also orders
+// memory for the whole group.
+__device__ __forceinline__ bool group_wait(uint64_t *bar, uint32_t parity, int gtid, int bar_id,
+                                           volatile int *abort_flag, unsigned *status) {
+  bool ok = true;
+  if (gtid == 0) ok = wait_or_abort(bar, parity, abort_flag, status);
+  return group_all(ok, bar_id);
+}
+
+// 32 consecutive floats (16-byte aligned) into registers with 128-bit loads,
+// before a loop that also stores to shared memory (so the loads are not
+// serialised behind those stores).
+__device__ __forceinline__ void load32(const float *p, float *out) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float4 t = reinterpret_cast<const float4 *>(p)[q];
+    out[4 * q] = t.x;
+    out[4 * q + 1] = t.y;
+    out[4 * q + 2] = t.z;
+    out[4 * q + 3] = t.w;
+  }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t *>(&h);
