@@ -151,7 +151,7 @@ chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q
   if (tid == 0) {
     for (int s = 0; s < kNS; ++s) {
       mbar_init(&full[s], 2);   // TMA bytes + the producer's gate prefix
-      mbar_init(&empty[s], 2);  // key group + state-side MMA commit
+      mbar_init(&empty[s], 1);  // state-side MMA commit after the chunk's last MMA
       mbar_init(&key_ready[s], 1);
     }
     for (int m = 0; m < kNM; ++m) mbar_init(&mfree[m], 1);
@@ -328,15 +328,15 @@ chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q
         mma_commit(u_full);
         if (!wait_or_abort(u_ready, i & 1, abort_flag, p.status)) break;
         tc_fence_after();
+        const uint32_t a_p = smem_u32(sm + L.p + (uint32_t)(i & 1) * 8192u);
+#pragma unroll
+        for (int kk = 0; kk < kC / 16; ++kk)
+          mma_bf16(d_o, desc_sw128(a_wu + kk * 32, 16, 1024), desc_sw128(a_p + kk * 32, 16, 1024), id_o2, 1);
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)
           mma_bf16(tbase + kColS, desc_sw128(a_wu + kk * 32, 16, 1024),
                    desc_sw128(a_qk + 8192 + kk * 2048, 16384, 1024), id_su, 1);
         mma_commit(s_done);
-        const uint32_t a_p = smem_u32(sm + L.p + (uint32_t)(i & 1) * 8192u);
-#pragma unroll
-        for (int kk = 0; kk < kC / 16; ++kk)
-          mma_bf16(d_o, desc_sw128(a_wu + kk * 32, 16, 1024), desc_sw128(a_p + kk * 32, 16, 1024), id_o2, 1);
         mma_commit(&o_done[i & 1]);
         mma_commit(&empty[s]);
         mma_commit(kfree);
@@ -359,10 +359,40 @@ chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q
       if (i < nchunks) {
         const int s = i % kNS;
         const float *ms = mslot(i);
-        bool ok = wait_or_abort(&key_ready[s], (i / kNS) & 1, abort_flag, p.status);
+        // W^T of this chunk is in TMEM, and the previous chunk's MMAs have
+        // finished with the shared -W / U buffer and with the state
+        bool ok = wait_or_abort(w_full, i & 1, abort_flag, p.status);
         if (ok && i > 0) ok = wait_or_abort(s_done, (i - 1) & 1, abort_flag, p.status);
         if (!group_all(ok, kBarSG)) { alive = false; break; }
         tc_fence_after();
+        // -W as the MN-major B operand [c][r] (TMEM lane = key channel c)
+#pragma unroll 1
+        for (int r0 = 0; r0 < kC; r0 += 32) {
+          float x[32];
+          tmem_ld32(tl + kColW + r0, x);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[e] = -x[e];
+          store_row32_bf16(sm + L.wu, 16384, v, r0, x);
+        }
+        // Qt = Diag(e^b) Q, Kt = Diag(e^{b_last - b}) K in place (row v of [Q; K])
+        if (gated) {
+          uint8_t *qk = stage(s) + L.qk;
+          const int r = v & (kC - 1);
+          const float rs = (v < kC) ? ms[kMsEB + r] : ms[kMsVS + r];
+          uint4 u[16];
+#pragma unroll
+          for (int g8 = 0; g8 < 16; ++g8)
+            u[g8] = *reinterpret_cast<const uint4 *>(qk + (g8 >> 3) * 16384 + sw128_off(v, (g8 & 7) * 8));
+#pragma unroll
+          for (int g8 = 0; g8 < 16; ++g8) {
+            float f[8];
+            unpack8(u[g8], f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] *= rs;
+            *reinterpret_cast<uint4 *>(qk + (g8 >> 3) * 16384 + sw128_off(v, (g8 & 7) * 8)) = pack8(f);
+          }
+        }
         // state round trip: bf16 operand copy of S_prev, decay in place
         const float dec = ms[kMsDec];
 #pragma unroll 1
@@ -449,7 +479,6 @@ chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q
       const int s = j % kNS, n = min(kC, T - j * kC);
       uint8_t *st = stage(s);
       float *ms = mslot(j);
-      uint8_t *qk = st + L.qk;
       bool ok = wait_or_abort(&full[s], (j / kNS) & 1, abort_flag, p.status);
       if (ok) ok = wait_or_abort(d1_full, j & 1, abort_flag, p.status);
       if (!group_all(ok, kBarKG)) break;
@@ -558,44 +587,9 @@ chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q
       }
       fence_proxy_async();
       group_sync(kBarKG);
-      if (kg == 0) mbar_arrive(t_ready);
-      // ---- -W (MN-major B operand [c][r]) from W^T in TMEM (lane = key channel c)
-      ok = wait_or_abort(w_full, j & 1, abort_flag, p.status);
-      if (!group_all(ok, kBarKG)) break;
-      tc_fence_after();
-#pragma unroll 1
-      for (int r0 = 0; r0 < kC; r0 += 32) {
-        float x[32];
-        tmem_ld32(tl + kColW + r0, x);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) x[e] = -x[e];
-        store_row32_bf16(sm + L.wu, 16384, kg, r0, x);
-      }
-      // ---- Qt = Diag(e^b) Q, Kt = Diag(e^{b_last - b}) K in place
-      if (gated) {
-        const int row = kg;  // row of [Q; K]
-        const int r = row & (kC - 1);
-        const float rs = (row < kC) ? ms[kMsEB + r] : ms[kMsVS + r];
-        uint4 u[16];
-#pragma unroll
-        for (int g8 = 0; g8 < 16; ++g8)
-          u[g8] = *reinterpret_cast<const uint4 *>(qk + (g8 >> 3) * 16384 + sw128_off(row, (g8 & 7) * 8));
-#pragma unroll
-        for (int g8 = 0; g8 < 16; ++g8) {
-          float f[8];
-          unpack8(u[g8], f);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] *= rs;
-          *reinterpret_cast<uint4 *>(qk + (g8 >> 3) * 16384 + sw128_off(row, (g8 & 7) * 8)) = pack8(f);
-        }
-      }
-      tc_fence_before();
-      fence_proxy_async();
-      group_sync(kBarKG);
       if (kg == 0) {
-        mbar_arrive(&key_ready[s]);
-        mbar_arrive(&empty[s]);
+        mbar_arrive(t_ready);        // T'' for the W MMA
+        mbar_arrive(&key_ready[s]);  // T' and P for the state side
       }
     }
   }
