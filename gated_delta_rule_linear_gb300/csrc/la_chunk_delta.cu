@@ -43,7 +43,7 @@ constexpr int kSG = 128, kKG = 256;
 constexpr int kBarSG = 1, kBarKG = 2;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kFastLimit = 100.f;
-constexpr int kAp = kC + 1;  // fp32 pitch of A and T
+constexpr int kAp = kC + 4;  // pitch of A and T: 16-byte rows, conflict-free MMA fragments
 
 // per-chunk scalars (floats)
 constexpr int kMsB2 = 0, kMsEB = 64, kMsBeta = 128, kMsDec = 192, kMsB2L = 193, kMsFast = 194,
@@ -81,6 +81,7 @@ __device__ __forceinline__ uint32_t to_tf32(float x) {
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
   return r;
 }
+__device__ __forceinline__ float round_tf32(float x) { return __uint_as_float(to_tf32(x)); }
 // Warp-level 16x8x8 tf32 MMA (register fragments), fp32 accumulate.
 __device__ __forceinline__ void mma_16x8x8_tf32(float *d, const uint32_t *a, const uint32_t *b) {
   asm volatile(
@@ -89,35 +90,35 @@ __device__ __forceinline__ void mma_16x8x8_tf32(float *d, const uint32_t *a, con
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
-// acc (16x16, two 16x8 fragments) += Ab (16x16) * Bb (16x16), fp32 blocks of
-// pitch kAp in shared memory, one warp.
+// acc (16x16, two 16x8 fragments) += Ab (16x16) * Bb (16x16): blocks of pitch
+// kAp in shared memory holding values already rounded to tf32; one warp.
 __device__ __forceinline__ void block_mma_16(float (&acc)[2][4], const float *Ab, const float *Bb, int lane) {
   const int g = lane >> 2, t = lane & 3;
 #pragma unroll
   for (int ks = 0; ks < 2; ++ks) {
     uint32_t a[4];
-    a[0] = to_tf32(Ab[g * kAp + 8 * ks + t]);
-    a[1] = to_tf32(Ab[(g + 8) * kAp + 8 * ks + t]);
-    a[2] = to_tf32(Ab[g * kAp + 8 * ks + t + 4]);
-    a[3] = to_tf32(Ab[(g + 8) * kAp + 8 * ks + t + 4]);
+    a[0] = __float_as_uint(Ab[g * kAp + 8 * ks + t]);
+    a[1] = __float_as_uint(Ab[(g + 8) * kAp + 8 * ks + t]);
+    a[2] = __float_as_uint(Ab[g * kAp + 8 * ks + t + 4]);
+    a[3] = __float_as_uint(Ab[(g + 8) * kAp + 8 * ks + t + 4]);
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       uint32_t b[2];
-      b[0] = to_tf32(Bb[(8 * ks + t) * kAp + 8 * nt + g]);
-      b[1] = to_tf32(Bb[(8 * ks + t + 4) * kAp + 8 * nt + g]);
+      b[0] = __float_as_uint(Bb[(8 * ks + t) * kAp + 8 * nt + g]);
+      b[1] = __float_as_uint(Bb[(8 * ks + t + 4) * kAp + 8 * nt + g]);
       mma_16x8x8_tf32(acc[nt], a, b);
     }
   }
 }
-// Store a 16x16 accumulator (scaled by sgn) into an fp32 block of pitch kAp.
+// Store a 16x16 accumulator (scaled by sgn, rounded to tf32) into a block of pitch kAp.
 __device__ __forceinline__ void block_store_16(float *Cb, const float (&acc)[2][4], float sgn, int lane) {
   const int g = lane >> 2, t = lane & 3;
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
-    Cb[g * kAp + 8 * nt + 2 * t] = sgn * acc[nt][0];
-    Cb[g * kAp + 8 * nt + 2 * t + 1] = sgn * acc[nt][1];
-    Cb[(g + 8) * kAp + 8 * nt + 2 * t] = sgn * acc[nt][2];
-    Cb[(g + 8) * kAp + 8 * nt + 2 * t + 1] = sgn * acc[nt][3];
+    *reinterpret_cast<float2 *>(Cb + g * kAp + 8 * nt + 2 * t) =
+        make_float2(round_tf32(sgn * acc[nt][0]), round_tf32(sgn * acc[nt][1]));
+    *reinterpret_cast<float2 *>(Cb + (g + 8) * kAp + 8 * nt + 2 * t) =
+        make_float2(round_tf32(sgn * acc[nt][2]), round_tf32(sgn * acc[nt][3]));
   }
 }
 
@@ -515,10 +516,12 @@ chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q
           for (int e = 0; e < 32; ++e) {
             const int sc = s0 + e;
             const float g = fast ? ar * fs[e] : br * exp2f(sc < r ? b2r - fs[e] : 0.f);
-            d[e] = (sc < r && r < n) ? d[e] * g : 0.f;
+            d[e] = (sc < r && r < n) ? round_tf32(d[e] * g) : 0.f;
           }
 #pragma unroll
-          for (int e = 0; e < 32; ++e) Af[r * kAp + s0 + e] = d[e];
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4 *>(Af + r * kAp + s0 + 4 * q) =
+                make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
         }
       }
       tc_fence_before();
@@ -537,7 +540,7 @@ chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q
           x[r] = (r < jc) ? 0.f : acc;
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Tf[(base + r) * kAp + base + jc] = x[r];
+        for (int r = 0; r < 16; ++r) Tf[(base + r) * kAp + base + jc] = round_tf32(x[r]);
       }
       group_sync(kBarKG);
       // off-diagonal blocks level by level: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj,
@@ -570,8 +573,9 @@ chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q
         float tv[32], bt[32], bb[32];
         load32(ms + kMsBeta + g0 * 8, bt);
         load32(ms + kMsBEB + g0 * 8, bb);
+        load32(Tf + r * kAp + g0 * 8, tv);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) tv[e] = (g0 * 8 + e <= r) ? Tf[r * kAp + g0 * 8 + e] : 0.f;
+        for (int e = 0; e < 32; ++e) tv[e] = (g0 * 8 + e <= r) ? tv[e] : 0.f;
 #pragma unroll
         for (int gi = 0; gi < 4; ++gi) {
           const int g8 = g0 + gi;
