@@ -39,8 +39,19 @@ import workloads  # noqa: E402
 METRIC = "tokens/sec and TFLOP/s of chunk fwd at 1 GB300; % of roofline"
 UNIT = "tokens/s"
 PROFILE_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-KERNEL_SOURCES = ["gated_delta_rule_linear_gb300/csrc/la_chunk_tc.cu",
+KERNEL_SOURCES = ["gated_delta_rule_linear_gb300/csrc/la_chunk_delta.cu",
+                  "gated_delta_rule_linear_gb300/csrc/la_chunk_ws.cu",
+                  "gated_delta_rule_linear_gb300/csrc/la_tc_common.cuh",
                   "gated_delta_rule_linear_gb300/csrc/la_sm100.cuh"]
+
+
+def kernel_name(wl) -> str:
+    """The kernel one la_chunk_fwd launch of this workload runs."""
+    if wl.dtype == "f32":
+        return "chunk_simt_kernel"
+    if wl.mode == "gdn":
+        return "chunk_delta_kernel" if wl.dk == 128 and wl.dv == 128 else "chunk_tc_kernel"
+    return "chunk_ws_kernel"
 
 
 # ---------------------------------------------------------------- cost model
@@ -312,7 +323,7 @@ def main():
     roof["traffic"] = traffic
     roof["peak_source"] = peak_src
     roof["algorithmic_bytes"] = alg_bytes
-    roof["kernel"] = "chunk_tc_kernel" if wl.dtype == "bf16" else "chunk_simt_kernel"
+    roof["kernel"] = kernel_name(wl)
     roof["launch_ms_mean"] = round(statistics.mean(launch_ms), 4)
 
     # ---- end to end through the C ABI with host buffers ----
