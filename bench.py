@@ -41,13 +41,16 @@ UNIT = "tokens/s"
 PROFILE_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 KERNEL_SOURCES = ["gated_delta_rule_linear_gb300/csrc/la_chunk_delta.cu",
                   "gated_delta_rule_linear_gb300/csrc/la_chunk_ws.cu",
+                  "gated_delta_rule_linear_gb300/csrc/la_chunk_mat.cu",
                   "gated_delta_rule_linear_gb300/csrc/la_tc_common.cuh",
                   "gated_delta_rule_linear_gb300/csrc/la_sm100.cuh"]
 
 
-def kernel_name(wl) -> str:
+def kernel_name(wl, variant=None) -> str:
     """The kernel one la_chunk_fwd launch of this workload runs."""
-    if wl.dtype == "f32":
+    if variant == "mat":
+        return "chunk_state_kernel+chunk_output_kernel"
+    if wl.dtype == "f32" or variant == "simt":
         return "chunk_simt_kernel"
     if wl.mode == "gdn":
         return "chunk_delta_kernel" if wl.dk == 128 and wl.dv == 128 else "chunk_tc_kernel"
@@ -226,7 +229,11 @@ def main():
     ap.add_argument("--B", type=int, default=None, help="override batch (profiling of a smaller case)")
     ap.add_argument("--H", type=int, default=None)
     ap.add_argument("--T", type=int, default=None)
+    ap.add_argument("--variant", default=None, choices=["tc", "nonmat", "mat", "simt"],
+                    help="force a kernel variant (default: the library's per-shape choice)")
     args = ap.parse_args()
+    if args.variant:
+        os.environ["LA_VARIANT"] = args.variant
     if args.warmup < 3:
         args.warmup = 3
 
@@ -323,7 +330,7 @@ def main():
     roof["traffic"] = traffic
     roof["peak_source"] = peak_src
     roof["algorithmic_bytes"] = alg_bytes
-    roof["kernel"] = kernel_name(wl)
+    roof["kernel"] = kernel_name(wl, args.variant)
     roof["launch_ms_mean"] = round(statistics.mean(launch_ms), 4)
 
     # ---- end to end through the C ABI with host buffers ----
@@ -353,7 +360,7 @@ def main():
             "cpu_baseline": cpu,
             "clocks": clk,
             "e2e": e2e,
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * (2 if args.variant == "mat" else 1),
         }
         print(json.dumps(line), flush=True)
     if dist:

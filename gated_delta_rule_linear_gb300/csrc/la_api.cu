@@ -22,6 +22,34 @@ constexpr int kMaxDevices = 64;
 unsigned *g_status_ptr[kMaxDevices] = {};
 std::mutex g_status_mu;
 
+// Stream-ordered pool for the materialised variant's workspace, one per
+// device, owned by the library. It keeps freed memory for the next call
+// (release threshold = max) instead of unmapping it at every synchronisation.
+cudaMemPool_t g_pool[kMaxDevices] = {};
+std::mutex g_pool_mu;
+
+cudaMemPool_t workspace_pool() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_pool_mu);
+  if (!g_pool[dev]) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
+    uint64_t keep = ~0ull;
+    if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+      cudaMemPoolDestroy(pool);
+      return nullptr;
+    }
+    g_pool[dev] = pool;
+  }
+  return g_pool[dev];
+}
+
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 }  // namespace
 
@@ -44,13 +72,16 @@ unsigned *status_word() {
   return g_status_ptr[dev];
 }
 
-// Host-side kernel choice. bf16 inputs go to the tensor-core kernel when it
-// supports the shape, float32 inputs to the CUDA-core kernel. LA_VARIANT
-// (auto | tc | simt) overrides the choice for measurement sweeps.
+// Host-side kernel choice. float32 inputs go to the CUDA-core kernel. bf16
+// inputs go to the fused (non-materialised) tensor-core kernel, or, for the
+// unit-write modes when there are too few heads to fill the GPU, to the
+// materialised two-phase variant. LA_VARIANT (auto | tc | nonmat | mat |
+// simt) overrides the choice for measurement sweeps.
 int select_variant(const ChunkParams &p, int *chunk_out) {
   const char *env = getenv("LA_VARIANT");
   int want = -1;
-  if (env && strcmp(env, "tc") == 0) want = kVariantTc;
+  if (env && (strcmp(env, "tc") == 0 || strcmp(env, "nonmat") == 0)) want = kVariantTc;
+  if (env && strcmp(env, "mat") == 0) want = kVariantMat;
   if (env && strcmp(env, "simt") == 0) want = kVariantSimt;
   const int C = p.C == 0 ? 64 : p.C;
   if (C != 64) {
@@ -58,7 +89,11 @@ int select_variant(const ChunkParams &p, int *chunk_out) {
     return -1;
   }
   *chunk_out = C;
-  if (p.f32) return want == kVariantTc ? -2 : kVariantSimt;
+  if (p.f32) return (want == kVariantTc || want == kVariantMat) ? -2 : kVariantSimt;
+  if (want == kVariantMat && p.kind == kGdn) {
+    set_error("la_chunk_fwd: the materialised variant covers the unit-write modes only");
+    return -1;
+  }
   if (want >= 0) return want;
   return kVariantTc;
 }
@@ -174,6 +209,28 @@ int la_chunk_fwd(const void *q, const void *k, const void *v, const float *g, co
   if (variant < 0) return LA_ERR_UNSUPPORTED;
   p.C = chunk;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (variant == kVariantMat) {
+    // stream-ordered workspace: allocated and released on the caller's stream
+    void *ws = nullptr;
+    const size_t bytes = mat_workspace_bytes(p);
+    cudaMemPool_t pool = workspace_pool();
+    if (!pool) {
+      set_error("%s: could not create the workspace pool: %s", fn, cudaGetErrorString(cudaGetLastError()));
+      return LA_ERR_CUDA;
+    }
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes, pool, s);
+    if (e != cudaSuccess) {
+      set_error("%s: workspace allocation of %zu bytes failed: %s", fn, bytes, cudaGetErrorString(e));
+      return LA_ERR_CUDA;
+    }
+    rc = launch_chunk_mat(p, ws, s);
+    e = cudaFreeAsync(ws, s);
+    if (rc == LA_OK && e != cudaSuccess) {
+      set_error("%s: workspace release failed: %s", fn, cudaGetErrorString(e));
+      return LA_ERR_CUDA;
+    }
+    return rc;
+  }
   return variant == kVariantTc ? launch_chunk_tc(p, s) : launch_chunk_simt(p, s);
 }
 

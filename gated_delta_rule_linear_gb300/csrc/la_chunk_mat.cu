@@ -1,0 +1,737 @@
+// Materialised chunk forward for the unit-write modes (plain linear, elu+1,
+// RetNet, scalar decay, GLA), bf16 inputs: the two-phase variant "Talk Linear
+// Attention" section 4.1.2 describes (a serial state pass that materialises
+// the chunk-boundary states, then a fully parallel output pass).
+//
+//   state pass  one CTA per (b, h): S^T stays in TMEM; per chunk it writes the
+//               incoming state S_{i-1} as a bf16 operand image (one bulk copy
+//               of the 128B-swizzled shared-memory tile) and applies
+//               S <- Diag(e^{b_last}) S + Kt^T V on the tensor core.
+//   output pass one CTA per (b, h, chunk), all chunks in parallel:
+//               O = Diag(e^{b}) Q S_{i-1} + P V with P the masked, decayed
+//               local scores, S_{i-1} loaded straight into its operand layout.
+//
+// The workspace (one state image per chunk, plus z per chunk for elu+1) is
+// provided by the caller of these launchers.
+#include "la_tc_common.cuh"
+
+namespace la {
+namespace {
+
+using namespace sm100;
+using namespace tc;
+
+constexpr int kMid = kC / 2 - 1;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__host__ __device__ inline uint32_t up1k(uint32_t x) { return (x + 1023u) & ~1023u; }
+// bytes of one materialised state image: S^T as 128 rows (value axis, zero
+// padded when dv = 64) x dk bf16 in 64-column 128B-swizzled atoms
+__host__ __device__ constexpr uint32_t blob_bytes(int dk) { return (uint32_t)(dk / 64) * 16384u; }
+
+// ============================================================ state pass
+// For the unit-write modes every row of S (one key channel) evolves on its
+// own, so a CTA owns one 64-channel key block of one head: it writes exactly
+// one 64-column atom of each state image.
+//
+// The chunk-local update dS_i = V_i^T Kt_i (Kt = K e^{b_last - b}) has no
+// dependency between chunks, so the tensor core computes it for chunks ahead
+// into a ring of TMEM slots, and the state group keeps S^T in registers and
+// runs the scan S_i = Diag(e^{b_last}) S_{i-1} + dS_i ("Talk Linear Attention"
+// section 4.1.2: the states of the chunk boundaries, then the outputs).
+//
+// Roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer, warp 3 TMEM
+// owner, warps 4..7 the state group (lane = value row of S^T: writes S_{i-1}
+// as an image atom, adds dS_i), warps 8..11 the key group (gate prefix, Kt or
+// phi(K) in place, the elu+1 normaliser z).
+constexpr int kAThreads = 384;
+constexpr int kASG = 128;  // first thread of the state group
+constexpr int kAKG = 256;  // first thread of the key group
+constexpr int kASBar = 1, kAKBar = 2;
+constexpr int kKB = 64;    // key channels per state-pass CTA
+constexpr int kANB = 4;    // TMEM slots of dS (64 columns each)
+
+// Stages in flight, so that loads run several chunks ahead of the scan.
+template <int KIND>
+__host__ __device__ constexpr int a_stages() {
+  return KIND == kGla ? 4 : KIND == kElu1 ? 5 : 6;
+}
+constexpr int kAMaxStages = 6;
+
+struct ALayout {
+  uint32_t k, v, g, klo, stage, st, misc, tmp, bar, total;
+};
+__host__ __device__ inline ALayout a_layout(int kind, int ns) {
+  ALayout L;
+  const bool gla = kind == kGla, elu = kind == kElu1;
+  uint32_t o = 0;
+  L.k = o; o += 8192u;
+  L.v = o; o += 16384u;
+  L.g = o; o += gla ? (uint32_t)kC * kKB * 4u : 0u;
+  L.klo = o; o += elu ? 8192u : 0u;
+  L.stage = up1k(o);
+  o = (uint32_t)ns * L.stage;
+  L.st = o; o += 2u * 16384u;             // two image atoms (one bulk store may still be reading)
+  L.misc = o; o += (uint32_t)ns * 1024u;  // per stage: [64..127] e^{b_last} (scalar gates), [128..191] per-channel decay
+  L.tmp = o; o += 512u;                   // key-group exchange between row halves
+  L.bar = o; o += 512u;
+  L.total = o;
+  return L;
+}
+
+template <int DK, int DV, int KIND>
+__global__ void __launch_bounds__(kAThreads, 1)
+chunk_state_kernel(const ChunkParams p, uint8_t *__restrict__ ws, float *__restrict__ zws,
+                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                   const __grid_constant__ CUtensorMap tm_g) {
+  constexpr bool elu = KIND == kElu1, gla = KIND == kGla;
+  constexpr bool sgate = KIND == kRetnet || KIND == kScalar;
+  constexpr int Wmem = DV + (elu ? 1 : 0);
+  constexpr int nkb = DK / kKB;
+  constexpr int NS = a_stages<KIND>();
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const ALayout L = a_layout(KIND, NS);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x / nkb, kb = blockIdx.x % nkb, h = bh % p.H;
+  const int c_base = kb * kKB;
+  const int T = p.T, nch = (T + kC - 1) / kC;
+
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bar);
+  uint64_t *full = bars, *empty = bars + kAMaxStages, *kready = bars + 2 * kAMaxStages;
+  uint64_t *dfull = bars + 3 * kAMaxStages, *dfree = dfull + kANB, *drain = dfree + kANB;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 2);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  float *tmp = reinterpret_cast<float *>(sm + L.tmp);
+  auto stage = [&](int s) { return sm + (uint32_t)s * L.stage; };
+
+  if (warp == 3) {
+    tmem_alloc(tmem_slot, kANB * 64);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    // a stage is refilled once the tensor core has read it and the state group
+    // has read its decay factors, so the key group never laps the state group
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1 + 128);
+      mbar_init(&kready[s], 1);
+    }
+    for (int b = 0; b < kANB; ++b) {
+      mbar_init(&dfull[b], 1);
+      mbar_init(&dfree[b], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (DV == 64) {  // rows 64..127 of the value operand stay zero in every stage
+    for (int i = tid; i < NS * 512; i += kAThreads)
+      reinterpret_cast<uint4 *>(stage(i >> 9) + L.v + 8192)[i & 511] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {  // producer
+      constexpr uint32_t bytes = kKB * kC * 2u + DV * kC * 2u + (gla ? kKB * kC * 4u : 0u);
+      int issued = 0;
+      for (int j = 0; j < nch; ++j) {
+        const int s = j % NS;
+        if (!wait_or_abort(&empty[s], ((j / NS) & 1) ^ 1, abort_flag, p.status)) break;
+        uint8_t *st = stage(s);
+        mbar_arrive_expect_tx(&full[s], bytes);
+        tma_load_3d(st + L.k, &tm_k, &full[s], c_base, j * kC, bh);
+#pragma unroll
+        for (int a = 0; a < DV / 64; ++a) tma_load_3d(st + L.v + a * 8192, &tm_v, &full[s], 64 * a, j * kC, bh);
+        if (gla) tma_load_3d(st + L.g, &tm_g, &full[s], c_base, j * kC, bh);
+        issued = j + 1;
+      }
+      for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j)
+        (void)mbar_wait_bounded(&full[j % NS], (j / NS) & 1, kSpinLimit);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // chunk-local updates dS_i = V^T Kt into the TMEM ring
+      constexpr uint32_t id_su = idesc_bf16_f32(128, kKB, true, true);
+      for (int i = 0; i < nch; ++i) {
+        const int s = i % NS, b = i % kANB;
+        if (!wait_or_abort(&kready[s], (i / NS) & 1, abort_flag, p.status)) break;
+        if (!wait_or_abort(&dfree[b], ((i / kANB) & 1) ^ 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        uint8_t *st = stage(s);
+        const uint32_t a_v = smem_u32(st + L.v), a_k = smem_u32(st + L.k), d = tbase + (uint32_t)b * 64u;
+#pragma unroll
+        for (int kk = 0; kk < kC / 16; ++kk) {
+          const uint64_t dv_ = desc_sw128(a_v + kk * 2048, 8192, 1024);
+          mma_bf16(d, dv_, desc_sw128(a_k + kk * 2048, 8192, 1024), id_su, kk > 0);
+          if (elu) mma_bf16(d, dv_, desc_sw128(smem_u32(st + L.klo) + kk * 2048, 8192, 1024), id_su, 1);
+        }
+        mma_commit(&dfull[b]);
+        mma_commit(&empty[s]);
+      }
+      mma_commit(drain);
+      (void)mbar_wait_bounded(drain, 0, kSpinLimit);
+    }
+  } else if (tid >= kAKG) {
+    // ------------------------------------------------------------ key group
+    const int kt = tid - kAKG;
+    const int col = kt & 63, half = kt >> 6;  // GLA prefix / elu+1 z: channel and row half
+    const int cg = kt & 7, r0 = kt >> 3;      // transform: 8-channel group, rows r0 + 16 j
+    float z = 0.f;                            // elu+1 normaliser of channel c_base + col (half 0)
+    if (elu && half == 0 && p.S0) z = p.S0[((size_t)bh * DK + c_base + col) * Wmem + DV];
+    // scalar gates: every key warp scans the chunk's 64 gates itself, loaded one chunk ahead
+    auto gate = [&](int t) -> float {
+      if (t >= T) return 0.f;
+      return KIND == kRetnet ? __ldg(p.g + h) : __ldg(p.g + (size_t)bh * T + t);
+    };
+    float gn0 = 0.f, gn1 = 0.f;
+    if (sgate) {
+      gn0 = gate(lane);
+      gn1 = gate(lane + 32);
+    }
+    for (int i = 0; i < nch; ++i) {
+      const int s = i % NS, n = min(kC, T - i * kC);
+      uint8_t *st = stage(s);
+      float *ms = reinterpret_cast<float *>(sm + L.misc + (uint32_t)s * 1024u);
+      const float gc0 = gn0, gc1 = gn1;
+      if (sgate && i + 1 < nch) {
+        gn0 = gate((i + 1) * kC + lane);
+        gn1 = gate((i + 1) * kC + lane + 32);
+      }
+      if (!group_wait(&full[s], (i / NS) & 1, kt, kAKBar, abort_flag, p.status)) break;
+      if (elu && half == 0 && zws) zws[((size_t)bh * nch + i) * DK + c_base + col] = z;  // z before chunk i
+      float rs[4] = {1.f, 1.f, 1.f, 1.f};  // e^{b_last - b_r} of rows r0 + 16 j
+      if (sgate) {
+        float v0 = gc0 * kLog2e, v1 = gc1 * kLog2e;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const float a0 = __shfl_up_sync(0xffffffffu, v0, off);
+          const float a1 = __shfl_up_sync(0xffffffffu, v1, off);
+          if (lane >= off) {
+            v0 += a0;
+            v1 += a1;
+          }
+        }
+        v1 += __shfl_sync(0xffffffffu, v0, 31);
+        const float bl = __shfl_sync(0xffffffffu, v1, 31);
+        rs[0] = exp2f(bl - __shfl_sync(0xffffffffu, v0, r0));
+        rs[1] = exp2f(bl - __shfl_sync(0xffffffffu, v0, r0 + 16));
+        rs[2] = exp2f(bl - __shfl_sync(0xffffffffu, v1, r0));
+        rs[3] = exp2f(bl - __shfl_sync(0xffffffffu, v1, r0 + 16));
+        if (kt < 32) {
+          ms[64 + lane] = exp2f(bl);
+          ms[96 + lane] = exp2f(bl);
+        }
+      }
+      if (gla) {  // channel col, rows 32*half .. +31: prefix, then e^{b_last - b_r}
+        float *gt = reinterpret_cast<float *>(st + L.g);
+        float b[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) b[e] = gt[(32 * half + e) * kKB + col];
+#pragma unroll
+        for (int e = 1; e < 32; ++e) b[e] += b[e - 1];
+        if (half == 0) tmp[col] = b[31];
+        group_sync(kAKBar);
+        float bl;
+        if (half == 1) {
+          const float off = tmp[col];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) b[e] += off;
+          bl = b[31];
+          tmp[64 + col] = bl;
+          ms[128 + col] = __expf(bl);
+        }
+        group_sync(kAKBar);
+        if (half == 0) bl = tmp[64 + col];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) gt[(32 * half + e) * kKB + col] = __expf(bl - b[e]);
+        group_sync(kAKBar);
+      }
+      if (KIND != kLinear) {
+        // Kt (or phi(K) with its low half) in place; a quarter warp covers one row's 8 groups
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = r0 + 16 * j;
+          const uint32_t off = sw128_off(r, cg * 8);
+          float f[8];
+          unpack8(*reinterpret_cast<const uint4 *>(st + L.k + off), f);
+          if (elu) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = (r < n) ? (f[e] > 0.f ? f[e] + 1.f : __expf(f[e])) : 0.f;
+            const uint4 hi = pack8(f);
+            float fh[8];
+            unpack8(hi, fh);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) fh[e] = f[e] - fh[e];
+            *reinterpret_cast<uint4 *>(st + L.klo + off) = pack8(fh);
+            *reinterpret_cast<uint4 *>(st + L.k + off) = hi;
+          } else {
+            if (gla) {
+              const float4 *gp = reinterpret_cast<const float4 *>(st + L.g + (r * kKB + cg * 8) * 4);
+              const float4 ga = gp[0], gb = gp[1];
+              f[0] *= ga.x; f[1] *= ga.y; f[2] *= ga.z; f[3] *= ga.w;
+              f[4] *= gb.x; f[5] *= gb.y; f[6] *= gb.z; f[7] *= gb.w;
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) f[e] *= rs[j];
+            }
+            *reinterpret_cast<uint4 *>(st + L.k + off) = pack8(f);
+          }
+        }
+        fence_proxy_async();
+        group_sync(kAKBar);
+      }
+      if (elu) {  // z <- z + sum_s phi(k_s), from the hi and lo halves; rows split between halves
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const uint32_t off = sw128_off(32 * half + e, col);
+          a[e & 3] += bf16_at(st + L.k, off) + bf16_at(st + L.klo, off);
+        }
+        const float part = (a[0] + a[1]) + (a[2] + a[3]);
+        if (half == 1) tmp[col] = part;
+        group_sync(kAKBar);
+        if (half == 0) z += part + tmp[col];
+      }
+      if (kt == 0) mbar_arrive(&kready[s]);
+    }
+    if (elu && half == 0 && p.S_final)
+      p.S_final[((size_t)bh * DK + c_base + col) * Wmem + DV] = z;
+  } else if (tid >= kASG) {
+    // ------------------------------------------------------------ state group
+    const int v = tid - kASG;  // value row of S^T (TMEM lane of dS)
+    const uint32_t tl = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    float S[kKB];              // S^T[v][c_base .. c_base + 63]
+#pragma unroll
+    for (int c = 0; c < kKB; ++c)
+      S[c] = (p.S0 && v < DV) ? p.S0[((size_t)bh * DK + c_base + c) * Wmem + v] : 0.f;
+    bool alive = true;
+    for (int i = 0; i < nch; ++i) {
+      const int s = i % NS, b = i % kANB;
+      const float *ms = reinterpret_cast<const float *>(sm + L.misc + (uint32_t)s * 1024u);
+      // S_{i-1} as a bf16 image atom, shipped with one bulk copy
+      if (v == 0) bulk_wait_read<1>();  // the atom stored two chunks ago has left its buffer
+      group_sync(kASBar);
+      uint8_t *img = sm + L.st + (uint32_t)(i & 1) * 16384u;
+      store_row32_bf16(img, 16384, v, 0, S);
+      store_row32_bf16(img, 16384, v, 32, S + 32);
+      fence_proxy_async();
+      // decay factors of chunk i (key group) and its local update (tensor core)
+      if (!group_wait(&kready[s], (i / NS) & 1, v, kASBar, abort_flag, p.status)) {
+        alive = false;
+        break;
+      }
+      if (v == 0) {
+        bulk_store(ws + ((size_t)bh * nch + i) * blob_bytes(DK) + (size_t)kb * 16384u, img, 16384u);
+        bulk_commit();
+      }
+      if (!group_wait(&dfull[b], (i / kANB) & 1, v, kASBar, abort_flag, p.status)) {
+        alive = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c0 = 0; c0 < kKB; c0 += 32) {
+        float d[32];
+        tmem_ld32(tl + (uint32_t)b * 64u + c0, d);
+        tmem_wait_ld();
+        if (c0 + 32 == kKB) {
+          tc_fence_before();
+          mbar_arrive(&dfree[b]);
+        }
+        if (sgate || gla) {
+          float dc[32];
+          load32(ms + (gla ? 128 + c0 : 64), dc);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) S[c0 + e] = fmaf(dc[e], S[c0 + e], d[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) S[c0 + e] += d[e];
+        }
+      }
+      mbar_arrive(&empty[s]);
+    }
+    if (v == 0) bulk_wait<0>();
+    if (alive && p.S_final && v < DV) {
+#pragma unroll
+      for (int c = 0; c < kKB; ++c) p.S_final[((size_t)bh * DK + c_base + c) * Wmem + v] = S[c];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 3) tmem_dealloc(tbase, kANB * 64);
+}
+
+// ============================================================ output pass
+constexpr int kBThreads = 128;
+
+struct BLayout {
+  uint32_t qk, v, g, s, p, ot, misc, bar, total;
+};
+__host__ __device__ inline BLayout b_layout(int dk, int kind) {
+  BLayout L;
+  const bool gla = kind == kGla;
+  uint32_t o = 0;
+  L.qk = o; o += (uint32_t)(dk / 64) * 16384u;
+  L.v = o; o += 16384u;
+  L.g = o; o += gla ? up1k((uint32_t)kC * dk * 4u) : 0u;
+  L.s = o; o += blob_bytes(dk);
+  L.p = o; o += 8192u;
+  L.ot = o; o += 16384u;
+  L.misc = o; o += 2048u;
+  L.bar = o; o += 64u;
+  L.total = o;
+  return L;
+}
+
+template <int DK, int DV, int KIND>
+__global__ void __launch_bounds__(kBThreads)
+chunk_output_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const float *__restrict__ zws,
+                    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                    const __grid_constant__ CUtensorMap tm_o) {
+  constexpr bool elu = KIND == kElu1, gla = KIND == kGla;
+  constexpr bool sgate = KIND == kRetnet || KIND == kScalar;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const BLayout L = b_layout(DK, KIND);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = p.T, nch = (T + kC - 1) / kC;
+  const int bh = blockIdx.x / nch, i = blockIdx.x % nch, h = bh % p.H;
+  const int t0 = i * kC, n = min(kC, T - t0);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L.bar);
+  uint64_t *mbar = bar + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 2);
+  float *ms = reinterpret_cast<float *>(sm + L.misc);
+  // ms: b2[64] | eb[64] | den[64] | qz[64] | bm[128] (e^{b_m}) ... GLA per channel
+  float *b2 = ms, *eb = ms + 64, *den = ms + 128, *qz = ms + 192, *ebm = ms + 256;
+  uint8_t *qk = sm + L.qk;
+  float *gt = reinterpret_cast<float *>(sm + L.g);
+
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 128);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    mbar_init(mbar, 1);
+    fence_mbar_init();
+    constexpr uint32_t bytes = 2u * DK * kC * 2u + DV * kC * 2u + (gla ? DK * kC * 4u : 0u) + blob_bytes(DK);
+    mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+    for (int a = 0; a < DK / 64; ++a) {
+      tma_load_3d(qk + a * 16384, &tm_q, bar, 64 * a, t0, bh);
+      tma_load_3d(qk + a * 16384 + 8192, &tm_k, bar, 64 * a, t0, bh);
+    }
+#pragma unroll
+    for (int a = 0; a < DV / 64; ++a) tma_load_3d(sm + L.v + a * 8192, &tm_v, bar, 64 * a, t0, bh);
+    if (gla) tma_load_3d(sm + L.g, &tm_g, bar, 0, t0, bh);
+    bulk_load(sm + L.s, ws + ((size_t)bh * nch + i) * blob_bytes(DK), blob_bytes(DK), bar);
+  }
+  if (DV == 64) {
+    for (int q = tid; q < 512; q += kBThreads)
+      reinterpret_cast<uint4 *>(sm + L.v + 8192)[q] = make_uint4(0, 0, 0, 0);
+  }
+  // scalar gates of this chunk (warp 0), while the tiles stream in
+  if (sgate && warp == 0) {
+    const int t = t0 + lane;
+    float g0, g1;
+    if (KIND == kRetnet) {
+      const float g = __ldg(p.g + h);
+      g0 = (t < T) ? g : 0.f;
+      g1 = (t + 32 < T) ? g : 0.f;
+    } else {
+      g0 = (t < T) ? __ldg(p.g + (size_t)bh * T + t) : 0.f;
+      g1 = (t + 32 < T) ? __ldg(p.g + (size_t)bh * T + t + 32) : 0.f;
+    }
+    float v0 = g0 * kLog2e, v1 = g1 * kLog2e;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float a0 = __shfl_up_sync(0xffffffffu, v0, off);
+      const float a1 = __shfl_up_sync(0xffffffffu, v1, off);
+      if (lane >= off) { v0 += a0; v1 += a1; }
+    }
+    v1 += __shfl_sync(0xffffffffu, v0, 31);
+    b2[lane] = v0;
+    b2[lane + 32] = v1;
+    eb[lane] = exp2f(v0);
+    eb[lane + 32] = exp2f(v1);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint32_t tl = tbase + (static_cast<uint32_t>(warp * 32) << 16);
+  // D1 is read out before the output MMAs are issued, so O1 reuses its columns
+  constexpr uint32_t kD1 = 0, kO1 = 0, kO2 = 64;
+  bool ok = mbar_wait_bounded(bar, 0, kSpinLimit);
+  if (!__syncthreads_and(ok)) {
+    if (tid == 0) atomicOr(p.status, kStatusTimeout);
+  } else {
+    // ---- GLA prefix per key channel; q/k transforms
+    if (gla && tid < DK) {
+      float acc = 0.f, bmid = 0.f;
+      for (int r = 0; r < kC; ++r) {
+        acc += gt[r * DK + tid];
+        gt[r * DK + tid] = acc;
+        if (r == kMid) bmid = acc;
+      }
+      ebm[tid] = __expf(bmid);
+    }
+    __syncthreads();
+    if (elu || gla) {
+      const int row = tid;  // row of [Q; K]
+      const int r = row & (kC - 1);
+      const bool is_k = row >= kC;
+#pragma unroll 4
+      for (int g8 = 0; g8 < DK / 8; ++g8) {
+        uint8_t *ptr = qk + (g8 >> 3) * 16384 + sw128_off(row, (g8 & 7) * 8);
+        float f[8];
+        unpack8(*reinterpret_cast<uint4 *>(ptr), f);
+        if (elu) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = (r < n) ? (f[e] > 0.f ? f[e] + 1.f : __expf(f[e])) : 0.f;
+        } else {
+          const float *brow = gt + r * DK + g8 * 8;
+          const float *bmid = gt + kMid * DK + g8 * 8;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float d = (brow[e] - bmid[e]) * kLog2e;
+            f[e] *= exp2f(is_k ? -d : d);
+          }
+        }
+        *reinterpret_cast<uint4 *>(ptr) = pack8(f);
+      }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t a_qk = smem_u32(qk);
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 64, false, false);
+#pragma unroll
+      for (int kk = 0; kk < DK / 16; ++kk) {
+        const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+        mma_bf16(tbase + kD1, desc_sw128(a_qk + ko, 16, 1024), desc_sw128(a_qk + ko + 8192, 16, 1024), idesc,
+                 kk > 0);
+      }
+      mma_commit(mbar);
+    }
+    ok = mbar_wait_bounded(mbar, 0, kSpinLimit);
+    if (!__syncthreads_and(ok)) {
+      if (tid == 0) atomicOr(p.status, kStatusTimeout);
+    } else {
+      tc_fence_after();
+      // ---- masked, decayed scores P (TMEM lanes 0..63); elu+1: q.z
+      if (tid < kC) {
+        const int r = tid;
+        const float b2r = sgate ? b2[r] : 0.f;
+        float rowsum = 0.f;
+#pragma unroll 1
+        for (int s0 = 0; s0 < kC; s0 += 32) {
+          float d[32], fs[32];
+          if (sgate) load32(b2 + s0, fs);
+          tmem_ld32(tl + kD1 + s0, d);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int sc = s0 + e;
+            float x = (sc <= r && r < n) ? d[e] : 0.f;
+            if (sgate) x *= exp2f(sc <= r ? b2r - fs[e] : 0.f);
+            if (elu) {
+              x = __bfloat162float(__float2bfloat16_rn(x));
+              rowsum += x;
+            }
+            d[e] = x;
+          }
+          store_row32_bf16(sm + L.p, 8192, r, s0, d);
+        }
+        if (elu) den[r] = rowsum;
+      } else if (elu) {
+        const int r = tid - kC;
+        const float *zp = zws + ((size_t)bh * nch + i) * DK;
+        float acc = 0.f;
+        for (int g8 = 0; g8 < DK / 8; ++g8) {
+          float f[8];
+          unpack8(*reinterpret_cast<const uint4 *>(qk + (g8 >> 3) * 16384 + sw128_off(r, (g8 & 7) * 8)), f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc = fmaf(f[e], __ldg(zp + g8 * 8 + e), acc);
+        }
+        qz[r] = acc;
+      }
+      tc_fence_before();
+      __syncthreads();
+      // ---- Qt for the inter-chunk term: GLA Q e^{b - b_m} -> Q e^{b}
+      if (gla && tid < kC) {
+        const int r = tid;
+#pragma unroll 4
+        for (int g8 = 0; g8 < DK / 8; ++g8) {
+          uint8_t *ptr = qk + (g8 >> 3) * 16384 + sw128_off(r, (g8 & 7) * 8);
+          float f[8];
+          unpack8(*reinterpret_cast<uint4 *>(ptr), f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] *= ebm[g8 * 8 + e];
+          *reinterpret_cast<uint4 *>(ptr) = pack8(f);
+        }
+      }
+      if (elu && tid < kC) den[tid] += qz[tid];
+      fence_proxy_async();
+      tc_fence_before();
+      __syncthreads();
+      if (tid == 0) {
+        tc_fence_after();
+        const uint32_t a_s = smem_u32(sm + L.s), a_qk = smem_u32(qk), a_v = smem_u32(sm + L.v),
+                       a_p = smem_u32(sm + L.p);
+        constexpr uint32_t id_o1 = idesc_bf16_f32(128, 64, false, false);
+        constexpr uint32_t id_o2 = idesc_bf16_f32(128, 64, true, false);
+#pragma unroll
+        for (int kk = 0; kk < DK / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_bf16(tbase + kO1, desc_sw128(a_s + ko, 16, 1024), desc_sw128(a_qk + ko, 16, 1024), id_o1, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kC / 16; ++kk)
+          mma_bf16(tbase + kO2, desc_sw128(a_v + kk * 2048, 8192, 1024), desc_sw128(a_p + kk * 32, 16, 1024),
+                   id_o2, kk > 0);
+        mma_commit(mbar);
+      }
+      ok = mbar_wait_bounded(mbar, 1, kSpinLimit);
+      if (!__syncthreads_and(ok)) {
+        if (tid == 0) atomicOr(p.status, kStatusTimeout);
+      } else {
+        tc_fence_after();
+        const int v = tid;
+        uint8_t *ot = sm + L.ot + (uint32_t)(v >> 6) * 8192u;
+        const bool odd = lane & 1;
+#pragma unroll 1
+        for (int r0 = 0; r0 < kC; r0 += 32) {
+          float a[32], b[32], f[32];
+          tmem_ld32(tl + kO1 + r0, a);
+          tmem_ld32(tl + kO2 + r0, b);
+          if (sgate) load32(eb + r0, f);
+          if (elu) load32(den + r0, f);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            float y = sgate ? fmaf(f[e], a[e], b[e]) : a[e] + b[e];
+            if (elu) y = __fdividef(y, f[e]);
+            a[e] = y;
+          }
+          if (v < DV) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float send = odd ? a[e] : a[e + 1];
+              const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+              const int r = r0 + e + (odd ? 1 : 0);
+              const uint32_t w = odd ? pack_bf16(recv, a[e + 1]) : pack_bf16(a[e], recv);
+              *reinterpret_cast<uint32_t *>(ot + sw128_off(r, (v & 63) - (odd ? 1 : 0))) = w;
+            }
+          }
+        }
+        fence_proxy_async();
+        __syncthreads();
+        if (tid == 0) {
+#pragma unroll
+          for (int a = 0; a < DV / 64; ++a) tma_store_3d(&tm_o, sm + L.ot + a * 8192, 64 * a, t0, bh);
+          bulk_commit();
+          bulk_wait<0>();
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tbase, 128);
+}
+
+// ---------------------------------------------------------------- launch
+
+template <int DK, int DV, int KIND>
+int launch_typed(const ChunkParams &p, uint8_t *ws, float *zws, cudaStream_t stream) {
+  const int BH = p.B * p.H, nch = (p.T + kC - 1) / kC;
+  const ALayout La = a_layout(KIND, a_stages<KIND>());
+  const BLayout Lb = b_layout(DK, KIND);
+  const size_t sa = La.total + 1024, sb = Lb.total + 1024;
+  if (sa > 232448 || sb > 232448) {
+    set_error("la_chunk_fwd: materialised kernels need %zu / %zu bytes of shared memory", sa, sb);
+    return LA_ERR_UNSUPPORTED;
+  }
+  CUtensorMap mq, mk, mv, mg, mgA, mo;
+  bool ok = make_map(&mq, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DK, p.T, BH, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_map(&mk, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DK, p.T, BH, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_map(&mv, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DV, p.T, BH, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_map(&mo, p.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DV, p.T, BH, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (ok && KIND == kGla) {
+    ok = make_map(&mg, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, DK, p.T, BH, DK, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+         make_map(&mgA, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, DK, p.T, BH, kKB, CU_TENSOR_MAP_SWIZZLE_NONE);
+  } else {
+    mg = mq;
+    mgA = mq;
+  }
+  if (!ok) {
+    set_error("la_chunk_fwd: cuTensorMapEncodeTiled rejected a tensor map");
+    return LA_ERR_CUDA;
+  }
+  auto ka = chunk_state_kernel<DK, DV, KIND>;
+  auto kb = chunk_output_kernel<DK, DV, KIND>;
+  cudaError_t e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sa);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sb);
+  if (e == cudaSuccess) {
+    ka<<<(unsigned)(BH * (DK / kKB)), kAThreads, sa, stream>>>(p, ws, zws, mk, mv, mgA);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) {
+    kb<<<(unsigned)((size_t)BH * nch), kBThreads, sb, stream>>>(p, ws, zws, mq, mk, mv, mg, mo);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) {
+    set_error("la_chunk_fwd: materialised kernels failed to launch: %s", cudaGetErrorString(e));
+    return LA_ERR_CUDA;
+  }
+  return LA_OK;
+}
+
+template <int KIND>
+int launch_kind(const ChunkParams &p, uint8_t *ws, float *zws, cudaStream_t stream) {
+  if (p.dk == 128 && p.dv == 128) return launch_typed<128, 128, KIND>(p, ws, zws, stream);
+  if (p.dk == 128 && p.dv == 64) return launch_typed<128, 64, KIND>(p, ws, zws, stream);
+  if (p.dk == 64 && p.dv == 128) return launch_typed<64, 128, KIND>(p, ws, zws, stream);
+  return launch_typed<64, 64, KIND>(p, ws, zws, stream);
+}
+
+}  // namespace
+
+size_t mat_workspace_bytes(const ChunkParams &p) {
+  const size_t nch = (size_t)(p.T + kC - 1) / kC, BH = (size_t)p.B * p.H;
+  size_t b = BH * nch * blob_bytes(p.dk);
+  if (p.kind == kElu1) b += BH * nch * p.dk * sizeof(float);
+  return b;
+}
+
+int launch_chunk_mat(const ChunkParams &p, void *workspace, cudaStream_t stream) {
+  if (!encode_fn()) {
+    set_error("la_chunk_fwd: cuTensorMapEncodeTiled is unavailable");
+    return LA_ERR_CUDA;
+  }
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  const size_t nch = (size_t)(p.T + kC - 1) / kC, BH = (size_t)p.B * p.H;
+  float *zws = (p.kind == kElu1) ? reinterpret_cast<float *>(ws + BH * nch * blob_bytes(p.dk)) : nullptr;
+  switch (p.kind) {
+    case kLinear: return launch_kind<kLinear>(p, ws, zws, stream);
+    case kElu1: return launch_kind<kElu1>(p, ws, zws, stream);
+    case kRetnet: return launch_kind<kRetnet>(p, ws, zws, stream);
+    case kScalar: return launch_kind<kScalar>(p, ws, zws, stream);
+    case kGla: return launch_kind<kGla>(p, ws, zws, stream);
+    default:
+      set_error("la_chunk_fwd: the materialised variant covers the unit-write modes only");
+      return LA_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace la

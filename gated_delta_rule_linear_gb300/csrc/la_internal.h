@@ -58,9 +58,13 @@ int launch_chunk_tc(const ChunkParams &p, cudaStream_t stream);
 int launch_chunk_ws(const ChunkParams &p, cudaStream_t stream);
 int launch_chunk_delta(const ChunkParams &p, cudaStream_t stream);
 int launch_step(const StepParams &p, cudaStream_t stream);
+// Materialised (two-phase) variant: chunk-state pass then a parallel output
+// pass, through a caller-provided workspace of mat_workspace_bytes(p) bytes.
+size_t mat_workspace_bytes(const ChunkParams &p);
+int launch_chunk_mat(const ChunkParams &p, void *workspace, cudaStream_t stream);
 
 // Which chunk-forward kernel a shape goes to (host-side selection).
-enum Variant : int { kVariantSimt = 0, kVariantTc = 1 };
+enum Variant : int { kVariantSimt = 0, kVariantTc = 1, kVariantMat = 2 };
 int select_variant(const ChunkParams &p, int *chunk_out);
 
 }  // namespace la

@@ -1,0 +1,117 @@
+"""GPU parity of the materialised (two-phase) variant against the float64 oracle.
+
+The variant writes every chunk's incoming state to a workspace in a serial
+state pass and then computes all chunks' outputs in parallel; it covers the
+unit-write modes (everything but the delta rule). It is selected with
+LA_VARIANT=mat and must agree with the oracle to the same tolerance as the
+fused kernel, and with the fused kernel itself.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_linear_gb300 as la
+from paritylib import assert_close, f64, make, run_cuda, run_oracle, to_dev
+from test_gpu_parity import _inputs
+
+pytestmark = pytest.mark.gpu
+
+UNIT_WRITE = ["linear", "elu1", "retnet", "gla", "scalar"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from gated_delta_rule_linear_gb300 import build
+    build.build()
+    la.load_library()
+    assert torch.cuda.is_available()
+
+
+@pytest.fixture
+def mat(monkeypatch):
+    monkeypatch.setenv("LA_VARIANT", "mat")
+
+
+@pytest.mark.parametrize("mode", UNIT_WRITE)
+@pytest.mark.parametrize("dims", [(128, 128), (64, 64), (64, 128), (128, 64)])
+def test_mat_small_parity(mode, dims, mat):
+    dk, dv = dims
+    inp = _inputs(mode, "bf16", dk=dk, dv=dv)
+    o, S = run_cuda(inp)
+    o_ref, S_ref = run_oracle(inp)
+    assert_close(f64(o), o_ref, "bf16", f"{mode} o")
+    assert_close(f64(S), S_ref, "bf16", f"{mode} S_final")
+
+
+@pytest.mark.parametrize("mode", UNIT_WRITE)
+@pytest.mark.parametrize("T", [1, 17, 63, 64, 65, 129, 1000])
+def test_mat_ragged_lengths(mode, T, mat):
+    inp = _inputs(mode, "bf16", B=1, H=3, T=T)
+    o, S = run_cuda(inp)
+    o_ref, S_ref = run_oracle(inp)
+    assert_close(f64(o), o_ref, "bf16", f"{mode} T={T} o")
+    assert_close(f64(S), S_ref, "bf16", f"{mode} T={T} S")
+
+
+@pytest.mark.parametrize("mode", UNIT_WRITE)
+def test_mat_zero_initial_state_and_no_state_output(mode, mat):
+    inp = _inputs(mode, "bf16", B=1, H=2, T=150, s0=False)
+    o, S = run_cuda(inp, with_state=False)
+    assert S is None
+    o_ref, _ = run_oracle(inp)
+    assert_close(f64(o), o_ref, "bf16", f"{mode} o")
+
+
+@pytest.mark.parametrize("mode", ["gla", "elu1", "retnet"])
+def test_mat_split_call_resumes_from_final_state(mode, mat):
+    T, T1 = 300, 100
+    inp = _inputs(mode, "bf16", B=1, H=2, T=T)
+    d = to_dev(inp)
+
+    def sl(x, a, b):
+        if x is None or (mode == "retnet" and x is d["g"]):
+            return x
+        return x[:, :, a:b].contiguous()
+
+    o1, S1 = la.chunk_fwd(sl(d["q"], 0, T1), sl(d["k"], 0, T1), sl(d["v"], 0, T1), mode,
+                          g=sl(d["g"], 0, T1), S0=d["S0"])
+    o2, S2 = la.chunk_fwd(sl(d["q"], T1, T), sl(d["k"], T1, T), sl(d["v"], T1, T), mode,
+                          g=sl(d["g"], T1, T), S0=S1)
+    torch.cuda.synchronize()
+    o_ref, S_ref = run_oracle(inp)
+    assert_close(np.concatenate([f64(o1), f64(o2)], axis=2), o_ref, "bf16", "split o")
+    assert_close(f64(S2), S_ref, "bf16", "split S")
+
+
+@pytest.mark.parametrize("mode", ["retnet", "gla"])
+def test_mat_agrees_with_fused_kernel(mode, monkeypatch):
+    inp = _inputs(mode, "bf16", B=2, H=3, T=700)
+    monkeypatch.setenv("LA_VARIANT", "tc")
+    o_a, S_a = run_cuda(inp)
+    monkeypatch.setenv("LA_VARIANT", "mat")
+    o_b, S_b = run_cuda(inp)
+    assert_close(f64(o_b), f64(o_a), "bf16", "mat vs fused o")
+    assert_close(f64(S_b), f64(S_a), "bf16", "mat vs fused S")
+
+
+def test_mat_rejects_the_delta_rule(mat):
+    inp = _inputs("gdn", "bf16", B=1, H=1, T=64)
+    with pytest.raises(la.LAError) as e:
+        run_cuda(inp)
+    assert e.value.code == la.CONSTANTS["LA_ERR_UNSUPPORTED"]
+    assert "unit-write" in str(e.value)
+
+
+@pytest.mark.parametrize("name", ["elu1", "retnet", "gla"])
+def test_mat_full_size_workload_sampled_heads(name, mat):
+    inp = make(name)
+    wl = inp["wl"]
+    o, S = run_cuda(inp, C=wl.C)
+    B, H = wl.B, wl.H
+    heads = [(0, 0), (B - 1, H - 1), (B // 2, H // 3)]
+    o_ref, S_ref = run_oracle(inp, heads=heads, use_c=True)
+    o_got = np.stack([f64(o[b, h]) for b, h in heads])[None]
+    S_got = np.stack([f64(S[b, h]) for b, h in heads])[None]
+    assert_close(o_got, o_ref, wl.dtype, f"{name} o (sampled heads)")
+    assert_close(S_got, S_ref, wl.dtype, f"{name} S_final (sampled heads)")
+    assert torch.isfinite(o.float()).all()
