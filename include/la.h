@@ -26,7 +26,10 @@
  *   - The state is float32 [B][H][dk][W] with W = dv, except for
  *     LA_ELU1_NORM where W = dv + 1 and column dv holds the normaliser z.
  *   - All pointers are DEVICE pointers owned by the caller. The library never
- *     frees or retains them and allocates no device memory of its own.
+ *     frees or retains them. Device memory of its own is taken only by the
+ *     materialised variant of la_chunk_fwd: a workspace allocated and freed
+ *     on `stream` from a library-owned stream-ordered pool (one per device)
+ *     that keeps freed memory for the next call.
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream);
  *     nothing synchronises with the host.
  *   - Return value: LA_OK, or an LA_ERR_* code with a message available from
@@ -99,6 +102,15 @@ typedef struct CUstream_st *la_stream_t;
  *
  * S_final of one call passed as S0 of the next continues the sequence
  * (the recurrent state is the whole checkpoint).
+ *
+ * Kernel variants ("Talk Linear Attention" section 4.1.2). Fused: one CTA per
+ * head walks the chunks, keeping the state on chip; nothing but q, k, v, o and
+ * the states touches memory. Materialised (unit-write modes, bfloat16): a
+ * serial pass writes every chunk's incoming state to a workspace of
+ * B*H*ceil(T/64)*dk*256 bytes (plus B*H*ceil(T/64)*dk*4 for LA_ELU1_NORM),
+ * then all chunks' outputs are computed in parallel; it wins when B*H is too
+ * small to fill the GPU. The choice is made per shape; the environment
+ * variable LA_VARIANT = tc (or nonmat) | mat | simt forces one.
  */
 int la_chunk_fwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
                  void *o, const float *S0, float *S_final,
