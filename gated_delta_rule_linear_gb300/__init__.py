@@ -7,10 +7,10 @@ scalar decay, Gated DeltaNet) and its one-token decode step. This package is
 only the binding: ctypes marshalling plus a build helper.
 """
 from ._binding import (CONSTANTS, LIB_PATH, MODE_IDS, SIGNATURES, LAError, chunk_fwd,
-                       la_chunk_fwd, la_last_error, la_recurrent_step, la_stream_status,
+                       la_chunk_fwd, la_chunk_fwd_noalloc, la_last_error, la_recurrent_step, la_stream_status,
                        la_version, load_library, recurrent_step)
 from ._binding import *  # noqa: F401,F403  (LA_* constants)
 
-__all__ = ["chunk_fwd", "recurrent_step", "la_chunk_fwd", "la_recurrent_step",
+__all__ = ["chunk_fwd", "recurrent_step", "la_chunk_fwd", "la_chunk_fwd_noalloc", "la_recurrent_step",
            "la_stream_status", "la_last_error", "la_version", "load_library", "LAError",
            "CONSTANTS", "MODE_IDS", "SIGNATURES", "LIB_PATH"]

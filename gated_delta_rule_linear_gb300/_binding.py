@@ -45,6 +45,7 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 SIGNATURES = {
     "la_chunk_fwd": ([_P] * 8 + [_I] * 7 + [_P], _I),
+    "la_chunk_fwd_noalloc": ([_P] * 8 + [_I] * 7 + [_P], _I),
     "la_recurrent_step": ([_P] * 7 + [_I] * 5 + [_P], _I),
     "la_stream_status": ([_P], _I),
     "la_last_error": ([], ctypes.c_char_p),
@@ -90,6 +91,12 @@ def _ptr(x):
 def la_chunk_fwd(q, k, v, g, beta, o, S0, S_final, B, H, T, dk, dv, C, mode, stream):
     return load_library().la_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(o),
                                        _ptr(S0), _ptr(S_final), B, H, T, dk, dv, C, mode, stream)
+
+
+def la_chunk_fwd_noalloc(q, k, v, g, beta, o, S0, S_final, B, H, T, dk, dv, C, mode, stream):
+    return load_library().la_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                               _ptr(o), _ptr(S0), _ptr(S_final), B, H, T, dk, dv,
+                                               C, mode, stream)
 
 
 def la_recurrent_step(q, k, v, g, beta, o, S, B, H, dk, dv, mode, stream):

@@ -117,6 +117,30 @@ int la_chunk_fwd(const void *q, const void *k, const void *v, const float *g, co
                  int B, int H, int T, int dk, int dv, int C, int mode, la_stream_t stream);
 
 /*
+ * la_chunk_fwd_noalloc -- la_chunk_fwd's materialised variant with its
+ * workspace in a static device array instead of an allocation, for callers
+ * that cannot allocate device memory. The pages have no counterpart to this
+ * entry point: it is an interface of this library only.
+ *
+ *   Arguments, layouts and results as la_chunk_fwd, restricted to the
+ *   unit-write modes (not LA_GDN), bfloat16 (no LA_F32) and C = 0 or 64.
+ *   Scratch needed: B*H*ceil(T/64)*dk*256 bytes, plus B*H*ceil(T/64)*dk*4
+ *   for LA_ELU1_NORM. A call that needs more than LA_NOALLOC_SCRATCH_BYTES
+ *   is rejected with LA_ERR_INVALID_ARG before anything is launched.
+ *   Allocates nothing: no cudaMalloc, cudaFree or stream-ordered allocation.
+ *   The scratch is one array per device, shared by every call on that
+ *   device: calls that overlap on the GPU (several streams or host threads)
+ *   race on it, so the caller orders them. Nothing in it needs to start at
+ *   zero. The first call on each device looks up the array's address (which
+ *   may load the module holding it): make that first call before any stream
+ *   capture.
+ */
+#define LA_NOALLOC_SCRATCH_BYTES 0x2000000  /* 32 MiB */
+int la_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *g,
+                         const float *beta, void *o, const float *S0, float *S_final,
+                         int B, int H, int T, int dk, int dv, int C, int mode, la_stream_t stream);
+
+/*
  * la_recurrent_step -- one decode step (the recurrent form, "Talk Linear
  * Attention" section 2.1; kernel-attention notes section 14): for every
  * (b, h), apply the mode's update with this token and write o = S^T q

@@ -30,8 +30,8 @@ def _declared_functions():
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    assert names == sorted(["la_chunk_fwd", "la_recurrent_step", "la_stream_status",
-                            "la_last_error", "la_version"])
+    assert names == sorted(["la_chunk_fwd", "la_chunk_fwd_noalloc", "la_recurrent_step",
+                            "la_stream_status", "la_last_error", "la_version"])
     assert set(names) == set(la.SIGNATURES)
 
 
