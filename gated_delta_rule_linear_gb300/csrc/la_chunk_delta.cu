@@ -76,11 +76,10 @@ __host__ __device__ inline DLayout d_layout() {
   return L;
 }
 
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
+// Round to the nearest tf32 value, ties away from zero (finite inputs): add
+// half of the 13 dropped mantissa bits, then clear them; a mantissa carry
+// moves into the exponent as it should. Two integer operations.
+__device__ __forceinline__ uint32_t to_tf32(float x) { return (__float_as_uint(x) + 0x1000u) & 0xffffe000u; }
 __device__ __forceinline__ float round_tf32(float x) { return __uint_as_float(to_tf32(x)); }
 // Warp-level 16x8x8 tf32 MMA (register fragments), fp32 accumulate.
 __device__ __forceinline__ void mma_16x8x8_tf32(float *d, const uint32_t *a, const uint32_t *b) {
@@ -249,6 +248,16 @@ chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q
           tma_load_3d(st + L.v + a * 8192, &tm_v, &full[s], 64 * a, t0, bh);
         }
         mbar_arrive(&full[s]);
+        // the load of chunk j + kNS waits for this chunk's last MMA; warm L2 now
+        // so that it does not pay the DRAM latency then
+        if (j + kNS < nchunks) {
+#pragma unroll
+          for (int a = 0; a < 2; ++a) {
+            tma_prefetch_3d(&tm_q, 64 * a, t0 + kNS * kC, bh);
+            tma_prefetch_3d(&tm_k, 64 * a, t0 + kNS * kC, bh);
+            tma_prefetch_3d(&tm_v, 64 * a, t0 + kNS * kC, bh);
+          }
+        }
       }
       issued = j + 1;
     }
@@ -315,6 +324,9 @@ chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q
         for (int kk = 0; kk < kC / 16; ++kk)
           mma_bf16(tbase + kColU, desc_sw128(a_v + kk * 2048, 8192, 1024), desc_sw128(a_tp + kk * 32, 16, 1024),
                    id_ut, kk > 0);
+        // T' has been read (and T'' by the W MMA before s_ready): the key
+        // group may write the next chunk's T' and T''
+        mma_commit(kfree);
 #pragma unroll
         for (int kk = 0; kk < DK / 16; ++kk) {
           const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -340,7 +352,6 @@ chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q
         mma_commit(s_done);
         mma_commit(&o_done[i & 1]);
         mma_commit(&empty[s]);
-        mma_commit(kfree);
       }
       mma_commit(&drain[1]);
       (void)mbar_wait_bounded(&drain[1], 0, kSpinLimit);
@@ -486,7 +497,12 @@ chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q
       tc_fence_after();
       const bool fast = ms[kMsFast] != 0.f;
       // ---- P (TMEM lanes 0..63 = Q K^T rows) and A (lanes 64..127 = K K^T rows)
+      bool okp = true;
       if (kg < kC) {
+        // P buffer j & 1 is free once chunk j - 2's output MMA has read it
+        okp = wait_or_abort(&o_done[j & 1], ((j >> 1) & 1) ^ 1, abort_flag, p.status);
+      }
+      if (kg < kC && okp) {
         const int r = kg;
         const float b2r = ms[kMsB2 + r], fr = ms[kMsF + r];
 #pragma unroll 1
@@ -495,15 +511,19 @@ chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q
           load32(ms + (fast ? kMsVS : kMsB2) + s0, fs);
           tmem_ld32(tl + kColD1 + s0, d);
           tmem_wait_ld();
+          if (fast) {  // uniform per chunk: the common case issues no exponentials
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int sc = s0 + e;
-            const float g = fast ? fr * fs[e] : exp2f(sc <= r ? b2r - fs[e] : 0.f);
-            d[e] = (sc <= r && r < n) ? d[e] * g : 0.f;
+            for (int e = 0; e < 32; ++e) d[e] = (s0 + e <= r && r < n) ? d[e] * (fr * fs[e]) : 0.f;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int sc = s0 + e;
+              d[e] = (sc <= r && r < n) ? d[e] * exp2f(b2r - fs[e]) : 0.f;
+            }
           }
           store_row32_bf16(sm + L.p + (uint32_t)(j & 1) * 8192u, 8192, r, s0, d);
         }
-      } else {
+      } else if (kg >= kC) {
         const int r = kg - kC;
         const float b2r = ms[kMsB2 + r], ar = ms[kMsAR + r], br = ms[kMsBeta + r];
 #pragma unroll 1
@@ -512,11 +532,15 @@ chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q
           load32(ms + (fast ? kMsVS : kMsB2) + s0, fs);
           tmem_ld32(tl + kColD1 + s0, d);
           tmem_wait_ld();
+          if (fast) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int sc = s0 + e;
-            const float g = fast ? ar * fs[e] : br * exp2f(sc < r ? b2r - fs[e] : 0.f);
-            d[e] = (sc < r && r < n) ? round_tf32(d[e] * g) : 0.f;
+            for (int e = 0; e < 32; ++e) d[e] = (s0 + e < r && r < n) ? round_tf32(d[e] * (ar * fs[e])) : 0.f;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int sc = s0 + e;
+              d[e] = (sc < r && r < n) ? round_tf32(d[e] * (br * exp2f(b2r - fs[e]))) : 0.f;
+            }
           }
 #pragma unroll
           for (int q = 0; q < 8; ++q)
@@ -525,7 +549,7 @@ chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q
         }
       }
       tc_fence_before();
-      group_sync(kBarKG);
+      if (!group_all(okp, kBarKG)) break;
       if (kg == 0) mbar_arrive(d1_free);
       // ---- T = (I + A)^-1: 16x16 diagonal blocks, then three block levels
       if (kg < kC) {
