@@ -46,9 +46,18 @@ KERNEL_SOURCES = ["gated_delta_rule_linear_gb300/csrc/la_chunk_delta.cu",
                   "gated_delta_rule_linear_gb300/csrc/la_sm100.cuh"]
 
 
-def kernel_name(wl, variant=None) -> str:
+def uses_materialised(wl, variant=None, sm_count=152) -> bool:
+    """Whether la_chunk_fwd runs the materialised variant for this workload
+    (the library's per-shape rule, or a forced LA_VARIANT)."""
+    if variant is not None:
+        return variant == "mat"
+    return (wl.dtype == "bf16" and wl.mode != "gdn" and wl.T >= 512
+            and 2 * wl.B * wl.H <= sm_count)
+
+
+def kernel_name(wl, variant=None, sm_count=152) -> str:
     """The kernel one la_chunk_fwd launch of this workload runs."""
-    if variant == "mat":
+    if uses_materialised(wl, variant, sm_count):
         return "chunk_state_kernel+chunk_output_kernel"
     if wl.dtype == "f32" or variant == "simt":
         return "chunk_simt_kernel"
@@ -330,7 +339,9 @@ def main():
     roof["traffic"] = traffic
     roof["peak_source"] = peak_src
     roof["algorithmic_bytes"] = alg_bytes
-    roof["kernel"] = kernel_name(wl, args.variant)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mat = uses_materialised(wl, args.variant, sms)
+    roof["kernel"] = kernel_name(wl, args.variant, sms)
     roof["launch_ms_mean"] = round(statistics.mean(launch_ms), 4)
 
     # ---- end to end through the C ABI with host buffers ----
@@ -360,7 +371,7 @@ def main():
             "cpu_baseline": cpu,
             "clocks": clk,
             "e2e": e2e,
-            "gpu_launches": args.steps * (2 if args.variant == "mat" else 1),
+            "gpu_launches": args.steps * (2 if mat else 1),
         }
         print(json.dumps(line), flush=True)
     if dist:

@@ -72,11 +72,21 @@ unsigned *status_word() {
   return g_status_ptr[dev];
 }
 
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return n;
+}
+
 // Host-side kernel choice. float32 inputs go to the CUDA-core kernel. bf16
-// inputs go to the fused (non-materialised) tensor-core kernel, or, for the
-// unit-write modes when there are too few heads to fill the GPU, to the
-// materialised two-phase variant. LA_VARIANT (auto | tc | nonmat | mat |
-// simt) overrides the choice for measurement sweeps.
+// inputs go to the fused (non-materialised) tensor-core kernel, which runs
+// one CTA per head, or, for the unit-write modes when B*H is at most half the
+// SM count (the fused grid would leave most of the GPU idle) and the sequence
+// spans at least 8 chunks, to the materialised two-phase variant, whose
+// output pass uses every SM. LA_VARIANT (auto | tc | nonmat | mat | simt)
+// overrides the choice for measurement sweeps.
 int select_variant(const ChunkParams &p, int *chunk_out) {
   const char *env = getenv("LA_VARIANT");
   int want = -1;
@@ -95,6 +105,8 @@ int select_variant(const ChunkParams &p, int *chunk_out) {
     return -1;
   }
   if (want >= 0) return want;
+  const long long BH = (long long)p.B * p.H;
+  if (p.kind != kGdn && p.T >= 8 * 64 && 2 * BH <= sm_count()) return kVariantMat;
   return kVariantTc;
 }
 

@@ -47,7 +47,7 @@ __host__ __device__ constexpr uint32_t blob_bytes(int dk) { return (uint32_t)(dk
 constexpr int kAThreads = 384;
 constexpr int kASG = 128;  // first thread of the state group
 constexpr int kAKG = 256;  // first thread of the key group
-constexpr int kASBar = 1, kAKBar = 2;
+constexpr int kAKBar = 2;  // key-group named barrier
 constexpr int kKB = 64;    // key channels per state-pass CTA
 constexpr int kANB = 4;    // TMEM slots of dS (64 columns each)
 
@@ -100,7 +100,8 @@ chunk_state_kernel(const ChunkParams p, uint8_t *__restrict__ ws, float *__restr
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bar);
   uint64_t *full = bars, *empty = bars + kAMaxStages, *kready = bars + 2 * kAMaxStages;
   uint64_t *dfull = bars + 3 * kAMaxStages, *dfree = dfull + kANB, *drain = dfree + kANB;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 2);
+  uint64_t *img_full = drain + 1, *img_free = img_full + 2;  // [2] each
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(img_free + 2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   float *tmp = reinterpret_cast<float *>(sm + L.tmp);
   auto stage = [&](int s) { return sm + (uint32_t)s * L.stage; };
@@ -122,6 +123,10 @@ chunk_state_kernel(const ChunkParams p, uint8_t *__restrict__ ws, float *__restr
       mbar_init(&dfree[b], 128);
     }
     mbar_init(drain, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&img_full[b], 128);  // every state-group thread has written its row
+      mbar_init(&img_free[b], 1);    // the bulk store has read the buffer
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -174,6 +179,24 @@ chunk_state_kernel(const ChunkParams p, uint8_t *__restrict__ ws, float *__restr
       }
       mma_commit(drain);
       (void)mbar_wait_bounded(drain, 0, kSpinLimit);
+    }
+  } else if (warp == 2) {
+    if (lane == 0) {  // ships each image atom with one bulk copy; one copy in flight
+      int done = 0;
+      for (int i = 0; i < nch; ++i) {
+        const int ib = i & 1;
+        if (!wait_or_abort(&img_full[ib], (i >> 1) & 1, abort_flag, p.status)) break;
+        bulk_store(ws + ((size_t)bh * nch + i) * blob_bytes(DK) + (size_t)kb * 16384u,
+                   sm + L.st + (uint32_t)ib * 16384u, 16384u);
+        bulk_commit();
+        if (i > 0) {
+          bulk_wait_read<1>();  // the copy of chunk i - 1 has read its buffer
+          mbar_arrive(&img_free[ib ^ 1]);
+        }
+        done = i + 1;
+      }
+      bulk_wait<0>();
+      if (done > 0) mbar_arrive(&img_free[(done - 1) & 1]);
     }
   } else if (tid >= kAKG) {
     // ------------------------------------------------------------ key group
@@ -308,27 +331,25 @@ chunk_state_kernel(const ChunkParams p, uint8_t *__restrict__ ws, float *__restr
 #pragma unroll
     for (int c = 0; c < kKB; ++c)
       S[c] = (p.S0 && v < DV) ? p.S0[((size_t)bh * DK + c_base + c) * Wmem + v] : 0.f;
+    // Waits here are per thread (no group barrier in the loop), so a thread
+    // that gives up cannot leave the others blocked on a named barrier.
     bool alive = true;
     for (int i = 0; i < nch; ++i) {
-      const int s = i % NS, b = i % kANB;
+      const int s = i % NS, b = i % kANB, ib = i & 1;
       const float *ms = reinterpret_cast<const float *>(sm + L.misc + (uint32_t)s * 1024u);
-      // S_{i-1} as a bf16 image atom, shipped with one bulk copy
-      if (v == 0) bulk_wait_read<1>();  // the atom stored two chunks ago has left its buffer
-      group_sync(kASBar);
-      uint8_t *img = sm + L.st + (uint32_t)(i & 1) * 16384u;
-      store_row32_bf16(img, 16384, v, 0, S);
-      store_row32_bf16(img, 16384, v, 32, S + 32);
-      fence_proxy_async();
-      // decay factors of chunk i (key group) and its local update (tensor core)
-      if (!group_wait(&kready[s], (i / NS) & 1, v, kASBar, abort_flag, p.status)) {
+      // S_{i-1} as a bf16 image atom (warp 2 ships it)
+      if (!wait_or_abort(&img_free[ib], ((i >> 1) & 1) ^ 1, abort_flag, p.status)) {
         alive = false;
         break;
       }
-      if (v == 0) {
-        bulk_store(ws + ((size_t)bh * nch + i) * blob_bytes(DK) + (size_t)kb * 16384u, img, 16384u);
-        bulk_commit();
-      }
-      if (!group_wait(&dfull[b], (i / kANB) & 1, v, kASBar, abort_flag, p.status)) {
+      uint8_t *img = sm + L.st + (uint32_t)ib * 16384u;
+      store_row32_bf16(img, 16384, v, 0, S);
+      store_row32_bf16(img, 16384, v, 32, S + 32);
+      fence_proxy_async();
+      mbar_arrive(&img_full[ib]);
+      // decay factors of chunk i (key group) and its local update (tensor core)
+      if (!wait_or_abort(&kready[s], (i / NS) & 1, abort_flag, p.status) ||
+          !wait_or_abort(&dfull[b], (i / kANB) & 1, abort_flag, p.status)) {
         alive = false;
         break;
       }
@@ -354,7 +375,6 @@ chunk_state_kernel(const ChunkParams p, uint8_t *__restrict__ ws, float *__restr
       }
       mbar_arrive(&empty[s]);
     }
-    if (v == 0) bulk_wait<0>();
     if (alive && p.S_final && v < DV) {
 #pragma unroll
       for (int c = 0; c < kKB; ++c) p.S_final[((size_t)bh * DK + c_base + c) * Wmem + v] = S[c];
