@@ -392,17 +392,20 @@ chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q
           uint8_t *qk = stage(s) + L.qk;
           const int r = v & (kC - 1);
           const float rs = (v < kC) ? ms[kMsEB + r] : ms[kMsVS + r];
-          uint4 u[16];
+#pragma unroll 1
+          for (int g0 = 0; g0 < 16; g0 += 4) {  // rolled: keeps the hot loop's code small
+            uint4 u[4];
 #pragma unroll
-          for (int g8 = 0; g8 < 16; ++g8)
-            u[g8] = *reinterpret_cast<const uint4 *>(qk + (g8 >> 3) * 16384 + sw128_off(v, (g8 & 7) * 8));
+            for (int q = 0; q < 4; ++q)
+              u[q] = *reinterpret_cast<const uint4 *>(qk + ((g0 + q) >> 3) * 16384 + sw128_off(v, ((g0 + q) & 7) * 8));
 #pragma unroll
-          for (int g8 = 0; g8 < 16; ++g8) {
-            float f[8];
-            unpack8(u[g8], f);
+            for (int q = 0; q < 4; ++q) {
+              float f[8];
+              unpack8(u[q], f);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] *= rs;
-            *reinterpret_cast<uint4 *>(qk + (g8 >> 3) * 16384 + sw128_off(v, (g8 & 7) * 8)) = pack8(f);
+              for (int e = 0; e < 8; ++e) f[e] *= rs;
+              *reinterpret_cast<uint4 *>(qk + ((g0 + q) >> 3) * 16384 + sw128_off(v, ((g0 + q) & 7) * 8)) = pack8(f);
+            }
           }
         }
         // state round trip: bf16 operand copy of S_prev, decay in place
@@ -449,12 +452,12 @@ chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q
         __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(p.o) + ((size_t)bh * T + (size_t)c * kC) * DV;
         const bool odd = lane & 1;
 #pragma unroll 1
-        for (int r0 = 0; r0 < kC; r0 += 32) {
-          float a[32];
-          tmem_ld32(tl + kColO + ob * 64 + r0, a);
+        for (int r0 = 0; r0 < kC; r0 += 16) {
+          float a[16];
+          tmem_ld16(tl + kColO + ob * 64 + r0, a);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
+          for (int e = 0; e < 16; e += 2) {
             const float send = odd ? a[e] : a[e + 1];
             const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
             const int r = r0 + e + (odd ? 1 : 0);
@@ -571,7 +574,7 @@ chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q
       // one warp per 16x16 output block (tf32 warp MMAs)
       {
         const int kw = kg >> 5;
-#pragma unroll
+#pragma unroll 1
         for (int lvl = 1; lvl < 4; ++lvl) {
           if (kw < 4 - lvl) {
             const int ib = kw + lvl, jb = kw;

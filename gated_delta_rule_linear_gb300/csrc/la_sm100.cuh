@@ -57,6 +57,7 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parit
 // the caller) if the phase has not completed after `limit` polls; every poll
 // after the first few sleeps briefly, so the limit bounds wall time.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint32_t limit) {
+#pragma unroll 1
   for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (i > 32) __nanosleep(64);

@@ -73,6 +73,9 @@ __device__ __forceinline__ bool group_all(bool v, int id) {
 constexpr uint32_t kSpinLimit = 1u << 24;  // polls before a wait gives up (well over 100 ms)
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                               unsigned *status) {
+  // rolled: every inlined copy of an unrolled spin loop costs kilobytes of
+  // instruction cache, and instruction fetch limits these kernels when many SMs are busy
+#pragma unroll 1
   for (uint32_t i = 0; i < kSpinLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
