@@ -43,7 +43,9 @@ constexpr uint32_t kSpin = 1u << 24;  // polls before a wait gives up (well over
 constexpr int kNM = 4;                // slots of the per-chunk scalar ring
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: state, two score buffers, two output buffers
-constexpr uint32_t kColS = 0, kColD1 = 128, kColO = 256;
+// O: two 64-column buffers; scalar gates keep the inter-chunk part S^T Q^T in
+// its own pair (O1) so that e^{b} is applied in the epilogue, not to Q in place
+constexpr uint32_t kColS = 0, kColD1 = 128, kColO = 256, kColO1 = 384;
 constexpr int kSG = 128, kKG = 256;    // first thread of each group
 constexpr int kBarSG = 1, kBarKG = 2;  // named barriers of the groups
 constexpr float kLog2e = 1.4426950408889634f;
@@ -283,8 +285,9 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
                      id_su, 1);
         }
         mma_commit(s_done);
-        // O^T = S_prev^T Qt^T (bf16 state copy; Qt = Diag(e^b) Q) ...
-        const uint32_t d_o1 = tbase + kColO + (uint32_t)(i & 1) * 64u, d_o2 = d_o1;
+        // O^T = S_prev^T Q^T (bf16 state copy; scalar gates: own buffer, times e^b in the epilogue) ...
+        const uint32_t d_o2 = tbase + kColO + (uint32_t)(i & 1) * 64u;
+        const uint32_t d_o1 = sgate ? tbase + kColO1 + (uint32_t)(i & 1) * 64u : d_o2;
 #pragma unroll
         for (int kk = 0; kk < DK / 16; ++kk) {
           const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -295,7 +298,7 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)
           mma_bf16(d_o2, desc_sw128(a_v + kk * 2048, 8192, 1024), desc_sw128(a_p + kk * 32, 16, 1024),
-                   id_o2, 1);
+                   id_o2, sgate ? (kk > 0) : 1);
         mma_commit(&o_done[i & 1]);
         mma_commit(&empty[s]);
       }
@@ -371,6 +374,14 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
         for (int r0 = 0; r0 < kC; r0 += 32) {
           float a[32];
           tmem_ld32(tl + kColO + ob * 64 + r0, a);
+          if (sgate) {  // O = e^{b_r} (S^T Q^T) + (local part)
+            float b[32], f[32];
+            tmem_ld32(tl + kColO1 + ob * 64 + r0, b);
+            load32(ms + kMsEB + r0, f);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) a[e] = fmaf(f[e], b[e], a[e]);
+          }
           tmem_wait_ld();
           if (elu) {
             float den[32];
@@ -440,21 +451,55 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
       if (!group_all(ok, kBarKG)) break;
       // ---- inclusive log-gate prefix
       if (gla) {
-        if (kg < DK) {
-          float acc = 0.f, bmid = 0.f;
-          for (int r = 0; r < kC; ++r) {
-            acc += gt[r * DK + kg];
-            gt[r * DK + kg] = acc;
-            if (r == kMid) bmid = acc;
-          }
-          ms[kMsBM + kg] = __expf(bmid);
-          ms[kMsBL + kg] = __expf(acc);
-          ms[kMsLM + kg] = __expf(acc - bmid);
+        if (kg < DK) {  // channel kg: all 64 loads first, then the scan in registers
+          float b[kC];
+#pragma unroll
+          for (int r = 0; r < kC; ++r) b[r] = gt[r * DK + kg];
+#pragma unroll
+          for (int r = 1; r < kC; ++r) b[r] += b[r - 1];
+#pragma unroll
+          for (int r = 0; r < kC; ++r) gt[r * DK + kg] = b[r];
+          ms[kMsBM + kg] = __expf(b[kMid]);
+          ms[kMsBL + kg] = __expf(b[kC - 1]);
+          ms[kMsLM + kg] = __expf(b[kC - 1] - b[kMid]);
         }
+        group_sync(kBarKG);
+        // Q e^{b - b_mid}, K e^{b_mid - b} in place: thread kg owns 8-channel
+        // group cg of rows r0 + kStep m (conflict-free tile and gate accesses)
+        constexpr int kGroups = DK / 8, kStep = 128 / kGroups, kRows = kC / kStep;
+        const int cg = kg % kGroups, r0 = kg / kGroups;
+        float bm[8];
+        {
+          const float4 *mp = reinterpret_cast<const float4 *>(gt + kMid * DK + cg * 8);
+          const float4 m0 = mp[0], m1 = mp[1];
+          bm[0] = m0.x; bm[1] = m0.y; bm[2] = m0.z; bm[3] = m0.w;
+          bm[4] = m1.x; bm[5] = m1.y; bm[6] = m1.z; bm[7] = m1.w;
+        }
+#pragma unroll 2
+        for (int m = 0; m < kRows; ++m) {
+          const int r = r0 + kStep * m;
+          const float4 *gp = reinterpret_cast<const float4 *>(gt + r * DK + cg * 8);
+          const float4 g0 = gp[0], g1 = gp[1];
+          const float bv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+          uint4 *pq = reinterpret_cast<uint4 *>(qk + (cg >> 3) * 16384 + sw128_off(r, (cg & 7) * 8));
+          uint4 *pk = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(pq) + 8192);
+          float fq[8], fk[8];
+          unpack8(*pq, fq);
+          unpack8(*pk, fk);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float d = bv[e] - bm[e];
+            fq[e] *= __expf(d);
+            fk[e] *= __expf(-d);
+          }
+          *pq = pack8(fq);
+          *pk = pack8(fk);
+        }
+        fence_proxy_async();
+        group_sync(kBarKG);
       }
-      if (gla) group_sync(kBarKG);
-      // ---- elementwise transforms of the q/k tiles
-      if (elu || gla) {
+      // ---- elementwise transforms of the q/k tiles (elu+1)
+      if (elu) {
         constexpr int kPer = 2 * kC * DK / 8 / 128;  // 16-byte groups per thread
         const int row = kg;                          // row of [Q; K]
         const int r = row & (kC - 1);
@@ -478,15 +523,6 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
                   pack8(fh);
             }
             *reinterpret_cast<uint4 *>(ptr) = hi;
-          } else {
-            const float *brow = gt + r * DK + g8 * 8;
-            const float *bmid = gt + kMid * DK + g8 * 8;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float d = (brow[e] - bmid[e]) * kLog2e;
-              f[e] *= exp2f(is_k ? -d : d);
-            }
-            *reinterpret_cast<uint4 *>(ptr) = pack8(f);
           }
         }
         fence_proxy_async();
@@ -540,69 +576,49 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
       tc_fence_before();
       group_sync(kBarKG);
       if (kg == 0) mbar_arrive(&d1_free[j & 1]);
-      if (sgate) {  // Qt = Diag(e^{b}) Q for the inter-chunk output
-        constexpr int kHalf = DK / 16;
-        const int r = kg >> 1, g0 = (kg & 1) * kHalf;
-        const float rs = ms[kMsEB + r];
-        uint4 u[kHalf];
+      // Row scalings in place. Thread kg owns 16-byte column group cg of rows
+      // r0 + 8 m: a quarter warp covers one row's eight groups of one atom, so
+      // every access is free of bank conflicts.
+      {
+        const int cg = kg & 15, r0 = kg >> 4;
+        // ---- e^{b_last - b_s} V (fast) or Kt; elu+1: z, den
+        if (fast) {
+          if (cg < DV / 8) {
+            uint8_t *base = st + L.v + (cg >> 3) * 8192;
+#pragma unroll 2
+            for (int m = 0; m < 8; ++m) {
+              const int r = r0 + 8 * m;
+              const float rs = ms[kMsVS + r];
+              uint4 *ptr = reinterpret_cast<uint4 *>(base + sw128_off(r, (cg & 7) * 8));
+              float f[8];
+              unpack8(*ptr, f);
 #pragma unroll
-        for (int i = 0; i < kHalf; ++i) {
-          const int g8 = g0 + i;
-          u[i] = *reinterpret_cast<const uint4 *>(qk + (g8 >> 3) * 16384 + sw128_off(r, (g8 & 7) * 8));
-        }
+              for (int e = 0; e < 8; ++e) f[e] *= rs;
+              *ptr = pack8(f);
+            }
+          }
+        } else if (sgate || gla) {
+          if (cg < DK / 8) {
+            float lm[8];
+            if (gla) {
+              const float4 *lp = reinterpret_cast<const float4 *>(ms + kMsLM + cg * 8);
+              const float4 l0 = lp[0], l1 = lp[1];
+              lm[0] = l0.x; lm[1] = l0.y; lm[2] = l0.z; lm[3] = l0.w;
+              lm[4] = l1.x; lm[5] = l1.y; lm[6] = l1.z; lm[7] = l1.w;
+            }
+            uint8_t *base = qk + 8192 + (cg >> 3) * 16384;
+#pragma unroll 2
+            for (int m = 0; m < 8; ++m) {
+              const int r = r0 + 8 * m;
+              const float rs = sgate ? ms[kMsVS + r] : 1.f;
+              uint4 *ptr = reinterpret_cast<uint4 *>(base + sw128_off(r, (cg & 7) * 8));
+              float f[8];
+              unpack8(*ptr, f);
 #pragma unroll
-        for (int i = 0; i < kHalf; ++i) {
-          const int g8 = g0 + i;
-          float f[8];
-          unpack8(u[i], f);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] *= rs;
-          *reinterpret_cast<uint4 *>(qk + (g8 >> 3) * 16384 + sw128_off(r, (g8 & 7) * 8)) = pack8(f);
-        }
-      }
-      // ---- row scaling in place: e^{b_last - b_s} V (fast) or Kt; elu+1: z, den
-      if (fast) {
-        constexpr int kHalf = DV / 16;
-        const int r = kg >> 1, g0 = (kg & 1) * kHalf;
-        const float rs = ms[kMsVS + r];
-        uint4 u[kHalf];
-#pragma unroll
-        for (int i = 0; i < kHalf; ++i) {
-          const int g8 = g0 + i;
-          u[i] = *reinterpret_cast<const uint4 *>(st + L.v + (g8 >> 3) * 8192 + sw128_off(r, (g8 & 7) * 8));
-        }
-#pragma unroll
-        for (int i = 0; i < kHalf; ++i) {
-          const int g8 = g0 + i;
-          float f[8];
-          unpack8(u[i], f);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] *= rs;
-          *reinterpret_cast<uint4 *>(st + L.v + (g8 >> 3) * 8192 + sw128_off(r, (g8 & 7) * 8)) = pack8(f);
-        }
-      } else if (sgate || gla) {
-        constexpr int kHalf = DK / 16;  // 16-byte groups per half row
-        const int r = kg >> 1, g0 = (kg & 1) * kHalf;
-        const float rs = sgate ? ms[kMsVS + r] : 1.f;
-        float lm[gla ? 8 * kHalf : 1];
-        if (gla) {
-#pragma unroll
-          for (int q = 0; q < kHalf / 4; ++q) load32(ms + kMsLM + g0 * 8 + 32 * q, lm + 32 * q);
-        }
-        uint4 u[kHalf];
-#pragma unroll
-        for (int i = 0; i < kHalf; ++i) {
-          const int g8 = g0 + i;
-          u[i] = *reinterpret_cast<const uint4 *>(qk + 8192 + (g8 >> 3) * 16384 + sw128_off(r, (g8 & 7) * 8));
-        }
-#pragma unroll
-        for (int i = 0; i < kHalf; ++i) {
-          const int g8 = g0 + i;
-          float f[8];
-          unpack8(u[i], f);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] *= gla ? lm[(gla ? i * 8 + e : 0)] : rs;
-          *reinterpret_cast<uint4 *>(qk + 8192 + (g8 >> 3) * 16384 + sw128_off(r, (g8 & 7) * 8)) = pack8(f);
+              for (int e = 0; e < 8; ++e) f[e] *= gla ? lm[e] : rs;
+              *ptr = pack8(f);
+            }
+          }
         }
       }
       if (elu) {
