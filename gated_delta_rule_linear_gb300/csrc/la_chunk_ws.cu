@@ -230,6 +230,18 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
           tma_load_3d(st + L.v + a * 8192, &tm_v, &full[s], 64 * a, t0, bh);
         if (gla) tma_load_3d(st + L.g, &tm_g, &full[s], 0, t0, bh);
         if (sgate) mbar_arrive(&full[s]);  // the gate prefix of this chunk is in place
+        // the load of chunk j + ns waits for this chunk's last MMA; warm L2 now
+        if (j + ns < nchunks) {
+          const int tp = t0 + ns * kC;
+#pragma unroll
+          for (int a = 0; a < DK / 64; ++a) {
+            tma_prefetch_3d(&tm_q, 64 * a, tp, bh);
+            tma_prefetch_3d(&tm_k, 64 * a, tp, bh);
+          }
+#pragma unroll
+          for (int a = 0; a < DV / 64; ++a) tma_prefetch_3d(&tm_v, 64 * a, tp, bh);
+          if (gla) tma_prefetch_3d(&tm_g, 0, tp, bh);
+        }
       }
       issued = j + 1;
     }
