@@ -26,12 +26,14 @@
 // epilogue), warps 8-11 key group (P, A, triangular solve, W epilogue,
 // in-place Qt / Kt). All waits are bounded (device status word on expiry).
 #include "la_tc_common.cuh"
+#include "la_wy.cuh"
 
 namespace la {
 namespace {
 
 using namespace sm100;
 using namespace tc;
+using namespace wy;
 
 constexpr int kThreads = 384;
 constexpr int DK = 128, DV = 128;
@@ -43,7 +45,6 @@ constexpr int kSG = 128, kKG = 256;
 constexpr int kBarSG = 1, kBarKG = 2;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kFastLimit = 100.f;
-constexpr int kAp = kC + 4;  // pitch of A and T: 16-byte rows, conflict-free MMA fragments
 
 // per-chunk scalars (floats)
 constexpr int kMsB2 = 0, kMsEB = 64, kMsBeta = 128, kMsDec = 192, kMsB2L = 193, kMsFast = 194,
@@ -74,51 +75,6 @@ __host__ __device__ inline DLayout d_layout() {
   L.bar = o; o += 512u;
   L.total = o;
   return L;
-}
-
-// Round to the nearest tf32 value, ties away from zero (finite inputs): add
-// half of the 13 dropped mantissa bits, then clear them; a mantissa carry
-// moves into the exponent as it should. Two integer operations.
-__device__ __forceinline__ uint32_t to_tf32(float x) { return (__float_as_uint(x) + 0x1000u) & 0xffffe000u; }
-__device__ __forceinline__ float round_tf32(float x) { return __uint_as_float(to_tf32(x)); }
-// Warp-level 16x8x8 tf32 MMA (register fragments), fp32 accumulate.
-__device__ __forceinline__ void mma_16x8x8_tf32(float *d, const uint32_t *a, const uint32_t *b) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-// acc (16x16, two 16x8 fragments) += Ab (16x16) * Bb (16x16): blocks of pitch
-// kAp in shared memory holding values already rounded to tf32; one warp.
-__device__ __forceinline__ void block_mma_16(float (&acc)[2][4], const float *Ab, const float *Bb, int lane) {
-  const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-  for (int ks = 0; ks < 2; ++ks) {
-    uint32_t a[4];
-    a[0] = __float_as_uint(Ab[g * kAp + 8 * ks + t]);
-    a[1] = __float_as_uint(Ab[(g + 8) * kAp + 8 * ks + t]);
-    a[2] = __float_as_uint(Ab[g * kAp + 8 * ks + t + 4]);
-    a[3] = __float_as_uint(Ab[(g + 8) * kAp + 8 * ks + t + 4]);
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      uint32_t b[2];
-      b[0] = __float_as_uint(Bb[(8 * ks + t) * kAp + 8 * nt + g]);
-      b[1] = __float_as_uint(Bb[(8 * ks + t + 4) * kAp + 8 * nt + g]);
-      mma_16x8x8_tf32(acc[nt], a, b);
-    }
-  }
-}
-// Store a 16x16 accumulator (scaled by sgn, rounded to tf32) into a block of pitch kAp.
-__device__ __forceinline__ void block_store_16(float *Cb, const float (&acc)[2][4], float sgn, int lane) {
-  const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
-    *reinterpret_cast<float2 *>(Cb + g * kAp + 8 * nt + 2 * t) =
-        make_float2(round_tf32(sgn * acc[nt][0]), round_tf32(sgn * acc[nt][1]));
-    *reinterpret_cast<float2 *>(Cb + (g + 8) * kAp + 8 * nt + 2 * t) =
-        make_float2(round_tf32(sgn * acc[nt][2]), round_tf32(sgn * acc[nt][3]));
-  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)

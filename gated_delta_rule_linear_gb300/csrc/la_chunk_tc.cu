@@ -34,6 +34,8 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "la_internal.h"
@@ -633,8 +635,20 @@ int launch_chunk_tc(const ChunkParams &p, cudaStream_t stream) {
     return LA_ERR_CUDA;
   }
   if (p.kind != kGdn) return launch_chunk_ws(p, stream);
-  if (p.dk == 128 && p.dv == 128) return launch_chunk_delta(p, stream);
-  if (p.dk == 128 && p.dv == 128) return launch_typed<128, 128>(p, stream);
+  if (p.dk == 128 && p.dv == 128) {
+    // two CTAs per head (value halves, alternate chunks' key side) while the
+    // doubled grid still fits on the GPU at once; LA_DELTA = pair | single forces one
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 0;
+    bool pair = 2LL * p.B * p.H <= sms;
+    if (const char *env = getenv("LA_DELTA")) {
+      if (strcmp(env, "pair") == 0) pair = true;
+      if (strcmp(env, "single") == 0) pair = false;
+    }
+    return pair ? launch_chunk_delta_pair(p, stream) : launch_chunk_delta(p, stream);
+  }
   if (p.dk == 128 && p.dv == 64) return launch_typed<128, 64>(p, stream);
   if (p.dk == 64 && p.dv == 128) return launch_typed<64, 128>(p, stream);
   return launch_typed<64, 64>(p, stream);

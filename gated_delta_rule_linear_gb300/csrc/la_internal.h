@@ -57,6 +57,7 @@ int launch_chunk_simt(const ChunkParams &p, cudaStream_t stream);
 int launch_chunk_tc(const ChunkParams &p, cudaStream_t stream);
 int launch_chunk_ws(const ChunkParams &p, cudaStream_t stream);
 int launch_chunk_delta(const ChunkParams &p, cudaStream_t stream);
+int launch_chunk_delta_pair(const ChunkParams &p, cudaStream_t stream);
 int launch_step(const StepParams &p, cudaStream_t stream);
 // Materialised (two-phase) variant: chunk-state pass then a parallel output
 // pass, through a caller-provided workspace of mat_workspace_bytes(p) bytes.

@@ -85,6 +85,19 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
   return false;
 }
 
+// wait_or_abort for an mbarrier that another CTA of the cluster arrives on.
+__device__ __forceinline__ bool wait_or_abort_cluster(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                                      unsigned *status) {
+#pragma unroll 1
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (*abort_flag) return false;
+  }
+  *abort_flag = 1;
+  atomicOr(status, kStatusTimeout);
+  return false;
+}
+
 // Group-wide wait: one elected thread polls the mbarrier while the rest of
 // the 128-thread group sleeps on the group's named barrier (no issue slots
 // used); the outcome is shared by the barrier reduction, which also orders

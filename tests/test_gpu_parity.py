@@ -207,3 +207,46 @@ def test_full_size_workload_sampled_heads(name):
     assert_close(S_got, S_ref, wl.dtype, f"{name} S_final (sampled heads)")
     # every head: finite output
     assert torch.isfinite(o.float()).all()
+
+
+# --- delta rule: one CTA per head, or a CTA pair per head ---------------------
+
+@pytest.mark.parametrize("path", ["single", "pair"])
+@pytest.mark.parametrize("T", [1, 64, 65, 200, 1000])
+@pytest.mark.parametrize("gated", [True, False])
+def test_delta_kernel_paths(path, T, gated, monkeypatch):
+    monkeypatch.setenv("LA_DELTA", path)
+    inp = _inputs("gdn", "bf16", B=2, H=3, T=T)
+    if not gated:
+        inp["g"] = None
+    o, S = run_cuda(inp)
+    o_ref, S_ref = run_oracle(inp)
+    assert_close(f64(o), o_ref, "bf16", f"{path} T={T} o")
+    assert_close(f64(S), S_ref, "bf16", f"{path} T={T} S")
+
+
+@pytest.mark.parametrize("path", ["single", "pair"])
+def test_delta_kernel_paths_aliased_state_and_split(path, monkeypatch):
+    monkeypatch.setenv("LA_DELTA", path)
+    inp = _inputs("gdn", "bf16", B=1, H=2, T=300)
+    d = to_dev(inp)
+    S = d["S0"].clone()
+    o, _ = la.chunk_fwd(d["q"], d["k"], d["v"], "gdn", g=d["g"], beta=d["beta"], S0=S, S_final=S)
+    torch.cuda.synchronize()
+    o_ref, S_ref = run_oracle(inp)
+    assert_close(f64(o), o_ref, "bf16", "aliased o")
+    assert_close(f64(S), S_ref, "bf16", "aliased S")
+
+
+def test_delta_pair_and_single_agree():
+    inp = _inputs("gdn", "bf16", B=2, H=4, T=777)
+    import os
+    outs = []
+    for path in ("single", "pair"):
+        os.environ["LA_DELTA"] = path
+        try:
+            outs.append(run_cuda(inp))
+        finally:
+            del os.environ["LA_DELTA"]
+    assert_close(f64(outs[1][0]), f64(outs[0][0]), "bf16", "pair vs single o")
+    assert_close(f64(outs[1][1]), f64(outs[0][1]), "bf16", "pair vs single S")
