@@ -40,6 +40,8 @@ METRIC = "tokens/sec and TFLOP/s of chunk fwd at 1 GB300; % of roofline"
 UNIT = "tokens/s"
 PROFILE_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 KERNEL_SOURCES = ["gated_delta_rule_linear_gb300/csrc/la_chunk_delta.cu",
+                  "gated_delta_rule_linear_gb300/csrc/la_chunk_delta_pair.cu",
+                  "gated_delta_rule_linear_gb300/csrc/la_wy.cuh",
                   "gated_delta_rule_linear_gb300/csrc/la_chunk_ws.cu",
                   "gated_delta_rule_linear_gb300/csrc/la_chunk_mat.cu",
                   "gated_delta_rule_linear_gb300/csrc/la_tc_common.cuh",
@@ -62,7 +64,10 @@ def kernel_name(wl, variant=None, sm_count=152) -> str:
     if wl.dtype == "f32" or variant == "simt":
         return "chunk_simt_kernel"
     if wl.mode == "gdn":
-        return "chunk_delta_kernel" if wl.dk == 128 and wl.dv == 128 else "chunk_tc_kernel"
+        if wl.dk == 128 and wl.dv == 128:
+            pair = os.environ.get("LA_DELTA", "pair" if 2 * wl.B * wl.H <= sm_count else "single")
+            return "chunk_delta_pair_kernel" if pair == "pair" else "chunk_delta_kernel"
+        return "chunk_tc_kernel"
     return "chunk_ws_kernel"
 
 
