@@ -102,14 +102,20 @@ def kronecker_delta(q, k, v, beta, S0=None, log_alpha=None):
                  + beta_t vec(k_t v_t^T),
     the Kronecker-product statement of the reparameterised delta rule
     S_t = (I - beta k k^T) alpha S_{t-1} + beta k v^T ("Talk Linear
-    Attention", section 6.2, transposed to key-major). Tiny sizes only."""
+    Attention", section 6.2, transposed to key-major). With a per-channel
+    log_alpha [T, dk] the factor is (I - beta k k^T) Diag(alpha_t), the Kimi
+    Delta Attention update as the "LLM attention optimisation" page writes it
+    (its Kimi Delta Attention section). Tiny sizes only."""
     T, dk = k.shape
     dv = v.shape[1]
     s = np.zeros(dk * dv) if S0 is None else np.asarray(S0, dtype=np.float64).reshape(-1, order="F")
     o = np.zeros((T, dv))
     for t in range(T):
-        a = 1.0 if log_alpha is None else np.exp(log_alpha[t])
-        Ht = a * (np.eye(dk) - beta[t] * np.outer(k[t], k[t]))
+        if log_alpha is None:
+            D = np.eye(dk)
+        else:
+            D = np.diag(np.broadcast_to(np.exp(np.asarray(log_alpha[t], dtype=np.float64)), (dk,)))
+        Ht = (np.eye(dk) - beta[t] * np.outer(k[t], k[t])) @ D
         s = np.kron(np.eye(dv), Ht) @ s + beta[t] * np.outer(k[t], v[t]).reshape(-1, order="F")
         St = s.reshape(dk, dv, order="F")
         o[t] = St.T @ q[t]
@@ -128,13 +134,16 @@ def chunk_form(q, k, v, mode, g=None, beta=None, S0=None, C=64):
       U  = T (diag(beta) V - diag(beta e^b) K S),  T = (I + A)^{-1},
            A_rs = beta_r exp(b_r - b_s) k_r.k_s for s < r   (delta rule: the
            WY/UT form of section 6.2 that removes the serial dependency)
+    kda takes the per-channel prefix of gla into the delta rule: the factors
+    e^{b} act channel by channel, A_rs = beta_r sum_c k_rc k_sc e^{b_rc - b_sc},
+    U = T (diag(beta) V - diag(beta) (K ⊙ e^b) S), S <- Diag(e^{b_last}) S + Kt^T U.
       O  = Qt S + P U                         (inter-chunk + local, section 3.2)
       S <- Diag(exp(b_last)) S + Kt^T U       (state passing, section 3.2)
     elu1 applies phi to q and k first and divides by Qt z + P 1, carrying
     z <- z + sum phi(k). C=1 reduces this to the recurrence and C=T to the
     parallel form (section 3.3).
 
-    g: retnet scalar log gamma for this head; scalar/gdn [T]; gla [T, dk].
+    g: retnet scalar log gamma for this head; scalar/gdn [T]; gla/kda [T, dk].
     Returns (o [T, dv], S [dk, dv] or [dk, dv + 1] for elu1).
     """
     q = np.asarray(q, dtype=np.float64)
@@ -161,13 +170,13 @@ def chunk_form(q, k, v, mode, g=None, beta=None, S0=None, C=64):
             lg = np.full(n, float(g))
         elif mode in ("scalar",) or (mode == "gdn" and g is not None):
             lg = np.asarray(g[t0:t1], dtype=np.float64)
-        elif mode == "gla":
+        elif mode in ("gla", "kda"):
             lg = np.asarray(g[t0:t1], dtype=np.float64)
         else:
             lg = np.zeros(n)
         b = np.cumsum(lg, axis=0)
         tril = np.tril(np.ones((n, n)))
-        if mode == "gla":
+        if mode in ("gla", "kda"):
             P = ((Q * np.exp(b)) @ (K * np.exp(-b)).T) * tril
             Qt = Q * np.exp(b)
             Kt = K * np.exp(b[-1][None, :] - b)
@@ -181,6 +190,11 @@ def chunk_form(q, k, v, mode, g=None, beta=None, S0=None, C=64):
             bet = np.ones(n) if beta is None else np.asarray(beta[t0:t1], dtype=np.float64)
             A = np.tril(bet[:, None] * np.exp(b[:, None] - b[None, :]) * (K @ K.T), -1)
             rhs = bet[:, None] * V - (bet * np.exp(b))[:, None] * (K @ S)
+            U = solve_triangular(np.eye(n) + A, rhs, lower=True, unit_diagonal=True)
+        elif mode == "kda":
+            bet = np.ones(n) if beta is None else np.asarray(beta[t0:t1], dtype=np.float64)
+            A = np.tril(bet[:, None] * ((K * np.exp(b)) @ (K * np.exp(-b)).T), -1)
+            rhs = bet[:, None] * (V - (K * np.exp(b)) @ S)
             U = solve_triangular(np.eye(n) + A, rhs, lower=True, unit_diagonal=True)
         else:
             U = V

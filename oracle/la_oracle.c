@@ -19,6 +19,8 @@
  *   mode 4 scalar : S = alpha_t S + k v^T, g[b,h,t]
  *   mode 5 gdn    : S = alpha_t S; u = beta_t (v - S^T k); S += k u^T
  *                   (Gated DeltaNet: decay, then the delta rule)
+ *   mode 6 kda    : S = Diag(alpha_t) S; u = beta_t (v - S^T k); S += k u^T
+ *                   (Kimi Delta Attention: per-key-channel gate g[b,h,t,c])
  *
  * Layouts: q,k [B,H,T,dk], v,o [B,H,T,dv], S0/S [B,H,dk,W] with W = dv+1 for
  * elu1 (z in column dv) and W = dv otherwise. g/beta/S0 may be NULL where the
@@ -75,7 +77,7 @@ static void run_head(const job_t *J, int bh) {
             if (mode == 2) a = exp(J->g[h]);
             else a = exp(J->g[(size_t)bh * T + t]);
             for (size_t i = 0; i < (size_t)dk * dv; ++i) S[i] *= a;
-        } else if (mode == 3) {
+        } else if (mode == 3 || mode == 6) {
             const double *gt = J->g + ((size_t)bh * T + t) * dk;
             for (int c = 0; c < dk; ++c) {
                 double a = exp(gt[c]);
@@ -83,7 +85,7 @@ static void run_head(const job_t *J, int bh) {
             }
         }
         /* write */
-        if (mode == 5) {
+        if (mode == 5 || mode == 6) {
             double b = J->beta ? J->beta[(size_t)bh * T + t] : 1.0;
             for (int j = 0; j < dv; ++j) u[j] = 0.0;
             for (int c = 0; c < dk; ++c)
@@ -128,9 +130,9 @@ static void *worker(void *arg) {
 int la_oracle_fwd(const double *q, const double *k, const double *v, const double *g,
                   const double *beta, const double *S0, double *o, double *S,
                   int B, int H, int T, int dk, int dv, int mode, int nthreads) {
-    if (!q || !k || !v || !o || B < 1 || H < 1 || T < 0 || dk < 1 || dv < 1 || mode < 0 || mode > 5)
+    if (!q || !k || !v || !o || B < 1 || H < 1 || T < 0 || dk < 1 || dv < 1 || mode < 0 || mode > 6)
         return -1;
-    if ((mode == 2 || mode == 3 || mode == 4) && !g) return -1;
+    if ((mode == 2 || mode == 3 || mode == 4 || mode == 6) && !g) return -1;
     const int BH = B * H;
     if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
     if (nthreads < 1) nthreads = 1;

@@ -27,10 +27,16 @@ Per (b, h), starting from S0 (zero when absent), for t = 0..T-1:
           o_t = S^T q_t  (Gated DeltaNet: decay first, then the delta rule,
           "LLM attention optimisation" page, Gated DeltaNet section;
           "Talk Linear Attention" section 6.2 reparameterised form)
+  kda     S <- Diag(alpha_t) S ; u = beta_t (v_t - S^T k_t) ; S <- S + k_t u^T
+          (Kimi Delta Attention: Gated DeltaNet with a per-key-channel gate,
+          S_t = (I - beta k k^T) Diag(alpha_t) S_{t-1} + beta k v^T in this
+          key-major orientation; "LLM attention optimisation" page, Kimi Delta
+          Attention section)
 
 Gates are natural logs: alpha = exp(g). retnet takes g of shape [H]; scalar
-and gdn take [B, H, T]; gla takes [B, H, T, dk]. gdn takes beta [B, H, T];
-a missing g means alpha = 1 (plain DeltaNet) and a missing beta means 1.
+and gdn take [B, H, T]; gla and kda take [B, H, T, dk]. gdn and kda take beta
+[B, H, T]; a missing g means alpha = 1 (plain DeltaNet, gdn only) and a
+missing beta means 1.
 
 For elu1 the state carries z as an extra value column: S has shape
 [dk, dv + 1] with z in column dv, both in S0 and in the returned state.
@@ -46,7 +52,7 @@ import numpy as np
 
 __all__ = ["recurrence", "phi_elu1", "MODES"]
 
-MODES = ("linear", "elu1", "retnet", "gla", "scalar", "gdn")
+MODES = ("linear", "elu1", "retnet", "gla", "scalar", "gdn", "kda")
 
 
 def phi_elu1(x):
@@ -105,8 +111,10 @@ def recurrence(q, k, v, mode, g=None, beta=None, S0=None):
             alpha = np.exp(g[:, :, t])[..., :, None]              # [B,H,dk,1]
             S = alpha * S + kt[..., :, None] * vt[..., None, :]
             o[:, :, t] = np.einsum("bhc,bhcv->bhv", qt, S)
-        else:  # gdn
-            if g is not None:
+        else:  # gdn, kda: decay first, then the delta rule
+            if mode == "kda":
+                S = np.exp(g[:, :, t])[..., :, None] * S          # Diag(alpha_t) on the key axis
+            elif g is not None:
                 S = np.exp(g[:, :, t])[..., None, None] * S
             b = 1.0 if beta is None else beta[:, :, t][..., None]   # [B,H,1]
             retrieved = np.einsum("bhc,bhcv->bhv", kt, S)         # S^T k_t

@@ -173,6 +173,66 @@ def test_gdn_beta_one_overwrites_repeated_key():
     np.testing.assert_allclose(S_lin[0, 0].T @ e[0], 4.0, atol=1e-15)
 
 
+# --- Kimi Delta Attention (per-key-channel gate) --------------------------------
+
+def _kda_case(T=7, dk=4, dv=3):
+    q, k, v = _heads(1, 1, T, dk, dv)
+    beta = 1.0 / (1.0 + np.exp(-_rand(1, 1, T)))
+    g = -np.abs(_rand(1, 1, T, dk, scale=0.4))
+    S0 = _rand(1, 1, dk, dv, scale=0.5)
+    return q, k, v, g, beta, S0
+
+
+def test_kda_equals_kronecker_brute_force():
+    # the page's product S_t = (I - beta k k^T) Diag(alpha_t) S_{t-1} + beta k v^T
+    q, k, v, g, beta, S0 = _kda_case()
+    o, S = recurrence(q, k, v, "kda", g=g, beta=beta, S0=S0)
+    o_ref, S_ref = forms.kronecker_delta(q[0, 0], k[0, 0], v[0, 0], beta[0, 0], S0[0, 0], g[0, 0])
+    _close(o[0, 0], o_ref, 1e-12)
+    _close(S[0, 0], S_ref, 1e-12)
+
+
+def test_kda_with_equal_channel_gates_is_gdn():
+    q, k, v, g, beta, S0 = _kda_case(T=20, dk=5, dv=4)
+    gs = g[..., 0]                                    # one gate per token
+    gk = np.repeat(gs[..., None], 5, axis=-1)         # ... given to every channel
+    o1, S1 = recurrence(q, k, v, "kda", g=gk, beta=beta, S0=S0)
+    o2, S2 = recurrence(q, k, v, "gdn", g=gs, beta=beta, S0=S0)
+    _close(o1, o2, 1e-13)
+    _close(S1, S2, 1e-13)
+
+
+def test_kda_beta_zero_is_pure_channel_decay():
+    # beta = 0 writes nothing: S_t = Diag(exp(sum_{s<=t} g_s)) S0 row by row
+    q, k, v, g, _, S0 = _kda_case(T=9, dk=4, dv=3)
+    o, S = recurrence(q, k, v, "kda", g=g, beta=np.zeros((1, 1, 9)), S0=S0)
+    cum = np.cumsum(g[0, 0], axis=0)                  # [T, dk]
+    for t in range(9):
+        St = np.exp(cum[t])[:, None] * S0[0, 0]
+        _close(o[0, 0, t], St.T @ q[0, 0, t], 1e-13)
+    _close(S[0, 0], np.exp(cum[-1])[:, None] * S0[0, 0], 1e-13)
+
+
+def test_kda_pins_detect_planted_mistakes():
+    q, k, v, g, beta, S0 = _kda_case()
+    o_ref, S_ref = forms.kronecker_delta(q[0, 0], k[0, 0], v[0, 0], beta[0, 0], S0[0, 0], g[0, 0])
+
+    def passes(o, S):
+        return np.max(np.abs(o[0, 0] - o_ref)) < 1e-10 and np.max(np.abs(S[0, 0] - S_ref)) < 1e-10
+
+    assert passes(*recurrence(q, k, v, "kda", g=g, beta=beta, S0=S0))
+    # channels of the gate permuted (a wrong index on the key axis)
+    assert not passes(*recurrence(q, k, v, "kda", g=g[..., ::-1], beta=beta, S0=S0))
+    # the gate of the next token (off by one in time)
+    assert not passes(*recurrence(q, k, v, "kda", g=np.roll(g, -1, axis=2), beta=beta, S0=S0))
+    # wrong sign of the delta correction
+    assert not passes(*recurrence(q, k, v, "kda", g=g, beta=-beta, S0=S0))
+    # unit write instead of the delta rule
+    assert not passes(*recurrence(q, k, v, "gla", g=g, S0=S0))
+    # one scalar gate per token (the channel structure dropped)
+    assert not passes(*recurrence(q, k, v, "gdn", g=g.mean(-1), beta=beta, S0=S0))
+
+
 # --- chunk form limits and chunk sizes ---------------------------------------
 
 def _mode_inputs(mode, T, dk=8, dv=6, s0=True):
@@ -182,9 +242,9 @@ def _mode_inputs(mode, T, dk=8, dv=6, s0=True):
         g = np.array([np.log1p(-2.0 ** -3)])
     elif mode in ("scalar", "gdn"):
         g = -np.abs(_rand(1, 1, T, scale=0.15))
-    elif mode == "gla":
+    elif mode in ("gla", "kda"):
         g = -np.abs(_rand(1, 1, T, dk, scale=0.05))
-    if mode == "gdn":
+    if mode in ("gdn", "kda"):
         k = k / np.linalg.norm(k, axis=-1, keepdims=True)
         beta = 1.0 / (1.0 + np.exp(-_rand(1, 1, T)))
     S0 = None
@@ -244,9 +304,9 @@ def test_c_oracle_matches_numpy(mode):
         g = np.log1p(-(2.0 ** (-5.0 - np.arange(H))))
     elif mode in ("scalar", "gdn"):
         g = -np.abs(_rand(B, H, T, scale=0.1))
-    elif mode == "gla":
+    elif mode in ("gla", "kda"):
         g = -np.abs(_rand(B, H, T, dk, scale=0.1))
-    if mode == "gdn":
+    if mode in ("gdn", "kda"):
         beta = 1.0 / (1.0 + np.exp(-_rand(B, H, T)))
     S0 = _rand(B, H, dk, dv + (mode == "elu1"), scale=0.2)
     if mode == "elu1":
