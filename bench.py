@@ -53,7 +53,7 @@ def uses_materialised(wl, variant=None, sm_count=152) -> bool:
     (the library's per-shape rule, or a forced LA_VARIANT)."""
     if variant is not None:
         return variant == "mat"
-    return (wl.dtype == "bf16" and wl.mode != "gdn" and wl.T >= 512
+    return (wl.dtype == "bf16" and wl.mode not in ("gdn", "kda") and wl.T >= 512
             and 2 * wl.B * wl.H <= sm_count)
 
 
@@ -63,6 +63,8 @@ def kernel_name(wl, variant=None, sm_count=152) -> str:
         return "chunk_state_kernel+chunk_output_kernel"
     if wl.dtype == "f32" or variant == "simt":
         return "chunk_simt_kernel"
+    if wl.mode == "kda":
+        return "chunk_tc_kernel"
     if wl.mode == "gdn":
         if wl.dk == 128 and wl.dv == 128:
             pair = os.environ.get("LA_DELTA", "pair" if 2 * wl.B * wl.H <= sm_count else "single")
@@ -81,7 +83,7 @@ def flops_per_token_head(mode: str, dk: int, dv: int, C: int = 64) -> float:
     (2*dk*dv). elu+1 carries one extra value column (the normaliser)."""
     if mode == "elu1":
         dv = dv + 1
-    if mode == "gdn":
+    if mode in ("gdn", "kda"):  # the per-channel gate of kda changes no contraction size
         return 2 * C * (3 * dk + 2 * dv) + C * C / 3.0 + 6 * dk * dv
     return 2 * C * (dk + dv) + 4 * dk * dv
 
@@ -94,9 +96,9 @@ def algorithmic_bytes(wl, has_s0: bool) -> float:
     per_tok = e * (2 * dk + dv) + e * dv
     if wl.mode in ("scalar", "gdn"):
         per_tok += 4
-    if wl.mode == "gdn":
+    if wl.mode in ("gdn", "kda"):
         per_tok += 4
-    if wl.mode == "gla":
+    if wl.mode in ("gla", "kda"):
         per_tok += 4 * dk
     W = dv + 1 if wl.mode == "elu1" else dv
     state = 4 * dk * W * (2 if has_s0 else 1)

@@ -38,6 +38,7 @@ MODE_IDS = {
     "gla": CONSTANTS["LA_GLA"],
     "scalar": CONSTANTS["LA_SCALAR_GATE"],
     "gdn": CONSTANTS["LA_GDN"],
+    "kda": CONSTANTS["LA_KDA"],
 }
 
 # Every function the header declares, with its ctypes signature.

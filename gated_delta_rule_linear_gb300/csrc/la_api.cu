@@ -99,7 +99,18 @@ int select_variant(const ChunkParams &p, int *chunk_out) {
     return -1;
   }
   *chunk_out = C;
+  if (p.f32 && p.kind == kKda) {
+    set_error("la_chunk_fwd: LA_KDA takes bfloat16 inputs only");
+    return -1;
+  }
   if (p.f32) return (want == kVariantTc || want == kVariantMat) ? -2 : kVariantSimt;
+  if (p.kind == kKda) {  // the tensor-core kernel only
+    if (want == kVariantMat || want == kVariantSimt) {
+      set_error("la_chunk_fwd: LA_KDA runs on the fused tensor-core kernel only");
+      return -1;
+    }
+    return kVariantTc;
+  }
   if (want == kVariantMat && p.kind == kGdn) {
     set_error("la_chunk_fwd: the materialised variant covers the unit-write modes only");
     return -1;
@@ -147,11 +158,11 @@ int la_stream_status(la_stream_t stream) {
 
 static int check_mode(int mode, const float *g, const float *beta, const char *fn) {
   const int kind = mode & 0xff;
-  if ((mode & ~(0xff | LA_F32)) != 0 || kind < LA_LINEAR || kind > LA_GDN) {
+  if ((mode & ~(0xff | LA_F32)) != 0 || kind < LA_LINEAR || kind > LA_KDA) {
     set_error("%s: unknown mode 0x%x", fn, mode);
     return LA_ERR_INVALID_ARG;
   }
-  const bool needs_g = kind == LA_RETNET || kind == LA_GLA || kind == LA_SCALAR_GATE;
+  const bool needs_g = kind == LA_RETNET || kind == LA_GLA || kind == LA_SCALAR_GATE || kind == LA_KDA;
   const bool takes_g = needs_g || kind == LA_GDN;
   if (needs_g && !g) {
     set_error("%s: mode %d needs log-gates g", fn, kind);
@@ -161,8 +172,8 @@ static int check_mode(int mode, const float *g, const float *beta, const char *f
     set_error("%s: mode %d takes no gates (g must be NULL)", fn, kind);
     return LA_ERR_INVALID_ARG;
   }
-  if (kind != LA_GDN && beta) {
-    set_error("%s: beta is only used by LA_GDN (must be NULL for mode %d)", fn, kind);
+  if (kind != LA_GDN && kind != LA_KDA && beta) {
+    set_error("%s: beta is only used by LA_GDN and LA_KDA (must be NULL for mode %d)", fn, kind);
     return LA_ERR_INVALID_ARG;
   }
   return LA_OK;
@@ -200,9 +211,9 @@ int la_chunk_fwd(const void *q, const void *k, const void *v, const float *g, co
     set_error("%s: q, k, v and o must be 16-byte aligned", fn);
     return LA_ERR_INVALID_ARG;
   }
-  if ((g && !aligned(g, kind == LA_GLA ? 16 : 4)) || (beta && !aligned(beta, 4)) ||
+  if ((g && !aligned(g, (kind == LA_GLA || kind == LA_KDA) ? 16 : 4)) || (beta && !aligned(beta, 4)) ||
       (S0 && !aligned(S0, 4)) || (S_final && !aligned(S_final, 4))) {
-    set_error("%s: g (16 bytes for LA_GLA), beta, S0 and S_final must be aligned", fn);
+    set_error("%s: g (16 bytes for LA_GLA and LA_KDA), beta, S0 and S_final must be aligned", fn);
     return LA_ERR_INVALID_ARG;
   }
 

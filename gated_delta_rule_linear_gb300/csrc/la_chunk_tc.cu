@@ -57,7 +57,8 @@ constexpr uint32_t kColS = 0, kColD1 = 128, kColO1 = 192, kColO2 = 256, kColY = 
 constexpr int kAp = kC + 1;  // fp32 pitch of the A / T work matrices
 
 struct TcLayout {
-  uint32_t qk[2], v[2], g[2], st, p, t, z, u, af, tf, x, klo, misc, bar, total;
+  uint32_t qk[2], v[2], g[2], st, p, t, z, u, af, tf, x, klo, kb, misc, bar, total;
+  int ns;  // q/k/v(/g) stages: two, one for Kimi Delta Attention (gate tile + solve buffers)
 };
 
 __host__ __device__ inline uint32_t up1k(uint32_t x) { return (x + 1023u) & ~1023u; }
@@ -65,12 +66,17 @@ __host__ __device__ inline uint32_t up1k(uint32_t x) { return (x + 1023u) & ~102
 __host__ __device__ inline TcLayout tc_layout(int dk, int dv, int kind) {
   (void)dv;
   TcLayout L;
-  const bool gla = kind == kGla, delta = kind == kGdn;
+  const bool kda = kind == kKda, pg = kind == kGla || kda, delta = kind == kGdn || kda;
   const uint32_t qk_bytes = (uint32_t)(dk / 64) * 16384u;
+  L.ns = kda ? 1 : 2;
   uint32_t o = 0;
-  for (int s = 0; s < 2; ++s) { L.qk[s] = o; o += qk_bytes; }
-  for (int s = 0; s < 2; ++s) { L.v[s] = o; o += 16384u; }  // second 8 KB is a zero pad when dv = 64
-  for (int s = 0; s < 2; ++s) { L.g[s] = o; o += gla ? up1k((uint32_t)kC * dk * 4u) : 0u; }
+  for (int s = 0; s < 2; ++s) { L.qk[s] = (s < L.ns) ? o : L.qk[0]; o += (s < L.ns) ? qk_bytes : 0u; }
+  for (int s = 0; s < 2; ++s) { L.v[s] = (s < L.ns) ? o : L.v[0]; o += (s < L.ns) ? 16384u : 0u; }  // second 8 KB: zero pad when dv = 64
+  for (int s = 0; s < 2; ++s) {
+    const uint32_t gb = pg ? up1k((uint32_t)kC * dk * 4u) : 0u;
+    L.g[s] = (s < L.ns) ? o : L.g[0];
+    o += (s < L.ns) ? gb : 0u;
+  }
   L.st = o; o += qk_bytes;          // bf16 S^T operand copy: 128 rows x dk
   L.p = o; o += 8192u;              // P, 64 x 64 bf16
   L.t = o; o += delta ? 8192u : 0u;
@@ -80,6 +86,7 @@ __host__ __device__ inline TcLayout tc_layout(int dk, int dv, int kind) {
   L.tf = o; o += delta ? up1k(kC * kAp * 4u) : 0u;
   L.x = o; o += delta ? up1k(3u * 256u * 4u) : 0u;
   L.klo = o; o += (kind == kElu1) ? (uint32_t)(dk / 64) * 8192u : 0u;  // low half of phi(k)
+  L.kb = o; o += kda ? (uint32_t)(dk / 64) * 8192u : 0u;  // KDA: K e^{b_m - B}, then K e^{b_last - B}
   L.misc = o; o += up1k((7u * kC + 4u * 128u) * 4u);
   L.bar = o; o += 64u;
   L.total = o;
@@ -96,7 +103,9 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                                             ~static_cast<uintptr_t>(1023));
   const int kind = p.kind;
   const TcLayout L = tc_layout(DK, DV, kind);
-  const bool elu = kind == kElu1, gla = kind == kGla, delta = kind == kGdn;
+  const bool elu = kind == kElu1, gla = kind == kGla, kda = kind == kKda;
+  const bool pg = gla || kda;                // per-key-channel gates (midpoint fold)
+  const bool delta = kind == kGdn || kda;
   const bool sgate = kind == kRetnet || kind == kScalar || (kind == kGdn && p.g != nullptr);
   const int tid = threadIdx.x, warp = tid >> 5;
   const int bh = blockIdx.x, h = bh % p.H;
@@ -133,7 +142,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
-    if (gla) prefetch_tmap(&tm_g);
+    if (pg) prefetch_tmap(&tm_g);
   }
   if (DV == 64) {  // zero pad block above the 64 real value rows of each V stage
     for (int i = tid; i < 2 * 512; i += kThreads) {
@@ -147,7 +156,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
   const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
   const uint32_t tl = tbase + lane_base;  // this thread's TMEM lane, column 0
 
-  const uint32_t stage_bytes = 2u * DK * kC * 2u + DV * kC * 2u + (gla ? DK * kC * 4u : 0u);
+  const uint32_t stage_bytes = 2u * DK * kC * 2u + DV * kC * 2u + (pg ? DK * kC * 4u : 0u);
   auto issue_loads = [&](int chunk, int s) {
     const int t0 = chunk * kC;
     mbar_arrive_expect_tx(&bar_full[s], stage_bytes);
@@ -159,11 +168,11 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
     for (int a = 0; a < DV / 64; ++a)
       tma_load_3d(sm + L.v[s] + a * 8192, &tm_v, &bar_full[s], 64 * a, t0, bh);
-    if (gla) tma_load_3d(sm + L.g[s], &tm_g, &bar_full[s], 0, t0, bh);
+    if (pg) tma_load_3d(sm + L.g[s], &tm_g, &bar_full[s], 0, t0, bh);
   };
   int pending[2] = {-1, -1};  // chunk whose copies are in flight per stage (thread 0)
   if (tid == 0) {
-    for (int s = 0; s < 2 && s < nchunks; ++s) {
+    for (int s = 0; s < L.ns && s < nchunks; ++s) {
       issue_loads(s, s);
       pending[s] = s;
     }
@@ -205,8 +214,8 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
   const uint32_t id_su = idesc_bf16_f32(128, DK, !delta, true);
 
   for (int i = 0; i < nchunks; ++i) {
-    const int t0 = i * kC, n = min(kC, T - t0), s = i & 1;
-    const uint32_t fpar = (i >> 1) & 1;
+    const int t0 = i * kC, n = min(kC, T - t0), s = i % L.ns;
+    const uint32_t fpar = (i / L.ns) & 1;
     uint8_t *qk = sm + L.qk[s];
     uint8_t *vt = sm + L.v[s];
     float *gt = reinterpret_cast<float *>(sm + L.g[s]);
@@ -221,7 +230,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
     if (tid == 0) pending[s] = -1;
 
     // ---- inclusive log-gate prefix ----------------------------------------
-    if (gla) {
+    if (pg) {
       if (tid < DK) {
         float acc = 0.f, bmid = 0.f;
         for (int r = 0; r < kC; ++r) {
@@ -255,7 +264,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
     __syncthreads();
 
     // ---- elementwise prologue on the Q / K tiles -------------------------
-    if (elu || gla) {
+    if (elu || pg) {
       constexpr int kChunks = 2 * kC * DK / 8;  // 16-byte groups in [Q;K]
       for (int ci = tid; ci < kChunks; ci += kThreads) {
         const int g8 = ci % (DK / 8), row = ci / (DK / 8);  // row 0..127 of [Q;K]
@@ -277,13 +286,20 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
                 f32_to_bf16x8(fh);
           }
         } else {
+          // GLA: Q e^{B - b_m}, K e^{b_m - B}. KDA: Q and K rows both e^{B - b_m} (the A rows
+          // of K K^T and the key side of Y = (K e^B) S), K e^{b_m - B} apart (scores' B operand)
           const float *brow = gt + r * DK + g8 * 8;
           const float *bmid = gt + kMid * DK + g8 * 8;
+          float fo[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const float d = brow[e] - bmid[e];
-            f[e] *= __expf(is_k ? -d : d);
+            fo[e] = f[e] * __expf(-d);
+            f[e] *= __expf((is_k && !kda) ? -d : d);
           }
+          if (kda && is_k)
+            *reinterpret_cast<uint4 *>(sm + L.kb + (g8 >> 3) * 8192 + sw128_off(r, (g8 & 7) * 8)) =
+                f32_to_bf16x8(fo);
         }
         *reinterpret_cast<uint4 *>(ptr) = f32_to_bf16x8(f);
       }
@@ -291,17 +307,17 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
 
     // ---- state round trip: bf16 operand copy, then decay in place --------
     {
-      const bool decays = sgate || gla;
+      const bool decays = sgate || pg;
       for (int c0 = 0; c0 < DK; c0 += 16) {
         float vals[16], cp[16];
         tmem_ld16(tl + kColS + c0, vals);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) cp[e] = gla ? vals[e] * sbm[c0 + e] : vals[e];
+        for (int e = 0; e < 16; ++e) cp[e] = pg ? vals[e] * sbm[c0 + e] : vals[e];
         store_row16_bf16(sm + L.st, 16384, tid, c0, cp);
         if (decays) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) vals[e] *= gla ? sblast[c0 + e] : sdec[0];
+          for (int e = 0; e < 16; ++e) vals[e] *= pg ? sblast[c0 + e] : sdec[0];
           tmem_st16(tl + kColS + c0, vals);
         }
       }
@@ -314,14 +330,15 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
     // ---- MMA group 1: scores, inter-chunk output, (delta) S^T K^T --------
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t a_qk = smem_u32(qk), a_st = smem_u32(sm + L.st);
+      const uint32_t a_qk = smem_u32(qk), a_st = smem_u32(sm + L.st), a_kb = smem_u32(sm + L.kb);
 #pragma unroll
       for (int kk = 0; kk < DK / 16; ++kk) {
         const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
         const uint64_t dq = desc_sw128(a_qk + ko, 16, 1024);          // rows 0..127: [Q; K]
         const uint64_t dk_ = desc_sw128(a_qk + ko + 8192, 16, 1024);  // rows 0..63: K
         const uint64_t ds = desc_sw128(a_st + ko, 16, 1024);          // S^T copy
-        mma_bf16(tbase + kColD1, dq, dk_, id_d1, kk > 0);
+        const uint64_t dkb = kda ? desc_sw128(a_kb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024) : dk_;
+        mma_bf16(tbase + kColD1, dq, dkb, id_d1, kk > 0);
         mma_bf16(tbase + kColO1, ds, dq, id_kk, kk > 0);
         if (delta) mma_bf16(tbase + kColY, ds, dk_, id_kk, kk > 0);
       }
@@ -389,16 +406,32 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int r = r0 + e;
-          y[e] = (v < DV) ? sbeta[r] * (bf16_at(vb, sw128_off(r, v & 63)) - seb[r] * y[e]) : 0.f;
+          const float ey = kda ? 1.f : seb[r];  // KDA: e^{B} is inside (K e^B) S already
+          y[e] = (v < DV) ? sbeta[r] * (bf16_at(vb, sw128_off(r, v & 63)) - ey * y[e]) : 0.f;
         }
         store_row16_bf16(sm + L.z, 16384, v, r0, y);
       }
     }
     tc_fence_before();
     __syncthreads();
+    if (L.ns == 1 && tid == 0 && i + 1 < nchunks) {  // the only stage is consumed: stream the next chunk
+      issue_loads(i + 1, 0);
+      pending[0] = i + 1;
+    }
 
     // ---- K -> Kt in place (state-update operand); elu+1 z and den --------
-    if (sgate || gla) {
+    if (kda) {  // K e^{b_m - B} -> K e^{b_last - B}
+      constexpr int kChunks = kC * DK / 8;
+      for (int ci = tid; ci < kChunks; ci += kThreads) {
+        const int g8 = ci % (DK / 8), r = ci / (DK / 8);
+        uint8_t *ptr = sm + L.kb + (g8 >> 3) * 8192 + sw128_off(r, (g8 & 7) * 8);
+        float f[8];
+        bf16x8_to_f32(*reinterpret_cast<uint4 *>(ptr), f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] *= selm[g8 * 8 + e];
+        *reinterpret_cast<uint4 *>(ptr) = f32_to_bf16x8(f);
+      }
+    } else if (sgate || gla) {
       constexpr int kChunks = kC * DK / 8;
       for (int ci = tid; ci < kChunks; ci += kThreads) {
         const int g8 = ci % (DK / 8), r = ci / (DK / 8);
@@ -513,7 +546,9 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
         const uint64_t du = delta ? desc_sw128(a_u + kk * 32, 16, 1024)
                                   : desc_sw128(a_u + kk * 2048, 8192, 1024);
         mma_bf16(tbase + kColO2, du, desc_sw128(a_p + kk * 32, 16, 1024), id_o2, kk > 0);
-        mma_bf16(tbase + kColS, du, desc_sw128(a_k + kk * 2048, 16384, 1024), id_su, 1);
+        const uint64_t dkt = kda ? desc_sw128(smem_u32(sm + L.kb) + kk * 2048, 8192, 1024)
+                                 : desc_sw128(a_k + kk * 2048, 16384, 1024);
+        mma_bf16(tbase + kColS, du, dkt, id_su, 1);
         if (elu)
           mma_bf16(tbase + kColS, du, desc_sw128(smem_u32(sm + L.klo) + kk * 2048, 8192, 1024),
                    id_su, 1);
@@ -524,7 +559,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
     mma_phase ^= 1;
     if (__syncthreads_or(!ok)) { abort = true; break; }
     tc_fence_after();
-    if (tid == 0 && i + 2 < nchunks) {  // the stage is free: stream chunk i + 2 into it
+    if (L.ns == 2 && tid == 0 && i + 2 < nchunks) {  // the stage is free: stream chunk i + 2 into it
       issue_loads(i + 2, s);
       pending[s] = i + 2;
     }
@@ -543,7 +578,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
           for (int e = 0; e < 16; ++e) {
             const int r = r0 + e;
             if (r < n) {
-              float x = (gla || !sgate) ? a[e] + b[e] : fmaf(seb[r], a[e], b[e]);
+              float x = (pg || !sgate) ? a[e] + b[e] : fmaf(seb[r], a[e], b[e]);
               if (elu) x = x / sden[r];
               o[(size_t)r * DV] = __float2bfloat16_rn(x);
             }
@@ -573,8 +608,8 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
   } else if (tid == 0) {
     atomicOr(p.status, kStatusTimeout);
     // let copies and MMAs already in flight land before the memory goes away
-    for (int s = 0; s < 2; ++s)
-      if (pending[s] >= 0) (void)mbar_wait_bounded(&bar_full[s], (pending[s] >> 1) & 1, kSpin);
+    for (int s = 0; s < L.ns; ++s)
+      if (pending[s] >= 0) (void)mbar_wait_bounded(&bar_full[s], (pending[s] / L.ns) & 1, kSpin);
     (void)mbar_wait_bounded(bar_mma, mma_phase, kSpin);
   }
   tc_fence_before();
@@ -601,7 +636,7 @@ int launch_typed(const ChunkParams &p, cudaStream_t stream) {
                      CU_TENSOR_MAP_SWIZZLE_128B) &&
             make_map(&mv, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DV, p.T, BH, 64,
                      CU_TENSOR_MAP_SWIZZLE_128B);
-  if (ok && p.kind == kGla)
+  if (ok && (p.kind == kGla || p.kind == kKda))
     ok = make_map(&mg, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, DK, p.T, BH, DK,
                   CU_TENSOR_MAP_SWIZZLE_NONE);
   else
@@ -633,6 +668,12 @@ int launch_chunk_tc(const ChunkParams &p, cudaStream_t stream) {
   if (!encode_fn()) {
     set_error("la_chunk_fwd: cuTensorMapEncodeTiled is unavailable");
     return LA_ERR_CUDA;
+  }
+  if (p.kind == kKda) {  // Kimi Delta Attention: the sequential-phase kernel, one stage
+    if (p.dk == 128 && p.dv == 128) return launch_typed<128, 128>(p, stream);
+    if (p.dk == 128 && p.dv == 64) return launch_typed<128, 64>(p, stream);
+    if (p.dk == 64 && p.dv == 128) return launch_typed<64, 128>(p, stream);
+    return launch_typed<64, 64>(p, stream);
   }
   if (p.kind != kGdn) return launch_chunk_ws(p, stream);
   if (p.dk == 128 && p.dv == 128) {

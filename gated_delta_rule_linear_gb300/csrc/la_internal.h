@@ -16,6 +16,7 @@ enum Kind : int {
   kGla = LA_GLA,
   kScalar = LA_SCALAR_GATE,
   kGdn = LA_GDN,
+  kKda = LA_KDA,
 };
 
 // Bits of the device status word (one per device, see la_status.cu).

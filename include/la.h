@@ -82,6 +82,15 @@ typedef struct CUstream_st *la_stream_t;
  * Attention" section 6.2). g = float32 [B][H][T] or NULL (alpha = 1, plain
  * DeltaNet); beta = float32 [B][H][T] or NULL (beta = 1). */
 #define LA_GDN           5
+/* Kimi Delta Attention: Gated DeltaNet with a per-key-channel gate,
+ * S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ * ("LLM attention optimisation", Kimi Delta Attention section; Diag(alpha_t)
+ * acts on the key axis). g = float32 [B][H][T][dk] (per step [B][H][dk]),
+ * 16-byte aligned; beta = float32 [B][H][T] or NULL (beta = 1). bfloat16
+ * inputs only in la_chunk_fwd (LA_F32 is LA_ERR_UNSUPPORTED); chunked
+ * evaluation folds exp(b_r - b_s) per channel around the chunk midpoint as
+ * for LA_GLA, with the same range limit. */
+#define LA_KDA           6
 /* Flag: q, k, v and o are float32 instead of bfloat16. */
 #define LA_F32           0x100
 

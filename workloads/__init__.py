@@ -27,7 +27,7 @@ __all__ = ["Workload", "WORKLOADS", "make_inputs", "MODES"]
 
 # Mode names used throughout the Python side. The C ABI has its own enum;
 # the binding maps these names onto it.
-MODES = ("linear", "elu1", "retnet", "gla", "scalar", "gdn")
+MODES = ("linear", "elu1", "retnet", "gla", "scalar", "gdn", "kda")
 
 
 @dataclass(frozen=True)
@@ -74,6 +74,11 @@ WORKLOADS = {
     # Not one of the five headline workloads; used by parity tests only.
     "scalar": Workload("scalar", "scalar", 2, 4, 1024, 128, 128, "bf16", 64, seed=6,
                        qkv_scale=1.0 / math.sqrt(128.0), s0=True),
+    # Kimi Delta Attention (Gated DeltaNet with a per-key-channel gate): the Gated
+    # DeltaNet shape and q/k/beta recipe with the GLA gate distribution per channel.
+    # The next row after the headline workloads; parity tests and its own bench line.
+    "kda": Workload("kda", "kda", 4, 16, 16384, 128, 128, "bf16", 64, seed=7,
+                    l2norm_qk=True, s0=True),
 }
 
 
@@ -121,6 +126,9 @@ def make_inputs(wl: Workload | str, **sizes) -> dict:
         g = -F.softplus(_normal(gen, (B, H, T))) / 8.0
         beta = torch.sigmoid(_normal(gen, (B, H, T)))
         # draw order is q,k,v,g,beta,S0: g above is drawn before beta
+    elif wl.mode == "kda":
+        g = F.logsigmoid(_normal(gen, (B, H, T, dk))) / 16.0
+        beta = torch.sigmoid(_normal(gen, (B, H, T)))
     S0 = None
     if wl.s0:
         width = dv + 1 if wl.mode == "elu1" else dv
