@@ -81,6 +81,9 @@ def _call(**kw):
     (dict(mode=4), "LA_ERR_INVALID_ARG"),             # scalar needs g
     (dict(mode=2, g=A, beta=A), "LA_ERR_INVALID_ARG"),  # beta only for gdn
     (dict(mode=1, g=A), "LA_ERR_INVALID_ARG"),        # elu1 takes no gates
+    (dict(mode=6), "LA_ERR_INVALID_ARG"),             # kda needs per-channel g
+    (dict(mode=6, g=A + 4), "LA_ERR_INVALID_ARG"),    # kda g must be 16-byte aligned
+    (dict(mode=7), "LA_ERR_INVALID_ARG"),             # no mode 7
     (dict(S0=A + 1), "LA_ERR_INVALID_ARG"),
 ])
 def test_chunk_fwd_rejects_bad_arguments(lib, kw, code):
