@@ -511,20 +511,7 @@ chunk_delta_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q
       if (!group_all(okp, kBarKG)) break;
       if (kg == 0) mbar_arrive(d1_free);
       // ---- T = (I + A)^-1: 16x16 diagonal blocks, then three block levels
-      if (kg < kC) {
-        const int blk = kg >> 4, jc = kg & 15, base = blk * 16;
-        float x[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          float acc = (r == jc) ? 1.f : 0.f;
-#pragma unroll
-          for (int m = 0; m < r; ++m)
-            if (m >= jc) acc = fmaf(-Af[(base + r) * kAp + base + m], x[m], acc);
-          x[r] = (r < jc) ? 0.f : acc;
-        }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) Tf[(base + r) * kAp + base + jc] = round_tf32(x[r]);
-      }
+      if (kg < kC) diag_inverse_16(Af, Tf, kg >> 4, kg & 15);
       group_sync(kBarKG);
       // off-diagonal blocks level by level: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj,
       // one warp per 16x16 output block (tf32 warp MMAs)

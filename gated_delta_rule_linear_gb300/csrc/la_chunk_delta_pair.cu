@@ -18,9 +18,11 @@
 //     memory with one bulk copy each (cluster address space, completion on
 //     the receiver's mbarrier). Each key group therefore solves every other
 //     chunk.
-// The bf16 copy of S^T and the bf16 U^T are A operands taken from tensor
-// memory (packed pairs along K), which keeps shared memory for the exchange
-// buffers. Value rows 64..127 of the 128-row operands are zero.
+// The bf16 copy of S^T, the bf16 U^T and the key side's bf16 K^T are A
+// operands taken from tensor memory (packed pairs along K), which keeps shared
+// memory for the exchange buffers; the K^T copy frees the key side's [Q; K]
+// buffer for the next own chunk as soon as the scores MMA has read it. Value
+// rows 64..127 of the 128-row operands are zero.
 //
 // Roles (384 threads per CTA): warp 0 producer (TMA tiles, gate/beta prefix),
 // warp 1 key-side MMAs (D1, W) for this CTA's chunks, warp 2 state-side MMAs
@@ -47,8 +49,8 @@ constexpr int kNM = 3;                      // per-chunk scalar slots of the sta
 constexpr uint32_t kTmemCols = 512;
 // S fp32 (128), S^T bf16 copy (64 packed), D1 (64), W^T (64), U^T (64; the U
 // epilogue packs U^T into its first 32 columns and U^T Diag(e^{b_last - b})
-// into the other 32), O (2 x 64)
-constexpr uint32_t kColS = 0, kColSC = 128, kColD1 = 192, kColW = 256, kColU = 320, kColO = 384;
+// into the other 32), O (64), K^T of the key side's chunk (32 packed)
+constexpr uint32_t kColS = 0, kColSC = 128, kColD1 = 192, kColW = 256, kColU = 320, kColO = 384, kColKT = 448;
 constexpr int kSG = 128, kKG = 256;
 constexpr int kBarSG = 1, kBarKG = 2;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -108,7 +110,7 @@ chunk_delta_pair_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap
   uint64_t *d1_full = bars + 8, *d1_free = bars + 9, *t_ready = bars + 10, *w_full = bars + 11;
   uint64_t *kd_full = bars + 12, *kd_free = bars + 14;                               // [2], [2]
   uint64_t *s_ready = bars + 16, *u_full = bars + 17, *u_ready = bars + 18, *s_done = bars + 19;
-  uint64_t *o_done = bars + 20, *o_free = bars + 22, *drain = bars + 24;             // [2] each
+  uint64_t *o_done = bars + 20, *o_free = bars + 21, *kt_free = bars + 22, *drain = bars + 24;  // 1, 1, 1, [2]
   uint64_t *kt_full = bars + 26, *kms_free = bars + 27;                              // 1, [2]
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 30);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -138,10 +140,11 @@ chunk_delta_pair_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap
     for (int b = 0; b < 2; ++b) {
       mbar_init(&kd_full[b], 1);  // own: the key group's arrive; other: arm + the bulk copies' bytes
       mbar_init(&kd_free[b], 2);  // (own buffer only) both CTAs have consumed the chunk's key data
-      mbar_init(&o_done[b], 1);
-      mbar_init(&o_free[b], 1);
       mbar_init(&drain[b], 1);
     }
+    mbar_init(o_done, 1);
+    mbar_init(o_free, 1);
+    mbar_init(kt_free, 1);  // the key group has its scores and its K^T copy
     mbar_init(s_ready, 1);
     mbar_init(u_full, 1);
     mbar_init(u_ready, 1);
@@ -227,9 +230,10 @@ chunk_delta_pair_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap
         (void)mbar_wait_bounded(&full[j % kNS], (j / kNS) & 1, kSpinLimit);
   } else if (warp == 3) {
     // ------------------------------------------- key producer (own chunks)
-    // [Q; K] of this CTA's next chunk into its own buffer as soon as the
-    // previous one's W MMA has read it, and the key-side scalars, so that the
-    // key side never waits for the state side to recycle a stage.
+    // [Q; K] of this CTA's next chunk into its own buffer as soon as the key
+    // group has the previous one's scores and K^T copy, and the key-side
+    // scalars, so that the key side never waits for the state side to recycle
+    // a stage.
     for (int j = (int)rank, n = 0; j < nchunks; j += 2, ++n) {
       const int t0 = j * kC;
       int ok = 1;
@@ -273,8 +277,8 @@ chunk_delta_pair_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap
         if (lane == 0) ms[kMsFast] = (-bl < kFastLimit) ? 1.f : 0.f;
         __syncwarp();
       }
-      // the buffer is free once the previous own chunk's W MMA has completed
-      if (lane == 0 && n > 0) ok = wait_or_abort(w_full, (n - 1) & 1, abort_flag, p.status);
+      // the buffer is free once the previous own chunk's D1 MMA and K^T copy are done
+      if (lane == 0 && n > 0) ok = wait_or_abort(kt_free, (n - 1) & 1, abort_flag, p.status);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(kt_full, 32768u);
@@ -284,6 +288,14 @@ chunk_delta_pair_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap
           tma_load_3d(sm + L.kt + a * 16384 + 8192, &tm_k, kt_full, 64 * a, t0, bh);
         }
         mbar_arrive(kt_full);
+        // the next own chunk's load waits for this chunk's scores; warm L2 now
+        if (j + 2 < nchunks) {
+#pragma unroll
+          for (int a = 0; a < 2; ++a) {
+            tma_prefetch_3d(&tm_q, 64 * a, t0 + 2 * kC, bh);
+            tma_prefetch_3d(&tm_k, 64 * a, t0 + 2 * kC, bh);
+          }
+        }
       }
     }
     if (lane == 0) {  // no copy in flight when the CTA leaves
@@ -294,11 +306,10 @@ chunk_delta_pair_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap
     // ------------------------------------ key-side MMAs of this CTA's chunks
     if (lane == 0) {
       constexpr uint32_t id_d1 = idesc_bf16_f32(128, 64, false, false);
-      constexpr uint32_t id_w = idesc_bf16_f32(128, 64, true, false);
+      constexpr uint32_t id_w = idesc_bf16_f32(128, 64, false, false);
       const uint32_t a_tpp = smem_u32(sm + L.af), a_qk = smem_u32(sm + L.kt);
-      // D1 = [Q; K] K^T of own chunk j (own index n) once the key group read the previous one
-      auto issue_d1 = [&](int j, int n) -> bool {
-        (void)j;
+      // D1 = [Q; K] K^T of own chunk n once the key group has read the previous one
+      auto issue_d1 = [&](int n) -> bool {
         if (!wait_or_abort(kt_full, n & 1, abort_flag, p.status)) return false;
         if (!wait_or_abort(d1_free, (n & 1) ^ 1, abort_flag, p.status)) return false;
         tc_fence_after();
@@ -311,19 +322,18 @@ chunk_delta_pair_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap
         mma_commit(d1_full);
         return true;
       };
-      const int j0 = (int)rank;
-      bool ok = j0 < nchunks && issue_d1(j0, 0);
-      for (int j = j0, n = 0; j < nchunks && ok; j += 2, ++n) {
-        // W^T = K^T T''^T: K rows as MN-major A (M = dk), T'' K-major
+      const int nown = (nchunks - (int)rank + 1) / 2;
+      bool ok = nown > 0 && issue_d1(0);
+      for (int n = 0; n < nown && ok; ++n) {
+        // the next own chunk's scores, once the key group has consumed these
+        if (n + 1 < nown && !issue_d1(n + 1)) break;
+        // W^T = K^T T''^T: K^T from its TMEM copy (M = dk), T'' K-major
         if (!wait_or_abort(t_ready, n & 1, abort_flag, p.status)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)
-          mma_bf16(tbase + kColW, desc_sw128(a_qk + 8192 + kk * 2048, 16384, 1024),
-                   desc_sw128(a_tpp + kk * 32, 16, 1024), id_w, kk > 0);
+          mma_bf16_ts(tbase + kColW, tbase + kColKT + kk * 8, desc_sw128(a_tpp + kk * 32, 16, 1024), id_w, kk > 0);
         mma_commit(w_full);
-        // the next own chunk's [Q; K] replaces this one's once this W has read it
-        if (j + 2 < nchunks && !issue_d1(j + 2, n + 1)) break;
       }
       mma_commit(&drain[0]);
       (void)mbar_wait_bounded(&drain[0], 0, kSpinLimit);
@@ -341,12 +351,11 @@ chunk_delta_pair_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap
         const int s = i % kNS, b = i & 1;
         if (!wait_or_abort_cluster(&kd_full[b], (i >> 1) & 1, abort_flag, p.status)) break;
         if (!wait_or_abort(s_ready, i & 1, abort_flag, p.status)) break;
-        if (!wait_or_abort(&o_free[i & 1], ((i >> 1) & 1) ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
         uint8_t *st = stage(s);
         const uint32_t a_v = smem_u32(st + L.v), a_qk = smem_u32(st + L.qk);
         const uint32_t a_tp = smem_u32(tpbuf(b)), a_wn = smem_u32(wnbuf(b)), a_p = smem_u32(pbuf(b));
-        const uint32_t d_o = tbase + kColO + (uint32_t)(i & 1) * 64u;
+        const uint32_t d_o = tbase + kColO;
         // V^T (value rows 64..127 from the zero atom: LBO spans the two MN blocks)
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)
@@ -356,6 +365,9 @@ chunk_delta_pair_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap
         for (int kk = 0; kk < DK / 16; ++kk)
           mma_bf16_ts(tbase + kColU, tbase + kColSC + kk * 8, desc_sw128(a_wn + kk * 2048, 8192, 1024), id_us, 1);
         mma_commit(u_full);
+        // O is single-buffered: the previous chunk's output epilogue runs during this U
+        if (i > 0 && !wait_or_abort(o_free, (i - 1) & 1, abort_flag, p.status)) break;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < DK / 16; ++kk) {
           const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -372,7 +384,7 @@ chunk_delta_pair_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap
           mma_bf16_ts(tbase + kColS, tbase + kColU + 32 + kk * 8,
                       desc_sw128(a_qk + 8192 + kk * 2048, 16384, 1024), id_su, 1);
         mma_commit(s_done);
-        mma_commit(&o_done[i & 1]);
+        mma_commit(o_done);
         mma_commit(&empty[s]);
       }
       mma_commit(&drain[1]);
@@ -443,17 +455,25 @@ chunk_delta_pair_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap
         if (live) {
           const float dec = ms[kSsDec];
 #pragma unroll 1
-          for (int c0 = 0; c0 < DK; c0 += 32) {
-            float x[32], pk[16];
+          for (int c0 = 0; c0 < DK; c0 += 64) {
+            float x[32], y[32], pk[16];
             tmem_ld32(tl + kColS + c0, x);
+            tmem_ld32(tl + kColS + c0 + 32, y);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 16; ++e) pk[e] = __uint_as_float(pack_bf16(x[2 * e], x[2 * e + 1]));
             tmem_st16(tl + kColSC + c0 / 2, pk);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) pk[e] = __uint_as_float(pack_bf16(y[2 * e], y[2 * e + 1]));
+            tmem_st16(tl + kColSC + c0 / 2 + 16, pk);
             if (gated) {
 #pragma unroll
-              for (int e = 0; e < 32; ++e) x[e] *= dec;
+              for (int e = 0; e < 32; ++e) {
+                x[e] *= dec;
+                y[e] *= dec;
+              }
               tmem_st32(tl + kColS + c0, x);
+              tmem_st32(tl + kColS + c0 + 32, y);
             }
           }
           tmem_wait_st();
@@ -462,8 +482,44 @@ chunk_delta_pair_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap
         tc_fence_before();
         group_sync(kBarSG);
         if (v == 0) mbar_arrive(s_ready);
+      }
+      if (i > 0) {
+        // output epilogue of chunk c = i - 1: its MMAs completed before this chunk's round
+        // trip, and it fills the wait for this chunk's U MMA
+        const int c = i - 1, n = min(kC, T - c * kC);
+        bool ok = wait_or_abort(o_done, c & 1, abort_flag, p.status);
+        if (!group_all(ok, kBarSG)) { alive = false; break; }
+        tc_fence_after();
+        if (live) {
+          __nv_bfloat16 *og =
+              static_cast<__nv_bfloat16 *>(p.o) + ((size_t)bh * T + (size_t)c * kC) * DV + v_base;
+          const bool odd = lane & 1;
+#pragma unroll 1
+          for (int r0 = 0; r0 < kC; r0 += 16) {
+            float a[16];
+            tmem_ld16(tl + kColO + r0, a);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+              const float send = odd ? a[e] : a[e + 1];
+              const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+              const int r = r0 + e + (odd ? 1 : 0);
+              const int col = v - (odd ? 1 : 0);
+              const uint32_t w = odd ? pack_bf16(recv, a[e + 1]) : pack_bf16(a[e], recv);
+              if (r < n) *reinterpret_cast<uint32_t *>(og + (size_t)r * DV + col) = w;
+            }
+          }
+        }
+        tc_fence_before();
+        group_sync(kBarSG);
+        if (v == 0) {
+          mbar_arrive(o_free);
+          mbar_arrive(&mfree[c % kNM]);
+        }
+      }
+      if (i < nchunks) {
         // U epilogue: U^T (fp32) -> bf16 pairs in place, the A operand of the O and state MMAs
-        ok = wait_or_abort(u_full, i & 1, abort_flag, p.status);
+        bool ok = wait_or_abort(u_full, i & 1, abort_flag, p.status);
         if (!group_all(ok, kBarSG)) { alive = false; break; }
         tc_fence_after();
         if (live) {
@@ -493,39 +549,6 @@ chunk_delta_pair_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap
         group_sync(kBarSG);
         if (v == 0) mbar_arrive(u_ready);
       }
-      if (i > 0) {
-        // output epilogue of chunk c = i - 1 (overlaps the state update of chunk i)
-        const int c = i - 1, ob = c & 1, n = min(kC, T - c * kC);
-        bool ok = wait_or_abort(&o_done[ob], (c >> 1) & 1, abort_flag, p.status);
-        if (!group_all(ok, kBarSG)) { alive = false; break; }
-        tc_fence_after();
-        if (live) {
-          __nv_bfloat16 *og =
-              static_cast<__nv_bfloat16 *>(p.o) + ((size_t)bh * T + (size_t)c * kC) * DV + v_base;
-          const bool odd = lane & 1;
-#pragma unroll 1
-          for (int r0 = 0; r0 < kC; r0 += 16) {
-            float a[16];
-            tmem_ld16(tl + kColO + ob * 64 + r0, a);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-              const float send = odd ? a[e] : a[e + 1];
-              const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-              const int r = r0 + e + (odd ? 1 : 0);
-              const int col = v - (odd ? 1 : 0);
-              const uint32_t w = odd ? pack_bf16(recv, a[e + 1]) : pack_bf16(a[e], recv);
-              if (r < n) *reinterpret_cast<uint32_t *>(og + (size_t)r * DV + col) = w;
-            }
-          }
-        }
-        tc_fence_before();
-        group_sync(kBarSG);
-        if (v == 0) {
-          mbar_arrive(&o_free[ob]);
-          mbar_arrive(&mfree[c % kNM]);
-        }
-      }
     }
     if (alive && p.S_final) {
       bool ok = wait_or_abort(s_done, (nchunks - 1) & 1, abort_flag, p.status);
@@ -545,6 +568,22 @@ chunk_delta_pair_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap
     const int kg = tid - kKG;
     const int b = (int)rank;
     uint8_t *pb = pbuf(b), *tpb = tpbuf(b), *wnb = wnbuf(b);
+    // K^T of the own chunk into TMEM (lane = key channel kg, packed token pairs), the A
+    // operand of the W MMA, so that the [Q; K] buffer can take the next own chunk
+    auto kt_copy = [&]() {
+      const uint8_t *kb = sm + L.kt + (uint32_t)(kg >> 6) * 16384u + 8192u;
+      const uint32_t c = (uint32_t)kg & 63u;
+      float pk[32];
+#pragma unroll
+      for (int r2 = 0; r2 < 32; ++r2) {
+        const uint32_t lo = *reinterpret_cast<const uint16_t *>(kb + sw128_off(2 * r2, c));
+        const uint32_t hi = *reinterpret_cast<const uint16_t *>(kb + sw128_off(2 * r2 + 1, c));
+        pk[r2] = __uint_as_float(lo | (hi << 16));
+      }
+      tmem_st32(tl + kColKT, pk);
+      tmem_wait_st();
+      tc_fence_before();
+    };
     for (int j = (int)rank, n = 0; j < nchunks; j += 2, ++n) {
       const int nrow = min(kC, T - j * kC);
       float *ms = kslot(n);
@@ -554,7 +593,9 @@ chunk_delta_pair_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap
       if (!group_all(ok, kBarKG)) break;
       tc_fence_after();
       const bool fast = ms[kMsFast] != 0.f;
-      // ---- A from D1 lanes 64..127 (K K^T rows): only private buffers until the solve is done
+      // ---- A from D1 lanes 64..127 (K K^T rows) by warps 10-11: only private buffers until
+      // the solve is done; warps 8-9 copy their half of K^T meanwhile, warps 10-11 after
+      if (kg < kC) kt_copy();
       if (kg >= kC) {
         const int r = kg - kC;
         const float b2r = ms[kMsB2 + r], ar = ms[kMsAR + r], br = ms[kMsBeta + r];
@@ -579,23 +620,12 @@ chunk_delta_pair_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap
             *reinterpret_cast<float4 *>(Af + r * kAp + s0 + 4 * q) =
                 make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
         }
+        kt_copy();
       }
       group_sync(kBarKG);
+      if (kg == 0) mbar_arrive(kt_free);  // the D1 MMA and the K^T copy are done with [Q; K]
       // ---- T = (I + A)^-1: 16x16 diagonal blocks, then three block levels
-      if (kg < kC) {
-        const int blk = kg >> 4, jc = kg & 15, base = blk * 16;
-        float x[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          float acc = (r == jc) ? 1.f : 0.f;
-#pragma unroll
-          for (int m = 0; m < r; ++m)
-            if (m >= jc) acc = fmaf(-Af[(base + r) * kAp + base + m], x[m], acc);
-          x[r] = (r < jc) ? 0.f : acc;
-        }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) Tf[(base + r) * kAp + base + jc] = round_tf32(x[r]);
-      }
+      if (kg < kC) diag_inverse_16(Af, Tf, kg >> 4, kg & 15);
       group_sync(kBarKG);
       {
         const int kw = kg >> 5;

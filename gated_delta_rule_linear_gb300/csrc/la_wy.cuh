@@ -43,6 +43,38 @@ __device__ __forceinline__ void block_mma_16(float (&acc)[2][4], const float *Ab
     }
   }
 }
+// Column jc of the inverse of the unit lower-triangular 16x16 block I + A_bb
+// (blk = b, strictly lower part of A in shared memory with pitch kAp, zeros
+// elsewhere) by forward substitution in column (saxpy) order: once x_m is
+// final it updates every later row at once, so the dependent chain is 16
+// FMAs long instead of 120, and A is read as 16-byte row pieces. The FMAs
+// per row run in the same order as in the row-by-row form (rows before jc
+// contribute exact zeros). Writes the column, rounded to tf32, into T.
+__device__ __forceinline__ void diag_inverse_16(const float *Af, float *Tf, int blk, int jc) {
+  const int base = blk * 16;
+  float acc[16];
+#pragma unroll
+  for (int r = 0; r < 16; ++r) acc[r] = (r == jc) ? 1.f : 0.f;
+#pragma unroll
+  for (int g4 = 0; g4 < 4; ++g4) {
+    float4 a4[16];
+#pragma unroll
+    for (int r = 4 * g4 + 1; r < 16; ++r)
+      a4[r] = *reinterpret_cast<const float4 *>(Af + (base + r) * kAp + base + 4 * g4);
+#pragma unroll
+    for (int mm = 0; mm < 4; ++mm) {
+      const int m = 4 * g4 + mm;
+      const float xm = acc[m];  // final: rows above m are done
+#pragma unroll
+      for (int r = m + 1; r < 16; ++r) {
+        const float am = mm == 0 ? a4[r].x : mm == 1 ? a4[r].y : mm == 2 ? a4[r].z : a4[r].w;
+        acc[r] = fmaf(-am, xm, acc[r]);
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 16; ++r) Tf[(base + r) * kAp + base + jc] = round_tf32(acc[r]);
+}
 // Store a 16x16 accumulator (scaled by sgn, rounded to tf32) into a block of pitch kAp.
 __device__ __forceinline__ void block_store_16(float *Cb, const float (&acc)[2][4], float sgn, int lane) {
   const int g = lane >> 2, t = lane & 3;
