@@ -12,7 +12,10 @@
 //
 // GLA factors the per-channel exp(b_r - b_s) around the chunk midpoint m:
 // Q and K are scaled by e^{b - b_m} and e^{b_m - b}, the bf16 state copy by
-// e^{b_m}. elu+1 applies phi to q and k, splits phi(k) into bf16 high and low
+// e^{b_m}. The state update then uses the same K (e^{b_m - b}), so TMEM holds
+// X = S Diag(e^{b_m - b_last}) of the previous chunk: one per-channel factor
+// e^{b_m} e^{b_last' - b_m'} (this chunk's midpoint, the previous chunk's
+// midpoint-to-end decay) gives both the bf16 copy and the decayed state. elu+1 applies phi to q and k, splits phi(k) into bf16 high and low
 // halves for the state update, and divides o by q.z + P 1 (kernel-attention
 // notes, sections 13-14).
 //
@@ -53,8 +56,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 // per-stage scalars (floats): log2-domain gate prefix b2, e^{b}, elu+1
 // denominators, chunk decay, fast-path flag, per-row factors e^{b - b_last}
 // (scores) and e^{b_last - b} (value or key rows), GLA per-channel factors
+// (state factor e^{b_m} e^{b_last' - b_m'}, midpoint-to-end decay e^{b_last - b_m})
 constexpr int kMsB2 = 0, kMsEB = 64, kMsDen = 128, kMsDec = 192, kMsB2L = 193, kMsFast = 194,
-              kMsF = 256, kMsVS = 320, kMsBM = 384, kMsBL = 512, kMsLM = 640;
+              kMsF = 256, kMsVS = 320, kMsBM = 384, kMsLM = 640;
 // bytes of one scalar slot: the GLA per-channel factors need the upper part
 __host__ __device__ constexpr uint32_t ms_bytes(int kind) { return kind == kGla ? 3072u : 1536u; }
 // GLA's 32 KB gate tiles leave no room for an output staging tile: it stores o directly
@@ -345,15 +349,12 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
           float x[32];
           tmem_ld32(tl + kColS + c0, x);
           tmem_wait_ld();
-          if (gla) {
-            float cp[32], fm[32], fl[32];
+          if (gla) {  // one factor: the bf16 copy is the decayed state
+            float fm[32];
             load32(ms + kMsBM + c0, fm);
-            load32(ms + kMsBL + c0, fl);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) cp[e] = x[e] * fm[e];
-            store_row32_bf16(sm + L.st, 16384, v, c0, cp);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) x[e] *= fl[e];
+            for (int e = 0; e < 32; ++e) x[e] *= fm[e];
+            store_row32_bf16(sm + L.st, 16384, v, c0, x);
             tmem_st32(tl + kColS + c0, x);
           } else {
             store_row32_bf16(sm + L.st, 16384, v, c0, x);
@@ -442,6 +443,12 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
           float x[32];
           tmem_ld32(tl + kColS + c0, x);
           tmem_wait_ld();
+          if (gla) {  // the last chunk's midpoint-to-end decay
+            float fl[32];
+            load32(mslot(nchunks - 1) + kMsLM + c0, fl);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[e] *= fl[e];
+          }
           if (v < DV) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) p.S_final[((size_t)bh * DK + c0 + e) * Wmem + v] = x[e];
@@ -453,6 +460,7 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
     // -------------------------------------------------------------- key group
     const int kg = tid - kKG;
     if (elu && kg < DK) zs[kg] = p.S0 ? p.S0[((size_t)bh * DK + kg) * Wmem + DV] : 0.f;
+    float lm_prev = 1.f;  // GLA: the previous chunk's e^{b_last - b_m} of channel kg
     for (int j = 0; j < nchunks; ++j) {
       const int s = j % ns, n = min(kC, T - j * kC);
       uint8_t *st = stage(s);
@@ -463,17 +471,19 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
       if (!group_all(ok, kBarKG)) break;
       // ---- inclusive log-gate prefix
       if (gla) {
-        if (kg < DK) {  // channel kg: all 64 loads first, then the scan in registers
+        if (kg < DK) {  // channel kg: all 64 loads first, then the scan (log2 units) in registers
           float b[kC];
 #pragma unroll
           for (int r = 0; r < kC; ++r) b[r] = gt[r * DK + kg];
+          b[0] *= kLog2e;
 #pragma unroll
-          for (int r = 1; r < kC; ++r) b[r] += b[r - 1];
+          for (int r = 1; r < kC; ++r) b[r] = fmaf(b[r], kLog2e, b[r - 1]);
 #pragma unroll
           for (int r = 0; r < kC; ++r) gt[r * DK + kg] = b[r];
-          ms[kMsBM + kg] = __expf(b[kMid]);
-          ms[kMsBL + kg] = __expf(b[kC - 1]);
-          ms[kMsLM + kg] = __expf(b[kC - 1] - b[kMid]);
+          const float lm = ex2(b[kC - 1] - b[kMid]);
+          ms[kMsBM + kg] = ex2(b[kMid]) * lm_prev;
+          ms[kMsLM + kg] = lm;
+          lm_prev = lm;
         }
         group_sync(kBarKG);
         // Q e^{b - b_mid}, K e^{b_mid - b} in place: thread kg owns 8-channel
@@ -500,9 +510,9 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
           unpack8(*pk, fk);
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const float d = bv[e] - bm[e];
-            fq[e] *= __expf(d);
-            fk[e] *= __expf(-d);
+            const float d = bv[e] - bm[e];  // log2 units
+            fq[e] *= ex2(d);
+            fk[e] *= ex2(-d);
           }
           *pq = pack8(fq);
           *pk = pack8(fk);
@@ -609,25 +619,18 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
               *ptr = pack8(f);
             }
           }
-        } else if (sgate || gla) {
+        } else if (sgate) {
           if (cg < DK / 8) {
-            float lm[8];
-            if (gla) {
-              const float4 *lp = reinterpret_cast<const float4 *>(ms + kMsLM + cg * 8);
-              const float4 l0 = lp[0], l1 = lp[1];
-              lm[0] = l0.x; lm[1] = l0.y; lm[2] = l0.z; lm[3] = l0.w;
-              lm[4] = l1.x; lm[5] = l1.y; lm[6] = l1.z; lm[7] = l1.w;
-            }
             uint8_t *base = qk + 8192 + (cg >> 3) * 16384;
 #pragma unroll 2
             for (int m = 0; m < 8; ++m) {
               const int r = r0 + 8 * m;
-              const float rs = sgate ? ms[kMsVS + r] : 1.f;
+              const float rs = ms[kMsVS + r];
               uint4 *ptr = reinterpret_cast<uint4 *>(base + sw128_off(r, (cg & 7) * 8));
               float f[8];
               unpack8(*ptr, f);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) f[e] *= gla ? lm[e] : rs;
+              for (int e = 0; e < 8; ++e) f[e] *= rs;
               *ptr = pack8(f);
             }
           }

@@ -283,6 +283,14 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
       : "memory");
 }
 
+// 2^x on the special-function unit (PTX ex2.approx.ftz.f32: relative error
+// about 2^-22, subnormal results flushed to zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Byte offset of bf16 element (row, col) inside a 128-byte-swizzled tile
 // whose rows are 64 elements (128 B) long; row groups of 8 rows span 1024 B.
 __host__ __device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t col) {
