@@ -45,7 +45,8 @@ KERNEL_SOURCES = ["gated_delta_rule_linear_gb300/csrc/la_chunk_delta.cu",
                   "gated_delta_rule_linear_gb300/csrc/la_chunk_ws.cu",
                   "gated_delta_rule_linear_gb300/csrc/la_chunk_mat.cu",
                   "gated_delta_rule_linear_gb300/csrc/la_tc_common.cuh",
-                  "gated_delta_rule_linear_gb300/csrc/la_sm100.cuh"]
+                  "gated_delta_rule_linear_gb300/csrc/la_sm100.cuh",
+                  "gated_delta_rule_linear_gb300/csrc/la_prologue.cu"]
 
 
 def uses_materialised(wl, variant=None, sm_count=152) -> bool:
@@ -238,7 +239,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="gdn", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default="gdn",
+                    choices=sorted(workloads.WORKLOADS) + sorted(workloads.PROLOGUE_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -256,6 +258,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.workload in workloads.PROLOGUE_WORKLOADS:
+        return bench_prologue(args, rank, world, local_rank)
     wl = workloads.WORKLOADS[args.workload]
     over = {k: getattr(args, k) for k in ("B", "H", "T") if getattr(args, k) is not None}
     if over:
@@ -465,6 +469,200 @@ def run_reference(args, wl, rank, world):
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- prologue
+
+PRO_METRIC = "tokens/sec of the prologue (short conv + L2 norm + gate/beta activations) at 1 GB300; % of roofline"
+
+
+def prologue_bytes(wl) -> float:
+    """Minimum HBM traffic of one la_prologue call: read the three projections,
+    the gate and beta pre-activations and the weights once, write q, k, v, g
+    and beta once."""
+    B, H, T, dk, dv = wl.B, wl.H, wl.T, wl.dk, wl.dv
+    per_tok = 2 * 2 * (2 * dk + dv)
+    if wl.gate_kind != "none":
+        per_tok += 2 * 4 * wl.gate_width
+    if wl.beta:
+        per_tok += 2 * 4
+    return float(B * H * T * per_tok + H * 4 * wl.K * (2 * dk + dv))
+
+
+def _pro_args(la, d, wl, hist_out=None):
+    flags = (la.CONSTANTS["LA_PRO_L2NORM_Q"] if wl.l2q else 0) | (la.CONSTANTS["LA_PRO_L2NORM_K"] if wl.l2k else 0)
+    return (d["xq"], d["xk"], d["xv"], d["wq"], d["wk"], d["wv"], wl.K, None, hist_out, d.get("a_gate"),
+            la.GATE_KINDS[wl.gate_kind], wl.gate_width, wl.tau, d.get("a_beta"), d["q"], d["k"], d["v"],
+            d.get("g"), d.get("beta"), wl.B, wl.H, wl.T, wl.dk, wl.dv, flags)
+
+
+def time_prologue_oracle(wl, inp, target_s: float = 10.0):
+    """The float64 prologue oracle on this host, on a sample of heads over the
+    full sequence (numpy; it uses the threads numpy's own routines use)."""
+    import numpy as np
+    import oracle.prologue as P
+    f64 = lambda t: None if t is None else t.to(torch.float64).numpy()
+    BH = wl.B * wl.H
+    done, t0, tokens = 0, time.perf_counter(), 0
+    while done < BH and (time.perf_counter() - t0) < target_s:
+        b, h = done // wl.H, done % wl.H
+        sl = lambda t: None if t is None else t[b:b + 1, h:h + 1]
+        P.prologue(f64(sl(inp["xq"])), f64(sl(inp["xk"])), f64(sl(inp["xv"])),
+                   f64(inp["wq"][h:h + 1]), f64(inp["wk"][h:h + 1]), f64(inp["wv"][h:h + 1]),
+                   l2q=wl.l2q, l2k=wl.l2k, a_gate=f64(sl(inp["a_gate"])), gate_kind=wl.gate_kind,
+                   tau=wl.tau, a_beta=f64(sl(inp["a_beta"])), K=wl.K)
+        done += 1
+        tokens += wl.T
+    dt = time.perf_counter() - t0
+    # done head-sequences of T tokens = done/H of the workload's B*T tokens
+    sample = f"{done} of {BH} (batch, head) sequences, full T={wl.T}, float64 numpy"
+    return (tokens / wl.H) / dt, 1, sample, dt
+
+
+def bench_prologue(args, rank, world, local_rank):
+    wl = workloads.PROLOGUE_WORKLOADS[args.workload]
+    over = {k: getattr(args, k) for k in ("B", "H", "T") if getattr(args, k) is not None}
+    if over:
+        wl = wl.with_sizes(**over)
+    B, H, T = wl.B, wl.H, wl.T
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        inp = workloads.make_prologue_inputs(wl)
+        vals = []
+        for i in range(args.warmup + args.steps):
+            v, cores, sample, _ = time_prologue_oracle(wl, inp, target_s=3.0)
+            if i >= args.warmup:
+                vals.append(v)
+        value = statistics.mean(vals)
+        print(json.dumps({
+            "impl": "reference", "metric": PRO_METRIC, "value": round(value, 2), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(B * T / value * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; shapes and distributions of the workload)",
+            "config": {"workload": wl.name, "B": B, "H": H, "T": T, "dk": wl.dk, "dv": wl.dv, "K": wl.K,
+                       "global_batch": B, "seq_len": T, "parallelism": "single"},
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }), flush=True)
+        return
+
+    import gated_delta_rule_linear_gb300 as la
+    from gated_delta_rule_linear_gb300 import build as labuild
+    labuild.build()
+    la.load_library()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    inp = workloads.make_prologue_inputs(wl)
+    ins = [n for n in ("xq", "xk", "xv", "wq", "wk", "wv", "a_gate", "a_beta") if inp[n] is not None]
+    d = {n: inp[n].to(dev) for n in ins}
+    d["q"], d["k"], d["v"] = (torch.empty_like(d["xq"]), torch.empty_like(d["xk"]), torch.empty_like(d["xv"]))
+    if "a_gate" in d:
+        d["g"] = torch.empty_like(d["a_gate"])
+    if "a_beta" in d:
+        d["beta"] = torch.empty_like(d["a_beta"])
+    outs = [n for n in ("q", "k", "v", "g", "beta") if n in d]
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def step(dd):
+        rc = la.la_prologue(*_pro_args(la, dd, wl), sh)
+        if rc != 0:
+            raise RuntimeError(la.la_last_error())
+
+    for _ in range(args.warmup):
+        step(d)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[2 * i].record(stream)
+        step(d)
+        ev[2 * i + 1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    launch_ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * B * T * args.steps / (total_ms / 1e3)
+    alg = prologue_bytes(wl)
+    hbm_peak, _, peak_src = read_peaks()
+    achieved = alg / (statistics.mean(launch_ms) / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(achieved / hbm_peak, 4), "traffic": recorded_traffic(wl.name),
+            "peak_source": peak_src, "algorithmic_bytes": alg, "kernel": "prologue_kernel",
+            "launch_ms_mean": round(statistics.mean(launch_ms), 4)}
+
+    e2e = None
+    if not args.no_e2e:
+        host = {n: inp[n].pin_memory() for n in ins}
+        hout = {n: torch.empty_like(d[n], device="cpu").pin_memory() for n in outs}
+        dd = dict(d)
+        h2d = sum(host[n].numel() * host[n].element_size() for n in ins)
+        d2h = sum(hout[n].numel() * hout[n].element_size() for n in outs)
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for n in ins:
+                    dd[n].copy_(host[n], non_blocking=True)
+                step(dd)
+                for n in outs:
+                    hout[n].copy_(dd[n], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        steps = max(3, min(args.steps, 10))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+        e2e = {"value": round(world * B * T * steps / (ms / 1e3), 1), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
+               "ms_per_step": round(ms / steps, 4)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v_cpu, cores, sample, dt = time_prologue_oracle(wl, inp)
+        cpu = {"value": round(v_cpu, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": sample, "seconds": round(dt, 2)}
+    if rank == 0:
+        print(json.dumps({
+            "metric": PRO_METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; shapes and distributions of the workload)",
+            "config": {"workload": wl.name, "B": B, "H": H, "T": T, "dk": wl.dk, "dv": wl.dv, "K": wl.K,
+                       "gate": wl.gate_kind, "gate_width": wl.gate_width, "l2norm_qk": [wl.l2q, wl.l2k],
+                       "global_batch": B * world, "seq_len": T,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (no flush)" if alg > 129e6 else "inputs smaller than L2"},
+            "roofline": roof, "cpu_baseline": cpu, "clocks": clk, "e2e": e2e,
+            "gpu_launches": args.steps,
+        }), flush=True)
+    if dist:
+        dist.destroy_process_group()
 
 
 if __name__ == "__main__":

@@ -44,10 +44,12 @@ MODE_IDS = {
 # Every function the header declares, with its ctypes signature.
 _P = ctypes.c_void_p
 _I = ctypes.c_int
+_F = ctypes.c_float
 SIGNATURES = {
     "la_chunk_fwd": ([_P] * 8 + [_I] * 7 + [_P], _I),
     "la_chunk_fwd_noalloc": ([_P] * 8 + [_I] * 7 + [_P], _I),
     "la_recurrent_step": ([_P] * 7 + [_I] * 5 + [_P], _I),
+    "la_prologue": ([_P] * 6 + [_I] + [_P] * 3 + [_I, _I, _F] + [_P] * 6 + [_I] * 6 + [_P], _I),
     "la_stream_status": ([_P], _I),
     "la_last_error": ([], ctypes.c_char_p),
     "la_version": ([], _I),
@@ -105,6 +107,14 @@ def la_recurrent_step(q, k, v, g, beta, o, S, B, H, dk, dv, mode, stream):
                                             _ptr(o), _ptr(S), B, H, dk, dv, mode, stream)
 
 
+def la_prologue(xq, xk, xv, wq, wk, wv, K, hist_in, hist_out, a_gate, gate_kind, gate_width, tau,
+                a_beta, q, k, v, g, beta, B, H, T, dk, dv, flags, stream):
+    return load_library().la_prologue(_ptr(xq), _ptr(xk), _ptr(xv), _ptr(wq), _ptr(wk), _ptr(wv), K,
+                                      _ptr(hist_in), _ptr(hist_out), _ptr(a_gate), gate_kind,
+                                      gate_width, float(tau), _ptr(a_beta), _ptr(q), _ptr(k), _ptr(v),
+                                      _ptr(g), _ptr(beta), B, H, T, dk, dv, flags, stream)
+
+
 def la_stream_status(stream):
     return load_library().la_stream_status(stream)
 
@@ -160,6 +170,41 @@ def chunk_fwd(q, k, v, mode, g=None, beta=None, S0=None, C=0, with_state=True,
     if rc != 0:
         raise LAError(rc, la_last_error())
     return o, (S_final if with_state else None)
+
+
+GATE_KINDS = {"none": CONSTANTS["LA_GATE_NONE"], "logsigmoid": CONSTANTS["LA_GATE_LOGSIGMOID"],
+              "neg_softplus": CONSTANTS["LA_GATE_NEG_SOFTPLUS"]}
+
+
+def prologue(xq, xk, xv, wq=None, wk=None, wv=None, K=None, hist_in=None, with_hist=False,
+             l2q=False, l2k=False, a_gate=None, gate_kind="none", tau=1.0, a_beta=None, stream=None):
+    """Short convolution, L2 normalisation and gate/beta activations (la_prologue).
+    xq, xk [B,H,T,dk], xv [B,H,T,dv] bf16 CUDA tensors; w* [H,d,K] fp32 or None.
+    Returns a dict with q, k, v, g (or None), beta (or None), hist (or None)."""
+    import torch
+    for name, t in (("xq", xq), ("xk", xk), ("xv", xv), ("wq", wq), ("wk", wk), ("wv", wv),
+                    ("hist_in", hist_in), ("a_gate", a_gate), ("a_beta", a_beta)):
+        _check(t, name)
+    B, H, T, dk = xq.shape
+    dv = xv.shape[-1]
+    if K is None:
+        K = next((w.shape[-1] for w in (wq, wk, wv) if w is not None), 1)
+    kind = GATE_KINDS[gate_kind]
+    dev = xq.device
+    q = torch.empty_like(xq)
+    k = torch.empty_like(xk)
+    v = torch.empty_like(xv)
+    g = torch.empty_like(a_gate) if kind != 0 else None
+    beta = torch.empty_like(a_beta) if a_beta is not None else None
+    hist_out = (torch.empty((B, H, K - 1, 2 * dk + dv), dtype=torch.bfloat16, device=dev)
+                if with_hist and K > 1 else None)
+    width = 1 if a_gate is None or a_gate.dim() == 3 else a_gate.shape[-1]
+    flags = (CONSTANTS["LA_PRO_L2NORM_Q"] if l2q else 0) | (CONSTANTS["LA_PRO_L2NORM_K"] if l2k else 0)
+    rc = la_prologue(xq, xk, xv, wq, wk, wv, K, hist_in, hist_out, a_gate if kind else None, kind,
+                     width, tau, a_beta, q, k, v, g, beta, B, H, T, dk, dv, flags, _stream_handle(stream))
+    if rc != 0:
+        raise LAError(rc, la_last_error())
+    return {"q": q, "k": k, "v": v, "g": g, "beta": beta, "hist": hist_out}
 
 
 def recurrent_step(q, k, v, S, mode, g=None, beta=None, o=None, stream=None):

@@ -150,6 +150,61 @@ int la_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const floa
                          int B, int H, int T, int dk, int dv, int C, int mode, la_stream_t stream);
 
 /*
+ * la_prologue -- the per-token steps that turn the q/k/v/gate/beta
+ * projections into la_chunk_fwd's inputs, in one pass over memory:
+ *
+ *   1. short convolution ("LLM attention optimisation: linear attention",
+ *      DeltaNet section: a depthwise convolution over the last K tokens after
+ *      the projections), on each of q, k and v:
+ *          x~_t[c] = sum_{tau=0}^{K-1} w[h][c][tau] * x_{t-tau}[c]
+ *      Tokens before the first come from hist_in, else are zero.
+ *   2. optional L2 normalisation of q~ and/or k~ per token:
+ *          x / max(||x||_2, 1e-6)   (the pages do not state it; Gated DeltaNet
+ *          is used with L2-normalised q and k)
+ *   3. gate activation of a_gate into natural-log gates g:
+ *          LA_GATE_LOGSIGMOID    g = logsigmoid(a) / tau  (log of
+ *                                sigmoid(.)^(1/tau): "Talk Linear Attention"
+ *                                section 5.1, the GLA gate)
+ *          LA_GATE_NEG_SOFTPLUS  g = -softplus(a) / tau  (alpha in (0, 1))
+ *   4. beta = sigmoid(a_beta).
+ *
+ *   xq, xk  bfloat16 [B][H][T][dk]; xv bfloat16 [B][H][T][dv]; 16-byte aligned
+ *   wq, wk  float32 [H][dk][K], wv float32 [H][dv][K]; w[..][0] weights the
+ *           current token. NULL: no convolution for that tensor (identity).
+ *   K       convolution length, 1..4
+ *   hist_in / hist_out
+ *           bfloat16 [B][H][K-1][2*dk + dv]: per (b, h), the K-1 raw rows
+ *           (before the convolution) preceding this call's first token, oldest
+ *           first, each row the q, k and v projections side by side. hist_out
+ *           receives the last K-1 raw rows of hist_in ++ x, so passing it as
+ *           the next call's hist_in continues the sequence. Either may be NULL
+ *           (zero history / not written); they must not alias. Ignored if K = 1.
+ *   a_gate  float32 [B][H][T] (gate_width 1) or [B][H][T][dk] (gate_width dk);
+ *           gate_kind LA_GATE_NONE: a_gate, g unused (may be NULL)
+ *   tau     finite, > 0
+ *   a_beta  float32 [B][H][T] or NULL (then beta is not written)
+ *   q, k, v outputs, bfloat16, shapes of xq, xk, xv, 16-byte aligned
+ *   g, beta float32 outputs, shapes of a_gate, a_beta
+ *   flags   LA_PRO_L2NORM_Q | LA_PRO_L2NORM_K
+ *
+ * Arithmetic in float32; q, k, v rounded to bfloat16 once. Outputs must not
+ * overlap the inputs. The pages have no single routine for this: it bundles
+ * the steps they place before the recurrence.
+ */
+#define LA_GATE_NONE          0
+#define LA_GATE_LOGSIGMOID    1
+#define LA_GATE_NEG_SOFTPLUS  2
+#define LA_PRO_L2NORM_Q       1
+#define LA_PRO_L2NORM_K       2
+int la_prologue(const void *xq, const void *xk, const void *xv,
+                const float *wq, const float *wk, const float *wv, int K,
+                const void *hist_in, void *hist_out,
+                const float *a_gate, int gate_kind, int gate_width, float tau,
+                const float *a_beta,
+                void *q, void *k, void *v, float *g, float *beta,
+                int B, int H, int T, int dk, int dv, int flags, la_stream_t stream);
+
+/*
  * la_recurrent_step -- one decode step (the recurrent form, "Talk Linear
  * Attention" section 2.1; kernel-attention notes section 14): for every
  * (b, h), apply the mode's update with this token and write o = S^T q

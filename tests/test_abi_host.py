@@ -31,7 +31,7 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     assert names == sorted(["la_chunk_fwd", "la_chunk_fwd_noalloc", "la_recurrent_step",
-                            "la_stream_status", "la_last_error", "la_version"])
+                            "la_prologue", "la_stream_status", "la_last_error", "la_version"])
     assert set(names) == set(la.SIGNATURES)
 
 
@@ -134,3 +134,39 @@ def test_product_does_not_reference_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "la_oracle" not in text, f
+
+
+# ---- la_prologue argument checks (host only) --------------------------------
+
+def _pro(**kw):
+    args = dict(xq=A, xk=A, xv=A, wq=A, wk=A, wv=None, K=4, hist_in=None, hist_out=None,
+                a_gate=A, gate_kind=la.LA_GATE_NEG_SOFTPLUS, gate_width=1, tau=8.0, a_beta=A,
+                q=A, k=A, v=A, g=A, beta=A, B=1, H=1, T=64, dk=128, dv=128, flags=3, stream=None)
+    args.update(kw)
+    rc = la.la_prologue(**args)
+    return rc, la.la_last_error()
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(xq=None), "LA_ERR_INVALID_ARG"),
+    (dict(v=None), "LA_ERR_INVALID_ARG"),
+    (dict(T=0), "LA_ERR_INVALID_ARG"),
+    (dict(B=70000), "LA_ERR_INVALID_ARG"),             # grid y limit on B*H
+    (dict(dk=96), "LA_ERR_UNSUPPORTED"),
+    (dict(K=0), "LA_ERR_INVALID_ARG"),
+    (dict(K=5), "LA_ERR_INVALID_ARG"),
+    (dict(flags=4), "LA_ERR_INVALID_ARG"),
+    (dict(gate_kind=3), "LA_ERR_INVALID_ARG"),
+    (dict(a_gate=None), "LA_ERR_INVALID_ARG"),         # a gate kind without its input
+    (dict(gate_width=64), "LA_ERR_INVALID_ARG"),       # neither 1 nor dk
+    (dict(tau=0.0), "LA_ERR_INVALID_ARG"),
+    (dict(tau=float("nan")), "LA_ERR_INVALID_ARG"),
+    (dict(beta=None), "LA_ERR_INVALID_ARG"),           # a_beta without beta
+    (dict(hist_in=A, hist_out=A), "LA_ERR_INVALID_ARG"),  # aliasing histories
+    (dict(xk=A + 8), "LA_ERR_INVALID_ARG"),            # 16-byte alignment
+    (dict(hist_out=A + 4), "LA_ERR_INVALID_ARG"),
+])
+def test_prologue_rejects_bad_arguments(lib, kw, code):
+    rc, msg = _pro(**kw)
+    assert rc == la.CONSTANTS[code], (rc, msg)
+    assert msg.startswith("la_prologue")

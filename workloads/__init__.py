@@ -23,7 +23,8 @@ from dataclasses import dataclass, field, replace
 import torch
 import torch.nn.functional as F
 
-__all__ = ["Workload", "WORKLOADS", "make_inputs", "MODES"]
+__all__ = ["Workload", "WORKLOADS", "make_inputs", "MODES", "PrologueWorkload", "PROLOGUE_WORKLOADS",
+           "make_prologue_inputs"]
 
 # Mode names used throughout the Python side. The C ABI has its own enum;
 # the binding maps these names onto it.
@@ -145,3 +146,71 @@ def make_inputs(wl: Workload | str, **sizes) -> dict:
         "S0": None if S0 is None else S0.contiguous(),
     }
 
+
+
+# ---------------------------------------------------------------- prologue
+
+@dataclass(frozen=True)
+class PrologueWorkload:
+    """Inputs of the prologue in front of the chunk forward pass: the raw
+    q/k/v projections, depthwise convolution weights, and the gate and beta
+    pre-activations (drawn here; the activations themselves are the method's)."""
+    name: str
+    B: int
+    H: int
+    T: int
+    dk: int
+    dv: int
+    K: int                 # convolution length
+    gate_kind: str         # "none", "logsigmoid" or "neg_softplus"
+    gate_width: int        # 1 (scalar) or dk (per key channel)
+    tau: float
+    l2q: bool
+    l2k: bool
+    beta: bool
+    seed: int
+
+    def with_sizes(self, **kw) -> "PrologueWorkload":
+        return replace(self, **kw)
+
+
+PROLOGUE_WORKLOADS = {
+    # The Gated DeltaNet shape: K = 4 convolution on q, k and v, L2-normalised
+    # q and k, alpha = exp(-softplus(a)/8), beta = sigmoid(a_beta).
+    "prologue": PrologueWorkload("prologue", 4, 16, 16384, 128, 128, 4, "neg_softplus", 1, 8.0,
+                                 True, True, True, seed=11),
+    # The GLA/KDA gate form: per-channel logsigmoid(a)/16, no beta.
+    "prologue_gla": PrologueWorkload("prologue_gla", 2, 8, 4096, 128, 128, 4, "logsigmoid", 128, 16.0,
+                                     False, False, False, seed=12),
+}
+
+
+def make_prologue_inputs(wl: PrologueWorkload | str, hist: bool = False, **sizes) -> dict:
+    """Draw one prologue workload's inputs on the CPU, in the order xq, xk, xv,
+    wq, wk, wv, a_gate, a_beta, history: projections N(0, 1) cast to bf16,
+    weights N(0, 1/K) float32 [H, d, K], pre-activations N(0, 1) float32, and
+    (hist=True) a random bf16 history [B, H, K-1, 2 dk + dv]."""
+    if isinstance(wl, str):
+        wl = PROLOGUE_WORKLOADS[wl]
+    if sizes:
+        wl = wl.with_sizes(**sizes)
+    B, H, T, dk, dv, K = wl.B, wl.H, wl.T, wl.dk, wl.dv, wl.K
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(wl.seed)
+    xq = _normal(gen, (B, H, T, dk)).to(torch.bfloat16).contiguous()
+    xk = _normal(gen, (B, H, T, dk)).to(torch.bfloat16).contiguous()
+    xv = _normal(gen, (B, H, T, dv)).to(torch.bfloat16).contiguous()
+    ws = 1.0 / math.sqrt(K)
+    wq = _normal(gen, (H, dk, K), ws).contiguous()
+    wk = _normal(gen, (H, dk, K), ws).contiguous()
+    wv = _normal(gen, (H, dv, K), ws).contiguous()
+    a_gate = None
+    if wl.gate_kind != "none":
+        shape = (B, H, T) if wl.gate_width == 1 else (B, H, T, wl.gate_width)
+        a_gate = _normal(gen, shape).contiguous()
+    a_beta = _normal(gen, (B, H, T)).contiguous() if wl.beta else None
+    h = None
+    if hist and K > 1:
+        h = _normal(gen, (B, H, K - 1, 2 * dk + dv)).to(torch.bfloat16).contiguous()
+    return {"wl": wl, "xq": xq, "xk": xk, "xv": xv, "wq": wq, "wk": wk, "wv": wv,
+            "a_gate": a_gate, "a_beta": a_beta, "hist": h}
