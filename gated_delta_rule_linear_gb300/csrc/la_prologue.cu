@@ -52,6 +52,8 @@ struct ProParams {
 };
 
 __host__ __device__ constexpr uint32_t tile_bytes(int d) { return (uint32_t)(kTile + kHalo) * d * 2u; }
+// the head's convolution weights in shared memory, [tensor][channel][tap], taps padded to kMaxK
+__host__ __device__ constexpr uint32_t wts_bytes(int dk, int dv) { return (uint32_t)(2 * dk + dv) * kMaxK * 4u; }
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float *f) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -86,23 +88,24 @@ __device__ __forceinline__ void issue_tile(const ProParams &p, int which, int bh
 
 // One tensor of one tile from shared memory: convolution, optional L2 norm, store.
 template <int D>
-__device__ __forceinline__ void conv_tile(const ProParams &p, int which, int bh, int t0, const uint8_t *tile) {
+__device__ __forceinline__ void conv_tile(const ProParams &p, int which, int bh, int t0, const uint8_t *tile,
+                                          const float *wsm) {
   constexpr int G = D / 8;         // 16-byte channel groups per row
   constexpr int S = kThreads / G;  // row streams
   constexpr int R = kTile / S;     // consecutive rows per stream
   const int tid = threadIdx.x, cg = tid % G, st = tid / G, lane = tid & 31;
-  const int h = bh % p.H, T = p.T, K = p.K;
+  const int T = p.T;
   __nv_bfloat16 *y = p.y[which] + (size_t)bh * T * D + cg * 8;
-  const float *wp = p.w[which];
   const bool l2 = (p.l2mask >> which) & 1;
   const unsigned gmask = (G == 32 ? 0xffffffffu : ((1u << G) - 1u)) << (lane & ~(G - 1));
-  float w[kMaxK][8];  // this thread's 8 channels, tap-major
+  float w[kMaxK][8];  // this thread's 8 channels, tap-major (16-byte rows in shared memory)
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    const float *we = wp ? wp + ((size_t)h * D + cg * 8 + e) * K : nullptr;
-#pragma unroll
-    for (int tau = 0; tau < kMaxK; ++tau)
-      w[tau][e] = we ? ((tau < K) ? __ldg(we + tau) : 0.f) : (tau == 0 ? 1.f : 0.f);
+    const float4 w4 = *reinterpret_cast<const float4 *>(wsm + (cg * 8 + e) * kMaxK);
+    w[0][e] = w4.x;
+    w[1][e] = w4.y;
+    w[2][e] = w4.z;
+    w[3][e] = w4.w;
   }
   const int r0 = st * R;  // first row of the block, relative to t0
   const uint8_t *trow = tile + (size_t)kHalo * D * 2 + cg * 16;  // row of token t0
@@ -148,7 +151,8 @@ template <int DK, int DV>
 __global__ void __launch_bounds__(kThreads, 2) prologue_kernel(const ProParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   auto tile = [&](int which) { return smem + (which == 0 ? 0u : (which == 1 ? tile_bytes(DK) : 2u * tile_bytes(DK))); };
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + 2 * tile_bytes(DK) + tile_bytes(DV));
+  float *wsm = reinterpret_cast<float *>(smem + 2 * tile_bytes(DK) + tile_bytes(DV));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + 2 * tile_bytes(DK) + tile_bytes(DV) + wts_bytes(DK, DV));
   const int bh = blockIdx.y, t0 = blockIdx.x * kTile, T = p.T, K = p.K;
   const int hist_w = 2 * DK + DV;
   if (threadIdx.x == 0) {
@@ -159,21 +163,46 @@ __global__ void __launch_bounds__(kThreads, 2) prologue_kernel(const ProParams p
     issue_tile<DK>(p, 1, bh, t0, tile(1), &bars[1]);
     issue_tile<DV>(p, 2, bh, t0, tile(2), &bars[2]);
   }
-  // gates and beta while the tiles land
-  const int n = min(kTile, T - t0);
-  if (p.gate_kind != LA_GATE_NONE) {
-    const size_t base = ((size_t)bh * T + t0) * p.gate_width;
-    const int cnt = n * p.gate_width;
-    for (int i = threadIdx.x; i < cnt; i += kThreads) {
-      const float a = __ldg(p.a_gate + base + i);
-      const float sp = (p.gate_kind == LA_GATE_LOGSIGMOID) ? softplus_f(-a) : softplus_f(a);
-      p.g[base + i] = -sp * p.inv_tau;
+  // the head's weights, taps padded with zeros (no weights: the identity)
+  {
+    const int h = bh % p.H;
+    for (int i = threadIdx.x; i < (2 * DK + DV) * kMaxK; i += kThreads) {
+      const int c = i / kMaxK, tau = i % kMaxK;
+      const int which = c < DK ? 0 : (c < 2 * DK ? 1 : 2);
+      const int D = which < 2 ? DK : DV, cc = c - (which == 0 ? 0 : (which == 1 ? DK : 2 * DK));
+      const float *wp = p.w[which];
+      wsm[i] = wp ? ((tau < K) ? __ldg(wp + ((size_t)h * D + cc) * K + tau) : 0.f) : (tau == 0 ? 1.f : 0.f);
     }
   }
-  if (p.a_beta) {
-    const size_t base = (size_t)bh * T + t0;
-    for (int i = threadIdx.x; i < n; i += kThreads) p.beta[base + i] = 1.f / (1.f + expf(-__ldg(p.a_beta + base + i)));
+  // gates and beta while the tiles land: loads in batches of independent
+  // requests, then the activations and stores
+  const int n = min(kTile, T - t0);
+  const int tid = threadIdx.x;
+  const float *__restrict__ a_beta = p.a_beta;
+  const size_t bbase = (size_t)bh * T + t0;
+  const float ba = (a_beta && tid < n) ? __ldg(a_beta + bbase + tid) : 0.f;
+  if (p.gate_kind != LA_GATE_NONE) {
+    constexpr int kBatch = 16;
+    const float *__restrict__ a_gate = p.a_gate;
+    float *__restrict__ g = p.g;
+    const size_t base = ((size_t)bh * T + t0) * p.gate_width;
+    const int cnt = n * p.gate_width;
+    const bool logsig = p.gate_kind == LA_GATE_LOGSIGMOID;
+    for (int i0 = tid; i0 < cnt; i0 += kThreads * kBatch) {
+      float a[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int idx = i0 + j * kThreads;
+        a[j] = idx < cnt ? __ldg(a_gate + base + idx) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int idx = i0 + j * kThreads;
+        if (idx < cnt) g[base + idx] = -(logsig ? softplus_f(-a[j]) : softplus_f(a[j])) * p.inv_tau;
+      }
+    }
   }
+  if (a_beta && tid < n) p.beta[bbase + tid] = 1.f / (1.f + expf(-ba));
   // halo rows before token 0 (first tile only): the history, or zero
   if (t0 == 0) {
     for (int i = threadIdx.x; i < kHalo * (hist_w / 8); i += kThreads) {
@@ -197,9 +226,9 @@ __global__ void __launch_bounds__(kThreads, 2) prologue_kernel(const ProParams p
   }
   ok = __syncthreads_and(ok);
   if (ok) {
-    conv_tile<DK>(p, 0, bh, t0, tile(0));
-    conv_tile<DK>(p, 1, bh, t0, tile(1));
-    conv_tile<DV>(p, 2, bh, t0, tile(2));
+    conv_tile<DK>(p, 0, bh, t0, tile(0), wsm);
+    conv_tile<DK>(p, 1, bh, t0, tile(1), wsm + DK * kMaxK);
+    conv_tile<DV>(p, 2, bh, t0, tile(2), wsm + 2 * DK * kMaxK);
   }
   // the last K-1 raw rows of history ++ x, by the CTA holding the last token
   if (p.hist_out && K > 1 && t0 + kTile >= T) {
@@ -220,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 2) prologue_kernel(const ProParams p
 
 template <int DK, int DV>
 int launch_prologue(const ProParams &p, cudaStream_t s) {
-  const size_t smem = 2 * tile_bytes(DK) + tile_bytes(DV) + 64;
+  const size_t smem = 2 * tile_bytes(DK) + tile_bytes(DV) + wts_bytes(DK, DV) + 64;
   // set on every launch: the attribute belongs to the current device's context
   if (cudaFuncSetAttribute(prologue_kernel<DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
