@@ -39,14 +39,21 @@ import workloads  # noqa: E402
 METRIC = "tokens/sec and TFLOP/s of chunk fwd at 1 GB300; % of roofline"
 UNIT = "tokens/s"
 PROFILE_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-KERNEL_SOURCES = ["gated_delta_rule_linear_gb300/csrc/la_chunk_delta.cu",
-                  "gated_delta_rule_linear_gb300/csrc/la_chunk_delta_pair.cu",
-                  "gated_delta_rule_linear_gb300/csrc/la_wy.cuh",
-                  "gated_delta_rule_linear_gb300/csrc/la_chunk_ws.cu",
-                  "gated_delta_rule_linear_gb300/csrc/la_chunk_mat.cu",
-                  "gated_delta_rule_linear_gb300/csrc/la_tc_common.cuh",
-                  "gated_delta_rule_linear_gb300/csrc/la_sm100.cuh",
-                  "gated_delta_rule_linear_gb300/csrc/la_prologue.cu"]
+_CS = "gated_delta_rule_linear_gb300/csrc/"
+_COMMON = [_CS + "la_tc_common.cuh", _CS + "la_sm100.cuh"]
+# The sources each workload's dominant kernel is built from: a recorded DRAM
+# traffic figure stays valid while these files are unchanged.
+KERNEL_SOURCES = {
+    "gdn": [_CS + "la_chunk_delta_pair.cu", _CS + "la_chunk_delta.cu", _CS + "la_wy.cuh"] + _COMMON,
+    "kda": [_CS + "la_chunk_tc.cu", _CS + "la_wy.cuh"] + _COMMON,
+    "retnet": [_CS + "la_chunk_ws.cu"] + _COMMON,
+    "gla": [_CS + "la_chunk_ws.cu"] + _COMMON,
+    "scalar": [_CS + "la_chunk_ws.cu", _CS + "la_chunk_mat.cu"] + _COMMON,
+    "elu1": [_CS + "la_chunk_ws.cu", _CS + "la_chunk_mat.cu"] + _COMMON,
+    "linear_fp32": [_CS + "la_chunk_simt.cu"],
+    "prologue": [_CS + "la_prologue.cu", _CS + "la_sm100.cuh"],
+    "prologue_gla": [_CS + "la_prologue.cu", _CS + "la_sm100.cuh"],
+}
 
 
 def uses_materialised(wl, variant=None, sm_count=152) -> bool:
@@ -115,9 +122,9 @@ def read_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def kernel_hash() -> str:
+def kernel_hash(workload: str) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES.get(workload, sorted({f for v in KERNEL_SOURCES.values() for f in v})):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -128,7 +135,7 @@ def recorded_traffic(workload: str):
     on the current kernel source for this workload; else None."""
     if not os.path.exists(PROFILE_FILE):
         return None
-    cur = kernel_hash()
+    cur = kernel_hash(workload)
     with open(PROFILE_FILE) as f:
         for line in f:
             m = re.match(r"\s*traffic\s+workload=(\S+)\s+kernel_hash=(\S+)\s+bytes_per_launch=(\d+)", line)
