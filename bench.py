@@ -51,6 +51,7 @@ KERNEL_SOURCES = {
     "scalar": [_CS + "la_chunk_ws.cu", _CS + "la_chunk_mat.cu"] + _COMMON,
     "elu1": [_CS + "la_chunk_ws.cu", _CS + "la_chunk_mat.cu"] + _COMMON,
     "linear_fp32": [_CS + "la_chunk_simt.cu"],
+    "noncausal": [_CS + "la_chunk_mat.cu"] + _COMMON,
     "prologue": [_CS + "la_prologue.cu", _CS + "la_sm100.cuh"],
     "prologue_gla": [_CS + "la_prologue.cu", _CS + "la_sm100.cuh"],
 }
@@ -65,8 +66,14 @@ def uses_materialised(wl, variant=None, sm_count=152) -> bool:
             and 2 * wl.B * wl.H <= sm_count)
 
 
+def is_noncausal(wl) -> bool:
+    return bool(wl.extra.get("noncausal"))
+
+
 def kernel_name(wl, variant=None, sm_count=152) -> str:
     """The kernel one la_chunk_fwd launch of this workload runs."""
+    if is_noncausal(wl):
+        return "nc_sum_kernel+nc_finalize_kernel+chunk_output_kernel"
     if uses_materialised(wl, variant, sm_count):
         return "chunk_state_kernel+chunk_output_kernel"
     if wl.dtype == "f32" or variant == "simt":
@@ -93,6 +100,8 @@ def flops_per_token_head(mode: str, dk: int, dv: int, C: int = 64) -> float:
         dv = dv + 1
     if mode in ("gdn", "kda"):  # the per-channel gate of kda changes no contraction size
         return 2 * C * (3 * dk + 2 * dv) + C * C / 3.0 + 6 * dk * dv
+    if mode == "noncausal":  # K^T V and Q S: no scores
+        return 4 * dk * dv
     return 2 * C * (dk + dv) + 4 * dk * dv
 
 
@@ -231,11 +240,17 @@ def time_oracle(wl, inp, target_s: float = 12.0, max_heads: int | None = None):
              else pick(g))
     beta, S0 = pick(inp["beta"]), pick(inp["S0"])
     t0 = time.perf_counter()
-    oracle.recurrence_c(q, k, v, wl.mode, g=g, beta=beta, S0=S0, nthreads=cores)
+    if is_noncausal(wl):
+        from oracle.noncausal import noncausal
+        noncausal(q, k, v, wl.mode, S0=S0)
+        cores = 1
+    else:
+        oracle.recurrence_c(q, k, v, wl.mode, g=g, beta=beta, S0=S0, nthreads=cores)
     dt = time.perf_counter() - t0
     # nh head-sequences of T tokens = nh/H of the workload's B*T tokens
     tokens = nh * wl.T / wl.H
-    sample = f"{nh} of {BH} (batch, head) sequences, full T={wl.T}, float64, {cores} threads"
+    sample = (f"{nh} of {BH} (batch, head) sequences, full T={wl.T}, float64, "
+              + ("numpy" if is_noncausal(wl) else f"{cores} threads"))
     return tokens / dt, cores, sample, dt
 
 
@@ -296,6 +311,8 @@ def main():
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     mode_id = la.MODE_IDS[wl.mode] | (la.CONSTANTS["LA_F32"] if wl.dtype == "f32" else 0)
+    if is_noncausal(wl):
+        mode_id |= la.CONSTANTS["LA_NONCAUSAL"]
     ptr = lambda t: None if t is None else t.data_ptr()
 
     def step():
@@ -338,7 +355,7 @@ def main():
     ms_per_step = total_ms / args.steps
     tokens_per_step = B * T
     value = world * tokens_per_step * args.steps / (total_ms / 1e3)
-    flop_call = B * H * T * flops_per_token_head(wl.mode, dk, dv)
+    flop_call = B * H * T * flops_per_token_head("noncausal" if is_noncausal(wl) else wl.mode, dk, dv)
     tflops = world * flop_call * args.steps / (total_ms / 1e3) / 1e12
     avg_launch_s = statistics.mean(launch_ms) / 1e3
     alg_bytes = algorithmic_bytes(wl, d["S0"] is not None)
@@ -379,7 +396,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": wl.dtype, "data": "synthetic (seeded; shapes and distributions of the workload)",
-            "config": {"workload": wl.name, "mode": wl.mode, "B": B, "H": H, "T": T, "dk": dk,
+            "config": {"workload": wl.name, "mode": wl.mode + ("+noncausal" if is_noncausal(wl) else ""), "B": B, "H": H, "T": T, "dk": dk,
                        "dv": dv, "C": wl.C, "global_batch": B * world, "seq_len": T,
                        "parallelism": "replicas" if world > 1 else "single",
                        "l2": "inputs larger than L2 (no flush)" if alg_bytes > 129e6 else
@@ -389,7 +406,7 @@ def main():
             "cpu_baseline": cpu,
             "clocks": clk,
             "e2e": e2e,
-            "gpu_launches": args.steps * (2 if mat else 1),
+            "gpu_launches": args.steps * (3 if is_noncausal(wl) else (2 if mat else 1)),
         }
         print(json.dumps(line), flush=True)
     if dist:
@@ -467,7 +484,7 @@ def run_reference(args, wl, rank, world):
         "ms_per_step": round(B * T / value * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; shapes and distributions of the workload)",
-        "config": {"workload": wl.name, "mode": wl.mode, "B": B, "H": wl.H, "T": T, "dk": wl.dk,
+        "config": {"workload": wl.name, "mode": wl.mode + ("+noncausal" if is_noncausal(wl) else ""), "B": B, "H": wl.H, "T": T, "dk": wl.dk,
                    "dv": wl.dv, "C": wl.C, "global_batch": B, "seq_len": T,
                    "parallelism": "single"},
         "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle",

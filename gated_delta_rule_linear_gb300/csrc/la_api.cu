@@ -156,10 +156,15 @@ int la_stream_status(la_stream_t stream) {
   return LA_OK;
 }
 
-static int check_mode(int mode, const float *g, const float *beta, const char *fn) {
+static int check_mode(int mode, const float *g, const float *beta, const char *fn, bool allow_nc = false) {
   const int kind = mode & 0xff;
-  if ((mode & ~(0xff | LA_F32)) != 0 || kind < LA_LINEAR || kind > LA_KDA) {
+  const int flags = allow_nc ? (LA_F32 | LA_NONCAUSAL) : LA_F32;
+  if ((mode & ~(0xff | flags)) != 0 || kind < LA_LINEAR || kind > LA_KDA) {
     set_error("%s: unknown mode 0x%x", fn, mode);
+    return LA_ERR_INVALID_ARG;
+  }
+  if ((mode & LA_NONCAUSAL) && kind != LA_LINEAR && kind != LA_ELU1_NORM) {
+    set_error("%s: LA_NONCAUSAL goes with LA_LINEAR or LA_ELU1_NORM only", fn);
     return LA_ERR_INVALID_ARG;
   }
   const bool needs_g = kind == LA_RETNET || kind == LA_GLA || kind == LA_SCALAR_GATE || kind == LA_KDA;
@@ -204,9 +209,17 @@ int la_chunk_fwd(const void *q, const void *k, const void *v, const float *g, co
     set_error("%s: C must be 0, 64 or 128 (got %d)", fn, C);
     return LA_ERR_INVALID_ARG;
   }
-  int rc = check_mode(mode, g, beta, fn);
+  int rc = check_mode(mode, g, beta, fn, true);
   if (rc) return rc;
   const int kind = mode & 0xff;
+  if ((mode & LA_NONCAUSAL) && (mode & LA_F32)) {
+    set_error("%s: LA_NONCAUSAL takes bfloat16 inputs only", fn);
+    return LA_ERR_UNSUPPORTED;
+  }
+  if ((mode & LA_NONCAUSAL) && C != 0 && C != 64) {
+    set_error("%s: chunk length C=%d is not implemented in this build (use 0 or 64)", fn, C);
+    return LA_ERR_UNSUPPORTED;
+  }
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16)) {
     set_error("%s: q, k, v and o must be 16-byte aligned", fn);
     return LA_ERR_INVALID_ARG;
@@ -223,6 +236,29 @@ int la_chunk_fwd(const void *q, const void *k, const void *v, const float *g, co
     set_error("%s: no CUDA device available (%s)", fn, cudaGetErrorString(cudaGetLastError()));
     return LA_ERR_CUDA;
   }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (mode & LA_NONCAUSAL) {
+    p.C = 64;
+    void *ws = nullptr;
+    const size_t bytes = nc_workspace_bytes(p);
+    cudaMemPool_t pool = workspace_pool();
+    if (!pool) {
+      set_error("%s: could not create the workspace pool: %s", fn, cudaGetErrorString(cudaGetLastError()));
+      return LA_ERR_CUDA;
+    }
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes, pool, s);
+    if (e != cudaSuccess) {
+      set_error("%s: workspace allocation of %zu bytes failed: %s", fn, bytes, cudaGetErrorString(e));
+      return LA_ERR_CUDA;
+    }
+    rc = launch_chunk_noncausal(p, ws, s);
+    e = cudaFreeAsync(ws, s);
+    if (rc == LA_OK && e != cudaSuccess) {
+      set_error("%s: workspace release failed: %s", fn, cudaGetErrorString(e));
+      return LA_ERR_CUDA;
+    }
+    return rc;
+  }
   int chunk = 64;
   const int variant = select_variant(p, &chunk);
   if (variant == -2) {
@@ -231,7 +267,6 @@ int la_chunk_fwd(const void *q, const void *k, const void *v, const float *g, co
   }
   if (variant < 0) return LA_ERR_UNSUPPORTED;
   p.C = chunk;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (variant == kVariantMat) {
     // stream-ordered workspace: allocated and released on the caller's stream
     void *ws = nullptr;

@@ -13,6 +13,8 @@
 //
 // The workspace (one state image per chunk, plus z per chunk for elu+1) is
 // provided by the caller of these launchers.
+#include <algorithm>
+
 #include "la_tc_common.cuh"
 
 namespace la {
@@ -390,9 +392,10 @@ chunk_state_kernel(const ChunkParams p, uint8_t *__restrict__ ws, float *__restr
 constexpr int kBThreads = 128;
 
 struct BLayout {
-  uint32_t qk, v, g, s, p, ot, misc, bar, total;
+  uint32_t qk, v, g, s, s2, p, ot, misc, bar, total;
 };
-__host__ __device__ inline BLayout b_layout(int dk, int kind) {
+// nc: the non-causal pass also holds the low part of the state image (s2)
+__host__ __device__ inline BLayout b_layout(int dk, int kind, bool nc = false) {
   BLayout L;
   const bool gla = kind == kGla;
   uint32_t o = 0;
@@ -400,6 +403,7 @@ __host__ __device__ inline BLayout b_layout(int dk, int kind) {
   L.v = o; o += 16384u;
   L.g = o; o += gla ? up1k((uint32_t)kC * dk * 4u) : 0u;
   L.s = o; o += blob_bytes(dk);
+  L.s2 = o; o += nc ? blob_bytes(dk) : 0u;
   L.p = o; o += 8192u;
   L.ot = o; o += 16384u;
   L.misc = o; o += 2048u;
@@ -408,7 +412,10 @@ __host__ __device__ inline BLayout b_layout(int dk, int kind) {
   return L;
 }
 
-template <int DK, int DV, int KIND>
+// NC (non-causal, linear and elu+1): every chunk reads the one image of the
+// whole sequence's state and there is no intra-chunk term, so O = Q~ S_total
+// (elu+1: divided by phi(q).z_total); only the q tile is loaded.
+template <int DK, int DV, int KIND, bool NC = false>
 __global__ void __launch_bounds__(kBThreads)
 chunk_output_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const float *__restrict__ zws,
                     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -418,7 +425,7 @@ chunk_output_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const f
   constexpr bool sgate = KIND == kRetnet || KIND == kScalar;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const BLayout L = b_layout(DK, KIND);
+  const BLayout L = b_layout(DK, KIND, NC);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = p.T, nch = (T + kC - 1) / kC;
   const int bh = blockIdx.x / nch, i = blockIdx.x % nch, h = bh % p.H;
@@ -440,19 +447,25 @@ chunk_output_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const f
     mbar_init(bar, 1);
     mbar_init(mbar, 1);
     fence_mbar_init();
-    constexpr uint32_t bytes = 2u * DK * kC * 2u + DV * kC * 2u + (gla ? DK * kC * 4u : 0u) + blob_bytes(DK);
+    constexpr uint32_t bytes = NC ? DK * kC * 2u + 2u * blob_bytes(DK)
+                                  : 2u * DK * kC * 2u + DV * kC * 2u + (gla ? DK * kC * 4u : 0u) + blob_bytes(DK);
     mbar_arrive_expect_tx(bar, bytes);
 #pragma unroll
     for (int a = 0; a < DK / 64; ++a) {
       tma_load_3d(qk + a * 16384, &tm_q, bar, 64 * a, t0, bh);
-      tma_load_3d(qk + a * 16384 + 8192, &tm_k, bar, 64 * a, t0, bh);
+      if (!NC) tma_load_3d(qk + a * 16384 + 8192, &tm_k, bar, 64 * a, t0, bh);
     }
+    if (!NC) {
 #pragma unroll
-    for (int a = 0; a < DV / 64; ++a) tma_load_3d(sm + L.v + a * 8192, &tm_v, bar, 64 * a, t0, bh);
+      for (int a = 0; a < DV / 64; ++a) tma_load_3d(sm + L.v + a * 8192, &tm_v, bar, 64 * a, t0, bh);
+    }
     if (gla) tma_load_3d(sm + L.g, &tm_g, bar, 0, t0, bh);
-    bulk_load(sm + L.s, ws + ((size_t)bh * nch + i) * blob_bytes(DK), blob_bytes(DK), bar);
+    const size_t img = NC ? (size_t)bh : (size_t)bh * nch + i;  // the state image this chunk reads
+    bulk_load(sm + L.s, ws + img * blob_bytes(DK), blob_bytes(DK), bar);
+    if (NC)  // its low part (x - bf16(x)), B*H images further on
+      bulk_load(sm + L.s2, ws + ((size_t)p.B * p.H + bh) * blob_bytes(DK), blob_bytes(DK), bar);
   }
-  if (DV == 64) {
+  if (DV == 64 && !NC) {
     for (int q = tid; q < 512; q += kBThreads)
       reinterpret_cast<uint4 *>(sm + L.v + 8192)[q] = make_uint4(0, 0, 0, 0);
   }
@@ -503,7 +516,7 @@ chunk_output_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const f
       ebm[tid] = __expf(bmid);
     }
     __syncthreads();
-    if (elu || gla) {
+    if ((elu || gla) && !(NC && tid >= kC)) {  // NC: the q rows only
       const int row = tid;  // row of [Q; K]
       const int r = row & (kC - 1);
       const bool is_k = row >= kC;
@@ -530,7 +543,7 @@ chunk_output_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const f
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {
+    if (tid == 0 && !NC) {
       tc_fence_after();
       const uint32_t a_qk = smem_u32(qk);
       constexpr uint32_t idesc = idesc_bf16_f32(128, 64, false, false);
@@ -542,13 +555,26 @@ chunk_output_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const f
       }
       mma_commit(mbar);
     }
-    ok = mbar_wait_bounded(mbar, 0, kSpinLimit);
+    ok = NC ? true : mbar_wait_bounded(mbar, 0, kSpinLimit);
     if (!__syncthreads_and(ok)) {
       if (tid == 0) atomicOr(p.status, kStatusTimeout);
     } else {
       tc_fence_after();
       // ---- masked, decayed scores P (TMEM lanes 0..63); elu+1: q.z
-      if (tid < kC) {
+      if (NC) {
+        if (elu && tid < kC) {  // q.z_total
+          const int r = tid;
+          const float *zp = zws + (size_t)bh * DK;
+          float acc = 0.f;
+          for (int g8 = 0; g8 < DK / 8; ++g8) {
+            float f[8];
+            unpack8(*reinterpret_cast<const uint4 *>(qk + (g8 >> 3) * 16384 + sw128_off(r, (g8 & 7) * 8)), f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc = fmaf(f[e], __ldg(zp + g8 * 8 + e), acc);
+          }
+          den[r] = acc;
+        }
+      } else if (tid < kC) {
         const int r = tid;
         const float b2r = sgate ? b2[r] : 0.f;
         float rowsum = 0.f;
@@ -599,7 +625,7 @@ chunk_output_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const f
           *reinterpret_cast<uint4 *>(ptr) = pack8(f);
         }
       }
-      if (elu && tid < kC) den[tid] += qz[tid];
+      if (!NC && elu && tid < kC) den[tid] += qz[tid];
       fence_proxy_async();
       tc_fence_before();
       __syncthreads();
@@ -614,13 +640,23 @@ chunk_output_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const f
           const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
           mma_bf16(tbase + kO1, desc_sw128(a_s + ko, 16, 1024), desc_sw128(a_qk + ko, 16, 1024), id_o1, kk > 0);
         }
+        if (NC) {
+          const uint32_t a_s2 = smem_u32(sm + L.s2);
 #pragma unroll
-        for (int kk = 0; kk < kC / 16; ++kk)
-          mma_bf16(tbase + kO2, desc_sw128(a_v + kk * 2048, 8192, 1024), desc_sw128(a_p + kk * 32, 16, 1024),
-                   id_o2, kk > 0);
+          for (int kk = 0; kk < DK / 16; ++kk) {
+            const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_bf16(tbase + kO1, desc_sw128(a_s2 + ko, 16, 1024), desc_sw128(a_qk + ko, 16, 1024), id_o1, 1u);
+          }
+        }
+        if (!NC) {
+#pragma unroll
+          for (int kk = 0; kk < kC / 16; ++kk)
+            mma_bf16(tbase + kO2, desc_sw128(a_v + kk * 2048, 8192, 1024), desc_sw128(a_p + kk * 32, 16, 1024),
+                     id_o2, kk > 0);
+        }
         mma_commit(mbar);
       }
-      ok = mbar_wait_bounded(mbar, 1, kSpinLimit);
+      ok = mbar_wait_bounded(mbar, NC ? 0 : 1, kSpinLimit);
       if (!__syncthreads_and(ok)) {
         if (tid == 0) atomicOr(p.status, kStatusTimeout);
       } else {
@@ -632,7 +668,12 @@ chunk_output_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const f
         for (int r0 = 0; r0 < kC; r0 += 32) {
           float a[32], b[32], f[32];
           tmem_ld32(tl + kO1 + r0, a);
-          tmem_ld32(tl + kO2 + r0, b);
+          if (NC) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) b[e] = 0.f;
+          } else {
+            tmem_ld32(tl + kO2 + r0, b);
+          }
           if (sgate) load32(eb + r0, f);
           if (elu) load32(den + r0, f);
           tmem_wait_ld();
@@ -725,6 +766,283 @@ int launch_kind(const ChunkParams &p, uint8_t *ws, float *zws, cudaStream_t stre
   return launch_typed<64, 64, KIND>(p, ws, zws, stream);
 }
 
+// ================================================= non-causal forward
+// o_t = S_total^T q_t with S_total = S0 + sum_s k_s v_s^T over the whole
+// sequence (elu+1: phi on q and k, divided by phi(q).z_total): the
+// right-to-left product Q (K^T V) of the kernel-attention notes, section 3.
+// Three launches: a split-T reduction of V^T K on the
+// tensor cores (one CTA per head and T-range), a finalize pass per head (adds
+// S0 and the partial sums, writes S_final and the bf16 state image), and the
+// output pass above with NC = true (every chunk reads the same image).
+constexpr int kNThreads = 128;
+
+struct NLayout {
+  uint32_t k, klo, v, stage, bar, total;
+};
+__host__ __device__ inline NLayout n_layout(int dk, bool elu) {
+  NLayout L;
+  uint32_t o = 0;
+  L.k = o; o += (uint32_t)(dk / 64) * 8192u;
+  L.klo = o; o += elu ? (uint32_t)(dk / 64) * 8192u : 0u;  // phi(k) - bf16(phi(k))
+  L.v = o; o += 16384u;  // value rows 64..127 are a zero pad when dv = 64
+  L.stage = up1k(o);
+  o = 2u * L.stage;
+  L.bar = o; o += 64u;
+  L.total = o;
+  return L;
+}
+
+template <int DK, int DV, bool ELU>
+__global__ void __launch_bounds__(kNThreads)
+nc_sum_kernel(const ChunkParams p, int nsplit, float *__restrict__ part, float *__restrict__ zpart,
+              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const NLayout L = n_layout(DK, ELU);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int T = p.T, nch = (T + kC - 1) / kC;
+  const int bh = blockIdx.x / nsplit, sp = blockIdx.x % nsplit;
+  const int c0 = (int)(((long long)sp * nch) / nsplit), c1 = (int)(((long long)(sp + 1) * nch) / nsplit);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bar);
+  uint64_t *full = bars, *empty = bars + 2, *drain = bars + 4;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 5);
+  auto stage = [&](int s) { return sm + (uint32_t)s * L.stage; };
+  constexpr uint32_t bytes = DK * kC * 2u + DV * kC * 2u;
+  auto issue = [&](int j, int s) {
+    uint8_t *st = stage(s);
+    mbar_arrive_expect_tx(&full[s], bytes);
+#pragma unroll
+    for (int a = 0; a < DK / 64; ++a) tma_load_3d(st + L.k + a * 8192, &tm_k, &full[s], 64 * a, j * kC, bh);
+#pragma unroll
+    for (int a = 0; a < DV / 64; ++a) tma_load_3d(st + L.v + a * 8192, &tm_v, &full[s], 64 * a, j * kC, bh);
+  };
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 128);
+    tmem_relinquish();
+  }
+  if (DV == 64) {
+    for (int q = tid; q < 2 * 512; q += kNThreads)
+      reinterpret_cast<uint4 *>(stage(q >> 9) + L.v + 8192)[q & 511] = make_uint4(0, 0, 0, 0);
+  }
+  fence_proxy_async();
+  if (tid == 0) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&full[b], 1);
+      mbar_init(&empty[b], 1);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    for (int j = c0; j < c0 + 2 && j < c1; ++j) issue(j, j - c0);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint32_t tl = tbase + (static_cast<uint32_t>(warp * 32) << 16);
+  // elu+1: thread (cg, r0) owns key channels 8 cg .. 8 cg + 7 on rows r0, r0 + kStep, ...
+  constexpr int kGroups = DK / 8, kStep = kNThreads / kGroups;
+  const int cg = tid % kGroups, r0 = tid / kGroups;
+  float zacc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  // thread 0 tracks failures (a wait that gave up) and the last chunk loaded into each stage
+  bool ok = true;
+  int last0 = c0, last1 = min(c0 + 1, c1 - 1);
+  for (int j = c0; j < c1; ++j) {
+    const int it = j - c0, s = it & 1, n = min(kC, T - j * kC);
+    const uint32_t ph = (uint32_t)(it >> 1) & 1u;
+    if (tid == 0 && ok) ok = mbar_wait_bounded(&full[s], ph, kSpinLimit);
+    if (!__syncthreads_and(ok)) {  // every thread leaves together
+      ok = false;
+      break;
+    }
+    uint8_t *st = stage(s);
+    if (ELU) {  // phi(k) = elu(k) + 1 on the rows in [0, n), zero beyond; bf16 high part in place, low part apart
+#pragma unroll 2
+      for (int r = r0; r < kC; r += kStep) {
+        const uint32_t off = (uint32_t)(cg >> 3) * 8192u + sw128_off(r, (cg & 7) * 8);
+        float f[8], fh[8];
+        unpack8(*reinterpret_cast<const uint4 *>(st + L.k + off), f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          f[e] = (r < n) ? (f[e] > 0.f ? f[e] + 1.f : __expf(f[e])) : 0.f;
+          zacc[e] += f[e];
+        }
+        const uint4 hi = pack8(f);
+        unpack8(hi, fh);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) fh[e] = f[e] - fh[e];
+        *reinterpret_cast<uint4 *>(st + L.k + off) = hi;
+        *reinterpret_cast<uint4 *>(st + L.klo + off) = pack8(fh);
+      }
+      fence_proxy_async();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      // S^T += V^T K: V as MN-major A (M = 128 value rows), K as MN-major B (N = dk)
+      constexpr uint32_t id = idesc_bf16_f32(128, DK, true, true);
+      const uint32_t a_v = smem_u32(st + L.v), a_k = smem_u32(st + L.k), a_kl = smem_u32(st + L.klo);
+#pragma unroll
+      for (int kk = 0; kk < kC / 16; ++kk) {
+        const uint64_t dv_ = desc_sw128(a_v + kk * 2048, 8192, 1024);
+        mma_bf16(tbase, dv_, desc_sw128(a_k + kk * 2048, 8192, 1024), id, (it > 0 || kk > 0) ? 1u : 0u);
+        if (ELU) mma_bf16(tbase, dv_, desc_sw128(a_kl + kk * 2048, 8192, 1024), id, 1u);
+      }
+      mma_commit(&empty[s]);
+      if (j + 2 < c1) {  // the stage takes chunk j + 2 once these MMAs have read it
+        if (mbar_wait_bounded(&empty[s], ph, kSpinLimit)) {
+          issue(j + 2, s);
+          if (s == 0) last0 = j + 2; else last1 = j + 2;
+        } else {
+          ok = false;
+        }
+      }
+    }
+  }
+  if (tid == 0) {
+    mma_commit(drain);
+    if (!mbar_wait_bounded(drain, 0, kSpinLimit)) ok = false;
+    if (!ok) {
+      atomicOr(p.status, kStatusTimeout);
+      // loads still in flight land before the CTA leaves (bounded)
+      (void)mbar_wait_bounded(&full[0], (uint32_t)((last0 - c0) >> 1) & 1u, 4096);
+      if (c1 - c0 > 1) (void)mbar_wait_bounded(&full[1], (uint32_t)((last1 - c0) >> 1) & 1u, 4096);
+    }
+  }
+  ok = __syncthreads_and(ok);
+  tc_fence_after();
+  if (ok) {
+    // partial S^T of this T-range: thread = TMEM lane = value row
+    const int v = tid;
+    float *dst = part + ((size_t)bh * nsplit + sp) * DV * DK + (size_t)v * DK;
+#pragma unroll 1
+    for (int cc = 0; cc < DK; cc += 32) {
+      float x[32];
+      tmem_ld32(tl + cc, x);
+      tmem_wait_ld();
+      if (v < DV) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          reinterpret_cast<float4 *>(dst + cc)[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+      }
+    }
+    if (ELU) {  // z partial: reduce the row-strided thread sums per channel
+      float *zs = reinterpret_cast<float *>(stage(0));  // the stages are idle now
+#pragma unroll
+      for (int e = 0; e < 8; ++e) zs[r0 * DK + cg * 8 + e] = zacc[e];
+      __syncthreads();
+      if (tid < DK) {
+        float z = 0.f;
+        for (int r = 0; r < kStep; ++r) z += zs[r * DK + tid];
+        zpart[((size_t)bh * nsplit + sp) * DK + tid] = z;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tbase, 128);
+}
+
+// S_total^T = S0^T + sum of the partials; S_final and the bf16 image as a
+// high/low pair (x = hi + lo to about 2^-16; value rows beyond dv zero),
+// elu+1: z_total = z0 + sum of the partial z.
+template <int DK, int DV, bool ELU>
+__global__ void __launch_bounds__(128)
+nc_finalize_kernel(const ChunkParams p, int nsplit, const float *__restrict__ part, const float *__restrict__ zpart,
+                   uint8_t *__restrict__ img, float *__restrict__ zws) {
+  const int bh = blockIdx.x, c = threadIdx.x;
+  if (c >= DK) return;
+  constexpr int W = DV + (ELU ? 1 : 0);
+  uint8_t *im = img + (size_t)bh * blob_bytes(DK) + (size_t)(c >> 6) * 16384u;
+  const size_t lo_off = (size_t)p.B * p.H * blob_bytes(DK);  // the low parts follow the B*H high images
+  const float *pp = part + (size_t)bh * nsplit * DV * DK + c;
+#pragma unroll 1
+  for (int v = 0; v < 128; ++v) {
+    float x = 0.f;
+    if (v < DV) {
+      x = p.S0 ? p.S0[((size_t)bh * DK + c) * W + v] : 0.f;
+      for (int q = 0; q < nsplit; ++q) x += pp[(size_t)q * DV * DK + (size_t)v * DK];
+      if (p.S_final) p.S_final[((size_t)bh * DK + c) * W + v] = x;
+    }
+    const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+    *reinterpret_cast<__nv_bfloat16 *>(im + sw128_off(v, c & 63)) = hi;
+    *reinterpret_cast<__nv_bfloat16 *>(im + lo_off + sw128_off(v, c & 63)) =
+        __float2bfloat16_rn(x - __bfloat162float(hi));
+  }
+  if (ELU) {
+    float z = p.S0 ? p.S0[((size_t)bh * DK + c) * W + DV] : 0.f;
+    for (int q = 0; q < nsplit; ++q) z += zpart[((size_t)bh * nsplit + q) * DK + c];
+    zws[(size_t)bh * DK + c] = z;
+    if (p.S_final) p.S_final[((size_t)bh * DK + c) * W + DV] = z;
+  }
+}
+
+int nc_splits(const ChunkParams &p) {
+  const long long BH = (long long)p.B * p.H;
+  const int nch = (p.T + kC - 1) / kC;
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 148;
+  long long want = (2LL * sms + BH - 1) / BH;  // about two CTAs per SM
+  want = std::min<long long>(want, std::max(1, nch / 4));  // at least four chunks each
+  return (int)std::max<long long>(1, want);
+}
+
+template <int DK, int DV, int KIND>
+int launch_nc_typed(const ChunkParams &p, uint8_t *ws, cudaStream_t stream) {
+  constexpr bool ELU = KIND == kElu1;
+  const int BH = p.B * p.H, nch = (p.T + kC - 1) / kC, ns = nc_splits(p);
+  uint8_t *img = ws;  // B*H high images, then B*H low images
+  float *zws = reinterpret_cast<float *>(img + 2 * (size_t)BH * blob_bytes(DK));
+  float *part = zws + (size_t)BH * DK;
+  float *zpart = part + (size_t)BH * ns * DV * DK;
+  const NLayout Ln = n_layout(DK, ELU);
+  const BLayout Lb = b_layout(DK, KIND, true);
+  const size_t sn = Ln.total + 1024, sb = Lb.total + 1024;
+  CUtensorMap mq, mk, mv, mo;
+  const bool ok = make_map(&mq, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DK, p.T, BH, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+                  make_map(&mk, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DK, p.T, BH, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+                  make_map(&mv, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DV, p.T, BH, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+                  make_map(&mo, p.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DV, p.T, BH, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) {
+    set_error("la_chunk_fwd: cuTensorMapEncodeTiled rejected a tensor map");
+    return LA_ERR_CUDA;
+  }
+  auto ka = nc_sum_kernel<DK, DV, ELU>;
+  auto kf = nc_finalize_kernel<DK, DV, ELU>;
+  auto kb = chunk_output_kernel<DK, DV, KIND, true>;
+  cudaError_t e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sn);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sb);
+  if (e == cudaSuccess) {
+    ka<<<(unsigned)(BH * ns), kNThreads, sn, stream>>>(p, ns, part, zpart, mk, mv);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) {
+    kf<<<(unsigned)BH, 128, 0, stream>>>(p, ns, part, zpart, img, zws);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) {
+    kb<<<(unsigned)((size_t)BH * nch), kBThreads, sb, stream>>>(p, img, zws, mq, mk, mv, mq, mo);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) {
+    set_error("la_chunk_fwd: non-causal kernels failed to launch: %s", cudaGetErrorString(e));
+    return LA_ERR_CUDA;
+  }
+  return LA_OK;
+}
+
+template <int KIND>
+int launch_nc_kind(const ChunkParams &p, uint8_t *ws, cudaStream_t stream) {
+  if (p.dk == 128 && p.dv == 128) return launch_nc_typed<128, 128, KIND>(p, ws, stream);
+  if (p.dk == 128 && p.dv == 64) return launch_nc_typed<128, 64, KIND>(p, ws, stream);
+  if (p.dk == 64 && p.dv == 128) return launch_nc_typed<64, 128, KIND>(p, ws, stream);
+  return launch_nc_typed<64, 64, KIND>(p, ws, stream);
+}
+
 }  // namespace
 
 size_t mat_workspace_bytes(const ChunkParams &p) {
@@ -752,6 +1070,28 @@ int launch_chunk_mat(const ChunkParams &p, void *workspace, cudaStream_t stream)
       set_error("la_chunk_fwd: the materialised variant covers the unit-write modes only");
       return LA_ERR_UNSUPPORTED;
   }
+}
+
+}  // namespace la
+
+namespace la {
+
+size_t nc_workspace_bytes(const ChunkParams &p) {
+  const size_t BH = (size_t)p.B * p.H, ns = (size_t)nc_splits(p);
+  return 2 * BH * blob_bytes(p.dk) + BH * p.dk * sizeof(float) + BH * ns * p.dv * p.dk * sizeof(float) +
+         BH * ns * p.dk * sizeof(float);
+}
+
+int launch_chunk_noncausal(const ChunkParams &p, void *workspace, cudaStream_t stream) {
+  if (!encode_fn()) {
+    set_error("la_chunk_fwd: cuTensorMapEncodeTiled is unavailable");
+    return LA_ERR_CUDA;
+  }
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  if (p.kind == kLinear) return launch_nc_kind<kLinear>(p, ws, stream);
+  if (p.kind == kElu1) return launch_nc_kind<kElu1>(p, ws, stream);
+  set_error("la_chunk_fwd: LA_NONCAUSAL covers LA_LINEAR and LA_ELU1_NORM only");
+  return LA_ERR_UNSUPPORTED;
 }
 
 }  // namespace la

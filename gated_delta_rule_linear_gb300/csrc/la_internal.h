@@ -64,6 +64,11 @@ int launch_step(const StepParams &p, cudaStream_t stream);
 // pass, through a caller-provided workspace of mat_workspace_bytes(p) bytes.
 size_t mat_workspace_bytes(const ChunkParams &p);
 int launch_chunk_mat(const ChunkParams &p, void *workspace, cudaStream_t stream);
+// Non-causal forward (LA_NONCAUSAL; linear and elu+1, bf16): split-T state
+// reduction, finalize, parallel output pass, through a caller-provided
+// workspace of nc_workspace_bytes(p) bytes.
+size_t nc_workspace_bytes(const ChunkParams &p);
+int launch_chunk_noncausal(const ChunkParams &p, void *workspace, cudaStream_t stream);
 
 // Which chunk-forward kernel a shape goes to (host-side selection).
 enum Variant : int { kVariantSimt = 0, kVariantTc = 1, kVariantMat = 2 };

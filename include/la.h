@@ -93,6 +93,14 @@ typedef struct CUstream_st *la_stream_t;
 #define LA_KDA           6
 /* Flag: q, k, v and o are float32 instead of bfloat16. */
 #define LA_F32           0x100
+/* Flag (la_chunk_fwd only, with LA_LINEAR or LA_ELU1_NORM, bfloat16): the
+ * non-causal form, every token reads the state of the whole sequence,
+ *     o_t = S_T^T q_t,  S_T = S0 + sum_{s<T} k_s v_s^T
+ * (elu+1: o_t = S_T^T phi(q_t) / (z_T . phi(q_t))), computed right to left as
+ * Q (K^T V) (kernel-attention notes, section 3).
+ * S_final is S_T, as in the causal form. Uses a stream-ordered workspace
+ * from the library's pool (B*H*dk*(512 + 4 + 4*(dv+1)*splits) bytes). */
+#define LA_NONCAUSAL     0x200
 
 /*
  * la_chunk_fwd -- causal forward pass over a whole sequence, chunkwise.

@@ -13,6 +13,8 @@ Contents
                four-step update, a Kronecker brute force, the chunk form)
   recurrence_c the same recurrence in plain C (la_oracle.c), multi-threaded
                over heads, for full-length sequences and CPU timing
+  prologue     short convolution, L2 normalisation, gate and beta activations
+  noncausal    the non-causal form O = Q (K^T V) (linear, elu+1)
 """
 from __future__ import annotations
 

@@ -71,13 +71,16 @@ def _call(**kw):
     (dict(dv=32), "LA_ERR_UNSUPPORTED"),
     (dict(C=32), "LA_ERR_INVALID_ARG"),
     (dict(mode=9), "LA_ERR_INVALID_ARG"),
-    (dict(mode=0x200), "LA_ERR_INVALID_ARG"),
+    (dict(mode=0x400), "LA_ERR_INVALID_ARG"),          # unknown flag
     (dict(q=A + 8), "LA_ERR_INVALID_ARG"),            # 16-byte alignment
     (dict(o=A + 2), "LA_ERR_INVALID_ARG"),
     (dict(g=A), "LA_ERR_INVALID_ARG"),                # linear takes no gates
     (dict(mode=2), "LA_ERR_INVALID_ARG"),             # retnet needs g
     (dict(mode=3), "LA_ERR_INVALID_ARG"),             # gla needs g
     (dict(mode=3, g=A + 4), "LA_ERR_INVALID_ARG"),    # gla g must be 16-byte aligned
+    (dict(mode=2 | 0x200, g=A), "LA_ERR_INVALID_ARG"),  # non-causal: linear and elu1 only
+    (dict(mode=0x200 | 0x100), "LA_ERR_UNSUPPORTED"),   # non-causal: bf16 only
+    (dict(mode=0x200, C=128), "LA_ERR_UNSUPPORTED"),    # non-causal: C = 64
     (dict(mode=4), "LA_ERR_INVALID_ARG"),             # scalar needs g
     (dict(mode=2, g=A, beta=A), "LA_ERR_INVALID_ARG"),  # beta only for gdn
     (dict(mode=1, g=A), "LA_ERR_INVALID_ARG"),        # elu1 takes no gates

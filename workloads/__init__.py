@@ -80,6 +80,10 @@ WORKLOADS = {
     # The next row after the headline workloads; parity tests and its own bench line.
     "kda": Workload("kda", "kda", 4, 16, 16384, 128, 128, "bf16", 64, seed=7,
                     l2norm_qk=True, s0=True),
+    # Non-causal linear attention O = Q (K^T V) (a next row): the RetNet shape
+    # and q/k/v distribution, no gates.
+    "noncausal": Workload("noncausal", "linear", 8, 16, 4096, 128, 128, "bf16", 64, seed=8,
+                          qkv_scale=1.0 / math.sqrt(128.0), extra={"noncausal": True}),
 }
 
 
