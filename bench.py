@@ -73,7 +73,7 @@ def is_noncausal(wl) -> bool:
 def kernel_name(wl, variant=None, sm_count=152) -> str:
     """The kernel one la_chunk_fwd launch of this workload runs."""
     if is_noncausal(wl):
-        return "nc_sum_kernel+nc_finalize_kernel+chunk_output_kernel"
+        return "nc_sum_kernel+nc_finalize_kernel+nc_out_kernel"
     if uses_materialised(wl, variant, sm_count):
         return "chunk_state_kernel+chunk_output_kernel"
     if wl.dtype == "f32" or variant == "simt":

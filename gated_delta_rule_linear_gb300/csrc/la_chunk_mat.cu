@@ -392,10 +392,9 @@ chunk_state_kernel(const ChunkParams p, uint8_t *__restrict__ ws, float *__restr
 constexpr int kBThreads = 128;
 
 struct BLayout {
-  uint32_t qk, v, g, s, s2, p, ot, misc, bar, total;
+  uint32_t qk, v, g, s, p, ot, misc, bar, total;
 };
-// nc: the non-causal pass also holds the low part of the state image (s2)
-__host__ __device__ inline BLayout b_layout(int dk, int kind, bool nc = false) {
+__host__ __device__ inline BLayout b_layout(int dk, int kind) {
   BLayout L;
   const bool gla = kind == kGla;
   uint32_t o = 0;
@@ -403,7 +402,6 @@ __host__ __device__ inline BLayout b_layout(int dk, int kind, bool nc = false) {
   L.v = o; o += 16384u;
   L.g = o; o += gla ? up1k((uint32_t)kC * dk * 4u) : 0u;
   L.s = o; o += blob_bytes(dk);
-  L.s2 = o; o += nc ? blob_bytes(dk) : 0u;
   L.p = o; o += 8192u;
   L.ot = o; o += 16384u;
   L.misc = o; o += 2048u;
@@ -412,10 +410,7 @@ __host__ __device__ inline BLayout b_layout(int dk, int kind, bool nc = false) {
   return L;
 }
 
-// NC (non-causal, linear and elu+1): every chunk reads the one image of the
-// whole sequence's state and there is no intra-chunk term, so O = Q~ S_total
-// (elu+1: divided by phi(q).z_total); only the q tile is loaded.
-template <int DK, int DV, int KIND, bool NC = false>
+template <int DK, int DV, int KIND>
 __global__ void __launch_bounds__(kBThreads)
 chunk_output_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const float *__restrict__ zws,
                     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -425,7 +420,7 @@ chunk_output_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const f
   constexpr bool sgate = KIND == kRetnet || KIND == kScalar;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const BLayout L = b_layout(DK, KIND, NC);
+  const BLayout L = b_layout(DK, KIND);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = p.T, nch = (T + kC - 1) / kC;
   const int bh = blockIdx.x / nch, i = blockIdx.x % nch, h = bh % p.H;
@@ -447,25 +442,19 @@ chunk_output_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const f
     mbar_init(bar, 1);
     mbar_init(mbar, 1);
     fence_mbar_init();
-    constexpr uint32_t bytes = NC ? DK * kC * 2u + 2u * blob_bytes(DK)
-                                  : 2u * DK * kC * 2u + DV * kC * 2u + (gla ? DK * kC * 4u : 0u) + blob_bytes(DK);
+    constexpr uint32_t bytes = 2u * DK * kC * 2u + DV * kC * 2u + (gla ? DK * kC * 4u : 0u) + blob_bytes(DK);
     mbar_arrive_expect_tx(bar, bytes);
 #pragma unroll
     for (int a = 0; a < DK / 64; ++a) {
       tma_load_3d(qk + a * 16384, &tm_q, bar, 64 * a, t0, bh);
-      if (!NC) tma_load_3d(qk + a * 16384 + 8192, &tm_k, bar, 64 * a, t0, bh);
+      tma_load_3d(qk + a * 16384 + 8192, &tm_k, bar, 64 * a, t0, bh);
     }
-    if (!NC) {
 #pragma unroll
-      for (int a = 0; a < DV / 64; ++a) tma_load_3d(sm + L.v + a * 8192, &tm_v, bar, 64 * a, t0, bh);
-    }
+    for (int a = 0; a < DV / 64; ++a) tma_load_3d(sm + L.v + a * 8192, &tm_v, bar, 64 * a, t0, bh);
     if (gla) tma_load_3d(sm + L.g, &tm_g, bar, 0, t0, bh);
-    const size_t img = NC ? (size_t)bh : (size_t)bh * nch + i;  // the state image this chunk reads
-    bulk_load(sm + L.s, ws + img * blob_bytes(DK), blob_bytes(DK), bar);
-    if (NC)  // its low part (x - bf16(x)), B*H images further on
-      bulk_load(sm + L.s2, ws + ((size_t)p.B * p.H + bh) * blob_bytes(DK), blob_bytes(DK), bar);
+    bulk_load(sm + L.s, ws + ((size_t)bh * nch + i) * blob_bytes(DK), blob_bytes(DK), bar);
   }
-  if (DV == 64 && !NC) {
+  if (DV == 64) {
     for (int q = tid; q < 512; q += kBThreads)
       reinterpret_cast<uint4 *>(sm + L.v + 8192)[q] = make_uint4(0, 0, 0, 0);
   }
@@ -516,7 +505,7 @@ chunk_output_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const f
       ebm[tid] = __expf(bmid);
     }
     __syncthreads();
-    if ((elu || gla) && !(NC && tid >= kC)) {  // NC: the q rows only
+    if (elu || gla) {
       const int row = tid;  // row of [Q; K]
       const int r = row & (kC - 1);
       const bool is_k = row >= kC;
@@ -543,7 +532,7 @@ chunk_output_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const f
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0 && !NC) {
+    if (tid == 0) {
       tc_fence_after();
       const uint32_t a_qk = smem_u32(qk);
       constexpr uint32_t idesc = idesc_bf16_f32(128, 64, false, false);
@@ -555,26 +544,13 @@ chunk_output_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const f
       }
       mma_commit(mbar);
     }
-    ok = NC ? true : mbar_wait_bounded(mbar, 0, kSpinLimit);
+    ok = mbar_wait_bounded(mbar, 0, kSpinLimit);
     if (!__syncthreads_and(ok)) {
       if (tid == 0) atomicOr(p.status, kStatusTimeout);
     } else {
       tc_fence_after();
       // ---- masked, decayed scores P (TMEM lanes 0..63); elu+1: q.z
-      if (NC) {
-        if (elu && tid < kC) {  // q.z_total
-          const int r = tid;
-          const float *zp = zws + (size_t)bh * DK;
-          float acc = 0.f;
-          for (int g8 = 0; g8 < DK / 8; ++g8) {
-            float f[8];
-            unpack8(*reinterpret_cast<const uint4 *>(qk + (g8 >> 3) * 16384 + sw128_off(r, (g8 & 7) * 8)), f);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc = fmaf(f[e], __ldg(zp + g8 * 8 + e), acc);
-          }
-          den[r] = acc;
-        }
-      } else if (tid < kC) {
+      if (tid < kC) {
         const int r = tid;
         const float b2r = sgate ? b2[r] : 0.f;
         float rowsum = 0.f;
@@ -625,7 +601,7 @@ chunk_output_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const f
           *reinterpret_cast<uint4 *>(ptr) = pack8(f);
         }
       }
-      if (!NC && elu && tid < kC) den[tid] += qz[tid];
+      if (elu && tid < kC) den[tid] += qz[tid];
       fence_proxy_async();
       tc_fence_before();
       __syncthreads();
@@ -640,23 +616,13 @@ chunk_output_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const f
           const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
           mma_bf16(tbase + kO1, desc_sw128(a_s + ko, 16, 1024), desc_sw128(a_qk + ko, 16, 1024), id_o1, kk > 0);
         }
-        if (NC) {
-          const uint32_t a_s2 = smem_u32(sm + L.s2);
 #pragma unroll
-          for (int kk = 0; kk < DK / 16; ++kk) {
-            const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_bf16(tbase + kO1, desc_sw128(a_s2 + ko, 16, 1024), desc_sw128(a_qk + ko, 16, 1024), id_o1, 1u);
-          }
-        }
-        if (!NC) {
-#pragma unroll
-          for (int kk = 0; kk < kC / 16; ++kk)
-            mma_bf16(tbase + kO2, desc_sw128(a_v + kk * 2048, 8192, 1024), desc_sw128(a_p + kk * 32, 16, 1024),
-                     id_o2, kk > 0);
-        }
+        for (int kk = 0; kk < kC / 16; ++kk)
+          mma_bf16(tbase + kO2, desc_sw128(a_v + kk * 2048, 8192, 1024), desc_sw128(a_p + kk * 32, 16, 1024),
+                   id_o2, kk > 0);
         mma_commit(mbar);
       }
-      ok = mbar_wait_bounded(mbar, NC ? 0 : 1, kSpinLimit);
+      ok = mbar_wait_bounded(mbar, 1, kSpinLimit);
       if (!__syncthreads_and(ok)) {
         if (tid == 0) atomicOr(p.status, kStatusTimeout);
       } else {
@@ -668,12 +634,7 @@ chunk_output_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const f
         for (int r0 = 0; r0 < kC; r0 += 32) {
           float a[32], b[32], f[32];
           tmem_ld32(tl + kO1 + r0, a);
-          if (NC) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) b[e] = 0.f;
-          } else {
-            tmem_ld32(tl + kO2 + r0, b);
-          }
+          tmem_ld32(tl + kO2 + r0, b);
           if (sgate) load32(eb + r0, f);
           if (elu) load32(den + r0, f);
           tmem_wait_ld();
@@ -770,10 +731,10 @@ int launch_kind(const ChunkParams &p, uint8_t *ws, float *zws, cudaStream_t stre
 // o_t = S_total^T q_t with S_total = S0 + sum_s k_s v_s^T over the whole
 // sequence (elu+1: phi on q and k, divided by phi(q).z_total): the
 // right-to-left product Q (K^T V) of the kernel-attention notes, section 3.
-// Three launches: a split-T reduction of V^T K on the
-// tensor cores (one CTA per head and T-range), a finalize pass per head (adds
-// S0 and the partial sums, writes S_final and the bf16 state image), and the
-// output pass above with NC = true (every chunk reads the same image).
+// Three launches: a split-T reduction of V^T K on the tensor cores (one CTA
+// per head and T-range), a parallel finalize (S0 + partial sums -> S_final
+// and a bf16 high/low image of the state), and an output pass whose persistent
+// CTAs stream their run of query chunks through the image of each head.
 constexpr int kNThreads = 128;
 
 struct NLayout {
@@ -914,9 +875,10 @@ nc_sum_kernel(const ChunkParams p, int nsplit, float *__restrict__ part, float *
   ok = __syncthreads_and(ok);
   tc_fence_after();
   if (ok) {
-    // partial S^T of this T-range: thread = TMEM lane = value row
+    // partial S of this T-range, key-major [c][v]: thread = TMEM lane = value row v, so
+    // every store of one key channel is contiguous across the warp
     const int v = tid;
-    float *dst = part + ((size_t)bh * nsplit + sp) * DV * DK + (size_t)v * DK;
+    float *dst = part + ((size_t)bh * nsplit + sp) * DV * DK + v;
 #pragma unroll 1
     for (int cc = 0; cc < DK; cc += 32) {
       float x[32];
@@ -924,8 +886,7 @@ nc_sum_kernel(const ChunkParams p, int nsplit, float *__restrict__ part, float *
       tmem_wait_ld();
       if (v < DV) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          reinterpret_cast<float4 *>(dst + cc)[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+        for (int e = 0; e < 32; ++e) dst[(size_t)(cc + e) * DV] = x[e];
       }
     }
     if (ELU) {  // z partial: reduce the row-strided thread sums per channel
@@ -946,38 +907,252 @@ nc_sum_kernel(const ChunkParams p, int nsplit, float *__restrict__ part, float *
   if (warp == 0) tmem_dealloc(tbase, 128);
 }
 
-// S_total^T = S0^T + sum of the partials; S_final and the bf16 image as a
-// high/low pair (x = hi + lo to about 2^-16; value rows beyond dv zero),
-// elu+1: z_total = z0 + sum of the partial z.
+// S_total = S0 + the partial sums of the key-major partials; S_final, and the
+// bf16 image of S_total^T as a high/low pair (x = hi + lo to about 2^-16) in
+// the output kernel's operand layout (value rows beyond dv zero). One CTA per
+// (head, 16 value rows): the tile goes through shared memory so that both the
+// [c][v] reads and writes and the image rows are contiguous. elu+1: z_total.
+constexpr int kFRows = 16;
+
 template <int DK, int DV, bool ELU>
-__global__ void __launch_bounds__(128)
-nc_finalize_kernel(const ChunkParams p, int nsplit, const float *__restrict__ part, const float *__restrict__ zpart,
-                   uint8_t *__restrict__ img, float *__restrict__ zws) {
-  const int bh = blockIdx.x, c = threadIdx.x;
-  if (c >= DK) return;
+__global__ void __launch_bounds__(256)
+nc_finalize_kernel(const ChunkParams p, int nsplit, const float *__restrict__ part,
+                   const float *__restrict__ zpart, uint8_t *__restrict__ img, float *__restrict__ zws) {
   constexpr int W = DV + (ELU ? 1 : 0);
-  uint8_t *im = img + (size_t)bh * blob_bytes(DK) + (size_t)(c >> 6) * 16384u;
-  const size_t lo_off = (size_t)p.B * p.H * blob_bytes(DK);  // the low parts follow the B*H high images
-  const float *pp = part + (size_t)bh * nsplit * DV * DK + c;
-#pragma unroll 1
-  for (int v = 0; v < 128; ++v) {
+  __shared__ float tile[DK][kFRows + 1];
+  const int bh = blockIdx.x / (128 / kFRows), v0 = (blockIdx.x % (128 / kFRows)) * kFRows;
+  const int tid = threadIdx.x;
+  // sums: thread (c-slot, row) with the row fastest (16 contiguous floats of one channel)
+  for (int i = tid; i < DK * kFRows; i += 256) {
+    const int c = i / kFRows, r = i % kFRows, v = v0 + r;
     float x = 0.f;
     if (v < DV) {
       x = p.S0 ? p.S0[((size_t)bh * DK + c) * W + v] : 0.f;
-      for (int q = 0; q < nsplit; ++q) x += pp[(size_t)q * DV * DK + (size_t)v * DK];
+      const float *pp = part + (size_t)bh * nsplit * DV * DK + (size_t)c * DV + v;
+      for (int q = 0; q < nsplit; ++q) x += pp[(size_t)q * DV * DK];
       if (p.S_final) p.S_final[((size_t)bh * DK + c) * W + v] = x;
     }
-    const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-    *reinterpret_cast<__nv_bfloat16 *>(im + sw128_off(v, c & 63)) = hi;
-    *reinterpret_cast<__nv_bfloat16 *>(im + lo_off + sw128_off(v, c & 63)) =
-        __float2bfloat16_rn(x - __bfloat162float(hi));
+    tile[c][r] = x;
   }
-  if (ELU) {
-    float z = p.S0 ? p.S0[((size_t)bh * DK + c) * W + DV] : 0.f;
-    for (int q = 0; q < nsplit; ++q) z += zpart[((size_t)bh * nsplit + q) * DK + c];
-    zws[(size_t)bh * DK + c] = z;
-    if (p.S_final) p.S_final[((size_t)bh * DK + c) * W + DV] = z;
+  __syncthreads();
+  // image rows v0 .. v0+15: thread writes a 4-byte pair of keys of one row (rows contiguous)
+  const size_t lo_off = (size_t)p.B * p.H * blob_bytes(DK);
+  uint8_t *im = img + (size_t)bh * blob_bytes(DK);
+  for (int i = tid; i < kFRows * (DK / 2); i += 256) {
+    const int r = i / (DK / 2), c = 2 * (i % (DK / 2)), v = v0 + r;
+    const float x0 = tile[c][r], x1 = tile[c + 1][r];
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(x0, x1);
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(x0 - __low2float(hi), x1 - __high2float(hi));
+    const size_t off = (size_t)(c >> 6) * 16384u + sw128_off(v, c & 63);
+    *reinterpret_cast<__nv_bfloat162 *>(im + off) = hi;
+    *reinterpret_cast<__nv_bfloat162 *>(im + lo_off + off) = lo;
   }
+  if (ELU && v0 == 0 && tid < DK) {
+    float z = p.S0 ? p.S0[((size_t)bh * DK + tid) * W + DV] : 0.f;
+    for (int q = 0; q < nsplit; ++q) z += zpart[((size_t)bh * nsplit + q) * DK + tid];
+    zws[(size_t)bh * DK + tid] = z;
+    if (p.S_final) p.S_final[((size_t)bh * DK + tid) * W + DV] = z;
+  }
+}
+
+// Output of the non-causal form: one persistent CTA per SM walks a contiguous
+// run of (head, chunk) pairs. At each new head it takes the head's state
+// image (high and low parts) and z by bulk copies, then per chunk: q tile by
+// TMA (two stages), elu+1: phi(q) and phi(q).z, O^T = S_hi^T Q^T + S_lo^T Q^T
+// on the tensor cores, and o by TMA store.
+constexpr int kOThreads = 128;
+
+struct OLayout {
+  uint32_t shi, slo, q, ot, z, den, bar, total;
+};
+__host__ __device__ inline OLayout o_layout(int dk) {
+  OLayout L;
+  uint32_t o = 0;
+  L.shi = o; o += blob_bytes(dk);
+  L.slo = o; o += blob_bytes(dk);
+  L.q = o; o += 2u * (uint32_t)(dk / 64) * 8192u;  // two stages of the q tile
+  L.ot = o; o += 16384u;
+  L.z = o; o += 512u;
+  L.den = o; o += 256u;
+  L.bar = o; o += 64u;
+  L.total = o;
+  return L;
+}
+
+template <int DK, int DV, bool ELU>
+__global__ void __launch_bounds__(kOThreads, 1)
+nc_out_kernel(const ChunkParams p, const uint8_t *__restrict__ img, const float *__restrict__ zws,
+              const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const OLayout L = o_layout(DK);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = p.T, nch = (T + kC - 1) / kC;
+  const long long total = (long long)p.B * p.H * nch;
+  const long long g0 = (blockIdx.x * total) / gridDim.x, g1 = ((blockIdx.x + 1) * total) / gridDim.x;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bar);
+  uint64_t *qfull = bars, *mdone = bars + 2, *sfull = bars + 3;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 4);
+  float *zs = reinterpret_cast<float *>(sm + L.z), *den = reinterpret_cast<float *>(sm + L.den);
+  auto qstage = [&](int s) { return sm + L.q + (uint32_t)s * (DK / 64) * 8192u; };
+  auto issue = [&](long long g, int s) {
+    const int bh = (int)(g / nch), j = (int)(g % nch);
+    mbar_arrive_expect_tx(&qfull[s], DK * kC * 2u);
+#pragma unroll
+    for (int a = 0; a < DK / 64; ++a) tma_load_3d(qstage(s) + a * 8192, &tm_q, &qfull[s], 64 * a, j * kC, bh);
+  };
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 64);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&qfull[0], 1);
+    mbar_init(&qfull[1], 1);
+    mbar_init(mdone, 1);
+    mbar_init(sfull, 1);
+    fence_mbar_init();
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_o);
+    for (long long g = g0; g < g0 + 2 && g < g1; ++g) issue(g, (int)(g - g0));
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint32_t tl = tbase + (static_cast<uint32_t>(warp * 32) << 16);
+  bool ok = true;
+  int cur_bh = -1, nloads = 0;
+  long long last0 = g0, last1 = g0 + 1;  // thread 0: the last chunk loaded into each stage
+  for (long long g = g0; g < g1; ++g) {
+    const int it = (int)(g - g0), s = it & 1, bh = (int)(g / nch), j = (int)(g % nch);
+    const uint32_t ph = (uint32_t)(it >> 1) & 1u;
+    if (bh != cur_bh) {
+      // the head's state image and z (the previous head's MMAs have completed: each chunk
+      // waits for its own)
+      if (tid == 0 && ok) {
+        const size_t lo_off = (size_t)p.B * p.H * blob_bytes(DK);
+        mbar_arrive_expect_tx(sfull, 2u * blob_bytes(DK) + (ELU ? DK * 4u : 0u));
+        bulk_load(sm + L.shi, img + (size_t)bh * blob_bytes(DK), blob_bytes(DK), sfull);
+        bulk_load(sm + L.slo, img + lo_off + (size_t)bh * blob_bytes(DK), blob_bytes(DK), sfull);
+        if (ELU) bulk_load(zs, zws + (size_t)bh * DK, DK * 4u, sfull);
+        ok = mbar_wait_bounded(sfull, (uint32_t)nloads & 1u, kSpinLimit);
+      }
+      ++nloads;
+      cur_bh = bh;
+    }
+    if (tid == 0 && ok) ok = mbar_wait_bounded(&qfull[s], ph, kSpinLimit);
+    if (!__syncthreads_and(ok)) {  // every thread leaves together
+      ok = false;
+      break;
+    }
+    uint8_t *qt = qstage(s);
+    const int n = min(kC, T - j * kC);
+    if (ELU) {  // phi(q) on rows in [0, n), zero beyond; then phi(q).z per row
+      constexpr int kGroups = DK / 8, kStep = kOThreads / kGroups;
+      const int cg = tid % kGroups;
+#pragma unroll 2
+      for (int r = tid / kGroups; r < kC; r += kStep) {
+        uint4 *ptr = reinterpret_cast<uint4 *>(qt + (uint32_t)(cg >> 3) * 8192u + sw128_off(r, (cg & 7) * 8));
+        float f[8];
+        unpack8(*ptr, f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = (r < n) ? (f[e] > 0.f ? f[e] + 1.f : __expf(f[e])) : 0.f;
+        *ptr = pack8(f);
+      }
+      __syncthreads();
+      if (tid < kC) {
+        float acc = 0.f;
+        for (int g8 = 0; g8 < DK / 8; ++g8) {
+          float f[8];
+          unpack8(*reinterpret_cast<const uint4 *>(qt + (uint32_t)(g8 >> 3) * 8192u + sw128_off(tid, (g8 & 7) * 8)), f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc = fmaf(f[e], zs[g8 * 8 + e], acc);
+        }
+        den[tid] = acc;
+      }
+      fence_proxy_async();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      // O^T = S_hi^T Q^T + S_lo^T Q^T: the image K-major (key blocks 16 KB apart), q K-major (8 KB apart)
+      constexpr uint32_t id = idesc_bf16_f32(128, 64, false, false);
+      const uint32_t a_hi = smem_u32(sm + L.shi), a_lo = smem_u32(sm + L.slo), a_q = smem_u32(qt);
+#pragma unroll
+      for (int kk = 0; kk < DK / 16; ++kk) {
+        const uint32_t ka = (kk >> 2) * 16384 + (kk & 3) * 32, kb = (kk >> 2) * 8192 + (kk & 3) * 32;
+        mma_bf16(tbase, desc_sw128(a_hi + ka, 16, 1024), desc_sw128(a_q + kb, 16, 1024), id, kk > 0 ? 1u : 0u);
+      }
+#pragma unroll
+      for (int kk = 0; kk < DK / 16; ++kk) {
+        const uint32_t ka = (kk >> 2) * 16384 + (kk & 3) * 32, kb = (kk >> 2) * 8192 + (kk & 3) * 32;
+        mma_bf16(tbase, desc_sw128(a_lo + ka, 16, 1024), desc_sw128(a_q + kb, 16, 1024), id, 1u);
+      }
+      mma_commit(mdone);
+      ok = mbar_wait_bounded(mdone, (uint32_t)it & 1u, kSpinLimit);
+      if (ok && g + 2 < g1) {  // the stage is free once the MMAs have read it
+        issue(g + 2, s);
+        if (s == 0) last0 = g + 2; else last1 = g + 2;
+      }
+      if (ok) bulk_wait_read<0>();  // the previous output tile has left the staging buffer
+    }
+    if (!__syncthreads_and(ok)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    {  // epilogue: thread = TMEM lane = value row v; pairs of rows exchanged so each thread writes 4 bytes
+      const int v = tid;
+      const bool odd = lane & 1;
+      uint8_t *ot = sm + L.ot + (uint32_t)(v >> 6) * 8192u;
+#pragma unroll 1
+      for (int r0 = 0; r0 < kC; r0 += 32) {
+        float a[32];
+        tmem_ld32(tl + r0, a);
+        tmem_wait_ld();
+        if (ELU) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) a[e] = __fdividef(a[e], den[r0 + e]);
+        }
+        if (v < DV) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float send = odd ? a[e] : a[e + 1];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+            const int r = r0 + e + (odd ? 1 : 0);
+            const uint32_t w = odd ? pack_bf16(recv, a[e + 1]) : pack_bf16(a[e], recv);
+            *reinterpret_cast<uint32_t *>(ot + sw128_off(r, (v & 63) - (odd ? 1 : 0))) = w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) (void)__shfl_xor_sync(0xffffffffu, a[e], 1);
+        }
+      }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+#pragma unroll
+      for (int a = 0; a < DV / 64; ++a) tma_store_3d(&tm_o, sm + L.ot + a * 8192, 64 * a, j * kC, bh);
+      bulk_commit();
+    }
+  }
+  if (tid == 0) {
+    bulk_wait<0>();
+    if (!ok) {
+      atomicOr(p.status, kStatusTimeout);
+      // loads still in flight land before the CTA leaves (bounded)
+      (void)mbar_wait_bounded(&qfull[0], (uint32_t)((last0 - g0) >> 1) & 1u, 4096);
+      if (g1 - g0 > 1) (void)mbar_wait_bounded(&qfull[1], (uint32_t)((last1 - g0) >> 1) & 1u, 4096);
+      if (nloads > 0) (void)mbar_wait_bounded(sfull, (uint32_t)(nloads - 1) & 1u, 4096);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tbase, 64);
 }
 
 int nc_splits(const ChunkParams &p) {
@@ -996,12 +1171,11 @@ int launch_nc_typed(const ChunkParams &p, uint8_t *ws, cudaStream_t stream) {
   constexpr bool ELU = KIND == kElu1;
   const int BH = p.B * p.H, nch = (p.T + kC - 1) / kC, ns = nc_splits(p);
   uint8_t *img = ws;  // B*H high images, then B*H low images
-  float *zws = reinterpret_cast<float *>(img + 2 * (size_t)BH * blob_bytes(DK));
-  float *part = zws + (size_t)BH * DK;
-  float *zpart = part + (size_t)BH * ns * DV * DK;
+  float *zws = reinterpret_cast<float *>(img + 2 * (size_t)BH * blob_bytes(DK));  // [B*H][dk] z_total
+  float *part = zws + (size_t)BH * DK;  // [B*H][splits][dk][dv] partial S
+  float *zpart = part + (size_t)BH * ns * DV * DK;  // [B*H][splits][dk] partial z (elu+1)
   const NLayout Ln = n_layout(DK, ELU);
-  const BLayout Lb = b_layout(DK, KIND, true);
-  const size_t sn = Ln.total + 1024, sb = Lb.total + 1024;
+  const size_t sn = Ln.total + 1024;
   CUtensorMap mq, mk, mv, mo;
   const bool ok = make_map(&mq, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DK, p.T, BH, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
                   make_map(&mk, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DK, p.T, BH, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
@@ -1013,19 +1187,24 @@ int launch_nc_typed(const ChunkParams &p, uint8_t *ws, cudaStream_t stream) {
   }
   auto ka = nc_sum_kernel<DK, DV, ELU>;
   auto kf = nc_finalize_kernel<DK, DV, ELU>;
-  auto kb = chunk_output_kernel<DK, DV, KIND, true>;
+  auto kb = nc_out_kernel<DK, DV, ELU>;
+  const size_t so = o_layout(DK).total + 1024;
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 148;
+  const long long nout = std::min<long long>((long long)BH * nch, sms);
   cudaError_t e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sn);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sb);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)so);
   if (e == cudaSuccess) {
     ka<<<(unsigned)(BH * ns), kNThreads, sn, stream>>>(p, ns, part, zpart, mk, mv);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) {
-    kf<<<(unsigned)BH, 128, 0, stream>>>(p, ns, part, zpart, img, zws);
+    kf<<<(unsigned)(BH * (128 / kFRows)), 256, 0, stream>>>(p, ns, part, zpart, img, zws);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) {
-    kb<<<(unsigned)((size_t)BH * nch), kBThreads, sb, stream>>>(p, img, zws, mq, mk, mv, mq, mo);
+    kb<<<(unsigned)nout, kOThreads, so, stream>>>(p, img, zws, mq, mo);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) {

@@ -99,7 +99,7 @@ typedef struct CUstream_st *la_stream_t;
  * (elu+1: o_t = S_T^T phi(q_t) / (z_T . phi(q_t))), computed right to left as
  * Q (K^T V) (kernel-attention notes, section 3).
  * S_final is S_T, as in the causal form. Uses a stream-ordered workspace
- * from the library's pool (B*H*dk*(512 + 4 + 4*(dv+1)*splits) bytes). */
+ * from the library's pool (B*H*splits*dk*(dv + 1)*4 bytes, splits <= 2*SMs/(B*H)). */
 #define LA_NONCAUSAL     0x200
 
 /*
