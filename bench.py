@@ -52,6 +52,7 @@ KERNEL_SOURCES = {
     "elu1": [_CS + "la_chunk_ws.cu", _CS + "la_chunk_mat.cu"] + _COMMON,
     "linear_fp32": [_CS + "la_chunk_simt.cu"],
     "noncausal": [_CS + "la_chunk_mat.cu"] + _COMMON,
+    "backward": [_CS + "la_backward.cu", _CS + "la_chunk_ws.cu", _CS + "la_chunk_mat.cu"] + _COMMON,
     "prologue": [_CS + "la_prologue.cu", _CS + "la_sm100.cuh"],
     "prologue_gla": [_CS + "la_prologue.cu", _CS + "la_sm100.cuh"],
 }
@@ -282,6 +283,8 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.workload in workloads.PROLOGUE_WORKLOADS:
         return bench_prologue(args, rank, world, local_rank)
+    if workloads.WORKLOADS[args.workload].extra.get("backward"):
+        return bench_backward(args, rank, world, local_rank)
     wl = workloads.WORKLOADS[args.workload]
     over = {k: getattr(args, k) for k in ("B", "H", "T") if getattr(args, k) is not None}
     if over:
@@ -684,6 +687,182 @@ def bench_prologue(args, rank, world, local_rank):
                        "l2": "inputs larger than L2 (no flush)" if alg > 129e6 else "inputs smaller than L2"},
             "roofline": roof, "cpu_baseline": cpu, "clocks": clk, "e2e": e2e,
             "gpu_launches": args.steps,
+        }), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- backward
+
+BWD_METRIC = "tokens/sec of the chunk backward (dq, dk, dv, dS0) at 1 GB300; % of roofline"
+
+
+def backward_inputs(wl):
+    """The forward workload's inputs plus dO ~ N(0,1)/sqrt(dv) and dS_final ~ N(0, 0.01)."""
+    inp = workloads.make_inputs(wl)
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(wl.seed + 1000)
+    inp["dO"] = (torch.randn(wl.B, wl.H, wl.T, wl.dv, generator=gen) / math.sqrt(wl.dv)).to(wl.torch_dtype)
+    inp["dS"] = torch.randn(wl.B, wl.H, wl.dk, wl.dv, generator=gen) * 0.1
+    return inp
+
+
+def backward_bytes(wl) -> float:
+    """Minimum HBM traffic of one backward call: read q, k, v, dO, write dq, dk, dv
+    once, read dS_final and write dS0."""
+    e = 2 if wl.dtype == "bf16" else 4
+    per_tok = e * (2 * wl.dk + 2 * wl.dv) + e * (2 * wl.dk + wl.dv)
+    return float(wl.B * wl.H * (wl.T * per_tok + 2 * 4 * wl.dk * wl.dv))
+
+
+def time_backward_oracle(wl, inp, target_s: float = 10.0):
+    from oracle.backward import backward
+    f64 = lambda t: None if t is None else t.to(torch.float64).numpy()
+    BH = wl.B * wl.H
+    done, t0 = 0, time.perf_counter()
+    while done < BH and (time.perf_counter() - t0) < target_s:
+        b, h = done // wl.H, done % wl.H
+        sl = lambda t: f64(t[b:b + 1, h:h + 1])
+        backward(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["dO"]), wl.mode,
+                 g=None if inp["g"] is None else f64(inp["g"])[h:h + 1], dS=sl(inp["dS"]))
+        done += 1
+    dt = time.perf_counter() - t0
+    return (done * wl.T / wl.H) / dt, 1, f"{done} of {BH} (batch, head) sequences, full T={wl.T}, float64 numpy", dt
+
+
+def bench_backward(args, rank, world, local_rank):
+    wl = workloads.WORKLOADS[args.workload]
+    over = {k: getattr(args, k) for k in ("B", "H", "T") if getattr(args, k) is not None}
+    if over:
+        wl = wl.with_sizes(**over)
+    B, H, T, dk, dv = wl.B, wl.H, wl.T, wl.dk, wl.dv
+    cfg = {"workload": wl.name, "mode": wl.mode + "+backward", "B": B, "H": H, "T": T, "dk": dk, "dv": dv, "C": wl.C,
+           "global_batch": B * world, "seq_len": T, "parallelism": "replicas" if world > 1 else "single"}
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        inp = backward_inputs(wl)
+        vals = []
+        for i in range(args.warmup + args.steps):
+            v, cores, sample, _ = time_backward_oracle(wl, inp, target_s=3.0)
+            if i >= args.warmup:
+                vals.append(v)
+        value = statistics.mean(vals)
+        print(json.dumps({
+            "impl": "reference", "metric": BWD_METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(B * T / value * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; shapes and distributions of the workload)", "config": cfg,
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }), flush=True)
+        return
+    import gated_delta_rule_linear_gb300 as la
+    from gated_delta_rule_linear_gb300 import build as labuild
+    labuild.build()
+    la.load_library()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    inp = backward_inputs(wl)
+    names = [n for n in ("q", "k", "v", "g", "dO", "dS") if inp[n] is not None]
+    d = {n: inp[n].to(dev) for n in names}
+    outs = {"dq": torch.empty_like(d["q"]), "dk": torch.empty_like(d["k"]), "dv": torch.empty_like(d["v"]),
+            "dS0": torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)}
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    mode_id = la.MODE_IDS[wl.mode] | (la.CONSTANTS["LA_F32"] if wl.dtype == "f32" else 0)
+
+    def step(dd, oo):
+        rc = la.la_chunk_bwd(dd["q"], dd["k"], dd["v"], dd.get("g"), dd["dO"], dd["dS"], None, oo["dq"], oo["dk"],
+                             oo["dv"], oo["dS0"], B, H, T, dk, dv, wl.C, mode_id, sh)
+        if rc != 0:
+            raise RuntimeError(la.la_last_error())
+
+    for _ in range(args.warmup):
+        step(d, outs)
+    torch.cuda.synchronize()
+    if la.la_stream_status(sh) != 0:
+        raise RuntimeError(la.la_last_error())
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[2 * i].record(stream)
+        step(d, outs)
+        ev[2 * i + 1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    launch_ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * B * T * args.steps / (total_ms / 1e3)
+    flop = 3 * B * H * T * flops_per_token_head(wl.mode, dk, dv)
+    alg = backward_bytes(wl)
+    hbm_peak, _, peak_src = read_peaks()
+    achieved = alg / (statistics.mean(launch_ms) / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(achieved / hbm_peak, 4), "traffic": recorded_traffic(wl.name), "peak_source": peak_src,
+            "algorithmic_bytes": alg, "kernel": "3 x chunk forward (dq; dk and dv reversed) + flip_kernel",
+            "launch_ms_mean": round(statistics.mean(launch_ms), 4)}
+    e2e = None
+    if not args.no_e2e:
+        host = {n: inp[n].pin_memory() for n in names}
+        hout = {n: torch.empty_like(outs[n], device="cpu").pin_memory() for n in outs}
+        dd, oo = dict(d), dict(outs)
+        h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+        d2h = sum(hout[n].numel() * hout[n].element_size() for n in outs)
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for n in names:
+                    dd[n].copy_(host[n], non_blocking=True)
+                step(dd, oo)
+                for n in outs:
+                    hout[n].copy_(oo[n], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        steps = max(3, min(args.steps, 10))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+        e2e = {"value": round(world * B * T * steps / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": steps, "ms_per_step": round(ms / steps, 4)}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v_cpu, cores, sample, dt = time_backward_oracle(wl, inp)
+        cpu = {"value": round(v_cpu, 2), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+               "seconds": round(dt, 2)}
+    if rank == 0:
+        cfg["l2"] = "inputs larger than L2 (no flush)" if alg > 129e6 else "inputs smaller than L2"
+        print(json.dumps({
+            "metric": BWD_METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+            "data": "synthetic (seeded; shapes and distributions of the workload)", "config": cfg,
+            "tflops": round(world * flop * args.steps / (total_ms / 1e3) / 1e12, 2), "roofline": roof,
+            "cpu_baseline": cpu, "clocks": clk, "e2e": e2e,
+            "gpu_launches": args.steps * 11,  # state prep, 3 forward passes, 6 reversals, dS0 scaling
         }), flush=True)
     if dist:
         dist.destroy_process_group()

@@ -8,12 +8,13 @@ step, and the prologue in front of it (short convolution, L2 normalisation,
 gate activations). This package is
 only the binding: ctypes marshalling plus a build helper.
 """
-from ._binding import (CONSTANTS, GATE_KINDS, LIB_PATH, MODE_IDS, SIGNATURES, LAError, chunk_fwd,
-                       la_chunk_fwd, la_chunk_fwd_noalloc, la_last_error, la_prologue, la_recurrent_step,
-                       la_stream_status, la_version, load_library, prologue, recurrent_step)
+from ._binding import (CONSTANTS, GATE_KINDS, LIB_PATH, MODE_IDS, SIGNATURES, LAError, chunk_bwd, chunk_fwd,
+                       la_chunk_bwd, la_chunk_fwd, la_chunk_fwd_noalloc, la_last_error, la_prologue,
+                       la_recurrent_step, la_stream_status, la_version, load_library, prologue, recurrent_step)
 from ._binding import *  # noqa: F401,F403  (LA_* constants)
 
-__all__ = ["chunk_fwd", "recurrent_step", "prologue", "la_chunk_fwd", "la_chunk_fwd_noalloc",
+__all__ = ["chunk_fwd", "chunk_bwd", "recurrent_step", "prologue", "la_chunk_fwd", "la_chunk_bwd",
+           "la_chunk_fwd_noalloc",
            "la_prologue", "la_recurrent_step", "GATE_KINDS",
            "la_stream_status", "la_last_error", "la_version", "load_library", "LAError",
            "CONSTANTS", "MODE_IDS", "SIGNATURES", "LIB_PATH"]

@@ -53,6 +53,8 @@ cudaMemPool_t workspace_pool() {
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 }  // namespace
 
+cudaMemPool_t library_pool() { return workspace_pool(); }
+
 void set_error(const char *fmt, ...) {
   va_list ap;
   va_start(ap, fmt);

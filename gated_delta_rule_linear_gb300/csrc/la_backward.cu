@@ -1,0 +1,193 @@
+// la_chunk_bwd: the backward pass of la_chunk_fwd for plain linear attention
+// and RetNet's fixed decay ("Talk Linear Attention" sections 2.1 and 5.2; the
+// states are recomputed, as section 4.1.2 describes, not stored). With
+// alpha = 1 or gamma_h,
+//
+//   dq_t = alpha^(t+1) S0 dO_t + sum_{s<=t} alpha^(t-s) (dO_t . v_s) k_s
+//   dk_s = sum_{t>=s} alpha^(t-s) (dO_t . v_s) q_t + alpha^(T-1-s) dS v_s
+//   dv_s = sum_{t>=s} alpha^(t-s) (q_t . k_s) dO_t + alpha^(T-1-s) dS^T k_s
+//   dS0  = sum_t alpha^(t+1) q_t dO_t^T + alpha^T dS
+//
+// Each line is itself a causal linear attention with the same decay, so the
+// backward runs the forward kernels three times: dq directly (queries dO,
+// keys v, values k, initial state S0^T); dk and dv on the time-reversed
+// sequences (queries v / k, keys dO / q, values q / dO, initial states
+// dS^T / alpha and dS / alpha), and dS0 = alpha times the last pass's final
+// state. This file adds the time reversal and the initial-state preparation.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "la_internal.h"
+
+namespace la {
+namespace {
+
+// out[bh][T-1-t][:] = in[bh][t][:], rows of row_bytes (a multiple of 16)
+__global__ void __launch_bounds__(256) flip_kernel(const uint4 *__restrict__ in, uint4 *__restrict__ out, int T,
+                                                   int row16, long long rows) {
+  const long long n = rows * row16;
+  for (long long i = blockIdx.x * 256ll + threadIdx.x; i < n; i += (long long)gridDim.x * 256) {
+    const long long row = i / row16, c = i % row16;
+    const long long bh = row / T, t = row % T;
+    out[(bh * T + (T - 1 - t)) * row16 + c] = __ldg(in + i);
+  }
+}
+
+// Initial states of the three passes, per head (alpha = exp(g_h) for RetNet, 1 otherwise):
+// s0t = S0^T, dst = dS^T / alpha, dss = dS / alpha   ([B*H][.][.] float32)
+__global__ void __launch_bounds__(256) state_prep_kernel(const float *__restrict__ S0, const float *__restrict__ dS,
+                                                         const float *__restrict__ g, int H, int dk, int dv,
+                                                         float *__restrict__ s0t, float *__restrict__ dst,
+                                                         float *__restrict__ dss) {
+  const int bh = blockIdx.y;
+  const float inv = g ? expf(-__ldg(g + bh % H)) : 1.f;
+  const size_t base = (size_t)bh * dk * dv;
+  for (int i = blockIdx.x * 256 + threadIdx.x; i < dk * dv; i += gridDim.x * 256) {
+    const int c = i / dv, v = i % dv;  // element (c, v) of a [dk][dv] state
+    if (S0) s0t[base + (size_t)v * dk + c] = S0[base + i];
+    if (dS) {
+      const float x = dS[base + i] * inv;
+      dst[base + (size_t)v * dk + c] = x;
+      dss[base + i] = x;
+    }
+  }
+}
+
+// dS0 = alpha * S, per head
+__global__ void __launch_bounds__(256) scale_state_kernel(const float *__restrict__ S, const float *__restrict__ g,
+                                                          int H, int n, float *__restrict__ out) {
+  const int bh = blockIdx.y;
+  const float a = g ? expf(__ldg(g + bh % H)) : 1.f;
+  for (int i = blockIdx.x * 256 + threadIdx.x; i < n; i += gridDim.x * 256)
+    out[(size_t)bh * n + i] = a * S[(size_t)bh * n + i];
+}
+
+bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int flip(const void *in, void *out, int B, int H, int T, int d, size_t esz, cudaStream_t s) {
+  const int row16 = (int)(d * esz / 16);
+  const long long rows = (long long)B * H * T;
+  const long long n = rows * row16;
+  const int blocks = (int)std::min<long long>((n + 255) / 256, 152ll * 16);
+  flip_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4 *>(in), static_cast<uint4 *>(out), T, row16, rows);
+  return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace la
+
+using namespace la;
+
+extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const float *g, const void *dO,
+                            const float *dS_final, const float *S0, void *dq_out, void *dk_out, void *dv_out,
+                            float *dS0, int B, int H, int T, int dk, int dv, int C, int mode, la_stream_t stream) {
+  void *dq = dq_out, *dkg = dk_out, *dvg = dv_out;
+  const int dk_ = dk, dv_ = dv;
+  const char *fn = "la_chunk_bwd";
+  set_error("%s", "");
+  const int kind = mode & 0xff;
+  if (!q || !k || !v || !dO || !dq || !dkg || !dvg) {
+    set_error("%s: q, k, v, dO, dq, dk and dv are required", fn);
+    return LA_ERR_INVALID_ARG;
+  }
+  if (B < 1 || H < 1 || T < 1 || (long long)B * H > 65535) {
+    set_error("%s: need B, H, T >= 1 and B*H <= 65535 (got %d, %d, %d)", fn, B, H, T);
+    return LA_ERR_INVALID_ARG;
+  }
+  if ((dk_ != 64 && dk_ != 128) || (dv_ != 64 && dv_ != 128)) {
+    set_error("%s: dk and dv must be 64 or 128 (got %d, %d)", fn, dk_, dv_);
+    return LA_ERR_UNSUPPORTED;
+  }
+  if ((mode & ~(0xff | LA_F32)) != 0 || (kind != LA_LINEAR && kind != LA_RETNET)) {
+    set_error("%s: mode 0x%x: the backward pass covers LA_LINEAR and LA_RETNET (optionally | LA_F32)", fn, mode);
+    return (mode & ~(0xff | LA_F32)) == 0 && kind >= LA_LINEAR && kind <= LA_KDA ? LA_ERR_UNSUPPORTED
+                                                                                  : LA_ERR_INVALID_ARG;
+  }
+  if ((kind == LA_RETNET) != (g != nullptr)) {
+    set_error("%s: LA_RETNET needs g (float32 [H] log-decay), LA_LINEAR takes none", fn);
+    return LA_ERR_INVALID_ARG;
+  }
+  if (C != 0 && C != 64) {
+    set_error("%s: chunk length C=%d is not implemented in this build (use 0 or 64)", fn, C);
+    return LA_ERR_UNSUPPORTED;
+  }
+  const void *p16[] = {q, k, v, dO, dq, dkg, dvg};
+  for (const void *ptr : p16)
+    if (!al16(ptr)) {
+      set_error("%s: q, k, v, dO, dq, dk and dv must be 16-byte aligned", fn);
+      return LA_ERR_INVALID_ARG;
+    }
+  if ((S0 && !al16(S0)) || (dS_final && !al16(dS_final)) || (dS0 && !al16(dS0)) || (g && !al16(g))) {
+    set_error("%s: S0, dS_final, dS0 and g must be 16-byte aligned", fn);
+    return LA_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t esz = (mode & LA_F32) ? 4 : 2;
+  const size_t BHT = (size_t)B * H * T, BH = (size_t)B * H;
+  // workspace: reversed q, k, v, dO; reversed dk, dv; three initial states; the last pass's final state
+  const size_t n_q = BHT * dk_ * esz, n_v = BHT * dv_ * esz, n_s = BH * dk_ * dv_ * 4;
+  const size_t bytes = 3 * n_q + 3 * n_v + 4 * n_s;
+  uint8_t *ws = nullptr;
+  cudaMemPool_t pool = library_pool();
+  if (!pool) {
+    set_error("%s: could not create the workspace pool: %s", fn, cudaGetErrorString(cudaGetLastError()));
+    return LA_ERR_CUDA;
+  }
+  cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&ws), bytes, pool, s);
+  if (e != cudaSuccess) {
+    set_error("%s: workspace allocation of %zu bytes failed: %s", fn, bytes, cudaGetErrorString(e));
+    return LA_ERR_CUDA;
+  }
+  uint8_t *q_r = ws, *k_r = q_r + n_q, *dk_r = k_r + n_q, *v_r = dk_r + n_q, *dO_r = v_r + n_v, *dv_r = dO_r + n_v;
+  float *s0t = reinterpret_cast<float *>(dv_r + n_v), *dst = s0t + BH * dk_ * dv_, *dss = dst + BH * dk_ * dv_,
+        *sfin = dss + BH * dk_ * dv_;
+  int rc = LA_OK;
+  auto fail = [&](const char *what) {
+    if (rc == LA_OK) {
+      set_error("%s: %s failed: %s", fn, what, la_last_error()[0] ? la_last_error() : cudaGetErrorString(cudaGetLastError()));
+      rc = LA_ERR_CUDA;
+    }
+  };
+  if (S0 || dS_final) {
+    state_prep_kernel<<<dim3(8, (unsigned)BH), 256, 0, s>>>(S0, dS_final, g, H, dk_, dv_, s0t, dst, dss);
+    if (cudaGetLastError() != cudaSuccess) fail("initial-state preparation");
+  }
+  const int fwd_mode = mode & (0xff | LA_F32);
+  // dq: queries dO, keys v, values k (key width dv, value width dk), initial state S0^T
+  if (rc == LA_OK) {
+    const int r = la_chunk_fwd(dO, v, k, g, nullptr, dq, S0 ? s0t : nullptr, nullptr, B, H, T, dv_, dk_, C, fwd_mode,
+                               stream);
+    if (r != LA_OK) {
+      rc = r;
+    }
+  }
+  if (rc == LA_OK && (flip(q, q_r, B, H, T, dk_, esz, s) || flip(k, k_r, B, H, T, dk_, esz, s) ||
+                      flip(v, v_r, B, H, T, dv_, esz, s) || flip(dO, dO_r, B, H, T, dv_, esz, s)))
+    fail("time reversal");
+  // dk (reversed): queries v_r, keys dO_r, values q_r, initial state dS^T / alpha
+  if (rc == LA_OK) {
+    const int r = la_chunk_fwd(v_r, dO_r, q_r, g, nullptr, dk_r, dS_final ? dst : nullptr, nullptr, B, H, T, dv_, dk_, C,
+                               fwd_mode, stream);
+    if (r != LA_OK) rc = r;
+  }
+  // dv (reversed): queries k_r, keys q_r, values dO_r, initial state dS / alpha; its final state / alpha = dS0
+  if (rc == LA_OK) {
+    const int r = la_chunk_fwd(k_r, q_r, dO_r, g, nullptr, dv_r, dS_final ? dss : nullptr, dS0 ? sfin : nullptr, B, H,
+                               T, dk_, dv_, C, fwd_mode, stream);
+    if (r != LA_OK) rc = r;
+  }
+  if (rc == LA_OK && (flip(dk_r, dkg, B, H, T, dk_, esz, s) || flip(dv_r, dvg, B, H, T, dv_, esz, s)))
+    fail("time reversal of dk, dv");
+  if (rc == LA_OK && dS0) {
+    scale_state_kernel<<<dim3(8, (unsigned)BH), 256, 0, s>>>(sfin, g, H, dk_ * dv_, dS0);
+    if (cudaGetLastError() != cudaSuccess) fail("dS0 scaling");
+  }
+  e = cudaFreeAsync(ws, s);
+  if (rc == LA_OK && e != cudaSuccess) {
+    set_error("%s: workspace release failed: %s", fn, cudaGetErrorString(e));
+    rc = LA_ERR_CUDA;
+  }
+  return rc;
+}

@@ -47,6 +47,10 @@ struct StepParams {
   int f32;
 };
 
+// The library's stream-ordered workspace pool on the current device (keeps
+// freed memory for the next call), or null if it cannot be created.
+cudaMemPool_t library_pool();
+
 // Thread-local error message for la_last_error().
 void set_error(const char *fmt, ...);
 

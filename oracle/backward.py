@@ -1,0 +1,68 @@
+"""Float64 oracle of the backward pass of the causal forward, for the modes
+whose decay is not a learned input: plain linear attention and RetNet's fixed
+per-head decay.
+
+TEST INFRASTRUCTURE ONLY. Nothing in the product path imports this module;
+only tests/ and bench.py's CPU legs do. It shares no code with the CUDA path.
+
+Forward, per (b, h), with alpha = 1 (linear) or gamma_h = exp(g_h) (RetNet):
+
+  S_t = alpha S_{t-1} + k_t v_t^T,  o_t = S_t^T q_t,  S_final = S_{T-1}
+  so  o_t = alpha^(t+1) S0^T q_t + sum_{s<=t} alpha^(t-s) (q_t . k_s) v_s
+      S_final = alpha^T S0 + sum_s alpha^(T-1-s) k_s v_s^T
+
+("Talk Linear Attention" sections 2.1 and 5.2; section 4.1.2 of the same page
+notes that the backward pass recomputes the chunk states rather than storing
+them).
+Given dO = dL/do and dS = dL/dS_final, the gradients are the plain sums
+
+  dq_t = alpha^(t+1) S0 dO_t + sum_{s<=t} alpha^(t-s) (dO_t . v_s) k_s
+  dk_s = sum_{t>=s} alpha^(t-s) (dO_t . v_s) q_t + alpha^(T-1-s) dS v_s
+  dv_s = sum_{t>=s} alpha^(t-s) (q_t . k_s) dO_t + alpha^(T-1-s) dS^T k_s
+  dS0  = sum_t alpha^(t+1) q_t dO_t^T + alpha^T dS
+
+written out below with explicit decay matrices (no reordering beyond the sums).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = ["backward"]
+
+
+def backward(q, k, v, dO, mode, g=None, S0=None, dS=None):
+    """q, k [B,H,T,dk]; v, dO [B,H,T,dv]; g [H] log-decay for retnet; S0, dS
+    [B,H,dk,dv] or None. Returns dq, dk, dv, dS0 (float64)."""
+    q, k, v, dO = (np.asarray(x, dtype=np.float64) for x in (q, k, v, dO))
+    B, H, T, dkk = q.shape
+    dvv = v.shape[-1]
+    if mode == "linear":
+        logs = np.zeros(H)
+    elif mode == "retnet":
+        logs = np.asarray(g, dtype=np.float64).reshape(H)
+    else:
+        raise ValueError(f"backward is defined here for linear and retnet, not {mode}")
+    S0 = np.zeros((B, H, dkk, dvv)) if S0 is None else np.asarray(S0, dtype=np.float64)
+    dS = np.zeros((B, H, dkk, dvv)) if dS is None else np.asarray(dS, dtype=np.float64)
+    t = np.arange(T)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    dS0 = np.zeros_like(S0)
+    for h in range(H):
+        la = logs[h]
+        # D[t, s] = alpha^(t-s) for s <= t, else 0
+        diff = t[:, None] - t[None, :]
+        D = np.where(diff >= 0, np.exp(la * np.maximum(diff, 0)), 0.0)
+        a_t1 = np.exp(la * (t + 1))        # alpha^(t+1)
+        a_last = np.exp(la * (T - 1 - t))  # alpha^(T-1-s)
+        aT = np.exp(la * T)
+        for b in range(B):
+            Q, K, V, G = q[b, h], k[b, h], v[b, h], dO[b, h]
+            Mo = (G @ V.T) * D                  # [t, s] = alpha^(t-s) (dO_t . v_s), s <= t
+            Mk = (Q @ K.T) * D                  # [t, s] = alpha^(t-s) (q_t . k_s)
+            dq[b, h] = a_t1[:, None] * (G @ S0[b, h].T) + Mo @ K
+            dk[b, h] = Mo.T @ Q + a_last[:, None] * (V @ dS[b, h].T)
+            dv[b, h] = Mk.T @ G + a_last[:, None] * (K @ dS[b, h])
+            dS0[b, h] = (Q * a_t1[:, None]).T @ G + aT * dS[b, h]
+    return dq, dk, dv, dS0

@@ -30,7 +30,7 @@ def _declared_functions():
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    assert names == sorted(["la_chunk_fwd", "la_chunk_fwd_noalloc", "la_recurrent_step",
+    assert names == sorted(["la_chunk_fwd", "la_chunk_fwd_noalloc", "la_chunk_bwd", "la_recurrent_step",
                             "la_prologue", "la_stream_status", "la_last_error", "la_version"])
     assert set(names) == set(la.SIGNATURES)
 
@@ -173,3 +173,32 @@ def test_prologue_rejects_bad_arguments(lib, kw, code):
     rc, msg = _pro(**kw)
     assert rc == la.CONSTANTS[code], (rc, msg)
     assert msg.startswith("la_prologue")
+
+
+# ---- la_chunk_bwd argument checks (host only) -------------------------------
+
+def _bwd(**kw):
+    args = dict(q=A, k=A, v=A, g=None, dO=A, dS_final=None, S0=None, dq_out=A, dk_out=A, dv_out=A, dS0=None,
+                B=1, H=1, T=64, dk=128, dv=128, C=0, mode=la.LA_LINEAR, stream=None)
+    args.update(kw)
+    rc = la.la_chunk_bwd(**args)
+    return rc, la.la_last_error()
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dO=None), "LA_ERR_INVALID_ARG"),
+    (dict(dv_out=None), "LA_ERR_INVALID_ARG"),
+    (dict(T=0), "LA_ERR_INVALID_ARG"),
+    (dict(dk=96), "LA_ERR_UNSUPPORTED"),
+    (dict(mode=5), "LA_ERR_UNSUPPORTED"),             # gdn: no backward in this build
+    (dict(mode=9), "LA_ERR_INVALID_ARG"),
+    (dict(mode=2), "LA_ERR_INVALID_ARG"),             # retnet needs g
+    (dict(g=A), "LA_ERR_INVALID_ARG"),                # linear takes none
+    (dict(C=128), "LA_ERR_UNSUPPORTED"),
+    (dict(dq_out=A + 8), "LA_ERR_INVALID_ARG"),
+    (dict(dS0=A + 4), "LA_ERR_INVALID_ARG"),
+])
+def test_chunk_bwd_rejects_bad_arguments(lib, kw, code):
+    rc, msg = _bwd(**kw)
+    assert rc == la.CONSTANTS[code], (rc, msg)
+    assert msg.startswith("la_chunk_bwd")

@@ -1,0 +1,87 @@
+"""Pins of the backward oracle (linear, RetNet) to gradients computed another
+way: central finite differences of the float64 token recurrence on tiny
+inputs, and reverse-mode automatic differentiation (torch.autograd, float64)
+of a separately written step-by-step recurrence. The last test plants
+mistakes and checks that the pins catch them. CPU only."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import recurrence
+from oracle.backward import backward
+
+RNG = np.random.default_rng(5)
+
+
+def _case(mode, B=1, H=2, T=9, dk=3, dv=4):
+    q = RNG.standard_normal((B, H, T, dk)) * 0.5
+    k = RNG.standard_normal((B, H, T, dk)) * 0.5
+    v = RNG.standard_normal((B, H, T, dv))
+    g = np.log(np.array([0.9, 0.6])[:H]) if mode == "retnet" else None
+    S0 = RNG.standard_normal((B, H, dk, dv)) * 0.3
+    dO = RNG.standard_normal((B, H, T, dv))
+    dS = RNG.standard_normal((B, H, dk, dv))
+    return q, k, v, g, S0, dO, dS
+
+
+def _loss(q, k, v, g, S0, dO, dS, mode):
+    o, S = recurrence(q, k, v, mode, g=g, S0=S0)
+    return float(np.sum(o * dO) + np.sum(S * dS))
+
+
+@pytest.mark.parametrize("mode", ["linear", "retnet"])
+def test_backward_matches_finite_differences(mode):
+    q, k, v, g, S0, dO, dS = _case(mode)
+    dq, dk, dv, dS0 = backward(q, k, v, dO, mode, g=g, S0=S0, dS=dS)
+    eps = 1e-6
+    for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv), ("S0", S0, dS0)):
+        num = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            old = x[idx]
+            x[idx] = old + eps
+            lp = _loss(q, k, v, g, S0, dO, dS, mode)
+            x[idx] = old - eps
+            lm = _loss(q, k, v, g, S0, dO, dS, mode)
+            x[idx] = old
+            num[idx] = (lp - lm) / (2 * eps)
+        assert np.allclose(grad, num, rtol=1e-6, atol=1e-7), name
+
+
+def _torch_recurrence(q, k, v, g, S0, mode):
+    """A step-by-step recurrence in torch (float64), written for autograd."""
+    B, H, T, dk = q.shape
+    S = S0.clone()
+    outs = []
+    alpha = torch.ones(H, dtype=torch.float64) if mode == "linear" else torch.exp(g)
+    for t in range(T):
+        S = alpha[None, :, None, None] * S + k[:, :, t, :, None] * v[:, :, t, None, :]
+        outs.append(torch.einsum("bhc,bhcv->bhv", q[:, :, t], S))
+    return torch.stack(outs, dim=2), S
+
+
+@pytest.mark.parametrize("mode", ["linear", "retnet"])
+def test_backward_matches_autograd(mode):
+    q, k, v, g, S0, dO, dS = _case(mode, B=2, H=2, T=40, dk=5, dv=6)
+    tq, tk, tv, tS0 = (torch.tensor(x, requires_grad=True) for x in (q, k, v, S0))
+    tg = None if g is None else torch.tensor(g)
+    o, S = _torch_recurrence(tq, tk, tv, tg, tS0, mode)
+    (o * torch.tensor(dO)).sum().add((S * torch.tensor(dS)).sum()).backward()
+    dq, dk, dv, dS0 = backward(q, k, v, dO, mode, g=g, S0=S0, dS=dS)
+    for name, a, b in (("q", dq, tq.grad), ("k", dk, tk.grad), ("v", dv, tv.grad), ("S0", dS0, tS0.grad)):
+        assert np.allclose(a, b.numpy(), rtol=1e-11, atol=1e-11), name
+
+
+def test_planted_mistakes_are_caught():
+    q, k, v, g, S0, dO, dS = _case("retnet", T=12)
+    tq, tk, tv, tS0 = (torch.tensor(x, requires_grad=True) for x in (q, k, v, S0))
+    o, S = _torch_recurrence(tq, tk, tv, torch.tensor(g), tS0, "retnet")
+    (o * torch.tensor(dO)).sum().add((S * torch.tensor(dS)).sum()).backward()
+    dq, dk, dv, dS0 = backward(q, k, v, dO, "retnet", g=g, S0=S0, dS=dS)
+    assert np.allclose(dk, tk.grad.numpy(), atol=1e-10)
+    # a decay applied the wrong way round (alpha^(s-t)), and the final-state term dropped
+    bad_dk, _, _, _ = backward(q, k, v, dO, "retnet", g=-np.asarray(g), S0=S0, dS=dS)
+    _, bad2, _, _ = backward(q, k, v, dO, "retnet", g=g, S0=S0, dS=None)
+    assert not np.allclose(bad_dk, tk.grad.numpy(), atol=1e-6)
+    assert not np.allclose(bad2, tk.grad.numpy(), atol=1e-6)

@@ -84,6 +84,11 @@ WORKLOADS = {
     # and q/k/v distribution, no gates.
     "noncausal": Workload("noncausal", "linear", 8, 16, 4096, 128, 128, "bf16", 64, seed=8,
                           qkv_scale=1.0 / math.sqrt(128.0), extra={"noncausal": True}),
+    # Backward pass of the RetNet workload (a next row): q, k, v as retnet; the
+    # output gradient dO ~ N(0,1)/sqrt(128) and dS_final ~ N(0, 0.01), drawn
+    # after S0 by bench.py's backward leg from the same generator recipe.
+    "backward": Workload("backward", "retnet", 8, 16, 4096, 128, 128, "bf16", 64, seed=9,
+                         qkv_scale=1.0 / math.sqrt(128.0), extra={"backward": True}),
 }
 
 
