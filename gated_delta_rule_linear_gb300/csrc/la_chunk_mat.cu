@@ -955,15 +955,16 @@ nc_finalize_kernel(const ChunkParams p, int nsplit, const float *__restrict__ pa
   }
 }
 
-// Output of the non-causal form: one persistent CTA per SM walks a contiguous
-// run of (head, chunk) pairs. At each new head it takes the head's state
-// image (high and low parts) and z by bulk copies, then per chunk: q tile by
-// TMA (two stages), elu+1: phi(q) and phi(q).z, O^T = S_hi^T Q^T + S_lo^T Q^T
-// on the tensor cores, and o by TMA store.
+// Output of the non-causal form: persistent CTAs (two per SM) each walk a
+// contiguous run of (head, chunk) pairs. At each new head a CTA takes the
+// head's state image (high and low parts) and z by bulk copies, then per
+// chunk: q tile by TMA (two stages), elu+1: phi(q) and phi(q).z,
+// O^T = S_hi^T Q^T + S_lo^T Q^T on the tensor cores, and o stored straight
+// from registers (pairs of rows exchanged between lanes: 4-byte stores).
 constexpr int kOThreads = 128;
 
 struct OLayout {
-  uint32_t shi, slo, q, ot, z, den, bar, total;
+  uint32_t shi, slo, q, z, den, bar, total;
 };
 __host__ __device__ inline OLayout o_layout(int dk) {
   OLayout L;
@@ -971,7 +972,6 @@ __host__ __device__ inline OLayout o_layout(int dk) {
   L.shi = o; o += blob_bytes(dk);
   L.slo = o; o += blob_bytes(dk);
   L.q = o; o += 2u * (uint32_t)(dk / 64) * 8192u;  // two stages of the q tile
-  L.ot = o; o += 16384u;
   L.z = o; o += 512u;
   L.den = o; o += 256u;
   L.bar = o; o += 64u;
@@ -980,9 +980,9 @@ __host__ __device__ inline OLayout o_layout(int dk) {
 }
 
 template <int DK, int DV, bool ELU>
-__global__ void __launch_bounds__(kOThreads, 1)
+__global__ void __launch_bounds__(kOThreads, 2)
 nc_out_kernel(const ChunkParams p, const uint8_t *__restrict__ img, const float *__restrict__ zws,
-              const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o) {
+              const __grid_constant__ CUtensorMap tm_q) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const OLayout L = o_layout(DK);
@@ -1012,7 +1012,6 @@ nc_out_kernel(const ChunkParams p, const uint8_t *__restrict__ img, const float 
     mbar_init(sfull, 1);
     fence_mbar_init();
     prefetch_tmap(&tm_q);
-    prefetch_tmap(&tm_o);
     for (long long g = g0; g < g0 + 2 && g < g1; ++g) issue(g, (int)(g - g0));
   }
   tc_fence_before();
@@ -1095,7 +1094,6 @@ nc_out_kernel(const ChunkParams p, const uint8_t *__restrict__ img, const float 
         issue(g + 2, s);
         if (s == 0) last0 = g + 2; else last1 = g + 2;
       }
-      if (ok) bulk_wait_read<0>();  // the previous output tile has left the staging buffer
     }
     if (!__syncthreads_and(ok)) {
       ok = false;
@@ -1105,7 +1103,7 @@ nc_out_kernel(const ChunkParams p, const uint8_t *__restrict__ img, const float 
     {  // epilogue: thread = TMEM lane = value row v; pairs of rows exchanged so each thread writes 4 bytes
       const int v = tid;
       const bool odd = lane & 1;
-      uint8_t *ot = sm + L.ot + (uint32_t)(v >> 6) * 8192u;
+      __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(p.o) + ((size_t)bh * T + (size_t)j * kC) * DV;
 #pragma unroll 1
       for (int r0 = 0; r0 < kC; r0 += 32) {
         float a[32];
@@ -1122,7 +1120,7 @@ nc_out_kernel(const ChunkParams p, const uint8_t *__restrict__ img, const float 
             const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
             const int r = r0 + e + (odd ? 1 : 0);
             const uint32_t w = odd ? pack_bf16(recv, a[e + 1]) : pack_bf16(a[e], recv);
-            *reinterpret_cast<uint32_t *>(ot + sw128_off(r, (v & 63) - (odd ? 1 : 0))) = w;
+            if (r < n) *reinterpret_cast<uint32_t *>(og + (size_t)r * DV + v - (odd ? 1 : 0)) = w;
           }
         } else {
 #pragma unroll
@@ -1130,17 +1128,9 @@ nc_out_kernel(const ChunkParams p, const uint8_t *__restrict__ img, const float 
         }
       }
     }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-#pragma unroll
-      for (int a = 0; a < DV / 64; ++a) tma_store_3d(&tm_o, sm + L.ot + a * 8192, 64 * a, j * kC, bh);
-      bulk_commit();
-    }
+    tc_fence_before();  // the TMEM reads are done before the next chunk's MMAs overwrite it
   }
   if (tid == 0) {
-    bulk_wait<0>();
     if (!ok) {
       atomicOr(p.status, kStatusTimeout);
       // loads still in flight land before the CTA leaves (bounded)
@@ -1192,7 +1182,7 @@ int launch_nc_typed(const ChunkParams &p, uint8_t *ws, cudaStream_t stream) {
   int sms = 0, dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 148;
-  const long long nout = std::min<long long>((long long)BH * nch, sms);
+  const long long nout = std::min<long long>((long long)BH * nch, 2LL * sms);
   cudaError_t e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sn);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)so);
   if (e == cudaSuccess) {
@@ -1204,7 +1194,7 @@ int launch_nc_typed(const ChunkParams &p, uint8_t *ws, cudaStream_t stream) {
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) {
-    kb<<<(unsigned)nout, kOThreads, so, stream>>>(p, img, zws, mq, mo);
+    kb<<<(unsigned)nout, kOThreads, so, stream>>>(p, img, zws, mq);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) {
