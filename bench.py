@@ -53,6 +53,7 @@ KERNEL_SOURCES = {
     "linear_fp32": [_CS + "la_chunk_simt.cu"],
     "noncausal": [_CS + "la_chunk_mat.cu"] + _COMMON,
     "backward": [_CS + "la_backward.cu", _CS + "la_chunk_ws.cu", _CS + "la_chunk_mat.cu"] + _COMMON,
+    "decode": [_CS + "la_step.cu"],
     "prologue": [_CS + "la_prologue.cu", _CS + "la_sm100.cuh"],
     "prologue_gla": [_CS + "la_prologue.cu", _CS + "la_sm100.cuh"],
 }
@@ -285,6 +286,8 @@ def main():
         return bench_prologue(args, rank, world, local_rank)
     if workloads.WORKLOADS[args.workload].extra.get("backward"):
         return bench_backward(args, rank, world, local_rank)
+    if workloads.WORKLOADS[args.workload].extra.get("decode"):
+        return bench_decode(args, rank, world, local_rank)
     wl = workloads.WORKLOADS[args.workload]
     over = {k: getattr(args, k) for k in ("B", "H", "T") if getattr(args, k) is not None}
     if over:
@@ -863,6 +866,170 @@ def bench_backward(args, rank, world, local_rank):
             "tflops": round(world * flop * args.steps / (total_ms / 1e3) / 1e12, 2), "roofline": roof,
             "cpu_baseline": cpu, "clocks": clk, "e2e": e2e,
             "gpu_launches": args.steps * 11,  # state prep, 3 forward passes, 6 reversals, dS0 scaling
+        }), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- decode
+
+DEC_METRIC = "tokens/sec of one decode step (la_recurrent_step, states resident) at 1 GB300; % of roofline"
+
+
+def decode_bytes(wl) -> float:
+    """Minimum HBM traffic of one step: read and write every head's state once,
+    read q, k, v and the gates, write o."""
+    e = 2 if wl.dtype == "bf16" else 4
+    W = wl.dv + 1 if wl.mode == "elu1" else wl.dv
+    per_head = 2 * 4 * wl.dk * W + e * (2 * wl.dk + 2 * wl.dv) + 8
+    return float(wl.B * wl.H * per_head)
+
+
+def bench_decode(args, rank, world, local_rank):
+    wl = workloads.WORKLOADS[args.workload]
+    over = {k: getattr(args, k) for k in ("B", "H") if getattr(args, k) is not None}
+    if over:
+        wl = wl.with_sizes(**over)
+    B, H, dk, dv = wl.B, wl.H, wl.dk, wl.dv
+    inp = workloads.make_inputs(wl)
+    sq = lambda t: None if t is None else t[:, :, 0].contiguous() if t.dim() >= 3 else t
+    step_in = {"q": sq(inp["q"]), "k": sq(inp["k"]), "v": sq(inp["v"]),
+               "g": None if inp["g"] is None else inp["g"][:, :, 0].contiguous(),
+               "beta": None if inp["beta"] is None else inp["beta"][:, :, 0].contiguous()}
+    cfg = {"workload": wl.name, "mode": wl.mode + "+decode", "B": B, "H": H, "dk": dk, "dv": dv,
+           "global_batch": B * world, "seq_len": 1, "parallelism": "replicas" if world > 1 else "single"}
+
+    def time_cpu(target_s):
+        import numpy as np
+        from oracle import recurrence
+        f64 = lambda t: None if t is None else t.to(torch.float64).numpy()
+        BH, done, t0 = B * H, 0, time.perf_counter()
+        while done < BH and time.perf_counter() - t0 < target_s:
+            b, h = done // H, done % H
+            sl = lambda t: None if t is None else f64(t[b:b + 1, h:h + 1])
+            recurrence(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), wl.mode, g=sl(inp["g"]), beta=sl(inp["beta"]),
+                       S0=sl(inp["S0"]))
+            done += 1
+        dt = time.perf_counter() - t0
+        return (done / H) / dt, 1, f"{done} of {BH} (batch, head) one-token steps, float64 numpy", dt
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        vals = []
+        for i in range(args.warmup + args.steps):
+            v, cores, sample, _ = time_cpu(1.0)
+            if i >= args.warmup:
+                vals.append(v)
+        value = statistics.mean(vals)
+        print(json.dumps({
+            "impl": "reference", "metric": DEC_METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(B / value * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; shapes and distributions of the workload)", "config": cfg,
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }), flush=True)
+        return
+    import gated_delta_rule_linear_gb300 as la
+    from gated_delta_rule_linear_gb300 import build as labuild
+    labuild.build()
+    la.load_library()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    names = [n for n in ("q", "k", "v", "g", "beta") if step_in[n] is not None]
+    d = {n: step_in[n].to(dev) for n in names}
+    S = inp["S0"].to(dev).contiguous()
+    o = torch.empty(B, H, dv, dtype=wl.torch_dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    mode_id = la.MODE_IDS[wl.mode] | (la.CONSTANTS["LA_F32"] if wl.dtype == "f32" else 0)
+
+    def step(dd, oo):
+        rc = la.la_recurrent_step(dd["q"], dd["k"], dd["v"], dd.get("g"), dd.get("beta"), oo, S, B, H, dk, dv,
+                                  mode_id, sh)
+        if rc != 0:
+            raise RuntimeError(la.la_last_error())
+
+    for _ in range(args.warmup):
+        step(d, o)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    steps = max(args.steps, 50)  # a step is ~20 us: enough of them to time
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(steps):
+        ev[2 * i].record(stream)
+        step(d, o)
+        ev[2 * i + 1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    launch_ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(steps)]
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * B * steps / (total_ms / 1e3)
+    alg = decode_bytes(wl)
+    hbm_peak, _, peak_src = read_peaks()
+    achieved = alg / (statistics.mean(launch_ms) / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(achieved / hbm_peak, 4), "traffic": recorded_traffic(wl.name), "peak_source": peak_src,
+            "algorithmic_bytes": alg, "kernel": "step_kernel", "launch_ms_mean": round(statistics.mean(launch_ms), 4)}
+    e2e = None
+    if not args.no_e2e:
+        host = {n: step_in[n].pin_memory() for n in names}
+        o_h = torch.empty(B, H, dv, dtype=wl.torch_dtype).pin_memory()
+        dd = dict(d)
+        h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+        d2h = o_h.numel() * o_h.element_size()
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for n in names:
+                    dd[n].copy_(host[n], non_blocking=True)
+                step(dd, o)
+                o_h.copy_(o, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+        e2e = {"value": round(world * B * steps / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": steps, "ms_per_step": round(ms / steps, 4)}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v_cpu, cores, sample, dt = time_cpu(10.0)
+        cpu = {"value": round(v_cpu, 2), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+               "seconds": round(dt, 2)}
+    if rank == 0:
+        cfg["l2"] = ("state larger than L2 (no flush)" if alg > 129e6 else
+                     "state smaller than L2: successive steps may hit L2")
+        print(json.dumps({
+            "metric": DEC_METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": round(total_ms / steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+            "data": "synthetic (seeded; shapes and distributions of the workload)", "config": cfg,
+            "roofline": roof, "cpu_baseline": cpu, "clocks": clk, "e2e": e2e, "gpu_launches": steps,
         }), flush=True)
     if dist:
         dist.destroy_process_group()

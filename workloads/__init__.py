@@ -89,6 +89,11 @@ WORKLOADS = {
     # after S0 by bench.py's backward leg from the same generator recipe.
     "backward": Workload("backward", "retnet", 8, 16, 4096, 128, 128, "bf16", 64, seed=9,
                          qkv_scale=1.0 / math.sqrt(128.0), extra={"backward": True}),
+    # One Gated DeltaNet decode step (la_recurrent_step) for a batch of 128
+    # sequences x 16 heads with resident states: the gdn recipe with T = 1
+    # and a random state S ~ N(0, 0.01).
+    "decode": Workload("decode", "gdn", 128, 16, 1, 128, 128, "bf16", 64, seed=10,
+                       l2norm_qk=True, s0=True, extra={"decode": True}),
 }
 
 
