@@ -124,6 +124,22 @@ def algorithmic_bytes(wl, has_s0: bool) -> float:
     return float(B * H * (T * per_tok + state))
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest of x over all ranks (the job is as slow as its slowest
+    replica); x itself with a single process."""
+    if not dist:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput of `world` replicas that each processed
+    units_per_rank in ms milliseconds (the max over ranks)."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -354,13 +370,10 @@ def main():
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
     launch_ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
     ms_per_step = total_ms / args.steps
     tokens_per_step = B * T
-    value = world * tokens_per_step * args.steps / (total_ms / 1e3)
+    value = replica_throughput(tokens_per_step * args.steps, world, total_ms)
     flop_call = B * H * T * flops_per_token_head("noncausal" if is_noncausal(wl) else wl.mode, dk, dv)
     tflops = world * flop_call * args.steps / (total_ms / 1e3) / 1e12
     avg_launch_s = statistics.mean(launch_ms) / 1e3
@@ -461,10 +474,7 @@ def run_e2e(la, wl, inp, dev, stream, mode_id, args, world, dist):
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
     return {"value": round(world * B * T * steps / (ms / 1e3), 1), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
             "ms_per_step": round(ms / steps, 4)}
@@ -628,11 +638,8 @@ def bench_prologue(args, rank, world, local_rank):
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
     launch_ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * B * T * args.steps / (total_ms / 1e3)
+    total_ms = max_over_ranks(total_ms, dist, dev)
+    value = replica_throughput(B * T * args.steps, world, total_ms)
     alg = prologue_bytes(wl)
     hbm_peak, _, peak_src = read_peaks()
     achieved = alg / (statistics.mean(launch_ms) / 1e3) / 1e9
@@ -809,11 +816,8 @@ def bench_backward(args, rank, world, local_rank):
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
     launch_ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * B * T * args.steps / (total_ms / 1e3)
+    total_ms = max_over_ranks(total_ms, dist, dev)
+    value = replica_throughput(B * T * args.steps, world, total_ms)
     flop = 3 * B * H * T * flops_per_token_head(wl.mode, dk, dv)
     alg = backward_bytes(wl)
     hbm_peak, _, peak_src = read_peaks()
@@ -978,11 +982,8 @@ def bench_decode(args, rank, world, local_rank):
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
     launch_ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(steps)]
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * B * steps / (total_ms / 1e3)
+    total_ms = max_over_ranks(total_ms, dist, dev)
+    value = replica_throughput(B * steps, world, total_ms)
     alg = decode_bytes(wl)
     hbm_peak, _, peak_src = read_peaks()
     achieved = alg / (statistics.mean(launch_ms) / 1e3) / 1e9
