@@ -824,7 +824,7 @@ def bench_backward(args, rank, world, local_rank):
     achieved = alg / (statistics.mean(launch_ms) / 1e3) / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
             "frac": round(achieved / hbm_peak, 4), "traffic": recorded_traffic(wl.name), "peak_source": peak_src,
-            "algorithmic_bytes": alg, "kernel": "3 x chunk forward (dq; dk and dv reversed) + flip_kernel",
+            "algorithmic_bytes": alg, "kernel": "3 x chunk_ws_kernel (dq causal; dk and dv reversed runs)",
             "launch_ms_mean": round(statistics.mean(launch_ms), 4)}
     e2e = None
     if not args.no_e2e:
@@ -869,7 +869,7 @@ def bench_backward(args, rank, world, local_rank):
             "data": "synthetic (seeded; shapes and distributions of the workload)", "config": cfg,
             "tflops": round(world * flop * args.steps / (total_ms / 1e3) / 1e12, 2), "roofline": roof,
             "cpu_baseline": cpu, "clocks": clk, "e2e": e2e,
-            "gpu_launches": args.steps * 11,  # state prep, 3 forward passes, 6 reversals, dS0 scaling
+            "gpu_launches": args.steps * 5,  # state prep, 3 forward passes, dS0 scaling
         }), flush=True)
     if dist:
         dist.destroy_process_group()

@@ -13,7 +13,9 @@
 // keys v, values k, initial state S0^T); dk and dv on the time-reversed
 // sequences (queries v / k, keys dO / q, values q / dO, initial states
 // dS^T / alpha and dS / alpha), and dS0 = alpha times the last pass's final
-// state. This file adds the time reversal and the initial-state preparation.
+// state. The reversed passes are the forward kernels' reversed runs, which
+// read and write the tensors in stored order, so nothing is copied; this file
+// adds the initial-state preparation.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -23,17 +25,6 @@
 
 namespace la {
 namespace {
-
-// out[bh][T-1-t][:] = in[bh][t][:], rows of row_bytes (a multiple of 16)
-__global__ void __launch_bounds__(256) flip_kernel(const uint4 *__restrict__ in, uint4 *__restrict__ out, int T,
-                                                   int row16, long long rows) {
-  const long long n = rows * row16;
-  for (long long i = blockIdx.x * 256ll + threadIdx.x; i < n; i += (long long)gridDim.x * 256) {
-    const long long row = i / row16, c = i % row16;
-    const long long bh = row / T, t = row % T;
-    out[(bh * T + (T - 1 - t)) * row16 + c] = __ldg(in + i);
-  }
-}
 
 // Initial states of the three passes, per head (alpha = exp(g_h) for RetNet, 1 otherwise):
 // s0t = S0^T, dst = dS^T / alpha, dss = dS / alpha   ([B*H][.][.] float32)
@@ -66,13 +57,16 @@ __global__ void __launch_bounds__(256) scale_state_kernel(const float *__restric
 
 bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int flip(const void *in, void *out, int B, int H, int T, int d, size_t esz, cudaStream_t s) {
-  const int row16 = (int)(d * esz / 16);
-  const long long rows = (long long)B * H * T;
-  const long long n = rows * row16;
-  const int blocks = (int)std::min<long long>((n + 255) / 256, 152ll * 16);
-  flip_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4 *>(in), static_cast<uint4 *>(out), T, row16, rows);
-  return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+// The forward recurrence over the time-reversed sequence, through the
+// kernels' reversed runs (tensor cores for bf16, CUDA cores for float32).
+int run_reversed(const void *q, const void *k, const void *v, const float *g, void *o, const float *S0,
+                 float *S_final, int B, int H, int T, int dk, int dv, int kind, bool f32, cudaStream_t s) {
+  ChunkParams p{q, k, v, g, nullptr, o, S0, S_final, B, H, T, dk, dv, 64, kind, f32 ? 1 : 0, status_word(), 1};
+  if (!p.status) {
+    set_error("la_chunk_bwd: no CUDA device available (%s)", cudaGetErrorString(cudaGetLastError()));
+    return LA_ERR_CUDA;
+  }
+  return f32 ? launch_chunk_simt(p, s) : launch_chunk_ws(p, s);
 }
 
 }  // namespace
@@ -124,11 +118,11 @@ extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const f
     return LA_ERR_INVALID_ARG;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const size_t esz = (mode & LA_F32) ? 4 : 2;
-  const size_t BHT = (size_t)B * H * T, BH = (size_t)B * H;
-  // workspace: reversed q, k, v, dO; reversed dk, dv; three initial states; the last pass's final state
-  const size_t n_q = BHT * dk_ * esz, n_v = BHT * dv_ * esz, n_s = BH * dk_ * dv_ * 4;
-  const size_t bytes = 3 * n_q + 3 * n_v + 4 * n_s;
+  const bool f32 = (mode & LA_F32) != 0;
+  const size_t BH = (size_t)B * H;
+  // workspace: three initial states and the last pass's final state
+  const size_t n_s = BH * dk_ * dv_ * 4;
+  const size_t bytes = 4 * n_s;
   uint8_t *ws = nullptr;
   cudaMemPool_t pool = library_pool();
   if (!pool) {
@@ -140,8 +134,7 @@ extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const f
     set_error("%s: workspace allocation of %zu bytes failed: %s", fn, bytes, cudaGetErrorString(e));
     return LA_ERR_CUDA;
   }
-  uint8_t *q_r = ws, *k_r = q_r + n_q, *dk_r = k_r + n_q, *v_r = dk_r + n_q, *dO_r = v_r + n_v, *dv_r = dO_r + n_v;
-  float *s0t = reinterpret_cast<float *>(dv_r + n_v), *dst = s0t + BH * dk_ * dv_, *dss = dst + BH * dk_ * dv_,
+  float *s0t = reinterpret_cast<float *>(ws), *dst = s0t + BH * dk_ * dv_, *dss = dst + BH * dk_ * dv_,
         *sfin = dss + BH * dk_ * dv_;
   int rc = LA_OK;
   auto fail = [&](const char *what) {
@@ -163,23 +156,13 @@ extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const f
       rc = r;
     }
   }
-  if (rc == LA_OK && (flip(q, q_r, B, H, T, dk_, esz, s) || flip(k, k_r, B, H, T, dk_, esz, s) ||
-                      flip(v, v_r, B, H, T, dv_, esz, s) || flip(dO, dO_r, B, H, T, dv_, esz, s)))
-    fail("time reversal");
-  // dk (reversed): queries v_r, keys dO_r, values q_r, initial state dS^T / alpha
-  if (rc == LA_OK) {
-    const int r = la_chunk_fwd(v_r, dO_r, q_r, g, nullptr, dk_r, dS_final ? dst : nullptr, nullptr, B, H, T, dv_, dk_, C,
-                               fwd_mode, stream);
-    if (r != LA_OK) rc = r;
-  }
-  // dv (reversed): queries k_r, keys q_r, values dO_r, initial state dS / alpha; its final state / alpha = dS0
-  if (rc == LA_OK) {
-    const int r = la_chunk_fwd(k_r, q_r, dO_r, g, nullptr, dv_r, dS_final ? dss : nullptr, dS0 ? sfin : nullptr, B, H,
-                               T, dk_, dv_, C, fwd_mode, stream);
-    if (r != LA_OK) rc = r;
-  }
-  if (rc == LA_OK && (flip(dk_r, dkg, B, H, T, dk_, esz, s) || flip(dv_r, dvg, B, H, T, dv_, esz, s)))
-    fail("time reversal of dk, dv");
+  // dk (reversed run): queries v, keys dO, values q, initial state dS^T / alpha
+  if (rc == LA_OK)
+    rc = run_reversed(v, dO, q, g, dkg, dS_final ? dst : nullptr, nullptr, B, H, T, dv_, dk_, kind, f32, s);
+  // dv (reversed run): queries k, keys q, values dO, initial state dS / alpha; its final state / alpha = dS0
+  if (rc == LA_OK)
+    rc = run_reversed(k, q, dO, g, dvg, dS_final ? dss : nullptr, dS0 ? sfin : nullptr, B, H, T, dk_, dv_, kind, f32,
+                      s);
   if (rc == LA_OK && dS0) {
     scale_state_kernel<<<dim3(8, (unsigned)BH), 256, 0, s>>>(sfin, g, H, dk_ * dv_, dS0);
     if (cudaGetLastError() != cudaSuccess) fail("dS0 scaling");

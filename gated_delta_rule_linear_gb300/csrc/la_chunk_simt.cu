@@ -19,6 +19,9 @@
 //
 // All arithmetic is float32; this kernel is the float32-input path and is
 // written for clarity over speed (the bf16 path runs on the tensor cores).
+// With p.rev it runs the same recurrence over the stored sequence read from
+// its end (token t is memory row T-1-t, for every input and the output): the
+// anti-causal passes of the backward.
 #include <cuda_bf16.h>
 
 #include "la_internal.h"
@@ -96,6 +99,8 @@ chunk_simt_kernel(const ChunkParams p, int tile_w) {
   const Tin *k = static_cast<const Tin *>(p.k) + (size_t)bh * T * dk;
   const Tin *v = static_cast<const Tin *>(p.v) + (size_t)bh * T * dv;
   Tin *o = static_cast<Tin *>(p.o) + (size_t)bh * T * dv;
+  // memory row of token t: reversed runs walk the stored sequence from its end
+  const auto row = [&](int t) { return (size_t)(p.rev ? T - 1 - t : t); };
 
   // Initial state slice.
   for (int i = tid; i < dk * W; i += kThreads) {
@@ -116,8 +121,8 @@ chunk_simt_kernel(const ChunkParams p, int tile_w) {
       const int r = i / dk, c = i % dk;
       float qv = 0.f, kv = 0.f;
       if (r < n) {
-        qv = ld_in(q + (size_t)(t0 + r) * dk + c);
-        kv = ld_in(k + (size_t)(t0 + r) * dk + c);
+        qv = ld_in(q + row(t0 + r) * dk + c);
+        kv = ld_in(k + row(t0 + r) * dk + c);
         if (elu) { qv = phi(qv); kv = phi(kv); }
       }
       Q[r * L.pk + c] = qv;
@@ -126,23 +131,23 @@ chunk_simt_kernel(const ChunkParams p, int tile_w) {
     for (int i = tid; i < kC * W; i += kThreads) {
       const int r = i / W, j = i % W;
       float x = 0.f;
-      if (r < n) x = (j < wv) ? ld_in(v + (size_t)(t0 + r) * dv + j0 + j) : 1.f;
+      if (r < n) x = (j < wv) ? ld_in(v + row(t0 + r) * dv + j0 + j) : 1.f;
       V[r * L.pw + j] = x;
     }
     if (gla) {
       for (int i = tid; i < kC * dk; i += kThreads) {
         const int r = i / dk, c = i % dk;
-        Bg[i] = (r < n) ? __ldg(p.g + ((size_t)bh * T + t0 + r) * dk + c) : 0.f;
+        Bg[i] = (r < n) ? __ldg(p.g + ((size_t)bh * T + row(t0 + r)) * dk + c) : 0.f;
       }
     } else if (tid < kC) {
       const int r = tid;
       float lg = 0.f;
       if (r < n) {
         if (kind == kRetnet) lg = __ldg(p.g + h);
-        else if (kind == kScalar || (kind == kGdn && p.g)) lg = __ldg(p.g + (size_t)bh * T + t0 + r);
+        else if (kind == kScalar || (kind == kGdn && p.g)) lg = __ldg(p.g + (size_t)bh * T + row(t0 + r));
       }
       Bg[r] = lg;
-      bet[r] = (r < n) ? (p.beta ? __ldg(p.beta + (size_t)bh * T + t0 + r) : 1.f) : 0.f;
+      bet[r] = (r < n) ? (p.beta ? __ldg(p.beta + (size_t)bh * T + row(t0 + r)) : 1.f) : 0.f;
     }
     __syncthreads();
     // ---- inclusive log-gate prefix ----
@@ -239,7 +244,7 @@ chunk_simt_kernel(const ChunkParams p, int tile_w) {
       if (r >= n) continue;
       float x = O[r * L.pw + j];
       if (elu) x = x / O[r * L.pw + wv];
-      st_out(o + (size_t)(t0 + r) * dv + j0 + j, x);
+      st_out(o + row(t0 + r) * dv + j0 + j, x);
     }
     // ---- state passing ----
     for (int i = tid; i < dk * W; i += kThreads) {

@@ -19,6 +19,14 @@
 // halves for the state update, and divides o by q.z + P 1 (kernel-attention
 // notes, sections 13-14).
 //
+// REV (plain linear attention and RetNet) runs the same recurrence over the
+// time-reversed sequence without copying it: chunk j is the 64-row window
+// ending at row T-1-64j of the stored tensors (its TMA load may start above
+// row 0, where the fill is zero), and its smem row m is reversed row 63-m.
+// The per-row gate factors are written to the slots of the smem rows, the
+// masks become s >= r, and o lands in stored order, so the anti-causal passes
+// of the backward read and write q, k, v, dO, dk, dv where they are.
+//
 // Roles (384 threads):
 //   warp 0      TMA producer: q/k/v (and GLA gate) tiles into an ns-stage ring
 //   warp 1      issues the score MMA of each chunk
@@ -99,13 +107,14 @@ __host__ __device__ inline WsLayout ws_layout(int dk, int kind, int ns) {
   return L;
 }
 
-template <int DK, int DV, int KIND>
+template <int DK, int DV, int KIND, bool REV>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_o) {
   constexpr bool elu = KIND == kElu1, gla = KIND == kGla;
   constexpr bool sgate = KIND == kRetnet || KIND == kScalar;
+  static_assert(!REV || KIND == kLinear || KIND == kRetnet, "reversed runs: unit-write, per-head decay only");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const WsLayout L = ws_layout(DK, KIND, ns);
@@ -177,7 +186,7 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
     int issued = 0;
     for (int j = 0; j < nchunks; ++j) {
       const int s = j % ns;
-      const int t0 = j * kC;
+      const int t0 = REV ? T - (j + 1) * kC : j * kC;  // first stored row of the tile
       int ok = 1;
       // per-chunk scalars first (their slot frees after the chunk kNM back has
       // been written out), so the gate loads overlap the wait for a stage
@@ -185,7 +194,7 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       if (sgate) {
         float *ms = mslot(j);
-        const int t = t0 + lane;
+        const int t = j * kC + lane;  // position in the (possibly reversed) sequence
         float g0, g1;
         if (KIND == kRetnet) {
           const float g = __ldg(p.g + h);
@@ -204,14 +213,16 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
         }
         v1 += __shfl_sync(0xffffffffu, v0, 31);
         const float bl = __shfl_sync(0xffffffffu, v1, 31);
-        ms[kMsB2 + lane] = v0;
-        ms[kMsB2 + lane + 32] = v1;
-        ms[kMsEB + lane] = exp2f(v0);
-        ms[kMsEB + lane + 32] = exp2f(v1);
-        ms[kMsF + lane] = exp2f(v0 - bl);
-        ms[kMsF + lane + 32] = exp2f(v1 - bl);
-        ms[kMsVS + lane] = exp2f(bl - v0);
-        ms[kMsVS + lane + 32] = exp2f(bl - v1);
+        // slots are indexed by the tile's smem row (reversed: row 63 - r)
+        const int m0 = REV ? kC - 1 - lane : lane, m1 = REV ? kC / 2 - 1 - lane : lane + 32;
+        ms[kMsB2 + m0] = v0;
+        ms[kMsB2 + m1] = v1;
+        ms[kMsEB + m0] = exp2f(v0);
+        ms[kMsEB + m1] = exp2f(v1);
+        ms[kMsF + m0] = exp2f(v0 - bl);
+        ms[kMsF + m1] = exp2f(v1 - bl);
+        ms[kMsVS + m0] = exp2f(bl - v0);
+        ms[kMsVS + m1] = exp2f(bl - v1);
         if (lane == 0) {
           ms[kMsDec] = exp2f(bl);
           ms[kMsB2L] = bl;
@@ -235,8 +246,9 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
         if (gla) tma_load_3d(st + L.g, &tm_g, &full[s], 0, t0, bh);
         if (sgate) mbar_arrive(&full[s]);  // the gate prefix of this chunk is in place
         // the load of chunk j + ns waits for this chunk's last MMA; warm L2 now
-        if (j + ns < nchunks) {
-          const int tp = t0 + ns * kC;
+        // (a prefetch is a hint: the reversed run skips a window that starts above row 0)
+        if (j + ns < nchunks && (!REV || t0 - ns * kC >= 0)) {
+          const int tp = REV ? t0 - ns * kC : t0 + ns * kC;
 #pragma unroll
           for (int a = 0; a < DK / 64; ++a) {
             tma_prefetch_3d(&tm_q, 64 * a, tp, bh);
@@ -381,7 +393,12 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
         if (!group_all(ok, kBarSG)) { alive = false; break; }
         tc_fence_after();
         uint8_t *ot = sm + L.ot + (uint32_t)(v >> 6) * 8192u;
-        __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(p.o) + ((size_t)bh * T + (size_t)c * kC) * DV;
+        // first stored row of the tile; a reversed window that starts above row 0
+        // (the last one when 64 does not divide T) is written row by row, since a
+        // TMA store may not start at a negative coordinate
+        const int t0c = REV ? T - (c + 1) * kC : c * kC;
+        const bool staged = staged_out(KIND) && (!REV || t0c >= 0);
+        __nv_bfloat16 *obh = static_cast<__nv_bfloat16 *>(p.o) + (size_t)bh * T * DV;
         const bool odd = lane & 1;
 #pragma unroll 1
         for (int r0 = 0; r0 < kC; r0 += 32) {
@@ -412,21 +429,21 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
               const int r = r0 + e + (odd ? 1 : 0);
               const int col = v - (odd ? 1 : 0);
               const uint32_t w = odd ? pack_bf16(recv, a[e + 1]) : pack_bf16(a[e], recv);
-              if (staged_out(KIND))
+              if (staged)
                 *reinterpret_cast<uint32_t *>(ot + sw128_off(r, col & 63)) = w;
-              else if (r < n)
-                *reinterpret_cast<uint32_t *>(og + (size_t)r * DV + col) = w;
+              else if (REV ? r >= kC - n : r < n)
+                *reinterpret_cast<uint32_t *>(obh + (size_t)(t0c + r) * DV + col) = w;
             }
           }
         }
-        if (staged_out(KIND)) fence_proxy_async();
+        if (staged) fence_proxy_async();
         tc_fence_before();
         group_sync(kBarSG);
         if (v == 0) {
-          if (staged_out(KIND)) {
+          if (staged) {
 #pragma unroll
             for (int a = 0; a < DV / 64; ++a)
-              tma_store_3d(&tm_o, sm + L.ot + a * 8192, 64 * a, c * kC, bh);
+              tma_store_3d(&tm_o, sm + L.ot + a * 8192, 64 * a, t0c, bh);
             bulk_commit();
           }
           mbar_arrive(&o_free[ob]);
@@ -570,10 +587,13 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int sc = s0 + e;
-            float x = (sc <= r && r < n) ? d[e] : 0.f;
+            // causal: s <= r and r a real row; reversed (smem rows): s >= r and r in the
+            // last n rows of the window
+            const bool keep = REV ? (sc >= r && r >= kC - n) : (sc <= r && r < n);
+            float x = keep ? d[e] : 0.f;
             // fast path: P' = Q K^T e^{b_r - b_last} against e^{b_last - b_s} V;
             // exact path: P = Q K^T e^{b_r - b_s} against Kt = e^{b_last - b_s} K
-            if (sgate) x *= fast ? fr : exp2f(sc <= r ? b2r - b2s[e] : 0.f);
+            if (sgate) x *= fast ? fr : exp2f(keep ? b2r - b2s[e] : 0.f);
             if (elu) {
               x = __bfloat162float(__float2bfloat16_rn(x));
               rowsum += x;
@@ -669,7 +689,7 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
   if (warp == 3) tmem_dealloc(tbase, kTmemCols);
 }
 
-template <int DK, int DV, int KIND>
+template <int DK, int DV, int KIND, bool REV>
 int launch_typed(const ChunkParams &p, cudaStream_t stream) {
   int ns = 3;
   WsLayout L = ws_layout(DK, KIND, ns);
@@ -698,7 +718,7 @@ int launch_typed(const ChunkParams &p, cudaStream_t stream) {
     set_error("la_chunk_fwd: cuTensorMapEncodeTiled rejected a tensor map");
     return LA_ERR_CUDA;
   }
-  auto kern = chunk_ws_kernel<DK, DV, KIND>;
+  auto kern = chunk_ws_kernel<DK, DV, KIND, REV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess) {
     kern<<<BH, kThreads, smem, stream>>>(p, ns, mq, mk, mv, mg, mo);
@@ -711,12 +731,12 @@ int launch_typed(const ChunkParams &p, cudaStream_t stream) {
   return LA_OK;
 }
 
-template <int KIND>
+template <int KIND, bool REV = false>
 int launch_kind(const ChunkParams &p, cudaStream_t stream) {
-  if (p.dk == 128 && p.dv == 128) return launch_typed<128, 128, KIND>(p, stream);
-  if (p.dk == 128 && p.dv == 64) return launch_typed<128, 64, KIND>(p, stream);
-  if (p.dk == 64 && p.dv == 128) return launch_typed<64, 128, KIND>(p, stream);
-  return launch_typed<64, 64, KIND>(p, stream);
+  if (p.dk == 128 && p.dv == 128) return launch_typed<128, 128, KIND, REV>(p, stream);
+  if (p.dk == 128 && p.dv == 64) return launch_typed<128, 64, KIND, REV>(p, stream);
+  if (p.dk == 64 && p.dv == 128) return launch_typed<64, 128, KIND, REV>(p, stream);
+  return launch_typed<64, 64, KIND, REV>(p, stream);
 }
 
 }  // namespace
@@ -725,6 +745,12 @@ int launch_chunk_ws(const ChunkParams &p, cudaStream_t stream) {
   if (!encode_fn()) {
     set_error("la_chunk_fwd: cuTensorMapEncodeTiled is unavailable");
     return LA_ERR_CUDA;
+  }
+  if (p.rev) {
+    if (p.kind == kLinear) return launch_kind<kLinear, true>(p, stream);
+    if (p.kind == kRetnet) return launch_kind<kRetnet, true>(p, stream);
+    set_error("la_chunk_fwd: the reversed run covers plain linear attention and RetNet only (mode %d)", p.kind);
+    return LA_ERR_UNSUPPORTED;
   }
   switch (p.kind) {
     case kLinear: return launch_kind<kLinear>(p, stream);

@@ -35,6 +35,8 @@ struct ChunkParams {
   int kind;
   int f32;          // 1: q/k/v/o are float32, 0: bfloat16
   unsigned *status; // device status word
+  int rev;          // 1: run on the time-reversed sequence (row t of q, k, v, o is token T-1-t);
+                    // the unit-write kernels (linear and RetNet) and the float32 kernel only
 };
 
 struct StepParams {

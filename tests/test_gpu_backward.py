@@ -1,7 +1,10 @@
 """GPU parity of la_chunk_bwd (linear and RetNet; three chunk-forward passes,
-two on time-reversed copies) with the float64 backward oracle, through the C
-ABI, at the library's tolerance (bf16: max-abs 2e-2 and relative Frobenius
-5e-3; fp32: relative 1e-4) on dq, dk, dv and dS0."""
+two of them the kernels' reversed runs over the stored tensors) with the
+float64 backward oracle, through the C ABI, at the library's tolerance (bf16:
+max-abs 2e-2 and relative Frobenius 5e-3; fp32: relative 1e-4) on dq, dk, dv
+and dS0. Lengths that 64 does not divide put the last reversed window above
+row 0 (zero-filled rows, row-by-row output); 700 tokens wrap the kernels'
+three-stage ring several times."""
 import numpy as np
 import pytest
 import torch
@@ -44,8 +47,8 @@ def _run(mode, q, k, v, g, dO, S0, dS):
 
 @pytest.mark.parametrize("mode", ["linear", "retnet"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("dims", [(128, 128), (64, 128), (128, 64)])
-@pytest.mark.parametrize("T", [1, 64, 200])
+@pytest.mark.parametrize("dims", [(128, 128), (64, 128), (128, 64), (64, 64)])
+@pytest.mark.parametrize("T", [1, 64, 129, 200, 700])
 def test_backward_parity(mode, dtype, dims, T):
     dk, dv = dims
     q, k, v, g, dO, S0, dS = _case(mode, dtype, 2, 3, T, dk, dv, s0=True, ds=True)
