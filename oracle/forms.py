@@ -137,13 +137,18 @@ def chunk_form(q, k, v, mode, g=None, beta=None, S0=None, C=64):
     kda takes the per-channel prefix of gla into the delta rule: the factors
     e^{b} act channel by channel, A_rs = beta_r sum_c k_rc k_sc e^{b_rc - b_sc},
     U = T (diag(beta) V - diag(beta) (K ⊙ e^b) S), S <- Diag(e^{b_last}) S + Kt^T U.
+    outer adds the value-axis prefix bv (log beta): each value column v is a
+    decay e^{bv_r - bv_s} of its own, so V is divided by e^{bv} before the
+    products and O multiplied by it after, and the state decays by
+    e^{b_last} on the key axis and e^{bv_last} on the value axis.
       O  = Qt S + P U                         (inter-chunk + local, section 3.2)
       S <- Diag(exp(b_last)) S + Kt^T U       (state passing, section 3.2)
     elu1 applies phi to q and k first and divides by Qt z + P 1, carrying
     z <- z + sum phi(k). C=1 reduces this to the recurrence and C=T to the
     parallel form (section 3.3).
 
-    g: retnet scalar log gamma for this head; scalar/gdn [T]; gla/kda [T, dk].
+    g: retnet scalar log gamma for this head; scalar/gdn [T]; gla/kda/outer [T, dk];
+    outer takes the value-axis log-gates [T, dv] in beta.
     Returns (o [T, dv], S [dk, dv] or [dk, dv + 1] for elu1).
     """
     q = np.asarray(q, dtype=np.float64)
@@ -170,13 +175,13 @@ def chunk_form(q, k, v, mode, g=None, beta=None, S0=None, C=64):
             lg = np.full(n, float(g))
         elif mode in ("scalar",) or (mode == "gdn" and g is not None):
             lg = np.asarray(g[t0:t1], dtype=np.float64)
-        elif mode in ("gla", "kda"):
+        elif mode in ("gla", "kda", "outer"):
             lg = np.asarray(g[t0:t1], dtype=np.float64)
         else:
             lg = np.zeros(n)
         b = np.cumsum(lg, axis=0)
         tril = np.tril(np.ones((n, n)))
-        if mode in ("gla", "kda"):
+        if mode in ("gla", "kda", "outer"):
             P = ((Q * np.exp(b)) @ (K * np.exp(-b)).T) * tril
             Qt = Q * np.exp(b)
             Kt = K * np.exp(b[-1][None, :] - b)
@@ -196,15 +201,23 @@ def chunk_form(q, k, v, mode, g=None, beta=None, S0=None, C=64):
             A = np.tril(bet[:, None] * ((K * np.exp(b)) @ (K * np.exp(-b)).T), -1)
             rhs = bet[:, None] * (V - (K * np.exp(b)) @ S)
             U = solve_triangular(np.eye(n) + A, rhs, lower=True, unit_diagonal=True)
+        elif mode == "outer":
+            bv = np.cumsum(np.asarray(beta[t0:t1], dtype=np.float64), axis=0)   # [n, dv]
+            U = V * np.exp(-bv)
         else:
             U = V
         O = Qt @ S + P @ U
+        if mode == "outer":
+            O = O * np.exp(bv)
         if mode == "elu1":
             den = Qt @ z + P.sum(1)
             O = O / den[:, None]
             z = z + K.sum(0)
         o[t0:t1] = O
-        S = decay * S + Kt.T @ U
+        if mode == "outer":  # decay of both axes to the chunk end
+            S = decay * np.exp(bv[-1])[None, :] * S + Kt.T @ (U * np.exp(bv[-1])[None, :])
+        else:
+            S = decay * S + Kt.T @ U
     if mode == "elu1":
         S = np.concatenate([S, z[:, None]], axis=1)
     return o, S

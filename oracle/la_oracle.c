@@ -21,6 +21,9 @@
  *                   (Gated DeltaNet: decay, then the delta rule)
  *   mode 6 kda    : S = Diag(alpha_t) S; u = beta_t (v - S^T k); S += k u^T
  *                   (Kimi Delta Attention: per-key-channel gate g[b,h,t,c])
+ *   mode 7 outer  : S = (alpha_t beta_t^T) ⊙ S + k v^T, g[b,h,t,c] = log alpha,
+ *                   beta[b,h,t,j] = log beta (outer-product gate,
+ *                   "Talk Linear Attention" 5.4)
  *
  * Layouts: q,k [B,H,T,dk], v,o [B,H,T,dv], S0/S [B,H,dk,W] with W = dv+1 for
  * elu1 (z in column dv) and W = dv otherwise. g/beta/S0 may be NULL where the
@@ -83,6 +86,13 @@ static void run_head(const job_t *J, int bh) {
                 double a = exp(gt[c]);
                 for (int j = 0; j < dv; ++j) S[(size_t)c * dv + j] *= a;
             }
+        } else if (mode == 7) {
+            const double *gt = J->g + ((size_t)bh * T + t) * dk;
+            const double *bt = J->beta + ((size_t)bh * T + t) * dv;
+            for (int c = 0; c < dk; ++c) {
+                double a = exp(gt[c]);
+                for (int j = 0; j < dv; ++j) S[(size_t)c * dv + j] *= a * exp(bt[j]);
+            }
         }
         /* write */
         if (mode == 5 || mode == 6) {
@@ -130,9 +140,10 @@ static void *worker(void *arg) {
 int la_oracle_fwd(const double *q, const double *k, const double *v, const double *g,
                   const double *beta, const double *S0, double *o, double *S,
                   int B, int H, int T, int dk, int dv, int mode, int nthreads) {
-    if (!q || !k || !v || !o || B < 1 || H < 1 || T < 0 || dk < 1 || dv < 1 || mode < 0 || mode > 6)
+    if (!q || !k || !v || !o || B < 1 || H < 1 || T < 0 || dk < 1 || dv < 1 || mode < 0 || mode > 7)
         return -1;
-    if ((mode == 2 || mode == 3 || mode == 4 || mode == 6) && !g) return -1;
+    if ((mode == 2 || mode == 3 || mode == 4 || mode == 6 || mode == 7) && !g) return -1;
+    if (mode == 7 && !beta) return -1;
     const int BH = B * H;
     if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
     if (nthreads < 1) nthreads = 1;

@@ -32,11 +32,17 @@ Per (b, h), starting from S0 (zero when absent), for t = 0..T-1:
           S_t = (I - beta k k^T) Diag(alpha_t) S_{t-1} + beta k v^T in this
           key-major orientation; "LLM attention optimisation" page, Kimi Delta
           Attention section)
+  outer   S <- (alpha_t beta_t^T) ⊙ S + k_t v_t^T  o_t = S^T q_t
+          (gate G_t = alpha_t beta_t^T, an outer product of a key-axis and a
+          value-axis gate: the form "Talk Linear Attention" section 5.4 gives
+          for gated linear attention that stays a matrix product; alpha_t
+          scales row c of S, beta_t column v)
 
 Gates are natural logs: alpha = exp(g). retnet takes g of shape [H]; scalar
 and gdn take [B, H, T]; gla and kda take [B, H, T, dk]. gdn and kda take beta
 [B, H, T]; a missing g means alpha = 1 (plain DeltaNet, gdn only) and a
-missing beta means 1.
+missing beta means 1. outer takes g = log alpha [B, H, T, dk] and, in the
+beta argument, log beta [B, H, T, dv] (both required).
 
 For elu1 the state carries z as an extra value column: S has shape
 [dk, dv + 1] with z in column dv, both in S0 and in the returned state.
@@ -52,7 +58,7 @@ import numpy as np
 
 __all__ = ["recurrence", "phi_elu1", "MODES"]
 
-MODES = ("linear", "elu1", "retnet", "gla", "scalar", "gdn", "kda")
+MODES = ("linear", "elu1", "retnet", "gla", "scalar", "gdn", "kda", "outer")
 
 
 def phi_elu1(x):
@@ -110,6 +116,10 @@ def recurrence(q, k, v, mode, g=None, beta=None, S0=None):
         elif mode == "gla":
             alpha = np.exp(g[:, :, t])[..., :, None]              # [B,H,dk,1]
             S = alpha * S + kt[..., :, None] * vt[..., None, :]
+            o[:, :, t] = np.einsum("bhc,bhcv->bhv", qt, S)
+        elif mode == "outer":
+            G = np.exp(g[:, :, t])[..., :, None] * np.exp(beta[:, :, t])[..., None, :]  # [B,H,dk,dv]
+            S = G * S + kt[..., :, None] * vt[..., None, :]
             o[:, :, t] = np.einsum("bhc,bhcv->bhv", qt, S)
         else:  # gdn, kda: decay first, then the delta rule
             if mode == "kda":

@@ -242,8 +242,10 @@ def _mode_inputs(mode, T, dk=8, dv=6, s0=True):
         g = np.array([np.log1p(-2.0 ** -3)])
     elif mode in ("scalar", "gdn"):
         g = -np.abs(_rand(1, 1, T, scale=0.15))
-    elif mode in ("gla", "kda"):
+    elif mode in ("gla", "kda", "outer"):
         g = -np.abs(_rand(1, 1, T, dk, scale=0.05))
+    if mode == "outer":  # value-axis log-gates ride in beta
+        beta = -np.abs(_rand(1, 1, T, dv, scale=0.05))
     if mode in ("gdn", "kda"):
         k = k / np.linalg.norm(k, axis=-1, keepdims=True)
         beta = 1.0 / (1.0 + np.exp(-_rand(1, 1, T)))
@@ -304,10 +306,12 @@ def test_c_oracle_matches_numpy(mode):
         g = np.log1p(-(2.0 ** (-5.0 - np.arange(H))))
     elif mode in ("scalar", "gdn"):
         g = -np.abs(_rand(B, H, T, scale=0.1))
-    elif mode in ("gla", "kda"):
+    elif mode in ("gla", "kda", "outer"):
         g = -np.abs(_rand(B, H, T, dk, scale=0.1))
     if mode in ("gdn", "kda"):
         beta = 1.0 / (1.0 + np.exp(-_rand(B, H, T)))
+    if mode == "outer":
+        beta = -np.abs(_rand(B, H, T, dv, scale=0.1))
     S0 = _rand(B, H, dk, dv + (mode == "elu1"), scale=0.2)
     if mode == "elu1":
         S0[..., dv] = np.abs(S0[..., dv]) + 1.0
