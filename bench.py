@@ -48,6 +48,7 @@ KERNEL_SOURCES = {
     "kda": [_CS + "la_chunk_tc.cu", _CS + "la_wy.cuh"] + _COMMON,
     "retnet": [_CS + "la_chunk_ws.cu"] + _COMMON,
     "gla": [_CS + "la_chunk_ws.cu"] + _COMMON,
+    "outer": [_CS + "la_chunk_ws.cu"] + _COMMON,
     "scalar": [_CS + "la_chunk_ws.cu", _CS + "la_chunk_mat.cu"] + _COMMON,
     "elu1": [_CS + "la_chunk_ws.cu", _CS + "la_chunk_mat.cu"] + _COMMON,
     "linear_fp32": [_CS + "la_chunk_simt.cu"],
@@ -64,7 +65,7 @@ def uses_materialised(wl, variant=None, sm_count=152) -> bool:
     (the library's per-shape rule, or a forced LA_VARIANT)."""
     if variant is not None:
         return variant == "mat"
-    return (wl.dtype == "bf16" and wl.mode not in ("gdn", "kda") and wl.T >= 512
+    return (wl.dtype == "bf16" and wl.mode not in ("gdn", "kda", "outer") and wl.T >= 512
             and 2 * wl.B * wl.H <= sm_count)
 
 
@@ -117,8 +118,10 @@ def algorithmic_bytes(wl, has_s0: bool) -> float:
         per_tok += 4
     if wl.mode in ("gdn", "kda"):
         per_tok += 4
-    if wl.mode in ("gla", "kda"):
+    if wl.mode in ("gla", "kda", "outer"):
         per_tok += 4 * dk
+    if wl.mode == "outer":  # value-axis gates
+        per_tok += 4 * dv
     W = dv + 1 if wl.mode == "elu1" else dv
     state = 4 * dk * W * (2 if has_s0 else 1)
     return float(B * H * (T * per_tok + state))

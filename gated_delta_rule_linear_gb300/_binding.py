@@ -39,6 +39,7 @@ MODE_IDS = {
     "scalar": CONSTANTS["LA_SCALAR_GATE"],
     "gdn": CONSTANTS["LA_GDN"],
     "kda": CONSTANTS["LA_KDA"],
+    "outer": CONSTANTS["LA_OUTER_GATE"],  # beta carries the value-axis log-gates
 }
 
 # Every function the header declares, with its ctypes signature.

@@ -101,8 +101,8 @@ int select_variant(const ChunkParams &p, int *chunk_out) {
     return -1;
   }
   *chunk_out = C;
-  if (p.f32 && p.kind == kKda) {
-    set_error("la_chunk_fwd: LA_KDA takes bfloat16 inputs only");
+  if (p.f32 && (p.kind == kKda || p.kind == kOuter)) {
+    set_error("la_chunk_fwd: LA_KDA and LA_OUTER_GATE take bfloat16 inputs only");
     return -1;
   }
   if (p.f32) return (want == kVariantTc || want == kVariantMat) ? -2 : kVariantSimt;
@@ -113,13 +113,17 @@ int select_variant(const ChunkParams &p, int *chunk_out) {
     }
     return kVariantTc;
   }
+  if ((want == kVariantMat || want == kVariantSimt) && p.kind == kOuter) {
+    set_error("la_chunk_fwd: LA_OUTER_GATE runs on the pipelined tensor-core kernel only");
+    return -1;
+  }
   if (want == kVariantMat && p.kind == kGdn) {
     set_error("la_chunk_fwd: the materialised variant covers the unit-write modes only");
     return -1;
   }
   if (want >= 0) return want;
   const long long BH = (long long)p.B * p.H;
-  if (p.kind != kGdn && p.T >= 8 * 64 && 2 * BH <= sm_count()) return kVariantMat;
+  if (p.kind != kGdn && p.kind != kOuter && p.T >= 8 * 64 && 2 * BH <= sm_count()) return kVariantMat;
   return kVariantTc;
 }
 
@@ -161,7 +165,7 @@ int la_stream_status(la_stream_t stream) {
 static int check_mode(int mode, const float *g, const float *beta, const char *fn, bool allow_nc = false) {
   const int kind = mode & 0xff;
   const int flags = allow_nc ? (LA_F32 | LA_NONCAUSAL) : LA_F32;
-  if ((mode & ~(0xff | flags)) != 0 || kind < LA_LINEAR || kind > LA_KDA) {
+  if ((mode & ~(0xff | flags)) != 0 || kind < LA_LINEAR || kind > LA_OUTER_GATE) {
     set_error("%s: unknown mode 0x%x", fn, mode);
     return LA_ERR_INVALID_ARG;
   }
@@ -169,7 +173,8 @@ static int check_mode(int mode, const float *g, const float *beta, const char *f
     set_error("%s: LA_NONCAUSAL goes with LA_LINEAR or LA_ELU1_NORM only", fn);
     return LA_ERR_INVALID_ARG;
   }
-  const bool needs_g = kind == LA_RETNET || kind == LA_GLA || kind == LA_SCALAR_GATE || kind == LA_KDA;
+  const bool needs_g = kind == LA_RETNET || kind == LA_GLA || kind == LA_SCALAR_GATE || kind == LA_KDA ||
+                       kind == LA_OUTER_GATE;
   const bool takes_g = needs_g || kind == LA_GDN;
   if (needs_g && !g) {
     set_error("%s: mode %d needs log-gates g", fn, kind);
@@ -179,8 +184,12 @@ static int check_mode(int mode, const float *g, const float *beta, const char *f
     set_error("%s: mode %d takes no gates (g must be NULL)", fn, kind);
     return LA_ERR_INVALID_ARG;
   }
-  if (kind != LA_GDN && kind != LA_KDA && beta) {
-    set_error("%s: beta is only used by LA_GDN and LA_KDA (must be NULL for mode %d)", fn, kind);
+  if (kind == LA_OUTER_GATE && !beta) {
+    set_error("%s: LA_OUTER_GATE needs the value-axis log-gates in beta", fn);
+    return LA_ERR_INVALID_ARG;
+  }
+  if (kind != LA_GDN && kind != LA_KDA && kind != LA_OUTER_GATE && beta) {
+    set_error("%s: beta is only used by LA_GDN, LA_KDA and LA_OUTER_GATE (must be NULL for mode %d)", fn, kind);
     return LA_ERR_INVALID_ARG;
   }
   return LA_OK;
@@ -226,9 +235,11 @@ int la_chunk_fwd(const void *q, const void *k, const void *v, const float *g, co
     set_error("%s: q, k, v and o must be 16-byte aligned", fn);
     return LA_ERR_INVALID_ARG;
   }
-  if ((g && !aligned(g, (kind == LA_GLA || kind == LA_KDA) ? 16 : 4)) || (beta && !aligned(beta, 4)) ||
+  const bool chan = kind == LA_GLA || kind == LA_KDA || kind == LA_OUTER_GATE;
+  if ((g && !aligned(g, chan ? 16 : 4)) || (beta && !aligned(beta, kind == LA_OUTER_GATE ? 16 : 4)) ||
       (S0 && !aligned(S0, 4)) || (S_final && !aligned(S_final, 4))) {
-    set_error("%s: g (16 bytes for LA_GLA and LA_KDA), beta, S0 and S_final must be aligned", fn);
+    set_error("%s: g (16 bytes for LA_GLA, LA_KDA, LA_OUTER_GATE), beta (16 bytes for LA_OUTER_GATE), S0 and "
+              "S_final must be aligned", fn);
     return LA_ERR_INVALID_ARG;
   }
 

@@ -96,7 +96,7 @@ extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const f
   }
   if ((mode & ~(0xff | LA_F32)) != 0 || (kind != LA_LINEAR && kind != LA_RETNET)) {
     set_error("%s: mode 0x%x: the backward pass covers LA_LINEAR and LA_RETNET (optionally | LA_F32)", fn, mode);
-    return (mode & ~(0xff | LA_F32)) == 0 && kind >= LA_LINEAR && kind <= LA_KDA ? LA_ERR_UNSUPPORTED
+    return (mode & ~(0xff | LA_F32)) == 0 && kind >= LA_LINEAR && kind <= LA_OUTER_GATE ? LA_ERR_UNSUPPORTED
                                                                                   : LA_ERR_INVALID_ARG;
   }
   if ((kind == LA_RETNET) != (g != nullptr)) {

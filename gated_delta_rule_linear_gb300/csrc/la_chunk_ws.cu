@@ -19,6 +19,13 @@
 // halves for the state update, and divides o by q.z + P 1 (kernel-attention
 // notes, sections 13-14).
 //
+// The outer-product gate (alpha_t beta_t^T, "Talk Linear Attention" section
+// 5.4) takes GLA's key-axis fold unchanged and adds the same fold on the
+// value axis: V is scaled by e^{bv_m - bv} in place, o by e^{bv - bv_m} in
+// the output epilogue (each state-group thread rescans its value column's
+// gates, which stay in L2), and the per-column factor e^{bv_m} e^{bv_last' -
+// bv_m'} rides on the state round trip next to the key-axis one.
+//
 // REV (plain linear attention and RetNet) runs the same recurrence over the
 // time-reversed sequence without copying it: chunk j is the 64-row window
 // ending at row T-1-64j of the stored tensors (its TMA load may start above
@@ -64,13 +71,18 @@ constexpr float kLog2e = 1.4426950408889634f;
 // per-stage scalars (floats): log2-domain gate prefix b2, e^{b}, elu+1
 // denominators, chunk decay, fast-path flag, per-row factors e^{b - b_last}
 // (scores) and e^{b_last - b} (value or key rows), GLA per-channel factors
-// (state factor e^{b_m} e^{b_last' - b_m'}, midpoint-to-end decay e^{b_last - b_m})
+// (state factor e^{b_m} e^{b_last' - b_m'}, midpoint-to-end decay e^{b_last - b_m}),
+// and for the outer-product gate the same two factors per value column
 constexpr int kMsB2 = 0, kMsEB = 64, kMsDen = 128, kMsDec = 192, kMsB2L = 193, kMsFast = 194,
-              kMsF = 256, kMsVS = 320, kMsBM = 384, kMsLM = 640;
-// bytes of one scalar slot: the GLA per-channel factors need the upper part
-__host__ __device__ constexpr uint32_t ms_bytes(int kind) { return kind == kGla ? 3072u : 1536u; }
-// GLA's 32 KB gate tiles leave no room for an output staging tile: it stores o directly
-__host__ __device__ constexpr bool staged_out(int kind) { return kind != kGla; }
+              kMsF = 256, kMsVS = 320, kMsBM = 384, kMsLM = 640, kMsBMV = 768, kMsLMV = 896;
+// per-key-channel gates (GLA, outer-product gate): a gate tile per stage, midpoint fold
+__host__ __device__ constexpr bool chan_gates(int kind) { return kind == kGla || kind == kOuter; }
+// bytes of one scalar slot: the per-channel factors need the upper part
+__host__ __device__ constexpr uint32_t ms_bytes(int kind) {
+  return kind == kOuter ? 4096u : kind == kGla ? 3072u : 1536u;
+}
+// the 32 KB gate tiles leave no room for an output staging tile: o is stored directly
+__host__ __device__ constexpr bool staged_out(int kind) { return !chan_gates(kind); }
 // A chunk whose total decay is below 2^-kFastLimit takes the exact path.
 constexpr float kFastLimit = 100.f;
 
@@ -85,14 +97,16 @@ struct WsLayout {
   uint32_t st, ot, misc, z, tmp, bar, total;
 };
 
-__host__ __device__ inline WsLayout ws_layout(int dk, int kind, int ns) {
+__host__ __device__ inline WsLayout ws_layout(int dk, int dv, int kind, int ns) {
   WsLayout L;
-  const bool gla = kind == kGla, elu = kind == kElu1;
+  const bool elu = kind == kElu1;
+  // the tile holds the key gates; the outer-product gate reuses it for its value-axis prefix
+  const int gw = kind == kOuter && dv > dk ? dv : dk;
   const uint32_t qk_bytes = (uint32_t)(dk / 64) * 16384u;
   uint32_t o = 0;
   L.qk = o; o += qk_bytes;
   L.v = o; o += 16384u;  // upper 8 KB is a zero pad when dv = 64
-  L.g = o; o += gla ? up1k((uint32_t)kC * dk * 4u) : 0u;
+  L.g = o; o += chan_gates(kind) ? up1k((uint32_t)kC * gw * 4u) : 0u;
   L.klo = o; o += elu ? (uint32_t)(dk / 64) * 8192u : 0u;
   L.p = o; o += 8192u;
   L.stage = o;
@@ -112,12 +126,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_o) {
-  constexpr bool elu = KIND == kElu1, gla = KIND == kGla;
+  constexpr bool elu = KIND == kElu1, outer = KIND == kOuter;
+  constexpr bool gla = chan_gates(KIND);  // key-axis channel gates (GLA and the outer-product gate)
   constexpr bool sgate = KIND == kRetnet || KIND == kScalar;
   static_assert(!REV || KIND == kLinear || KIND == kRetnet, "reversed runs: unit-write, per-head decay only");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const WsLayout L = ws_layout(DK, KIND, ns);
+  const WsLayout L = ws_layout(DK, DV, KIND, ns);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x, h = bh % p.H;
   const int T = p.T, nchunks = (T + kC - 1) / kC;
@@ -244,6 +259,8 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
         for (int a = 0; a < DV / 64; ++a)
           tma_load_3d(st + L.v + a * 8192, &tm_v, &full[s], 64 * a, t0, bh);
         if (gla) tma_load_3d(st + L.g, &tm_g, &full[s], 0, t0, bh);
+        if (outer)  // the value-axis gates are read with plain loads by the key and state groups
+          bulk_prefetch_l2(p.beta + ((size_t)bh * T + t0) * DV, (uint32_t)min(kC, T - t0) * DV * 4u);
         if (sgate) mbar_arrive(&full[s]);  // the gate prefix of this chunk is in place
         // the load of chunk j + ns waits for this chunk's last MMA; warm L2 now
         // (a prefetch is a hint: the reversed run skips a window that starts above row 0)
@@ -364,6 +381,11 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
           if (gla) {  // one factor: the bf16 copy is the decayed state
             float fm[32];
             load32(ms + kMsBM + c0, fm);
+            if (outer) {  // times this value column's factor
+              const float fv = v < DV ? ms[kMsBMV + v] : 0.f;
+#pragma unroll
+              for (int e = 0; e < 32; ++e) fm[e] *= fv;
+            }
 #pragma unroll
             for (int e = 0; e < 32; ++e) x[e] *= fm[e];
             store_row32_bf16(sm + L.st, 16384, v, c0, x);
@@ -400,9 +422,17 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
         const bool staged = staged_out(KIND) && (!REV || t0c >= 0);
         __nv_bfloat16 *obh = static_cast<__nv_bfloat16 *>(p.o) + (size_t)bh * T * DV;
         const bool odd = lane & 1;
+        // outer-product gate: value column v's log2 prefix over the chunk (the key
+        // group's scan, redone from L2), carried across the two halves
+        float vcar = 0.f, vbm = 0.f;
+        const float *gvc = outer ? p.beta + ((size_t)bh * T + (size_t)c * kC) * DV + v : nullptr;
 #pragma unroll 1
         for (int r0 = 0; r0 < kC; r0 += 32) {
-          float a[32];
+          float a[32], gq[outer ? 32 : 1];
+          if (outer) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) gq[e] = (v < DV && r0 + e < n) ? __ldg(gvc + (size_t)(r0 + e) * DV) : 0.f;
+          }
           tmem_ld32(tl + kColO + ob * 64 + r0, a);
           if (sgate) {  // O = e^{b_r} (S^T Q^T) + (local part)
             float b[32], f[32];
@@ -413,6 +443,16 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
             for (int e = 0; e < 32; ++e) a[e] = fmaf(f[e], b[e], a[e]);
           }
           tmem_wait_ld();
+          if (outer) {  // o = e^{bv - bv_m} (midpoint-relative value-axis products)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              vcar = fmaf(gq[e], kLog2e, vcar);
+              gq[e] = vcar;
+            }
+            if (r0 == 0) vbm = gq[kMid];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) a[e] *= ex2(gq[e] - vbm);
+          }
           if (elu) {
             float den[32];
             load32(ms + kMsDen + r0, den);
@@ -463,6 +503,11 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
           if (gla) {  // the last chunk's midpoint-to-end decay
             float fl[32];
             load32(mslot(nchunks - 1) + kMsLM + c0, fl);
+            if (outer) {  // of both axes
+              const float lv = v < DV ? mslot(nchunks - 1)[kMsLMV + v] : 0.f;
+#pragma unroll
+              for (int e = 0; e < 32; ++e) fl[e] *= lv;
+            }
 #pragma unroll
             for (int e = 0; e < 32; ++e) x[e] *= fl[e];
           }
@@ -478,6 +523,7 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
     const int kg = tid - kKG;
     if (elu && kg < DK) zs[kg] = p.S0 ? p.S0[((size_t)bh * DK + kg) * Wmem + DV] : 0.f;
     float lm_prev = 1.f;  // GLA: the previous chunk's e^{b_last - b_m} of channel kg
+    float lv_prev = 1.f;  // outer-product gate: the same for value column kg
     for (int j = 0; j < nchunks; ++j) {
       const int s = j % ns, n = min(kC, T - j * kC);
       uint8_t *st = stage(s);
@@ -487,6 +533,7 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
       bool ok = wait_or_abort(&full[s], (j / ns) & 1, abort_flag, p.status);
       if (!group_all(ok, kBarKG)) break;
       // ---- inclusive log-gate prefix
+      float gvr[outer ? kC : 1];  // outer-product gate: this thread's value-axis gates
       if (gla) {
         if (kg < DK) {  // channel kg: all 64 loads first, then the scan (log2 units) in registers
           float b[kC];
@@ -501,6 +548,11 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
           ms[kMsBM + kg] = ex2(b[kMid]) * lm_prev;
           ms[kMsLM + kg] = lm;
           lm_prev = lm;
+        }
+        if (outer && kg < DV) {  // value column kg: the loads fly during the q/k transform
+          const float *gp = p.beta + ((size_t)bh * T + (size_t)j * kC) * DV + kg;
+#pragma unroll
+          for (int r = 0; r < kC; ++r) gvr[r] = (r < n) ? __ldg(gp + (size_t)r * DV) : 0.f;
         }
         group_sync(kBarKG);
         // Q e^{b - b_mid}, K e^{b_mid - b} in place: thread kg owns 8-channel
@@ -568,6 +620,39 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
         group_sync(kBarKG);
       }
       if ((elu || gla) && kg == 0) mbar_arrive(&qk_ready[s]);
+      // ---- outer-product gate, value axis (while the score MMA runs): prefix of
+      // column kg, d = bv - bv_m into the dead gate tile, then V e^{-d} in place
+      if (outer) {
+        if (kg < DV) {
+          gvr[0] *= kLog2e;
+#pragma unroll
+          for (int r = 1; r < kC; ++r) gvr[r] = fmaf(gvr[r], kLog2e, gvr[r - 1]);
+          const float bm = gvr[kMid], lv = ex2(gvr[kC - 1] - bm);
+#pragma unroll
+          for (int r = 0; r < kC; ++r) gt[r * DV + kg] = gvr[r] - bm;
+          ms[kMsBMV + kg] = ex2(bm) * lv_prev;
+          ms[kMsLMV + kg] = lv;
+          lv_prev = lv;
+        }
+        group_sync(kBarKG);
+        const int cg = kg & 15, r0 = kg >> 4;  // 16-byte group cg of rows r0 + 8 m (as the row scalings)
+        if (cg < DV / 8) {
+          uint8_t *base = st + L.v + (cg >> 3) * 8192;
+#pragma unroll 2
+          for (int m = 0; m < 8; ++m) {
+            const int r = r0 + 8 * m;
+            const float4 *dp = reinterpret_cast<const float4 *>(gt + r * DV + cg * 8);
+            const float4 d0 = dp[0], d1 = dp[1];
+            const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+            uint4 *ptr = reinterpret_cast<uint4 *>(base + sw128_off(r, (cg & 7) * 8));
+            float f[8];
+            unpack8(*ptr, f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] *= ex2(-dd[e]);
+            *ptr = pack8(f);
+          }
+        }
+      }
       ok = wait_or_abort(&d1_full[j & 1], (j >> 1) & 1, abort_flag, p.status);
       if (!group_all(ok, kBarKG)) break;
       tc_fence_after();
@@ -692,8 +777,8 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
 template <int DK, int DV, int KIND, bool REV>
 int launch_typed(const ChunkParams &p, cudaStream_t stream) {
   int ns = 3;
-  WsLayout L = ws_layout(DK, KIND, ns);
-  while (ns > 2 && L.total + 1024 > 232448) L = ws_layout(DK, KIND, --ns);
+  WsLayout L = ws_layout(DK, DV, KIND, ns);
+  while (ns > 2 && L.total + 1024 > 232448) L = ws_layout(DK, DV, KIND, --ns);
   const size_t smem = L.total + 1024;
   if (smem > 232448) {
     set_error("la_chunk_fwd: pipelined kernel needs %zu bytes of shared memory", smem);
@@ -709,7 +794,7 @@ int launch_typed(const ChunkParams &p, cudaStream_t stream) {
                      CU_TENSOR_MAP_SWIZZLE_128B) &&
             make_map(&mv, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DV, p.T, BH, 64,
                      CU_TENSOR_MAP_SWIZZLE_128B);
-  if (ok && KIND == kGla)
+  if (ok && chan_gates(KIND))
     ok = make_map(&mg, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, DK, p.T, BH, DK,
                   CU_TENSOR_MAP_SWIZZLE_NONE);
   else
@@ -758,6 +843,7 @@ int launch_chunk_ws(const ChunkParams &p, cudaStream_t stream) {
     case kRetnet: return launch_kind<kRetnet>(p, stream);
     case kScalar: return launch_kind<kScalar>(p, stream);
     case kGla: return launch_kind<kGla>(p, stream);
+    case kOuter: return launch_kind<kOuter>(p, stream);
     default:
       set_error("la_chunk_fwd: mode %d is not handled by the pipelined kernel", p.kind);
       return LA_ERR_UNSUPPORTED;

@@ -17,6 +17,7 @@ enum Kind : int {
   kScalar = LA_SCALAR_GATE,
   kGdn = LA_GDN,
   kKda = LA_KDA,
+  kOuter = LA_OUTER_GATE,
 };
 
 // Bits of the device status word (one per device, see la_status.cu).

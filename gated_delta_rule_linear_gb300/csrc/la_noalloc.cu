@@ -72,12 +72,12 @@ extern "C" int la_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
     return LA_ERR_UNSUPPORTED;
   }
   const int kind = mode & 0xff;
-  if ((mode & ~0xff) != 0 || kind < LA_LINEAR || kind > LA_KDA) {
+  if ((mode & ~0xff) != 0 || kind < LA_LINEAR || kind > LA_OUTER_GATE) {
     set_error("%s: unknown mode 0x%x, or LA_F32 (bfloat16 inputs only)", fn, mode);
     return (mode & ~0xff) == LA_F32 ? LA_ERR_UNSUPPORTED : LA_ERR_INVALID_ARG;
   }
-  if (kind == LA_GDN || kind == LA_KDA) {
-    set_error("%s: covers the unit-write modes only (not LA_GDN or LA_KDA)", fn);
+  if (kind == LA_GDN || kind == LA_KDA || kind == LA_OUTER_GATE) {
+    set_error("%s: covers the unit-write modes with key-axis gates only (not LA_GDN, LA_KDA or LA_OUTER_GATE)", fn);
     return LA_ERR_UNSUPPORTED;
   }
   const bool needs_g = kind == LA_RETNET || kind == LA_GLA || kind == LA_SCALAR_GATE;

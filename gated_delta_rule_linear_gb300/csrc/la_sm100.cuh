@@ -283,6 +283,12 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
       : "memory");
 }
 
+// L2 prefetch of `bytes` contiguous global bytes (16-byte aligned address,
+// size a multiple of 16): a hint, no completion to wait for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 2^x on the special-function unit (PTX ex2.approx.ftz.f32: relative error
 // about 2^-22, subnormal results flushed to zero).
 __device__ __forceinline__ float ex2(float x) {

@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(160) step_kernel(const StepParams p) {
   __shared__ float sden;
   const int bh = blockIdx.x, h = bh % p.H, j = threadIdx.x;
   const int dv = p.dv, kind = p.kind;
-  const bool elu = kind == kElu1, delta = kind == kGdn || kind == kKda;
+  const bool elu = kind == kElu1, delta = kind == kGdn || kind == kKda, outer = kind == kOuter;
   const int W = dv + (elu ? 1 : 0);
   const Tin *q = static_cast<const Tin *>(p.q);
   const Tin *k = static_cast<const Tin *>(p.k);
@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(160) step_kernel(const StepParams p) {
     sk[c] = kc;
     float a = 1.f;
     if (kind == kRetnet) a = __expf(__ldg(p.g + h));
-    else if (kind == kGla || kind == kKda) a = __expf(__ldg(p.g + (size_t)bh * DK + c));
+    else if (kind == kGla || kind == kKda || outer) a = __expf(__ldg(p.g + (size_t)bh * DK + c));
     else if (kind == kScalar || (kind == kGdn && p.g)) a = __expf(__ldg(p.g + bh));
     sa[c] = a;
   }
@@ -57,8 +57,10 @@ __global__ void __launch_bounds__(160) step_kernel(const StepParams p) {
   if (active) {
     float *S = p.S + (size_t)bh * DK * W + j;
     float s[DK];
+    // outer-product gate: this value column's factor beta_j (log-gate in p.beta)
+    const float av = (outer && j < dv) ? __expf(__ldg(p.beta + (size_t)bh * dv + j)) : 1.f;
 #pragma unroll
-    for (int c = 0; c < DK; ++c) s[c] = S[(size_t)c * W] * sa[c];   // decay first
+    for (int c = 0; c < DK; ++c) s[c] = S[(size_t)c * W] * (sa[c] * av);   // decay first
     float w = (j < dv) ? ldv(v, (size_t)bh * dv + j) : 1.f;
     if (delta) {
       float r = 0.f;

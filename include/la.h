@@ -91,6 +91,16 @@ typedef struct CUstream_st *la_stream_t;
  * evaluation folds exp(b_r - b_s) per channel around the chunk midpoint as
  * for LA_GLA, with the same range limit. */
 #define LA_KDA           6
+/* Outer-product gate: S_t = (alpha_t beta_t^T) ⊙ S_{t-1} + k_t v_t^T, a
+ * key-axis gate alpha_t (row c of S) times a value-axis gate beta_t (column
+ * j) -- the gate form "Talk Linear Attention" section 5.4 gives for gated
+ * linear attention that remains a matrix product. g = float32 [B][H][T][dk]
+ * holding log alpha; the beta argument carries float32 [B][H][T][dv] holding
+ * log beta (both required, 16-byte aligned; per step [B][H][dk] and
+ * [B][H][dv]). bfloat16 inputs only in la_chunk_fwd. Chunked evaluation
+ * folds both axes' gates around the chunk midpoint, with LA_GLA's range
+ * limit on each axis. */
+#define LA_OUTER_GATE    7
 /* Flag: q, k, v and o are float32 instead of bfloat16. */
 #define LA_F32           0x100
 /* Flag (la_chunk_fwd only, with LA_LINEAR or LA_ELU1_NORM, bfloat16): the

@@ -28,7 +28,7 @@ __all__ = ["Workload", "WORKLOADS", "make_inputs", "MODES", "PrologueWorkload", 
 
 # Mode names used throughout the Python side. The C ABI has its own enum;
 # the binding maps these names onto it.
-MODES = ("linear", "elu1", "retnet", "gla", "scalar", "gdn", "kda")
+MODES = ("linear", "elu1", "retnet", "gla", "scalar", "gdn", "kda", "outer")
 
 
 @dataclass(frozen=True)
@@ -89,6 +89,10 @@ WORKLOADS = {
     # after S0 by bench.py's backward leg from the same generator recipe.
     "backward": Workload("backward", "retnet", 8, 16, 4096, 128, 128, "bf16", 64, seed=9,
                          qkv_scale=1.0 / math.sqrt(128.0), extra={"backward": True}),
+    # Outer-product gate alpha_t beta_t^T (a next row): the GLA shape and q/k/v
+    # recipe with GLA-distributed log-gates on both the key and the value axis.
+    "outer": Workload("outer", "outer", 8, 16, 8192, 128, 128, "bf16", 64, seed=11,
+                      qkv_scale=1.0 / math.sqrt(128.0)),
     # One Gated DeltaNet decode step (la_recurrent_step) for a batch of 128
     # sequences x 16 heads with resident states: the gdn recipe with T = 1
     # and a random state S ~ N(0, 0.01).
@@ -144,6 +148,11 @@ def make_inputs(wl: Workload | str, **sizes) -> dict:
     elif wl.mode == "kda":
         g = F.logsigmoid(_normal(gen, (B, H, T, dk))) / 16.0
         beta = torch.sigmoid(_normal(gen, (B, H, T)))
+    elif wl.mode == "outer":
+        # key-axis and value-axis log-gates, both with the GLA gate's distribution;
+        # the value-axis gates travel in the beta slot
+        g = F.logsigmoid(_normal(gen, (B, H, T, dk))) / 16.0
+        beta = F.logsigmoid(_normal(gen, (B, H, T, dv))) / 16.0
     S0 = None
     if wl.s0:
         width = dv + 1 if wl.mode == "elu1" else dv
