@@ -256,8 +256,9 @@ int la_chunk_bwd(const void *q, const void *k, const void *v, const float *g, co
  * (divided by z . phi(q) for LA_ELU1_NORM).
  *
  *   q, k [B][H][dk]; v, o [B][H][dv] (input dtype, 4-byte aligned)
- *   g    LA_RETNET [H]; LA_GLA [B][H][dk]; LA_SCALAR_GATE / LA_GDN [B][H]
- *   beta LA_GDN [B][H] or NULL
+ *   g    LA_RETNET [H]; LA_GLA / LA_KDA / LA_OUTER_GATE [B][H][dk];
+ *        LA_SCALAR_GATE / LA_GDN [B][H]
+ *   beta LA_GDN / LA_KDA [B][H] or NULL; LA_OUTER_GATE [B][H][dv] (log beta)
  *   S    float32 [B][H][dk][W], updated in place
  */
 int la_recurrent_step(const void *q, const void *k, const void *v, const float *g,

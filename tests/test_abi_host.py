@@ -86,7 +86,12 @@ def _call(**kw):
     (dict(mode=1, g=A), "LA_ERR_INVALID_ARG"),        # elu1 takes no gates
     (dict(mode=6), "LA_ERR_INVALID_ARG"),             # kda needs per-channel g
     (dict(mode=6, g=A + 4), "LA_ERR_INVALID_ARG"),    # kda g must be 16-byte aligned
-    (dict(mode=7), "LA_ERR_INVALID_ARG"),             # no mode 7
+    (dict(mode=8), "LA_ERR_INVALID_ARG"),             # no mode 8
+    (dict(mode=7), "LA_ERR_INVALID_ARG"),             # outer gate needs g
+    (dict(mode=7, g=A), "LA_ERR_INVALID_ARG"),        # ... and the value-axis gates in beta
+    (dict(mode=7, g=A, beta=A + 4), "LA_ERR_INVALID_ARG"),  # beta 16-byte aligned
+    (dict(mode=7, g=A + 4, beta=A), "LA_ERR_INVALID_ARG"),  # g 16-byte aligned
+    (dict(mode=7 | 0x200, g=A, beta=A), "LA_ERR_INVALID_ARG"),  # non-causal: linear and elu1 only
     (dict(S0=A + 1), "LA_ERR_INVALID_ARG"),
 ])
 def test_chunk_fwd_rejects_bad_arguments(lib, kw, code):
@@ -101,6 +106,7 @@ def test_chunk_fwd_rejects_bad_arguments(lib, kw, code):
     (dict(dk=100), "LA_ERR_UNSUPPORTED"),
     (dict(mode=5, beta=A, g=A + 1), "LA_ERR_INVALID_ARG"),
     (dict(mode=0, beta=A), "LA_ERR_INVALID_ARG"),
+    (dict(mode=7, g=A), "LA_ERR_INVALID_ARG"),        # outer gate: value-axis gates in beta
 ])
 def test_recurrent_step_rejects_bad_arguments(lib, kw, code):
     args = dict(q=A, k=A, v=A, g=None, beta=None, o=A, S=A, B=1, H=1, dk=64, dv=64,
