@@ -15,6 +15,7 @@ Contents
                over heads, for full-length sequences and CPU timing
   prologue     short convolution, L2 normalisation, gate and beta activations
   noncausal    the non-causal form O = Q (K^T V) (linear, elu+1)
+  gdelta       the generalised delta rule S <- (I - b a^T) S + k v^T
 """
 from __future__ import annotations
 
