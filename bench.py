@@ -55,6 +55,7 @@ KERNEL_SOURCES = {
     "noncausal": [_CS + "la_chunk_mat.cu"] + _COMMON,
     "backward": [_CS + "la_backward.cu", _CS + "la_chunk_ws.cu", _CS + "la_chunk_mat.cu"] + _COMMON,
     "decode": [_CS + "la_step.cu"],
+    "gdelta": [_CS + "la_chunk_gdelta.cu"],
     "prologue": [_CS + "la_prologue.cu", _CS + "la_sm100.cuh"],
     "prologue_gla": [_CS + "la_prologue.cu", _CS + "la_sm100.cuh"],
 }
@@ -307,6 +308,8 @@ def main():
         return bench_backward(args, rank, world, local_rank)
     if workloads.WORKLOADS[args.workload].extra.get("decode"):
         return bench_decode(args, rank, world, local_rank)
+    if workloads.WORKLOADS[args.workload].mode == "gdelta":
+        return bench_gdelta(args, rank, world, local_rank)
     wl = workloads.WORKLOADS[args.workload]
     over = {k: getattr(args, k) for k in ("B", "H", "T") if getattr(args, k) is not None}
     if over:
@@ -890,6 +893,164 @@ def decode_bytes(wl) -> float:
     W = wl.dv + 1 if wl.mode == "elu1" else wl.dv
     per_head = 2 * 4 * wl.dk * W + e * (2 * wl.dk + 2 * wl.dv) + 8
     return float(wl.B * wl.H * per_head)
+
+
+GD_METRIC = "tokens/sec of the generalised-delta-rule chunk forward (la_chunk_fwd_gdelta) at 1 GB300; % of roofline"
+
+
+def gdelta_flops_per_token_head(dk: int, dv: int, C: int = 64) -> float:
+    """Chunk form at C = 64: the four C x C products Q K^T, A B^T, A K^T, Q B^T
+    (half each under the masks, counted whole), A S and Q S (2 dk dv each),
+    L_ak V, T R, M(Q K^T) V and M(Q B^T) U (2 C dv each, counted whole), the
+    triangular solve (C^2 / 3) and the state update K^T V - B^T U (4 dk dv)."""
+    return 8 * C * dk + 8 * C * dv + C * C / 3.0 + 8 * dk * dv
+
+
+def time_gdelta_oracle(wl, inp, target_s: float = 10.0):
+    from oracle.gdelta import recurrence_gdelta
+    f64 = lambda t: None if t is None else t.to(torch.float64).numpy()
+    BH = wl.B * wl.H
+    done, t0 = 0, time.perf_counter()
+    while done < BH and (time.perf_counter() - t0) < target_s:
+        b, h = done // wl.H, done % wl.H
+        sl = lambda t: f64(t[b:b + 1, h:h + 1])
+        recurrence_gdelta(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["a"]), sl(inp["b"]),
+                          S0=None if inp["S0"] is None else sl(inp["S0"]))
+        done += 1
+    dt = time.perf_counter() - t0
+    return (done * wl.T / wl.H) / dt, 1, f"{done} of {BH} (batch, head) sequences, full T={wl.T}, float64 numpy", dt
+
+
+def bench_gdelta(args, rank, world, local_rank):
+    wl = workloads.WORKLOADS[args.workload]
+    over = {k: getattr(args, k) for k in ("B", "H", "T") if getattr(args, k) is not None}
+    if over:
+        wl = wl.with_sizes(**over)
+    B, H, T, dk, dv = wl.B, wl.H, wl.T, wl.dk, wl.dv
+    cfg = {"workload": wl.name, "mode": "gdelta", "B": B, "H": H, "T": T, "dk": dk, "dv": dv, "C": wl.C,
+           "global_batch": B * world, "seq_len": T, "parallelism": "replicas" if world > 1 else "single"}
+    inp = workloads.make_inputs(wl)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        vals = []
+        for i in range(args.warmup + args.steps):
+            v, cores, sample, _ = time_gdelta_oracle(wl, inp, target_s=3.0)
+            if i >= args.warmup:
+                vals.append(v)
+        value = statistics.mean(vals)
+        print(json.dumps({
+            "impl": "reference", "metric": GD_METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(B * T / value * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; shapes and distributions of the workload)", "config": cfg,
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }), flush=True)
+        return
+    import gated_delta_rule_linear_gb300 as la
+    from gated_delta_rule_linear_gb300 import build as labuild
+    labuild.build()
+    la.load_library()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    names = [n for n in ("q", "k", "v", "a", "b", "S0") if inp[n] is not None]
+    d = {n: inp[n].to(dev) for n in names}
+    outs = {"o": torch.empty((B, H, T, dv), dtype=wl.torch_dtype, device=dev),
+            "S": torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)}
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    mode = la.CONSTANTS["LA_F32"] if wl.dtype == "f32" else 0
+
+    def step(dd, oo):
+        rc = la.la_chunk_fwd_gdelta(dd["q"], dd["k"], dd["v"], dd["a"], dd["b"], oo["o"], dd.get("S0"), oo["S"],
+                                    B, H, T, dk, dv, wl.C, mode, sh)
+        if rc != 0:
+            raise RuntimeError(la.la_last_error())
+
+    for _ in range(args.warmup):
+        step(d, outs)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[2 * i].record(stream)
+        step(d, outs)
+        ev[2 * i + 1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
+    launch_ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
+    value = replica_throughput(B * T * args.steps, world, total_ms)
+    flop = B * H * T * gdelta_flops_per_token_head(dk, dv)
+    e = 2 if wl.dtype == "bf16" else 4
+    alg = float(B * H * (T * e * (4 * dk + 2 * dv) + 4 * dk * dv * (2 if inp["S0"] is not None else 1)))
+    hbm_peak, tc_peak, peak_src = read_peaks()
+    t_launch = statistics.mean(launch_ms) / 1e3
+    # the arithmetic intensity (~100 FLOP/byte at d = 64) sits below the bf16 ridge: an HBM roofline
+    roof = {"bound": "hbm", "achieved": round(alg / t_launch / 1e9, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(alg / t_launch / 1e9 / hbm_peak, 4), "traffic": recorded_traffic(wl.name),
+            "peak_source": peak_src, "algorithmic_bytes": alg, "kernel": "chunk_gdelta_kernel (CUDA cores, fp32)",
+            "launch_ms_mean": round(statistics.mean(launch_ms), 4)}
+    e2e = None
+    if not args.no_e2e:
+        host = {n: inp[n].pin_memory() for n in names}
+        hout = {n: torch.empty_like(outs[n], device="cpu").pin_memory() for n in outs}
+        dd, oo = dict(d), dict(outs)
+        h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+        d2h = sum(hout[n].numel() * hout[n].element_size() for n in outs)
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for n in names:
+                    dd[n].copy_(host[n], non_blocking=True)
+                step(dd, oo)
+                for n in outs:
+                    hout[n].copy_(oo[n], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        steps = max(3, min(args.steps, 10))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+        e2e = {"value": round(world * B * T * steps / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": steps, "ms_per_step": round(ms / steps, 4)}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v_cpu, cores, sample, dt = time_gdelta_oracle(wl, inp)
+        cpu = {"value": round(v_cpu, 2), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+               "seconds": round(dt, 2)}
+    if rank == 0:
+        cfg["l2"] = "inputs larger than L2 (no flush)" if alg > 129e6 else "inputs smaller than L2"
+        print(json.dumps({
+            "metric": GD_METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+            "data": "synthetic (seeded; shapes and distributions of the workload)", "config": cfg,
+            "tflops": round(world * flop * args.steps / (total_ms / 1e3) / 1e12, 2), "roofline": roof,
+            "cpu_baseline": cpu, "clocks": clk, "e2e": e2e, "gpu_launches": args.steps,
+        }), flush=True)
+    if dist:
+        dist.destroy_process_group()
 
 
 def bench_decode(args, rank, world, local_rank):

@@ -3,18 +3,20 @@
 The compute lives in libla.so (C ABI, include/la.h): hand-written CUDA
 kernels for the chunkwise causal forward pass of the gated delta-rule family
 (plain linear attention, elu+1 normalised attention, RetNet decay, GLA gates,
-scalar decay, Gated DeltaNet, Kimi Delta Attention), its one-token decode
+scalar decay, Gated DeltaNet, Kimi Delta Attention, the outer-product gate;
+the generalised delta rule), the backward pass of the first two, its one-token decode
 step, and the prologue in front of it (short convolution, L2 normalisation,
 gate activations). This package is
 only the binding: ctypes marshalling plus a build helper.
 """
 from ._binding import (CONSTANTS, GATE_KINDS, LIB_PATH, MODE_IDS, SIGNATURES, LAError, chunk_bwd, chunk_fwd,
-                       la_chunk_bwd, la_chunk_fwd, la_chunk_fwd_noalloc, la_last_error, la_prologue,
+                       chunk_fwd_gdelta, la_chunk_bwd, la_chunk_fwd, la_chunk_fwd_gdelta, la_chunk_fwd_noalloc,
+                       la_last_error, la_prologue,
                        la_recurrent_step, la_stream_status, la_version, load_library, prologue, recurrent_step)
 from ._binding import *  # noqa: F401,F403  (LA_* constants)
 
-__all__ = ["chunk_fwd", "chunk_bwd", "recurrent_step", "prologue", "la_chunk_fwd", "la_chunk_bwd",
-           "la_chunk_fwd_noalloc",
+__all__ = ["chunk_fwd", "chunk_bwd", "chunk_fwd_gdelta", "recurrent_step", "prologue", "la_chunk_fwd",
+           "la_chunk_bwd", "la_chunk_fwd_gdelta", "la_chunk_fwd_noalloc",
            "la_prologue", "la_recurrent_step", "GATE_KINDS",
            "la_stream_status", "la_last_error", "la_version", "load_library", "LAError",
            "CONSTANTS", "MODE_IDS", "SIGNATURES", "LIB_PATH"]

@@ -48,6 +48,7 @@ _I = ctypes.c_int
 _F = ctypes.c_float
 SIGNATURES = {
     "la_chunk_fwd": ([_P] * 8 + [_I] * 7 + [_P], _I),
+    "la_chunk_fwd_gdelta": ([_P] * 8 + [_I] * 7 + [_P], _I),
     "la_chunk_fwd_noalloc": ([_P] * 8 + [_I] * 7 + [_P], _I),
     "la_recurrent_step": ([_P] * 7 + [_I] * 5 + [_P], _I),
     "la_chunk_bwd": ([_P] * 11 + [_I] * 7 + [_P], _I),
@@ -102,6 +103,11 @@ def la_chunk_fwd_noalloc(q, k, v, g, beta, o, S0, S_final, B, H, T, dk, dv, C, m
     return load_library().la_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                                _ptr(o), _ptr(S0), _ptr(S_final), B, H, T, dk, dv,
                                                C, mode, stream)
+
+
+def la_chunk_fwd_gdelta(q, k, v, a, b, o, S0, S_final, B, H, T, dk, dv, C, mode, stream):
+    return load_library().la_chunk_fwd_gdelta(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(o),
+                                              _ptr(S0), _ptr(S_final), B, H, T, dk, dv, C, mode, stream)
 
 
 def la_chunk_bwd(q, k, v, g, dO, dS_final, S0, dq_out, dk_out, dv_out, dS0, B, H, T, dk, dv, C, mode, stream):
@@ -213,6 +219,27 @@ def prologue(xq, xk, xv, wq=None, wk=None, wv=None, K=None, hist_in=None, with_h
     if rc != 0:
         raise LAError(rc, la_last_error())
     return {"q": q, "k": k, "v": v, "g": g, "beta": beta, "hist": hist_out}
+
+
+def chunk_fwd_gdelta(q, k, v, a, b, S0=None, C=0, with_state=True, o=None, S_final=None, stream=None):
+    """Generalised delta rule S <- (I - b a^T) S + k v^T (la_chunk_fwd_gdelta).
+    q, k, a, b [B,H,T,dk], v [B,H,T,dv] (bf16 or fp32, CUDA, contiguous).
+    Returns (o, S_final or None)."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("a", a), ("b", b), ("S0", S0)):
+        _check(t, name)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    mode = CONSTANTS["LA_F32"] if q.dtype == torch.float32 else 0
+    if o is None:
+        o = torch.empty((B, H, T, dv), dtype=q.dtype, device=q.device)
+    if with_state and S_final is None:
+        S_final = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    rc = la_chunk_fwd_gdelta(q, k, v, a, b, o, S0, S_final if with_state else None,
+                             B, H, T, dk, dv, C, mode, _stream_handle(stream))
+    if rc != 0:
+        raise LAError(rc, la_last_error())
+    return o, (S_final if with_state else None)
 
 
 def chunk_bwd(q, k, v, dO, mode, g=None, S0=None, dS_final=None, with_dS0=True, C=0, stream=None):

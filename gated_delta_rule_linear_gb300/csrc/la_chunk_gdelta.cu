@@ -1,0 +1,264 @@
+// la_chunk_fwd_gdelta: chunkwise forward of the generalised delta rule
+// ("Talk Linear Attention", section 7.1: an identity-plus-rank-one
+// transition between linear-attention steps), in this library's key-major
+// orientation
+//
+//   S_t = (I - b_t a_t^T) S_{t-1} + k_t v_t^T,   o_t = S_t^T q_t
+//
+// (the page writes the value-major S_{t-1}(I - a_t b_t^T) + v_t k_t^T; the
+// state here is its transpose). Per chunk of C = 64 tokens with incoming
+// state S and rows q_r, k_r, v_r, a_r, b_r, the retrieved values
+// u_r = S_{r-1}^T a_r solve a unit lower-triangular system (the WY form of
+// section 6.2 with separate retrieve and erase vectors):
+//
+//   U = (I + L_ab)^{-1} (A S + L_ak V),  L_ab[r,s] = a_r.b_s, L_ak[r,s] = a_r.k_s (s < r)
+//   O = Q S + M(Q K^T) V - M(Q B^T) U    (M: inclusive causal mask)
+//   S <- S + K^T V - B^T U
+//
+// CUDA cores, float32 arithmetic for bf16 or float32 inputs; one CTA per
+// (b, h) and 16-column tile of the value axis, the state slice in shared
+// memory for the whole sequence.
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "la_internal.h"
+
+namespace la {
+namespace {
+
+constexpr int kC = 64;
+constexpr int kThreads = 256;
+constexpr int kTile = 16;  // value columns per CTA
+
+template <typename T> __device__ __forceinline__ float ld(const T *p);
+template <> __device__ __forceinline__ float ld<float>(const float *p) { return __ldg(p); }
+template <> __device__ __forceinline__ float ld<__nv_bfloat16>(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+template <typename T> __device__ __forceinline__ void st(T *p, float x);
+template <> __device__ __forceinline__ void st<float>(float *p, float x) { *p = x; }
+template <> __device__ __forceinline__ void st<__nv_bfloat16>(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+struct GdLayout {
+  int pk, pw, pc;  // row pitches (floats): key rows dk + 1, value rows kTile + 1, C x C rows C + 1
+  int q, k, a, b, v, s, r, u, p, lab, t, x, total;
+};
+
+__host__ __device__ inline GdLayout gd_layout(int dk) {
+  GdLayout L;
+  L.pk = dk + 1;
+  L.pw = kTile + 1;
+  L.pc = kC + 1;
+  int o = 0;
+  L.q = o; o += kC * L.pk;
+  L.k = o; o += kC * L.pk;
+  L.a = o; o += kC * L.pk;
+  L.b = o; o += kC * L.pk;
+  L.v = o; o += kC * L.pw;
+  L.s = o; o += dk * L.pw;
+  L.r = o; o += kC * L.pw;   // A S + L_ak V, later O
+  L.u = o; o += kC * L.pw;
+  L.p = o; o += kC * L.pc;   // M(Q K^T)
+  L.lab = o; o += kC * L.pc; // L_ab
+  L.t = o; o += kC * L.pc;   // (I + L_ab)^-1
+  L.x = o; o += kC * L.pc;   // L_ak, then M(Q B^T)
+  L.total = o;
+  return L;
+}
+
+struct GdParams {
+  const void *q, *k, *v, *a, *b;
+  void *o;
+  const float *S0;
+  float *S_final;
+  int B, H, T, dk, dv;
+};
+
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads) chunk_gdelta_kernel(const GdParams p) {
+  extern __shared__ float sm[];
+  const int tid = threadIdx.x, bh = blockIdx.x, j0 = blockIdx.y * kTile;
+  const int dk = p.dk, dv = p.dv, T = p.T;
+  const int wv = min(kTile, dv - j0);
+  const GdLayout L = gd_layout(dk);
+  float *Q = sm + L.q, *K = sm + L.k, *A = sm + L.a, *Bm = sm + L.b, *V = sm + L.v, *S = sm + L.s;
+  float *R = sm + L.r, *U = sm + L.u, *P = sm + L.p, *Lab = sm + L.lab, *Tm = sm + L.t, *X = sm + L.x;
+  const size_t kbase = (size_t)bh * T * dk, vbase = (size_t)bh * T * dv;
+  const Tin *q = static_cast<const Tin *>(p.q) + kbase, *k = static_cast<const Tin *>(p.k) + kbase;
+  const Tin *a = static_cast<const Tin *>(p.a) + kbase, *b = static_cast<const Tin *>(p.b) + kbase;
+  const Tin *v = static_cast<const Tin *>(p.v) + vbase;
+  Tin *o = static_cast<Tin *>(p.o) + vbase;
+
+  for (int i = tid; i < dk * kTile; i += kThreads) {
+    const int c = i / kTile, j = i % kTile;
+    S[c * L.pw + j] = (p.S0 && j < wv) ? p.S0[((size_t)bh * dk + c) * dv + j0 + j] : 0.f;
+  }
+  for (int t0 = 0; t0 < T; t0 += kC) {
+    const int n = min(kC, T - t0);
+    __syncthreads();
+    // ---- stage the chunk (rows past the end are zero) ----
+    for (int i = tid; i < kC * dk; i += kThreads) {
+      const int r = i / dk, c = i % dk;
+      const bool in = r < n;
+      const size_t g = (size_t)(t0 + r) * dk + c;
+      Q[r * L.pk + c] = in ? ld(q + g) : 0.f;
+      K[r * L.pk + c] = in ? ld(k + g) : 0.f;
+      A[r * L.pk + c] = in ? ld(a + g) : 0.f;
+      Bm[r * L.pk + c] = in ? ld(b + g) : 0.f;
+    }
+    for (int i = tid; i < kC * kTile; i += kThreads) {
+      const int r = i / kTile, j = i % kTile;
+      V[r * L.pw + j] = (r < n && j < wv) ? ld(v + (size_t)(t0 + r) * dv + j0 + j) : 0.f;
+    }
+    __syncthreads();
+    // ---- M(Q K^T), L_ab, L_ak ----
+    for (int i = tid; i < kC * kC; i += kThreads) {
+      const int r = i / kC, s = i % kC;
+      float qk = 0.f, ab = 0.f, ak = 0.f;
+      if (s <= r && r < n) {
+        const float *qr = Q + r * L.pk, *ar = A + r * L.pk, *ks = K + s * L.pk, *bs = Bm + s * L.pk;
+        for (int c = 0; c < dk; ++c) {
+          qk = fmaf(qr[c], ks[c], qk);
+          ab = fmaf(ar[c], bs[c], ab);
+          ak = fmaf(ar[c], ks[c], ak);
+        }
+      }
+      P[r * L.pc + s] = qk;
+      Lab[r * L.pc + s] = (s < r) ? ab : 0.f;
+      X[r * L.pc + s] = (s < r) ? ak : 0.f;
+    }
+    __syncthreads();
+    // ---- (I + L_ab)^-1 by forward substitution, one column per thread; R = A S + L_ak V ----
+    if (tid < kC) {
+      const int jc = tid;
+      for (int r = 0; r < kC; ++r) {
+        float acc = (r == jc) ? 1.f : 0.f;
+        for (int s = jc; s < r; ++s) acc = fmaf(-Lab[r * L.pc + s], Tm[s * L.pc + jc], acc);
+        Tm[r * L.pc + jc] = (r < jc) ? 0.f : acc;
+      }
+    }
+    for (int i = tid; i < kC * kTile; i += kThreads) {
+      const int r = i / kTile, j = i % kTile;
+      float acc = 0.f;
+      const float *ar = A + r * L.pk;
+      for (int c = 0; c < dk; ++c) acc = fmaf(ar[c], S[c * L.pw + j], acc);
+      for (int s = 0; s < r; ++s) acc = fmaf(X[r * L.pc + s], V[s * L.pw + j], acc);
+      R[r * L.pw + j] = acc;
+    }
+    __syncthreads();
+    // ---- U = T R; M(Q B^T) into X (L_ak is dead) ----
+    for (int i = tid; i < kC * kTile; i += kThreads) {
+      const int r = i / kTile, j = i % kTile;
+      float acc = 0.f;
+      for (int s = 0; s <= r; ++s) acc = fmaf(Tm[r * L.pc + s], R[s * L.pw + j], acc);
+      U[r * L.pw + j] = acc;
+    }
+    for (int i = tid; i < kC * kC; i += kThreads) {
+      const int r = i / kC, s = i % kC;
+      float qb = 0.f;
+      if (s <= r && r < n) {
+        const float *qr = Q + r * L.pk, *bs = Bm + s * L.pk;
+        for (int c = 0; c < dk; ++c) qb = fmaf(qr[c], bs[c], qb);
+      }
+      X[r * L.pc + s] = qb;
+    }
+    __syncthreads();
+    // ---- O = Q S + M(Q K^T) V - M(Q B^T) U (into R) ----
+    for (int i = tid; i < kC * kTile; i += kThreads) {
+      const int r = i / kTile, j = i % kTile;
+      float acc = 0.f;
+      const float *qr = Q + r * L.pk;
+      for (int c = 0; c < dk; ++c) acc = fmaf(qr[c], S[c * L.pw + j], acc);
+      for (int s = 0; s <= r; ++s) {
+        acc = fmaf(P[r * L.pc + s], V[s * L.pw + j], acc);
+        acc = fmaf(-X[r * L.pc + s], U[s * L.pw + j], acc);
+      }
+      R[r * L.pw + j] = acc;
+    }
+    __syncthreads();
+    for (int i = tid; i < kC * kTile; i += kThreads) {
+      const int r = i / kTile, j = i % kTile;
+      if (r < n && j < wv) st(o + (size_t)(t0 + r) * dv + j0 + j, R[r * L.pw + j]);
+    }
+    // ---- S <- S + K^T V - B^T U ----
+    for (int i = tid; i < dk * kTile; i += kThreads) {
+      const int c = i / kTile, j = i % kTile;
+      float acc = S[c * L.pw + j];
+      for (int s = 0; s < kC; ++s) {
+        acc = fmaf(K[s * L.pk + c], V[s * L.pw + j], acc);
+        acc = fmaf(-Bm[s * L.pk + c], U[s * L.pw + j], acc);
+      }
+      S[c * L.pw + j] = acc;
+    }
+  }
+  __syncthreads();
+  if (p.S_final) {
+    for (int i = tid; i < dk * kTile; i += kThreads) {
+      const int c = i / kTile, j = i % kTile;
+      if (j < wv) p.S_final[((size_t)bh * dk + c) * dv + j0 + j] = S[c * L.pw + j];
+    }
+  }
+}
+
+bool al16(const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; }
+
+}  // namespace
+}  // namespace la
+
+using namespace la;
+
+extern "C" int la_chunk_fwd_gdelta(const void *q, const void *k, const void *v, const void *a, const void *b,
+                                   void *o, const float *S0, float *S_final, int B, int H, int T, int dk, int dv,
+                                   int C, int mode, la_stream_t stream) {
+  const char *fn = "la_chunk_fwd_gdelta";
+  set_error("%s", "");
+  if (!q || !k || !v || !a || !b || !o) {
+    set_error("%s: q, k, v, a, b and o are required", fn);
+    return LA_ERR_INVALID_ARG;
+  }
+  if (B < 1 || H < 1 || T < 1 || (long long)B * H > 0x7fffffffLL) {
+    set_error("%s: B, H and T must be >= 1 (got %d, %d, %d)", fn, B, H, T);
+    return LA_ERR_INVALID_ARG;
+  }
+  if ((dk != 64 && dk != 128) || (dv != 64 && dv != 128)) {
+    set_error("%s: dk and dv must be 64 or 128 (got %d, %d)", fn, dk, dv);
+    return LA_ERR_UNSUPPORTED;
+  }
+  if (mode != 0 && mode != LA_F32) {
+    set_error("%s: mode 0x%x: only 0 (bfloat16 inputs) or LA_F32 (float32 inputs)", fn, mode);
+    return LA_ERR_INVALID_ARG;
+  }
+  if (C != 0 && C != 64) {
+    set_error("%s: chunk length C=%d is not implemented in this build (use 0 or 64)", fn, C);
+    return LA_ERR_UNSUPPORTED;
+  }
+  const void *p16[] = {q, k, v, a, b, o};
+  for (const void *ptr : p16)
+    if (!al16(ptr)) {
+      set_error("%s: q, k, v, a, b and o must be 16-byte aligned", fn);
+      return LA_ERR_INVALID_ARG;
+    }
+  if ((S0 && !al16(S0)) || (S_final && !al16(S_final))) {
+    set_error("%s: S0 and S_final must be 16-byte aligned", fn);
+    return LA_ERR_INVALID_ARG;
+  }
+  const GdParams p{q, k, v, a, b, o, S0, S_final, B, H, T, dk, dv};
+  const GdLayout L = gd_layout(dk);
+  const size_t smem = sizeof(float) * (size_t)L.total;
+  const dim3 grid((unsigned)(B * H), (unsigned)((dv + kTile - 1) / kTile));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (mode == LA_F32) {
+    e = cudaFuncSetAttribute(chunk_gdelta_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) chunk_gdelta_kernel<float><<<grid, kThreads, smem, s>>>(p);
+  } else {
+    e = cudaFuncSetAttribute(chunk_gdelta_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e == cudaSuccess) chunk_gdelta_kernel<__nv_bfloat16><<<grid, kThreads, smem, s>>>(p);
+  }
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("%s: launch failed: %s", fn, cudaGetErrorString(e));
+    return LA_ERR_CUDA;
+  }
+  return LA_OK;
+}

@@ -241,13 +241,38 @@ int la_prologue(const void *xq, const void *xk, const void *xv,
  *   dS0      float32 [B][H][dk][dv] output, or NULL (not computed)
  *   16-byte alignment for every pointer. For LA_RETNET, g_h > -80 (the
  *   passes divide dS_final by gamma_h). C = 0 or 64.
- * Runs as three chunk-forward passes (two on time-reversed copies) on
- * `stream`, with a workspace from the library's pool of
- * B*H*T*(3 dk + 3 dv)*esize + 16*B*H*dk*dv bytes.
+ * Runs as three chunk-forward passes on `stream` (two of them run the
+ * recurrence over the time-reversed sequence, reading and writing the
+ * tensors where they are), with a workspace from the library's pool of
+ * 16*B*H*dk*dv bytes (initial states of the passes).
  */
 int la_chunk_bwd(const void *q, const void *k, const void *v, const float *g, const void *dO,
                  const float *dS_final, const float *S0, void *dq_out, void *dk_out, void *dv_out,
                  float *dS0, int B, int H, int T, int dk, int dv, int C, int mode, la_stream_t stream);
+
+/*
+ * la_chunk_fwd_gdelta -- causal forward of the generalised delta rule, an
+ * identity-plus-rank-one transition between linear-attention steps ("Talk
+ * Linear Attention", section 7.1, which writes the value-major
+ * S_t = S_{t-1}(I - a_t b_t^T) + v_t k_t^T). In this library's key-major
+ * orientation:
+ *
+ *   S_t = (I - b_t a_t^T) S_{t-1} + k_t v_t^T,   o_t = S_t^T q_t
+ *
+ * (retrieve with a_t, erase along b_t, unit write). a = b = sqrt(beta) k with
+ * beta k as the write key gives DeltaNet.
+ *
+ *   q, k, a, b [B][H][T][dk]; v, o [B][H][T][dv]: bfloat16, or float32 with
+ *            mode = LA_F32 (mode 0: bfloat16); 16-byte aligned
+ *   S0, S_final  float32 [B][H][dk][dv] or NULL (zero / not written),
+ *            16-byte aligned; S_final may alias S0
+ *   C        0 or 64
+ * Chunkwise (C = 64) in float32 on the CUDA cores. Errors as la_chunk_fwd;
+ * asynchronous on `stream`, no workspace.
+ */
+int la_chunk_fwd_gdelta(const void *q, const void *k, const void *v, const void *a, const void *b,
+                        void *o, const float *S0, float *S_final, int B, int H, int T, int dk, int dv,
+                        int C, int mode, la_stream_t stream);
 
 /*
  * la_recurrent_step -- one decode step (the recurrent form, "Talk Linear

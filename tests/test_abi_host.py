@@ -30,8 +30,9 @@ def _declared_functions():
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    assert names == sorted(["la_chunk_fwd", "la_chunk_fwd_noalloc", "la_chunk_bwd", "la_recurrent_step",
-                            "la_prologue", "la_stream_status", "la_last_error", "la_version"])
+    assert names == sorted(["la_chunk_fwd", "la_chunk_fwd_noalloc", "la_chunk_fwd_gdelta", "la_chunk_bwd",
+                            "la_recurrent_step", "la_prologue", "la_stream_status", "la_last_error",
+                            "la_version"])
     assert set(names) == set(la.SIGNATURES)
 
 
@@ -208,3 +209,23 @@ def test_chunk_bwd_rejects_bad_arguments(lib, kw, code):
     rc, msg = _bwd(**kw)
     assert rc == la.CONSTANTS[code], (rc, msg)
     assert msg.startswith("la_chunk_bwd")
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(a=None), "LA_ERR_INVALID_ARG"),
+    (dict(b=None), "LA_ERR_INVALID_ARG"),
+    (dict(q=None), "LA_ERR_INVALID_ARG"),
+    (dict(T=0), "LA_ERR_INVALID_ARG"),
+    (dict(dk=96), "LA_ERR_UNSUPPORTED"),
+    (dict(C=128), "LA_ERR_UNSUPPORTED"),
+    (dict(mode=2), "LA_ERR_INVALID_ARG"),              # flags only: 0 or LA_F32
+    (dict(a=A + 4), "LA_ERR_INVALID_ARG"),             # 16-byte alignment
+    (dict(S0=A + 4), "LA_ERR_INVALID_ARG"),
+])
+def test_gdelta_rejects_bad_arguments(lib, kw, code):
+    args = dict(q=A, k=A, v=A, a=A, b=A, o=A, S0=None, S_final=None, B=1, H=1, T=64, dk=64, dv=64,
+                C=0, mode=0, stream=None)
+    args.update(kw)
+    rc = la.la_chunk_fwd_gdelta(**args)
+    assert rc == la.CONSTANTS[code], (rc, la.la_last_error())
+    assert la.la_last_error().startswith("la_chunk_fwd_gdelta:")

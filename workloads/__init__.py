@@ -28,7 +28,7 @@ __all__ = ["Workload", "WORKLOADS", "make_inputs", "MODES", "PrologueWorkload", 
 
 # Mode names used throughout the Python side. The C ABI has its own enum;
 # the binding maps these names onto it.
-MODES = ("linear", "elu1", "retnet", "gla", "scalar", "gdn", "kda", "outer")
+MODES = ("linear", "elu1", "retnet", "gla", "scalar", "gdn", "kda", "outer", "gdelta")
 
 
 @dataclass(frozen=True)
@@ -93,6 +93,11 @@ WORKLOADS = {
     # recipe with GLA-distributed log-gates on both the key and the value axis.
     "outer": Workload("outer", "outer", 8, 16, 8192, 128, 128, "bf16", 64, seed=11,
                       qkv_scale=1.0 / math.sqrt(128.0)),
+    # Generalised delta rule S <- (I - b a^T) S + k v^T (a next row): q, k
+    # L2-normalised, v ~ N(0, 1/4), a = sqrt(beta) k and b = sqrt(beta) times a
+    # unit vector near k (so a != b and a.b = beta cos < 1), beta = sigmoid(N(0,1)).
+    "gdelta": Workload("gdelta", "gdelta", 4, 8, 2048, 64, 64, "bf16", 64, seed=12,
+                       qkv_scale=0.5, l2norm_qk=True, s0=True),
     # One Gated DeltaNet decode step (la_recurrent_step) for a batch of 128
     # sequences x 16 heads with resident states: the gdn recipe with T = 1
     # and a random state S ~ N(0, 0.01).
@@ -148,6 +153,8 @@ def make_inputs(wl: Workload | str, **sizes) -> dict:
     elif wl.mode == "kda":
         g = F.logsigmoid(_normal(gen, (B, H, T, dk))) / 16.0
         beta = torch.sigmoid(_normal(gen, (B, H, T)))
+    elif wl.mode == "gdelta":
+        pass  # its own inputs a and b are drawn below, after S0
     elif wl.mode == "outer":
         # key-axis and value-axis log-gates, both with the GLA gate's distribution;
         # the value-axis gates travel in the beta slot
@@ -159,6 +166,13 @@ def make_inputs(wl: Workload | str, **sizes) -> dict:
         S0 = _normal(gen, (B, H, dk, width), 0.1)  # N(0, 0.01): variance 0.01
 
     dt = wl.torch_dtype
+    a = b = None
+    if wl.mode == "gdelta":  # drawn after S0: sqrt(beta) k and sqrt(beta) (a unit vector near k)
+        wb = torch.sigmoid(_normal(gen, (B, H, T)))
+        e = _normal(gen, (B, H, T, dk), 1.0 / math.sqrt(dk))
+        root = wb.sqrt()[..., None]
+        a = (root * k).to(dt).contiguous()
+        b = (root * F.normalize(k + 0.5 * e, dim=-1)).to(dt).contiguous()
     return {
         "wl": wl,
         "q": q.to(dt).contiguous(),
@@ -167,6 +181,8 @@ def make_inputs(wl: Workload | str, **sizes) -> dict:
         "g": None if g is None else g.contiguous(),
         "beta": None if beta is None else beta.contiguous(),
         "S0": None if S0 is None else S0.contiguous(),
+        "a": a,
+        "b": b,
     }
 
 
