@@ -17,7 +17,12 @@
 //
 // CUDA cores, float32 arithmetic for bf16 or float32 inputs; one CTA per
 // (b, h) and 16-column tile of the value axis, the state slice in shared
-// memory for the whole sequence.
+// memory for the whole sequence. The four C x C products come from one
+// register-tiled pass (a 4 x 4 block of (r, s) per thread, 16 shared-memory
+// loads per 64 FMAs); the retrieved values U are found by forward
+// substitution straight from (I + L_ab) U = R, one value column per half
+// warp (the 16 lanes split the sum and reduce by shuffles), so no inverse
+// is formed.
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -40,7 +45,7 @@ template <> __device__ __forceinline__ void st<__nv_bfloat16>(__nv_bfloat16 *p, 
 
 struct GdLayout {
   int pk, pw, pc;  // row pitches (floats): key rows dk + 1, value rows kTile + 1, C x C rows C + 1
-  int q, k, a, b, v, s, r, u, p, lab, t, x, total;
+  int q, k, a, b, v, s, r, u, p, lab, y, x, total;
 };
 
 __host__ __device__ inline GdLayout gd_layout(int dk) {
@@ -59,8 +64,8 @@ __host__ __device__ inline GdLayout gd_layout(int dk) {
   L.u = o; o += kC * L.pw;
   L.p = o; o += kC * L.pc;   // M(Q K^T)
   L.lab = o; o += kC * L.pc; // L_ab
-  L.t = o; o += kC * L.pc;   // (I + L_ab)^-1
-  L.x = o; o += kC * L.pc;   // L_ak, then M(Q B^T)
+  L.y = o; o += kC * L.pc;   // M(Q B^T)
+  L.x = o; o += kC * L.pc;   // L_ak
   L.total = o;
   return L;
 }
@@ -81,7 +86,8 @@ __global__ void __launch_bounds__(kThreads) chunk_gdelta_kernel(const GdParams p
   const int wv = min(kTile, dv - j0);
   const GdLayout L = gd_layout(dk);
   float *Q = sm + L.q, *K = sm + L.k, *A = sm + L.a, *Bm = sm + L.b, *V = sm + L.v, *S = sm + L.s;
-  float *R = sm + L.r, *U = sm + L.u, *P = sm + L.p, *Lab = sm + L.lab, *Tm = sm + L.t, *X = sm + L.x;
+  float *R = sm + L.r, *U = sm + L.u, *P = sm + L.p, *Lab = sm + L.lab, *Y = sm + L.y, *X = sm + L.x;
+  const int warp = tid >> 5, lane = tid & 31;
   const size_t kbase = (size_t)bh * T * dk, vbase = (size_t)bh * T * dv;
   const Tin *q = static_cast<const Tin *>(p.q) + kbase, *k = static_cast<const Tin *>(p.k) + kbase;
   const Tin *a = static_cast<const Tin *>(p.a) + kbase, *b = static_cast<const Tin *>(p.b) + kbase;
@@ -110,56 +116,63 @@ __global__ void __launch_bounds__(kThreads) chunk_gdelta_kernel(const GdParams p
       V[r * L.pw + j] = (r < n && j < wv) ? ld(v + (size_t)(t0 + r) * dv + j0 + j) : 0.f;
     }
     __syncthreads();
-    // ---- M(Q K^T), L_ab, L_ak ----
-    for (int i = tid; i < kC * kC; i += kThreads) {
-      const int r = i / kC, s = i % kC;
-      float qk = 0.f, ab = 0.f, ak = 0.f;
-      if (s <= r && r < n) {
-        const float *qr = Q + r * L.pk, *ar = A + r * L.pk, *ks = K + s * L.pk, *bs = Bm + s * L.pk;
-        for (int c = 0; c < dk; ++c) {
-          qk = fmaf(qr[c], ks[c], qk);
-          ab = fmaf(ar[c], bs[c], ab);
-          ak = fmaf(ar[c], ks[c], ak);
+    // ---- M(Q K^T), L_ab, L_ak, M(Q B^T): rows tr + 16 i, columns ts + 16 j of one thread ----
+    {
+      const int tr = tid >> 4, ts = tid & 15;
+      float qk[4][4] = {}, ab[4][4] = {}, ak[4][4] = {}, qb[4][4] = {};
+      for (int c = 0; c < dk; ++c) {
+        float qv[4], av[4], kv[4], bv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          qv[i] = Q[(tr + 16 * i) * L.pk + c];
+          av[i] = A[(tr + 16 * i) * L.pk + c];
+          kv[i] = K[(ts + 16 * i) * L.pk + c];
+          bv[i] = Bm[(ts + 16 * i) * L.pk + c];
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            qk[i][j] = fmaf(qv[i], kv[j], qk[i][j]);
+            ab[i][j] = fmaf(av[i], bv[j], ab[i][j]);
+            ak[i][j] = fmaf(av[i], kv[j], ak[i][j]);
+            qb[i][j] = fmaf(qv[i], bv[j], qb[i][j]);
+          }
       }
-      P[r * L.pc + s] = qk;
-      Lab[r * L.pc + s] = (s < r) ? ab : 0.f;
-      X[r * L.pc + s] = (s < r) ? ak : 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = tr + 16 * i, sc = ts + 16 * j;
+          const bool incl = sc <= r && r < n, strict = sc < r && r < n;
+          P[r * L.pc + sc] = incl ? qk[i][j] : 0.f;
+          Y[r * L.pc + sc] = incl ? qb[i][j] : 0.f;
+          Lab[r * L.pc + sc] = strict ? ab[i][j] : 0.f;
+          X[r * L.pc + sc] = strict ? ak[i][j] : 0.f;
+        }
     }
     __syncthreads();
-    // ---- (I + L_ab)^-1 by forward substitution, one column per thread; R = A S + L_ak V ----
-    if (tid < kC) {
-      const int jc = tid;
-      for (int r = 0; r < kC; ++r) {
-        float acc = (r == jc) ? 1.f : 0.f;
-        for (int s = jc; s < r; ++s) acc = fmaf(-Lab[r * L.pc + s], Tm[s * L.pc + jc], acc);
-        Tm[r * L.pc + jc] = (r < jc) ? 0.f : acc;
-      }
-    }
+    // ---- R = A S + L_ak V ----
     for (int i = tid; i < kC * kTile; i += kThreads) {
       const int r = i / kTile, j = i % kTile;
       float acc = 0.f;
       const float *ar = A + r * L.pk;
       for (int c = 0; c < dk; ++c) acc = fmaf(ar[c], S[c * L.pw + j], acc);
-      for (int s = 0; s < r; ++s) acc = fmaf(X[r * L.pc + s], V[s * L.pw + j], acc);
+      for (int sc = 0; sc < r; ++sc) acc = fmaf(X[r * L.pc + sc], V[sc * L.pw + j], acc);
       R[r * L.pw + j] = acc;
     }
     __syncthreads();
-    // ---- U = T R; M(Q B^T) into X (L_ak is dead) ----
-    for (int i = tid; i < kC * kTile; i += kThreads) {
-      const int r = i / kTile, j = i % kTile;
-      float acc = 0.f;
-      for (int s = 0; s <= r; ++s) acc = fmaf(Tm[r * L.pc + s], R[s * L.pw + j], acc);
-      U[r * L.pw + j] = acc;
-    }
-    for (int i = tid; i < kC * kC; i += kThreads) {
-      const int r = i / kC, s = i % kC;
-      float qb = 0.f;
-      if (s <= r && r < n) {
-        const float *qr = Q + r * L.pk, *bs = Bm + s * L.pk;
-        for (int c = 0; c < dk; ++c) qb = fmaf(qr[c], bs[c], qb);
+    // ---- (I + L_ab) U = R by forward substitution: value column 2 warp + (lane >= 16) ----
+    {
+      const int jw = 2 * warp + (lane >> 4), l16 = lane & 15;
+      for (int r = 0; r < kC; ++r) {
+        float part = 0.f;
+        for (int sc = l16; sc < r; sc += 16) part = fmaf(Lab[r * L.pc + sc], U[sc * L.pw + jw], part);
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+        if (l16 == 0) U[r * L.pw + jw] = R[r * L.pw + jw] - part;
+        __syncwarp();
       }
-      X[r * L.pc + s] = qb;
     }
     __syncthreads();
     // ---- O = Q S + M(Q K^T) V - M(Q B^T) U (into R) ----
@@ -170,7 +183,7 @@ __global__ void __launch_bounds__(kThreads) chunk_gdelta_kernel(const GdParams p
       for (int c = 0; c < dk; ++c) acc = fmaf(qr[c], S[c * L.pw + j], acc);
       for (int s = 0; s <= r; ++s) {
         acc = fmaf(P[r * L.pc + s], V[s * L.pw + j], acc);
-        acc = fmaf(-X[r * L.pc + s], U[s * L.pw + j], acc);
+        acc = fmaf(-Y[r * L.pc + s], U[s * L.pw + j], acc);
       }
       R[r * L.pw + j] = acc;
     }
