@@ -39,6 +39,19 @@ constexpr int kTile = 16;  // value columns per CTA
 template <typename T> __device__ __forceinline__ float ld(const T *p);
 template <> __device__ __forceinline__ float ld<float>(const float *p) { return __ldg(p); }
 template <> __device__ __forceinline__ float ld<__nv_bfloat16>(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+// 16 bytes of input -> floats (8 bfloat16 or 4 float32)
+template <typename T> __device__ __forceinline__ void unpack16(uint4 u, float *f);
+template <> __device__ __forceinline__ void unpack16<float>(uint4 u, float *f) {
+  f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y); f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+}
+template <> __device__ __forceinline__ void unpack16<__nv_bfloat16>(uint4 u, float *f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
 template <typename T> __device__ __forceinline__ void st(T *p, float x);
 template <> __device__ __forceinline__ void st<float>(float *p, float x) { *p = x; }
 template <> __device__ __forceinline__ void st<__nv_bfloat16>(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
@@ -101,15 +114,29 @@ __global__ void __launch_bounds__(kThreads) chunk_gdelta_kernel(const GdParams p
   for (int t0 = 0; t0 < T; t0 += kC) {
     const int n = min(kC, T - t0);
     __syncthreads();
-    // ---- stage the chunk (rows past the end are zero) ----
-    for (int i = tid; i < kC * dk; i += kThreads) {
-      const int r = i / dk, c = i % dk;
-      const bool in = r < n;
-      const size_t g = (size_t)(t0 + r) * dk + c;
-      Q[r * L.pk + c] = in ? ld(q + g) : 0.f;
-      K[r * L.pk + c] = in ? ld(k + g) : 0.f;
-      A[r * L.pk + c] = in ? ld(a + g) : 0.f;
-      Bm[r * L.pk + c] = in ? ld(b + g) : 0.f;
+    // ---- stage the chunk (rows past the end are zero), 16-byte loads all in flight ----
+    {
+      constexpr int kVec = 16 / (int)sizeof(Tin);
+      const int gpr = dk / kVec;
+      for (int i = tid; i < kC * gpr; i += kThreads) {
+        const int r = i / gpr, c0 = (i % gpr) * kVec;
+        uint4 u[4] = {};
+        if (r < n) {
+          const size_t g = ((size_t)(t0 + r) * dk + c0) / kVec;
+          u[0] = __ldg(reinterpret_cast<const uint4 *>(q) + g);
+          u[1] = __ldg(reinterpret_cast<const uint4 *>(k) + g);
+          u[2] = __ldg(reinterpret_cast<const uint4 *>(a) + g);
+          u[3] = __ldg(reinterpret_cast<const uint4 *>(b) + g);
+        }
+        float *dst[4] = {Q, K, A, Bm};
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          float f[kVec];
+          unpack16<Tin>(u[m], f);
+#pragma unroll
+          for (int e = 0; e < kVec; ++e) dst[m][r * L.pk + c0 + e] = f[e];
+        }
+      }
     }
     for (int i = tid; i < kC * kTile; i += kThreads) {
       const int r = i / kTile, j = i % kTile;
@@ -152,14 +179,23 @@ __global__ void __launch_bounds__(kThreads) chunk_gdelta_kernel(const GdParams p
         }
     }
     __syncthreads();
-    // ---- R = A S + L_ak V ----
-    for (int i = tid; i < kC * kTile; i += kThreads) {
-      const int r = i / kTile, j = i % kTile;
-      float acc = 0.f;
-      const float *ar = A + r * L.pk;
-      for (int c = 0; c < dk; ++c) acc = fmaf(ar[c], S[c * L.pw + j], acc);
-      for (int sc = 0; sc < r; ++sc) acc = fmaf(X[r * L.pc + sc], V[sc * L.pw + j], acc);
-      R[r * L.pw + j] = acc;
+    // value column jt = tid % 16 and rows rt + 16 i of one thread (four independent sums)
+    const int jt = tid & 15, rt = tid >> 4;
+    // ---- R = A S + L_ak V (L_ak is zero on and above the diagonal) ----
+    {
+      float acc[4] = {};
+      for (int c = 0; c < dk; ++c) {
+        const float sv = S[c * L.pw + jt];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] = fmaf(A[(rt + 16 * i) * L.pk + c], sv, acc[i]);
+      }
+      for (int sc = 0; sc < kC; ++sc) {
+        const float vv = V[sc * L.pw + jt];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] = fmaf(X[(rt + 16 * i) * L.pc + sc], vv, acc[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) R[(rt + 16 * i) * L.pw + jt] = acc[i];
     }
     __syncthreads();
     // ---- (I + L_ab) U = R by forward substitution: value column 2 warp + (lane >= 16) ----
@@ -175,32 +211,48 @@ __global__ void __launch_bounds__(kThreads) chunk_gdelta_kernel(const GdParams p
       }
     }
     __syncthreads();
-    // ---- O = Q S + M(Q K^T) V - M(Q B^T) U (into R) ----
-    for (int i = tid; i < kC * kTile; i += kThreads) {
-      const int r = i / kTile, j = i % kTile;
-      float acc = 0.f;
-      const float *qr = Q + r * L.pk;
-      for (int c = 0; c < dk; ++c) acc = fmaf(qr[c], S[c * L.pw + j], acc);
-      for (int s = 0; s <= r; ++s) {
-        acc = fmaf(P[r * L.pc + s], V[s * L.pw + j], acc);
-        acc = fmaf(-Y[r * L.pc + s], U[s * L.pw + j], acc);
+    // ---- O = Q S + M(Q K^T) V - M(Q B^T) U (into R; the masked products are zero above the diagonal) ----
+    {
+      float acc[4] = {};
+      for (int c = 0; c < dk; ++c) {
+        const float sv = S[c * L.pw + jt];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] = fmaf(Q[(rt + 16 * i) * L.pk + c], sv, acc[i]);
       }
-      R[r * L.pw + j] = acc;
+      for (int sc = 0; sc < kC; ++sc) {
+        const float vv = V[sc * L.pw + jt], uu = U[sc * L.pw + jt];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[i] = fmaf(P[(rt + 16 * i) * L.pc + sc], vv, acc[i]);
+          acc[i] = fmaf(-Y[(rt + 16 * i) * L.pc + sc], uu, acc[i]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) R[(rt + 16 * i) * L.pw + jt] = acc[i];
     }
     __syncthreads();
     for (int i = tid; i < kC * kTile; i += kThreads) {
       const int r = i / kTile, j = i % kTile;
       if (r < n && j < wv) st(o + (size_t)(t0 + r) * dv + j0 + j, R[r * L.pw + j]);
     }
-    // ---- S <- S + K^T V - B^T U ----
-    for (int i = tid; i < dk * kTile; i += kThreads) {
-      const int c = i / kTile, j = i % kTile;
-      float acc = S[c * L.pw + j];
-      for (int s = 0; s < kC; ++s) {
-        acc = fmaf(K[s * L.pk + c], V[s * L.pw + j], acc);
-        acc = fmaf(-Bm[s * L.pk + c], U[s * L.pw + j], acc);
+    // ---- S <- S + K^T V - B^T U: key rows rt + 16 i (i < dk / 16) of column jt ----
+    {
+      const int nc = dk / 16;
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = (i < nc) ? S[(rt + 16 * i) * L.pw + jt] : 0.f;
+      for (int sc = 0; sc < kC; ++sc) {
+        const float vv = V[sc * L.pw + jt], uu = U[sc * L.pw + jt];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (i < nc) {
+            acc[i] = fmaf(K[sc * L.pk + rt + 16 * i], vv, acc[i]);
+            acc[i] = fmaf(-Bm[sc * L.pk + rt + 16 * i], uu, acc[i]);
+          }
       }
-      S[c * L.pw + j] = acc;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (i < nc) S[(rt + 16 * i) * L.pw + jt] = acc[i];
     }
   }
   __syncthreads();
