@@ -98,8 +98,10 @@ typedef struct CUstream_st *la_stream_t;
  * holding log alpha; the beta argument carries float32 [B][H][T][dv] holding
  * log beta (both required, 16-byte aligned; per step [B][H][dk] and
  * [B][H][dv]). bfloat16 inputs only in la_chunk_fwd. Chunked evaluation
- * folds both axes' gates around the chunk midpoint, with LA_GLA's range
- * limit on each axis. */
+ * folds both axes' gates around the chunk midpoint; the range limit of
+ * LA_GLA applies to the sum of the two axes' log-gates: for every key
+ * channel c and value column j, log alpha_c + log beta_j summed over half a
+ * chunk (32 tokens) must stay above about -80, else the state overflows. */
 #define LA_OUTER_GATE    7
 /* Flag: q, k, v and o are float32 instead of bfloat16. */
 #define LA_F32           0x100
