@@ -27,7 +27,7 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["backward"]
+__all__ = ["backward", "backward_scalar"]
 
 
 def backward(q, k, v, dO, mode, g=None, S0=None, dS=None):
@@ -66,3 +66,45 @@ def backward(q, k, v, dO, mode, g=None, S0=None, dS=None):
             dv[b, h] = Mk.T @ G + a_last[:, None] * (K @ dS[b, h])
             dS0[b, h] = (Q * a_t1[:, None]).T @ G + aT * dS[b, h]
     return dq, dk, dv, dS0
+
+
+def backward_scalar(q, k, v, dO, g, S0=None, dS=None):
+    """The same gradients for the data-dependent scalar decay (alpha_t =
+    exp(g_t), g [B, H, T]), plus the gradient of the log-gates. With the
+    inclusive prefix G_t = sum_{tau<=t} g_tau the decay between positions is
+    alpha(t, s) = exp(G_t - G_s), so dq, dk, dv and dS0 are the sums above with
+    those factors, and, since G_u enters with + where u reads (o_u, and
+    S_final through G_{T-1}) and with - where u writes,
+
+      dL/dG_u = q_u . dq_u - k_u . dk_u + [u = T-1] sum(dS ⊙ S_final),
+      dg_tau  = sum_{u >= tau} dL/dG_u.
+
+    Returns dq, dk, dv, dS0, dg (float64)."""
+    q, k, v, dO, g = (np.asarray(x, dtype=np.float64) for x in (q, k, v, dO, g))
+    B, H, T, dkk = q.shape
+    dvv = v.shape[-1]
+    S0 = np.zeros((B, H, dkk, dvv)) if S0 is None else np.asarray(S0, dtype=np.float64)
+    dS = np.zeros((B, H, dkk, dvv)) if dS is None else np.asarray(dS, dtype=np.float64)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    dS0 = np.zeros_like(S0)
+    dg = np.zeros((B, H, T))
+    tri = np.tril(np.ones((T, T)))
+    for b in range(B):
+        for h in range(H):
+            G = np.cumsum(g[b, h])
+            D = np.exp(np.where(tri > 0, G[:, None] - G[None, :], -np.inf))   # alpha(t, s), s <= t
+            a_t1 = np.exp(G)                  # alpha(t, -1)
+            a_last = np.exp(G[-1] - G)        # alpha(T-1, s)
+            aT = np.exp(G[-1])
+            Q, K, V, Gd = q[b, h], k[b, h], v[b, h], dO[b, h]
+            Mo = (Gd @ V.T) * D
+            Mk = (Q @ K.T) * D
+            dq[b, h] = a_t1[:, None] * (Gd @ S0[b, h].T) + Mo @ K
+            dk[b, h] = Mo.T @ Q + a_last[:, None] * (V @ dS[b, h].T)
+            dv[b, h] = Mk.T @ Gd + a_last[:, None] * (K @ dS[b, h])
+            dS0[b, h] = (Q * a_t1[:, None]).T @ Gd + aT * dS[b, h]
+            S_T = aT * S0[b, h] + (K * a_last[:, None]).T @ V
+            dG = np.sum(Q * dq[b, h], axis=1) - np.sum(K * dk[b, h], axis=1)
+            dG[-1] += np.sum(dS[b, h] * S_T)
+            dg[b, h] = np.cumsum(dG[::-1])[::-1]
+    return dq, dk, dv, dS0, dg

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from oracle import recurrence
-from oracle.backward import backward
+from oracle.backward import backward, backward_scalar
 
 RNG = np.random.default_rng(5)
 
@@ -85,3 +85,73 @@ def test_planted_mistakes_are_caught():
     _, bad2, _, _ = backward(q, k, v, dO, "retnet", g=g, S0=S0, dS=None)
     assert not np.allclose(bad_dk, tk.grad.numpy(), atol=1e-6)
     assert not np.allclose(bad2, tk.grad.numpy(), atol=1e-6)
+
+
+# --- the data-dependent scalar decay, with the gradient of the log-gates ---------
+
+def _scalar_case(B=1, H=2, T=9, dk=3, dv=4):
+    q, k, v, _, S0, dO, dS = _case("linear", B=B, H=H, T=T, dk=dk, dv=dv)
+    g = -np.abs(RNG.standard_normal((B, H, T))) * 0.3
+    return q, k, v, g, S0, dO, dS
+
+
+def test_scalar_backward_matches_finite_differences():
+    q, k, v, g, S0, dO, dS = _scalar_case()
+    grads = dict(zip(("q", "k", "v", "S0", "g"), (backward_scalar(q, k, v, dO, g, S0=S0, dS=dS)[i]
+                                                   for i in (0, 1, 2, 3, 4))))
+    eps = 1e-6
+    for name, x in (("q", q), ("k", k), ("v", v), ("S0", S0), ("g", g)):
+        num = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            old = x[idx]
+            x[idx] = old + eps
+            lp = _loss(q, k, v, g, S0, dO, dS, "scalar")
+            x[idx] = old - eps
+            lm = _loss(q, k, v, g, S0, dO, dS, "scalar")
+            x[idx] = old
+            num[idx] = (lp - lm) / (2 * eps)
+        assert np.allclose(grads[name], num, rtol=1e-6, atol=1e-7), name
+
+
+def test_scalar_backward_matches_autograd():
+    q, k, v, g, S0, dO, dS = _scalar_case(B=2, H=2, T=40, dk=5, dv=6)
+    tq, tk, tv, tg, tS0 = (torch.tensor(x, requires_grad=True) for x in (q, k, v, g, S0))
+    S = tS0
+    outs = []
+    for t in range(40):  # written afresh for autograd: per-token scalar decay, then the write
+        S = torch.exp(tg[:, :, t])[..., None, None] * S + tk[:, :, t, :, None] * tv[:, :, t, None, :]
+        outs.append(torch.einsum("bhc,bhcv->bhv", tq[:, :, t], S))
+    o = torch.stack(outs, dim=2)
+    (o * torch.tensor(dO)).sum().add((S * torch.tensor(dS)).sum()).backward()
+    got = backward_scalar(q, k, v, dO, g, S0=S0, dS=dS)
+    for name, a, b in zip(("q", "k", "v", "S0", "g"), got, (tq.grad, tk.grad, tv.grad, tS0.grad, tg.grad)):
+        assert np.allclose(a, b.numpy(), rtol=1e-10, atol=1e-11), name
+
+
+def test_scalar_backward_with_zero_gates_is_linear():
+    q, k, v, g, S0, dO, dS = _scalar_case(T=20)
+    lin = backward(q, k, v, dO, "linear", S0=S0, dS=dS)
+    sc = backward_scalar(q, k, v, dO, np.zeros_like(g), S0=S0, dS=dS)
+    for a, b in zip(lin, sc[:4]):
+        assert np.allclose(a, b, rtol=0, atol=1e-12)
+
+
+def test_scalar_dg_pins_catch_an_exclusive_suffix_sum():
+    q, k, v, g, S0, dO, dS = _scalar_case()
+    dg = backward_scalar(q, k, v, dO, g, S0=S0, dS=dS)[4]
+    eps = 1e-6
+    num = np.zeros_like(g)
+    for idx in np.ndindex(g.shape):
+        old = g[idx]
+        g[idx] = old + eps
+        lp = _loss(q, k, v, g, S0, dO, dS, "scalar")
+        g[idx] = old - eps
+        lm = _loss(q, k, v, g, S0, dO, dS, "scalar")
+        g[idx] = old
+        num[idx] = (lp - lm) / (2 * eps)
+    assert np.allclose(dg, num, rtol=1e-6, atol=1e-7)
+    # the suffix sum taken exclusively (the token's own term dropped) is rejected
+    shifted = np.concatenate([dg[..., 1:], np.zeros_like(dg[..., :1])], axis=-1)
+    assert not np.allclose(shifted, num, rtol=1e-3, atol=1e-4)
