@@ -54,6 +54,7 @@ KERNEL_SOURCES = {
     "linear_fp32": [_CS + "la_chunk_simt.cu"],
     "noncausal": [_CS + "la_chunk_mat.cu"] + _COMMON,
     "backward": [_CS + "la_backward.cu", _CS + "la_chunk_ws.cu", _CS + "la_chunk_mat.cu"] + _COMMON,
+    "backward_scalar": [_CS + "la_backward.cu", _CS + "la_chunk_ws.cu", _CS + "la_chunk_mat.cu"] + _COMMON,
     "decode": [_CS + "la_step.cu"],
     "gdelta": [_CS + "la_chunk_gdelta.cu"],
     "prologue": [_CS + "la_prologue.cu", _CS + "la_sm100.cuh"],
@@ -728,19 +729,24 @@ def backward_bytes(wl) -> float:
     once, read dS_final and write dS0."""
     e = 2 if wl.dtype == "bf16" else 4
     per_tok = e * (2 * wl.dk + 2 * wl.dv) + e * (2 * wl.dk + wl.dv)
+    if wl.mode == "scalar":  # read g, write dg
+        per_tok += 8
     return float(wl.B * wl.H * (wl.T * per_tok + 2 * 4 * wl.dk * wl.dv))
 
 
 def time_backward_oracle(wl, inp, target_s: float = 10.0):
-    from oracle.backward import backward
+    from oracle.backward import backward, backward_scalar
     f64 = lambda t: None if t is None else t.to(torch.float64).numpy()
     BH = wl.B * wl.H
     done, t0 = 0, time.perf_counter()
     while done < BH and (time.perf_counter() - t0) < target_s:
         b, h = done // wl.H, done % wl.H
         sl = lambda t: f64(t[b:b + 1, h:h + 1])
-        backward(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["dO"]), wl.mode,
-                 g=None if inp["g"] is None else f64(inp["g"])[h:h + 1], dS=sl(inp["dS"]))
+        if wl.mode == "scalar":
+            backward_scalar(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["dO"]), sl(inp["g"]), dS=sl(inp["dS"]))
+        else:
+            backward(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["dO"]), wl.mode,
+                     g=None if inp["g"] is None else f64(inp["g"])[h:h + 1], dS=sl(inp["dS"]))
         done += 1
     dt = time.perf_counter() - t0
     return (done * wl.T / wl.H) / dt, 1, f"{done} of {BH} (batch, head) sequences, full T={wl.T}, float64 numpy", dt
@@ -788,13 +794,15 @@ def bench_backward(args, rank, world, local_rank):
     d = {n: inp[n].to(dev) for n in names}
     outs = {"dq": torch.empty_like(d["q"]), "dk": torch.empty_like(d["k"]), "dv": torch.empty_like(d["v"]),
             "dS0": torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)}
+    if wl.mode == "scalar":
+        outs["dg"] = torch.empty(B, H, T, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     mode_id = la.MODE_IDS[wl.mode] | (la.CONSTANTS["LA_F32"] if wl.dtype == "f32" else 0)
 
     def step(dd, oo):
         rc = la.la_chunk_bwd(dd["q"], dd["k"], dd["v"], dd.get("g"), dd["dO"], dd["dS"], None, oo["dq"], oo["dk"],
-                             oo["dv"], oo["dS0"], B, H, T, dk, dv, wl.C, mode_id, sh)
+                             oo["dv"], oo["dS0"], oo.get("dg"), B, H, T, dk, dv, wl.C, mode_id, sh)
         if rc != 0:
             raise RuntimeError(la.la_last_error())
 
@@ -830,7 +838,8 @@ def bench_backward(args, rank, world, local_rank):
     achieved = alg / (statistics.mean(launch_ms) / 1e3) / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
             "frac": round(achieved / hbm_peak, 4), "traffic": recorded_traffic(wl.name), "peak_source": peak_src,
-            "algorithmic_bytes": alg, "kernel": "3 x chunk_ws_kernel (dq causal; dk and dv reversed runs)",
+            "algorithmic_bytes": alg, "kernel": "3 x chunk_ws_kernel (dq causal; dk and dv reversed runs)"
+            + (" + forward for S_final + dg_kernel" if wl.mode == "scalar" else ""),
             "launch_ms_mean": round(statistics.mean(launch_ms), 4)}
     e2e = None
     if not args.no_e2e:
@@ -875,7 +884,8 @@ def bench_backward(args, rank, world, local_rank):
             "data": "synthetic (seeded; shapes and distributions of the workload)", "config": cfg,
             "tflops": round(world * flop * args.steps / (total_ms / 1e3) / 1e12, 2), "roofline": roof,
             "cpu_baseline": cpu, "clocks": clk, "e2e": e2e,
-            "gpu_launches": args.steps * 5,  # state prep, 3 forward passes, dS0 scaling
+            # state prep, 3 passes, dS0 scaling (+ the forward for S_final and the dg suffix sums)
+            "gpu_launches": args.steps * (7 if wl.mode == "scalar" else 5),
         }), flush=True)
     if dist:
         dist.destroy_process_group()

@@ -51,7 +51,7 @@ SIGNATURES = {
     "la_chunk_fwd_gdelta": ([_P] * 8 + [_I] * 7 + [_P], _I),
     "la_chunk_fwd_noalloc": ([_P] * 8 + [_I] * 7 + [_P], _I),
     "la_recurrent_step": ([_P] * 7 + [_I] * 5 + [_P], _I),
-    "la_chunk_bwd": ([_P] * 11 + [_I] * 7 + [_P], _I),
+    "la_chunk_bwd": ([_P] * 12 + [_I] * 7 + [_P], _I),
     "la_prologue": ([_P] * 6 + [_I] + [_P] * 3 + [_I, _I, _F] + [_P] * 6 + [_I] * 6 + [_P], _I),
     "la_stream_status": ([_P], _I),
     "la_last_error": ([], ctypes.c_char_p),
@@ -110,10 +110,11 @@ def la_chunk_fwd_gdelta(q, k, v, a, b, o, S0, S_final, B, H, T, dk, dv, C, mode,
                                               _ptr(S0), _ptr(S_final), B, H, T, dk, dv, C, mode, stream)
 
 
-def la_chunk_bwd(q, k, v, g, dO, dS_final, S0, dq_out, dk_out, dv_out, dS0, B, H, T, dk, dv, C, mode, stream):
+def la_chunk_bwd(q, k, v, g, dO, dS_final, S0, dq_out, dk_out, dv_out, dS0, dg_out, B, H, T, dk, dv, C, mode,
+                 stream):
     return load_library().la_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(dO), _ptr(dS_final), _ptr(S0),
-                                       _ptr(dq_out), _ptr(dk_out), _ptr(dv_out), _ptr(dS0), B, H, T, dk, dv, C,
-                                       mode, stream)
+                                       _ptr(dq_out), _ptr(dk_out), _ptr(dv_out), _ptr(dS0), _ptr(dg_out), B, H, T,
+                                       dk, dv, C, mode, stream)
 
 
 def la_recurrent_step(q, k, v, g, beta, o, S, B, H, dk, dv, mode, stream):
@@ -242,9 +243,10 @@ def chunk_fwd_gdelta(q, k, v, a, b, S0=None, C=0, with_state=True, o=None, S_fin
     return o, (S_final if with_state else None)
 
 
-def chunk_bwd(q, k, v, dO, mode, g=None, S0=None, dS_final=None, with_dS0=True, C=0, stream=None):
-    """Backward pass of chunk_fwd for "linear" and "retnet": returns dq, dk, dv
-    (dtype of q) and dS0 (float32, or None)."""
+def chunk_bwd(q, k, v, dO, mode, g=None, S0=None, dS_final=None, with_dS0=True, with_dg=True, C=0, stream=None):
+    """Backward pass of chunk_fwd for "linear", "retnet" and "scalar": returns
+    dq, dk, dv (dtype of q), dS0 (float32, or None) and dg (float32 [B,H,T]
+    for "scalar" with with_dg, else None)."""
     import torch
     for name, t in (("q", q), ("k", k), ("v", v), ("dO", dO), ("g", g), ("S0", S0), ("dS_final", dS_final)):
         _check(t, name)
@@ -253,11 +255,13 @@ def chunk_bwd(q, k, v, dO, mode, g=None, S0=None, dS_final=None, with_dS0=True, 
     mid = _mode_id(mode, q.dtype)
     dq, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dS0 = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device) if with_dS0 else None
-    rc = la_chunk_bwd(q, k, v, g, dO, dS_final, S0, dq, dk_, dv_, dS0, B, H, T, dk, dv, C, mid,
+    scalar = (mid & 0xFF) == CONSTANTS["LA_SCALAR_GATE"]
+    dg = torch.empty((B, H, T), dtype=torch.float32, device=q.device) if (scalar and with_dg) else None
+    rc = la_chunk_bwd(q, k, v, g, dO, dS_final, S0, dq, dk_, dv_, dS0, dg, B, H, T, dk, dv, C, mid,
                       _stream_handle(stream))
     if rc != 0:
         raise LAError(rc, la_last_error())
-    return dq, dk_, dv_, dS0
+    return dq, dk_, dv_, dS0, dg
 
 
 def recurrent_step(q, k, v, S, mode, g=None, beta=None, o=None, stream=None):

@@ -1,7 +1,8 @@
-// la_chunk_bwd: the backward pass of la_chunk_fwd for plain linear attention
-// and RetNet's fixed decay ("Talk Linear Attention" sections 2.1 and 5.2; the
-// states are recomputed, as section 4.1.2 describes, not stored). With
-// alpha = 1 or gamma_h,
+// la_chunk_bwd: the backward pass of la_chunk_fwd for plain linear attention,
+// RetNet's fixed decay and the data-dependent scalar decay ("Talk Linear
+// Attention" sections 2.1 and 5.2; the states are recomputed, as section
+// 4.1.2 describes, not stored). With alpha = 1 or gamma_h (for the scalar
+// decay, alpha^(t-s) reads as the product of the gates of s+1 .. t),
 //
 //   dq_t = alpha^(t+1) S0 dO_t + sum_{s<=t} alpha^(t-s) (dO_t . v_s) k_s
 //   dk_s = sum_{t>=s} alpha^(t-s) (dO_t . v_s) q_t + alpha^(T-1-s) dS v_s
@@ -15,7 +16,14 @@
 // dS^T / alpha and dS / alpha), and dS0 = alpha times the last pass's final
 // state. The reversed passes are the forward kernels' reversed runs, which
 // read and write the tensors in stored order, so nothing is copied; this file
-// adds the initial-state preparation.
+// adds the initial-state preparation. For the scalar decay the reversed runs
+// take each position's gate from the stored token after it, so the initial
+// states need no division, dS0 = alpha_0 times the last pass's final state,
+// and the log-gate gradient is a suffix sum,
+//
+//   dg_tau = sum_{u >= tau} (q_u . dq_u - k_u . dk_u) + sum(dS_final ⊙ S_final),
+//
+// with S_final from a fourth (forward) pass.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -33,7 +41,7 @@ __global__ void __launch_bounds__(256) state_prep_kernel(const float *__restrict
                                                          float *__restrict__ s0t, float *__restrict__ dst,
                                                          float *__restrict__ dss) {
   const int bh = blockIdx.y;
-  const float inv = g ? expf(-__ldg(g + bh % H)) : 1.f;
+  const float inv = g ? expf(-__ldg(g + bh % H)) : 1.f;  // g: RetNet's per-head log-decay, else NULL
   const size_t base = (size_t)bh * dk * dv;
   for (int i = blockIdx.x * 256 + threadIdx.x; i < dk * dv; i += gridDim.x * 256) {
     const int c = i / dv, v = i % dv;  // element (c, v) of a [dk][dv] state
@@ -46,13 +54,68 @@ __global__ void __launch_bounds__(256) state_prep_kernel(const float *__restrict
   }
 }
 
-// dS0 = alpha * S, per head
+// dS0 = alpha * S, per head: alpha = exp(g[h]) (RetNet, gstride 0) or the
+// first token's gate exp(g[bh * gstride]) (scalar decay, gstride T)
 __global__ void __launch_bounds__(256) scale_state_kernel(const float *__restrict__ S, const float *__restrict__ g,
-                                                          int H, int n, float *__restrict__ out) {
+                                                          int H, long long gstride, int n, float *__restrict__ out) {
   const int bh = blockIdx.y;
-  const float a = g ? expf(__ldg(g + bh % H)) : 1.f;
+  const float a = g ? expf(__ldg(g + (gstride ? (size_t)bh * gstride : (size_t)(bh % H)))) : 1.f;
   for (int i = blockIdx.x * 256 + threadIdx.x; i < n; i += gridDim.x * 256)
     out[(size_t)bh * n + i] = a * S[(size_t)bh * n + i];
+}
+
+template <typename T> __device__ __forceinline__ float ldf(const T *p);
+template <> __device__ __forceinline__ float ldf<float>(const float *p) { return __ldg(p); }
+template <> __device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+
+// dg for the scalar decay, one CTA per (b, h): w_u = q_u . dq_u - k_u . dk_u
+// (one token per thread), a suffix scan over 256-token tiles from the end of
+// the sequence, plus the final-state term c = sum(dS ⊙ S_final).
+template <typename Tin>
+__global__ void __launch_bounds__(256) dg_kernel(const Tin *__restrict__ q, const Tin *__restrict__ dq,
+                                                 const Tin *__restrict__ k, const Tin *__restrict__ dk,
+                                                 const float *__restrict__ dS, const float *__restrict__ S_final,
+                                                 int T, int dkk, int dv, float *__restrict__ dg) {
+  __shared__ float red[8];
+  const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float c = 0.f;
+  if (dS)
+    for (int i = tid; i < dkk * dv; i += 256) c = fmaf(dS[(size_t)bh * dkk * dv + i], S_final[(size_t)bh * dkk * dv + i], c);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+  if (lane == 0) red[warp] = c;
+  __syncthreads();
+  c = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) c += red[w];
+  __syncthreads();
+  const size_t base = (size_t)bh * T;
+  float carry = c;
+  for (int t1 = T; t1 > 0; t1 -= 256) {  // tile [t1 - 256, t1), the last tokens first
+    const int u = t1 - 256 + tid;
+    float w = 0.f;
+    if (u >= 0) {
+      const size_t r = (base + u) * dkk;
+      for (int e = 0; e < dkk; ++e) w += ldf(q + r + e) * ldf(dq + r + e) - ldf(k + r + e) * ldf(dk + r + e);
+    }
+    // inclusive suffix sum within the warp, then over the later warps of the tile
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float y = __shfl_down_sync(0xffffffffu, w, off);
+      if (lane + off < 32) w += y;
+    }
+    if (lane == 0) red[warp] = w;
+    __syncthreads();
+    float later = 0.f, tile = 0.f;
+#pragma unroll
+    for (int wq = 0; wq < 8; ++wq) {
+      tile += red[wq];
+      if (wq > warp) later += red[wq];
+    }
+    if (u >= 0) dg[base + u] = carry + later + w;
+    carry += tile;
+    __syncthreads();
+  }
 }
 
 bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -76,7 +139,8 @@ using namespace la;
 
 extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const float *g, const void *dO,
                             const float *dS_final, const float *S0, void *dq_out, void *dk_out, void *dv_out,
-                            float *dS0, int B, int H, int T, int dk, int dv, int C, int mode, la_stream_t stream) {
+                            float *dS0, float *dg_out, int B, int H, int T, int dk, int dv, int C, int mode,
+                            la_stream_t stream) {
   void *dq = dq_out, *dkg = dk_out, *dvg = dv_out;
   const int dk_ = dk, dv_ = dv;
   const char *fn = "la_chunk_bwd";
@@ -94,13 +158,19 @@ extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const f
     set_error("%s: dk and dv must be 64 or 128 (got %d, %d)", fn, dk_, dv_);
     return LA_ERR_UNSUPPORTED;
   }
-  if ((mode & ~(0xff | LA_F32)) != 0 || (kind != LA_LINEAR && kind != LA_RETNET)) {
-    set_error("%s: mode 0x%x: the backward pass covers LA_LINEAR and LA_RETNET (optionally | LA_F32)", fn, mode);
+  if ((mode & ~(0xff | LA_F32)) != 0 || (kind != LA_LINEAR && kind != LA_RETNET && kind != LA_SCALAR_GATE)) {
+    set_error("%s: mode 0x%x: the backward pass covers LA_LINEAR, LA_RETNET and LA_SCALAR_GATE (optionally | LA_F32)",
+              fn, mode);
     return (mode & ~(0xff | LA_F32)) == 0 && kind >= LA_LINEAR && kind <= LA_OUTER_GATE ? LA_ERR_UNSUPPORTED
                                                                                   : LA_ERR_INVALID_ARG;
   }
-  if ((kind == LA_RETNET) != (g != nullptr)) {
-    set_error("%s: LA_RETNET needs g (float32 [H] log-decay), LA_LINEAR takes none", fn);
+  const bool scalar = kind == LA_SCALAR_GATE;
+  if ((kind == LA_LINEAR) != (g == nullptr)) {
+    set_error("%s: LA_RETNET needs g (float32 [H]) and LA_SCALAR_GATE g (float32 [B][H][T]); LA_LINEAR takes none", fn);
+    return LA_ERR_INVALID_ARG;
+  }
+  if (dg_out && !scalar) {
+    set_error("%s: dg is the gradient of LA_SCALAR_GATE's log-gates (NULL for other modes)", fn);
     return LA_ERR_INVALID_ARG;
   }
   if (C != 0 && C != 64) {
@@ -113,16 +183,19 @@ extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const f
       set_error("%s: q, k, v, dO, dq, dk and dv must be 16-byte aligned", fn);
       return LA_ERR_INVALID_ARG;
     }
-  if ((S0 && !al16(S0)) || (dS_final && !al16(dS_final)) || (dS0 && !al16(dS0)) || (g && !al16(g))) {
-    set_error("%s: S0, dS_final, dS0 and g must be 16-byte aligned", fn);
+  if ((S0 && !al16(S0)) || (dS_final && !al16(dS_final)) || (dS0 && !al16(dS0)) || (g && !al16(g)) ||
+      (dg_out && !al16(dg_out))) {
+    set_error("%s: S0, dS_final, dS0, g and dg must be 16-byte aligned", fn);
     return LA_ERR_INVALID_ARG;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool f32 = (mode & LA_F32) != 0;
+  const size_t esz = f32 ? 4 : 2;
   const size_t BH = (size_t)B * H;
-  // workspace: three initial states and the last pass's final state
+  // workspace: three initial states and the last pass's final state; for dg also the
+  // forward's final state and a scratch output of the forward pass that produces it
   const size_t n_s = BH * dk_ * dv_ * 4;
-  const size_t bytes = 4 * n_s;
+  const size_t bytes = (dg_out ? 5 : 4) * n_s + (dg_out ? BH * (size_t)T * dv_ * esz : 0);
   uint8_t *ws = nullptr;
   cudaMemPool_t pool = library_pool();
   if (!pool) {
@@ -135,7 +208,8 @@ extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const f
     return LA_ERR_CUDA;
   }
   float *s0t = reinterpret_cast<float *>(ws), *dst = s0t + BH * dk_ * dv_, *dss = dst + BH * dk_ * dv_,
-        *sfin = dss + BH * dk_ * dv_;
+        *sfin = dss + BH * dk_ * dv_, *sT = sfin + BH * dk_ * dv_;
+  void *oscr = sT + BH * dk_ * dv_;
   int rc = LA_OK;
   auto fail = [&](const char *what) {
     if (rc == LA_OK) {
@@ -143,8 +217,11 @@ extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const f
       rc = LA_ERR_CUDA;
     }
   };
+  // RetNet's reversed passes use the unshifted per-head decay, so their initial
+  // states carry 1 / gamma; the scalar decay's reversed runs shift the gates instead
+  const float *g_head = kind == LA_RETNET ? g : nullptr;
   if (S0 || dS_final) {
-    state_prep_kernel<<<dim3(8, (unsigned)BH), 256, 0, s>>>(S0, dS_final, g, H, dk_, dv_, s0t, dst, dss);
+    state_prep_kernel<<<dim3(8, (unsigned)BH), 256, 0, s>>>(S0, dS_final, g_head, H, dk_, dv_, s0t, dst, dss);
     if (cudaGetLastError() != cudaSuccess) fail("initial-state preparation");
   }
   const int fwd_mode = mode & (0xff | LA_F32);
@@ -156,16 +233,35 @@ extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const f
       rc = r;
     }
   }
-  // dk (reversed run): queries v, keys dO, values q, initial state dS^T / alpha
+  // dk (reversed run): queries v, keys dO, values q, initial state dS^T (/ gamma)
   if (rc == LA_OK)
     rc = run_reversed(v, dO, q, g, dkg, dS_final ? dst : nullptr, nullptr, B, H, T, dv_, dk_, kind, f32, s);
-  // dv (reversed run): queries k, keys q, values dO, initial state dS / alpha; its final state / alpha = dS0
+  // dv (reversed run): queries k, keys q, values dO, initial state dS (/ gamma); its final state x alpha = dS0
   if (rc == LA_OK)
     rc = run_reversed(k, q, dO, g, dvg, dS_final ? dss : nullptr, dS0 ? sfin : nullptr, B, H, T, dk_, dv_, kind, f32,
                       s);
   if (rc == LA_OK && dS0) {
-    scale_state_kernel<<<dim3(8, (unsigned)BH), 256, 0, s>>>(sfin, g, H, dk_ * dv_, dS0);
+    scale_state_kernel<<<dim3(8, (unsigned)BH), 256, 0, s>>>(sfin, g, H, scalar ? (long long)T : 0ll, dk_ * dv_, dS0);
     if (cudaGetLastError() != cudaSuccess) fail("dS0 scaling");
+  }
+  if (rc == LA_OK && dg_out) {
+    // the forward's final state (for the dS_final term of dg), then the suffix sums
+    if (dS_final) {
+      const int r = la_chunk_fwd(q, k, v, g, nullptr, oscr, S0, sT, B, H, T, dk_, dv_, C, fwd_mode, stream);
+      if (r != LA_OK) rc = r;
+    }
+    if (rc == LA_OK) {
+      if (f32)
+        dg_kernel<float><<<(unsigned)BH, 256, 0, s>>>(static_cast<const float *>(q), static_cast<const float *>(dq),
+                                                      static_cast<const float *>(k), static_cast<const float *>(dkg),
+                                                      dS_final, sT, T, dk_, dv_, dg_out);
+      else
+        dg_kernel<__nv_bfloat16><<<(unsigned)BH, 256, 0, s>>>(
+            static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(dq),
+            static_cast<const __nv_bfloat16 *>(k), static_cast<const __nv_bfloat16 *>(dkg), dS_final, sT, T, dk_,
+            dv_, dg_out);
+      if (cudaGetLastError() != cudaSuccess) fail("dg suffix sums");
+    }
   }
   e = cudaFreeAsync(ws, s);
   if (rc == LA_OK && e != cudaSuccess) {

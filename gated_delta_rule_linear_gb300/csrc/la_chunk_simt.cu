@@ -21,7 +21,9 @@
 // written for clarity over speed (the bf16 path runs on the tensor cores).
 // With p.rev it runs the same recurrence over the stored sequence read from
 // its end (token t is memory row T-1-t, for every input and the output): the
-// anti-causal passes of the backward.
+// anti-causal passes of the backward. Scalar data-dependent gates are then
+// taken from the stored token after each position (index T - t, none at
+// t = 0), the decay those passes need.
 #include <cuda_bf16.h>
 
 #include "la_internal.h"
@@ -144,6 +146,8 @@ chunk_simt_kernel(const ChunkParams p, int tile_w) {
       float lg = 0.f;
       if (r < n) {
         if (kind == kRetnet) lg = __ldg(p.g + h);
+        else if (kind == kScalar && p.rev)  // reversed: the gate of the stored token after it
+          lg = (t0 + r >= 1) ? __ldg(p.g + (size_t)bh * T + (T - t0 - r)) : 0.f;
         else if (kind == kScalar || (kind == kGdn && p.g)) lg = __ldg(p.g + (size_t)bh * T + row(t0 + r));
       }
       Bg[r] = lg;

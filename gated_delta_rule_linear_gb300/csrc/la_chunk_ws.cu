@@ -26,13 +26,17 @@
 // gates, which stay in L2), and the per-column factor e^{bv_m} e^{bv_last' -
 // bv_m'} rides on the state round trip next to the key-axis one.
 //
-// REV (plain linear attention and RetNet) runs the same recurrence over the
-// time-reversed sequence without copying it: chunk j is the 64-row window
+// REV (plain linear attention, RetNet, scalar decay) runs the same recurrence
+// over the time-reversed sequence without copying it: chunk j is the 64-row window
 // ending at row T-1-64j of the stored tensors (its TMA load may start above
 // row 0, where the fill is zero), and its smem row m is reversed row 63-m.
 // The per-row gate factors are written to the slots of the smem rows, the
 // masks become s >= r, and o lands in stored order, so the anti-causal passes
-// of the backward read and write q, k, v, dO, dk, dv where they are.
+// of the backward read and write q, k, v, dO, dk, dv where they are. With
+// data-dependent scalar gates, position t of a reversed run decays by the
+// gate of the stored token after it (index T - t; none at t = 0): the decay
+// between stored tokens s < u is then the product of the gates of s+1 .. u,
+// as the backward's anti-causal sums need.
 //
 // Roles (384 threads):
 //   warp 0      TMA producer: q/k/v (and GLA gate) tiles into an ns-stage ring
@@ -129,7 +133,8 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
   constexpr bool elu = KIND == kElu1, outer = KIND == kOuter;
   constexpr bool gla = chan_gates(KIND);  // key-axis channel gates (GLA and the outer-product gate)
   constexpr bool sgate = KIND == kRetnet || KIND == kScalar;
-  static_assert(!REV || KIND == kLinear || KIND == kRetnet, "reversed runs: unit-write, per-head decay only");
+  static_assert(!REV || KIND == kLinear || KIND == kRetnet || KIND == kScalar,
+                "reversed runs: unit write with no gate, a per-head or a per-token scalar decay");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const WsLayout L = ws_layout(DK, DV, KIND, ns);
@@ -215,6 +220,9 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
           const float g = __ldg(p.g + h);
           g0 = (t < T) ? g : 0.f;
           g1 = (t + 32 < T) ? g : 0.f;
+        } else if (REV) {  // the gate of the stored token after each position
+          g0 = (t >= 1 && t < T) ? __ldg(p.g + (size_t)bh * T + (T - t)) : 0.f;
+          g1 = (t + 32 < T) ? __ldg(p.g + (size_t)bh * T + (T - t - 32)) : 0.f;
         } else {
           g0 = (t < T) ? __ldg(p.g + (size_t)bh * T + t) : 0.f;
           g1 = (t + 32 < T) ? __ldg(p.g + (size_t)bh * T + t + 32) : 0.f;
@@ -834,7 +842,9 @@ int launch_chunk_ws(const ChunkParams &p, cudaStream_t stream) {
   if (p.rev) {
     if (p.kind == kLinear) return launch_kind<kLinear, true>(p, stream);
     if (p.kind == kRetnet) return launch_kind<kRetnet, true>(p, stream);
-    set_error("la_chunk_fwd: the reversed run covers plain linear attention and RetNet only (mode %d)", p.kind);
+    if (p.kind == kScalar) return launch_kind<kScalar, true>(p, stream);
+    set_error("la_chunk_fwd: the reversed run covers linear attention, RetNet and scalar decay only (mode %d)",
+              p.kind);
     return LA_ERR_UNSUPPORTED;
   }
   switch (p.kind) {

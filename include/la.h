@@ -225,32 +225,43 @@ int la_prologue(const void *xq, const void *xk, const void *xv,
                 int B, int H, int T, int dk, int dv, int flags, la_stream_t stream);
 
 /*
- * la_chunk_bwd -- the backward pass of la_chunk_fwd for LA_LINEAR and
- * LA_RETNET (whose decay is not a learned input), optionally | LA_F32:
- * given dO = dL/do and dS_final = dL/dS_final, the gradients
+ * la_chunk_bwd -- the backward pass of la_chunk_fwd for LA_LINEAR, LA_RETNET
+ * and LA_SCALAR_GATE, optionally | LA_F32: given dO = dL/do and
+ * dS_final = dL/dS_final, the gradients
  *
  *   dq_t = alpha^(t+1) S0 dO_t + sum_{s<=t} alpha^(t-s) (dO_t . v_s) k_s
  *   dk_s = sum_{t>=s} alpha^(t-s) (dO_t . v_s) q_t + alpha^(T-1-s) dS_final v_s
  *   dv_s = sum_{t>=s} alpha^(t-s) (q_t . k_s) dO_t + alpha^(T-1-s) dS_final^T k_s
  *   dS0  = sum_t alpha^(t+1) q_t dO_t^T + alpha^T dS_final
  *
- * (alpha = 1, or gamma_h = exp(g_h)). The chunk states are recomputed, not
- * stored ("Talk Linear Attention" section 4.1.2).
+ * (alpha = 1, or gamma_h = exp(g_h); for LA_SCALAR_GATE alpha^(t-s) stands
+ * for the product of exp(g) over the tokens s+1 .. t, and alpha^(t+1) for
+ * tokens 0 .. t), and for LA_SCALAR_GATE the gradient of the log-gates
+ *
+ *   dg_tau = sum_{u>=tau} (q_u . dq_u - k_u . dk_u) + sum(dS_final ⊙ S_final).
+ *
+ * The chunk states are recomputed, not stored ("Talk Linear Attention"
+ * section 4.1.2).
  *
  *   q, k, v, g, S0  as passed to la_chunk_fwd (S0 may be NULL: zero)
  *   dO       [B][H][T][dv], input dtype; dS_final float32 [B][H][dk][dv] or NULL (zero)
  *   dq_out, dk_out [B][H][T][dk]; dv_out [B][H][T][dv]: dq, dk, dv, input dtype
  *   dS0      float32 [B][H][dk][dv] output, or NULL (not computed)
+ *   dg_out   float32 [B][H][T] output for LA_SCALAR_GATE, or NULL (not
+ *            computed); must be NULL for the other modes
  *   16-byte alignment for every pointer. For LA_RETNET, g_h > -80 (the
  *   passes divide dS_final by gamma_h). C = 0 or 64.
  * Runs as three chunk-forward passes on `stream` (two of them run the
  * recurrence over the time-reversed sequence, reading and writing the
- * tensors where they are), with a workspace from the library's pool of
- * 16*B*H*dk*dv bytes (initial states of the passes).
+ * tensors where they are), plus, for dg with dS_final, a forward pass for
+ * S_final and a suffix-sum kernel; workspace from the library's pool of
+ * 16*B*H*dk*dv bytes (initial states of the passes), + 4*B*H*dk*dv +
+ * B*H*T*dv*esize with dg.
  */
 int la_chunk_bwd(const void *q, const void *k, const void *v, const float *g, const void *dO,
                  const float *dS_final, const float *S0, void *dq_out, void *dk_out, void *dv_out,
-                 float *dS0, int B, int H, int T, int dk, int dv, int C, int mode, la_stream_t stream);
+                 float *dS0, float *dg_out, int B, int H, int T, int dk, int dv, int C, int mode,
+                 la_stream_t stream);
 
 /*
  * la_chunk_fwd_gdelta -- causal forward of the generalised delta rule, an

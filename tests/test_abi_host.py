@@ -186,7 +186,7 @@ def test_prologue_rejects_bad_arguments(lib, kw, code):
 
 def _bwd(**kw):
     args = dict(q=A, k=A, v=A, g=None, dO=A, dS_final=None, S0=None, dq_out=A, dk_out=A, dv_out=A, dS0=None,
-                B=1, H=1, T=64, dk=128, dv=128, C=0, mode=la.LA_LINEAR, stream=None)
+                dg_out=None, B=1, H=1, T=64, dk=128, dv=128, C=0, mode=la.LA_LINEAR, stream=None)
     args.update(kw)
     rc = la.la_chunk_bwd(**args)
     return rc, la.la_last_error()
@@ -204,6 +204,11 @@ def _bwd(**kw):
     (dict(C=128), "LA_ERR_UNSUPPORTED"),
     (dict(dq_out=A + 8), "LA_ERR_INVALID_ARG"),
     (dict(dS0=A + 4), "LA_ERR_INVALID_ARG"),
+    (dict(mode=4), "LA_ERR_INVALID_ARG"),             # scalar decay needs g
+    (dict(dg_out=A), "LA_ERR_INVALID_ARG"),           # dg only for the scalar decay
+    (dict(mode=2, g=A, dg_out=A), "LA_ERR_INVALID_ARG"),
+    (dict(mode=4, g=A, dg_out=A + 4), "LA_ERR_INVALID_ARG"),  # dg 16-byte aligned
+    (dict(mode=3, g=A), "LA_ERR_UNSUPPORTED"),        # gla: no backward in this build
 ])
 def test_chunk_bwd_rejects_bad_arguments(lib, kw, code):
     rc, msg = _bwd(**kw)

@@ -1,4 +1,4 @@
-"""GPU parity of la_chunk_bwd (linear and RetNet; three chunk-forward passes,
+"""GPU parity of la_chunk_bwd (linear, RetNet, scalar decay; three chunk-forward passes,
 two of them the kernels' reversed runs over the stored tensors) with the
 float64 backward oracle, through the C ABI, at the library's tolerance (bf16:
 max-abs 2e-2 and relative Frobenius 5e-3; fp32: relative 1e-4) on dq, dk, dv
@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle.backward import backward
+from oracle.backward import backward, backward_scalar
 from paritylib import assert_close, f64, make
 
 pytestmark = pytest.mark.gpu
@@ -42,7 +42,8 @@ def _run(mode, q, k, v, g, dO, S0, dS):
     cu = lambda t: None if t is None else t.to(dev).contiguous()
     out = la.chunk_bwd(cu(q), cu(k), cu(v), cu(dO), mode, g=cu(g), S0=cu(S0), dS_final=cu(dS))
     torch.cuda.synchronize()
-    return out
+    assert out[4] is None or mode == "scalar"
+    return out[:4] if mode != "scalar" else out
 
 
 @pytest.mark.parametrize("mode", ["linear", "retnet"])
@@ -79,3 +80,56 @@ def test_backward_bench_shape_sampled():
         ref = backward(sl(q), sl(k), sl(v), sl(dO), "retnet", g=f64(g)[h:h + 1], dS=sl(dS))
         for name, got, r in (("dq", dq, ref[0]), ("dk", dk_, ref[1]), ("dv", dv_, ref[2]), ("dS0", dS0, ref[3])):
             assert_close(f64(got[b:b + 1, h:h + 1]), r, "bf16", f"head {b},{h} {name}")
+
+
+# --- the data-dependent scalar decay, with dg ------------------------------------------
+# dg is a suffix sum over up to T tokens of w_u = q_u.dq_u - k_u.dk_u, formed
+# from the dq and dk the passes write in the input dtype. Rounding dq and dk
+# to bfloat16 moves each product by at most 2^-9 of its size, so
+#   |dg_tau - ref_tau| <= 2^-8 * sum_{u>=tau} sum_c (|q_u,c dq_u,c| + |k_u,c dk_u,c|) + 1e-5
+# (twice the rounding bound, for the float32 accumulation); the terms of w
+# cancel, so a relative bound on dg itself would not follow from the
+# arithmetic. float32 inputs: the library's float32 tolerance.
+
+def _scalar_case(dtype, B, H, T, dk, dv, seed=0):
+    from workloads import WORKLOADS
+    wl = WORKLOADS["scalar"].with_sizes(B=B, H=H, T=T, dk=dk, dv=dv, dtype=dtype, s0=True, seed=60 + seed)
+    inp = make(wl)
+    gen = torch.Generator().manual_seed(70 + seed)
+    dO = (torch.randn(B, H, T, dv, generator=gen) / np.sqrt(dv)).to(wl.torch_dtype)
+    dS = torch.randn(B, H, dk, dv, generator=gen) * 0.1
+    return inp["q"], inp["k"], inp["v"], inp["g"], dO, inp["S0"], dS
+
+
+def _check_dg(got, ref, dtype, what, q, k):
+    """ref = backward_scalar's outputs; q, k the float64 inputs."""
+    if dtype == "f32":
+        assert_close(got, ref[4], dtype, what)
+        return
+    assert np.all(np.isfinite(got)), what
+    mag = np.sum(np.abs(q * ref[0]) + np.abs(k * ref[1]), axis=-1)        # [B, H, T]
+    bound = 2.0 ** -8 * np.cumsum(mag[..., ::-1], axis=-1)[..., ::-1] + 1e-5
+    bad = np.abs(got - ref[4]) > bound
+    assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} outside the rounding bound"
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dims", [(128, 128), (64, 128), (64, 64)])
+@pytest.mark.parametrize("T", [1, 64, 129, 700])
+def test_scalar_backward_parity(dtype, dims, T):
+    dk, dv = dims
+    q, k, v, g, dO, S0, dS = _scalar_case(dtype, 2, 3, T, dk, dv)
+    dq, dk_, dv_, dS0, dg = _run("scalar", q, k, v, g, dO, S0, dS)
+    ref = backward_scalar(f64(q), f64(k), f64(v), f64(dO), f64(g), S0=f64(S0), dS=f64(dS))
+    for name, got, r in (("dq", dq, ref[0]), ("dk", dk_, ref[1]), ("dv", dv_, ref[2]), ("dS0", dS0, ref[3])):
+        assert_close(f64(got), r, dtype, f"scalar {dtype} T={T} {name}")
+    _check_dg(f64(dg), ref, dtype, f"scalar {dtype} T={T} dg", f64(q), f64(k))
+
+
+def test_scalar_backward_without_states_or_dS():
+    q, k, v, g, dO, S0, dS = _scalar_case("bf16", 1, 2, 333, 128, 128, seed=1)
+    dq, dk_, dv_, dS0, dg = _run("scalar", q, k, v, g, dO, None, None)
+    ref = backward_scalar(f64(q), f64(k), f64(v), f64(dO), f64(g))
+    for name, got, r in (("dq", dq, ref[0]), ("dk", dk_, ref[1]), ("dv", dv_, ref[2]), ("dS0", dS0, ref[3])):
+        assert_close(f64(got), r, "bf16", f"scalar {name}")
+    _check_dg(f64(dg), ref, "bf16", "scalar dg", f64(q), f64(k))

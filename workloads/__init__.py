@@ -89,6 +89,11 @@ WORKLOADS = {
     # after S0 by bench.py's backward leg from the same generator recipe.
     "backward": Workload("backward", "retnet", 8, 16, 4096, 128, 128, "bf16", 64, seed=9,
                          qkv_scale=1.0 / math.sqrt(128.0), extra={"backward": True}),
+    # Backward of the data-dependent scalar decay, with the log-gate gradient dg:
+    # the retnet shape and q/k/v recipe, g = -softplus(N(0,1))/8 per token, dO and
+    # dS_final as for the backward workload.
+    "backward_scalar": Workload("backward_scalar", "scalar", 8, 16, 4096, 128, 128, "bf16", 64, seed=13,
+                                qkv_scale=1.0 / math.sqrt(128.0), extra={"backward": True}),
     # Outer-product gate alpha_t beta_t^T (a next row): the GLA shape and q/k/v
     # recipe with GLA-distributed log-gates on both the key and the value axis.
     "outer": Workload("outer", "outer", 8, 16, 8192, 128, 128, "bf16", 64, seed=11,
