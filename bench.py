@@ -839,7 +839,7 @@ def bench_backward(args, rank, world, local_rank):
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
             "frac": round(achieved / hbm_peak, 4), "traffic": recorded_traffic(wl.name), "peak_source": peak_src,
             "algorithmic_bytes": alg, "kernel": "3 x chunk_ws_kernel (dq causal; dk and dv reversed runs)"
-            + (" + forward for S_final + dg_kernel" if wl.mode == "scalar" else ""),
+            + (" + forward for S_final + dg_tile_kernel + dg_carry_kernel" if wl.mode == "scalar" else ""),
             "launch_ms_mean": round(statistics.mean(launch_ms), 4)}
     e2e = None
     if not args.no_e2e:
@@ -884,8 +884,8 @@ def bench_backward(args, rank, world, local_rank):
             "data": "synthetic (seeded; shapes and distributions of the workload)", "config": cfg,
             "tflops": round(world * flop * args.steps / (total_ms / 1e3) / 1e12, 2), "roofline": roof,
             "cpu_baseline": cpu, "clocks": clk, "e2e": e2e,
-            # state prep, 3 passes, dS0 scaling (+ the forward for S_final and the dg suffix sums)
-            "gpu_launches": args.steps * (7 if wl.mode == "scalar" else 5),
+            # state prep, 3 passes, dS0 scaling (+ the forward for S_final and the two dg launches)
+            "gpu_launches": args.steps * (8 if wl.mode == "scalar" else 5),
         }), flush=True)
     if dist:
         dist.destroy_process_group()

@@ -68,19 +68,61 @@ template <typename T> __device__ __forceinline__ float ldf(const T *p);
 template <> __device__ __forceinline__ float ldf<float>(const float *p) { return __ldg(p); }
 template <> __device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 
-// dg for the scalar decay, one CTA per (b, h): w_u = q_u . dq_u - k_u . dk_u
-// (one token per thread), a suffix scan over 256-token tiles from the end of
-// the sequence, plus the final-state term c = sum(dS ⊙ S_final).
+// dg for the scalar decay in two launches. dg_tile_kernel, one CTA per
+// (b, h, 256-token tile): w_u = q_u . dq_u - k_u . dk_u (a warp per token,
+// lanes over the channels, coalesced) and the suffix sum of w inside the tile,
+// written to dg, with the tile's total in `tot`. dg_carry_kernel, one CTA per
+// (b, h): the final-state term c = sum(dS ⊙ S_final) plus the totals of the
+// later tiles, added to every token of a tile.
 template <typename Tin>
-__global__ void __launch_bounds__(256) dg_kernel(const Tin *__restrict__ q, const Tin *__restrict__ dq,
-                                                 const Tin *__restrict__ k, const Tin *__restrict__ dk,
-                                                 const float *__restrict__ dS, const float *__restrict__ S_final,
-                                                 int T, int dkk, int dv, float *__restrict__ dg) {
+__global__ void __launch_bounds__(256) dg_tile_kernel(const Tin *__restrict__ q, const Tin *__restrict__ dq,
+                                                      const Tin *__restrict__ k, const Tin *__restrict__ dk, int T,
+                                                      int dkk, float *__restrict__ dg, float *__restrict__ tot) {
   __shared__ float red[8];
+  __shared__ float wt[256];
+  const int bh = blockIdx.x, tile = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const size_t base = (size_t)bh * T;
+  const int t0 = tile * 256, per = dkk / 32;  // channels per lane (2 or 4)
+#pragma unroll 4
+  for (int i = warp; i < 256; i += 8) {
+    const int u = t0 + i;
+    float x = 0.f;
+    if (u < T) {
+      const size_t r = (base + u) * dkk + (size_t)lane * per;
+      for (int e = 0; e < per; ++e) x += ldf(q + r + e) * ldf(dq + r + e) - ldf(k + r + e) * ldf(dk + r + e);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    if (lane == 0) wt[i] = x;
+  }
+  __syncthreads();
+  float w = wt[tid];
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {  // inclusive suffix sum within the warp
+    const float y = __shfl_down_sync(0xffffffffu, w, off);
+    if (lane + off < 32) w += y;
+  }
+  if (lane == 0) red[warp] = w;
+  __syncthreads();
+  float later = 0.f, all = 0.f;
+#pragma unroll
+  for (int wq = 0; wq < 8; ++wq) {
+    all += red[wq];
+    if (wq > warp) later += red[wq];
+  }
+  if (t0 + tid < T) dg[base + t0 + tid] = later + w;
+  if (tid == 0) tot[(size_t)bh * gridDim.y + tile] = all;
+}
+
+__global__ void __launch_bounds__(256) dg_carry_kernel(const float *__restrict__ dS, const float *__restrict__ S_final,
+                                                       const float *__restrict__ tot, int ntiles, int T, int n,
+                                                       float *__restrict__ dg) {
+  __shared__ float red[8];
+  __shared__ float carry[1024];  // suffix sums of the tile totals, in chunks of 1024 tiles
   const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   float c = 0.f;
   if (dS)
-    for (int i = tid; i < dkk * dv; i += 256) c = fmaf(dS[(size_t)bh * dkk * dv + i], S_final[(size_t)bh * dkk * dv + i], c);
+    for (int i = tid; i < n; i += 256) c = fmaf(dS[(size_t)bh * n + i], S_final[(size_t)bh * n + i], c);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
   if (lane == 0) red[warp] = c;
@@ -88,33 +130,21 @@ __global__ void __launch_bounds__(256) dg_kernel(const Tin *__restrict__ q, cons
   c = 0.f;
 #pragma unroll
   for (int w = 0; w < 8; ++w) c += red[w];
-  __syncthreads();
-  const size_t base = (size_t)bh * T;
-  float carry = c;
-  for (int t1 = T; t1 > 0; t1 -= 256) {  // tile [t1 - 256, t1), the last tokens first
-    const int u = t1 - 256 + tid;
-    float w = 0.f;
-    if (u >= 0) {
-      const size_t r = (base + u) * dkk;
-      for (int e = 0; e < dkk; ++e) w += ldf(q + r + e) * ldf(dq + r + e) - ldf(k + r + e) * ldf(dk + r + e);
-    }
-    // inclusive suffix sum within the warp, then over the later warps of the tile
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const float y = __shfl_down_sync(0xffffffffu, w, off);
-      if (lane + off < 32) w += y;
-    }
-    if (lane == 0) red[warp] = w;
+  // tiles from the end, 1024 at a time: carry of tile j = c + totals of tiles j+1 ..
+  for (int j1 = ntiles; j1 > 0; j1 -= 1024) {
+    const int j0 = j1 > 1024 ? j1 - 1024 : 0;
     __syncthreads();
-    float later = 0.f, tile = 0.f;
-#pragma unroll
-    for (int wq = 0; wq < 8; ++wq) {
-      tile += red[wq];
-      if (wq > warp) later += red[wq];
+    if (tid == 0) {
+      float acc = c;
+      for (int j = j1 - 1; j >= j0; --j) {
+        carry[j - j0] = acc;
+        acc += tot[(size_t)bh * ntiles + j];
+      }
+      red[0] = acc;
     }
-    if (u >= 0) dg[base + u] = carry + later + w;
-    carry += tile;
     __syncthreads();
+    for (int u = j0 * 256 + tid; u < j1 * 256 && u < T; u += 256) dg[(size_t)bh * T + u] += carry[u / 256 - j0];
+    c = red[0];
   }
 }
 
@@ -195,7 +225,8 @@ extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const f
   // workspace: three initial states and the last pass's final state; for dg also the
   // forward's final state and a scratch output of the forward pass that produces it
   const size_t n_s = BH * dk_ * dv_ * 4;
-  const size_t bytes = (dg_out ? 5 : 4) * n_s + (dg_out ? BH * (size_t)T * dv_ * esz : 0);
+  const int ntiles = (T + 255) / 256;  // dg's 256-token tiles
+  const size_t bytes = (dg_out ? 5 : 4) * n_s + (dg_out ? BH * (size_t)T * dv_ * esz + ((BH * ntiles + 3) & ~static_cast<size_t>(3)) * 4 : 0);
   uint8_t *ws = nullptr;
   cudaMemPool_t pool = library_pool();
   if (!pool) {
@@ -209,7 +240,8 @@ extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const f
   }
   float *s0t = reinterpret_cast<float *>(ws), *dst = s0t + BH * dk_ * dv_, *dss = dst + BH * dk_ * dv_,
         *sfin = dss + BH * dk_ * dv_, *sT = sfin + BH * dk_ * dv_;
-  void *oscr = sT + BH * dk_ * dv_;
+  float *tiles = sT + BH * dk_ * dv_;  // dg's per-tile totals, then the forward's scratch output
+  void *oscr = tiles + ((BH * ntiles + 3) & ~static_cast<size_t>(3));
   int rc = LA_OK;
   auto fail = [&](const char *what) {
     if (rc == LA_OK) {
@@ -251,15 +283,17 @@ extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const f
       if (r != LA_OK) rc = r;
     }
     if (rc == LA_OK) {
+      const dim3 grid((unsigned)BH, (unsigned)ntiles);
       if (f32)
-        dg_kernel<float><<<(unsigned)BH, 256, 0, s>>>(static_cast<const float *>(q), static_cast<const float *>(dq),
-                                                      static_cast<const float *>(k), static_cast<const float *>(dkg),
-                                                      dS_final, sT, T, dk_, dv_, dg_out);
+        dg_tile_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float *>(q), static_cast<const float *>(dq),
+                                                   static_cast<const float *>(k), static_cast<const float *>(dkg), T,
+                                                   dk_, dg_out, tiles);
       else
-        dg_kernel<__nv_bfloat16><<<(unsigned)BH, 256, 0, s>>>(
+        dg_tile_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
             static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(dq),
-            static_cast<const __nv_bfloat16 *>(k), static_cast<const __nv_bfloat16 *>(dkg), dS_final, sT, T, dk_,
-            dv_, dg_out);
+            static_cast<const __nv_bfloat16 *>(k), static_cast<const __nv_bfloat16 *>(dkg), T, dk_, dg_out, tiles);
+      if (cudaGetLastError() == cudaSuccess)
+        dg_carry_kernel<<<(unsigned)BH, 256, 0, s>>>(dS_final, sT, tiles, ntiles, T, dk_ * dv_, dg_out);
       if (cudaGetLastError() != cudaSuccess) fail("dg suffix sums");
     }
   }
