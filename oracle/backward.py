@@ -27,7 +27,7 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["backward", "backward_scalar"]
+__all__ = ["backward", "backward_scalar", "backward_gla"]
 
 
 def backward(q, k, v, dO, mode, g=None, S0=None, dS=None):
@@ -107,4 +107,54 @@ def backward_scalar(q, k, v, dO, g, S0=None, dS=None):
             dG = np.sum(Q * dq[b, h], axis=1) - np.sum(K * dk[b, h], axis=1)
             dG[-1] += np.sum(dS[b, h] * S_T)
             dg[b, h] = np.cumsum(dG[::-1])[::-1]
+    return dq, dk, dv, dS0, dg
+
+
+def backward_gla(q, k, v, dO, g, S0=None, dS=None):
+    """The gradients for GLA's per-key-channel decay (alpha_t[c] = exp(g_t[c]),
+    g [B, H, T, dk]). With the inclusive prefix G_t[c], the decay of channel c
+    between positions is alpha_c(t, s) = exp(G_t[c] - G_s[c]), and
+
+      dq_t[c] = sum_{s<=t} (dO_t . v_s) alpha_c(t, s) k_s[c] + alpha_c(t, -1) (S0 dO_t)[c]
+      dk_s[c] = sum_{t>=s} (dO_t . v_s) alpha_c(t, s) q_t[c] + alpha_c(T-1, s) (dS v_s)[c]
+      dv_s    = sum_{t>=s} (sum_c q_t[c] alpha_c(t, s) k_s[c]) dO_t + dS^T (alpha(T-1, s) ⊙ k_s)
+      dS0[c]  = sum_t alpha_c(t, -1) q_t[c] dO_t + alpha_c(T-1, -1) dS[c]
+      dg_tau[c] = sum_{u>=tau} (q_u[c] dq_u[c] - k_u[c] dk_u[c]) + sum_j dS[c, j] S_final[c, j]
+
+    (G_u[c] enters with + where u reads and with - where u writes, as for the
+    scalar decay, now channel by channel). Written as explicit sums over token
+    pairs. Returns dq, dk, dv, dS0, dg (float64)."""
+    q, k, v, dO, g = (np.asarray(x, dtype=np.float64) for x in (q, k, v, dO, g))
+    B, H, T, dkk = q.shape
+    dvv = v.shape[-1]
+    S0 = np.zeros((B, H, dkk, dvv)) if S0 is None else np.asarray(S0, dtype=np.float64)
+    dS = np.zeros((B, H, dkk, dvv)) if dS is None else np.asarray(dS, dtype=np.float64)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    dS0 = np.zeros_like(S0)
+    dg = np.zeros_like(g)
+    for b in range(B):
+        for h in range(H):
+            G = np.cumsum(g[b, h], axis=0)                       # [T, dk]
+            Q, K, V, Gd = q[b, h], k[b, h], v[b, h], dO[b, h]
+            S_T = np.exp(G[-1])[:, None] * S0[b, h]
+            for t in range(T):
+                a0 = np.exp(G[t])                                # alpha(t, -1)
+                dq[b, h, t] += a0 * (S0[b, h] @ Gd[t])
+                dS0[b, h] += np.outer(a0 * Q[t], Gd[t])
+                for s in range(t + 1):
+                    a = np.exp(G[t] - G[s])                      # alpha(t, s) per channel
+                    w = Gd[t] @ V[s]
+                    dq[b, h, t] += w * a * K[s]
+                    dk[b, h, s] += w * a * Q[t]
+                    dv[b, h, s] += (Q[t] @ (a * K[s])) * Gd[t]
+            aT = np.exp(G[-1])
+            dS0[b, h] += aT[:, None] * dS[b, h]
+            for s in range(T):
+                al = np.exp(G[-1] - G[s])                        # alpha(T-1, s)
+                dk[b, h, s] += al * (dS[b, h] @ V[s])
+                dv[b, h, s] += dS[b, h].T @ (al * K[s])
+                S_T += np.outer(al * K[s], V[s])
+            dGu = Q * dq[b, h] - K * dk[b, h]                    # [T, dk]
+            dGu[-1] += np.sum(dS[b, h] * S_T, axis=1)
+            dg[b, h] = np.cumsum(dGu[::-1], axis=0)[::-1]
     return dq, dk, dv, dS0, dg

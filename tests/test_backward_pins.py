@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from oracle import recurrence
-from oracle.backward import backward, backward_scalar
+from oracle.backward import backward, backward_gla, backward_scalar
 
 RNG = np.random.default_rng(5)
 
@@ -155,3 +155,53 @@ def test_scalar_dg_pins_catch_an_exclusive_suffix_sum():
     # the suffix sum taken exclusively (the token's own term dropped) is rejected
     shifted = np.concatenate([dg[..., 1:], np.zeros_like(dg[..., :1])], axis=-1)
     assert not np.allclose(shifted, num, rtol=1e-3, atol=1e-4)
+
+
+# --- GLA's per-channel decay, with the per-channel log-gate gradient ------------------
+
+def _gla_case(B=1, H=2, T=7, dk=3, dv=4):
+    q, k, v, _, S0, dO, dS = _case("linear", B=B, H=H, T=T, dk=dk, dv=dv)
+    g = -np.abs(RNG.standard_normal((B, H, T, dk))) * 0.3
+    return q, k, v, g, S0, dO, dS
+
+
+def test_gla_backward_matches_finite_differences():
+    q, k, v, g, S0, dO, dS = _gla_case()
+    got = backward_gla(q, k, v, dO, g, S0=S0, dS=dS)
+    eps = 1e-6
+    for name, x, grad in (("q", q, got[0]), ("k", k, got[1]), ("v", v, got[2]), ("S0", S0, got[3]), ("g", g, got[4])):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            old = x[idx]
+            x[idx] = old + eps
+            lp = _loss(q, k, v, g, S0, dO, dS, "gla")
+            x[idx] = old - eps
+            lm = _loss(q, k, v, g, S0, dO, dS, "gla")
+            x[idx] = old
+            num[idx] = (lp - lm) / (2 * eps)
+        assert np.allclose(grad, num, rtol=1e-6, atol=1e-7), name
+
+
+def test_gla_backward_matches_autograd():
+    q, k, v, g, S0, dO, dS = _gla_case(B=1, H=2, T=24, dk=5, dv=6)
+    tq, tk, tv, tg, tS0 = (torch.tensor(x, requires_grad=True) for x in (q, k, v, g, S0))
+    S = tS0
+    outs = []
+    for t in range(24):  # written afresh for autograd: per-key-channel decay, then the write
+        S = torch.exp(tg[:, :, t])[..., :, None] * S + tk[:, :, t, :, None] * tv[:, :, t, None, :]
+        outs.append(torch.einsum("bhc,bhcv->bhv", tq[:, :, t], S))
+    o = torch.stack(outs, dim=2)
+    (o * torch.tensor(dO)).sum().add((S * torch.tensor(dS)).sum()).backward()
+    got = backward_gla(q, k, v, dO, g, S0=S0, dS=dS)
+    for name, a, b in zip(("q", "k", "v", "S0", "g"), got, (tq.grad, tk.grad, tv.grad, tS0.grad, tg.grad)):
+        assert np.allclose(a, b.numpy(), rtol=1e-10, atol=1e-11), name
+
+
+def test_gla_backward_with_equal_channel_gates_is_the_scalar_decay():
+    q, k, v, g, S0, dO, dS = _gla_case(T=15)
+    gs = g[..., 0]
+    gla = backward_gla(q, k, v, dO, np.repeat(gs[..., None], q.shape[-1], axis=-1), S0=S0, dS=dS)
+    sc = backward_scalar(q, k, v, dO, gs, S0=S0, dS=dS)
+    for a, b in zip(gla[:4], sc[:4]):
+        assert np.allclose(a, b, rtol=0, atol=1e-12)
+    assert np.allclose(gla[4].sum(-1), sc[4], rtol=0, atol=1e-12)  # dg summed over the shared channels
