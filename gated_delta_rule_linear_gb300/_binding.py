@@ -244,9 +244,9 @@ def chunk_fwd_gdelta(q, k, v, a, b, S0=None, C=0, with_state=True, o=None, S_fin
 
 
 def chunk_bwd(q, k, v, dO, mode, g=None, S0=None, dS_final=None, with_dS0=True, with_dg=True, C=0, stream=None):
-    """Backward pass of chunk_fwd for "linear", "retnet" and "scalar": returns
-    dq, dk, dv (dtype of q), dS0 (float32, or None) and dg (float32 [B,H,T]
-    for "scalar" with with_dg, else None)."""
+    """Backward pass of chunk_fwd for "linear", "retnet", "scalar" and "gla":
+    returns dq, dk, dv (dtype of q), dS0 (float32, or None) and dg (float32,
+    [B,H,T] for "scalar", [B,H,T,dk] for "gla", with with_dg; else None)."""
     import torch
     for name, t in (("q", q), ("k", k), ("v", v), ("dO", dO), ("g", g), ("S0", S0), ("dS_final", dS_final)):
         _check(t, name)
@@ -255,8 +255,12 @@ def chunk_bwd(q, k, v, dO, mode, g=None, S0=None, dS_final=None, with_dS0=True, 
     mid = _mode_id(mode, q.dtype)
     dq, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dS0 = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device) if with_dS0 else None
-    scalar = (mid & 0xFF) == CONSTANTS["LA_SCALAR_GATE"]
-    dg = torch.empty((B, H, T), dtype=torch.float32, device=q.device) if (scalar and with_dg) else None
+    kind = mid & 0xFF
+    dg = None
+    if with_dg and kind == CONSTANTS["LA_SCALAR_GATE"]:
+        dg = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    elif with_dg and kind == CONSTANTS["LA_GLA"]:
+        dg = torch.empty((B, H, T, dk), dtype=torch.float32, device=q.device)
     rc = la_chunk_bwd(q, k, v, g, dO, dS_final, S0, dq, dk_, dv_, dS0, dg, B, H, T, dk, dv, C, mid,
                       _stream_handle(stream))
     if rc != 0:

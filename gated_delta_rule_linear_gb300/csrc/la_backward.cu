@@ -148,13 +148,63 @@ __global__ void __launch_bounds__(256) dg_carry_kernel(const float *__restrict__
   }
 }
 
+// GLA: dS0[c][j] = exp(g_0[c]) * S[c][j], the first token's per-channel gate
+__global__ void __launch_bounds__(256) scale_rows_kernel(const float *__restrict__ S, const float *__restrict__ g,
+                                                         int T, int dkk, int dv, float *__restrict__ out) {
+  const int bh = blockIdx.y;
+  const size_t base = (size_t)bh * dkk * dv;
+  for (int i = blockIdx.x * 256 + threadIdx.x; i < dkk * dv; i += gridDim.x * 256)
+    out[base + i] = expf(__ldg(g + (size_t)bh * T * dkk + i / dv)) * S[base + i];
+}
+
+// dg for GLA, per key channel, in two launches. dgc_tile_kernel, one CTA per
+// (b, h, 256-token tile), one thread per channel: the suffix sum over the
+// tile of q[c] dq[c] - k[c] dk[c] (coalesced over the channels), with the
+// tile's totals in `tot`. dgc_carry_kernel, one CTA per (b, h): row sums of
+// dS ⊙ S_final plus the later tiles' totals, added to the tile's tokens.
+template <typename Tin>
+__global__ void __launch_bounds__(128) dgc_tile_kernel(const Tin *__restrict__ q, const Tin *__restrict__ dq,
+                                                       const Tin *__restrict__ k, const Tin *__restrict__ dk, int T,
+                                                       int dkk, float *__restrict__ dg, float *__restrict__ tot) {
+  const int bh = blockIdx.x, tile = blockIdx.y, c = threadIdx.x;
+  if (c >= dkk) return;
+  const int t0 = tile * 256, t1 = min(t0 + 256, T);
+  float acc = 0.f;
+#pragma unroll 4
+  for (int u = t1 - 1; u >= t0; --u) {
+    const size_t r = ((size_t)bh * T + u) * dkk + c;
+    acc += ldf(q + r) * ldf(dq + r) - ldf(k + r) * ldf(dk + r);
+    dg[r] = acc;
+  }
+  tot[((size_t)bh * gridDim.y + tile) * dkk + c] = acc;
+}
+
+__global__ void __launch_bounds__(128) dgc_carry_kernel(const float *__restrict__ dS, const float *__restrict__ S_final,
+                                                        const float *__restrict__ tot, int ntiles, int T, int dkk,
+                                                        int dv, float *__restrict__ dg) {
+  const int bh = blockIdx.x, c = threadIdx.x;
+  if (c >= dkk) return;
+  float carry = 0.f;
+  if (dS)
+    for (int j = 0; j < dv; ++j) {
+      const size_t i = ((size_t)bh * dkk + c) * dv + j;
+      carry = fmaf(dS[i], S_final[i], carry);
+    }
+  for (int tile = ntiles - 1; tile >= 0; --tile) {
+    const int t0 = tile * 256, t1 = min(t0 + 256, T);
+    for (int u = t0; u < t1; ++u) dg[((size_t)bh * T + u) * dkk + c] += carry;
+    carry += tot[((size_t)bh * ntiles + tile) * dkk + c];
+  }
+}
+
 bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // The forward recurrence over the time-reversed sequence, through the
 // kernels' reversed runs (tensor cores for bf16, CUDA cores for float32).
-int run_reversed(const void *q, const void *k, const void *v, const float *g, void *o, const float *S0,
-                 float *S_final, int B, int H, int T, int dk, int dv, int kind, bool f32, cudaStream_t s) {
-  ChunkParams p{q, k, v, g, nullptr, o, S0, S_final, B, H, T, dk, dv, 64, kind, f32 ? 1 : 0, status_word(), 1};
+int run_reversed(const void *q, const void *k, const void *v, const float *g, const float *beta, void *o,
+                 const float *S0, float *S_final, int B, int H, int T, int dk, int dv, int kind, bool f32,
+                 cudaStream_t s) {
+  ChunkParams p{q, k, v, g, beta, o, S0, S_final, B, H, T, dk, dv, 64, kind, f32 ? 1 : 0, status_word(), 1};
   if (!p.status) {
     set_error("la_chunk_bwd: no CUDA device available (%s)", cudaGetErrorString(cudaGetLastError()));
     return LA_ERR_CUDA;
@@ -188,20 +238,26 @@ extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const f
     set_error("%s: dk and dv must be 64 or 128 (got %d, %d)", fn, dk_, dv_);
     return LA_ERR_UNSUPPORTED;
   }
-  if ((mode & ~(0xff | LA_F32)) != 0 || (kind != LA_LINEAR && kind != LA_RETNET && kind != LA_SCALAR_GATE)) {
-    set_error("%s: mode 0x%x: the backward pass covers LA_LINEAR, LA_RETNET and LA_SCALAR_GATE (optionally | LA_F32)",
-              fn, mode);
+  if ((mode & ~(0xff | LA_F32)) != 0 ||
+      (kind != LA_LINEAR && kind != LA_RETNET && kind != LA_SCALAR_GATE && kind != LA_GLA)) {
+    set_error("%s: mode 0x%x: the backward pass covers LA_LINEAR, LA_RETNET, LA_SCALAR_GATE and LA_GLA "
+              "(optionally | LA_F32)", fn, mode);
     return (mode & ~(0xff | LA_F32)) == 0 && kind >= LA_LINEAR && kind <= LA_OUTER_GATE ? LA_ERR_UNSUPPORTED
                                                                                   : LA_ERR_INVALID_ARG;
   }
-  const bool scalar = kind == LA_SCALAR_GATE;
+  const bool scalar = kind == LA_SCALAR_GATE, gla = kind == LA_GLA;
   if ((kind == LA_LINEAR) != (g == nullptr)) {
-    set_error("%s: LA_RETNET needs g (float32 [H]) and LA_SCALAR_GATE g (float32 [B][H][T]); LA_LINEAR takes none", fn);
+    set_error("%s: LA_RETNET needs g (float32 [H]), LA_SCALAR_GATE g [B][H][T], LA_GLA g [B][H][T][dk]; "
+              "LA_LINEAR takes none", fn);
     return LA_ERR_INVALID_ARG;
   }
-  if (dg_out && !scalar) {
-    set_error("%s: dg is the gradient of LA_SCALAR_GATE's log-gates (NULL for other modes)", fn);
+  if (dg_out && !scalar && !gla) {
+    set_error("%s: dg is the gradient of the data-dependent log-gates (LA_SCALAR_GATE, LA_GLA; NULL otherwise)", fn);
     return LA_ERR_INVALID_ARG;
+  }
+  if (gla && (mode & LA_F32)) {
+    set_error("%s: the LA_GLA backward takes bfloat16 inputs only", fn);
+    return LA_ERR_UNSUPPORTED;
   }
   if (C != 0 && C != 64) {
     set_error("%s: chunk length C=%d is not implemented in this build (use 0 or 64)", fn, C);
@@ -226,7 +282,10 @@ extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const f
   // forward's final state and a scratch output of the forward pass that produces it
   const size_t n_s = BH * dk_ * dv_ * 4;
   const int ntiles = (T + 255) / 256;  // dg's 256-token tiles
-  const size_t bytes = (dg_out ? 5 : 4) * n_s + (dg_out ? BH * (size_t)T * dv_ * esz + ((BH * ntiles + 3) & ~static_cast<size_t>(3)) * 4 : 0);
+  const size_t ntot = (BH * ntiles * (gla ? dk_ : 1) + 3) & ~static_cast<size_t>(3);  // their totals (floats)
+  // GLA: zero key-axis gates [B][H][T][dv] for the outer-product-gate passes (dq, dk)
+  const size_t nzero = gla ? BH * (size_t)T * dv_ * 4 : 0;
+  const size_t bytes = (dg_out ? 5 : 4) * n_s + (dg_out ? BH * (size_t)T * dv_ * esz + ntot * 4 : 0) + nzero;
   uint8_t *ws = nullptr;
   cudaMemPool_t pool = library_pool();
   if (!pool) {
@@ -241,7 +300,8 @@ extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const f
   float *s0t = reinterpret_cast<float *>(ws), *dst = s0t + BH * dk_ * dv_, *dss = dst + BH * dk_ * dv_,
         *sfin = dss + BH * dk_ * dv_, *sT = sfin + BH * dk_ * dv_;
   float *tiles = sT + BH * dk_ * dv_;  // dg's per-tile totals, then the forward's scratch output
-  void *oscr = tiles + ((BH * ntiles + 3) & ~static_cast<size_t>(3));
+  uint8_t *oscr = reinterpret_cast<uint8_t *>(tiles + (dg_out ? ntot : 0));
+  float *zg = reinterpret_cast<float *>(oscr + (dg_out ? BH * (size_t)T * dv_ * esz : 0));
   int rc = LA_OK;
   auto fail = [&](const char *what) {
     if (rc == LA_OK) {
@@ -252,28 +312,36 @@ extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const f
   // RetNet's reversed passes use the unshifted per-head decay, so their initial
   // states carry 1 / gamma; the scalar decay's reversed runs shift the gates instead
   const float *g_head = kind == LA_RETNET ? g : nullptr;
+  if (gla && cudaMemsetAsync(zg, 0, nzero, s) != cudaSuccess) fail("zero gates");
   if (S0 || dS_final) {
     state_prep_kernel<<<dim3(8, (unsigned)BH), 256, 0, s>>>(S0, dS_final, g_head, H, dk_, dv_, s0t, dst, dss);
     if (cudaGetLastError() != cudaSuccess) fail("initial-state preparation");
   }
   const int fwd_mode = mode & (0xff | LA_F32);
-  // dq: queries dO, keys v, values k (key width dv, value width dk), initial state S0^T
+  // dq: queries dO, keys v, values k (key width dv, value width dk), initial state S0^T; for GLA the
+  // decay acts on k's channels, the value axis of this pass: the outer-product gate with unit key gates
   if (rc == LA_OK) {
-    const int r = la_chunk_fwd(dO, v, k, g, nullptr, dq, S0 ? s0t : nullptr, nullptr, B, H, T, dv_, dk_, C, fwd_mode,
-                               stream);
-    if (r != LA_OK) {
-      rc = r;
-    }
+    const int r = gla ? la_chunk_fwd(dO, v, k, zg, g, dq, S0 ? s0t : nullptr, nullptr, B, H, T, dv_, dk_, C,
+                                     LA_OUTER_GATE, stream)
+                      : la_chunk_fwd(dO, v, k, g, nullptr, dq, S0 ? s0t : nullptr, nullptr, B, H, T, dv_, dk_, C,
+                                     fwd_mode, stream);
+    if (r != LA_OK) rc = r;
   }
-  // dk (reversed run): queries v, keys dO, values q, initial state dS^T (/ gamma)
+  // dk (reversed run): queries v, keys dO, values q, initial state dS^T (/ gamma); GLA again on the value axis
   if (rc == LA_OK)
-    rc = run_reversed(v, dO, q, g, dkg, dS_final ? dst : nullptr, nullptr, B, H, T, dv_, dk_, kind, f32, s);
+    rc = gla ? run_reversed(v, dO, q, zg, g, dkg, dS_final ? dst : nullptr, nullptr, B, H, T, dv_, dk_, kOuter, f32, s)
+             : run_reversed(v, dO, q, g, nullptr, dkg, dS_final ? dst : nullptr, nullptr, B, H, T, dv_, dk_, kind, f32,
+                            s);
   // dv (reversed run): queries k, keys q, values dO, initial state dS (/ gamma); its final state x alpha = dS0
   if (rc == LA_OK)
-    rc = run_reversed(k, q, dO, g, dvg, dS_final ? dss : nullptr, dS0 ? sfin : nullptr, B, H, T, dk_, dv_, kind, f32,
-                      s);
+    rc = run_reversed(k, q, dO, g, nullptr, dvg, dS_final ? dss : nullptr, dS0 ? sfin : nullptr, B, H, T, dk_, dv_,
+                      kind, f32, s);
   if (rc == LA_OK && dS0) {
-    scale_state_kernel<<<dim3(8, (unsigned)BH), 256, 0, s>>>(sfin, g, H, scalar ? (long long)T : 0ll, dk_ * dv_, dS0);
+    if (gla)
+      scale_rows_kernel<<<dim3(8, (unsigned)BH), 256, 0, s>>>(sfin, g, T, dk_, dv_, dS0);
+    else
+      scale_state_kernel<<<dim3(8, (unsigned)BH), 256, 0, s>>>(sfin, g, H, scalar ? (long long)T : 0ll, dk_ * dv_,
+                                                                dS0);
     if (cudaGetLastError() != cudaSuccess) fail("dS0 scaling");
   }
   if (rc == LA_OK && dg_out) {
@@ -282,7 +350,15 @@ extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const f
       const int r = la_chunk_fwd(q, k, v, g, nullptr, oscr, S0, sT, B, H, T, dk_, dv_, C, fwd_mode, stream);
       if (r != LA_OK) rc = r;
     }
-    if (rc == LA_OK) {
+    if (rc == LA_OK && gla) {
+      const dim3 grid((unsigned)BH, (unsigned)ntiles);
+      dgc_tile_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(
+          static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(dq),
+          static_cast<const __nv_bfloat16 *>(k), static_cast<const __nv_bfloat16 *>(dkg), T, dk_, dg_out, tiles);
+      if (cudaGetLastError() == cudaSuccess)
+        dgc_carry_kernel<<<(unsigned)BH, 128, 0, s>>>(dS_final, sT, tiles, ntiles, T, dk_, dv_, dg_out);
+      if (cudaGetLastError() != cudaSuccess) fail("dg suffix sums");
+    } else if (rc == LA_OK) {
       const dim3 grid((unsigned)BH, (unsigned)ntiles);
       if (f32)
         dg_tile_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float *>(q), static_cast<const float *>(dq),

@@ -26,17 +26,19 @@
 // gates, which stay in L2), and the per-column factor e^{bv_m} e^{bv_last' -
 // bv_m'} rides on the state round trip next to the key-axis one.
 //
-// REV (plain linear attention, RetNet, scalar decay) runs the same recurrence
-// over the time-reversed sequence without copying it: chunk j is the 64-row window
+// REV (every unit-write mode but elu+1) runs the same recurrence over the
+// time-reversed sequence without copying it: chunk j is the 64-row window
 // ending at row T-1-64j of the stored tensors (its TMA load may start above
 // row 0, where the fill is zero), and its smem row m is reversed row 63-m.
 // The per-row gate factors are written to the slots of the smem rows, the
 // masks become s >= r, and o lands in stored order, so the anti-causal passes
 // of the backward read and write q, k, v, dO, dk, dv where they are. With
-// data-dependent scalar gates, position t of a reversed run decays by the
-// gate of the stored token after it (index T - t; none at t = 0): the decay
-// between stored tokens s < u is then the product of the gates of s+1 .. u,
-// as the backward's anti-causal sums need.
+// data-dependent gates (scalar, per key channel, per value column), position
+// t of a reversed run decays by the gate of the stored token after it (index
+// T - t; none at t = 0): the decay between stored tokens s < u is then the
+// product of the gates of s+1 .. u, as the backward's anti-causal sums need.
+// The per-channel prefixes then run from smem row 63 down to 0, with the
+// midpoint at smem row 32 (reversed row 31).
 //
 // Roles (384 threads):
 //   warp 0      TMA producer: q/k/v (and GLA gate) tiles into an ns-stage ring
@@ -133,8 +135,9 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
   constexpr bool elu = KIND == kElu1, outer = KIND == kOuter;
   constexpr bool gla = chan_gates(KIND);  // key-axis channel gates (GLA and the outer-product gate)
   constexpr bool sgate = KIND == kRetnet || KIND == kScalar;
-  static_assert(!REV || KIND == kLinear || KIND == kRetnet || KIND == kScalar,
-                "reversed runs: unit write with no gate, a per-head or a per-token scalar decay");
+  static_assert(!REV || KIND != kElu1, "reversed runs: the unit-write modes without a normaliser");
+  // smem rows of the chunk midpoint and of its last token (reversed runs: rows 32 and 0)
+  constexpr int kMidRow = REV ? kC - 1 - kMid : kMid, kLastRow = REV ? 0 : kC - 1;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const WsLayout L = ws_layout(DK, DV, KIND, ns);
@@ -266,9 +269,12 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
 #pragma unroll
         for (int a = 0; a < DV / 64; ++a)
           tma_load_3d(st + L.v + a * 8192, &tm_v, &full[s], 64 * a, t0, bh);
-        if (gla) tma_load_3d(st + L.g, &tm_g, &full[s], 0, t0, bh);
-        if (outer)  // the value-axis gates are read with plain loads by the key and state groups
-          bulk_prefetch_l2(p.beta + ((size_t)bh * T + t0) * DV, (uint32_t)min(kC, T - t0) * DV * 4u);
+        // (reversed runs: the gates of the stored tokens one row later; rows past T read zero)
+        if (gla) tma_load_3d(st + L.g, &tm_g, &full[s], 0, REV ? t0 + 1 : t0, bh);
+        if (outer) {  // the value-axis gates are read with plain loads by the key and state groups
+          const int g0r = REV ? max(t0 + 1, 0) : t0, g1r = REV ? min(t0 + 1 + kC, T) : min(t0 + kC, T);
+          if (g1r > g0r) bulk_prefetch_l2(p.beta + ((size_t)bh * T + g0r) * DV, (uint32_t)(g1r - g0r) * DV * 4u);
+        }
         if (sgate) mbar_arrive(&full[s]);  // the gate prefix of this chunk is in place
         // the load of chunk j + ns waits for this chunk's last MMA; warm L2 now
         // (a prefetch is a hint: the reversed run skips a window that starts above row 0)
@@ -281,7 +287,7 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
           }
 #pragma unroll
           for (int a = 0; a < DV / 64; ++a) tma_prefetch_3d(&tm_v, 64 * a, tp, bh);
-          if (gla) tma_prefetch_3d(&tm_g, 0, tp, bh);
+          if (gla) tma_prefetch_3d(&tm_g, 0, REV ? tp + 1 : tp, bh);
         }
       }
       issued = j + 1;
@@ -433,13 +439,26 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
         // outer-product gate: value column v's log2 prefix over the chunk (the key
         // group's scan, redone from L2), carried across the two halves
         float vcar = 0.f, vbm = 0.f;
-        const float *gvc = outer ? p.beta + ((size_t)bh * T + (size_t)c * kC) * DV + v : nullptr;
+        const int vrb = REV ? T - (c + 1) * kC + 1 : c * kC;  // stored row of smem row 0's gate
+        const float *gvc = outer ? p.beta + (size_t)bh * T * DV + v : nullptr;
+        auto vgate = [&](int m) {
+          return (v < DV && vrb + m >= 0 && vrb + m < T && (!REV || m >= kC - n)) ? __ldg(gvc + (size_t)(vrb + m) * DV)
+                                                                                  : 0.f;
+        };
+        if (outer && REV) {  // the scan runs from smem row 63: rows 32..63 first give the midpoint
+          float x[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[e] = vgate(32 + e);
+#pragma unroll
+          for (int e = 31; e >= 0; --e) vcar = fmaf(x[e], kLog2e, vcar);
+          vbm = vcar;
+        }
 #pragma unroll 1
         for (int r0 = 0; r0 < kC; r0 += 32) {
           float a[32], gq[outer ? 32 : 1];
           if (outer) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) gq[e] = (v < DV && r0 + e < n) ? __ldg(gvc + (size_t)(r0 + e) * DV) : 0.f;
+            for (int e = 0; e < 32; ++e) gq[e] = vgate(r0 + e);
           }
           tmem_ld32(tl + kColO + ob * 64 + r0, a);
           if (sgate) {  // O = e^{b_r} (S^T Q^T) + (local part)
@@ -452,12 +471,21 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
           }
           tmem_wait_ld();
           if (outer) {  // o = e^{bv - bv_m} (midpoint-relative value-axis products)
+            if (REV) {  // rows 0..31 continue from row 32; rows 32..63 start at row 63
+              float car = r0 == 0 ? vbm : 0.f;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              vcar = fmaf(gq[e], kLog2e, vcar);
-              gq[e] = vcar;
+              for (int e = 31; e >= 0; --e) {
+                car = fmaf(gq[e], kLog2e, car);
+                gq[e] = car;
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                vcar = fmaf(gq[e], kLog2e, vcar);
+                gq[e] = vcar;
+              }
+              if (r0 == 0) vbm = gq[kMid];
             }
-            if (r0 == 0) vbm = gq[kMid];
 #pragma unroll
             for (int e = 0; e < 32; ++e) a[e] *= ex2(gq[e] - vbm);
           }
@@ -545,22 +573,32 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
       if (gla) {
         if (kg < DK) {  // channel kg: all 64 loads first, then the scan (log2 units) in registers
           float b[kC];
+          // (reversed runs: the padding rows above a short last window read the gate of the
+          // stored row just below them, row 0's; they must not decay)
 #pragma unroll
-          for (int r = 0; r < kC; ++r) b[r] = gt[r * DK + kg];
-          b[0] *= kLog2e;
+          for (int r = 0; r < kC; ++r) b[r] = (!REV || r >= kC - n) ? gt[r * DK + kg] : 0.f;
+          if (REV) {  // the reversed sequence's order: smem row 63 first
+            b[kC - 1] *= kLog2e;
 #pragma unroll
-          for (int r = 1; r < kC; ++r) b[r] = fmaf(b[r], kLog2e, b[r - 1]);
+            for (int r = kC - 2; r >= 0; --r) b[r] = fmaf(b[r], kLog2e, b[r + 1]);
+          } else {
+            b[0] *= kLog2e;
+#pragma unroll
+            for (int r = 1; r < kC; ++r) b[r] = fmaf(b[r], kLog2e, b[r - 1]);
+          }
 #pragma unroll
           for (int r = 0; r < kC; ++r) gt[r * DK + kg] = b[r];
-          const float lm = ex2(b[kC - 1] - b[kMid]);
-          ms[kMsBM + kg] = ex2(b[kMid]) * lm_prev;
+          const float lm = ex2(b[kLastRow] - b[kMidRow]);
+          ms[kMsBM + kg] = ex2(b[kMidRow]) * lm_prev;
           ms[kMsLM + kg] = lm;
           lm_prev = lm;
         }
         if (outer && kg < DV) {  // value column kg: the loads fly during the q/k transform
-          const float *gp = p.beta + ((size_t)bh * T + (size_t)j * kC) * DV + kg;
+          const int rb = REV ? T - (j + 1) * kC + 1 : j * kC;  // stored row of smem row 0's gate
+          const float *gp = p.beta + (size_t)bh * T * DV + kg;
 #pragma unroll
-          for (int r = 0; r < kC; ++r) gvr[r] = (r < n) ? __ldg(gp + (size_t)r * DV) : 0.f;
+          for (int r = 0; r < kC; ++r)
+            gvr[r] = (rb + r >= 0 && rb + r < T && (!REV || r >= kC - n)) ? __ldg(gp + (size_t)(rb + r) * DV) : 0.f;
         }
         group_sync(kBarKG);
         // Q e^{b - b_mid}, K e^{b_mid - b} in place: thread kg owns 8-channel
@@ -569,7 +607,7 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
         const int cg = kg % kGroups, r0 = kg / kGroups;
         float bm[8];
         {
-          const float4 *mp = reinterpret_cast<const float4 *>(gt + kMid * DK + cg * 8);
+          const float4 *mp = reinterpret_cast<const float4 *>(gt + kMidRow * DK + cg * 8);
           const float4 m0 = mp[0], m1 = mp[1];
           bm[0] = m0.x; bm[1] = m0.y; bm[2] = m0.z; bm[3] = m0.w;
           bm[4] = m1.x; bm[5] = m1.y; bm[6] = m1.z; bm[7] = m1.w;
@@ -632,10 +670,16 @@ chunk_ws_kernel(const ChunkParams p, int ns, const __grid_constant__ CUtensorMap
       // column kg, d = bv - bv_m into the dead gate tile, then V e^{-d} in place
       if (outer) {
         if (kg < DV) {
-          gvr[0] *= kLog2e;
+          if (REV) {
+            gvr[kC - 1] *= kLog2e;
 #pragma unroll
-          for (int r = 1; r < kC; ++r) gvr[r] = fmaf(gvr[r], kLog2e, gvr[r - 1]);
-          const float bm = gvr[kMid], lv = ex2(gvr[kC - 1] - bm);
+            for (int r = kC - 2; r >= 0; --r) gvr[r] = fmaf(gvr[r], kLog2e, gvr[r + 1]);
+          } else {
+            gvr[0] *= kLog2e;
+#pragma unroll
+            for (int r = 1; r < kC; ++r) gvr[r] = fmaf(gvr[r], kLog2e, gvr[r - 1]);
+          }
+          const float bm = gvr[kMidRow], lv = ex2(gvr[kLastRow] - bm);
 #pragma unroll
           for (int r = 0; r < kC; ++r) gt[r * DV + kg] = gvr[r] - bm;
           ms[kMsBMV + kg] = ex2(bm) * lv_prev;
@@ -843,8 +887,9 @@ int launch_chunk_ws(const ChunkParams &p, cudaStream_t stream) {
     if (p.kind == kLinear) return launch_kind<kLinear, true>(p, stream);
     if (p.kind == kRetnet) return launch_kind<kRetnet, true>(p, stream);
     if (p.kind == kScalar) return launch_kind<kScalar, true>(p, stream);
-    set_error("la_chunk_fwd: the reversed run covers linear attention, RetNet and scalar decay only (mode %d)",
-              p.kind);
+    if (p.kind == kGla) return launch_kind<kGla, true>(p, stream);
+    if (p.kind == kOuter) return launch_kind<kOuter, true>(p, stream);
+    set_error("la_chunk_fwd: no reversed run for mode %d", p.kind);
     return LA_ERR_UNSUPPORTED;
   }
   switch (p.kind) {

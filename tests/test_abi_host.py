@@ -208,7 +208,8 @@ def _bwd(**kw):
     (dict(dg_out=A), "LA_ERR_INVALID_ARG"),           # dg only for the scalar decay
     (dict(mode=2, g=A, dg_out=A), "LA_ERR_INVALID_ARG"),
     (dict(mode=4, g=A, dg_out=A + 4), "LA_ERR_INVALID_ARG"),  # dg 16-byte aligned
-    (dict(mode=3, g=A), "LA_ERR_UNSUPPORTED"),        # gla: no backward in this build
+    (dict(mode=6, g=A), "LA_ERR_UNSUPPORTED"),        # kda: no backward in this build
+    (dict(mode=3 | 0x100, g=A), "LA_ERR_UNSUPPORTED"),  # gla backward: bf16 only
 ])
 def test_chunk_bwd_rejects_bad_arguments(lib, kw, code):
     rc, msg = _bwd(**kw)

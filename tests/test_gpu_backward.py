@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle.backward import backward, backward_scalar
+from oracle.backward import backward, backward_gla, backward_scalar
 from paritylib import assert_close, f64, make
 
 pytestmark = pytest.mark.gpu
@@ -42,8 +42,8 @@ def _run(mode, q, k, v, g, dO, S0, dS):
     cu = lambda t: None if t is None else t.to(dev).contiguous()
     out = la.chunk_bwd(cu(q), cu(k), cu(v), cu(dO), mode, g=cu(g), S0=cu(S0), dS_final=cu(dS))
     torch.cuda.synchronize()
-    assert out[4] is None or mode == "scalar"
-    return out[:4] if mode != "scalar" else out
+    assert out[4] is None or mode in ("scalar", "gla")
+    return out[:4] if mode not in ("scalar", "gla") else out
 
 
 @pytest.mark.parametrize("mode", ["linear", "retnet"])
@@ -133,3 +133,56 @@ def test_scalar_backward_without_states_or_dS():
     for name, got, r in (("dq", dq, ref[0]), ("dk", dk_, ref[1]), ("dv", dv_, ref[2]), ("dS0", dS0, ref[3])):
         assert_close(f64(got), r, "bf16", f"scalar {name}")
     _check_dg(f64(dg), ref, "bf16", "scalar dg", f64(q), f64(k))
+
+
+# --- GLA's per-channel decay, with the per-channel dg ------------------------------------
+# dq and dk come from outer-product-gate passes (the decay on their value axis),
+# dv from a reversed GLA run; dg[c] is held to the same rounding bound as the
+# scalar decay's, channel by channel.
+
+def _gla_case(B, H, T, dk, dv, seed=0):
+    from workloads import WORKLOADS
+    wl = WORKLOADS["gla"].with_sizes(B=B, H=H, T=T, dk=dk, dv=dv, s0=True, seed=80 + seed)
+    inp = make(wl)
+    gen = torch.Generator().manual_seed(90 + seed)
+    dO = (torch.randn(B, H, T, dv, generator=gen) / np.sqrt(dv)).to(torch.bfloat16)
+    dS = torch.randn(B, H, dk, dv, generator=gen) * 0.1
+    S0 = torch.randn(B, H, dk, dv, generator=gen) * 0.1
+    return inp["q"], inp["k"], inp["v"], inp["g"], dO, S0, dS
+
+
+def _check_dgc(got, ref, what, q, k, v, g, S0, dS):
+    """Besides the rounding of dq and dk, dg carries the final-state term
+    sum_j dS[c, j] S_final[c, j] with S_final from the bf16 forward kernel
+    (held to 2^-6 of sum_j |dS S_final|, the forward state's bf16 operand
+    rounding with margin)."""
+    from oracle import recurrence
+    assert np.all(np.isfinite(got)), what
+    mag = np.abs(q * ref[0]) + np.abs(k * ref[1])                         # [B, H, T, dk]
+    bound = 2.0 ** -8 * np.cumsum(mag[:, :, ::-1], axis=2)[:, :, ::-1] + 1e-5
+    if dS is not None:
+        _, S_T = recurrence(q, k, v, "gla", g=g, S0=S0)
+        bound = bound + 2.0 ** -6 * np.sum(np.abs(dS * S_T), axis=-1)[:, :, None, :]
+    bad = np.abs(got - ref[4]) > bound
+    assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} outside the rounding bound"
+
+
+@pytest.mark.parametrize("dims", [(128, 128), (64, 64), (64, 128)])
+@pytest.mark.parametrize("T", [1, 64, 129, 300])
+def test_gla_backward_parity(dims, T):
+    dk, dv = dims
+    q, k, v, g, dO, S0, dS = _gla_case(1, 2, T, dk, dv)
+    dq, dk_, dv_, dS0, dg = _run("gla", q, k, v, g, dO, S0, dS)
+    ref = backward_gla(f64(q), f64(k), f64(v), f64(dO), f64(g), S0=f64(S0), dS=f64(dS))
+    for name, got, r in (("dq", dq, ref[0]), ("dk", dk_, ref[1]), ("dv", dv_, ref[2]), ("dS0", dS0, ref[3])):
+        assert_close(f64(got), r, "bf16", f"gla T={T} {name}")
+    _check_dgc(f64(dg), ref, f"gla T={T} dg", f64(q), f64(k), f64(v), f64(g), f64(S0), f64(dS))
+
+
+def test_gla_backward_without_states_or_dS():
+    q, k, v, g, dO, S0, dS = _gla_case(1, 2, 200, 128, 128, seed=1)
+    dq, dk_, dv_, dS0, dg = _run("gla", q, k, v, g, dO, None, None)
+    ref = backward_gla(f64(q), f64(k), f64(v), f64(dO), f64(g))
+    for name, got, r in (("dq", dq, ref[0]), ("dk", dk_, ref[1]), ("dv", dv_, ref[2]), ("dS0", dS0, ref[3])):
+        assert_close(f64(got), r, "bf16", f"gla {name}")
+    _check_dgc(f64(dg), ref, "gla dg", f64(q), f64(k), f64(v), f64(g), None, None)
