@@ -84,12 +84,13 @@ def test_backward_bench_shape_sampled():
 
 # --- the data-dependent scalar decay, with dg ------------------------------------------
 # dg is a suffix sum over up to T tokens of w_u = q_u.dq_u - k_u.dk_u, formed
-# from the dq and dk the passes write in the input dtype. Rounding dq and dk
-# to bfloat16 moves each product by at most 2^-9 of its size, so
-#   |dg_tau - ref_tau| <= 2^-8 * sum_{u>=tau} sum_c (|q_u,c dq_u,c| + |k_u,c dk_u,c|) + 1e-5
-# (twice the rounding bound, for the float32 accumulation); the terms of w
-# cancel, so a relative bound on dg itself would not follow from the
-# arithmetic. float32 inputs: the library's float32 tolerance.
+# from the dq and dk the passes write in the input dtype. Each element of the
+# bf16 dq and dk carries the passes' bf16 arithmetic: the two MMA operands and
+# the state copy rounded to bf16 (2^-9 each) and the output rounding (2^-9),
+# about 2^-7 of the contributions' size; with a factor 2 of margin,
+#   |dg_tau - ref_tau| <= 2^-6 * sum_{u>=tau} sum_c (|q_u,c dq_u,c| + |k_u,c dk_u,c|) + 1e-5.
+# The terms of w cancel, so a relative bound on dg itself would not follow
+# from the arithmetic. float32 inputs: the library's float32 tolerance.
 
 def _scalar_case(dtype, B, H, T, dk, dv, seed=0):
     from workloads import WORKLOADS
@@ -108,7 +109,7 @@ def _check_dg(got, ref, dtype, what, q, k):
         return
     assert np.all(np.isfinite(got)), what
     mag = np.sum(np.abs(q * ref[0]) + np.abs(k * ref[1]), axis=-1)        # [B, H, T]
-    bound = 2.0 ** -8 * np.cumsum(mag[..., ::-1], axis=-1)[..., ::-1] + 1e-5
+    bound = 2.0 ** -6 * np.cumsum(mag[..., ::-1], axis=-1)[..., ::-1] + 1e-5
     bad = np.abs(got - ref[4]) > bound
     assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} outside the rounding bound"
 
@@ -137,8 +138,8 @@ def test_scalar_backward_without_states_or_dS():
 
 # --- GLA's per-channel decay, with the per-channel dg ------------------------------------
 # dq and dk come from outer-product-gate passes (the decay on their value axis),
-# dv from a reversed GLA run; dg[c] is held to the same rounding bound as the
-# scalar decay's, channel by channel.
+# dv from a reversed GLA run; dg[c] is held to the same bound as the scalar
+# decay's, channel by channel.
 
 def _gla_case(B, H, T, dk, dv, seed=0):
     from workloads import WORKLOADS
@@ -159,7 +160,7 @@ def _check_dgc(got, ref, what, q, k, v, g, S0, dS):
     from oracle import recurrence
     assert np.all(np.isfinite(got)), what
     mag = np.abs(q * ref[0]) + np.abs(k * ref[1])                         # [B, H, T, dk]
-    bound = 2.0 ** -8 * np.cumsum(mag[:, :, ::-1], axis=2)[:, :, ::-1] + 1e-5
+    bound = 2.0 ** -6 * np.cumsum(mag[:, :, ::-1], axis=2)[:, :, ::-1] + 1e-5
     if dS is not None:
         _, S_T = recurrence(q, k, v, "gla", g=g, S0=S0)
         bound = bound + 2.0 ** -6 * np.sum(np.abs(dS * S_T), axis=-1)[:, :, None, :]
