@@ -55,6 +55,7 @@ KERNEL_SOURCES = {
     "noncausal": [_CS + "la_chunk_mat.cu"] + _COMMON,
     "backward": [_CS + "la_backward.cu", _CS + "la_chunk_ws.cu", _CS + "la_chunk_mat.cu"] + _COMMON,
     "backward_scalar": [_CS + "la_backward.cu", _CS + "la_chunk_ws.cu", _CS + "la_chunk_mat.cu"] + _COMMON,
+    "backward_gla": [_CS + "la_backward.cu", _CS + "la_chunk_ws.cu"] + _COMMON,
     "decode": [_CS + "la_step.cu"],
     "gdelta": [_CS + "la_chunk_gdelta.cu"],
     "prologue": [_CS + "la_prologue.cu", _CS + "la_sm100.cuh"],
@@ -731,17 +732,26 @@ def backward_bytes(wl) -> float:
     per_tok = e * (2 * wl.dk + 2 * wl.dv) + e * (2 * wl.dk + wl.dv)
     if wl.mode == "scalar":  # read g, write dg
         per_tok += 8
+    elif wl.mode == "gla":
+        per_tok += 8 * wl.dk
     return float(wl.B * wl.H * (wl.T * per_tok + 2 * 4 * wl.dk * wl.dv))
 
 
 def time_backward_oracle(wl, inp, target_s: float = 10.0):
-    from oracle.backward import backward, backward_scalar
+    from oracle.backward import backward, backward_gla, backward_scalar
     f64 = lambda t: None if t is None else t.to(torch.float64).numpy()
     BH = wl.B * wl.H
     done, t0 = 0, time.perf_counter()
     while done < BH and (time.perf_counter() - t0) < target_s:
         b, h = done // wl.H, done % wl.H
         sl = lambda t: f64(t[b:b + 1, h:h + 1])
+        if wl.mode == "gla":  # quadratic in T: a 512-token prefix of one head
+            pre = lambda t: t[..., :512, :]
+            backward_gla(pre(sl(inp["q"])), pre(sl(inp["k"])), pre(sl(inp["v"])), pre(sl(inp["dO"])),
+                         pre(sl(inp["g"])), dS=sl(inp["dS"]))
+            dt = time.perf_counter() - t0
+            return 512 / wl.H / dt, 1, ("the first 512 tokens of 1 (batch, head) sequence, float64 numpy "
+                                        "(explicit pair sums: quadratic in T, so faster per token than at T=4096)"), dt
         if wl.mode == "scalar":
             backward_scalar(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["dO"]), sl(inp["g"]), dS=sl(inp["dS"]))
         else:
@@ -796,6 +806,8 @@ def bench_backward(args, rank, world, local_rank):
             "dS0": torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)}
     if wl.mode == "scalar":
         outs["dg"] = torch.empty(B, H, T, dtype=torch.float32, device=dev)
+    elif wl.mode == "gla":
+        outs["dg"] = torch.empty(B, H, T, dk, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     mode_id = la.MODE_IDS[wl.mode] | (la.CONSTANTS["LA_F32"] if wl.dtype == "f32" else 0)
@@ -839,7 +851,9 @@ def bench_backward(args, rank, world, local_rank):
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
             "frac": round(achieved / hbm_peak, 4), "traffic": recorded_traffic(wl.name), "peak_source": peak_src,
             "algorithmic_bytes": alg, "kernel": "3 x chunk_ws_kernel (dq causal; dk and dv reversed runs)"
-            + (" + forward for S_final + dg_tile_kernel + dg_carry_kernel" if wl.mode == "scalar" else ""),
+            + (" + forward for S_final + dg_tile_kernel + dg_carry_kernel" if wl.mode == "scalar" else
+               " + forward for S_final + dgc_tile_kernel + dgc_carry_kernel (dq, dk: outer-product-gate passes)"
+               if wl.mode == "gla" else ""),
             "launch_ms_mean": round(statistics.mean(launch_ms), 4)}
     e2e = None
     if not args.no_e2e:
@@ -885,7 +899,7 @@ def bench_backward(args, rank, world, local_rank):
             "tflops": round(world * flop * args.steps / (total_ms / 1e3) / 1e12, 2), "roofline": roof,
             "cpu_baseline": cpu, "clocks": clk, "e2e": e2e,
             # state prep, 3 passes, dS0 scaling (+ the forward for S_final and the two dg launches)
-            "gpu_launches": args.steps * (8 if wl.mode == "scalar" else 5),
+            "gpu_launches": args.steps * {"scalar": 8, "gla": 8}.get(wl.mode, 5),
         }), flush=True)
     if dist:
         dist.destroy_process_group()

@@ -94,6 +94,10 @@ WORKLOADS = {
     # dS_final as for the backward workload.
     "backward_scalar": Workload("backward_scalar", "scalar", 8, 16, 4096, 128, 128, "bf16", 64, seed=13,
                                 qkv_scale=1.0 / math.sqrt(128.0), extra={"backward": True}),
+    # Backward of GLA with the per-channel log-gate gradient: the retnet shape, the
+    # gla q/k/v and gate recipe, dO and dS_final as for the backward workload.
+    "backward_gla": Workload("backward_gla", "gla", 8, 16, 4096, 128, 128, "bf16", 64, seed=14,
+                             qkv_scale=1.0 / math.sqrt(128.0), extra={"backward": True}),
     # Outer-product gate alpha_t beta_t^T (a next row): the GLA shape and q/k/v
     # recipe with GLA-distributed log-gates on both the key and the value axis.
     "outer": Workload("outer", "outer", 8, 16, 8192, 128, 128, "bf16", 64, seed=11,
