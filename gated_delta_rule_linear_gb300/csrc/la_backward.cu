@@ -160,8 +160,8 @@ __global__ void __launch_bounds__(256) scale_rows_kernel(const float *__restrict
 // dg for GLA, per key channel, in two launches. dgc_tile_kernel, one CTA per
 // (b, h, 256-token tile), one thread per channel: the suffix sum over the
 // tile of q[c] dq[c] - k[c] dk[c] (coalesced over the channels), with the
-// tile's totals in `tot`. dgc_carry_kernel, one CTA per (b, h): row sums of
-// dS ⊙ S_final plus the later tiles' totals, added to the tile's tokens.
+// tile's totals in `tot`. dgc_carry_kernel, one CTA per (b, h, tile): row
+// sums of dS ⊙ S_final plus the later tiles' totals, added to the tile's tokens.
 template <typename Tin>
 __global__ void __launch_bounds__(128) dgc_tile_kernel(const Tin *__restrict__ q, const Tin *__restrict__ dq,
                                                        const Tin *__restrict__ k, const Tin *__restrict__ dk, int T,
@@ -170,11 +170,20 @@ __global__ void __launch_bounds__(128) dgc_tile_kernel(const Tin *__restrict__ q
   if (c >= dkk) return;
   const int t0 = tile * 256, t1 = min(t0 + 256, T);
   float acc = 0.f;
-#pragma unroll 4
-  for (int u = t1 - 1; u >= t0; --u) {
-    const size_t r = ((size_t)bh * T + u) * dkk + c;
-    acc += ldf(q + r) * ldf(dq + r) - ldf(k + r) * ldf(dk + r);
-    dg[r] = acc;
+  for (int u1 = t1; u1 > t0; u1 -= 8) {  // eight tokens' loads in flight, then their suffix sums
+    float w[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int u = u1 - 1 - e;
+      const size_t r = ((size_t)bh * T + u) * dkk + c;
+      w[e] = (u >= t0) ? ldf(q + r) * ldf(dq + r) - ldf(k + r) * ldf(dk + r) : 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int u = u1 - 1 - e;
+      acc += w[e];
+      if (u >= t0) dg[((size_t)bh * T + u) * dkk + c] = acc;
+    }
   }
   tot[((size_t)bh * gridDim.y + tile) * dkk + c] = acc;
 }
@@ -182,7 +191,8 @@ __global__ void __launch_bounds__(128) dgc_tile_kernel(const Tin *__restrict__ q
 __global__ void __launch_bounds__(128) dgc_carry_kernel(const float *__restrict__ dS, const float *__restrict__ S_final,
                                                         const float *__restrict__ tot, int ntiles, int T, int dkk,
                                                         int dv, float *__restrict__ dg) {
-  const int bh = blockIdx.x, c = threadIdx.x;
+  // one CTA per (b, h, tile): the row sum of dS ⊙ S_final plus the later tiles' totals
+  const int bh = blockIdx.x, tile = blockIdx.y, c = threadIdx.x;
   if (c >= dkk) return;
   float carry = 0.f;
   if (dS)
@@ -190,10 +200,15 @@ __global__ void __launch_bounds__(128) dgc_carry_kernel(const float *__restrict_
       const size_t i = ((size_t)bh * dkk + c) * dv + j;
       carry = fmaf(dS[i], S_final[i], carry);
     }
-  for (int tile = ntiles - 1; tile >= 0; --tile) {
-    const int t0 = tile * 256, t1 = min(t0 + 256, T);
-    for (int u = t0; u < t1; ++u) dg[((size_t)bh * T + u) * dkk + c] += carry;
-    carry += tot[((size_t)bh * ntiles + tile) * dkk + c];
+  for (int tl = ntiles - 1; tl > tile; --tl) carry += tot[((size_t)bh * ntiles + tl) * dkk + c];
+  const int t0 = tile * 256, t1 = min(t0 + 256, T);
+  for (int u0 = t0; u0 < t1; u0 += 8) {  // eight tokens read, then written
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = (u0 + e < t1) ? dg[((size_t)bh * T + u0 + e) * dkk + c] : 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (u0 + e < t1) dg[((size_t)bh * T + u0 + e) * dkk + c] = x[e] + carry;
   }
 }
 
@@ -356,7 +371,7 @@ extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const f
           static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(dq),
           static_cast<const __nv_bfloat16 *>(k), static_cast<const __nv_bfloat16 *>(dkg), T, dk_, dg_out, tiles);
       if (cudaGetLastError() == cudaSuccess)
-        dgc_carry_kernel<<<(unsigned)BH, 128, 0, s>>>(dS_final, sT, tiles, ntiles, T, dk_, dv_, dg_out);
+        dgc_carry_kernel<<<grid, 128, 0, s>>>(dS_final, sT, tiles, ntiles, T, dk_, dv_, dg_out);
       if (cudaGetLastError() != cudaSuccess) fail("dg suffix sums");
     } else if (rc == LA_OK) {
       const dim3 grid((unsigned)BH, (unsigned)ntiles);
