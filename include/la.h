@@ -17,6 +17,15 @@
  * chunk, state passing between chunks); the result equals the token-by-token
  * recurrence up to floating-point rounding.
  *
+ * Entry points: la_chunk_fwd (the causal forward in every mode, and the
+ * non-causal form), la_chunk_fwd_noalloc (its materialised variant without
+ * allocation), la_chunk_fwd_gdelta (the generalised delta rule
+ * S_t = (I - b_t a_t^T) S_{t-1} + k_t v_t^T), la_chunk_bwd (the backward pass
+ * for LA_LINEAR, LA_RETNET, LA_SCALAR_GATE and LA_GLA), la_recurrent_step
+ * (one decode step), la_prologue (short convolution, L2 norm and gate
+ * activations in front of the forward), la_stream_status, la_last_error,
+ * la_version.
+ *
  * Conventions for every entry point
  *   - Tensors are dense row-major: q, k [B][H][T][dk], v, o [B][H][T][dv]
  *     (d fastest). Decode steps drop the T axis.
@@ -27,9 +36,10 @@
  *     LA_ELU1_NORM where W = dv + 1 and column dv holds the normaliser z.
  *   - All pointers are DEVICE pointers owned by the caller. The library never
  *     frees or retains them. Device memory of its own is taken only by the
- *     materialised variant of la_chunk_fwd: a workspace allocated and freed
- *     on `stream` from a library-owned stream-ordered pool (one per device)
- *     that keeps freed memory for the next call.
+ *     materialised variant and the non-causal form of la_chunk_fwd and by
+ *     la_chunk_bwd: workspaces allocated and freed on `stream` from a
+ *     library-owned stream-ordered pool (one per device) that keeps freed
+ *     memory for the next call.
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream);
  *     nothing synchronises with the host.
  *   - Return value: LA_OK, or an LA_ERR_* code with a message available from
