@@ -225,6 +225,17 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tm_q,
       sbeta[tid] = bt_next;
     }
     load_gate(i + 1, lg_next, bt_next);
+    if (L.ns == 1 && tid == 0 && i + 1 < nchunks) {  // one stage: warm L2 with the next chunk's tiles
+      const int tp = (i + 1) * kC;
+#pragma unroll
+      for (int a = 0; a < DK / 64; ++a) {
+        tma_prefetch_3d(&tm_q, 64 * a, tp, bh);
+        tma_prefetch_3d(&tm_k, 64 * a, tp, bh);
+      }
+#pragma unroll
+      for (int a = 0; a < DV / 64; ++a) tma_prefetch_3d(&tm_v, 64 * a, tp, bh);
+      if (pg) tma_prefetch_3d(&tm_g, 0, tp, bh);
+    }
     bool ok = mbar_wait_bounded(&bar_full[s], fpar, kSpin);
     if (__syncthreads_or(!ok)) { abort = true; break; }
     if (tid == 0) pending[s] = -1;
