@@ -210,6 +210,9 @@ def _bwd(**kw):
     (dict(mode=4, g=A, dg_out=A + 4), "LA_ERR_INVALID_ARG"),  # dg 16-byte aligned
     (dict(mode=6, g=A), "LA_ERR_UNSUPPORTED"),        # kda: no backward in this build
     (dict(mode=3 | 0x100, g=A), "LA_ERR_UNSUPPORTED"),  # gla backward: bf16 only
+    (dict(mode=3), "LA_ERR_INVALID_ARG"),             # gla needs g
+    (dict(mode=3, g=A, dg_out=A + 4), "LA_ERR_INVALID_ARG"),  # dg 16-byte aligned
+    (dict(mode=7, g=A), "LA_ERR_UNSUPPORTED"),        # outer-product gate: no backward
 ])
 def test_chunk_bwd_rejects_bad_arguments(lib, kw, code):
     rc, msg = _bwd(**kw)
