@@ -23,7 +23,13 @@
 //
 //   dg_tau = sum_{u >= tau} (q_u . dq_u - k_u . dk_u) + sum(dS_final ⊙ S_final),
 //
-// with S_final from a fourth (forward) pass.
+// with S_final from a fourth (forward) pass. GLA ("Talk Linear Attention"
+// section 5.1) is the same channel by channel: its decay acts on the key
+// channels, which are the value axis of the dq and dk passes, so those run on
+// the outer-product gate (unit gates on their key axis, g on their value
+// axis) and dv on GLA itself; dS0[c] = exp(g_0[c]) times row c of the last
+// pass's final state, and dg[c] is the suffix sum of q[c] dq[c] - k[c] dk[c]
+// plus row c's sum of dS_final ⊙ S_final.
 #include <cuda_bf16.h>
 
 #include <algorithm>
