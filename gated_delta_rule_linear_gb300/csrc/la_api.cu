@@ -19,8 +19,6 @@ thread_local char g_err[512] = "";
 __device__ unsigned g_status_word;
 
 constexpr int kMaxDevices = 64;
-unsigned *g_status_ptr[kMaxDevices] = {};
-std::mutex g_status_mu;
 
 // Stream-ordered pool for the materialised variant's workspace, one per
 // device, owned by the library. It keeps freed memory for the next call
@@ -62,16 +60,13 @@ void set_error(const char *fmt, ...) {
   va_end(ap);
 }
 
+// Looked up in the current context on every call (no synchronisation once
+// the module is loaded): a cached address would go stale if the context were
+// destroyed and created again.
 unsigned *status_word() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_status_mu);
-  if (!g_status_ptr[dev]) {
-    void *ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return nullptr;
-    g_status_ptr[dev] = static_cast<unsigned *>(ptr);
-  }
-  return g_status_ptr[dev];
+  void *ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return nullptr;
+  return static_cast<unsigned *>(ptr);
 }
 
 int sm_count() {
@@ -222,13 +217,13 @@ int la_chunk_fwd(const void *q, const void *k, const void *v, const float *g, co
   }
   int rc = check_mode(mode, g, beta, fn, true);
   if (rc) return rc;
+  if (C == 128) {  // a valid chunk length no kernel of this build implements
+    set_error("%s: chunk length C=128 is not implemented in this build (use 0 or 64)", fn);
+    return LA_ERR_UNSUPPORTED;
+  }
   const int kind = mode & 0xff;
   if ((mode & LA_NONCAUSAL) && (mode & LA_F32)) {
     set_error("%s: LA_NONCAUSAL takes bfloat16 inputs only", fn);
-    return LA_ERR_UNSUPPORTED;
-  }
-  if ((mode & LA_NONCAUSAL) && C != 0 && C != 64) {
-    set_error("%s: chunk length C=%d is not implemented in this build (use 0 or 64)", fn, C);
     return LA_ERR_UNSUPPORTED;
   }
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16)) {

@@ -163,11 +163,12 @@ __global__ void __launch_bounds__(256) scale_rows_kernel(const float *__restrict
     out[base + i] = expf(__ldg(g + (size_t)bh * T * dkk + i / dv)) * S[base + i];
 }
 
-// dg for GLA, per key channel, in two launches. dgc_tile_kernel, one CTA per
-// (b, h, 256-token tile), one thread per channel: the suffix sum over the
+// dg for GLA, per key channel, in three launches. dgc_tile_kernel, one CTA
+// per (b, h, 256-token tile), one thread per channel: the suffix sum over the
 // tile of q[c] dq[c] - k[c] dk[c] (coalesced over the channels), with the
-// tile's totals in `tot`. dgc_carry_kernel, one CTA per (b, h, tile): row
-// sums of dS ⊙ S_final plus the later tiles' totals, added to the tile's tokens.
+// tile's totals in `tot`. dgc_suffix_kernel turns the totals into carries
+// (row sums of dS ⊙ S_final plus the later tiles' totals); dgc_carry_kernel
+// adds them to the tile's tokens.
 template <typename Tin>
 __global__ void __launch_bounds__(128) dgc_tile_kernel(const Tin *__restrict__ q, const Tin *__restrict__ dq,
                                                        const Tin *__restrict__ k, const Tin *__restrict__ dk, int T,
@@ -194,11 +195,12 @@ __global__ void __launch_bounds__(128) dgc_tile_kernel(const Tin *__restrict__ q
   tot[((size_t)bh * gridDim.y + tile) * dkk + c] = acc;
 }
 
-__global__ void __launch_bounds__(128) dgc_carry_kernel(const float *__restrict__ dS, const float *__restrict__ S_final,
-                                                        const float *__restrict__ tot, int ntiles, int T, int dkk,
-                                                        int dv, float *__restrict__ dg) {
-  // one CTA per (b, h, tile): the row sum of dS ⊙ S_final plus the later tiles' totals
-  const int bh = blockIdx.x, tile = blockIdx.y, c = threadIdx.x;
+// One CTA per (b, h), a thread per channel: turns the per-tile totals into
+// per-tile carries in place, tot[tile] <- sum(dS ⊙ S_final)[c] + the totals of
+// the later tiles (a suffix sum, taken once per channel).
+__global__ void __launch_bounds__(128) dgc_suffix_kernel(const float *__restrict__ dS, const float *__restrict__ S_final,
+                                                         float *__restrict__ tot, int ntiles, int dkk, int dv) {
+  const int bh = blockIdx.x, c = threadIdx.x;
   if (c >= dkk) return;
   float carry = 0.f;
   if (dS)
@@ -206,7 +208,20 @@ __global__ void __launch_bounds__(128) dgc_carry_kernel(const float *__restrict_
       const size_t i = ((size_t)bh * dkk + c) * dv + j;
       carry = fmaf(dS[i], S_final[i], carry);
     }
-  for (int tl = ntiles - 1; tl > tile; --tl) carry += tot[((size_t)bh * ntiles + tl) * dkk + c];
+  for (int tl = ntiles - 1; tl >= 0; --tl) {
+    float *t = tot + ((size_t)bh * ntiles + tl) * dkk + c;
+    const float x = *t;
+    *t = carry;
+    carry += x;
+  }
+}
+
+// One CTA per (b, h, tile): adds the tile's carry to its tokens.
+__global__ void __launch_bounds__(128) dgc_carry_kernel(const float *__restrict__ tot, int ntiles, int T, int dkk,
+                                                        float *__restrict__ dg) {
+  const int bh = blockIdx.x, tile = blockIdx.y, c = threadIdx.x;
+  if (c >= dkk) return;
+  const float carry = tot[((size_t)bh * ntiles + tile) * dkk + c];
   const int t0 = tile * 256, t1 = min(t0 + 256, T);
   for (int u0 = t0; u0 < t1; u0 += 8) {  // eight tokens read, then written
     float x[8];
@@ -282,6 +297,10 @@ extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const f
   }
   if (C != 0 && C != 64) {
     set_error("%s: chunk length C=%d is not implemented in this build (use 0 or 64)", fn, C);
+    return LA_ERR_UNSUPPORTED;
+  }
+  if (dg_out && (T + 255) / 256 > 65535) {  // dg's 256-token tiles index the grid's y dimension
+    set_error("%s: dg covers T <= %d tokens (got %d)", fn, 65535 * 256, T);
     return LA_ERR_UNSUPPORTED;
   }
   const void *p16[] = {q, k, v, dO, dq, dkg, dvg};
@@ -377,7 +396,9 @@ extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const f
           static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(dq),
           static_cast<const __nv_bfloat16 *>(k), static_cast<const __nv_bfloat16 *>(dkg), T, dk_, dg_out, tiles);
       if (cudaGetLastError() == cudaSuccess)
-        dgc_carry_kernel<<<grid, 128, 0, s>>>(dS_final, sT, tiles, ntiles, T, dk_, dv_, dg_out);
+        dgc_suffix_kernel<<<(unsigned)BH, 128, 0, s>>>(dS_final, sT, tiles, ntiles, dk_, dv_);
+      if (cudaGetLastError() == cudaSuccess)
+        dgc_carry_kernel<<<grid, 128, 0, s>>>(tiles, ntiles, T, dk_, dg_out);
       if (cudaGetLastError() != cudaSuccess) fail("dg suffix sums");
     } else if (rc == LA_OK) {
       const dim3 grid((unsigned)BH, (unsigned)ntiles);

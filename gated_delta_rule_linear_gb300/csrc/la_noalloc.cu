@@ -3,9 +3,9 @@
 // memory. The kernels are the materialised variant's (la_chunk_mat.cu); only
 // the origin of the workspace differs. Nothing here allocates: the array is
 // part of this translation unit's device image, and its address is looked up
-// once per device.
+// on every call, so that a context that was destroyed and created again (the
+// module then loads anew, possibly elsewhere) never receives a stale address.
 #include <cstddef>
-#include <mutex>
 
 #include "la_internal.h"
 
@@ -17,30 +17,18 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[LA_NOALLOC_SCRA
 namespace la {
 namespace {
 
-constexpr int kMaxDevices = 64;
-void *g_scratch_ptr[kMaxDevices] = {};
-std::mutex g_scratch_mu;
-
-// Device address of the scratch array on the current device, looked up on
-// the first call for that device (which may load this module's image, so
-// that first call belongs before any stream capture).
+// Device address of the scratch array in the current context. The lookup
+// does not synchronise once the module is loaded; the first call on a device
+// may load this module's image, so that first call belongs before any stream
+// capture.
 void *scratch_address(const char *fn) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-    set_error("%s: no usable CUDA device", fn);
+  void *ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress((void **)&ptr, g_noalloc_scratch);
+  if (e != cudaSuccess || !ptr) {
+    set_error("%s: cudaGetSymbolAddress of the static scratch failed: %s", fn, cudaGetErrorString(e));
     return nullptr;
   }
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void *ptr = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress((void **)&ptr, g_noalloc_scratch);
-    if (e != cudaSuccess || !ptr) {
-      set_error("%s: cudaGetSymbolAddress of the static scratch failed: %s", fn, cudaGetErrorString(e));
-      return nullptr;
-    }
-    g_scratch_ptr[dev] = ptr;
-  }
-  return g_scratch_ptr[dev];
+  return ptr;
 }
 
 bool is_aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -67,8 +55,12 @@ extern "C" int la_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
     set_error("%s: dk and dv must be 64 or 128 (got %d, %d)", fn, dk, dv);
     return LA_ERR_UNSUPPORTED;
   }
-  if (C != 0 && C != 64) {
+  if (C != 0 && C != 64 && C != 128) {
     set_error("%s: C must be 0 or 64 (got %d)", fn, C);
+    return LA_ERR_INVALID_ARG;
+  }
+  if (C == 128) {
+    set_error("%s: chunk length C=128 is not implemented in this build (use 0 or 64)", fn);
     return LA_ERR_UNSUPPORTED;
   }
   const int kind = mode & 0xff;

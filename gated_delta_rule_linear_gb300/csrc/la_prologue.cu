@@ -23,6 +23,8 @@
 #include <cuda_bf16.h>
 
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 
 #include "la_internal.h"
 #include "la_sm100.cuh"
@@ -49,6 +51,8 @@ struct ProParams {
   unsigned *status;
   int B, H, T, K, gate_kind, gate_width, l2mask;
   float inv_tau;
+  uint32_t wait_limit;  // polls before a copy is given up (kSpinLimit unless a test shortens it)
+  int skip_k_copy;      // test hook, 0 in normal use: arm k's barrier but start no copy
 };
 
 __host__ __device__ constexpr uint32_t tile_bytes(int d) { return (uint32_t)(kTile + kHalo) * d * 2u; }
@@ -83,6 +87,9 @@ __device__ __forceinline__ void issue_tile(const ProParams &p, int which, int bh
   const int lo = max(t0 - kHalo, 0), hi = min(t0 + kTile, p.T);
   const uint32_t bytes = (uint32_t)(hi - lo) * D * 2u;
   mbar_arrive_expect_tx(bar, bytes);
+  // the test hook leaves k's barrier waiting for bytes that never come (no copy
+  // is in flight when the wait gives up)
+  if (p.skip_k_copy && which == 1) return;
   bulk_load(tile + (size_t)(lo - (t0 - kHalo)) * D * 2, p.x[which] + ((size_t)bh * p.T + lo) * D, bytes, bar);
 }
 
@@ -219,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 2) prologue_kernel(const ProParams p
   bool ok = true;
 #pragma unroll
   for (int i = 0; i < 3; ++i) {
-    if (threadIdx.x == 0 && !mbar_wait_bounded(&bars[i], 0, kSpinLimit)) {
+    if (threadIdx.x == 0 && !mbar_wait_bounded(&bars[i], 0, p.wait_limit)) {
       atomicOr(p.status, kStatusTimeout);
       ok = false;
     }
@@ -340,6 +347,19 @@ extern "C" int la_prologue(const void *xq, const void *xk, const void *xv, const
   p.gate_width = gate_kind == LA_GATE_NONE ? 1 : gate_width;
   p.l2mask = flags;
   p.inv_tau = gate_kind == LA_GATE_NONE ? 1.f : 1.f / tau;
+  p.wait_limit = kSpinLimit;
+  p.skip_k_copy = 0;
+  {
+    // Failure-detection test hook, off unless the environment asks for it:
+    // LA_TEST_FAULT=prologue_wait makes every CTA arm k's copy barrier without
+    // starting the copy and give up after a short bounded wait, so the call
+    // reports LA_ERR_TIMEOUT through la_stream_status without faulting.
+    const char *f = getenv("LA_TEST_FAULT");
+    if (f && strcmp(f, "prologue_wait") == 0) {
+      p.skip_k_copy = 1;
+      p.wait_limit = 4096;
+    }
+  }
   p.status = status_word();
   if (!p.status) {
     set_error("%s: no CUDA device available (%s)", fn, cudaGetErrorString(cudaGetLastError()));

@@ -136,7 +136,10 @@ typedef struct CUstream_st *la_stream_t;
  *   S_final float32 [B][H][dk][W] final state, or NULL to skip writing it
  *           (may alias S0: every head reads its S0 before writing S_final)
  *   B, H, T >= 1; dk, dv in {64, 128}
- *   C       chunk length: 0 (pick per shape), 64 or 128
+ *   C       chunk length: 0 (pick per shape) or 64. C = 128 is a valid
+ *           request that this build does not implement: it returns
+ *           LA_ERR_UNSUPPORTED on the host, before any CUDA call; any other
+ *           value is LA_ERR_INVALID_ARG.
  *   mode    one LA_* mode, optionally | LA_F32
  *
  * S_final of one call passed as S0 of the next continues the sequence
@@ -161,18 +164,26 @@ int la_chunk_fwd(const void *q, const void *k, const void *v, const float *g, co
  * that cannot allocate device memory. The pages have no counterpart to this
  * entry point: it is an interface of this library only.
  *
- *   Arguments, layouts and results as la_chunk_fwd, restricted to the
- *   unit-write modes (not LA_GDN), bfloat16 (no LA_F32) and C = 0 or 64.
- *   Scratch needed: B*H*ceil(T/64)*dk*256 bytes, plus B*H*ceil(T/64)*dk*4
+ *   Arguments, layouts and results as la_chunk_fwd, restricted to the modes
+ *   the materialised variant covers: LA_LINEAR, LA_ELU1_NORM, LA_RETNET,
+ *   LA_GLA and LA_SCALAR_GATE, bfloat16, causal, C = 0 or 64. Rejected on
+ *   the host before any CUDA call: LA_GDN, LA_KDA and LA_OUTER_GATE
+ *   (LA_ERR_UNSUPPORTED), LA_F32 (LA_ERR_UNSUPPORTED), C = 128
+ *   (LA_ERR_UNSUPPORTED), LA_NONCAUSAL or any other flag, an unknown mode, a
+ *   missing or superfluous g, any beta (LA_ERR_INVALID_ARG). Scratch needed: B*H*ceil(T/64)*dk*256 bytes, plus B*H*ceil(T/64)*dk*4
  *   for LA_ELU1_NORM. A call that needs more than LA_NOALLOC_SCRATCH_BYTES
  *   is rejected with LA_ERR_INVALID_ARG before anything is launched.
  *   Allocates nothing: no cudaMalloc, cudaFree or stream-ordered allocation.
  *   The scratch is one array per device, shared by every call on that
  *   device: calls that overlap on the GPU (several streams or host threads)
  *   race on it, so the caller orders them. Nothing in it needs to start at
- *   zero. The first call on each device looks up the array's address (which
- *   may load the module holding it): make that first call before any stream
- *   capture.
+ *   zero. Every call looks up the array's address on the current device
+ *   (the first call on a device may load the module holding it: make that
+ *   first call before any stream capture). The array is device memory held
+ *   for the life of the CUDA context once its module is loaded: with lazy
+ *   module loading (the CUDA default) that is the first la_chunk_fwd_noalloc
+ *   call on the device; with CUDA_MODULE_LOADING=EAGER every process that
+ *   loads libla.so holds the 32 MiB on every device it uses.
  */
 #define LA_NOALLOC_SCRATCH_BYTES 0x2000000  /* 32 MiB */
 int la_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *g,

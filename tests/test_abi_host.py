@@ -71,6 +71,10 @@ def _call(**kw):
     (dict(dk=96), "LA_ERR_UNSUPPORTED"),
     (dict(dv=32), "LA_ERR_UNSUPPORTED"),
     (dict(C=32), "LA_ERR_INVALID_ARG"),
+    (dict(C=128), "LA_ERR_UNSUPPORTED"),              # documented: valid, not implemented
+    (dict(C=128, mode=5), "LA_ERR_UNSUPPORTED"),
+    (dict(C=128, mode=2, g=A), "LA_ERR_UNSUPPORTED"),
+    (dict(C=128, mode=0x100), "LA_ERR_UNSUPPORTED"),
     (dict(mode=9), "LA_ERR_INVALID_ARG"),
     (dict(mode=0x400), "LA_ERR_INVALID_ARG"),          # unknown flag
     (dict(q=A + 8), "LA_ERR_INVALID_ARG"),            # 16-byte alignment
@@ -213,6 +217,8 @@ def _bwd(**kw):
     (dict(mode=3), "LA_ERR_INVALID_ARG"),             # gla needs g
     (dict(mode=3, g=A, dg_out=A + 4), "LA_ERR_INVALID_ARG"),  # dg 16-byte aligned
     (dict(mode=7, g=A), "LA_ERR_UNSUPPORTED"),        # outer-product gate: no backward
+    (dict(mode=4, g=A, dg_out=A, T=65535 * 256 + 1), "LA_ERR_UNSUPPORTED"),  # dg's tile grid
+    (dict(mode=3, g=A, dg_out=A, T=65535 * 256 + 1), "LA_ERR_UNSUPPORTED"),
 ])
 def test_chunk_bwd_rejects_bad_arguments(lib, kw, code):
     rc, msg = _bwd(**kw)

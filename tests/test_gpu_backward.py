@@ -84,13 +84,33 @@ def test_backward_bench_shape_sampled():
 
 # --- the data-dependent scalar decay, with dg ------------------------------------------
 # dg is a suffix sum over up to T tokens of w_u = q_u.dq_u - k_u.dk_u, formed
-# from the dq and dk the passes write in the input dtype. Each element of the
-# bf16 dq and dk carries the passes' bf16 arithmetic: the two MMA operands and
-# the state copy rounded to bf16 (2^-9 each) and the output rounding (2^-9),
-# about 2^-7 of the contributions' size; with a factor 2 of margin,
-#   |dg_tau - ref_tau| <= 2^-6 * sum_{u>=tau} sum_c (|q_u,c dq_u,c| + |k_u,c dk_u,c|) + 1e-5.
-# The terms of w cancel, so a relative bound on dg itself would not follow
-# from the arithmetic. float32 inputs: the library's float32 tolerance.
+# from the dq and dk the passes write. Expanding dq and dk fully, each element
+# is a sum of elementary products (for the scalar decay, e.g. dq_t[c] =
+# sum_j a(t) S0[c,j] dO_t[j] + sum_{s<=t} sum_j a(t,s) dO_t[j] v_s[j] k_s[c]).
+# Every rounding on a product's way through the chunk passes perturbs it by at
+# most one unit roundoff u relative to its own size: in bf16 the decayed
+# operand copy, the intermediate score or state tile and the bf16 MMA operand
+# (2^-9 each) and the output rounding (2^-9), at most four, so 4u = 2^-7;
+# in float32 (LA_F32) up to eight float32 roundings, 8 * 2^-24 = 2^-21. So
+# with M_dq, M_dk the same sums taken over the products' absolute values (the
+# oracle's backward evaluated on |q|, |k|, |v|, |dO|, |S0|, |dS| with the
+# same, positive, decay factors):
+#   |dg_tau - ref_tau| <= eps * sum_{u>=tau} sum_c (|q_u,c| M_dq(u,c) + |k_u,c| M_dk(u,c)) + 1e-6,
+# eps = 2^-7 for bf16 and 2^-21 for float32. Cancellation inside w or inside
+# dq and dk cannot break it, since M bounds every intermediate's size; a
+# relative bound on dg itself would not follow from the arithmetic.
+
+def _dg_bound(q, k, v, dO, g, S0, dS, eps, backward_fn):
+    """Suffix sums of eps * (|q| M_dq + |k| M_dk) along the token axis (axis 2),
+    per token for the scalar decay and per channel for GLA."""
+    a = np.abs
+    M = backward_fn(a(q), a(k), a(v), a(dO), g, S0=None if S0 is None else a(S0),
+                    dS=None if dS is None else a(dS))
+    mag = a(q) * M[0] + a(k) * M[1]
+    if M[4].ndim == 3:                         # scalar decay: one gate per token
+        mag = mag.sum(-1)
+    return eps * np.flip(np.cumsum(np.flip(mag, 2), 2), 2) + 1e-6
+
 
 def _scalar_case(dtype, B, H, T, dk, dv, seed=0):
     from workloads import WORKLOADS
@@ -102,14 +122,12 @@ def _scalar_case(dtype, B, H, T, dk, dv, seed=0):
     return inp["q"], inp["k"], inp["v"], inp["g"], dO, inp["S0"], dS
 
 
-def _check_dg(got, ref, dtype, what, q, k):
-    """ref = backward_scalar's outputs; q, k the float64 inputs."""
+def _check_dg(got, ref, dtype, what, q, k, v, dO, g, S0, dS):
+    """ref = backward_scalar's outputs; the rest the float64 inputs."""
+    assert np.all(np.isfinite(got)), what
     if dtype == "f32":
         assert_close(got, ref[4], dtype, what)
-        return
-    assert np.all(np.isfinite(got)), what
-    mag = np.sum(np.abs(q * ref[0]) + np.abs(k * ref[1]), axis=-1)        # [B, H, T]
-    bound = 2.0 ** -6 * np.cumsum(mag[..., ::-1], axis=-1)[..., ::-1] + 1e-5
+    bound = _dg_bound(q, k, v, dO, g, S0, dS, 2.0 ** -7 if dtype == "bf16" else 2.0 ** -21, backward_scalar)
     bad = np.abs(got - ref[4]) > bound
     assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} outside the rounding bound"
 
@@ -124,7 +142,8 @@ def test_scalar_backward_parity(dtype, dims, T):
     ref = backward_scalar(f64(q), f64(k), f64(v), f64(dO), f64(g), S0=f64(S0), dS=f64(dS))
     for name, got, r in (("dq", dq, ref[0]), ("dk", dk_, ref[1]), ("dv", dv_, ref[2]), ("dS0", dS0, ref[3])):
         assert_close(f64(got), r, dtype, f"scalar {dtype} T={T} {name}")
-    _check_dg(f64(dg), ref, dtype, f"scalar {dtype} T={T} dg", f64(q), f64(k))
+    _check_dg(f64(dg), ref, dtype, f"scalar {dtype} T={T} dg", f64(q), f64(k), f64(v), f64(dO), f64(g),
+              f64(S0), f64(dS))
 
 
 def test_scalar_backward_without_states_or_dS():
@@ -133,7 +152,7 @@ def test_scalar_backward_without_states_or_dS():
     ref = backward_scalar(f64(q), f64(k), f64(v), f64(dO), f64(g))
     for name, got, r in (("dq", dq, ref[0]), ("dk", dk_, ref[1]), ("dv", dv_, ref[2]), ("dS0", dS0, ref[3])):
         assert_close(f64(got), r, "bf16", f"scalar {name}")
-    _check_dg(f64(dg), ref, "bf16", "scalar dg", f64(q), f64(k))
+    _check_dg(f64(dg), ref, "bf16", "scalar dg", f64(q), f64(k), f64(v), f64(dO), f64(g), None, None)
 
 
 # --- GLA's per-channel decay, with the per-channel dg ------------------------------------
@@ -152,18 +171,20 @@ def _gla_case(B, H, T, dk, dv, seed=0):
     return inp["q"], inp["k"], inp["v"], inp["g"], dO, S0, dS
 
 
-def _check_dgc(got, ref, what, q, k, v, g, S0, dS):
-    """Besides the rounding of dq and dk, dg carries the final-state term
-    sum_j dS[c, j] S_final[c, j] with S_final from the bf16 forward kernel
-    (held to 2^-6 of sum_j |dS S_final|, the forward state's bf16 operand
-    rounding with margin)."""
+def _check_dgc(got, ref, what, q, k, v, dO, g, S0, dS):
+    """The bound of the scalar decay, channel by channel (eps = 2^-7), plus the
+    final-state term sum_j dS[c, j] S_final[c, j], whose S_final comes from the
+    bf16 forward kernel: held to eps * sum_j |dS| S_abs, S_abs the final state
+    of the same recurrence on the absolute values (a bound on every product
+    that forms S_final)."""
     from oracle import recurrence
     assert np.all(np.isfinite(got)), what
-    mag = np.abs(q * ref[0]) + np.abs(k * ref[1])                         # [B, H, T, dk]
-    bound = 2.0 ** -6 * np.cumsum(mag[:, :, ::-1], axis=2)[:, :, ::-1] + 1e-5
+    eps = 2.0 ** -7
+    bound = _dg_bound(q, k, v, dO, g, S0, dS, eps, backward_gla)
     if dS is not None:
-        _, S_T = recurrence(q, k, v, "gla", g=g, S0=S0)
-        bound = bound + 2.0 ** -6 * np.sum(np.abs(dS * S_T), axis=-1)[:, :, None, :]
+        a = np.abs
+        _, S_abs = recurrence(a(q), a(k), a(v), "gla", g=g, S0=None if S0 is None else a(S0))
+        bound = bound + eps * np.sum(a(dS) * S_abs, axis=-1)[:, :, None, :]
     bad = np.abs(got - ref[4]) > bound
     assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} outside the rounding bound"
 
@@ -177,7 +198,7 @@ def test_gla_backward_parity(dims, T):
     ref = backward_gla(f64(q), f64(k), f64(v), f64(dO), f64(g), S0=f64(S0), dS=f64(dS))
     for name, got, r in (("dq", dq, ref[0]), ("dk", dk_, ref[1]), ("dv", dv_, ref[2]), ("dS0", dS0, ref[3])):
         assert_close(f64(got), r, "bf16", f"gla T={T} {name}")
-    _check_dgc(f64(dg), ref, f"gla T={T} dg", f64(q), f64(k), f64(v), f64(g), f64(S0), f64(dS))
+    _check_dgc(f64(dg), ref, f"gla T={T} dg", f64(q), f64(k), f64(v), f64(dO), f64(g), f64(S0), f64(dS))
 
 
 def test_gla_backward_without_states_or_dS():
@@ -186,4 +207,4 @@ def test_gla_backward_without_states_or_dS():
     ref = backward_gla(f64(q), f64(k), f64(v), f64(dO), f64(g))
     for name, got, r in (("dq", dq, ref[0]), ("dk", dk_, ref[1]), ("dv", dv_, ref[2]), ("dS0", dS0, ref[3])):
         assert_close(f64(got), r, "bf16", f"gla {name}")
-    _check_dgc(f64(dg), ref, "gla dg", f64(q), f64(k), f64(v), f64(g), None, None)
+    _check_dgc(f64(dg), ref, "gla dg", f64(q), f64(k), f64(v), f64(dO), f64(g), None, None)

@@ -41,9 +41,17 @@ def test_scratch_limit_is_exact(lib):
 
 
 @pytest.mark.parametrize("kw,code", [
+    # every rejection the header lists
     (dict(mode=la.LA_GDN), "LA_ERR_UNSUPPORTED"),
+    (dict(mode=la.LA_KDA, g=A), "LA_ERR_UNSUPPORTED"),
+    (dict(mode=la.LA_OUTER_GATE, g=A, beta=A), "LA_ERR_UNSUPPORTED"),
     (dict(mode=la.LA_LINEAR | la.LA_F32), "LA_ERR_UNSUPPORTED"),
     (dict(C=128), "LA_ERR_UNSUPPORTED"),
+    (dict(C=32), "LA_ERR_INVALID_ARG"),
+    (dict(mode=la.LA_LINEAR | la.LA_NONCAUSAL), "LA_ERR_INVALID_ARG"),
+    (dict(mode=9), "LA_ERR_INVALID_ARG"),
+    (dict(mode=la.LA_LINEAR, g=A), "LA_ERR_INVALID_ARG"),      # superfluous g
+    (dict(mode=la.LA_GLA, g=A, beta=A), "LA_ERR_INVALID_ARG"),  # any beta
     (dict(mode=la.LA_RETNET), "LA_ERR_INVALID_ARG"),         # missing g
     (dict(q=None), "LA_ERR_INVALID_ARG"),
     (dict(o=A + 2), "LA_ERR_INVALID_ARG"),
@@ -70,17 +78,29 @@ def test_noalloc_matches_materialised_entry_point_on_two_calls(lib, mode, monkey
     stream = torch.cuda.current_stream()
     # two different problems in a row; the second also runs at the scratch limit (dk = 128)
     shapes = [(1, 2, 300, 11), (1, 8, 8192, 12) if mode != "elu1" else (2, 4, 4000, 12)]
+    # references (la_chunk_fwd's materialised variant, workspace from the library's
+    # pool) and output buffers first, so that nothing but the two no-alloc calls
+    # runs between the device-memory readings below
+    cases = []
     for B, H, T, seed in shapes:
         wl, d = _inputs(mode, B, H, T, seed)
-        mode_id = la.MODE_IDS[wl.mode]
         monkeypatch.setenv("LA_VARIANT", "mat")
         o_ref, S_ref = la.chunk_fwd(d["q"], d["k"], d["v"], wl.mode, g=d["g"], S0=d["S0"])
         monkeypatch.delenv("LA_VARIANT")
         o = torch.full_like(o_ref, float("nan"))
         S = torch.full_like(S_ref, float("nan"))
+        cases.append((B, H, T, wl, d, o_ref, S_ref, o, S))
+    torch.cuda.synchronize()
+    free = []
+    for B, H, T, wl, d, o_ref, S_ref, o, S in cases:
         rc = la.la_chunk_fwd_noalloc(d["q"], d["k"], d["v"], d["g"], None, o, d["S0"], S,
-                                     B, H, T, wl.dk, wl.dv, 0, mode_id, stream.cuda_stream)
+                                     B, H, T, wl.dk, wl.dv, 0, la.MODE_IDS[wl.mode], stream.cuda_stream)
         assert rc == 0, la.la_last_error()
         assert la.la_stream_status(stream.cuda_stream) == 0, la.la_last_error()
+        free.append(torch.cuda.mem_get_info()[0])
+    for B, H, T, wl, d, o_ref, S_ref, o, S in cases:
         assert torch.equal(o, o_ref), f"{mode} T={T}: o differs from la_chunk_fwd (materialised)"
         assert torch.equal(S, S_ref), f"{mode} T={T}: S_final differs from la_chunk_fwd (materialised)"
+    # the first call may load the module that holds the static array; the second,
+    # larger call must not take any device memory
+    assert free[1] == free[0], f"device memory changed by {free[0] - free[1]} bytes across a no-alloc call"
