@@ -67,7 +67,7 @@ def uses_materialised(wl, variant=None, sm_count=152) -> bool:
     """Whether la_chunk_fwd runs the materialised variant for this workload
     (the library's per-shape rule, or a forced LA_VARIANT)."""
     if variant is not None:
-        return variant == "mat"
+        return variant == "mat" and wl.mode not in ("gdn", "kda", "outer")
     return (wl.dtype == "bf16" and wl.mode not in ("gdn", "kda", "outer") and wl.T >= 512
             and 2 * wl.B * wl.H <= sm_count)
 
@@ -88,8 +88,11 @@ def kernel_name(wl, variant=None, sm_count=152) -> str:
         return "chunk_tc_kernel"
     if wl.mode == "gdn":
         if wl.dk == 128 and wl.dv == 128:
-            pair = os.environ.get("LA_DELTA", "pair" if 2 * wl.B * wl.H <= sm_count else "single")
-            return "chunk_delta_pair_kernel" if pair == "pair" else "chunk_delta_kernel"
+            path = os.environ.get("LA_DELTA", "pair" if 2 * wl.B * wl.H <= sm_count else "single")
+            if variant == "mat":
+                path = "wy"
+            return {"pair": "chunk_delta_pair_kernel", "single": "chunk_delta_kernel"}.get(
+                path, "wy_kernel+chain_kernel")
         return "chunk_tc_kernel"
     return "chunk_ws_kernel"
 

@@ -112,9 +112,21 @@ int select_variant(const ChunkParams &p, int *chunk_out) {
     set_error("la_chunk_fwd: LA_OUTER_GATE runs on the pipelined tensor-core kernel only");
     return -1;
   }
-  if (want == kVariantMat && p.kind == kGdn) {
-    set_error("la_chunk_fwd: the materialised variant covers the unit-write modes only");
-    return -1;
+  if (p.kind == kGdn) {
+    // the delta rule: the fused kernels (a CTA pair per head while 2*B*H fits the GPU,
+    // else one CTA per head; la_chunk_tc.cu), measured faster on GB300 than the
+    // two-phase path (the solve for every chunk in parallel into T' images, then the
+    // state chain on a CTA pair: dk = dv = 128), which LA_DELTA=wy or LA_VARIANT=mat
+    // selects
+    const bool big = p.dk == 128 && p.dv == 128;
+    const char *d = getenv("LA_DELTA");
+    const bool two_phase = (d && strcmp(d, "wy") == 0) || want == kVariantMat;
+    if (two_phase && !big) {
+      set_error("la_chunk_fwd: the two-phase delta-rule path takes dk = dv = 128");
+      return -1;
+    }
+    if (want == kVariantSimt) return kVariantSimt;
+    return two_phase ? kVariantDeltaWy : kVariantTc;
   }
   if (want >= 0) return want;
   const long long BH = (long long)p.B * p.H;
@@ -290,6 +302,28 @@ int la_chunk_fwd(const void *q, const void *k, const void *v, const float *g, co
       return LA_ERR_CUDA;
     }
     rc = launch_chunk_mat(p, ws, s);
+    e = cudaFreeAsync(ws, s);
+    if (rc == LA_OK && e != cudaSuccess) {
+      set_error("%s: workspace release failed: %s", fn, cudaGetErrorString(e));
+      return LA_ERR_CUDA;
+    }
+    return rc;
+  }
+  if (variant == kVariantDeltaWy) {
+    // stream-ordered workspace for the T' images, from the library's pool
+    void *ws = nullptr;
+    const size_t bytes = delta_wy_workspace_bytes(p);
+    cudaMemPool_t pool = workspace_pool();
+    if (!pool) {
+      set_error("%s: could not create the workspace pool: %s", fn, cudaGetErrorString(cudaGetLastError()));
+      return LA_ERR_CUDA;
+    }
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes, pool, s);
+    if (e != cudaSuccess) {
+      set_error("%s: workspace allocation of %zu bytes failed: %s", fn, bytes, cudaGetErrorString(e));
+      return LA_ERR_CUDA;
+    }
+    rc = launch_chunk_delta_wy(p, ws, s);
     e = cudaFreeAsync(ws, s);
     if (rc == LA_OK && e != cudaSuccess) {
       set_error("%s: workspace release failed: %s", fn, cudaGetErrorString(e));

@@ -308,6 +308,7 @@ chunk_delta_pair_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap
       constexpr uint32_t id_d1 = idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t id_w = idesc_bf16_f32(128, 64, false, false);
       const uint32_t a_tpp = smem_u32(sm + L.af), a_qk = smem_u32(sm + L.kt);
+      const uint64_t d_qk = desc_sw128(a_qk, 16, 1024), d_tpp = desc_sw128(a_tpp, 16, 1024);
       // D1 = [Q; K] K^T of own chunk n once the key group has read the previous one
       auto issue_d1 = [&](int n) -> bool {
         if (!wait_or_abort(kt_full, n & 1, abort_flag, p.status)) return false;
@@ -316,8 +317,7 @@ chunk_delta_pair_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap
 #pragma unroll
         for (int kk = 0; kk < DK / 16; ++kk) {
           const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16(tbase + kColD1, desc_sw128(a_qk + ko, 16, 1024), desc_sw128(a_qk + ko + 8192, 16, 1024),
-                   id_d1, kk > 0);
+          mma_bf16(tbase + kColD1, desc_add(d_qk, ko), desc_add(d_qk, ko + 8192), id_d1, kk > 0);
         }
         mma_commit(d1_full);
         return true;
@@ -332,7 +332,7 @@ chunk_delta_pair_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)
-          mma_bf16_ts(tbase + kColW, tbase + kColKT + kk * 8, desc_sw128(a_tpp + kk * 32, 16, 1024), id_w, kk > 0);
+          mma_bf16_ts(tbase + kColW, tbase + kColKT + kk * 8, desc_add(d_tpp, kk * 32), id_w, kk > 0);
         mma_commit(w_full);
       }
       mma_commit(&drain[0]);
@@ -356,14 +356,17 @@ chunk_delta_pair_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap
         const uint32_t a_v = smem_u32(st + L.v), a_qk = smem_u32(st + L.qk);
         const uint32_t a_tp = smem_u32(tpbuf(b)), a_wn = smem_u32(wnbuf(b)), a_p = smem_u32(pbuf(b));
         const uint32_t d_o = tbase + kColO;
+        // base descriptors of this chunk's operands (constant offsets per K step below)
+        const uint64_t dv = desc_sw128(a_v, a_zero - a_v, 1024), dtp = desc_sw128(a_tp, 16, 1024),
+                       dwn = desc_sw128(a_wn, 8192, 1024), dqk = desc_sw128(a_qk, 16, 1024),
+                       dp = desc_sw128(a_p, 16, 1024), dkmn = desc_sw128(a_qk + 8192, 16384, 1024);
         // V^T (value rows 64..127 from the zero atom: LBO spans the two MN blocks)
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)
-          mma_bf16(tbase + kColU, desc_sw128(a_v + kk * 2048, a_zero - a_v, 1024),
-                   desc_sw128(a_tp + kk * 32, 16, 1024), id_ut, kk > 0);
+          mma_bf16(tbase + kColU, desc_add(dv, kk * 2048), desc_add(dtp, kk * 32), id_ut, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < DK / 16; ++kk)
-          mma_bf16_ts(tbase + kColU, tbase + kColSC + kk * 8, desc_sw128(a_wn + kk * 2048, 8192, 1024), id_us, 1);
+          mma_bf16_ts(tbase + kColU, tbase + kColSC + kk * 8, desc_add(dwn, kk * 2048), id_us, 1);
         mma_commit(u_full);
         // O is single-buffered: the previous chunk's output epilogue runs during this U
         if (i > 0 && !wait_or_abort(o_free, (i - 1) & 1, abort_flag, p.status)) break;
@@ -371,18 +374,18 @@ chunk_delta_pair_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap
 #pragma unroll
         for (int kk = 0; kk < DK / 16; ++kk) {
           const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ts(d_o, tbase + kColSC + kk * 8, desc_sw128(a_qk + ko, 16, 1024), id_o1, kk > 0);
+          mma_bf16_ts(d_o, tbase + kColSC + kk * 8, desc_add(dqk, ko), id_o1, kk > 0);
         }
         if (!wait_or_abort(u_ready, i & 1, abort_flag, p.status)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)
-          mma_bf16_ts(d_o, tbase + kColU + kk * 8, desc_sw128(a_p + kk * 32, 16, 1024), id_o2, 1);
+          mma_bf16_ts(d_o, tbase + kColU + kk * 8, desc_add(dp, kk * 32), id_o2, 1);
         // S^T += (U^T Diag(e^{b_last - b})) K: the decay to the chunk end rides on U, so K stays unscaled
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)
           mma_bf16_ts(tbase + kColS, tbase + kColU + 32 + kk * 8,
-                      desc_sw128(a_qk + 8192 + kk * 2048, 16384, 1024), id_su, 1);
+                      desc_add(dkmn, kk * 2048), id_su, 1);
         mma_commit(s_done);
         mma_commit(o_done);
         mma_commit(&empty[s]);

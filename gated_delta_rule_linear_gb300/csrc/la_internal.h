@@ -77,8 +77,14 @@ int launch_chunk_mat(const ChunkParams &p, void *workspace, cudaStream_t stream)
 size_t nc_workspace_bytes(const ChunkParams &p);
 int launch_chunk_noncausal(const ChunkParams &p, void *workspace, cudaStream_t stream);
 
+// Gated delta rule (dk = dv = 128, bf16) in two kernels: the triangular solve for
+// every (head, chunk) into a workspace of delta_wy_workspace_bytes(p) bytes (one
+// bf16 T' image per chunk), then the state chain on a CTA pair per head.
+size_t delta_wy_workspace_bytes(const ChunkParams &p);
+int launch_chunk_delta_wy(const ChunkParams &p, void *workspace, cudaStream_t stream);
+
 // Which chunk-forward kernel a shape goes to (host-side selection).
-enum Variant : int { kVariantSimt = 0, kVariantTc = 1, kVariantMat = 2 };
+enum Variant : int { kVariantSimt = 0, kVariantTc = 1, kVariantMat = 2, kVariantDeltaWy = 3 };
 int select_variant(const ChunkParams &p, int *chunk_out);
 
 }  // namespace la

@@ -169,6 +169,15 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float *v) {
 }
 
 
+// 32 lanes x 32 bits, 8 consecutive columns per thread.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float *v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+               "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+               "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+               : "memory");
+}
+
 // 32 lanes x 32 bits, 32 consecutive columns per thread.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
   uint32_t r[32];
@@ -245,6 +254,13 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uin
   d |= (uint64_t)2u << 61;   // 128-byte swizzle
   return d;
 }
+
+// A descriptor advanced by `bytes` along its operand: the address field is bits 0..13
+// in 16-byte units and shared-memory operands stay below 256 KB, so the sum never
+// carries out of the field. Issuing threads compute a base descriptor once and add
+// constant offsets per K step: a full desc_sw128 per MMA is a serial chain of integer
+// operations that otherwise sets the issue rate of the MMAs.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
 
 // Instruction descriptor, kind::f16 with bf16 A/B and an fp32 accumulator.
 // a_mn / b_mn select MN-major (transposed) operands.

@@ -34,7 +34,7 @@ def _check(inp, what):
     assert_close(f64(S), S_ref, "bf16", f"{what} S")
 
 
-@pytest.mark.parametrize("path", ["single", "pair"])
+@pytest.mark.parametrize("path", ["single", "pair", "wy"])
 @pytest.mark.parametrize("beta", [0.0, 1.0])
 def test_delta_rule_with_no_write_and_full_overwrite(path, beta, monkeypatch):
     """beta = 0: the state only decays (o = alpha-decayed S0^T q); beta = 1: each

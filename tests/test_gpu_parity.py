@@ -209,9 +209,10 @@ def test_full_size_workload_sampled_heads(name):
     assert torch.isfinite(o.float()).all()
 
 
-# --- delta rule: one CTA per head, or a CTA pair per head ---------------------
+# --- delta rule: one CTA per head, a CTA pair per head, or the two-phase path
+# (the solve for every chunk first, then the state chain on a CTA pair) -------
 
-@pytest.mark.parametrize("path", ["single", "pair"])
+@pytest.mark.parametrize("path", ["single", "pair", "wy"])
 @pytest.mark.parametrize("T", [1, 64, 65, 200, 1000])
 @pytest.mark.parametrize("gated", [True, False])
 def test_delta_kernel_paths(path, T, gated, monkeypatch):
@@ -225,7 +226,7 @@ def test_delta_kernel_paths(path, T, gated, monkeypatch):
     assert_close(f64(S), S_ref, "bf16", f"{path} T={T} S")
 
 
-@pytest.mark.parametrize("path", ["single", "pair"])
+@pytest.mark.parametrize("path", ["single", "pair", "wy"])
 def test_delta_kernel_paths_aliased_state_and_split(path, monkeypatch):
     monkeypatch.setenv("LA_DELTA", path)
     inp = _inputs("gdn", "bf16", B=1, H=2, T=300)
@@ -242,7 +243,7 @@ def test_delta_pair_and_single_agree():
     inp = _inputs("gdn", "bf16", B=2, H=4, T=777)
     import os
     outs = []
-    for path in ("single", "pair"):
+    for path in ("single", "pair", "wy"):
         os.environ["LA_DELTA"] = path
         try:
             outs.append(run_cuda(inp))
@@ -250,3 +251,5 @@ def test_delta_pair_and_single_agree():
             del os.environ["LA_DELTA"]
     assert_close(f64(outs[1][0]), f64(outs[0][0]), "bf16", "pair vs single o")
     assert_close(f64(outs[1][1]), f64(outs[0][1]), "bf16", "pair vs single S")
+    assert_close(f64(outs[2][0]), f64(outs[0][0]), "bf16", "two-phase vs single o")
+    assert_close(f64(outs[2][1]), f64(outs[0][1]), "bf16", "two-phase vs single S")
