@@ -68,8 +68,9 @@ def uses_materialised(wl, variant=None, sm_count=152) -> bool:
     (the library's per-shape rule, or a forced LA_VARIANT)."""
     if variant is not None:
         return variant == "mat" and wl.mode not in ("gdn", "kda", "outer")
-    return (wl.dtype == "bf16" and wl.mode not in ("gdn", "kda", "outer") and wl.T >= 512
-            and 2 * wl.B * wl.H <= sm_count)
+    bh = wl.B * wl.H
+    small = 4 * bh <= sm_count if wl.mode == "gla" else 2 * bh <= sm_count
+    return wl.dtype == "bf16" and wl.mode not in ("gdn", "kda", "outer") and wl.T >= 512 and small
 
 
 def is_noncausal(wl) -> bool:

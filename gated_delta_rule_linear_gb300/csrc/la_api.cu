@@ -129,8 +129,16 @@ int select_variant(const ChunkParams &p, int *chunk_out) {
     return two_phase ? kVariantDeltaWy : kVariantTc;
   }
   if (want >= 0) return want;
-  const long long BH = (long long)p.B * p.H;
-  if (p.kind != kGdn && p.kind != kOuter && p.T >= 8 * 64 && 2 * BH <= sm_count()) return kVariantMat;
+  // Materialised when its DRAM time stays below the fused kernel's serial time:
+  // the fused kernel takes ~T/64 chunk periods whatever B*H (up to one CTA per SM);
+  // the materialised one moves ~2.4x the bytes (GLA ~3.5 KB per token-head, the
+  // others ~2.5 KB, measured by ncu) through a fully parallel output pass. The
+  // measured crossover lies between B*H = 64 and 128 for RetNet, the scalar decay
+  // and elu+1 (SMs / 2), and below 64 for GLA, whose fused chunk is the longest and
+  // whose materialised pass moves the most (SMs / 4).
+  const long long BH = (long long)p.B * p.H, sms = sm_count();
+  const bool small = p.kind == kGla ? 4 * BH <= sms : 2 * BH <= sms;
+  if (p.kind != kGdn && p.kind != kOuter && p.T >= 8 * 64 && small) return kVariantMat;
   return kVariantTc;
 }
 

@@ -36,8 +36,9 @@
  *     LA_ELU1_NORM where W = dv + 1 and column dv holds the normaliser z.
  *   - All pointers are DEVICE pointers owned by the caller. The library never
  *     frees or retains them. Device memory of its own is taken only by the
- *     materialised variant and the non-causal form of la_chunk_fwd and by
- *     la_chunk_bwd: workspaces allocated and freed on `stream` from a
+ *     materialised variant, the two-phase delta-rule variant and the
+ *     non-causal form of la_chunk_fwd and by la_chunk_bwd: workspaces
+ *     allocated and freed on `stream` from a
  *     library-owned stream-ordered pool (one per device) that keeps freed
  *     memory for the next call.
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream);
@@ -151,8 +152,13 @@ typedef struct CUstream_st *la_stream_t;
  * serial pass writes every chunk's incoming state to a workspace of
  * B*H*ceil(T/64)*dk*256 bytes (plus B*H*ceil(T/64)*dk*4 for LA_ELU1_NORM),
  * then all chunks' outputs are computed in parallel; it wins when B*H is too
- * small to fill the GPU. The choice is made per shape; the environment
- * variable LA_VARIANT = tc (or nonmat) | mat | simt forces one.
+ * small to fill the GPU. The choice is made per shape: materialised for the
+ * unit-write modes when T >= 512 and B*H <= SMs / 2 (GLA: SMs / 4), fused
+ * otherwise. Gated DeltaNet runs fused by default; its two-phase variant (the
+ * triangular solve of every chunk first, written as one 8 KB image per chunk of
+ * 64 tokens to a workspace of B*H*ceil(T/64)*8192 bytes, then the state chain,
+ * dk = dv = 128) is selected by LA_DELTA=wy. The environment variable
+ * LA_VARIANT = tc (or nonmat) | mat | simt forces a variant.
  */
 int la_chunk_fwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
                  void *o, const float *S0, float *S_final,
