@@ -68,9 +68,19 @@ def uses_materialised(wl, variant=None, sm_count=152) -> bool:
     (the library's per-shape rule, or a forced LA_VARIANT)."""
     if variant is not None:
         return variant == "mat" and wl.mode not in ("gdn", "kda", "outer")
+    if wl.C == 128:
+        return True
     bh = wl.B * wl.H
-    small = 4 * bh <= sm_count if wl.mode == "gla" else 2 * bh <= sm_count
+    small = 4 * bh <= sm_count if wl.mode == "gla" else True if wl.mode == "elu1" else 2 * bh <= sm_count
     return wl.dtype == "bf16" and wl.mode not in ("gdn", "kda", "outer") and wl.T >= 512 and small
+
+
+def mat_chunk(wl) -> int:
+    """The chunk length the materialised variant runs for this workload
+    (the library's rule for C = 0, else the workload's C)."""
+    if wl.C:
+        return wl.C
+    return 128 if wl.mode != "gla" and (wl.mode in ("linear", "elu1") or wl.T >= 2048) else 64
 
 
 def is_noncausal(wl) -> bool:
@@ -82,7 +92,7 @@ def kernel_name(wl, variant=None, sm_count=152) -> str:
     if is_noncausal(wl):
         return "nc_sum_kernel+nc_finalize_kernel+nc_out_kernel"
     if uses_materialised(wl, variant, sm_count):
-        return "chunk_state_kernel+chunk_output_kernel"
+        return "chunk_state_kernel+" + ("chunk_output128_kernel" if mat_chunk(wl) == 128 else "chunk_output_kernel")
     if wl.dtype == "f32" or variant == "simt":
         return "chunk_simt_kernel"
     if wl.mode == "kda":
@@ -297,6 +307,8 @@ def main():
     ap.add_argument("--B", type=int, default=None, help="override batch (profiling of a smaller case)")
     ap.add_argument("--H", type=int, default=None)
     ap.add_argument("--T", type=int, default=None)
+    ap.add_argument("--chunk", type=int, default=None, choices=[0, 64, 128],
+                    help="override the workload's chunk length C (0: the library's per-shape choice)")
     ap.add_argument("--variant", default=None, choices=["tc", "nonmat", "mat", "simt"],
                     help="force a kernel variant (default: the library's per-shape choice)")
     args = ap.parse_args()
@@ -318,6 +330,8 @@ def main():
         return bench_gdelta(args, rank, world, local_rank)
     wl = workloads.WORKLOADS[args.workload]
     over = {k: getattr(args, k) for k in ("B", "H", "T") if getattr(args, k) is not None}
+    if args.chunk is not None:
+        over["C"] = args.chunk
     if over:
         wl = wl.with_sizes(**over)
 

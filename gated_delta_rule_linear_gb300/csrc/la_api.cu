@@ -90,12 +90,15 @@ int select_variant(const ChunkParams &p, int *chunk_out) {
   if (env && (strcmp(env, "tc") == 0 || strcmp(env, "nonmat") == 0)) want = kVariantTc;
   if (env && strcmp(env, "mat") == 0) want = kVariantMat;
   if (env && strcmp(env, "simt") == 0) want = kVariantSimt;
-  const int C = p.C == 0 ? 64 : p.C;
-  if (C != 64) {
-    set_error("la_chunk_fwd: chunk length C=%d is not implemented in this build (use 0 or 64)", p.C);
-    return -1;
+  if (p.C == 128) {  // the 128-token output pass of the materialised variant (modes checked by the caller)
+    if (want == kVariantTc || want == kVariantSimt) {
+      set_error("la_chunk_fwd: C=128 runs on the materialised variant only");
+      return -1;
+    }
+    *chunk_out = 128;
+    return kVariantMat;
   }
-  *chunk_out = C;
+  *chunk_out = 64;
   if (p.f32 && (p.kind == kKda || p.kind == kOuter)) {
     set_error("la_chunk_fwd: LA_KDA and LA_OUTER_GATE take bfloat16 inputs only");
     return -1;
@@ -131,14 +134,24 @@ int select_variant(const ChunkParams &p, int *chunk_out) {
   if (want >= 0) return want;
   // Materialised when its DRAM time stays below the fused kernel's serial time:
   // the fused kernel takes ~T/64 chunk periods whatever B*H (up to one CTA per SM);
-  // the materialised one moves ~2.4x the bytes (GLA ~3.5 KB per token-head, the
-  // others ~2.5 KB, measured by ncu) through a fully parallel output pass. The
-  // measured crossover lies between B*H = 64 and 128 for RetNet, the scalar decay
-  // and elu+1 (SMs / 2), and below 64 for GLA, whose fused chunk is the longest and
-  // whose materialised pass moves the most (SMs / 4).
+  // the materialised one moves ~2.4x the bytes at C = 64 (GLA ~3.5 KB per
+  // token-head, the others ~2.5 KB, measured by ncu) through a fully parallel
+  // output pass. The measured crossover lies between B*H = 64 and 128 for RetNet,
+  // the scalar decay and plain linear attention (SMs / 2), and below 64 for GLA,
+  // whose fused chunk is the longest and whose materialised pass moves the most
+  // (SMs / 4). elu+1's fused chunk is slow (~5 us) and its materialised pass at
+  // C = 128 was faster at every B*H measured (up to 256): materialised from 8
+  // chunks on.
+  // Chunk length of the materialised pass: 128 (one state image per 128 tokens,
+  // ~20% fewer DRAM bytes, measured faster or equal) for the modes without
+  // per-channel gates, except RetNet and the scalar decay below 2048 tokens where
+  // the two measured within a few percent either way; 64 for GLA.
   const long long BH = (long long)p.B * p.H, sms = sm_count();
-  const bool small = p.kind == kGla ? 4 * BH <= sms : 2 * BH <= sms;
-  if (p.kind != kGdn && p.kind != kOuter && p.T >= 8 * 64 && small) return kVariantMat;
+  const bool small = p.kind == kGla ? 4 * BH <= sms : p.kind == kElu1 ? true : 2 * BH <= sms;
+  if (p.kind != kGdn && p.kind != kOuter && p.T >= 8 * 64 && small) {
+    if (p.C == 0 && p.kind != kGla && (p.kind == kLinear || p.kind == kElu1 || p.T >= 2048)) *chunk_out = 128;
+    return kVariantMat;
+  }
   return kVariantTc;
 }
 
@@ -237,11 +250,12 @@ int la_chunk_fwd(const void *q, const void *k, const void *v, const float *g, co
   }
   int rc = check_mode(mode, g, beta, fn, true);
   if (rc) return rc;
-  if (C == 128) {  // a valid chunk length no kernel of this build implements
-    set_error("%s: chunk length C=128 is not implemented in this build (use 0 or 64)", fn);
+  const int kind = mode & 0xff;
+  if (C == 128 && !c128_mode(mode)) {
+    set_error("%s: C=128 is implemented for the materialised variant of LA_LINEAR, LA_ELU1_NORM, LA_RETNET "
+              "and LA_SCALAR_GATE (bfloat16, causal)", fn);
     return LA_ERR_UNSUPPORTED;
   }
-  const int kind = mode & 0xff;
   if ((mode & LA_NONCAUSAL) && (mode & LA_F32)) {
     set_error("%s: LA_NONCAUSAL takes bfloat16 inputs only", fn);
     return LA_ERR_UNSUPPORTED;

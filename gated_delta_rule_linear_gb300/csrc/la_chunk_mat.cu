@@ -83,7 +83,7 @@ __host__ __device__ inline ALayout a_layout(int kind, int ns) {
 
 template <int DK, int DV, int KIND>
 __global__ void __launch_bounds__(kAThreads, 1)
-chunk_state_kernel(const ChunkParams p, uint8_t *__restrict__ ws, float *__restrict__ zws,
+chunk_state_kernel(const ChunkParams p, uint8_t *__restrict__ ws, float *__restrict__ zws, int istride,
                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const __grid_constant__ CUtensorMap tm_g) {
   constexpr bool elu = KIND == kElu1, gla = KIND == kGla;
@@ -98,6 +98,8 @@ chunk_state_kernel(const ChunkParams p, uint8_t *__restrict__ ws, float *__restr
   const int bh = blockIdx.x / nkb, kb = blockIdx.x % nkb, h = bh % p.H;
   const int c_base = kb * kKB;
   const int T = p.T, nch = (T + kC - 1) / kC;
+  // one image every istride chunks (istride = 2 for the 128-token output pass)
+  const int nimg = (nch + istride - 1) / istride;
 
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bar);
   uint64_t *full = bars, *empty = bars + kAMaxStages, *kready = bars + 2 * kAMaxStages;
@@ -185,10 +187,10 @@ chunk_state_kernel(const ChunkParams p, uint8_t *__restrict__ ws, float *__restr
   } else if (warp == 2) {
     if (lane == 0) {  // ships each image atom with one bulk copy; one copy in flight
       int done = 0;
-      for (int i = 0; i < nch; ++i) {
+      for (int i = 0; i < nimg; ++i) {
         const int ib = i & 1;
         if (!wait_or_abort(&img_full[ib], (i >> 1) & 1, abort_flag, p.status)) break;
-        bulk_store(ws + ((size_t)bh * nch + i) * blob_bytes(DK) + (size_t)kb * 16384u,
+        bulk_store(ws + ((size_t)bh * nimg + i) * blob_bytes(DK) + (size_t)kb * 16384u,
                    sm + L.st + (uint32_t)ib * 16384u, 16384u);
         bulk_commit();
         if (i > 0) {
@@ -227,7 +229,8 @@ chunk_state_kernel(const ChunkParams p, uint8_t *__restrict__ ws, float *__restr
         gn1 = gate((i + 1) * kC + lane + 32);
       }
       if (!group_wait(&full[s], (i / NS) & 1, kt, kAKBar, abort_flag, p.status)) break;
-      if (elu && half == 0 && zws) zws[((size_t)bh * nch + i) * DK + c_base + col] = z;  // z before chunk i
+      if (elu && half == 0 && zws && i % istride == 0)  // z before chunk i, at image boundaries
+        zws[((size_t)bh * nimg + i / istride) * DK + c_base + col] = z;
       float rs[4] = {1.f, 1.f, 1.f, 1.f};  // e^{b_last - b_r} of rows r0 + 16 j
       if (sgate) {
         float v0 = gc0 * kLog2e, v1 = gc1 * kLog2e;
@@ -337,18 +340,20 @@ chunk_state_kernel(const ChunkParams p, uint8_t *__restrict__ ws, float *__restr
     // that gives up cannot leave the others blocked on a named barrier.
     bool alive = true;
     for (int i = 0; i < nch; ++i) {
-      const int s = i % NS, b = i % kANB, ib = i & 1;
+      const int s = i % NS, b = i % kANB;
       const float *ms = reinterpret_cast<const float *>(sm + L.misc + (uint32_t)s * 1024u);
-      // S_{i-1} as a bf16 image atom (warp 2 ships it)
-      if (!wait_or_abort(&img_free[ib], ((i >> 1) & 1) ^ 1, abort_flag, p.status)) {
-        alive = false;
-        break;
+      if (i % istride == 0) {  // S_{i-1} as a bf16 image atom (warp 2 ships it)
+        const int j = i / istride, ib = j & 1;
+        if (!wait_or_abort(&img_free[ib], ((j >> 1) & 1) ^ 1, abort_flag, p.status)) {
+          alive = false;
+          break;
+        }
+        uint8_t *img = sm + L.st + (uint32_t)ib * 16384u;
+        store_row32_bf16(img, 16384, v, 0, S);
+        store_row32_bf16(img, 16384, v, 32, S + 32);
+        fence_proxy_async();
+        mbar_arrive(&img_full[ib]);
       }
-      uint8_t *img = sm + L.st + (uint32_t)ib * 16384u;
-      store_row32_bf16(img, 16384, v, 0, S);
-      store_row32_bf16(img, 16384, v, 32, S + 32);
-      fence_proxy_async();
-      mbar_arrive(&img_full[ib]);
       // decay factors of chunk i (key group) and its local update (tensor core)
       if (!wait_or_abort(&kready[s], (i / NS) & 1, abort_flag, p.status) ||
           !wait_or_abort(&dfull[b], (i / kANB) & 1, abort_flag, p.status)) {
@@ -661,7 +666,7 @@ chunk_output_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const f
 #pragma unroll
           for (int a = 0; a < DV / 64; ++a) tma_store_3d(&tm_o, sm + L.ot + a * 8192, 64 * a, t0, bh);
           bulk_commit();
-          bulk_wait<0>();
+          bulk_wait_read<0>();  // the tile is read; the global writes complete with the grid
         }
       }
     }
@@ -670,6 +675,248 @@ chunk_output_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const f
   __syncthreads();
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tbase, 128);
+}
+
+// ============================================= output pass, C = 128
+// Chunk length 128 ("Talk Linear Attention" section 3.3: the chunk size trades
+// the quadratic intra-chunk work against the number of materialised states)
+// for the modes without per-channel gates. The state pass writes one image per
+// 128 tokens, half the bytes of C = 64, and each output CTA computes one
+// 128-token chunk for one 64-column half of the value axis, token-major:
+//   D1 = Q K^T (M = N = 128), P = the masked, decayed scores (bf16, packed in
+//   TMEM as the A operand), O1 = Q S_{i-1} (S^T image half as a K-major B),
+//   O2 = P V (V half as an MN-major B), o = Diag(e^b) O1 + O2.
+// The two value halves of a chunk are neighbouring CTAs: both compute D1 and P
+// (the tensor core has room to spare) and share q and k through L2. 256
+// threads, ~100 KB of shared memory and 256 TMEM columns let two CTAs share an
+// SM, so one CTA's loads overlap the other's MMAs and epilogue.
+constexpr int kC2 = 128;
+constexpr int kB2Threads = 256;
+
+struct B2Layout {
+  uint32_t q, k, v, s, misc, bar, total;
+};
+__host__ __device__ inline B2Layout b2_layout(int dk) {
+  B2Layout L;
+  uint32_t o = 0;
+  L.q = o; o += (uint32_t)(dk / 64) * 16384u;  // also the output staging tile once O1 is done
+  L.k = o; o += (uint32_t)(dk / 64) * 16384u;
+  L.v = o; o += 16384u;                       // 128 tokens x one 64-column half of V
+  L.s = o; o += (uint32_t)(dk / 64) * 8192u;  // 64 value rows of the S^T image
+  L.misc = o; o += 4096u;
+  L.bar = o; o += 64u;
+  L.total = o;
+  return L;
+}
+
+template <int DK, int DV, int KIND>
+__global__ void __launch_bounds__(kB2Threads, 2)
+chunk_output128_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const float *__restrict__ zws,
+                       const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o) {
+  constexpr bool elu = KIND == kElu1;
+  constexpr bool sgate = KIND == kRetnet || KIND == kScalar;
+  constexpr int NVH = DV / 64;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const B2Layout L = b2_layout(DK);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = p.T, nimg = (T + kC2 - 1) / kC2;
+  const int vh = blockIdx.x % NVH, ci = blockIdx.x / NVH;
+  const int bh = ci / nimg, j = ci % nimg, h = bh % p.H;
+  const int t0 = j * kC2, n = min(kC2, T - t0);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L.bar);  // q and k landed
+  uint64_t *mbar = bar + 1;                                   // MMA commits
+  uint64_t *bar_vs = bar + 2;                                 // v and the state image landed
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 3);
+  float *ms = reinterpret_cast<float *>(sm + L.misc);
+  // b2[128] log2 prefix | eb[128] e^{b} | den[128] | part[2][128] row sums / q.z halves
+  float *b2 = ms, *eb = ms + 128, *den = ms + 256, *part = ms + 384, *qzp = ms + 640;
+  uint8_t *sq = sm + L.q, *sk = sm + L.k;
+
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    mbar_init(mbar, 1);
+    mbar_init(bar_vs, 1);
+    fence_mbar_init();
+    // q and k first (the score MMAs wait for them), then v and the state image
+    mbar_arrive_expect_tx(bar, 2u * DK * kC2 * 2u);
+#pragma unroll
+    for (int a = 0; a < DK / 64; ++a) {
+      tma_load_3d(sq + a * 16384, &tm_q, bar, 64 * a, t0, bh);
+      tma_load_3d(sk + a * 16384, &tm_k, bar, 64 * a, t0, bh);
+    }
+    mbar_arrive_expect_tx(bar_vs, 64u * kC2 * 2u + (uint32_t)(DK / 64) * 8192u);
+    tma_load_3d(sm + L.v, &tm_v, bar_vs, 64 * vh, t0, bh);
+    const uint8_t *img = ws + ((size_t)bh * nimg + j) * blob_bytes(DK) + (size_t)vh * 8192u;
+#pragma unroll
+    for (int a = 0; a < DK / 64; ++a) bulk_load(sm + L.s + a * 8192, img + (size_t)a * 16384u, 8192u, bar_vs);
+  }
+  // scalar gates of this chunk (warp 1): 4 tokens per lane, then a warp scan
+  if (sgate && warp == 1) {
+    float gv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int t = t0 + 4 * lane + e;
+      gv[e] = (t < T) ? (KIND == kRetnet ? __ldg(p.g + h) : __ldg(p.g + (size_t)bh * T + t)) * kLog2e : 0.f;
+    }
+    gv[1] += gv[0];
+    gv[2] += gv[1];
+    gv[3] += gv[2];
+    float run = gv[3];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float a = __shfl_up_sync(0xffffffffu, run, off);
+      if (lane >= off) run += a;
+    }
+    const float base = run - gv[3];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      b2[4 * lane + e] = base + gv[e];
+      eb[4 * lane + e] = exp2f(base + gv[e]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const int row = 32 * (warp & 3) + lane, hc = warp >> 2;  // TMEM lane (token) and column half
+  const uint32_t tl = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+  // TMEM columns: D1 [0, 128); O1 [0, 64) and O2 [64, 128) once P is out of D1; P [128, 192)
+  constexpr uint32_t kD1 = 0, kO1 = 0, kO2 = 64, kP = 128;
+  bool ok = mbar_wait_bounded(bar, 0, kSpinLimit);
+  if (!__syncthreads_and(ok)) {
+    if (tid == 0) atomicOr(p.status, kStatusTimeout);
+  } else {
+    if (elu) {  // phi on the rows of [Q; K]; rows past the sequence end are zero
+      const int r = tid & (kC2 - 1);
+      uint8_t *base = tid < kC2 ? sq : sk;
+#pragma unroll 4
+      for (int g8 = 0; g8 < DK / 8; ++g8) {
+        uint8_t *ptr = base + (g8 >> 3) * 16384 + sw128_off(r, (g8 & 7) * 8);
+        float f[8];
+        unpack8(*reinterpret_cast<uint4 *>(ptr), f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = (r < n) ? (f[e] > 0.f ? f[e] + 1.f : __expf(f[e])) : 0.f;
+        *reinterpret_cast<uint4 *>(ptr) = pack8(f);
+      }
+      fence_proxy_async();
+      __syncthreads();
+    }
+    if (tid == 0) {
+      tc_fence_after();
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false, false);
+      const uint64_t dq = desc_sw128(smem_u32(sq), 16, 1024), dk_ = desc_sw128(smem_u32(sk), 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < DK / 16; ++kk) {
+        const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+        mma_bf16(tbase + kD1, desc_add(dq, ko), desc_add(dk_, ko), idesc, kk > 0);
+      }
+      mma_commit(mbar);
+    }
+    if (elu) {  // q.z for the normaliser, half of the key channels per thread, while D1 runs
+      const float *zp = zws + ((size_t)bh * nimg + j) * DK + hc * (DK / 2);
+      float acc = 0.f;
+#pragma unroll 4
+      for (int g8 = 0; g8 < DK / 16; ++g8) {
+        const int c = hc * (DK / 2) + g8 * 8;
+        float f[8];
+        unpack8(*reinterpret_cast<const uint4 *>(sq + (c >> 6) * 16384 + sw128_off(row, c & 63)), f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc = fmaf(f[e], __ldg(zp + g8 * 8 + e), acc);
+      }
+      qzp[hc * 128 + row] = acc;
+    }
+    ok = mbar_wait_bounded(mbar, 0, kSpinLimit);
+    if (!__syncthreads_and(ok)) {
+      if (tid == 0) atomicOr(p.status, kStatusTimeout);
+    } else {
+      tc_fence_after();
+      // ---- P = masked, decayed scores of row `row`, columns [64 hc, 64 hc + 64), bf16 into TMEM
+      const float b2r = sgate ? b2[row] : 0.f;
+      float rowsum = 0.f;
+#pragma unroll 1
+      for (int s0 = 64 * hc; s0 < 64 * hc + 64; s0 += 32) {
+        float d[32], fs[32];
+        if (sgate) load32(b2 + s0, fs);
+        tmem_ld32(tl + kD1 + s0, d);
+        tmem_wait_ld();
+        float pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float x0 = (s0 + e <= row && row < n) ? d[e] : 0.f;
+          float x1 = (s0 + e + 1 <= row && row < n) ? d[e + 1] : 0.f;
+          if (sgate) {
+            x0 *= exp2f(s0 + e <= row ? b2r - fs[e] : 0.f);
+            x1 *= exp2f(s0 + e + 1 <= row ? b2r - fs[e + 1] : 0.f);
+          }
+          const uint32_t w = pack_bf16(x0, x1);
+          if (elu) rowsum += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+          pk[e >> 1] = __uint_as_float(w);
+        }
+        tmem_st16(tl + kP + (uint32_t)(s0 >> 1), pk);
+      }
+      if (elu) part[hc * 128 + row] = rowsum;
+      tmem_wait_st();
+      tc_fence_before();
+      __syncthreads();
+      // v and the state image (loaded while the scores ran); only the issuing thread waits,
+      // so the MMAs are issued exactly when every thread goes on to wait for them
+      ok = tid == 0 ? mbar_wait_bounded(bar_vs, 0, kSpinLimit) : true;
+      if (tid == 0 && ok) {
+        tc_fence_after();
+        constexpr uint32_t id_o1 = idesc_bf16_f32(128, 64, false, false);
+        constexpr uint32_t id_o2 = idesc_bf16_f32(128, 64, false, true);
+        const uint64_t dq = desc_sw128(smem_u32(sq), 16, 1024), ds = desc_sw128(smem_u32(sm + L.s), 16, 1024);
+        const uint64_t dv = desc_sw128(smem_u32(sm + L.v), 16384, 1024);
+#pragma unroll
+        for (int kk = 0; kk < DK / 16; ++kk)
+          mma_bf16(tbase + kO1, desc_add(dq, (kk >> 2) * 16384 + (kk & 3) * 32),
+                   desc_add(ds, (kk >> 2) * 8192 + (kk & 3) * 32), id_o1, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kC2 / 16; ++kk)
+          mma_bf16_ts(tbase + kO2, tbase + kP + kk * 8, desc_add(dv, kk * 2048), id_o2, kk > 0);
+        mma_commit(mbar);
+      }
+      if (elu && tid < kC2) den[tid] = (part[tid] + part[128 + tid]) + (qzp[tid] + qzp[128 + tid]);
+      bool go = __syncthreads_and(ok);  // false: thread 0 gave up on bar_vs and issued nothing
+      if (go) go = __syncthreads_and(mbar_wait_bounded(mbar, 1, kSpinLimit));
+      if (!go) {
+        if (tid == 0) atomicOr(p.status, kStatusTimeout);
+      } else {
+        tc_fence_after();
+        // ---- o rows: value columns [32 hc, 32 hc + 32) of this half, staged token-major in the q tile
+        float a[32], b[32];
+        tmem_ld32(tl + kO1 + 32 * hc, a);
+        tmem_ld32(tl + kO2 + 32 * hc, b);
+        tmem_wait_ld();
+        const float sc = sgate ? eb[row] : 1.f;
+        const float dn = elu ? den[row] : 1.f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float y = sgate ? fmaf(sc, a[e], b[e]) : a[e] + b[e];
+          if (elu) y = __fdividef(y, dn);
+          a[e] = y;
+        }
+        store_row32_bf16(sq, 16384, row, 32 * hc, a);
+        fence_proxy_async();
+        __syncthreads();
+        if (tid == 0) {
+          tma_store_3d(&tm_o, sq, 64 * vh, t0, bh);
+          bulk_commit();
+          bulk_wait_read<0>();  // the tile is read; the global writes complete with the grid
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tbase, 256);
 }
 
 // ---------------------------------------------------------------- launch
@@ -701,13 +948,40 @@ int launch_typed(const ChunkParams &p, uint8_t *ws, float *zws, cudaStream_t str
     return LA_ERR_CUDA;
   }
   auto ka = chunk_state_kernel<DK, DV, KIND>;
-  auto kb = chunk_output_kernel<DK, DV, KIND>;
   cudaError_t e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sa);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sb);
+  const int istride = p.C == kC2 ? 2 : 1;
   if (e == cudaSuccess) {
-    ka<<<(unsigned)(BH * (DK / kKB)), kAThreads, sa, stream>>>(p, ws, zws, mk, mv, mgA);
+    ka<<<(unsigned)(BH * (DK / kKB)), kAThreads, sa, stream>>>(p, ws, zws, istride, mk, mv, mgA);
     e = cudaGetLastError();
   }
+  if constexpr (KIND != kGla) {
+    if (e == cudaSuccess && p.C == kC2) {
+      // the 128-token output pass: 128-row boxes, one CTA per (head, chunk, value half)
+      CUtensorMap mq2, mk2, mv2, mo2;
+      if (!(make_map(&mq2, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DK, p.T, BH, 64, CU_TENSOR_MAP_SWIZZLE_128B, kC2) &&
+            make_map(&mk2, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DK, p.T, BH, 64, CU_TENSOR_MAP_SWIZZLE_128B, kC2) &&
+            make_map(&mv2, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DV, p.T, BH, 64, CU_TENSOR_MAP_SWIZZLE_128B, kC2) &&
+            make_map(&mo2, p.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DV, p.T, BH, 64, CU_TENSOR_MAP_SWIZZLE_128B, kC2))) {
+        set_error("la_chunk_fwd: cuTensorMapEncodeTiled rejected a tensor map");
+        return LA_ERR_CUDA;
+      }
+      auto kc = chunk_output128_kernel<DK, DV, KIND>;
+      const size_t sc = b2_layout(DK).total + 1024;
+      const size_t nimg = (size_t)(p.T + kC2 - 1) / kC2;
+      e = cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc);
+      if (e == cudaSuccess) {
+        kc<<<(unsigned)((size_t)BH * nimg * (DV / 64)), kB2Threads, sc, stream>>>(p, ws, zws, mq2, mk2, mv2, mo2);
+        e = cudaGetLastError();
+      }
+      if (e != cudaSuccess) {
+        set_error("la_chunk_fwd: materialised kernels failed to launch: %s", cudaGetErrorString(e));
+        return LA_ERR_CUDA;
+      }
+      return LA_OK;
+    }
+  }
+  auto kb = chunk_output_kernel<DK, DV, KIND>;
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sb);
   if (e == cudaSuccess) {
     kb<<<(unsigned)((size_t)BH * nch), kBThreads, sb, stream>>>(p, ws, zws, mq, mk, mv, mg, mo);
     e = cudaGetLastError();
@@ -1215,7 +1489,9 @@ int launch_nc_kind(const ChunkParams &p, uint8_t *ws, cudaStream_t stream) {
 }  // namespace
 
 size_t mat_workspace_bytes(const ChunkParams &p) {
-  const size_t nch = (size_t)(p.T + kC - 1) / kC, BH = (size_t)p.B * p.H;
+  // one state image (and elu+1 normaliser) per chunk of p.C tokens
+  const size_t c = p.C == kC2 ? kC2 : kC;
+  const size_t nch = (size_t)(p.T + c - 1) / c, BH = (size_t)p.B * p.H;
   size_t b = BH * nch * blob_bytes(p.dk);
   if (p.kind == kElu1) b += BH * nch * p.dk * sizeof(float);
   return b;
@@ -1226,8 +1502,13 @@ int launch_chunk_mat(const ChunkParams &p, void *workspace, cudaStream_t stream)
     set_error("la_chunk_fwd: cuTensorMapEncodeTiled is unavailable");
     return LA_ERR_CUDA;
   }
+  if (p.C == kC2 && (p.kind == kGla || p.kind == kOuter || p.kind == kGdn || p.kind == kKda)) {
+    set_error("la_chunk_fwd: C=128 covers LA_LINEAR, LA_ELU1_NORM, LA_RETNET and LA_SCALAR_GATE");
+    return LA_ERR_UNSUPPORTED;
+  }
   uint8_t *ws = static_cast<uint8_t *>(workspace);
-  const size_t nch = (size_t)(p.T + kC - 1) / kC, BH = (size_t)p.B * p.H;
+  const size_t c = p.C == kC2 ? kC2 : kC;
+  const size_t nch = (size_t)(p.T + c - 1) / c, BH = (size_t)p.B * p.H;
   float *zws = (p.kind == kElu1) ? reinterpret_cast<float *>(ws + BH * nch * blob_bytes(p.dk)) : nullptr;
   switch (p.kind) {
     case kLinear: return launch_kind<kLinear>(p, ws, zws, stream);

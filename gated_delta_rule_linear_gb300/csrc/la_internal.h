@@ -25,6 +25,15 @@ enum StatusBits : unsigned {
   kStatusTimeout = 1u,
 };
 
+// Whether a mode word may request the 128-token chunk: the materialised
+// variant's output pass for the modes without per-channel gates, bfloat16,
+// causal (no flag bits).
+inline bool c128_mode(int mode) {
+  const int kind = mode & 0xff;
+  return (mode & ~0xff) == 0 &&
+         (kind == LA_LINEAR || kind == LA_ELU1_NORM || kind == LA_RETNET || kind == LA_SCALAR_GATE);
+}
+
 // Everything a chunk-forward kernel needs, by value.
 struct ChunkParams {
   const void *q, *k, *v;

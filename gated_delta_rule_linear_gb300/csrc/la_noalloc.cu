@@ -56,12 +56,8 @@ extern "C" int la_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
     return LA_ERR_UNSUPPORTED;
   }
   if (C != 0 && C != 64 && C != 128) {
-    set_error("%s: C must be 0 or 64 (got %d)", fn, C);
+    set_error("%s: C must be 0, 64 or 128 (got %d)", fn, C);
     return LA_ERR_INVALID_ARG;
-  }
-  if (C == 128) {
-    set_error("%s: chunk length C=128 is not implemented in this build (use 0 or 64)", fn);
-    return LA_ERR_UNSUPPORTED;
   }
   const int kind = mode & 0xff;
   if ((mode & ~0xff) != 0 || kind < LA_LINEAR || kind > LA_OUTER_GATE) {
@@ -70,6 +66,10 @@ extern "C" int la_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
   }
   if (kind == LA_GDN || kind == LA_KDA || kind == LA_OUTER_GATE) {
     set_error("%s: covers the unit-write modes with key-axis gates only (not LA_GDN, LA_KDA or LA_OUTER_GATE)", fn);
+    return LA_ERR_UNSUPPORTED;
+  }
+  if (C == 128 && !c128_mode(mode)) {
+    set_error("%s: C=128 covers LA_LINEAR, LA_ELU1_NORM, LA_RETNET and LA_SCALAR_GATE (not LA_GLA)", fn);
     return LA_ERR_UNSUPPORTED;
   }
   const bool needs_g = kind == LA_RETNET || kind == LA_GLA || kind == LA_SCALAR_GATE;
@@ -83,10 +83,10 @@ extern "C" int la_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
     set_error("%s: q, k, v, o (and g for LA_GLA) must be 16-byte aligned, S0 and S_final 4-byte", fn);
     return LA_ERR_INVALID_ARG;
   }
-  ChunkParams p{q, k, v, g, beta, o, S0, S_final, B, H, T, dk, dv, 64, kind, 0, nullptr};
+  ChunkParams p{q, k, v, g, beta, o, S0, S_final, B, H, T, dk, dv, C == 128 ? 128 : 64, kind, 0, nullptr};
   const size_t need = mat_workspace_bytes(p);
   if (need > (size_t)LA_NOALLOC_SCRATCH_BYTES) {
-    set_error("%s: this shape needs %zu bytes of scratch (B*H*ceil(T/64)*dk*256, plus dk*4 per chunk for "
+    set_error("%s: this shape needs %zu bytes of scratch (B*H*ceil(T/C)*dk*256, plus dk*4 per chunk for "
               "LA_ELU1_NORM); the static scratch holds %zu",
               fn, need, (size_t)LA_NOALLOC_SCRATCH_BYTES);
     return LA_ERR_INVALID_ARG;

@@ -137,10 +137,12 @@ typedef struct CUstream_st *la_stream_t;
  *   S_final float32 [B][H][dk][W] final state, or NULL to skip writing it
  *           (may alias S0: every head reads its S0 before writing S_final)
  *   B, H, T >= 1; dk, dv in {64, 128}
- *   C       chunk length: 0 (pick per shape) or 64. C = 128 is a valid
- *           request that this build does not implement: it returns
- *           LA_ERR_UNSUPPORTED on the host, before any CUDA call; any other
- *           value is LA_ERR_INVALID_ARG.
+ *   C       chunk length: 0 (pick per shape), 64 or 128. C = 128 runs the
+ *           materialised variant of LA_LINEAR, LA_ELU1_NORM, LA_RETNET and
+ *           LA_SCALAR_GATE (bfloat16, causal); for any other mode or flag it
+ *           returns LA_ERR_UNSUPPORTED on the host, before any CUDA call, as
+ *           it does when LA_VARIANT forces another variant. Any other value
+ *           is LA_ERR_INVALID_ARG.
  *   mode    one LA_* mode, optionally | LA_F32
  *
  * S_final of one call passed as S0 of the next continues the sequence
@@ -150,11 +152,13 @@ typedef struct CUstream_st *la_stream_t;
  * head walks the chunks, keeping the state on chip; nothing but q, k, v, o and
  * the states touches memory. Materialised (unit-write modes, bfloat16): a
  * serial pass writes every chunk's incoming state to a workspace of
- * B*H*ceil(T/64)*dk*256 bytes (plus B*H*ceil(T/64)*dk*4 for LA_ELU1_NORM),
+ * B*H*ceil(T/C)*dk*256 bytes (plus B*H*ceil(T/C)*dk*4 for LA_ELU1_NORM),
  * then all chunks' outputs are computed in parallel; it wins when B*H is too
  * small to fill the GPU. The choice is made per shape: materialised for the
- * unit-write modes when T >= 512 and B*H <= SMs / 2 (GLA: SMs / 4), fused
- * otherwise. Gated DeltaNet runs fused by default; its two-phase variant (the
+ * unit-write modes when T >= 512 and B*H <= SMs / 2 (GLA: SMs / 4; elu+1:
+ * any B*H), fused otherwise; with C = 0 the materialised variant runs C = 128
+ * for LA_LINEAR and LA_ELU1_NORM, and for LA_RETNET and LA_SCALAR_GATE when
+ * T >= 2048, else C = 64. The fused kernels run C = 64. Gated DeltaNet runs fused by default; its two-phase variant (the
  * triangular solve of every chunk first, written as one 8 KB image per chunk of
  * 64 tokens to a workspace of B*H*ceil(T/64)*8192 bytes, then the state chain,
  * dk = dv = 128) is selected by LA_DELTA=wy. The environment variable
@@ -172,12 +176,13 @@ int la_chunk_fwd(const void *q, const void *k, const void *v, const float *g, co
  *
  *   Arguments, layouts and results as la_chunk_fwd, restricted to the modes
  *   the materialised variant covers: LA_LINEAR, LA_ELU1_NORM, LA_RETNET,
- *   LA_GLA and LA_SCALAR_GATE, bfloat16, causal, C = 0 or 64. Rejected on
- *   the host before any CUDA call: LA_GDN, LA_KDA and LA_OUTER_GATE
- *   (LA_ERR_UNSUPPORTED), LA_F32 (LA_ERR_UNSUPPORTED), C = 128
- *   (LA_ERR_UNSUPPORTED), LA_NONCAUSAL or any other flag, an unknown mode, a
- *   missing or superfluous g, any beta (LA_ERR_INVALID_ARG). Scratch needed: B*H*ceil(T/64)*dk*256 bytes, plus B*H*ceil(T/64)*dk*4
- *   for LA_ELU1_NORM. A call that needs more than LA_NOALLOC_SCRATCH_BYTES
+ *   LA_GLA and LA_SCALAR_GATE, bfloat16, causal, C = 0 (64) or 64, or 128
+ *   for every one of them but LA_GLA. Rejected on the host before any CUDA
+ *   call: LA_GDN, LA_KDA and LA_OUTER_GATE (LA_ERR_UNSUPPORTED), LA_F32
+ *   (LA_ERR_UNSUPPORTED), C = 128 with LA_GLA (LA_ERR_UNSUPPORTED),
+ *   LA_NONCAUSAL or any other flag, an unknown mode, a missing or
+ *   superfluous g, any beta (LA_ERR_INVALID_ARG). Scratch needed:
+ *   B*H*ceil(T/C)*dk*256 bytes, plus B*H*ceil(T/C)*dk*4 for LA_ELU1_NORM. A call that needs more than LA_NOALLOC_SCRATCH_BYTES
  *   is rejected with LA_ERR_INVALID_ARG before anything is launched.
  *   Allocates nothing: no cudaMalloc, cudaFree or stream-ordered allocation.
  *   The scratch is one array per device, shared by every call on that

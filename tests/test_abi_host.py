@@ -71,10 +71,11 @@ def _call(**kw):
     (dict(dk=96), "LA_ERR_UNSUPPORTED"),
     (dict(dv=32), "LA_ERR_UNSUPPORTED"),
     (dict(C=32), "LA_ERR_INVALID_ARG"),
-    (dict(C=128), "LA_ERR_UNSUPPORTED"),              # documented: valid, not implemented
-    (dict(C=128, mode=5), "LA_ERR_UNSUPPORTED"),
-    (dict(C=128, mode=2, g=A), "LA_ERR_UNSUPPORTED"),
-    (dict(C=128, mode=0x100), "LA_ERR_UNSUPPORTED"),
+    (dict(C=128, mode=3, g=A), "LA_ERR_UNSUPPORTED"),  # C = 128: not for the per-channel gates
+    (dict(C=128, mode=5), "LA_ERR_UNSUPPORTED"),       # ... nor the delta rule
+    (dict(C=128, mode=6, g=A), "LA_ERR_UNSUPPORTED"),
+    (dict(C=128, mode=7, g=A, beta=A), "LA_ERR_UNSUPPORTED"),
+    (dict(C=128, mode=0x100), "LA_ERR_UNSUPPORTED"),   # ... nor float32
     (dict(mode=9), "LA_ERR_INVALID_ARG"),
     (dict(mode=0x400), "LA_ERR_INVALID_ARG"),          # unknown flag
     (dict(q=A + 8), "LA_ERR_INVALID_ARG"),            # 16-byte alignment

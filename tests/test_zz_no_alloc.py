@@ -46,7 +46,7 @@ def test_scratch_limit_is_exact(lib):
     (dict(mode=la.LA_KDA, g=A), "LA_ERR_UNSUPPORTED"),
     (dict(mode=la.LA_OUTER_GATE, g=A, beta=A), "LA_ERR_UNSUPPORTED"),
     (dict(mode=la.LA_LINEAR | la.LA_F32), "LA_ERR_UNSUPPORTED"),
-    (dict(C=128), "LA_ERR_UNSUPPORTED"),
+    (dict(mode=la.LA_GLA, g=A, C=128), "LA_ERR_UNSUPPORTED"),   # C = 128 without per-channel gates only
     (dict(C=32), "LA_ERR_INVALID_ARG"),
     (dict(mode=la.LA_LINEAR | la.LA_NONCAUSAL), "LA_ERR_INVALID_ARG"),
     (dict(mode=9), "LA_ERR_INVALID_ARG"),
@@ -104,3 +104,18 @@ def test_noalloc_matches_materialised_entry_point_on_two_calls(lib, mode, monkey
     # the first call may load the module that holds the static array; the second,
     # larger call must not take any device memory
     assert free[1] == free[0], f"device memory changed by {free[0] - free[1]} bytes across a no-alloc call"
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mode", ["retnet", "elu1"])
+def test_noalloc_c128_matches_entry_point(lib, mode):
+    stream = torch.cuda.current_stream()
+    wl, d = _inputs(mode, 1, 4, 1000, 13)
+    o_ref, S_ref = la.chunk_fwd(d["q"], d["k"], d["v"], wl.mode, g=d["g"], S0=d["S0"], C=128)
+    o = torch.full_like(o_ref, float("nan"))
+    S = torch.full_like(S_ref, float("nan"))
+    rc = la.la_chunk_fwd_noalloc(d["q"], d["k"], d["v"], d["g"], None, o, d["S0"], S,
+                                 1, 4, 1000, wl.dk, wl.dv, 128, la.MODE_IDS[wl.mode], stream.cuda_stream)
+    assert rc == 0, la.la_last_error()
+    assert la.la_stream_status(stream.cuda_stream) == 0, la.la_last_error()
+    assert torch.equal(o, o_ref) and torch.equal(S, S_ref)
