@@ -58,6 +58,7 @@ KERNEL_SOURCES = {
     "backward_gla": [_CS + "la_backward.cu", _CS + "la_chunk_ws.cu"] + _COMMON,
     "decode": [_CS + "la_step.cu"],
     "gdelta": [_CS + "la_chunk_gdelta.cu"],
+    "backward_gdn": [_CS + "la_backward_delta.cu", _CS + "la_wy.cuh", _CS + "la_tc_common.cuh"],
     "prologue": [_CS + "la_prologue.cu", _CS + "la_sm100.cuh"],
     "prologue_gla": [_CS + "la_prologue.cu", _CS + "la_sm100.cuh"],
 }
@@ -752,17 +753,26 @@ def backward_bytes(wl) -> float:
         per_tok += 8
     elif wl.mode == "gla":
         per_tok += 8 * wl.dk
+    elif wl.mode == "gdn":  # read g and beta, write dg and dbeta; also read S0
+        per_tok += 16
+        return float(wl.B * wl.H * (wl.T * per_tok + 3 * 4 * wl.dk * wl.dv))
     return float(wl.B * wl.H * (wl.T * per_tok + 2 * 4 * wl.dk * wl.dv))
 
 
 def time_backward_oracle(wl, inp, target_s: float = 10.0):
     from oracle.backward import backward, backward_gla, backward_scalar
+    from oracle.backward_delta import backward_delta
     f64 = lambda t: None if t is None else t.to(torch.float64).numpy()
     BH = wl.B * wl.H
     done, t0 = 0, time.perf_counter()
     while done < BH and (time.perf_counter() - t0) < target_s:
         b, h = done // wl.H, done % wl.H
-        sl = lambda t: f64(t[b:b + 1, h:h + 1])
+        sl = lambda t: None if t is None else f64(t[b:b + 1, h:h + 1])
+        if wl.mode == "gdn":  # one full-length head per iteration (the token recurrence, reversed)
+            backward_delta(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["dO"]), "gdn", g=sl(inp["g"]),
+                           beta=sl(inp["beta"]), S0=sl(inp["S0"]), dS=sl(inp["dS"]))
+            done += 1
+            continue
         if wl.mode == "gla":  # quadratic in T: a 512-token prefix of one head
             pre = lambda t: t[..., :512, :]
             backward_gla(pre(sl(inp["q"])), pre(sl(inp["k"])), pre(sl(inp["v"])), pre(sl(inp["dO"])),
@@ -818,12 +828,15 @@ def bench_backward(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     inp = backward_inputs(wl)
-    names = [n for n in ("q", "k", "v", "g", "dO", "dS") if inp[n] is not None]
+    delta = wl.mode == "gdn"
+    names = [n for n in ("q", "k", "v", "g", "dO", "dS") + (("beta", "S0") if delta else ()) if inp[n] is not None]
     d = {n: inp[n].to(dev) for n in names}
     outs = {"dq": torch.empty_like(d["q"]), "dk": torch.empty_like(d["k"]), "dv": torch.empty_like(d["v"]),
             "dS0": torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)}
-    if wl.mode == "scalar":
+    if wl.mode in ("scalar", "gdn"):
         outs["dg"] = torch.empty(B, H, T, dtype=torch.float32, device=dev)
+    if delta:
+        outs["dbeta"] = torch.empty(B, H, T, dtype=torch.float32, device=dev)
     elif wl.mode == "gla":
         outs["dg"] = torch.empty(B, H, T, dk, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -831,8 +844,13 @@ def bench_backward(args, rank, world, local_rank):
     mode_id = la.MODE_IDS[wl.mode] | (la.CONSTANTS["LA_F32"] if wl.dtype == "f32" else 0)
 
     def step(dd, oo):
-        rc = la.la_chunk_bwd(dd["q"], dd["k"], dd["v"], dd.get("g"), dd["dO"], dd["dS"], None, oo["dq"], oo["dk"],
-                             oo["dv"], oo["dS0"], oo.get("dg"), B, H, T, dk, dv, wl.C, mode_id, sh)
+        if delta:
+            rc = la.la_chunk_bwd_delta(dd["q"], dd["k"], dd["v"], dd.get("g"), dd.get("beta"), dd["dO"], dd["dS"],
+                                       dd.get("S0"), oo["dq"], oo["dk"], oo["dv"], oo["dbeta"], oo["dg"], oo["dS0"],
+                                       B, H, T, dk, dv, wl.C, mode_id, sh)
+        else:
+            rc = la.la_chunk_bwd(dd["q"], dd["k"], dd["v"], dd.get("g"), dd["dO"], dd["dS"], None, oo["dq"],
+                                 oo["dk"], oo["dv"], oo["dS0"], oo.get("dg"), B, H, T, dk, dv, wl.C, mode_id, sh)
         if rc != 0:
             raise RuntimeError(la.la_last_error())
 
@@ -868,7 +886,8 @@ def bench_backward(args, rank, world, local_rank):
     achieved = alg / (statistics.mean(launch_ms) / 1e3) / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
             "frac": round(achieved / hbm_peak, 4), "traffic": recorded_traffic(wl.name), "peak_source": peak_src,
-            "algorithmic_bytes": alg, "kernel": "3 x chunk_ws_kernel (dq causal; dk and dv reversed runs)"
+            "algorithmic_bytes": alg, "kernel": "bd_pre_kernel + bd_fwd_kernel + bd_bwd_kernel + bd_grad_kernel"
+            if delta else "3 x chunk_ws_kernel (dq causal; dk and dv reversed runs)"
             + (" + forward for S_final + dg_tile_kernel + dg_carry_kernel" if wl.mode == "scalar" else
                " + forward for S_final + dgc_tile_kernel + dgc_carry_kernel (dq, dk: outer-product-gate passes)"
                if wl.mode == "gla" else ""),

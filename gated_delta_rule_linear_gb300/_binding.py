@@ -52,6 +52,7 @@ SIGNATURES = {
     "la_chunk_fwd_noalloc": ([_P] * 8 + [_I] * 7 + [_P], _I),
     "la_recurrent_step": ([_P] * 7 + [_I] * 5 + [_P], _I),
     "la_chunk_bwd": ([_P] * 12 + [_I] * 7 + [_P], _I),
+    "la_chunk_bwd_delta": ([_P] * 14 + [_I] * 7 + [_P], _I),
     "la_prologue": ([_P] * 6 + [_I] + [_P] * 3 + [_I, _I, _F] + [_P] * 6 + [_I] * 6 + [_P], _I),
     "la_stream_status": ([_P], _I),
     "la_last_error": ([], ctypes.c_char_p),
@@ -115,6 +116,14 @@ def la_chunk_bwd(q, k, v, g, dO, dS_final, S0, dq_out, dk_out, dv_out, dS0, dg_o
     return load_library().la_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(dO), _ptr(dS_final), _ptr(S0),
                                        _ptr(dq_out), _ptr(dk_out), _ptr(dv_out), _ptr(dS0), _ptr(dg_out), B, H, T,
                                        dk, dv, C, mode, stream)
+
+
+def la_chunk_bwd_delta(q, k, v, g, beta, dO, dS_final, S0, dq_out, dk_out, dv_out, dbeta_out, dg_out, dS0,
+                       B, H, T, dk, dv, C, mode, stream):
+    return load_library().la_chunk_bwd_delta(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(dO),
+                                             _ptr(dS_final), _ptr(S0), _ptr(dq_out), _ptr(dk_out), _ptr(dv_out),
+                                             _ptr(dbeta_out), _ptr(dg_out), _ptr(dS0), B, H, T, dk, dv, C, mode,
+                                             stream)
 
 
 def la_recurrent_step(q, k, v, g, beta, o, S, B, H, dk, dv, mode, stream):
@@ -266,6 +275,31 @@ def chunk_bwd(q, k, v, dO, mode, g=None, S0=None, dS_final=None, with_dS0=True, 
     if rc != 0:
         raise LAError(rc, la_last_error())
     return dq, dk_, dv_, dS0, dg
+
+
+def chunk_bwd_delta(q, k, v, dO, g=None, beta=None, S0=None, dS_final=None, with_dS0=True, with_dg=True,
+                    with_dbeta=True, C=0, stream=None):
+    """Gated DeltaNet backward (la_chunk_bwd_delta). q, k [B,H,T,dk], v, dO
+    [B,H,T,dv] bf16 CUDA tensors; g, beta [B,H,T] fp32 or None; S0, dS_final
+    [B,H,dk,dv] fp32 or None. Returns dq, dk, dv, dbeta, dg, dS0 (None where
+    not requested; dg None without g)."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("dO", dO), ("g", g), ("beta", beta), ("S0", S0),
+                    ("dS_final", dS_final)):
+        _check(t, name)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    mid = _mode_id("gdn", q.dtype)
+    dq, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    f32 = dict(dtype=torch.float32, device=q.device)
+    dbeta = torch.empty((B, H, T), **f32) if with_dbeta else None
+    dg = torch.empty((B, H, T), **f32) if (with_dg and g is not None) else None
+    dS0 = torch.empty((B, H, dk, dv), **f32) if with_dS0 else None
+    rc = la_chunk_bwd_delta(q, k, v, g, beta, dO, dS_final, S0, dq, dk_, dv_, dbeta, dg, dS0, B, H, T, dk, dv,
+                            C, mid, _stream_handle(stream))
+    if rc != 0:
+        raise LAError(rc, la_last_error())
+    return dq, dk_, dv_, dbeta, dg, dS0
 
 
 def recurrent_step(q, k, v, S, mode, g=None, beta=None, o=None, stream=None):

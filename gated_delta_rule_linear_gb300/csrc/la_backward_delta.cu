@@ -1,0 +1,791 @@
+// la_chunk_bwd_delta: the backward pass of the delta-rule forward (Gated
+// DeltaNet: S_t = (I - beta_t k_t k_t^T) alpha_t S_{t-1} + beta_t k_t v_t^T,
+// o_t = S_t^T q_t; "LLM attention optimisation" page, Gated DeltaNet section;
+// "Talk Linear Attention" sections 6.2 and 4.1.2), chunkwise with C = 64.
+//
+// Per chunk with local prefix b_r of the log-gates (gamma_r = e^{b_r}, gL = the
+// last one, Gamma_rs = e^{b_r - b_s}), entering state S and the gradient
+// E = dL/dS at the chunk's end, the forward's WY form is
+//
+//   L = strict_lower(Gamma ⊙ K K^T),  T = (I + Diag(beta) L)^{-1}
+//   Z = V - Diag(gamma) K S,  U = T Diag(beta) Z,  P = lower(Gamma ⊙ Q K^T)
+//   O = Diag(gamma) Q S + P U,  S_next = gL S + Kt^T U,  Kt = Diag(gL / gamma) K
+//
+// and its reverse, read off line by line:
+//
+//   dU = Kt E + P^T dO,  Y = T^T dU,  dZ = Diag(beta) Y = dV
+//   dbeta_r = Y_r . Z_r + sum_s dA_rs L_rs,  dA = -strict_lower(Y U^T)
+//   dP = lower(dO U^T),  F = Diag(beta) dA ⊙ Gamma,  H = dP ⊙ Gamma
+//   dQ = Diag(gamma) dO S^T + H K
+//   dK = -Diag(gamma) dZ S^T + (gL / gamma) U E^T + F K + F^T K + H^T Q
+//   db_r = gamma_r (dO_r . (S^T q_r) - dZ_r . (S^T k_r)) + row/column sums of
+//          Diag(beta) dA ⊙ L and dP ⊙ P - (gL / gamma_r) k_r . (U E^T)_r,
+//          plus gL <S, E> + sum_r (gL / gamma_r) k_r . (U E^T)_r at the last row
+//   dg = the suffix sum of db inside the chunk
+//   E_prev = gL E + Q^T Diag(gamma) dO - K^T Diag(gamma) dZ
+//
+// Four launches:
+//   bd_pre_kernel   every chunk in parallel: L and P from one [Q; K] K^T
+//                   product, T by substitution; T and P to the workspace.
+//   bd_fwd_kernel   per (b, h) and 16 value columns, the chunks in order: S
+//                   entering each chunk to the workspace.
+//   bd_bwd_kernel   per (b, h) and 16 value columns, the chunks in reverse: E
+//                   at each chunk's end to the workspace; dS0.
+//   bd_grad_kernel  every chunk in parallel: the gradients above, the value
+//                   axis in blocks of 16 with dQ, dK, dA and dP held in
+//                   registers across the blocks.
+// Products are warp-level tf32 MMAs (16 x 8 x 8, fp32 accumulate) on tiles in
+// shared memory; bf16 inputs enter exactly (a bf16 is a tf32), fp32 operands
+// are rounded to the nearest tf32. A tail chunk is padded with zero rows, zero
+// gates and beta = 0, which leaves every real row's result unchanged.
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "la_internal.h"
+#include "la_wy.cuh"
+
+namespace la {
+namespace {
+
+using wy::mma_16x8x8_tf32;
+using wy::to_tf32;
+using tc::unpack8;
+
+constexpr int kCh = 64;        // chunk length
+constexpr int kCW = 16;        // value columns per block
+constexpr int kPf = kCh + 4;   // row pitch (floats) of C x C tiles
+constexpr int kPw = kCW + 4;   // row pitch (floats) of x 16 tiles
+template <int DK>
+struct Pitch {
+  static constexpr int h = DK + 8;  // row pitch (bf16) of q / k tiles: 16-byte rows
+};
+
+__device__ __forceinline__ uint32_t bfbits(const __nv_bfloat16 *p) {
+  return static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(p)) << 16;
+}
+__device__ __forceinline__ uint32_t tf(float x) { return to_tf32(x); }
+
+// acc[j] (the 16 x 8 tile at rows m0.., columns n0 + 8 j) += A[m0.., 0..K) B[0..K), ..]:
+// ga(m, k) and gb(k, n) return the tf32 bits of one element.
+template <int NT, class GA, class GB>
+__device__ __forceinline__ void wmma(float (&acc)[NT][4], int m0, int n0, int K, GA ga, GB gb, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll 2
+  for (int k0 = 0; k0 < K; k0 += 8) {
+    uint32_t a[4] = {ga(m0 + g, k0 + t), ga(m0 + g + 8, k0 + t), ga(m0 + g, k0 + t + 4),
+                     ga(m0 + g + 8, k0 + t + 4)};
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      uint32_t b[2] = {gb(k0 + t, n0 + 8 * j + g), gb(k0 + t + 4, n0 + 8 * j + g)};
+      mma_16x8x8_tf32(acc[j], a, b);
+    }
+  }
+}
+// f(row, col, value) over the elements of an accumulator set (values may be changed)
+template <int NT, class F>
+__device__ __forceinline__ void each(float (&acc)[NT][4], int m0, int n0, int lane, F f) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    f(m0 + g, n0 + 8 * j + 2 * t, acc[j][0]);
+    f(m0 + g, n0 + 8 * j + 2 * t + 1, acc[j][1]);
+    f(m0 + g + 8, n0 + 8 * j + 2 * t, acc[j][2]);
+    f(m0 + g + 8, n0 + 8 * j + 2 * t + 1, acc[j][3]);
+  }
+}
+template <int NT>
+__device__ __forceinline__ void zero(float (&acc)[NT][4]) {
+#pragma unroll
+  for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+}
+
+// Per-chunk scalars, by warp 0: gamma_r = e^{b_r}, e^{bL - b_r}, beta_r and b_r
+// (b the inclusive prefix of the chunk's log-gates); rows past the end get
+// zero gates and beta = 0.
+struct Scal {
+  float gam[kCh], glr[kCh], bet[kCh], b[kCh];
+};
+__device__ __forceinline__ void chunk_scalars(Scal &s, const float *g, const float *beta, size_t base, int n,
+                                              int lane) {
+  float x0 = 0.f, x1 = 0.f;
+  if (g) {
+    if (lane < n) x0 = __ldg(g + base + lane);
+    if (lane + 32 < n) x1 = __ldg(g + base + lane + 32);
+  }
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float a0 = __shfl_up_sync(0xffffffffu, x0, off), a1 = __shfl_up_sync(0xffffffffu, x1, off);
+    if (lane >= off) {
+      x0 += a0;
+      x1 += a1;
+    }
+  }
+  x1 += __shfl_sync(0xffffffffu, x0, 31);
+  const float bl = __shfl_sync(0xffffffffu, x1, 31);
+  s.b[lane] = x0;
+  s.b[lane + 32] = x1;
+  s.gam[lane] = __expf(x0);
+  s.gam[lane + 32] = __expf(x1);
+  s.glr[lane] = __expf(bl - x0);
+  s.glr[lane + 32] = __expf(bl - x1);
+  s.bet[lane] = lane < n ? (beta ? __ldg(beta + base + lane) : 1.f) : 0.f;
+  s.bet[lane + 32] = lane + 32 < n ? (beta ? __ldg(beta + base + lane + 32) : 1.f) : 0.f;
+}
+
+// rows [0, 64) of a [T][D] bf16 tensor from token t0 (n valid, zero beyond) into a tile of pitch P
+template <int D, int P>
+__device__ __forceinline__ void load_rows_bf16(__nv_bfloat16 *dst, const __nv_bfloat16 *src, int n, int tid,
+                                               int nthr) {
+  for (int i = tid; i < kCh * (D / 8); i += nthr) {
+    const int r = i / (D / 8), c = (i % (D / 8)) * 8;
+    uint4 u = make_uint4(0, 0, 0, 0);
+    if (r < n) u = *reinterpret_cast<const uint4 *>(src + (size_t)r * D + c);
+    *reinterpret_cast<uint4 *>(dst + r * P + c) = u;
+  }
+}
+// 64 x 16 columns [c0, c0 + 16) of a [T][D] bf16 tensor as float32 (pitch kPw)
+template <int D>
+__device__ __forceinline__ void load_cols_f32(float *dst, const __nv_bfloat16 *src, int c0, int n, int tid,
+                                              int nthr) {
+  for (int i = tid; i < kCh * 2; i += nthr) {
+    const int r = i >> 1, c = (i & 1) * 8;
+    uint4 u = make_uint4(0, 0, 0, 0);
+    if (r < n) u = *reinterpret_cast<const uint4 *>(src + (size_t)r * D + c0 + c);
+    float f[8];
+    unpack8(u, f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) dst[r * kPw + c + e] = f[e];
+  }
+}
+// a 64 x 64 float32 matrix (row-major, contiguous) into a tile of pitch kPf
+__device__ __forceinline__ void load_cc(float *dst, const float *src, int tid, int nthr) {
+  for (int i = tid; i < kCh * kCh / 4; i += nthr) {
+    const int r = i >> 4, c = (i & 15) * 4;
+    *reinterpret_cast<float4 *>(dst + r * kPf + c) = __ldg(reinterpret_cast<const float4 *>(src) + i);
+  }
+}
+
+// ============================================================ pre-pass
+template <int DK>
+struct PreSmem {
+  __nv_bfloat16 q[kCh * Pitch<DK>::h], k[kCh * Pitch<DK>::h];
+  float a[kCh * kPf];
+  Scal s;
+};
+
+template <int DK>
+__global__ void __launch_bounds__(128) bd_pre_kernel(const __nv_bfloat16 *__restrict__ q,
+                                                     const __nv_bfloat16 *__restrict__ k,
+                                                     const float *__restrict__ g, const float *__restrict__ beta,
+                                                     int T, float *__restrict__ Tw, float *__restrict__ Pw) {
+  constexpr int PH = Pitch<DK>::h;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  PreSmem<DK> &sm = *reinterpret_cast<PreSmem<DK> *>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int i = blockIdx.x, bh = blockIdx.y, nch = gridDim.x;
+  const int t0 = i * kCh, n = min(kCh, T - t0);
+  const size_t row0 = (size_t)bh * T + t0;
+  load_rows_bf16<DK, PH>(sm.q, q + row0 * DK, n, tid, 128);
+  load_rows_bf16<DK, PH>(sm.k, k + row0 * DK, n, tid, 128);
+  if (warp == 0) chunk_scalars(sm.s, g, beta, row0, n, lane);
+  __syncthreads();
+  // [Q; K] K^T: warps 0, 1 the rows of Q (P), warps 2, 3 the rows of K (A)
+  const __nv_bfloat16 *src = warp < 2 ? sm.q : sm.k;
+  const int rbase = (warp & 1) * 32;
+  float acc[2][8][4];
+  const size_t cbase = ((size_t)bh * nch + i) * kCh * kCh;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    zero(acc[h]);
+    wmma(acc[h], rbase + 16 * h, 0, DK, [&](int m, int kk) { return bfbits(src + m * PH + kk); },
+         [&](int kk, int nn) { return bfbits(sm.k + nn * PH + kk); }, lane);
+    if (warp < 2) {
+      each(acc[h], rbase + 16 * h, 0, lane, [&](int r, int s, float &v) {
+        Pw[cbase + r * kCh + s] = s <= r ? __expf(sm.s.b[r] - sm.s.b[s]) * v : 0.f;
+      });
+    } else {
+      each(acc[h], rbase + 16 * h, 0, lane, [&](int r, int s, float &v) {
+        sm.a[r * kPf + s] = s < r ? sm.s.bet[r] * __expf(sm.s.b[r] - sm.s.b[s]) * v : 0.f;
+      });
+    }
+  }
+  __syncthreads();
+  // T = (I + A)^{-1}, unit lower triangular: column j by forward substitution, in registers
+  if (tid < kCh) {
+    const int j = tid;
+    float tc[kCh];
+#pragma unroll
+    for (int r = 0; r < kCh; ++r) {
+      float x = r == j ? 1.f : 0.f;
+#pragma unroll
+      for (int s = 0; s < r; ++s) x = fmaf(-sm.a[r * kPf + s], tc[s], x);
+      tc[r] = r < j ? 0.f : x;
+    }
+#pragma unroll
+    for (int r = 0; r < kCh; ++r) Tw[cbase + r * kCh + j] = tc[r];
+  }
+}
+
+// ============================================================ state chain
+template <int DK>
+struct FwdSmem {
+  __nv_bfloat16 k[kCh * Pitch<DK>::h];
+  float v[kCh * kPw], t[kCh * kPf], s[DK * kPw], z[kCh * kPw], u[kCh * kPw];
+  Scal sc;
+};
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(128) bd_fwd_kernel(const __nv_bfloat16 *__restrict__ k,
+                                                     const __nv_bfloat16 *__restrict__ v,
+                                                     const float *__restrict__ g, const float *__restrict__ beta,
+                                                     const float *__restrict__ S0, int T,
+                                                     const float *__restrict__ Tw, float *__restrict__ Sin) {
+  constexpr int PH = Pitch<DK>::h, NCB = DV / kCW, RT = DK / 64;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  FwdSmem<DK> &sm = *reinterpret_cast<FwdSmem<DK> *>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x / NCB, c0 = (blockIdx.x % NCB) * kCW;
+  const int nch = (T + kCh - 1) / kCh;
+  // S[:, c0 .. c0 + 16) in registers: warp w holds row tiles w + 4 rt
+  float S[RT][2][4];
+#pragma unroll
+  for (int rt = 0; rt < RT; ++rt) {
+    zero(S[rt]);
+    if (S0)
+      each(S[rt], 16 * (warp + 4 * rt), 0, lane,
+           [&](int r, int c, float &x) { x = __ldg(S0 + ((size_t)bh * DK + r) * DV + c0 + c); });
+  }
+  for (int i = 0; i < nch; ++i) {
+    const int t0 = i * kCh, n = min(kCh, T - t0);
+    const size_t row0 = (size_t)bh * T + t0;
+    load_rows_bf16<DK, PH>(sm.k, k + row0 * DK, n, tid, 128);
+    load_cols_f32<DV>(sm.v, v + row0 * DV, c0, n, tid, 128);
+    load_cc(sm.t, Tw + ((size_t)bh * nch + i) * kCh * kCh, tid, 128);
+    if (warp == 0) chunk_scalars(sm.sc, g, beta, row0, n, lane);
+    float *sout = Sin + ((size_t)bh * nch + i) * DK * DV;
+#pragma unroll
+    for (int rt = 0; rt < RT; ++rt)
+      each(S[rt], 16 * (warp + 4 * rt), 0, lane, [&](int r, int c, float &x) {
+        sout[(size_t)r * DV + c0 + c] = x;
+        sm.s[r * kPw + c] = x;
+      });
+    __syncthreads();
+    // Z' = Diag(beta) (V - Diag(gamma) K S): warp w, rows 16 w
+    {
+      float a[2][4];
+      zero(a);
+      wmma(a, 16 * warp, 0, DK, [&](int m, int kk) { return bfbits(sm.k + m * PH + kk); },
+           [&](int kk, int nn) { return tf(sm.s[kk * kPw + nn]); }, lane);
+      each(a, 16 * warp, 0, lane, [&](int r, int c, float &x) {
+        sm.z[r * kPw + c] = sm.sc.bet[r] * (sm.v[r * kPw + c] - sm.sc.gam[r] * x);
+      });
+    }
+    __syncthreads();
+    // U' = Diag(gL / gamma) T Z'
+    {
+      float a[2][4];
+      zero(a);
+      wmma(a, 16 * warp, 0, kCh, [&](int m, int kk) { return tf(sm.t[m * kPf + kk]); },
+           [&](int kk, int nn) { return tf(sm.z[kk * kPw + nn]); }, lane);
+      each(a, 16 * warp, 0, lane, [&](int r, int c, float &x) { sm.u[r * kPw + c] = sm.sc.glr[r] * x; });
+    }
+    __syncthreads();
+    // S <- gL S + K^T U'
+    const float gL = sm.sc.gam[kCh - 1];
+#pragma unroll
+    for (int rt = 0; rt < RT; ++rt) {
+      each(S[rt], 0, 0, lane, [&](int, int, float &x) { x *= gL; });
+      wmma(S[rt], 16 * (warp + 4 * rt), 0, kCh, [&](int m, int kk) { return bfbits(sm.k + kk * PH + m); },
+           [&](int kk, int nn) { return tf(sm.u[kk * kPw + nn]); }, lane);
+    }
+    __syncthreads();
+  }
+}
+
+// ============================================================ gradient chain
+template <int DK>
+struct BwdSmem {
+  __nv_bfloat16 q[kCh * Pitch<DK>::h], k[kCh * Pitch<DK>::h];
+  float o[kCh * kPw], t[kCh * kPf], p[kCh * kPf], e[DK * kPw], du[kCh * kPw], y[kCh * kPw];
+  Scal sc;
+};
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(128) bd_bwd_kernel(const __nv_bfloat16 *__restrict__ q,
+                                                     const __nv_bfloat16 *__restrict__ k,
+                                                     const __nv_bfloat16 *__restrict__ dO,
+                                                     const float *__restrict__ g, const float *__restrict__ beta,
+                                                     const float *__restrict__ dS, int T,
+                                                     const float *__restrict__ Tw, const float *__restrict__ Pw,
+                                                     float *__restrict__ Eout, float *__restrict__ dS0) {
+  constexpr int PH = Pitch<DK>::h, NCB = DV / kCW, RT = DK / 64;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  BwdSmem<DK> &sm = *reinterpret_cast<BwdSmem<DK> *>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x / NCB, c0 = (blockIdx.x % NCB) * kCW;
+  const int nch = (T + kCh - 1) / kCh;
+  float E[RT][2][4];
+#pragma unroll
+  for (int rt = 0; rt < RT; ++rt) {
+    zero(E[rt]);
+    if (dS)
+      each(E[rt], 16 * (warp + 4 * rt), 0, lane,
+           [&](int r, int c, float &x) { x = __ldg(dS + ((size_t)bh * DK + r) * DV + c0 + c); });
+  }
+  for (int i = nch - 1; i >= 0; --i) {
+    const int t0 = i * kCh, n = min(kCh, T - t0);
+    const size_t row0 = (size_t)bh * T + t0;
+    load_rows_bf16<DK, PH>(sm.q, q + row0 * DK, n, tid, 128);
+    load_rows_bf16<DK, PH>(sm.k, k + row0 * DK, n, tid, 128);
+    load_cols_f32<DV>(sm.o, dO + row0 * DV, c0, n, tid, 128);
+    load_cc(sm.t, Tw + ((size_t)bh * nch + i) * kCh * kCh, tid, 128);
+    load_cc(sm.p, Pw + ((size_t)bh * nch + i) * kCh * kCh, tid, 128);
+    if (warp == 0) chunk_scalars(sm.sc, g, beta, row0, n, lane);
+    float *eout = Eout + ((size_t)bh * nch + i) * DK * DV;
+#pragma unroll
+    for (int rt = 0; rt < RT; ++rt)
+      each(E[rt], 16 * (warp + 4 * rt), 0, lane, [&](int r, int c, float &x) {
+        eout[(size_t)r * DV + c0 + c] = x;
+        sm.e[r * kPw + c] = x;
+      });
+    __syncthreads();
+    // dU = Diag(gL / gamma) K E + P^T dO
+    {
+      float a[2][4];
+      zero(a);
+      wmma(a, 16 * warp, 0, DK, [&](int m, int kk) { return bfbits(sm.k + m * PH + kk); },
+           [&](int kk, int nn) { return tf(sm.e[kk * kPw + nn]); }, lane);
+      each(a, 16 * warp, 0, lane, [&](int r, int, float &x) { x *= sm.sc.glr[r]; });
+      wmma(a, 16 * warp, 0, kCh, [&](int m, int kk) { return tf(sm.p[kk * kPf + m]); },
+           [&](int kk, int nn) { return tf(sm.o[kk * kPw + nn]); }, lane);
+      each(a, 16 * warp, 0, lane, [&](int r, int c, float &x) { sm.du[r * kPw + c] = x; });
+    }
+    __syncthreads();
+    // -Diag(gamma) dZ = -Diag(gamma beta) T^T dU
+    {
+      float a[2][4];
+      zero(a);
+      wmma(a, 16 * warp, 0, kCh, [&](int m, int kk) { return tf(sm.t[kk * kPf + m]); },
+           [&](int kk, int nn) { return tf(sm.du[kk * kPw + nn]); }, lane);
+      each(a, 16 * warp, 0, lane,
+           [&](int r, int c, float &x) { sm.y[r * kPw + c] = -sm.sc.gam[r] * sm.sc.bet[r] * x; });
+    }
+    __syncthreads();
+    // E <- gL E + Q^T Diag(gamma) dO - K^T Diag(gamma) dZ
+    const float gL = sm.sc.gam[kCh - 1];
+#pragma unroll
+    for (int rt = 0; rt < RT; ++rt) {
+      const int m0 = 16 * (warp + 4 * rt);
+      each(E[rt], 0, 0, lane, [&](int, int, float &x) { x *= gL; });
+      wmma(E[rt], m0, 0, kCh, [&](int m, int kk) { return bfbits(sm.q + kk * PH + m); },
+           [&](int kk, int nn) { return tf(sm.sc.gam[kk] * sm.o[kk * kPw + nn]); }, lane);
+      wmma(E[rt], m0, 0, kCh, [&](int m, int kk) { return bfbits(sm.k + kk * PH + m); },
+           [&](int kk, int nn) { return tf(sm.y[kk * kPw + nn]); }, lane);
+    }
+    __syncthreads();
+  }
+  if (dS0) {
+#pragma unroll
+    for (int rt = 0; rt < RT; ++rt)
+      each(E[rt], 16 * (warp + 4 * rt), 0, lane,
+           [&](int r, int c, float &x) { dS0[((size_t)bh * DK + r) * DV + c0 + c] = x; });
+  }
+}
+
+// ============================================================ gradients
+template <int DK>
+struct GradSmem {
+  __nv_bfloat16 q[kCh * Pitch<DK>::h], k[kCh * Pitch<DK>::h];
+  float t[kCh * kPf], p[kCh * kPf];
+  union {
+    struct {  // one block of 16 value columns
+      float s[DK * kPw], e[DK * kPw], v[kCh * kPw], o[kCh * kPw];
+      float ks[kCh * kPw], qs[kCh * kPw], ke[kCh * kPw], z[kCh * kPw], u[kCh * kPw], du[kCh * kPw],
+          y[kCh * kPw];
+    } blk;
+    struct {  // after the blocks: dA (then F), dP (then H), L
+      float da[kCh * kPf], dp[kCh * kPf], l[kCh * kPf];
+    } fin;
+  } w;
+  Scal sc;
+  float db[kCh], dbeta[kCh], kd[kCh], red[8];
+};
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(256, 1) bd_grad_kernel(
+    const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
+    const __nv_bfloat16 *__restrict__ dO, const float *__restrict__ g, const float *__restrict__ beta, int T,
+    const float *__restrict__ Tw, const float *__restrict__ Pw, const float *__restrict__ Sin,
+    const float *__restrict__ Eout, __nv_bfloat16 *__restrict__ dq, __nv_bfloat16 *__restrict__ dk,
+    __nv_bfloat16 *__restrict__ dv, float *__restrict__ dbeta, float *__restrict__ dg) {
+  constexpr int PH = Pitch<DK>::h, NT = DK / 16;  // 16 x 8 tiles per warp across dQ, dK (DK / 2 columns)
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  GradSmem<DK> &sm = *reinterpret_cast<GradSmem<DK> *>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int i = blockIdx.x, bh = blockIdx.y, nch = gridDim.x;
+  const int t0 = i * kCh, n = min(kCh, T - t0);
+  const size_t row0 = (size_t)bh * T + t0;
+  const size_t cbase = ((size_t)bh * nch + i) * kCh * kCh, sbase = ((size_t)bh * nch + i) * DK * DV;
+  load_rows_bf16<DK, PH>(sm.q, q + row0 * DK, n, tid, 256);
+  load_rows_bf16<DK, PH>(sm.k, k + row0 * DK, n, tid, 256);
+  load_cc(sm.t, Tw + cbase, tid, 256);
+  load_cc(sm.p, Pw + cbase, tid, 256);
+  if (warp == 0) chunk_scalars(sm.sc, g, beta, row0, n, lane);
+  if (tid < kCh) {
+    sm.db[tid] = 0.f;
+    sm.dbeta[tid] = 0.f;
+    sm.kd[tid] = 0.f;
+  }
+  // register accumulators: dQ, dK (rows 16 (w & 3), columns (w >> 2) DK / 2 ..), dA, dP (columns (w >> 2) 32 ..)
+  const int mr = 16 * (warp & 3), half = warp >> 2;
+  const int nq = half * (DK / 2), na = half * 32;
+  float aq[NT][4], ak[NT][4], aa[4][4], ap[4][4];
+  zero(aq);
+  zero(ak);
+  zero(aa);
+  zero(ap);
+  float se = 0.f;  // <S, E> over this thread's share
+  const int nc = 8 * half;  // x 16 tiles: warp w owns rows 16 (w & 3), columns 8 (w >> 2) .. + 8
+  auto& B = sm.w.blk;
+  __syncthreads();
+  for (int c0 = 0; c0 < DV; c0 += kCW) {
+    // ---- the block's S, E (float32) and V, dO columns
+    for (int x = tid; x < DK * kCW / 4; x += 256) {
+      const int r = x >> 2, c = (x & 3) * 4;
+      const float4 s4 = __ldg(reinterpret_cast<const float4 *>(Sin + sbase + (size_t)r * DV + c0 + c));
+      const float4 e4 = __ldg(reinterpret_cast<const float4 *>(Eout + sbase + (size_t)r * DV + c0 + c));
+      *reinterpret_cast<float4 *>(B.s + r * kPw + c) = s4;
+      *reinterpret_cast<float4 *>(B.e + r * kPw + c) = e4;
+      se += s4.x * e4.x + s4.y * e4.y + s4.z * e4.z + s4.w * e4.w;
+    }
+    load_cols_f32<DV>(B.v, v + row0 * DV, c0, n, tid, 256);
+    load_cols_f32<DV>(B.o, dO + row0 * DV, c0, n, tid, 256);
+    __syncthreads();
+    // ---- K S, Q S, Diag(gL / gamma) K E: one 16 x 8 tile each per warp
+    {
+      float a[1][4], b[1][4], c[1][4];
+      zero(a);
+      zero(b);
+      zero(c);
+      wmma(a, mr, nc, DK, [&](int m, int kk) { return bfbits(sm.k + m * PH + kk); },
+           [&](int kk, int nn) { return tf(B.s[kk * kPw + nn]); }, lane);
+      wmma(b, mr, nc, DK, [&](int m, int kk) { return bfbits(sm.q + m * PH + kk); },
+           [&](int kk, int nn) { return tf(B.s[kk * kPw + nn]); }, lane);
+      wmma(c, mr, nc, DK, [&](int m, int kk) { return bfbits(sm.k + m * PH + kk); },
+           [&](int kk, int nn) { return tf(B.e[kk * kPw + nn]); }, lane);
+      each(a, mr, nc, lane, [&](int r, int cc, float &x) { B.ks[r * kPw + cc] = x; });
+      each(b, mr, nc, lane, [&](int r, int cc, float &x) { B.qs[r * kPw + cc] = x; });
+      each(c, mr, nc, lane, [&](int r, int cc, float &x) { B.ke[r * kPw + cc] = sm.sc.glr[r] * x; });
+    }
+    __syncthreads();
+    // ---- Z = V - Diag(gamma) K S; db += gamma dO . (Q S)
+    {
+      const int r = tid >> 2, cq = (tid & 3) * 4;
+      float part = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = cq + e;
+        B.z[r * kPw + c] = B.v[r * kPw + c] - sm.sc.gam[r] * B.ks[r * kPw + c];
+        part += B.o[r * kPw + c] * B.qs[r * kPw + c];
+      }
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      if ((tid & 3) == 0) sm.db[r] += sm.sc.gam[r] * part;
+    }
+    __syncthreads();
+    // ---- U = T Diag(beta) Z; dU = Diag(gL / gamma) K E + P^T dO
+    {
+      float a[1][4], b[1][4];
+      zero(a);
+      wmma(a, mr, nc, kCh, [&](int m, int kk) { return tf(sm.t[m * kPf + kk]); },
+           [&](int kk, int nn) { return tf(sm.sc.bet[kk] * B.z[kk * kPw + nn]); }, lane);
+      each(a, mr, nc, lane, [&](int r, int cc, float &x) { B.u[r * kPw + cc] = x; });
+      each(b, mr, nc, lane, [&](int r, int cc, float &x) { x = B.ke[r * kPw + cc]; });
+      wmma(b, mr, nc, kCh, [&](int m, int kk) { return tf(sm.p[kk * kPf + m]); },
+           [&](int kk, int nn) { return tf(B.o[kk * kPw + nn]); }, lane);
+      each(b, mr, nc, lane, [&](int r, int cc, float &x) { B.du[r * kPw + cc] = x; });
+    }
+    __syncthreads();
+    // ---- Y = T^T dU; dV = Diag(beta) Y; dbeta += Y . Z; db -= gamma dZ . (K S); kd += U . (Kt E)
+    {
+      float a[1][4];
+      zero(a);
+      wmma(a, mr, nc, kCh, [&](int m, int kk) { return tf(sm.t[kk * kPf + m]); },
+           [&](int kk, int nn) { return tf(B.du[kk * kPw + nn]); }, lane);
+      const int gg = lane >> 2;
+      float pb[2] = {0.f, 0.f}, pd[2] = {0.f, 0.f}, pk[2] = {0.f, 0.f};
+      each(a, mr, nc, lane, [&](int r, int cc, float &y) {
+        const int h = (r - mr - gg) >> 3;  // 0: row g, 1: row g + 8
+        B.y[r * kPw + cc] = y;
+        const float dz = sm.sc.bet[r] * y;
+        if (r < n) dv[(row0 + r) * DV + c0 + cc] = __float2bfloat16_rn(dz);
+        pb[h] += y * B.z[r * kPw + cc];
+        pd[h] += dz * B.ks[r * kPw + cc];
+        pk[h] += B.u[r * kPw + cc] * B.ke[r * kPw + cc];
+      });
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int off = 1; off < 4; off <<= 1) {
+          pb[h] += __shfl_xor_sync(0xffffffffu, pb[h], off);
+          pd[h] += __shfl_xor_sync(0xffffffffu, pd[h], off);
+          pk[h] += __shfl_xor_sync(0xffffffffu, pk[h], off);
+        }
+        if ((lane & 3) == 0) {
+          const int r = mr + gg + 8 * h;
+          atomicAdd(&sm.dbeta[r], pb[h]);
+          atomicAdd(&sm.db[r], -sm.sc.gam[r] * pd[h]);
+          atomicAdd(&sm.kd[r], pk[h]);
+        }
+      }
+    }
+    __syncthreads();
+    // ---- dA -= Y U^T, dP += dO U^T, dQ += Diag(gamma) dO S^T,
+    //      dK += -Diag(gamma beta) Y S^T + Diag(gL / gamma) U E^T (K = 16 each)
+    wmma(aa, mr, na, kCW, [&](int m, int kk) { return tf(-B.y[m * kPw + kk]); },
+         [&](int kk, int nn) { return tf(B.u[nn * kPw + kk]); }, lane);
+    wmma(ap, mr, na, kCW, [&](int m, int kk) { return tf(B.o[m * kPw + kk]); },
+         [&](int kk, int nn) { return tf(B.u[nn * kPw + kk]); }, lane);
+    wmma(aq, mr, nq, kCW, [&](int m, int kk) { return tf(sm.sc.gam[m] * B.o[m * kPw + kk]); },
+         [&](int kk, int nn) { return tf(B.s[nn * kPw + kk]); }, lane);
+    wmma(ak, mr, nq, kCW, [&](int m, int kk) { return tf(-sm.sc.gam[m] * sm.sc.bet[m] * B.y[m * kPw + kk]); },
+         [&](int kk, int nn) { return tf(B.s[nn * kPw + kk]); }, lane);
+    wmma(ak, mr, nq, kCW, [&](int m, int kk) { return tf(sm.sc.glr[m] * B.u[m * kPw + kk]); },
+         [&](int kk, int nn) { return tf(B.e[nn * kPw + kk]); }, lane);
+    __syncthreads();
+  }
+  // ---- <S, E> over the block
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) se += __shfl_xor_sync(0xffffffffu, se, off);
+  if (lane == 0) sm.red[warp] = se;
+  // ---- dA, dP to shared memory; L = strict_lower(Gamma ⊙ K K^T)
+  auto& Fn = sm.w.fin;
+  each(aa, mr, na, lane, [&](int r, int s, float &x) { Fn.da[r * kPf + s] = x; });
+  each(ap, mr, na, lane, [&](int r, int s, float &x) { Fn.dp[r * kPf + s] = x; });
+  {
+    float a[4][4];
+    zero(a);
+    wmma(a, mr, na, DK, [&](int m, int kk) { return bfbits(sm.k + m * PH + kk); },
+         [&](int kk, int nn) { return bfbits(sm.k + nn * PH + kk); }, lane);
+    each(a, mr, na, lane, [&](int r, int s, float &x) {
+      Fn.l[r * kPf + s] = s < r ? __expf(sm.sc.b[r] - sm.sc.b[s]) * x : 0.f;
+    });
+  }
+  __syncthreads();
+  // ---- F = Diag(beta) dA ⊙ Gamma, H = dP ⊙ Gamma (in place); dbeta and the row / column sums of db
+  {
+    const int r = tid >> 2;
+    float rowp = 0.f, betp = 0.f;
+    for (int jj = 0; jj < kCh / 4; ++jj) {
+      const int s = (tid & 3) + 4 * jj;
+      const float gm = s <= r ? __expf(sm.sc.b[r] - sm.sc.b[s]) : 0.f;
+      const float a = s < r ? Fn.da[r * kPf + s] : 0.f;
+      const float l = Fn.l[r * kPf + s];
+      betp += a * l;
+      const float dl = sm.sc.bet[r] * a, dll = dl * l;
+      const float pp = s <= r ? Fn.dp[r * kPf + s] : 0.f;
+      const float ppp = pp * sm.p[r * kPf + s];
+      rowp += dll + ppp;
+      if (dll + ppp != 0.f) atomicAdd(&sm.db[s], -(dll + ppp));
+      Fn.da[r * kPf + s] = dl * gm;
+      Fn.dp[r * kPf + s] = pp * gm;
+    }
+    rowp += __shfl_xor_sync(0xffffffffu, rowp, 1);
+    rowp += __shfl_xor_sync(0xffffffffu, rowp, 2);
+    betp += __shfl_xor_sync(0xffffffffu, betp, 1);
+    betp += __shfl_xor_sync(0xffffffffu, betp, 2);
+    if ((tid & 3) == 0) {
+      atomicAdd(&sm.db[r], rowp);
+      sm.dbeta[r] += betp;
+    }
+  }
+  __syncthreads();
+  // ---- dQ += H K; dK += F K + F^T K + H^T Q
+  wmma(aq, mr, nq, kCh, [&](int m, int kk) { return tf(Fn.dp[m * kPf + kk]); },
+       [&](int kk, int nn) { return bfbits(sm.k + kk * PH + nn); }, lane);
+  wmma(ak, mr, nq, kCh, [&](int m, int kk) { return tf(Fn.da[m * kPf + kk]); },
+       [&](int kk, int nn) { return bfbits(sm.k + kk * PH + nn); }, lane);
+  wmma(ak, mr, nq, kCh, [&](int m, int kk) { return tf(Fn.da[kk * kPf + m]); },
+       [&](int kk, int nn) { return bfbits(sm.k + kk * PH + nn); }, lane);
+  wmma(ak, mr, nq, kCh, [&](int m, int kk) { return tf(Fn.dp[kk * kPf + m]); },
+       [&](int kk, int nn) { return bfbits(sm.q + kk * PH + nn); }, lane);
+  each(aq, mr, nq, lane, [&](int r, int c, float &x) {
+    if (r < n) dq[(row0 + r) * DK + c] = __float2bfloat16_rn(x);
+  });
+  each(ak, mr, nq, lane, [&](int r, int c, float &x) {
+    if (r < n) dk[(row0 + r) * DK + c] = __float2bfloat16_rn(x);
+  });
+  // ---- db: the Kt terms and gL <S, E> at the last row; dg = the suffix sum within the chunk
+  if (warp == 0) {
+    const float gL = sm.sc.gam[kCh - 1];
+    float sE = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) sE += sm.red[w];
+    const float k0 = sm.kd[lane], k1 = sm.kd[lane + 32];
+    float ksum = k0 + k1;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ksum += __shfl_xor_sync(0xffffffffu, ksum, off);
+    float d0 = sm.db[lane] - k0, d1 = sm.db[lane + 32] - k1;
+    if (lane == 31) d1 += ksum + gL * sE;
+    // suffix sums over 64 rows: lane holds rows lane and lane + 32
+    float s1 = d1, s0 = d0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float a1 = __shfl_down_sync(0xffffffffu, s1, off), a0 = __shfl_down_sync(0xffffffffu, s0, off);
+      if (lane + off < 32) {
+        s1 += a1;
+        s0 += a0;
+      }
+    }
+    s0 += __shfl_sync(0xffffffffu, s1, 0);
+    if (dg) {
+      if (lane < n) dg[row0 + lane] = s0;
+      if (lane + 32 < n) dg[row0 + lane + 32] = s1;
+    }
+    if (dbeta) {
+      if (lane < n) dbeta[row0 + lane] = sm.dbeta[lane];
+      if (lane + 32 < n) dbeta[row0 + lane + 32] = sm.dbeta[lane + 32];
+    }
+  }
+}
+
+template <class Smem, class K>
+cudaError_t set_smem(K kernel) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem));
+}
+
+template <int DK, int DV>
+int launch_typed(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v,
+                 const __nv_bfloat16 *dO, const float *g, const float *beta, const float *S0, const float *dS,
+                 __nv_bfloat16 *dq, __nv_bfloat16 *dk, __nv_bfloat16 *dv, float *dbeta, float *dg, float *dS0,
+                 int BH, int T, uint8_t *ws, cudaStream_t s) {
+  const int nch = (T + kCh - 1) / kCh;
+  const size_t ncc = (size_t)BH * nch * kCh * kCh, nss = (size_t)BH * nch * DK * DV;
+  float *Tw = reinterpret_cast<float *>(ws), *Pw = Tw + ncc, *Sin = Pw + ncc, *Eout = Sin + nss;
+  cudaError_t e = set_smem<PreSmem<DK>>(bd_pre_kernel<DK>);
+  if (e == cudaSuccess) e = set_smem<FwdSmem<DK>>(bd_fwd_kernel<DK, DV>);
+  if (e == cudaSuccess) e = set_smem<BwdSmem<DK>>(bd_bwd_kernel<DK, DV>);
+  if (e == cudaSuccess) e = set_smem<GradSmem<DK>>(bd_grad_kernel<DK, DV>);
+  if (e == cudaSuccess) {
+    bd_pre_kernel<DK><<<dim3(nch, BH), 128, sizeof(PreSmem<DK>), s>>>(q, k, g, beta, T, Tw, Pw);
+    e = cudaGetLastError();
+  }
+  const unsigned nchain = (unsigned)(BH * (DV / kCW));
+  if (e == cudaSuccess) {
+    bd_fwd_kernel<DK, DV><<<nchain, 128, sizeof(FwdSmem<DK>), s>>>(k, v, g, beta, S0, T, Tw, Sin);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) {
+    bd_bwd_kernel<DK, DV><<<nchain, 128, sizeof(BwdSmem<DK>), s>>>(q, k, dO, g, beta, dS, T, Tw, Pw, Eout, dS0);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) {
+    bd_grad_kernel<DK, DV><<<dim3(nch, BH), 256, sizeof(GradSmem<DK>), s>>>(q, k, v, dO, g, beta, T, Tw, Pw, Sin,
+                                                                           Eout, dq, dk, dv, dbeta, dg);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) {
+    set_error("la_chunk_bwd_delta: kernel launch failed: %s", cudaGetErrorString(e));
+    return LA_ERR_CUDA;
+  }
+  return LA_OK;
+}
+
+bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+size_t delta_bwd_workspace_bytes(int BH, int T, int dk, int dv) {
+  const size_t nch = (size_t)(T + kCh - 1) / kCh;
+  return (size_t)BH * nch * (2 * kCh * kCh + 2 * (size_t)dk * dv) * sizeof(float);
+}
+
+}  // namespace la
+
+using namespace la;
+
+extern "C" int la_chunk_bwd_delta(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                                  const void *dO, const float *dS_final, const float *S0, void *dq_out,
+                                  void *dk_out, void *dv_out, float *dbeta_out, float *dg_out, float *dS0,
+                                  int B, int H, int T, int dk, int dv, int C, int mode, la_stream_t stream) {
+  const char *fn = "la_chunk_bwd_delta";
+  set_error("%s", "");
+  if (!q || !k || !v || !dO || !dq_out || !dk_out || !dv_out) {
+    set_error("%s: q, k, v, dO, dq, dk and dv are required", fn);
+    return LA_ERR_INVALID_ARG;
+  }
+  if (B < 1 || H < 1 || T < 1 || (long long)B * H > 65535) {
+    set_error("%s: need B, H, T >= 1 and B*H <= 65535 (got %d, %d, %d)", fn, B, H, T);
+    return LA_ERR_INVALID_ARG;
+  }
+  if ((dk != 64 && dk != 128) || (dv != 64 && dv != 128)) {
+    set_error("%s: dk and dv must be 64 or 128 (got %d, %d)", fn, dk, dv);
+    return LA_ERR_UNSUPPORTED;
+  }
+  const int kind = mode & 0xff;
+  if ((mode & ~(0xff | LA_F32)) != 0 || kind < LA_LINEAR || kind > LA_OUTER_GATE) {
+    set_error("%s: unknown mode 0x%x", fn, mode);
+    return LA_ERR_INVALID_ARG;
+  }
+  if (kind != LA_GDN || (mode & LA_F32)) {
+    set_error("%s: covers LA_GDN with bfloat16 inputs (got mode 0x%x)", fn, mode);
+    return LA_ERR_UNSUPPORTED;
+  }
+  if (dg_out && !g) {
+    set_error("%s: dg needs the log-gates g (NULL g means alpha = 1, which has no gradient)", fn);
+    return LA_ERR_INVALID_ARG;
+  }
+  if (C != 0 && C != 64) {
+    set_error("%s: chunk length C=%d is not implemented (use 0 or 64)", fn, C);
+    return LA_ERR_UNSUPPORTED;
+  }
+  const void *p16[] = {q, k, v, dO, dq_out, dk_out, dv_out};
+  for (const void *ptr : p16)
+    if (!al16(ptr)) {
+      set_error("%s: q, k, v, dO, dq, dk and dv must be 16-byte aligned", fn);
+      return LA_ERR_INVALID_ARG;
+    }
+  if ((S0 && !al16(S0)) || (dS_final && !al16(dS_final)) || (dS0 && !al16(dS0)) || (g && !al16(g)) ||
+      (beta && !al16(beta)) || (dg_out && !al16(dg_out)) || (dbeta_out && !al16(dbeta_out))) {
+    set_error("%s: g, beta, S0, dS_final, dS0, dg and dbeta must be 16-byte aligned", fn);
+    return LA_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int BH = B * H;
+  const size_t bytes = delta_bwd_workspace_bytes(BH, T, dk, dv);
+  cudaMemPool_t pool = library_pool();
+  if (!pool) {
+    set_error("%s: could not create the workspace pool: %s", fn, cudaGetErrorString(cudaGetLastError()));
+    return LA_ERR_CUDA;
+  }
+  uint8_t *ws = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&ws), bytes, pool, s);
+  if (e != cudaSuccess) {
+    set_error("%s: workspace allocation of %zu bytes failed: %s", fn, bytes, cudaGetErrorString(e));
+    return LA_ERR_CUDA;
+  }
+  using bf = __nv_bfloat16;
+  auto qb = static_cast<const bf *>(q), kb = static_cast<const bf *>(k), vb = static_cast<const bf *>(v),
+       ob = static_cast<const bf *>(dO);
+  auto dqb = static_cast<bf *>(dq_out), dkb = static_cast<bf *>(dk_out), dvb = static_cast<bf *>(dv_out);
+  int rc;
+  if (dk == 128 && dv == 128)
+    rc = launch_typed<128, 128>(qb, kb, vb, ob, g, beta, S0, dS_final, dqb, dkb, dvb, dbeta_out, dg_out, dS0, BH, T,
+                                ws, s);
+  else if (dk == 128)
+    rc = launch_typed<128, 64>(qb, kb, vb, ob, g, beta, S0, dS_final, dqb, dkb, dvb, dbeta_out, dg_out, dS0, BH, T,
+                               ws, s);
+  else if (dv == 128)
+    rc = launch_typed<64, 128>(qb, kb, vb, ob, g, beta, S0, dS_final, dqb, dkb, dvb, dbeta_out, dg_out, dS0, BH, T,
+                               ws, s);
+  else
+    rc = launch_typed<64, 64>(qb, kb, vb, ob, g, beta, S0, dS_final, dqb, dkb, dvb, dbeta_out, dg_out, dS0, BH, T,
+                              ws, s);
+  e = cudaFreeAsync(ws, s);
+  if (rc == LA_OK && e != cudaSuccess) {
+    set_error("%s: workspace release failed: %s", fn, cudaGetErrorString(e));
+    return LA_ERR_CUDA;
+  }
+  return rc;
+}

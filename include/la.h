@@ -21,7 +21,8 @@
  * non-causal form), la_chunk_fwd_noalloc (its materialised variant without
  * allocation), la_chunk_fwd_gdelta (the generalised delta rule
  * S_t = (I - b_t a_t^T) S_{t-1} + k_t v_t^T), la_chunk_bwd (the backward pass
- * for LA_LINEAR, LA_RETNET, LA_SCALAR_GATE and LA_GLA), la_recurrent_step
+ * for LA_LINEAR, LA_RETNET, LA_SCALAR_GATE and LA_GLA), la_chunk_bwd_delta
+ * (the backward pass for LA_GDN), la_recurrent_step
  * (one decode step), la_prologue (short convolution, L2 norm and gate
  * activations in front of the forward), la_stream_status, la_last_error,
  * la_version.
@@ -37,7 +38,8 @@
  *   - All pointers are DEVICE pointers owned by the caller. The library never
  *     frees or retains them. Device memory of its own is taken only by the
  *     materialised variant, the two-phase delta-rule variant and the
- *     non-causal form of la_chunk_fwd and by la_chunk_bwd: workspaces
+ *     non-causal form of la_chunk_fwd and by la_chunk_bwd and
+ *     la_chunk_bwd_delta: workspaces
  *     allocated and freed on `stream` from a
  *     library-owned stream-ordered pool (one per device) that keeps freed
  *     memory for the next call.
@@ -294,6 +296,47 @@ int la_chunk_bwd(const void *q, const void *k, const void *v, const float *g, co
                  const float *dS_final, const float *S0, void *dq_out, void *dk_out, void *dv_out,
                  float *dS0, float *dg_out, int B, int H, int T, int dk, int dv, int C, int mode,
                  la_stream_t stream);
+
+/*
+ * la_chunk_bwd_delta -- the backward pass of la_chunk_fwd for LA_GDN (Gated
+ * DeltaNet, bfloat16): given dO = dL/do and dS_final = dL/dS_final, the
+ * gradients of L through the recurrence
+ *
+ *   R_t = alpha_t S_{t-1},  r_t = v_t - R_t^T k_t,  S_t = R_t + beta_t k_t r_t^T,
+ *   o_t = S_t^T q_t
+ *
+ * ("LLM attention optimisation" page, Gated DeltaNet section; "Talk Linear
+ * Attention" section 6.2), i.e. with Gh_t = dL/dS_t (later tokens and o_t):
+ *
+ *   dq_t = S_t dO_t,  dv_t = beta_t Gh_t^T k_t,  dbeta_t = (Gh_t^T k_t) . r_t,
+ *   dk_t = beta_t (Gh_t r_t - R_t Gh_t^T k_t),
+ *   dg_t = <(I - beta_t k_t k_t^T) Gh_t, R_t>,  dS0 = dL/dS_{-1}.
+ *
+ * Chunkwise (C = 64) through the WY form of the forward: the chunk states and
+ * the state gradients at the chunk boundaries are recomputed by two serial
+ * passes ("Talk Linear Attention" section 4.1.2), then every chunk's
+ * gradients are computed in parallel; float32 arithmetic on tf32 warp MMAs.
+ *
+ *   q, k, v, g, beta, S0  as passed to la_chunk_fwd for LA_GDN (g NULL: alpha
+ *            = 1; beta NULL: beta = 1; S0 NULL: zero); bfloat16 q, k, v
+ *   dO       [B][H][T][dv] bfloat16; dS_final float32 [B][H][dk][dv] or NULL (zero)
+ *   dq_out, dk_out [B][H][T][dk]; dv_out [B][H][T][dv]: bfloat16 outputs
+ *   dbeta_out float32 [B][H][T] or NULL (not written; with beta NULL it is the
+ *            gradient at beta = 1)
+ *   dg_out   float32 [B][H][T] or NULL; needs g (LA_ERR_INVALID_ARG otherwise)
+ *   dS0      float32 [B][H][dk][dv] or NULL
+ *   mode     LA_GDN (anything else: LA_ERR_UNSUPPORTED for a known mode or
+ *            LA_F32, LA_ERR_INVALID_ARG for an unknown one); C = 0 or 64
+ *   16-byte alignment for every pointer; B*H <= 65535.
+ * Workspace from the library's pool: B*H*ceil(T/64)*(2*64*64 + 2*dk*dv)*4
+ * bytes (the triangular inverses and masked scores of every chunk, and the
+ * states and state gradients at the chunk boundaries). Four kernels on
+ * `stream`; errors as la_chunk_fwd.
+ */
+int la_chunk_bwd_delta(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                       const void *dO, const float *dS_final, const float *S0, void *dq_out, void *dk_out,
+                       void *dv_out, float *dbeta_out, float *dg_out, float *dS0, int B, int H, int T,
+                       int dk, int dv, int C, int mode, la_stream_t stream);
 
 /*
  * la_chunk_fwd_gdelta -- causal forward of the generalised delta rule, an

@@ -31,7 +31,7 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     assert names == sorted(["la_chunk_fwd", "la_chunk_fwd_noalloc", "la_chunk_fwd_gdelta", "la_chunk_bwd",
-                            "la_recurrent_step", "la_prologue", "la_stream_status", "la_last_error",
+                            "la_chunk_bwd_delta", "la_recurrent_step", "la_prologue", "la_stream_status", "la_last_error",
                             "la_version"])
     assert set(names) == set(la.SIGNATURES)
 
@@ -245,3 +245,38 @@ def test_gdelta_rejects_bad_arguments(lib, kw, code):
     rc = la.la_chunk_fwd_gdelta(**args)
     assert rc == la.CONSTANTS[code], (rc, la.la_last_error())
     assert la.la_last_error().startswith("la_chunk_fwd_gdelta:")
+
+
+def _bwd_delta(**kw):
+    args = dict(q=A, k=A, v=A, g=A, beta=A, dO=A, dS_final=None, S0=None, dq_out=A, dk_out=A, dv_out=A,
+                dbeta_out=A, dg_out=A, dS0=None, B=1, H=1, T=64, dk=128, dv=128, C=0, mode=la.LA_GDN, stream=None)
+    args.update(kw)
+    rc = la.la_chunk_bwd_delta(**args)
+    return rc, la.la_last_error()
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), "LA_ERR_INVALID_ARG"),
+    (dict(dO=None), "LA_ERR_INVALID_ARG"),
+    (dict(dv_out=None), "LA_ERR_INVALID_ARG"),
+    (dict(T=0), "LA_ERR_INVALID_ARG"),
+    (dict(B=65536), "LA_ERR_INVALID_ARG"),
+    (dict(dk=96), "LA_ERR_UNSUPPORTED"),
+    (dict(mode=la.LA_KDA), "LA_ERR_UNSUPPORTED"),         # the delta rule with per-channel gates: not built
+    (dict(mode=la.LA_RETNET), "LA_ERR_UNSUPPORTED"),      # la_chunk_bwd covers the unit-write modes
+    (dict(mode=la.LA_GDN | la.LA_F32), "LA_ERR_UNSUPPORTED"),
+    (dict(mode=9), "LA_ERR_INVALID_ARG"),
+    (dict(mode=la.LA_GDN | 0x400), "LA_ERR_INVALID_ARG"),
+    (dict(C=128), "LA_ERR_UNSUPPORTED"),
+    (dict(C=32), "LA_ERR_UNSUPPORTED"),
+    (dict(g=None), "LA_ERR_INVALID_ARG"),                  # dg requested without gates
+    (dict(q=A + 8), "LA_ERR_INVALID_ARG"),
+    (dict(dq_out=A + 2), "LA_ERR_INVALID_ARG"),
+    (dict(beta=A + 4), "LA_ERR_INVALID_ARG"),
+    (dict(dbeta_out=A + 4), "LA_ERR_INVALID_ARG"),
+    (dict(S0=A + 4), "LA_ERR_INVALID_ARG"),
+])
+def test_chunk_bwd_delta_rejects_bad_arguments(lib, kw, code):
+    rc, msg = _bwd_delta(**kw)
+    assert rc == la.CONSTANTS[code], (rc, msg)
+    assert msg.startswith("la_chunk_bwd_delta")

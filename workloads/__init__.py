@@ -98,6 +98,10 @@ WORKLOADS = {
     # gla q/k/v and gate recipe, dO and dS_final as for the backward workload.
     "backward_gla": Workload("backward_gla", "gla", 8, 16, 4096, 128, 128, "bf16", 64, seed=14,
                              qkv_scale=1.0 / math.sqrt(128.0), extra={"backward": True}),
+    # Backward of Gated DeltaNet (dq, dk, dv, dbeta, dg, dS0): the gdn shape and
+    # q/k/v/gate/beta recipe, dO and dS_final as for the backward workload.
+    "backward_gdn": Workload("backward_gdn", "gdn", 4, 16, 16384, 128, 128, "bf16", 64, seed=15,
+                             l2norm_qk=True, s0=True, extra={"backward": True}),
     # Outer-product gate alpha_t beta_t^T (a next row): the GLA shape and q/k/v
     # recipe with GLA-distributed log-gates on both the key and the value axis.
     "outer": Workload("outer", "outer", 8, 16, 8192, 128, 128, "bf16", 64, seed=11,
