@@ -50,7 +50,7 @@ namespace {
 
 using wy::mma_16x8x8_tf32;
 using wy::to_tf32;
-using tc::unpack8;
+using sm100::smem_u32;
 
 constexpr int kCh = 64;        // chunk length
 constexpr int kCW = 16;        // value columns per block
@@ -71,7 +71,7 @@ __device__ __forceinline__ uint32_t tf(float x) { return to_tf32(x); }
 template <int NT, class GA, class GB>
 __device__ __forceinline__ void wmma(float (&acc)[NT][4], int m0, int n0, int K, GA ga, GB gb, int lane) {
   const int g = lane >> 2, t = lane & 3;
-#pragma unroll 2
+#pragma unroll
   for (int k0 = 0; k0 < K; k0 += 8) {
     uint32_t a[4] = {ga(m0 + g, k0 + t), ga(m0 + g + 8, k0 + t), ga(m0 + g, k0 + t + 4),
                      ga(m0 + g + 8, k0 + t + 4)};
@@ -100,19 +100,28 @@ __device__ __forceinline__ void zero(float (&acc)[NT][4]) {
   for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 }
 
-// Per-chunk scalars, by warp 0: gamma_r = e^{b_r}, e^{bL - b_r}, beta_r and b_r
-// (b the inclusive prefix of the chunk's log-gates); rows past the end get
-// zero gates and beta = 0.
+// Per-chunk scalars: gamma_r = e^{b_r}, e^{bL - b_r}, beta_r and b_r (b the
+// inclusive prefix of the chunk's log-gates); rows past the end get zero gates
+// and beta = 0. One warp: gate_loads issues the loads (two rows per lane),
+// gate_scan forms the prefix when they are needed.
 struct Scal {
   float gam[kCh], glr[kCh], bet[kCh], b[kCh];
 };
-__device__ __forceinline__ void chunk_scalars(Scal &s, const float *g, const float *beta, size_t base, int n,
-                                              int lane) {
-  float x0 = 0.f, x1 = 0.f;
+struct Gates {
+  float x0, x1, b0, b1;
+};
+__device__ __forceinline__ Gates gate_loads(const float *g, const float *beta, size_t base, int n, int lane) {
+  Gates r{0.f, 0.f, 0.f, 0.f};
   if (g) {
-    if (lane < n) x0 = __ldg(g + base + lane);
-    if (lane + 32 < n) x1 = __ldg(g + base + lane + 32);
+    if (lane < n) r.x0 = __ldg(g + base + lane);
+    if (lane + 32 < n) r.x1 = __ldg(g + base + lane + 32);
   }
+  r.b0 = lane < n ? (beta ? __ldg(beta + base + lane) : 1.f) : 0.f;
+  r.b1 = lane + 32 < n ? (beta ? __ldg(beta + base + lane + 32) : 1.f) : 0.f;
+  return r;
+}
+__device__ __forceinline__ void gate_scan(Scal &s, Gates gt, int lane) {
+  float x0 = gt.x0, x1 = gt.x1;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const float a0 = __shfl_up_sync(0xffffffffu, x0, off), a1 = __shfl_up_sync(0xffffffffu, x1, off);
@@ -129,42 +138,55 @@ __device__ __forceinline__ void chunk_scalars(Scal &s, const float *g, const flo
   s.gam[lane + 32] = __expf(x1);
   s.glr[lane] = __expf(bl - x0);
   s.glr[lane + 32] = __expf(bl - x1);
-  s.bet[lane] = lane < n ? (beta ? __ldg(beta + base + lane) : 1.f) : 0.f;
-  s.bet[lane + 32] = lane + 32 < n ? (beta ? __ldg(beta + base + lane + 32) : 1.f) : 0.f;
+  s.bet[lane] = gt.b0;
+  s.bet[lane + 32] = gt.b1;
 }
 
-// rows [0, 64) of a [T][D] bf16 tensor from token t0 (n valid, zero beyond) into a tile of pitch P
+// ---- asynchronous tile copies (16 bytes each; a copy of 0 source bytes fills zeros)
+constexpr int kPh = kCW + 8;  // row pitch (bf16) of x 16 bf16 tiles: 48-byte rows
+
+__device__ __forceinline__ void cpa16(void *dst, const void *src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(valid ? 16u : 0u)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// rows [0, 64) of a [T][D] bf16 tensor from the chunk's first token (n valid, zero beyond), pitch P
 template <int D, int P>
-__device__ __forceinline__ void load_rows_bf16(__nv_bfloat16 *dst, const __nv_bfloat16 *src, int n, int tid,
-                                               int nthr) {
+__device__ __forceinline__ void rows_async(__nv_bfloat16 *dst, const __nv_bfloat16 *src, int n, int tid, int nthr) {
   for (int i = tid; i < kCh * (D / 8); i += nthr) {
     const int r = i / (D / 8), c = (i % (D / 8)) * 8;
-    uint4 u = make_uint4(0, 0, 0, 0);
-    if (r < n) u = *reinterpret_cast<const uint4 *>(src + (size_t)r * D + c);
-    *reinterpret_cast<uint4 *>(dst + r * P + c) = u;
+    const bool ok = r < n;
+    cpa16(dst + r * P + c, src + (ok ? (size_t)r * D + c : 0), ok);
   }
 }
-// 64 x 16 columns [c0, c0 + 16) of a [T][D] bf16 tensor as float32 (pitch kPw)
+// the 64 x 16 columns [c0, c0 + 16) of a [T][D] bf16 tensor, pitch kPh
 template <int D>
-__device__ __forceinline__ void load_cols_f32(float *dst, const __nv_bfloat16 *src, int c0, int n, int tid,
-                                              int nthr) {
+__device__ __forceinline__ void cols_async(__nv_bfloat16 *dst, const __nv_bfloat16 *src, int c0, int n, int tid,
+                                           int nthr) {
   for (int i = tid; i < kCh * 2; i += nthr) {
     const int r = i >> 1, c = (i & 1) * 8;
-    uint4 u = make_uint4(0, 0, 0, 0);
-    if (r < n) u = *reinterpret_cast<const uint4 *>(src + (size_t)r * D + c0 + c);
-    float f[8];
-    unpack8(u, f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) dst[r * kPw + c + e] = f[e];
+    const bool ok = r < n;
+    cpa16(dst + r * kPh + c, src + (ok ? (size_t)r * D + c0 + c : 0), ok);
   }
 }
-// a 64 x 64 float32 matrix (row-major, contiguous) into a tile of pitch kPf
-__device__ __forceinline__ void load_cc(float *dst, const float *src, int tid, int nthr) {
-  for (int i = tid; i < kCh * kCh / 4; i += nthr) {
-    const int r = i >> 4, c = (i & 15) * 4;
-    *reinterpret_cast<float4 *>(dst + r * kPf + c) = __ldg(reinterpret_cast<const float4 *>(src) + i);
+// a 64 x 64 float32 matrix (row-major, contiguous), pitch kPf
+__device__ __forceinline__ void cc_async(float *dst, const float *src, int tid, int nthr) {
+  for (int i = tid; i < kCh * kCh / 4; i += nthr) cpa16(dst + (i >> 4) * kPf + (i & 15) * 4, src + 4 * i, true);
+}
+// the D x 16 columns [c0, c0 + 16) of a [D][DV] float32 matrix, pitch kPw
+template <int D, int DV>
+__device__ __forceinline__ void state_async(float *dst, const float *src, int c0, int tid, int nthr) {
+  for (int i = tid; i < D * 4; i += nthr) {
+    const int r = i >> 2, c = (i & 3) * 4;
+    cpa16(dst + r * kPw + c, src + (size_t)r * DV + c0 + c, true);
   }
 }
+__device__ __forceinline__ float bf(const __nv_bfloat16 *p) { return __uint_as_float(bfbits(p)); }
 
 // ============================================================ pre-pass
 template <int DK>
@@ -186,9 +208,11 @@ __global__ void __launch_bounds__(128) bd_pre_kernel(const __nv_bfloat16 *__rest
   const int i = blockIdx.x, bh = blockIdx.y, nch = gridDim.x;
   const int t0 = i * kCh, n = min(kCh, T - t0);
   const size_t row0 = (size_t)bh * T + t0;
-  load_rows_bf16<DK, PH>(sm.q, q + row0 * DK, n, tid, 128);
-  load_rows_bf16<DK, PH>(sm.k, k + row0 * DK, n, tid, 128);
-  if (warp == 0) chunk_scalars(sm.s, g, beta, row0, n, lane);
+  rows_async<DK, PH>(sm.q, q + row0 * DK, n, tid, 128);
+  rows_async<DK, PH>(sm.k, k + row0 * DK, n, tid, 128);
+  cp_commit();
+  if (warp == 0) gate_scan(sm.s, gate_loads(g, beta, row0, n, lane), lane);
+  cp_wait<0>();
   __syncthreads();
   // [Q; K] K^T: warps 0, 1 the rows of Q (P), warps 2, 3 the rows of K (A)
   const __nv_bfloat16 *src = warp < 2 ? sm.q : sm.k;
@@ -228,11 +252,17 @@ __global__ void __launch_bounds__(128) bd_pre_kernel(const __nv_bfloat16 *__rest
 }
 
 // ============================================================ state chain
+// Double-buffered: the next chunk's k, v and T land while this chunk computes.
+template <int DK>
+struct FwdBuf {
+  __nv_bfloat16 k[kCh * Pitch<DK>::h], v[kCh * kPh];
+  float t[kCh * kPf];
+};
 template <int DK>
 struct FwdSmem {
-  __nv_bfloat16 k[kCh * Pitch<DK>::h];
-  float v[kCh * kPw], t[kCh * kPf], s[DK * kPw], z[kCh * kPw], u[kCh * kPw];
-  Scal sc;
+  FwdBuf<DK> buf[2];
+  float s[DK * kPw], z[kCh * kPw], u[kCh * kPw];
+  Scal sc[2];
 };
 
 template <int DK, int DV>
@@ -247,6 +277,15 @@ __global__ void __launch_bounds__(128) bd_fwd_kernel(const __nv_bfloat16 *__rest
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x / NCB, c0 = (blockIdx.x % NCB) * kCW;
   const int nch = (T + kCh - 1) / kCh;
+  auto issue = [&](int i, FwdBuf<DK> &b) {
+    const int t0 = i * kCh, n = min(kCh, T - t0);
+    const size_t row0 = (size_t)bh * T + t0;
+    rows_async<DK, PH>(b.k, k + row0 * DK, n, tid, 128);
+    cols_async<DV>(b.v, v + row0 * DV, c0, n, tid, 128);
+    cc_async(b.t, Tw + ((size_t)bh * nch + i) * kCh * kCh, tid, 128);
+    cp_commit();
+  };
+  auto gates = [&](int i) { return gate_loads(g, beta, (size_t)bh * T + i * kCh, min(kCh, T - i * kCh), lane); };
   // S[:, c0 .. c0 + 16) in registers: warp w holds row tiles w + 4 rt
   float S[RT][2][4];
 #pragma unroll
@@ -256,13 +295,19 @@ __global__ void __launch_bounds__(128) bd_fwd_kernel(const __nv_bfloat16 *__rest
       each(S[rt], 16 * (warp + 4 * rt), 0, lane,
            [&](int r, int c, float &x) { x = __ldg(S0 + ((size_t)bh * DK + r) * DV + c0 + c); });
   }
+  issue(0, sm.buf[0]);
+  if (warp == 0) gate_scan(sm.sc[0], gates(0), lane);
   for (int i = 0; i < nch; ++i) {
-    const int t0 = i * kCh, n = min(kCh, T - t0);
-    const size_t row0 = (size_t)bh * T + t0;
-    load_rows_bf16<DK, PH>(sm.k, k + row0 * DK, n, tid, 128);
-    load_cols_f32<DV>(sm.v, v + row0 * DV, c0, n, tid, 128);
-    load_cc(sm.t, Tw + ((size_t)bh * nch + i) * kCh * kCh, tid, 128);
-    if (warp == 0) chunk_scalars(sm.sc, g, beta, row0, n, lane);
+    FwdBuf<DK> &b = sm.buf[i & 1];
+    const Scal &sc = sm.sc[i & 1];
+    Gates nxt{};
+    if (i + 1 < nch) {
+      issue(i + 1, sm.buf[(i + 1) & 1]);
+      if (warp == 0) nxt = gates(i + 1);
+      cp_wait<1>();
+    } else {
+      cp_wait<0>();
+    }
     float *sout = Sin + ((size_t)bh * nch + i) * DK * DV;
 #pragma unroll
     for (int rt = 0; rt < RT; ++rt)
@@ -275,10 +320,10 @@ __global__ void __launch_bounds__(128) bd_fwd_kernel(const __nv_bfloat16 *__rest
     {
       float a[2][4];
       zero(a);
-      wmma(a, 16 * warp, 0, DK, [&](int m, int kk) { return bfbits(sm.k + m * PH + kk); },
+      wmma(a, 16 * warp, 0, DK, [&](int m, int kk) { return bfbits(b.k + m * PH + kk); },
            [&](int kk, int nn) { return tf(sm.s[kk * kPw + nn]); }, lane);
       each(a, 16 * warp, 0, lane, [&](int r, int c, float &x) {
-        sm.z[r * kPw + c] = sm.sc.bet[r] * (sm.v[r * kPw + c] - sm.sc.gam[r] * x);
+        sm.z[r * kPw + c] = sc.bet[r] * (bf(b.v + r * kPh + c) - sc.gam[r] * x);
       });
     }
     __syncthreads();
@@ -286,29 +331,32 @@ __global__ void __launch_bounds__(128) bd_fwd_kernel(const __nv_bfloat16 *__rest
     {
       float a[2][4];
       zero(a);
-      wmma(a, 16 * warp, 0, kCh, [&](int m, int kk) { return tf(sm.t[m * kPf + kk]); },
+      wmma(a, 16 * warp, 0, kCh, [&](int m, int kk) { return tf(b.t[m * kPf + kk]); },
            [&](int kk, int nn) { return tf(sm.z[kk * kPw + nn]); }, lane);
-      each(a, 16 * warp, 0, lane, [&](int r, int c, float &x) { sm.u[r * kPw + c] = sm.sc.glr[r] * x; });
+      each(a, 16 * warp, 0, lane, [&](int r, int c, float &x) { sm.u[r * kPw + c] = sc.glr[r] * x; });
     }
     __syncthreads();
     // S <- gL S + K^T U'
-    const float gL = sm.sc.gam[kCh - 1];
+    const float gL = sc.gam[kCh - 1];
 #pragma unroll
     for (int rt = 0; rt < RT; ++rt) {
       each(S[rt], 0, 0, lane, [&](int, int, float &x) { x *= gL; });
-      wmma(S[rt], 16 * (warp + 4 * rt), 0, kCh, [&](int m, int kk) { return bfbits(sm.k + kk * PH + m); },
+      wmma(S[rt], 16 * (warp + 4 * rt), 0, kCh, [&](int m, int kk) { return bfbits(b.k + kk * PH + m); },
            [&](int kk, int nn) { return tf(sm.u[kk * kPw + nn]); }, lane);
     }
+    if (warp == 0 && i + 1 < nch) gate_scan(sm.sc[(i + 1) & 1], nxt, lane);
     __syncthreads();
   }
 }
 
 // ============================================================ gradient chain
+// The next chunk's T and P are fetched once this chunk's last use of them is
+// past (the solve), its q, k, dO at the chunk's end.
 template <int DK>
 struct BwdSmem {
-  __nv_bfloat16 q[kCh * Pitch<DK>::h], k[kCh * Pitch<DK>::h];
-  float o[kCh * kPw], t[kCh * kPf], p[kCh * kPf], e[DK * kPw], du[kCh * kPw], y[kCh * kPw];
-  Scal sc;
+  __nv_bfloat16 q[kCh * Pitch<DK>::h], k[kCh * Pitch<DK>::h], o[kCh * kPh];
+  float t[kCh * kPf], p[kCh * kPf], e[DK * kPw], du[kCh * kPw], y[kCh * kPw];
+  Scal sc[2];
 };
 
 template <int DK, int DV>
@@ -325,6 +373,20 @@ __global__ void __launch_bounds__(128) bd_bwd_kernel(const __nv_bfloat16 *__rest
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x / NCB, c0 = (blockIdx.x % NCB) * kCW;
   const int nch = (T + kCh - 1) / kCh;
+  auto issue_tp = [&](int i) {
+    cc_async(sm.t, Tw + ((size_t)bh * nch + i) * kCh * kCh, tid, 128);
+    cc_async(sm.p, Pw + ((size_t)bh * nch + i) * kCh * kCh, tid, 128);
+    cp_commit();
+  };
+  auto issue_qko = [&](int i) {
+    const int t0 = i * kCh, n = min(kCh, T - t0);
+    const size_t row0 = (size_t)bh * T + t0;
+    rows_async<DK, PH>(sm.q, q + row0 * DK, n, tid, 128);
+    rows_async<DK, PH>(sm.k, k + row0 * DK, n, tid, 128);
+    cols_async<DV>(sm.o, dO + row0 * DV, c0, n, tid, 128);
+    cp_commit();
+  };
+  auto gates = [&](int i) { return gate_loads(g, beta, (size_t)bh * T + i * kCh, min(kCh, T - i * kCh), lane); };
   float E[RT][2][4];
 #pragma unroll
   for (int rt = 0; rt < RT; ++rt) {
@@ -333,15 +395,14 @@ __global__ void __launch_bounds__(128) bd_bwd_kernel(const __nv_bfloat16 *__rest
       each(E[rt], 16 * (warp + 4 * rt), 0, lane,
            [&](int r, int c, float &x) { x = __ldg(dS + ((size_t)bh * DK + r) * DV + c0 + c); });
   }
+  issue_tp(nch - 1);
+  issue_qko(nch - 1);
+  if (warp == 0) gate_scan(sm.sc[(nch - 1) & 1], gates(nch - 1), lane);
   for (int i = nch - 1; i >= 0; --i) {
-    const int t0 = i * kCh, n = min(kCh, T - t0);
-    const size_t row0 = (size_t)bh * T + t0;
-    load_rows_bf16<DK, PH>(sm.q, q + row0 * DK, n, tid, 128);
-    load_rows_bf16<DK, PH>(sm.k, k + row0 * DK, n, tid, 128);
-    load_cols_f32<DV>(sm.o, dO + row0 * DV, c0, n, tid, 128);
-    load_cc(sm.t, Tw + ((size_t)bh * nch + i) * kCh * kCh, tid, 128);
-    load_cc(sm.p, Pw + ((size_t)bh * nch + i) * kCh * kCh, tid, 128);
-    if (warp == 0) chunk_scalars(sm.sc, g, beta, row0, n, lane);
+    const Scal &sc = sm.sc[i & 1];
+    Gates nxt{};
+    if (warp == 0 && i > 0) nxt = gates(i - 1);
+    cp_wait<0>();
     float *eout = Eout + ((size_t)bh * nch + i) * DK * DV;
 #pragma unroll
     for (int rt = 0; rt < RT; ++rt)
@@ -356,9 +417,9 @@ __global__ void __launch_bounds__(128) bd_bwd_kernel(const __nv_bfloat16 *__rest
       zero(a);
       wmma(a, 16 * warp, 0, DK, [&](int m, int kk) { return bfbits(sm.k + m * PH + kk); },
            [&](int kk, int nn) { return tf(sm.e[kk * kPw + nn]); }, lane);
-      each(a, 16 * warp, 0, lane, [&](int r, int, float &x) { x *= sm.sc.glr[r]; });
+      each(a, 16 * warp, 0, lane, [&](int r, int, float &x) { x *= sc.glr[r]; });
       wmma(a, 16 * warp, 0, kCh, [&](int m, int kk) { return tf(sm.p[kk * kPf + m]); },
-           [&](int kk, int nn) { return tf(sm.o[kk * kPw + nn]); }, lane);
+           [&](int kk, int nn) { return bfbits(sm.o + kk * kPh + nn); }, lane);
       each(a, 16 * warp, 0, lane, [&](int r, int c, float &x) { sm.du[r * kPw + c] = x; });
     }
     __syncthreads();
@@ -369,21 +430,24 @@ __global__ void __launch_bounds__(128) bd_bwd_kernel(const __nv_bfloat16 *__rest
       wmma(a, 16 * warp, 0, kCh, [&](int m, int kk) { return tf(sm.t[kk * kPf + m]); },
            [&](int kk, int nn) { return tf(sm.du[kk * kPw + nn]); }, lane);
       each(a, 16 * warp, 0, lane,
-           [&](int r, int c, float &x) { sm.y[r * kPw + c] = -sm.sc.gam[r] * sm.sc.bet[r] * x; });
+           [&](int r, int c, float &x) { sm.y[r * kPw + c] = -sc.gam[r] * sc.bet[r] * x; });
     }
     __syncthreads();
+    if (i > 0) issue_tp(i - 1);  // T and P of this chunk are no longer read
     // E <- gL E + Q^T Diag(gamma) dO - K^T Diag(gamma) dZ
-    const float gL = sm.sc.gam[kCh - 1];
+    const float gL = sc.gam[kCh - 1];
 #pragma unroll
     for (int rt = 0; rt < RT; ++rt) {
       const int m0 = 16 * (warp + 4 * rt);
       each(E[rt], 0, 0, lane, [&](int, int, float &x) { x *= gL; });
       wmma(E[rt], m0, 0, kCh, [&](int m, int kk) { return bfbits(sm.q + kk * PH + m); },
-           [&](int kk, int nn) { return tf(sm.sc.gam[kk] * sm.o[kk * kPw + nn]); }, lane);
+           [&](int kk, int nn) { return tf(sc.gam[kk] * bf(sm.o + kk * kPh + nn)); }, lane);
       wmma(E[rt], m0, 0, kCh, [&](int m, int kk) { return bfbits(sm.k + kk * PH + m); },
            [&](int kk, int nn) { return tf(sm.y[kk * kPw + nn]); }, lane);
     }
+    if (warp == 0 && i > 0) gate_scan(sm.sc[(i - 1) & 1], nxt, lane);
     __syncthreads();
+    if (i > 0) issue_qko(i - 1);
   }
   if (dS0) {
 #pragma unroll
@@ -394,13 +458,20 @@ __global__ void __launch_bounds__(128) bd_bwd_kernel(const __nv_bfloat16 *__rest
 }
 
 // ============================================================ gradients
+// One CTA per chunk; the value axis in blocks of 16 columns, double-buffered:
+// the next block's S, E (float32) and v, dO columns land while this one computes.
+template <int DK>
+struct GradBlk {
+  float s[DK * kPw], e[DK * kPw];
+  __nv_bfloat16 v[kCh * kPh], o[kCh * kPh];
+};
 template <int DK>
 struct GradSmem {
   __nv_bfloat16 q[kCh * Pitch<DK>::h], k[kCh * Pitch<DK>::h];
   float t[kCh * kPf], p[kCh * kPf];
   union {
-    struct {  // one block of 16 value columns
-      float s[DK * kPw], e[DK * kPw], v[kCh * kPw], o[kCh * kPw];
+    struct {
+      GradBlk<DK> b[2];
       float ks[kCh * kPw], qs[kCh * kPw], ke[kCh * kPw], z[kCh * kPw], u[kCh * kPw], du[kCh * kPw],
           y[kCh * kPw];
     } blk;
@@ -411,6 +482,22 @@ struct GradSmem {
   Scal sc;
   float db[kCh], dbeta[kCh], kd[kCh], red[8];
 };
+
+// acc_a += A B1, acc_b += A B2 with one A fragment per k step
+template <class GA, class GB1, class GB2>
+__device__ __forceinline__ void wmma2(float (&acc_a)[1][4], float (&acc_b)[1][4], int m0, int n0, int K, GA ga,
+                                      GB1 gb1, GB2 gb2, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int k0 = 0; k0 < K; k0 += 8) {
+    uint32_t a[4] = {ga(m0 + g, k0 + t), ga(m0 + g + 8, k0 + t), ga(m0 + g, k0 + t + 4),
+                     ga(m0 + g + 8, k0 + t + 4)};
+    uint32_t b1[2] = {gb1(k0 + t, n0 + g), gb1(k0 + t + 4, n0 + g)};
+    uint32_t b2[2] = {gb2(k0 + t, n0 + g), gb2(k0 + t + 4, n0 + g)};
+    mma_16x8x8_tf32(acc_a[0], a, b1);
+    mma_16x8x8_tf32(acc_b[0], a, b2);
+  }
+}
 
 template <int DK, int DV>
 __global__ void __launch_bounds__(256, 1) bd_grad_kernel(
@@ -427,11 +514,20 @@ __global__ void __launch_bounds__(256, 1) bd_grad_kernel(
   const int t0 = i * kCh, n = min(kCh, T - t0);
   const size_t row0 = (size_t)bh * T + t0;
   const size_t cbase = ((size_t)bh * nch + i) * kCh * kCh, sbase = ((size_t)bh * nch + i) * DK * DV;
-  load_rows_bf16<DK, PH>(sm.q, q + row0 * DK, n, tid, 256);
-  load_rows_bf16<DK, PH>(sm.k, k + row0 * DK, n, tid, 256);
-  load_cc(sm.t, Tw + cbase, tid, 256);
-  load_cc(sm.p, Pw + cbase, tid, 256);
-  if (warp == 0) chunk_scalars(sm.sc, g, beta, row0, n, lane);
+  auto& W = sm.w.blk;
+  auto issue_blk = [&](int c0, GradBlk<DK> &b) {
+    state_async<DK, DV>(b.s, Sin + sbase, c0, tid, 256);
+    state_async<DK, DV>(b.e, Eout + sbase, c0, tid, 256);
+    cols_async<DV>(b.v, v + row0 * DV, c0, n, tid, 256);
+    cols_async<DV>(b.o, dO + row0 * DV, c0, n, tid, 256);
+  };
+  rows_async<DK, PH>(sm.q, q + row0 * DK, n, tid, 256);
+  rows_async<DK, PH>(sm.k, k + row0 * DK, n, tid, 256);
+  cc_async(sm.t, Tw + cbase, tid, 256);
+  cc_async(sm.p, Pw + cbase, tid, 256);
+  issue_blk(0, W.b[0]);
+  cp_commit();
+  if (warp == 0) gate_scan(sm.sc, gate_loads(g, beta, row0, n, lane), lane);
   if (tid < kCh) {
     sm.db[tid] = 0.f;
     sm.dbeta[tid] = 0.f;
@@ -447,36 +543,31 @@ __global__ void __launch_bounds__(256, 1) bd_grad_kernel(
   zero(ap);
   float se = 0.f;  // <S, E> over this thread's share
   const int nc = 8 * half;  // x 16 tiles: warp w owns rows 16 (w & 3), columns 8 (w >> 2) .. + 8
-  auto& B = sm.w.blk;
-  __syncthreads();
-  for (int c0 = 0; c0 < DV; c0 += kCW) {
-    // ---- the block's S, E (float32) and V, dO columns
-    for (int x = tid; x < DK * kCW / 4; x += 256) {
-      const int r = x >> 2, c = (x & 3) * 4;
-      const float4 s4 = __ldg(reinterpret_cast<const float4 *>(Sin + sbase + (size_t)r * DV + c0 + c));
-      const float4 e4 = __ldg(reinterpret_cast<const float4 *>(Eout + sbase + (size_t)r * DV + c0 + c));
-      *reinterpret_cast<float4 *>(B.s + r * kPw + c) = s4;
-      *reinterpret_cast<float4 *>(B.e + r * kPw + c) = e4;
-      se += s4.x * e4.x + s4.y * e4.y + s4.z * e4.z + s4.w * e4.w;
+  for (int c0 = 0, cb = 0; c0 < DV; c0 += kCW, ++cb) {
+    GradBlk<DK> &B = W.b[cb & 1];
+    if (c0 + kCW < DV) {
+      issue_blk(c0 + kCW, W.b[(cb + 1) & 1]);
+      cp_commit();
+      cp_wait<1>();
+    } else {
+      cp_wait<0>();
     }
-    load_cols_f32<DV>(B.v, v + row0 * DV, c0, n, tid, 256);
-    load_cols_f32<DV>(B.o, dO + row0 * DV, c0, n, tid, 256);
     __syncthreads();
-    // ---- K S, Q S, Diag(gL / gamma) K E: one 16 x 8 tile each per warp
+    for (int x = tid; x < DK * kCW; x += 256) se += B.s[(x >> 4) * kPw + (x & 15)] * B.e[(x >> 4) * kPw + (x & 15)];
+    // ---- K S and Diag(gL / gamma) K E (one A fragment), Q S: one 16 x 8 tile each per warp
     {
       float a[1][4], b[1][4], c[1][4];
       zero(a);
       zero(b);
       zero(c);
-      wmma(a, mr, nc, DK, [&](int m, int kk) { return bfbits(sm.k + m * PH + kk); },
-           [&](int kk, int nn) { return tf(B.s[kk * kPw + nn]); }, lane);
+      wmma2(a, c, mr, nc, DK, [&](int m, int kk) { return bfbits(sm.k + m * PH + kk); },
+            [&](int kk, int nn) { return tf(B.s[kk * kPw + nn]); },
+            [&](int kk, int nn) { return tf(B.e[kk * kPw + nn]); }, lane);
       wmma(b, mr, nc, DK, [&](int m, int kk) { return bfbits(sm.q + m * PH + kk); },
            [&](int kk, int nn) { return tf(B.s[kk * kPw + nn]); }, lane);
-      wmma(c, mr, nc, DK, [&](int m, int kk) { return bfbits(sm.k + m * PH + kk); },
-           [&](int kk, int nn) { return tf(B.e[kk * kPw + nn]); }, lane);
-      each(a, mr, nc, lane, [&](int r, int cc, float &x) { B.ks[r * kPw + cc] = x; });
-      each(b, mr, nc, lane, [&](int r, int cc, float &x) { B.qs[r * kPw + cc] = x; });
-      each(c, mr, nc, lane, [&](int r, int cc, float &x) { B.ke[r * kPw + cc] = sm.sc.glr[r] * x; });
+      each(a, mr, nc, lane, [&](int r, int cc, float &x) { W.ks[r * kPw + cc] = x; });
+      each(b, mr, nc, lane, [&](int r, int cc, float &x) { W.qs[r * kPw + cc] = x; });
+      each(c, mr, nc, lane, [&](int r, int cc, float &x) { W.ke[r * kPw + cc] = sm.sc.glr[r] * x; });
     }
     __syncthreads();
     // ---- Z = V - Diag(gamma) K S; db += gamma dO . (Q S)
@@ -486,8 +577,8 @@ __global__ void __launch_bounds__(256, 1) bd_grad_kernel(
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int c = cq + e;
-        B.z[r * kPw + c] = B.v[r * kPw + c] - sm.sc.gam[r] * B.ks[r * kPw + c];
-        part += B.o[r * kPw + c] * B.qs[r * kPw + c];
+        W.z[r * kPw + c] = bf(B.v + r * kPh + c) - sm.sc.gam[r] * W.ks[r * kPw + c];
+        part += bf(B.o + r * kPh + c) * W.qs[r * kPw + c];
       }
       part += __shfl_xor_sync(0xffffffffu, part, 1);
       part += __shfl_xor_sync(0xffffffffu, part, 2);
@@ -499,12 +590,12 @@ __global__ void __launch_bounds__(256, 1) bd_grad_kernel(
       float a[1][4], b[1][4];
       zero(a);
       wmma(a, mr, nc, kCh, [&](int m, int kk) { return tf(sm.t[m * kPf + kk]); },
-           [&](int kk, int nn) { return tf(sm.sc.bet[kk] * B.z[kk * kPw + nn]); }, lane);
-      each(a, mr, nc, lane, [&](int r, int cc, float &x) { B.u[r * kPw + cc] = x; });
-      each(b, mr, nc, lane, [&](int r, int cc, float &x) { x = B.ke[r * kPw + cc]; });
+           [&](int kk, int nn) { return tf(sm.sc.bet[kk] * W.z[kk * kPw + nn]); }, lane);
+      each(a, mr, nc, lane, [&](int r, int cc, float &x) { W.u[r * kPw + cc] = x; });
+      each(b, mr, nc, lane, [&](int r, int cc, float &x) { x = W.ke[r * kPw + cc]; });
       wmma(b, mr, nc, kCh, [&](int m, int kk) { return tf(sm.p[kk * kPf + m]); },
-           [&](int kk, int nn) { return tf(B.o[kk * kPw + nn]); }, lane);
-      each(b, mr, nc, lane, [&](int r, int cc, float &x) { B.du[r * kPw + cc] = x; });
+           [&](int kk, int nn) { return bfbits(B.o + kk * kPh + nn); }, lane);
+      each(b, mr, nc, lane, [&](int r, int cc, float &x) { W.du[r * kPw + cc] = x; });
     }
     __syncthreads();
     // ---- Y = T^T dU; dV = Diag(beta) Y; dbeta += Y . Z; db -= gamma dZ . (K S); kd += U . (Kt E)
@@ -512,17 +603,17 @@ __global__ void __launch_bounds__(256, 1) bd_grad_kernel(
       float a[1][4];
       zero(a);
       wmma(a, mr, nc, kCh, [&](int m, int kk) { return tf(sm.t[kk * kPf + m]); },
-           [&](int kk, int nn) { return tf(B.du[kk * kPw + nn]); }, lane);
+           [&](int kk, int nn) { return tf(W.du[kk * kPw + nn]); }, lane);
       const int gg = lane >> 2;
       float pb[2] = {0.f, 0.f}, pd[2] = {0.f, 0.f}, pk[2] = {0.f, 0.f};
       each(a, mr, nc, lane, [&](int r, int cc, float &y) {
         const int h = (r - mr - gg) >> 3;  // 0: row g, 1: row g + 8
-        B.y[r * kPw + cc] = y;
+        W.y[r * kPw + cc] = y;
         const float dz = sm.sc.bet[r] * y;
         if (r < n) dv[(row0 + r) * DV + c0 + cc] = __float2bfloat16_rn(dz);
-        pb[h] += y * B.z[r * kPw + cc];
-        pd[h] += dz * B.ks[r * kPw + cc];
-        pk[h] += B.u[r * kPw + cc] * B.ke[r * kPw + cc];
+        pb[h] += y * W.z[r * kPw + cc];
+        pd[h] += dz * W.ks[r * kPw + cc];
+        pk[h] += W.u[r * kPw + cc] * W.ke[r * kPw + cc];
       });
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -543,15 +634,15 @@ __global__ void __launch_bounds__(256, 1) bd_grad_kernel(
     __syncthreads();
     // ---- dA -= Y U^T, dP += dO U^T, dQ += Diag(gamma) dO S^T,
     //      dK += -Diag(gamma beta) Y S^T + Diag(gL / gamma) U E^T (K = 16 each)
-    wmma(aa, mr, na, kCW, [&](int m, int kk) { return tf(-B.y[m * kPw + kk]); },
-         [&](int kk, int nn) { return tf(B.u[nn * kPw + kk]); }, lane);
-    wmma(ap, mr, na, kCW, [&](int m, int kk) { return tf(B.o[m * kPw + kk]); },
-         [&](int kk, int nn) { return tf(B.u[nn * kPw + kk]); }, lane);
-    wmma(aq, mr, nq, kCW, [&](int m, int kk) { return tf(sm.sc.gam[m] * B.o[m * kPw + kk]); },
+    wmma(aa, mr, na, kCW, [&](int m, int kk) { return tf(-W.y[m * kPw + kk]); },
+         [&](int kk, int nn) { return tf(W.u[nn * kPw + kk]); }, lane);
+    wmma(ap, mr, na, kCW, [&](int m, int kk) { return bfbits(B.o + m * kPh + kk); },
+         [&](int kk, int nn) { return tf(W.u[nn * kPw + kk]); }, lane);
+    wmma(aq, mr, nq, kCW, [&](int m, int kk) { return tf(sm.sc.gam[m] * bf(B.o + m * kPh + kk)); },
          [&](int kk, int nn) { return tf(B.s[nn * kPw + kk]); }, lane);
-    wmma(ak, mr, nq, kCW, [&](int m, int kk) { return tf(-sm.sc.gam[m] * sm.sc.bet[m] * B.y[m * kPw + kk]); },
+    wmma(ak, mr, nq, kCW, [&](int m, int kk) { return tf(-sm.sc.gam[m] * sm.sc.bet[m] * W.y[m * kPw + kk]); },
          [&](int kk, int nn) { return tf(B.s[nn * kPw + kk]); }, lane);
-    wmma(ak, mr, nq, kCW, [&](int m, int kk) { return tf(sm.sc.glr[m] * B.u[m * kPw + kk]); },
+    wmma(ak, mr, nq, kCW, [&](int m, int kk) { return tf(sm.sc.glr[m] * W.u[m * kPw + kk]); },
          [&](int kk, int nn) { return tf(B.e[nn * kPw + kk]); }, lane);
     __syncthreads();
   }
