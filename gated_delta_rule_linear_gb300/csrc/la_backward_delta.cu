@@ -54,8 +54,15 @@ using sm100::smem_u32;
 
 constexpr int kCh = 64;        // chunk length
 constexpr int kCW = 16;        // value columns per block
-constexpr int kPf = kCh + 4;   // row pitch (floats) of C x C tiles
-constexpr int kPw = kCW + 4;   // row pitch (floats) of x 16 tiles
+// float32 tiles are dense (64 or 16 floats a row) with the 16-byte groups of a
+// row permuted by an XOR of the row index, so that the tf32 fragment reads of
+// the warp MMAs -- by rows or by columns, as A or as B -- hit 32 distinct banks.
+constexpr int kPf = kCh;       // floats per row of C x C tiles
+constexpr int kPw = kCW;       // floats per row of x 16 tiles
+__host__ __device__ __forceinline__ int swz64(int r) { return ((r & 3) << 3) | (((r >> 2) & 1) << 2); }
+__host__ __device__ __forceinline__ int swz16(int r) { return (((r >> 1) & 1) << 3) | (((r >> 2) & 1) << 2); }
+__device__ __forceinline__ float &cc(float *p, int r, int c) { return p[r * kPf + (c ^ swz64(r))]; }
+__device__ __forceinline__ float &w16(float *p, int r, int c) { return p[r * kPw + (c ^ swz16(r))]; }
 template <int DK>
 struct Pitch {
   static constexpr int h = DK + 8;  // row pitch (bf16) of q / k tiles: 16-byte rows
@@ -68,9 +75,15 @@ __device__ __forceinline__ uint32_t tf(float x) { return to_tf32(x); }
 
 // acc[j] (the 16 x 8 tile at rows m0.., columns n0 + 8 j) += A[m0.., 0..K) B[0..K), ..]:
 // ga(m, k) and gb(k, n) return the tf32 bits of one element.
+// With one or two tiles the k steps alternate between two accumulator sets, so
+// consecutive MMAs do not wait on each other's results.
 template <int NT, class GA, class GB>
 __device__ __forceinline__ void wmma(float (&acc)[NT][4], int m0, int n0, int K, GA ga, GB gb, int lane) {
   const int g = lane >> 2, t = lane & 3;
+  constexpr bool split = NT <= 2;
+  float alt[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) alt[j][0] = alt[j][1] = alt[j][2] = alt[j][3] = 0.f;
 #pragma unroll
   for (int k0 = 0; k0 < K; k0 += 8) {
     uint32_t a[4] = {ga(m0 + g, k0 + t), ga(m0 + g + 8, k0 + t), ga(m0 + g, k0 + t + 4),
@@ -78,7 +91,16 @@ __device__ __forceinline__ void wmma(float (&acc)[NT][4], int m0, int n0, int K,
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
       uint32_t b[2] = {gb(k0 + t, n0 + 8 * j + g), gb(k0 + t + 4, n0 + 8 * j + g)};
-      mma_16x8x8_tf32(acc[j], a, b);
+      mma_16x8x8_tf32(split && (k0 & 8) ? alt[j] : acc[j], a, b);
+    }
+  }
+  if (split) {
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      acc[j][0] += alt[j][0];
+      acc[j][1] += alt[j][1];
+      acc[j][2] += alt[j][2];
+      acc[j][3] += alt[j][3];
     }
   }
 }
@@ -176,14 +198,17 @@ __device__ __forceinline__ void cols_async(__nv_bfloat16 *dst, const __nv_bfloat
 }
 // a 64 x 64 float32 matrix (row-major, contiguous), pitch kPf
 __device__ __forceinline__ void cc_async(float *dst, const float *src, int tid, int nthr) {
-  for (int i = tid; i < kCh * kCh / 4; i += nthr) cpa16(dst + (i >> 4) * kPf + (i & 15) * 4, src + 4 * i, true);
+  for (int i = tid; i < kCh * kCh / 4; i += nthr) {
+    const int r = i >> 4, c = (i & 15) * 4;
+    cpa16(dst + r * kPf + (c ^ swz64(r)), src + 4 * i, true);
+  }
 }
 // the D x 16 columns [c0, c0 + 16) of a [D][DV] float32 matrix, pitch kPw
 template <int D, int DV>
 __device__ __forceinline__ void state_async(float *dst, const float *src, int c0, int tid, int nthr) {
   for (int i = tid; i < D * 4; i += nthr) {
     const int r = i >> 2, c = (i & 3) * 4;
-    cpa16(dst + r * kPw + c, src + (size_t)r * DV + c0 + c, true);
+    cpa16(dst + r * kPw + (c ^ swz16(r)), src + (size_t)r * DV + c0 + c, true);
   }
 }
 __device__ __forceinline__ float bf(const __nv_bfloat16 *p) { return __uint_as_float(bfbits(p)); }
@@ -230,7 +255,7 @@ __global__ void __launch_bounds__(128) bd_pre_kernel(const __nv_bfloat16 *__rest
       });
     } else {
       each(acc[h], rbase + 16 * h, 0, lane, [&](int r, int s, float &v) {
-        sm.a[r * kPf + s] = s < r ? sm.s.bet[r] * __expf(sm.s.b[r] - sm.s.b[s]) * v : 0.f;
+        cc(sm.a, r, s) = s < r ? sm.s.bet[r] * __expf(sm.s.b[r] - sm.s.b[s]) * v : 0.f;
       });
     }
   }
@@ -243,7 +268,7 @@ __global__ void __launch_bounds__(128) bd_pre_kernel(const __nv_bfloat16 *__rest
     for (int r = 0; r < kCh; ++r) {
       float x = r == j ? 1.f : 0.f;
 #pragma unroll
-      for (int s = 0; s < r; ++s) x = fmaf(-sm.a[r * kPf + s], tc[s], x);
+      for (int s = 0; s < r; ++s) x = fmaf(-cc(sm.a, r, s), tc[s], x);
       tc[r] = r < j ? 0.f : x;
     }
 #pragma unroll
@@ -313,7 +338,7 @@ __global__ void __launch_bounds__(128) bd_fwd_kernel(const __nv_bfloat16 *__rest
     for (int rt = 0; rt < RT; ++rt)
       each(S[rt], 16 * (warp + 4 * rt), 0, lane, [&](int r, int c, float &x) {
         sout[(size_t)r * DV + c0 + c] = x;
-        sm.s[r * kPw + c] = x;
+        w16(sm.s, r, c) = x;
       });
     __syncthreads();
     // Z' = Diag(beta) (V - Diag(gamma) K S): warp w, rows 16 w
@@ -321,9 +346,9 @@ __global__ void __launch_bounds__(128) bd_fwd_kernel(const __nv_bfloat16 *__rest
       float a[2][4];
       zero(a);
       wmma(a, 16 * warp, 0, DK, [&](int m, int kk) { return bfbits(b.k + m * PH + kk); },
-           [&](int kk, int nn) { return tf(sm.s[kk * kPw + nn]); }, lane);
+           [&](int kk, int nn) { return tf(w16(sm.s, kk, nn)); }, lane);
       each(a, 16 * warp, 0, lane, [&](int r, int c, float &x) {
-        sm.z[r * kPw + c] = sc.bet[r] * (bf(b.v + r * kPh + c) - sc.gam[r] * x);
+        w16(sm.z, r, c) = sc.bet[r] * (bf(b.v + r * kPh + c) - sc.gam[r] * x);
       });
     }
     __syncthreads();
@@ -331,9 +356,9 @@ __global__ void __launch_bounds__(128) bd_fwd_kernel(const __nv_bfloat16 *__rest
     {
       float a[2][4];
       zero(a);
-      wmma(a, 16 * warp, 0, kCh, [&](int m, int kk) { return tf(b.t[m * kPf + kk]); },
-           [&](int kk, int nn) { return tf(sm.z[kk * kPw + nn]); }, lane);
-      each(a, 16 * warp, 0, lane, [&](int r, int c, float &x) { sm.u[r * kPw + c] = sc.glr[r] * x; });
+      wmma(a, 16 * warp, 0, kCh, [&](int m, int kk) { return tf(cc(b.t, m, kk)); },
+           [&](int kk, int nn) { return tf(w16(sm.z, kk, nn)); }, lane);
+      each(a, 16 * warp, 0, lane, [&](int r, int c, float &x) { w16(sm.u, r, c) = sc.glr[r] * x; });
     }
     __syncthreads();
     // S <- gL S + K^T U'
@@ -342,7 +367,7 @@ __global__ void __launch_bounds__(128) bd_fwd_kernel(const __nv_bfloat16 *__rest
     for (int rt = 0; rt < RT; ++rt) {
       each(S[rt], 0, 0, lane, [&](int, int, float &x) { x *= gL; });
       wmma(S[rt], 16 * (warp + 4 * rt), 0, kCh, [&](int m, int kk) { return bfbits(b.k + kk * PH + m); },
-           [&](int kk, int nn) { return tf(sm.u[kk * kPw + nn]); }, lane);
+           [&](int kk, int nn) { return tf(w16(sm.u, kk, nn)); }, lane);
     }
     if (warp == 0 && i + 1 < nch) gate_scan(sm.sc[(i + 1) & 1], nxt, lane);
     __syncthreads();
@@ -408,7 +433,7 @@ __global__ void __launch_bounds__(128) bd_bwd_kernel(const __nv_bfloat16 *__rest
     for (int rt = 0; rt < RT; ++rt)
       each(E[rt], 16 * (warp + 4 * rt), 0, lane, [&](int r, int c, float &x) {
         eout[(size_t)r * DV + c0 + c] = x;
-        sm.e[r * kPw + c] = x;
+        w16(sm.e, r, c) = x;
       });
     __syncthreads();
     // dU = Diag(gL / gamma) K E + P^T dO
@@ -416,21 +441,21 @@ __global__ void __launch_bounds__(128) bd_bwd_kernel(const __nv_bfloat16 *__rest
       float a[2][4];
       zero(a);
       wmma(a, 16 * warp, 0, DK, [&](int m, int kk) { return bfbits(sm.k + m * PH + kk); },
-           [&](int kk, int nn) { return tf(sm.e[kk * kPw + nn]); }, lane);
+           [&](int kk, int nn) { return tf(w16(sm.e, kk, nn)); }, lane);
       each(a, 16 * warp, 0, lane, [&](int r, int, float &x) { x *= sc.glr[r]; });
-      wmma(a, 16 * warp, 0, kCh, [&](int m, int kk) { return tf(sm.p[kk * kPf + m]); },
+      wmma(a, 16 * warp, 0, kCh, [&](int m, int kk) { return tf(cc(sm.p, kk, m)); },
            [&](int kk, int nn) { return bfbits(sm.o + kk * kPh + nn); }, lane);
-      each(a, 16 * warp, 0, lane, [&](int r, int c, float &x) { sm.du[r * kPw + c] = x; });
+      each(a, 16 * warp, 0, lane, [&](int r, int c, float &x) { w16(sm.du, r, c) = x; });
     }
     __syncthreads();
     // -Diag(gamma) dZ = -Diag(gamma beta) T^T dU
     {
       float a[2][4];
       zero(a);
-      wmma(a, 16 * warp, 0, kCh, [&](int m, int kk) { return tf(sm.t[kk * kPf + m]); },
-           [&](int kk, int nn) { return tf(sm.du[kk * kPw + nn]); }, lane);
+      wmma(a, 16 * warp, 0, kCh, [&](int m, int kk) { return tf(cc(sm.t, kk, m)); },
+           [&](int kk, int nn) { return tf(w16(sm.du, kk, nn)); }, lane);
       each(a, 16 * warp, 0, lane,
-           [&](int r, int c, float &x) { sm.y[r * kPw + c] = -sc.gam[r] * sc.bet[r] * x; });
+           [&](int r, int c, float &x) { w16(sm.y, r, c) = -sc.gam[r] * sc.bet[r] * x; });
     }
     __syncthreads();
     if (i > 0) issue_tp(i - 1);  // T and P of this chunk are no longer read
@@ -443,7 +468,7 @@ __global__ void __launch_bounds__(128) bd_bwd_kernel(const __nv_bfloat16 *__rest
       wmma(E[rt], m0, 0, kCh, [&](int m, int kk) { return bfbits(sm.q + kk * PH + m); },
            [&](int kk, int nn) { return tf(sc.gam[kk] * bf(sm.o + kk * kPh + nn)); }, lane);
       wmma(E[rt], m0, 0, kCh, [&](int m, int kk) { return bfbits(sm.k + kk * PH + m); },
-           [&](int kk, int nn) { return tf(sm.y[kk * kPw + nn]); }, lane);
+           [&](int kk, int nn) { return tf(w16(sm.y, kk, nn)); }, lane);
     }
     if (warp == 0 && i > 0) gate_scan(sm.sc[(i - 1) & 1], nxt, lane);
     __syncthreads();
@@ -488,14 +513,20 @@ template <class GA, class GB1, class GB2>
 __device__ __forceinline__ void wmma2(float (&acc_a)[1][4], float (&acc_b)[1][4], int m0, int n0, int K, GA ga,
                                       GB1 gb1, GB2 gb2, int lane) {
   const int g = lane >> 2, t = lane & 3;
+  float alt_a[4] = {0.f, 0.f, 0.f, 0.f}, alt_b[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int k0 = 0; k0 < K; k0 += 8) {
     uint32_t a[4] = {ga(m0 + g, k0 + t), ga(m0 + g + 8, k0 + t), ga(m0 + g, k0 + t + 4),
                      ga(m0 + g + 8, k0 + t + 4)};
     uint32_t b1[2] = {gb1(k0 + t, n0 + g), gb1(k0 + t + 4, n0 + g)};
     uint32_t b2[2] = {gb2(k0 + t, n0 + g), gb2(k0 + t + 4, n0 + g)};
-    mma_16x8x8_tf32(acc_a[0], a, b1);
-    mma_16x8x8_tf32(acc_b[0], a, b2);
+    mma_16x8x8_tf32((k0 & 8) ? alt_a : acc_a[0], a, b1);
+    mma_16x8x8_tf32((k0 & 8) ? alt_b : acc_b[0], a, b2);
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    acc_a[0][e] += alt_a[e];
+    acc_b[0][e] += alt_b[e];
   }
 }
 
@@ -553,7 +584,7 @@ __global__ void __launch_bounds__(256, 1) bd_grad_kernel(
       cp_wait<0>();
     }
     __syncthreads();
-    for (int x = tid; x < DK * kCW; x += 256) se += B.s[(x >> 4) * kPw + (x & 15)] * B.e[(x >> 4) * kPw + (x & 15)];
+    for (int x = tid; x < DK * kCW; x += 256) se += w16(B.s, (x >> 4), (x & 15)) * w16(B.e, (x >> 4), (x & 15));
     // ---- K S and Diag(gL / gamma) K E (one A fragment), Q S: one 16 x 8 tile each per warp
     {
       float a[1][4], b[1][4], c[1][4];
@@ -561,13 +592,13 @@ __global__ void __launch_bounds__(256, 1) bd_grad_kernel(
       zero(b);
       zero(c);
       wmma2(a, c, mr, nc, DK, [&](int m, int kk) { return bfbits(sm.k + m * PH + kk); },
-            [&](int kk, int nn) { return tf(B.s[kk * kPw + nn]); },
-            [&](int kk, int nn) { return tf(B.e[kk * kPw + nn]); }, lane);
+            [&](int kk, int nn) { return tf(w16(B.s, kk, nn)); },
+            [&](int kk, int nn) { return tf(w16(B.e, kk, nn)); }, lane);
       wmma(b, mr, nc, DK, [&](int m, int kk) { return bfbits(sm.q + m * PH + kk); },
-           [&](int kk, int nn) { return tf(B.s[kk * kPw + nn]); }, lane);
-      each(a, mr, nc, lane, [&](int r, int cc, float &x) { W.ks[r * kPw + cc] = x; });
-      each(b, mr, nc, lane, [&](int r, int cc, float &x) { W.qs[r * kPw + cc] = x; });
-      each(c, mr, nc, lane, [&](int r, int cc, float &x) { W.ke[r * kPw + cc] = sm.sc.glr[r] * x; });
+           [&](int kk, int nn) { return tf(w16(B.s, kk, nn)); }, lane);
+      each(a, mr, nc, lane, [&](int r, int col, float &x) { w16(W.ks, r, col) = x; });
+      each(b, mr, nc, lane, [&](int r, int col, float &x) { w16(W.qs, r, col) = x; });
+      each(c, mr, nc, lane, [&](int r, int col, float &x) { w16(W.ke, r, col) = sm.sc.glr[r] * x; });
     }
     __syncthreads();
     // ---- Z = V - Diag(gamma) K S; db += gamma dO . (Q S)
@@ -577,8 +608,8 @@ __global__ void __launch_bounds__(256, 1) bd_grad_kernel(
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int c = cq + e;
-        W.z[r * kPw + c] = bf(B.v + r * kPh + c) - sm.sc.gam[r] * W.ks[r * kPw + c];
-        part += bf(B.o + r * kPh + c) * W.qs[r * kPw + c];
+        w16(W.z, r, c) = bf(B.v + r * kPh + c) - sm.sc.gam[r] * w16(W.ks, r, c);
+        part += bf(B.o + r * kPh + c) * w16(W.qs, r, c);
       }
       part += __shfl_xor_sync(0xffffffffu, part, 1);
       part += __shfl_xor_sync(0xffffffffu, part, 2);
@@ -589,31 +620,31 @@ __global__ void __launch_bounds__(256, 1) bd_grad_kernel(
     {
       float a[1][4], b[1][4];
       zero(a);
-      wmma(a, mr, nc, kCh, [&](int m, int kk) { return tf(sm.t[m * kPf + kk]); },
-           [&](int kk, int nn) { return tf(sm.sc.bet[kk] * W.z[kk * kPw + nn]); }, lane);
-      each(a, mr, nc, lane, [&](int r, int cc, float &x) { W.u[r * kPw + cc] = x; });
-      each(b, mr, nc, lane, [&](int r, int cc, float &x) { x = W.ke[r * kPw + cc]; });
-      wmma(b, mr, nc, kCh, [&](int m, int kk) { return tf(sm.p[kk * kPf + m]); },
+      wmma(a, mr, nc, kCh, [&](int m, int kk) { return tf(cc(sm.t, m, kk)); },
+           [&](int kk, int nn) { return tf(sm.sc.bet[kk] * w16(W.z, kk, nn)); }, lane);
+      each(a, mr, nc, lane, [&](int r, int col, float &x) { w16(W.u, r, col) = x; });
+      each(b, mr, nc, lane, [&](int r, int col, float &x) { x = w16(W.ke, r, col); });
+      wmma(b, mr, nc, kCh, [&](int m, int kk) { return tf(cc(sm.p, kk, m)); },
            [&](int kk, int nn) { return bfbits(B.o + kk * kPh + nn); }, lane);
-      each(b, mr, nc, lane, [&](int r, int cc, float &x) { W.du[r * kPw + cc] = x; });
+      each(b, mr, nc, lane, [&](int r, int col, float &x) { w16(W.du, r, col) = x; });
     }
     __syncthreads();
     // ---- Y = T^T dU; dV = Diag(beta) Y; dbeta += Y . Z; db -= gamma dZ . (K S); kd += U . (Kt E)
     {
       float a[1][4];
       zero(a);
-      wmma(a, mr, nc, kCh, [&](int m, int kk) { return tf(sm.t[kk * kPf + m]); },
-           [&](int kk, int nn) { return tf(W.du[kk * kPw + nn]); }, lane);
+      wmma(a, mr, nc, kCh, [&](int m, int kk) { return tf(cc(sm.t, kk, m)); },
+           [&](int kk, int nn) { return tf(w16(W.du, kk, nn)); }, lane);
       const int gg = lane >> 2;
       float pb[2] = {0.f, 0.f}, pd[2] = {0.f, 0.f}, pk[2] = {0.f, 0.f};
-      each(a, mr, nc, lane, [&](int r, int cc, float &y) {
+      each(a, mr, nc, lane, [&](int r, int col, float &y) {
         const int h = (r - mr - gg) >> 3;  // 0: row g, 1: row g + 8
-        W.y[r * kPw + cc] = y;
+        w16(W.y, r, col) = y;
         const float dz = sm.sc.bet[r] * y;
-        if (r < n) dv[(row0 + r) * DV + c0 + cc] = __float2bfloat16_rn(dz);
-        pb[h] += y * W.z[r * kPw + cc];
-        pd[h] += dz * W.ks[r * kPw + cc];
-        pk[h] += W.u[r * kPw + cc] * W.ke[r * kPw + cc];
+        if (r < n) dv[(row0 + r) * DV + c0 + col] = __float2bfloat16_rn(dz);
+        pb[h] += y * w16(W.z, r, col);
+        pd[h] += dz * w16(W.ks, r, col);
+        pk[h] += w16(W.u, r, col) * w16(W.ke, r, col);
       });
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -634,16 +665,16 @@ __global__ void __launch_bounds__(256, 1) bd_grad_kernel(
     __syncthreads();
     // ---- dA -= Y U^T, dP += dO U^T, dQ += Diag(gamma) dO S^T,
     //      dK += -Diag(gamma beta) Y S^T + Diag(gL / gamma) U E^T (K = 16 each)
-    wmma(aa, mr, na, kCW, [&](int m, int kk) { return tf(-W.y[m * kPw + kk]); },
-         [&](int kk, int nn) { return tf(W.u[nn * kPw + kk]); }, lane);
+    wmma(aa, mr, na, kCW, [&](int m, int kk) { return tf(-w16(W.y, m, kk)); },
+         [&](int kk, int nn) { return tf(w16(W.u, nn, kk)); }, lane);
     wmma(ap, mr, na, kCW, [&](int m, int kk) { return bfbits(B.o + m * kPh + kk); },
-         [&](int kk, int nn) { return tf(W.u[nn * kPw + kk]); }, lane);
+         [&](int kk, int nn) { return tf(w16(W.u, nn, kk)); }, lane);
     wmma(aq, mr, nq, kCW, [&](int m, int kk) { return tf(sm.sc.gam[m] * bf(B.o + m * kPh + kk)); },
-         [&](int kk, int nn) { return tf(B.s[nn * kPw + kk]); }, lane);
-    wmma(ak, mr, nq, kCW, [&](int m, int kk) { return tf(-sm.sc.gam[m] * sm.sc.bet[m] * W.y[m * kPw + kk]); },
-         [&](int kk, int nn) { return tf(B.s[nn * kPw + kk]); }, lane);
-    wmma(ak, mr, nq, kCW, [&](int m, int kk) { return tf(sm.sc.glr[m] * W.u[m * kPw + kk]); },
-         [&](int kk, int nn) { return tf(B.e[nn * kPw + kk]); }, lane);
+         [&](int kk, int nn) { return tf(w16(B.s, nn, kk)); }, lane);
+    wmma(ak, mr, nq, kCW, [&](int m, int kk) { return tf(-sm.sc.gam[m] * sm.sc.bet[m] * w16(W.y, m, kk)); },
+         [&](int kk, int nn) { return tf(w16(B.s, nn, kk)); }, lane);
+    wmma(ak, mr, nq, kCW, [&](int m, int kk) { return tf(sm.sc.glr[m] * w16(W.u, m, kk)); },
+         [&](int kk, int nn) { return tf(w16(B.e, nn, kk)); }, lane);
     __syncthreads();
   }
   // ---- <S, E> over the block
@@ -652,15 +683,15 @@ __global__ void __launch_bounds__(256, 1) bd_grad_kernel(
   if (lane == 0) sm.red[warp] = se;
   // ---- dA, dP to shared memory; L = strict_lower(Gamma ⊙ K K^T)
   auto& Fn = sm.w.fin;
-  each(aa, mr, na, lane, [&](int r, int s, float &x) { Fn.da[r * kPf + s] = x; });
-  each(ap, mr, na, lane, [&](int r, int s, float &x) { Fn.dp[r * kPf + s] = x; });
+  each(aa, mr, na, lane, [&](int r, int s, float &x) { cc(Fn.da, r, s) = x; });
+  each(ap, mr, na, lane, [&](int r, int s, float &x) { cc(Fn.dp, r, s) = x; });
   {
     float a[4][4];
     zero(a);
     wmma(a, mr, na, DK, [&](int m, int kk) { return bfbits(sm.k + m * PH + kk); },
          [&](int kk, int nn) { return bfbits(sm.k + nn * PH + kk); }, lane);
     each(a, mr, na, lane, [&](int r, int s, float &x) {
-      Fn.l[r * kPf + s] = s < r ? __expf(sm.sc.b[r] - sm.sc.b[s]) * x : 0.f;
+      cc(Fn.l, r, s) = s < r ? __expf(sm.sc.b[r] - sm.sc.b[s]) * x : 0.f;
     });
   }
   __syncthreads();
@@ -671,16 +702,16 @@ __global__ void __launch_bounds__(256, 1) bd_grad_kernel(
     for (int jj = 0; jj < kCh / 4; ++jj) {
       const int s = (tid & 3) + 4 * jj;
       const float gm = s <= r ? __expf(sm.sc.b[r] - sm.sc.b[s]) : 0.f;
-      const float a = s < r ? Fn.da[r * kPf + s] : 0.f;
-      const float l = Fn.l[r * kPf + s];
+      const float a = s < r ? cc(Fn.da, r, s) : 0.f;
+      const float l = cc(Fn.l, r, s);
       betp += a * l;
       const float dl = sm.sc.bet[r] * a, dll = dl * l;
-      const float pp = s <= r ? Fn.dp[r * kPf + s] : 0.f;
-      const float ppp = pp * sm.p[r * kPf + s];
+      const float pp = s <= r ? cc(Fn.dp, r, s) : 0.f;
+      const float ppp = pp * cc(sm.p, r, s);
       rowp += dll + ppp;
       if (dll + ppp != 0.f) atomicAdd(&sm.db[s], -(dll + ppp));
-      Fn.da[r * kPf + s] = dl * gm;
-      Fn.dp[r * kPf + s] = pp * gm;
+      cc(Fn.da, r, s) = dl * gm;
+      cc(Fn.dp, r, s) = pp * gm;
     }
     rowp += __shfl_xor_sync(0xffffffffu, rowp, 1);
     rowp += __shfl_xor_sync(0xffffffffu, rowp, 2);
@@ -693,13 +724,13 @@ __global__ void __launch_bounds__(256, 1) bd_grad_kernel(
   }
   __syncthreads();
   // ---- dQ += H K; dK += F K + F^T K + H^T Q
-  wmma(aq, mr, nq, kCh, [&](int m, int kk) { return tf(Fn.dp[m * kPf + kk]); },
+  wmma(aq, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.dp, m, kk)); },
        [&](int kk, int nn) { return bfbits(sm.k + kk * PH + nn); }, lane);
-  wmma(ak, mr, nq, kCh, [&](int m, int kk) { return tf(Fn.da[m * kPf + kk]); },
+  wmma(ak, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.da, m, kk)); },
        [&](int kk, int nn) { return bfbits(sm.k + kk * PH + nn); }, lane);
-  wmma(ak, mr, nq, kCh, [&](int m, int kk) { return tf(Fn.da[kk * kPf + m]); },
+  wmma(ak, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.da, kk, m)); },
        [&](int kk, int nn) { return bfbits(sm.k + kk * PH + nn); }, lane);
-  wmma(ak, mr, nq, kCh, [&](int m, int kk) { return tf(Fn.dp[kk * kPf + m]); },
+  wmma(ak, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.dp, kk, m)); },
        [&](int kk, int nn) { return bfbits(sm.q + kk * PH + nn); }, lane);
   each(aq, mr, nq, lane, [&](int r, int c, float &x) {
     if (r < n) dq[(row0 + r) * DK + c] = __float2bfloat16_rn(x);
