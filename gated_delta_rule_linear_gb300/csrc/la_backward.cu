@@ -276,8 +276,8 @@ extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const f
   }
   if ((mode & ~(0xff | LA_F32)) != 0 ||
       (kind != LA_LINEAR && kind != LA_RETNET && kind != LA_SCALAR_GATE && kind != LA_GLA)) {
-    set_error("%s: mode 0x%x: the backward pass covers LA_LINEAR, LA_RETNET, LA_SCALAR_GATE and LA_GLA "
-              "(optionally | LA_F32)", fn, mode);
+    set_error("%s: mode 0x%x: this entry point covers LA_LINEAR, LA_RETNET, LA_SCALAR_GATE and LA_GLA "
+              "(optionally | LA_F32); LA_GDN has la_chunk_bwd_delta", fn, mode);
     return (mode & ~(0xff | LA_F32)) == 0 && kind >= LA_LINEAR && kind <= LA_OUTER_GATE ? LA_ERR_UNSUPPORTED
                                                                                   : LA_ERR_INVALID_ARG;
   }

@@ -202,7 +202,7 @@ def _bwd(**kw):
     (dict(dv_out=None), "LA_ERR_INVALID_ARG"),
     (dict(T=0), "LA_ERR_INVALID_ARG"),
     (dict(dk=96), "LA_ERR_UNSUPPORTED"),
-    (dict(mode=5), "LA_ERR_UNSUPPORTED"),             # gdn: no backward in this build
+    (dict(mode=5), "LA_ERR_UNSUPPORTED"),             # gdn: la_chunk_bwd_delta, not this entry point
     (dict(mode=9), "LA_ERR_INVALID_ARG"),
     (dict(mode=2), "LA_ERR_INVALID_ARG"),             # retnet needs g
     (dict(g=A), "LA_ERR_INVALID_ARG"),                # linear takes none
