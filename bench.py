@@ -57,7 +57,7 @@ KERNEL_SOURCES = {
     "backward_scalar": [_CS + "la_backward.cu", _CS + "la_chunk_ws.cu", _CS + "la_chunk_mat.cu"] + _COMMON,
     "backward_gla": [_CS + "la_backward.cu", _CS + "la_chunk_ws.cu"] + _COMMON,
     "decode": [_CS + "la_step.cu"],
-    "gdelta": [_CS + "la_chunk_gdelta.cu"],
+    "gdelta": [_CS + "la_chunk_gdelta.cu", _CS + "la_chunk_gdelta_wy.cu", _CS + "la_warp_mma.cuh"],
     "backward_gdn": [_CS + "la_backward_delta.cu", _CS + "la_wy.cuh", _CS + "la_tc_common.cuh"],
     "prologue": [_CS + "la_prologue.cu", _CS + "la_sm100.cuh"],
     "prologue_gla": [_CS + "la_prologue.cu", _CS + "la_sm100.cuh"],
@@ -1064,7 +1064,8 @@ def bench_gdelta(args, rank, world, local_rank):
     # the arithmetic intensity (~100 FLOP/byte at d = 64) sits below the bf16 ridge: an HBM roofline
     roof = {"bound": "hbm", "achieved": round(alg / t_launch / 1e9, 1), "peak": hbm_peak, "unit": "GB/s",
             "frac": round(alg / t_launch / 1e9 / hbm_peak, 4), "traffic": recorded_traffic(wl.name),
-            "peak_source": peak_src, "algorithmic_bytes": alg, "kernel": "chunk_gdelta_kernel (CUDA cores, fp32)",
+            "peak_source": peak_src, "algorithmic_bytes": alg, "kernel": "gdw_pre_kernel + gdw_chain_kernel (tf32 warp MMAs)"
+            if wl.dtype == "bf16" else "chunk_gdelta_kernel (CUDA cores, fp32)",
             "launch_ms_mean": round(statistics.mean(launch_ms), 4)}
     e2e = None
     if not args.no_e2e:

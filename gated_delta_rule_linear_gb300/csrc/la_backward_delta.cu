@@ -43,84 +43,12 @@
 #include <cstdint>
 
 #include "la_internal.h"
-#include "la_wy.cuh"
+#include "la_warp_mma.cuh"
 
 namespace la {
 namespace {
 
-using wy::mma_16x8x8_tf32;
-using wy::to_tf32;
-using sm100::smem_u32;
-
-constexpr int kCh = 64;        // chunk length
-constexpr int kCW = 16;        // value columns per block
-// float32 tiles are dense (64 or 16 floats a row) with the 16-byte groups of a
-// row permuted by an XOR of the row index, so that the tf32 fragment reads of
-// the warp MMAs -- by rows or by columns, as A or as B -- hit 32 distinct banks.
-constexpr int kPf = kCh;       // floats per row of C x C tiles
-constexpr int kPw = kCW;       // floats per row of x 16 tiles
-__host__ __device__ __forceinline__ int swz64(int r) { return ((r & 3) << 3) | (((r >> 2) & 1) << 2); }
-__host__ __device__ __forceinline__ int swz16(int r) { return (((r >> 1) & 1) << 3) | (((r >> 2) & 1) << 2); }
-__device__ __forceinline__ float &cc(float *p, int r, int c) { return p[r * kPf + (c ^ swz64(r))]; }
-__device__ __forceinline__ float &w16(float *p, int r, int c) { return p[r * kPw + (c ^ swz16(r))]; }
-template <int DK>
-struct Pitch {
-  static constexpr int h = DK + 8;  // row pitch (bf16) of q / k tiles: 16-byte rows
-};
-
-__device__ __forceinline__ uint32_t bfbits(const __nv_bfloat16 *p) {
-  return static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(p)) << 16;
-}
-__device__ __forceinline__ uint32_t tf(float x) { return to_tf32(x); }
-
-// acc[j] (the 16 x 8 tile at rows m0.., columns n0 + 8 j) += A[m0.., 0..K) B[0..K), ..]:
-// ga(m, k) and gb(k, n) return the tf32 bits of one element.
-// With one or two tiles the k steps alternate between two accumulator sets, so
-// consecutive MMAs do not wait on each other's results.
-template <int NT, class GA, class GB>
-__device__ __forceinline__ void wmma(float (&acc)[NT][4], int m0, int n0, int K, GA ga, GB gb, int lane) {
-  const int g = lane >> 2, t = lane & 3;
-  constexpr bool split = NT <= 2;
-  float alt[NT][4];
-#pragma unroll
-  for (int j = 0; j < NT; ++j) alt[j][0] = alt[j][1] = alt[j][2] = alt[j][3] = 0.f;
-#pragma unroll
-  for (int k0 = 0; k0 < K; k0 += 8) {
-    uint32_t a[4] = {ga(m0 + g, k0 + t), ga(m0 + g + 8, k0 + t), ga(m0 + g, k0 + t + 4),
-                     ga(m0 + g + 8, k0 + t + 4)};
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      uint32_t b[2] = {gb(k0 + t, n0 + 8 * j + g), gb(k0 + t + 4, n0 + 8 * j + g)};
-      mma_16x8x8_tf32(split && (k0 & 8) ? alt[j] : acc[j], a, b);
-    }
-  }
-  if (split) {
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      acc[j][0] += alt[j][0];
-      acc[j][1] += alt[j][1];
-      acc[j][2] += alt[j][2];
-      acc[j][3] += alt[j][3];
-    }
-  }
-}
-// f(row, col, value) over the elements of an accumulator set (values may be changed)
-template <int NT, class F>
-__device__ __forceinline__ void each(float (&acc)[NT][4], int m0, int n0, int lane, F f) {
-  const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    f(m0 + g, n0 + 8 * j + 2 * t, acc[j][0]);
-    f(m0 + g, n0 + 8 * j + 2 * t + 1, acc[j][1]);
-    f(m0 + g + 8, n0 + 8 * j + 2 * t, acc[j][2]);
-    f(m0 + g + 8, n0 + 8 * j + 2 * t + 1, acc[j][3]);
-  }
-}
-template <int NT>
-__device__ __forceinline__ void zero(float (&acc)[NT][4]) {
-#pragma unroll
-  for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-}
+using namespace wm;
 
 // Per-chunk scalars: gamma_r = e^{b_r}, e^{bL - b_r}, beta_r and b_r (b the
 // inclusive prefix of the chunk's log-gates); rows past the end get zero gates
@@ -163,55 +91,6 @@ __device__ __forceinline__ void gate_scan(Scal &s, Gates gt, int lane) {
   s.bet[lane] = gt.b0;
   s.bet[lane + 32] = gt.b1;
 }
-
-// ---- asynchronous tile copies (16 bytes each; a copy of 0 source bytes fills zeros)
-constexpr int kPh = kCW + 8;  // row pitch (bf16) of x 16 bf16 tiles: 48-byte rows
-
-__device__ __forceinline__ void cpa16(void *dst, const void *src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-               "r"(valid ? 16u : 0u)
-               : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-// rows [0, 64) of a [T][D] bf16 tensor from the chunk's first token (n valid, zero beyond), pitch P
-template <int D, int P>
-__device__ __forceinline__ void rows_async(__nv_bfloat16 *dst, const __nv_bfloat16 *src, int n, int tid, int nthr) {
-  for (int i = tid; i < kCh * (D / 8); i += nthr) {
-    const int r = i / (D / 8), c = (i % (D / 8)) * 8;
-    const bool ok = r < n;
-    cpa16(dst + r * P + c, src + (ok ? (size_t)r * D + c : 0), ok);
-  }
-}
-// the 64 x 16 columns [c0, c0 + 16) of a [T][D] bf16 tensor, pitch kPh
-template <int D>
-__device__ __forceinline__ void cols_async(__nv_bfloat16 *dst, const __nv_bfloat16 *src, int c0, int n, int tid,
-                                           int nthr) {
-  for (int i = tid; i < kCh * 2; i += nthr) {
-    const int r = i >> 1, c = (i & 1) * 8;
-    const bool ok = r < n;
-    cpa16(dst + r * kPh + c, src + (ok ? (size_t)r * D + c0 + c : 0), ok);
-  }
-}
-// a 64 x 64 float32 matrix (row-major, contiguous), pitch kPf
-__device__ __forceinline__ void cc_async(float *dst, const float *src, int tid, int nthr) {
-  for (int i = tid; i < kCh * kCh / 4; i += nthr) {
-    const int r = i >> 4, c = (i & 15) * 4;
-    cpa16(dst + r * kPf + (c ^ swz64(r)), src + 4 * i, true);
-  }
-}
-// the D x 16 columns [c0, c0 + 16) of a [D][DV] float32 matrix, pitch kPw
-template <int D, int DV>
-__device__ __forceinline__ void state_async(float *dst, const float *src, int c0, int tid, int nthr) {
-  for (int i = tid; i < D * 4; i += nthr) {
-    const int r = i >> 2, c = (i & 3) * 4;
-    cpa16(dst + r * kPw + (c ^ swz16(r)), src + (size_t)r * DV + c0 + c, true);
-  }
-}
-__device__ __forceinline__ float bf(const __nv_bfloat16 *p) { return __uint_as_float(bfbits(p)); }
 
 // ============================================================ pre-pass
 template <int DK>
@@ -266,10 +145,11 @@ __global__ void __launch_bounds__(128) bd_pre_kernel(const __nv_bfloat16 *__rest
     float tc[kCh];
 #pragma unroll
     for (int r = 0; r < kCh; ++r) {
-      float x = r == j ? 1.f : 0.f;
+      // four partial sums, so the row's FMAs do not form one dependent chain
+      float x[4] = {r == j ? 1.f : 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int s = 0; s < r; ++s) x = fmaf(-cc(sm.a, r, s), tc[s], x);
-      tc[r] = r < j ? 0.f : x;
+      for (int s = 0; s < r; ++s) x[s & 3] = fmaf(-cc(sm.a, r, s), tc[s], x[s & 3]);
+      tc[r] = r < j ? 0.f : (x[0] + x[1]) + (x[2] + x[3]);
     }
 #pragma unroll
     for (int r = 0; r < kCh; ++r) Tw[cbase + r * kCh + j] = tc[r];

@@ -15,8 +15,10 @@
 //   O = Q S + M(Q K^T) V - M(Q B^T) U    (M: inclusive causal mask)
 //   S <- S + K^T V - B^T U
 //
-// CUDA cores, float32 arithmetic for bf16 or float32 inputs; one CTA per
-// (b, h) and 16-column tile of the value axis, the state slice in shared
+// This file holds the CUDA-core kernel, which runs float32 inputs (and
+// bfloat16 ones when LA_GDELTA=simt; the default for bfloat16 is the
+// two-phase tensor-core path of la_chunk_gdelta_wy.cu): float32 arithmetic,
+// one CTA per (b, h) and 16-column tile of the value axis, the state slice in shared
 // memory for the whole sequence. The four C x C products come from one
 // register-tiled pass (a 4 x 4 block of (r, s) per thread, 16 shared-memory
 // loads per 64 FMAs); the retrieved values U are found by forward
@@ -26,6 +28,8 @@
 #include <cuda_bf16.h>
 
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 
 #include "la_internal.h"
 
@@ -306,11 +310,40 @@ extern "C" int la_chunk_fwd_gdelta(const void *q, const void *k, const void *v, 
     set_error("%s: S0 and S_final must be 16-byte aligned", fn);
     return LA_ERR_INVALID_ARG;
   }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const char *env = getenv("LA_GDELTA");
+  if (mode == 0 && !(env && strcmp(env, "simt") == 0)) {
+    // bfloat16: the two-phase path on the tensor cores (per-chunk key side, then the
+    // state chain), workspace from the library's pool on the caller's stream
+    const GdeltaArgs x{q, k, v, a, b, o, S0, S_final, B, H, T, dk, dv};
+    if ((long long)B * H > 65535) {
+      set_error("%s: B*H must be <= 65535 for bfloat16 inputs (got %lld)", fn, (long long)B * H);
+      return LA_ERR_UNSUPPORTED;
+    }
+    const size_t bytes = gdelta_wy_workspace_bytes(B * H, T, dk);
+    cudaMemPool_t pool = library_pool();
+    if (!pool) {
+      set_error("%s: could not create the workspace pool: %s", fn, cudaGetErrorString(cudaGetLastError()));
+      return LA_ERR_CUDA;
+    }
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes, pool, s);
+    if (e != cudaSuccess) {
+      set_error("%s: workspace allocation of %zu bytes failed: %s", fn, bytes, cudaGetErrorString(e));
+      return LA_ERR_CUDA;
+    }
+    const int rc = launch_gdelta_wy(x, ws, s);
+    e = cudaFreeAsync(ws, s);
+    if (rc == LA_OK && e != cudaSuccess) {
+      set_error("%s: workspace release failed: %s", fn, cudaGetErrorString(e));
+      return LA_ERR_CUDA;
+    }
+    return rc;
+  }
   const GdParams p{q, k, v, a, b, o, S0, S_final, B, H, T, dk, dv};
   const GdLayout L = gd_layout(dk);
   const size_t smem = sizeof(float) * (size_t)L.total;
   const dim3 grid((unsigned)(B * H), (unsigned)((dv + kTile - 1) / kTile));
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (mode == LA_F32) {
     e = cudaFuncSetAttribute(chunk_gdelta_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -25,6 +25,19 @@ enum StatusBits : unsigned {
   kStatusTimeout = 1u,
 };
 
+// Arguments of the generalised delta rule's forward (la_chunk_fwd_gdelta).
+struct GdeltaArgs {
+  const void *q, *k, *v, *a, *b;
+  void *o;
+  const float *S0;
+  float *S_final;
+  int B, H, T, dk, dv;
+};
+// The two-phase bf16 path: per-chunk key-side matrices into `workspace`
+// (gdelta_wy_workspace_bytes), then the state chain (la_chunk_gdelta_wy.cu).
+size_t gdelta_wy_workspace_bytes(int BH, int T, int dk);
+int launch_gdelta_wy(const GdeltaArgs &x, void *workspace, cudaStream_t stream);
+
 // Whether a mode word may request the 128-token chunk: the materialised
 // variant's output pass for the modes without per-channel gates, bfloat16,
 // causal (no flag bits).

@@ -120,3 +120,26 @@ def test_gdelta_full_size_workload_sampled_heads():
     o_ref, S_ref = _ref(inp, heads)
     assert_close(np.stack([f64(o[b, h]) for b, h in heads])[None], o_ref, "bf16", "gdelta o (sampled)")
     assert_close(np.stack([f64(S[b, h]) for b, h in heads])[None], S_ref, "bf16", "gdelta S (sampled)")
+
+
+@pytest.mark.parametrize("dims", [(64, 64), (128, 128)])
+@pytest.mark.parametrize("T", [1, 65, 300])
+def test_gdelta_bf16_cuda_core_path_parity(dims, T, monkeypatch):
+    # bfloat16 runs the two-phase tensor-core path by default; LA_GDELTA=simt keeps the
+    # one-pass CUDA-core kernel for it, which must meet the same tolerance
+    monkeypatch.setenv("LA_GDELTA", "simt")
+    dk, dv = dims
+    inp = _inputs("bf16", B=1, H=2, T=T, dk=dk, dv=dv, seed=31)
+    o, S = _gpu(inp)
+    o_ref, S_ref = _ref(inp)
+    assert_close(f64(o), o_ref, "bf16", "gdelta (CUDA cores) o")
+    assert_close(f64(S), S_ref, "bf16", "gdelta (CUDA cores) S_final")
+
+
+def test_gdelta_bf16_paths_agree(monkeypatch):
+    inp = _inputs("bf16", B=2, H=3, T=777, dk=64, dv=128, seed=32)
+    o_a, S_a = _gpu(inp)
+    monkeypatch.setenv("LA_GDELTA", "simt")
+    o_b, S_b = _gpu(inp)
+    assert_close(f64(o_a), f64(o_b), "bf16", "two-phase vs CUDA-core o")
+    assert_close(f64(S_a), f64(S_b), "bf16", "two-phase vs CUDA-core S_final")
