@@ -45,7 +45,7 @@ _COMMON = [_CS + "la_tc_common.cuh", _CS + "la_sm100.cuh"]
 # traffic figure stays valid while these files are unchanged.
 KERNEL_SOURCES = {
     "gdn": [_CS + "la_chunk_delta_pair.cu", _CS + "la_chunk_delta.cu", _CS + "la_wy.cuh"] + _COMMON,
-    "kda": [_CS + "la_chunk_tc.cu", _CS + "la_wy.cuh"] + _COMMON,
+    "kda": [_CS + "la_chunk_kda_wy.cu", _CS + "la_warp_mma.cuh", _CS + "la_wy.cuh"],
     "retnet": [_CS + "la_chunk_ws.cu"] + _COMMON,
     "gla": [_CS + "la_chunk_ws.cu"] + _COMMON,
     "outer": [_CS + "la_chunk_ws.cu"] + _COMMON,
@@ -97,7 +97,8 @@ def kernel_name(wl, variant=None, sm_count=152) -> str:
     if wl.dtype == "f32" or variant == "simt":
         return "chunk_simt_kernel"
     if wl.mode == "kda":
-        return "chunk_tc_kernel"
+        fused = variant in ("tc", "nonmat") or os.environ.get("LA_KDA") == "tc"
+        return "chunk_tc_kernel" if fused else "kdw_pre_kernel+kdw_chain_kernel"
     if wl.mode == "gdn":
         if wl.dk == 128 and wl.dv == 128:
             path = os.environ.get("LA_DELTA", "pair" if 2 * wl.B * wl.H <= sm_count else "single")

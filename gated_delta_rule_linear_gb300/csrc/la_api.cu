@@ -104,12 +104,16 @@ int select_variant(const ChunkParams &p, int *chunk_out) {
     return -1;
   }
   if (p.f32) return (want == kVariantTc || want == kVariantMat) ? -2 : kVariantSimt;
-  if (p.kind == kKda) {  // the tensor-core kernel only
+  if (p.kind == kKda) {
+    // the two-phase path (every chunk's key side in parallel, then the state chain per
+    // head and 32 value columns; la_chunk_kda_wy.cu), measured faster on GB300 than the
+    // fused sequential-phase kernel, which LA_VARIANT=tc or LA_KDA=tc selects
     if (want == kVariantMat || want == kVariantSimt) {
-      set_error("la_chunk_fwd: LA_KDA runs on the fused tensor-core kernel only");
+      set_error("la_chunk_fwd: LA_KDA runs on its two-phase path or the fused tensor-core kernel");
       return -1;
     }
-    return kVariantTc;
+    const char *kd = getenv("LA_KDA");
+    return (want == kVariantTc || (kd && strcmp(kd, "tc") == 0)) ? kVariantTc : kVariantKdaWy;
   }
   if ((want == kVariantMat || want == kVariantSimt) && p.kind == kOuter) {
     set_error("la_chunk_fwd: LA_OUTER_GATE runs on the pipelined tensor-core kernel only");
@@ -331,10 +335,10 @@ int la_chunk_fwd(const void *q, const void *k, const void *v, const float *g, co
     }
     return rc;
   }
-  if (variant == kVariantDeltaWy) {
-    // stream-ordered workspace for the T' images, from the library's pool
+  if (variant == kVariantDeltaWy || variant == kVariantKdaWy) {
+    // stream-ordered workspace for the per-chunk key-side images, from the library's pool
     void *ws = nullptr;
-    const size_t bytes = delta_wy_workspace_bytes(p);
+    const size_t bytes = variant == kVariantKdaWy ? kda_wy_workspace_bytes(p) : delta_wy_workspace_bytes(p);
     cudaMemPool_t pool = workspace_pool();
     if (!pool) {
       set_error("%s: could not create the workspace pool: %s", fn, cudaGetErrorString(cudaGetLastError()));
@@ -345,7 +349,7 @@ int la_chunk_fwd(const void *q, const void *k, const void *v, const float *g, co
       set_error("%s: workspace allocation of %zu bytes failed: %s", fn, bytes, cudaGetErrorString(e));
       return LA_ERR_CUDA;
     }
-    rc = launch_chunk_delta_wy(p, ws, s);
+    rc = variant == kVariantKdaWy ? launch_kda_wy(p, ws, s) : launch_chunk_delta_wy(p, ws, s);
     e = cudaFreeAsync(ws, s);
     if (rc == LA_OK && e != cudaSuccess) {
       set_error("%s: workspace release failed: %s", fn, cudaGetErrorString(e));

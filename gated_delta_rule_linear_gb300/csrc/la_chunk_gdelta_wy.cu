@@ -124,15 +124,6 @@ struct GwChainSmem {
   float w[kCh * DK], m[kCh * kPf], p1[kCh * kPf], p2[kCh * kPf], s[DK * kPw], u[kCh * kPw];
 };
 
-// a 64 x DK float32 matrix (row-major, contiguous) into the permuted layout fw<DK>
-template <int DK>
-__device__ __forceinline__ void wide_async(float *dst, const float *src, int tid, int nthr) {
-  for (int i = tid; i < kCh * DK / 4; i += nthr) {
-    const int r = i / (DK / 4), c = (i % (DK / 4)) * 4;
-    cpa16(dst + r * DK + (c ^ swz64(r)), src + 4 * i, true);
-  }
-}
-
 template <int DK, int DV>
 __global__ void __launch_bounds__(128) gdw_chain_kernel(
     const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,

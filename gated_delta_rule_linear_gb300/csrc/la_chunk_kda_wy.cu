@@ -1,0 +1,341 @@
+// Two-phase chunk forward of Kimi Delta Attention ("LLM attention
+// optimisation" page, Kimi Delta Attention section: Gated DeltaNet with a
+// per-key-channel gate), key-major,
+//
+//   S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T,  o_t = S_t^T q_t,
+//
+// bf16 inputs, fp32 state, on tf32 warp MMAs. Per chunk of C = 64 rows with
+// the per-channel inclusive prefix B[r][c] of the log-gates, its midpoint row
+// b_m[c] = B[31][c] and its last row B_L[c], the WY/UT form ("Talk Linear
+// Attention" section 6.2) with the decay folded per channel is
+//
+//   A = Diag(beta) strict_lower(K+ K-^T),  T = (I + A)^{-1},  T' = T Diag(beta)
+//   W = T' (K ⊙ e^B),  U = T' V - W S
+//   O = (Q ⊙ e^B) S + P U,  P = lower(Q+ K-^T)
+//   S <- Diag(e^{B_L}) S + (K ⊙ e^{B_L - B})^T U
+//
+// with Q+ = Q ⊙ e^{B - b_m}, K+ = K ⊙ e^{B - b_m}, K- = K ⊙ e^{b_m - B} (so
+// that Q+ K-^T carries e^{B_r - B_s} channel by channel without forming it;
+// a cumulative log-gate above ~80 within half a chunk overflows the fold, as
+// in the fused kernels).
+//
+// Phase 1 (kdw_pre_kernel, every chunk in parallel): the prefix, the folded
+// operands (bf16, as the fused kernels use them), A and P from one
+// [Q+; K+] K-^T product, T by substitution, T', W;
+// written to a workspace as bf16 operands (with Q ⊙ e^B and K ⊙ e^{B_L - B})
+// and e^{B_L}. Phase 2 (kdw_chain_kernel, per head and 32 value columns -- each value
+// column of S evolves on its own): the chunks in order, S in registers, the
+// next chunk's tiles copied while the current one finishes. A tail chunk is
+// padded with zero rows and zero gates, which leaves every real row's result
+// unchanged.
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "la_internal.h"
+#include "la_warp_mma.cuh"
+
+namespace la {
+namespace {
+
+using namespace wm;
+
+constexpr int kMid = kCh / 2 - 1;  // the fold's midpoint row
+constexpr int kVW = 32;            // value columns per chain CTA
+constexpr int kVP = kVW + 8;       // row pitch (bf16) of the chain's v tile
+constexpr int kCP = kCh + 8;       // row pitch (bf16) of its C x C tiles
+
+// Per-chunk workspace, in this order (bf16 operands, as the fused kernels use):
+// T' [64][64], W [64][DK], P [64][64], Q e^B [64][DK], K e^{B_L - B} [64][DK]
+// (all bf16, dense rows), e^{B_L} [DK] f32.
+template <int DK>
+struct KwOff {
+  static constexpr size_t tp = 0, w = tp + kCh * kCh * 2, p = w + (size_t)kCh * DK * 2,
+                          qt = p + kCh * kCh * 2, kt = qt + (size_t)kCh * DK * 2, gl = kt + (size_t)kCh * DK * 2,
+                          bytes = gl + (size_t)DK * 4;
+};
+
+// ============================================================ phase 1
+// One CTA per chunk, 128 threads, ~88 KB of shared memory (two CTAs per SM):
+// a thread per key channel forms the channel's prefix in registers and the
+// folded rows; the products run on the bf16 operand tiles; T comes from 16 x 16
+// diagonal blocks and three block levels on tf32 warp MMAs (la_wy.cuh).
+template <int DK>
+struct KwPreSmem {
+  union {
+    struct {
+      __nv_bfloat16 q[kCh * Pitch<DK>::h], k[kCh * Pitch<DK>::h];
+    } in;  // the chunk's rows, until the fold is done
+    struct {
+      float af[kCh * wy::kAp], tf[kCh * wy::kAp];  // A, then T and T' = T Diag(beta)
+    } s;
+  } u;
+  __nv_bfloat16 qp[kCh * Pitch<DK>::h], kp[kCh * Pitch<DK>::h], km[kCh * Pitch<DK>::h];
+  float bet[kCh], bm[DK];
+};
+
+template <int DK>
+__global__ void __launch_bounds__(128) kdw_pre_kernel(const __nv_bfloat16 *__restrict__ q,
+                                                      const __nv_bfloat16 *__restrict__ k,
+                                                      const float *__restrict__ g, const float *__restrict__ beta,
+                                                      int T, uint8_t *__restrict__ ws) {
+  constexpr int PH = Pitch<DK>::h;
+  using O = KwOff<DK>;
+  using bf16 = __nv_bfloat16;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  KwPreSmem<DK> &sm = *reinterpret_cast<KwPreSmem<DK> *>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int i = blockIdx.x, bh = blockIdx.y, nch = gridDim.x;
+  const int t0 = i * kCh, n = min(kCh, T - t0);
+  const size_t row0 = (size_t)bh * T + t0;
+  uint8_t *wc = ws + ((size_t)bh * nch + i) * O::bytes;
+  rows_async<DK, PH>(sm.u.in.q, q + row0 * DK, n, tid, 128);
+  rows_async<DK, PH>(sm.u.in.k, k + row0 * DK, n, tid, 128);
+  cp_commit();
+  if (tid < kCh) sm.bet[tid] = tid < n ? (beta ? __ldg(beta + row0 + tid) : 1.f) : 0.f;
+  // ---- channel c = tid: the prefix B[.][c] in registers (zero gates past the end)
+  float bc[kCh];
+  if (tid < DK) {
+    float acc = 0.f;
+#pragma unroll
+    for (int r = 0; r < kCh; ++r) {
+      acc += r < n ? __ldg(g + (row0 + r) * DK + tid) : 0.f;
+      bc[r] = acc;
+    }
+  }
+  cp_wait<0>();
+  __syncthreads();
+  // ---- folded rows: Q+, K+, K- (tiles), Q e^B and K e^{B_L - B} (workspace), e^{B_L}
+  if (tid < DK) {
+    const int c = tid;
+    const float bmid = bc[kMid], bl = bc[kCh - 1];
+    sm.bm[c] = bmid;
+    reinterpret_cast<float *>(wc + O::gl)[c] = __expf(bl);
+    bf16 *qt = reinterpret_cast<bf16 *>(wc + O::qt), *kt = reinterpret_cast<bf16 *>(wc + O::kt);
+#pragma unroll
+    for (int r = 0; r < kCh; ++r) {
+      const float qx = bf(sm.u.in.q + r * PH + c), kx = bf(sm.u.in.k + r * PH + c);
+      const float d = bc[r] - bmid, ep = __expf(d), em = __expf(-d);
+      sm.qp[r * PH + c] = __float2bfloat16_rn(qx * ep);
+      sm.kp[r * PH + c] = __float2bfloat16_rn(kx * ep);
+      sm.km[r * PH + c] = __float2bfloat16_rn(kx * em);
+      qt[r * DK + c] = __float2bfloat16_rn(qx * __expf(bc[r]));
+      kt[r * DK + c] = __float2bfloat16_rn(kx * __expf(bl - bc[r]));
+    }
+  }
+  __syncthreads();
+  // ---- [Q+; K+] K-^T: warps 0, 1 the rows of Q+ (P), warps 2, 3 the rows of K+ (A)
+  {
+    const bf16 *src = warp < 2 ? sm.qp : sm.kp;
+    bf16 *P = reinterpret_cast<bf16 *>(wc + O::p);
+    const int rbase = (warp & 1) * 32;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float acc[8][4];
+      zero(acc);
+      wmma(acc, rbase + 16 * h, 0, DK, [&](int m, int kk) { return bfbits(src + m * PH + kk); },
+           [&](int kk, int nn) { return bfbits(sm.km + nn * PH + kk); }, lane);
+      if (warp < 2)
+        each(acc, rbase + 16 * h, 0, lane,
+             [&](int r, int s, float &x) { P[r * kCh + s] = __float2bfloat16_rn(s <= r ? x : 0.f); });
+      else  // rounded to tf32 for the block MMAs of the solve
+        each(acc, rbase + 16 * h, 0, lane, [&](int r, int s, float &x) {
+          sm.u.s.af[r * wy::kAp + s] = s < r ? wy::round_tf32(sm.bet[r] * x) : 0.f;
+        });
+    }
+  }
+  __syncthreads();
+  // ---- T = (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution, then the
+  //      off-diagonal blocks in three levels, T_ij = -T_ii sum_{j<=k<i} A_ik T_kj
+  float *Af = sm.u.s.af, *Tf = sm.u.s.tf;
+  if (tid < kCh) wy::diag_inverse_16(Af, Tf, tid >> 4, tid & 15);
+  __syncthreads();
+#pragma unroll 1
+  for (int lvl = 1; lvl < 4; ++lvl) {
+    if (warp < 4 - lvl) {
+      const int ib = warp + lvl, jb = warp;
+      float a2[2][4] = {};
+      for (int kb = jb; kb < ib; ++kb)
+        wy::block_mma_16(a2, Af + ib * 16 * wy::kAp + kb * 16, Tf + kb * 16 * wy::kAp + jb * 16, lane);
+      float *Tij = Tf + ib * 16 * wy::kAp + jb * 16;
+      wy::block_store_16(Tij, a2, 1.f, lane);
+      __syncwarp();
+      float a3[2][4] = {};
+      wy::block_mma_16(a3, Tf + ib * 16 * wy::kAp + ib * 16, Tij, lane);
+      __syncwarp();
+      wy::block_store_16(Tij, a3, -1.f, lane);
+    }
+    __syncthreads();
+  }
+  // ---- T' = T Diag(beta) (zero above the diagonal) in place and to the workspace: thread tid
+  //      owns row tid / 2, columns 32 (tid % 2) .. + 31
+  {
+    const int r = tid >> 1, c0 = (tid & 1) * 32;
+    bf16 *tp = reinterpret_cast<bf16 *>(wc + O::tp) + r * kCh + c0;
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const int sc = c0 + e;
+      const float x0 = sc <= r ? Tf[r * wy::kAp + sc] * sm.bet[sc] : 0.f;
+      const float x1 = sc + 1 <= r ? Tf[r * wy::kAp + sc + 1] * sm.bet[sc + 1] : 0.f;
+      Tf[r * wy::kAp + sc] = x0;
+      Tf[r * wy::kAp + sc + 1] = x1;
+      reinterpret_cast<__nv_bfloat162 *>(tp)[e >> 1] = __floats2bfloat162_rn(x0, x1);
+    }
+  }
+  __syncthreads();
+  // ---- W = T' (K+ ⊙ e^{b_m}) = (T' K+) e^{b_m} per channel: warp w, rows 16 w
+  {
+    float acc[DK / 8][4];
+    zero(acc);
+    wmma(acc, 16 * warp, 0, kCh, [&](int m, int kk) { return tf(Tf[m * wy::kAp + kk]); },
+         [&](int kk, int nn) { return bfbits(sm.kp + kk * PH + nn); }, lane);
+    bf16 *W = reinterpret_cast<bf16 *>(wc + O::w);
+    each(acc, 16 * warp, 0, lane,
+         [&](int r, int c, float &x) { W[r * DK + c] = __float2bfloat16_rn(x * __expf(sm.bm[c])); });
+  }
+}
+
+// ============================================================ phase 2
+template <int DK>
+struct KwChainSmem {
+  float s[DK * kVW], u[kCh * kVW], gl[DK];
+  __nv_bfloat16 tp[kCh * kCP], p[kCh * kCP], w[kCh * Pitch<DK>::h], qt[kCh * Pitch<DK>::h],
+      kt[kCh * Pitch<DK>::h], v[kCh * kVP];
+};
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(128) kdw_chain_kernel(const __nv_bfloat16 *__restrict__ v,
+                                                        __nv_bfloat16 *__restrict__ o, const float *__restrict__ S0,
+                                                        float *__restrict__ S_final, int T,
+                                                        const uint8_t *__restrict__ ws) {
+  constexpr int PH = Pitch<DK>::h, NCB = DV / kVW, RT = DK / 64;
+  using O = KwOff<DK>;
+  using bf16 = __nv_bfloat16;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  KwChainSmem<DK> &sm = *reinterpret_cast<KwChainSmem<DK> *>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x / NCB, c0 = (blockIdx.x % NCB) * kVW;
+  const int nch = (T + kCh - 1) / kCh;
+  // a chunk's tiles in two groups: T', W, Q e^B and v are read in phase 1 only (the next
+  // chunk's copies start once phase 1 is done), P, K e^{B_L - B} and e^{B_L} in phase 2
+  auto issue_a = [&](int i) {
+    const uint8_t *wc = ws + ((size_t)bh * nch + i) * O::bytes;
+    const int t0 = i * kCh, n = min(kCh, T - t0);
+    rows_async<kCh, kCP>(sm.tp, reinterpret_cast<const bf16 *>(wc + O::tp), kCh, tid, 128);
+    rows_async<DK, PH>(sm.w, reinterpret_cast<const bf16 *>(wc + O::w), kCh, tid, 128);
+    rows_async<DK, PH>(sm.qt, reinterpret_cast<const bf16 *>(wc + O::qt), kCh, tid, 128);
+    const bf16 *vs = v + ((size_t)bh * T + t0) * DV + c0;
+    for (int x = tid; x < kCh * (kVW / 8); x += 128) {
+      const int r = x / (kVW / 8), c = (x % (kVW / 8)) * 8;
+      const bool ok = r < n;
+      cpa16(sm.v + r * kVP + c, vs + (ok ? (size_t)r * DV + c : 0), ok);
+    }
+    cp_commit();
+  };
+  auto issue_b = [&](int i) {
+    const uint8_t *wc = ws + ((size_t)bh * nch + i) * O::bytes;
+    rows_async<kCh, kCP>(sm.p, reinterpret_cast<const bf16 *>(wc + O::p), kCh, tid, 128);
+    rows_async<DK, PH>(sm.kt, reinterpret_cast<const bf16 *>(wc + O::kt), kCh, tid, 128);
+    for (int x = tid; x < DK / 4; x += 128) cpa16(sm.gl + 4 * x, wc + O::gl + 16 * x, true);
+    cp_commit();
+  };
+  // S[:, c0 .. c0 + 32) in registers: warp w holds row tiles w + 4 rt, four 8-column tiles
+  float S[RT][4][4];
+#pragma unroll
+  for (int rt = 0; rt < RT; ++rt) {
+    zero(S[rt]);
+    if (S0)
+      each(S[rt], 16 * (warp + 4 * rt), 0, lane,
+           [&](int r, int c, float &x) { x = __ldg(S0 + ((size_t)bh * DK + r) * DV + c0 + c); });
+  }
+  issue_a(0);
+  issue_b(0);
+  for (int i = 0; i < nch; ++i) {
+    const int t0 = i * kCh, n = min(kCh, T - t0);
+    const size_t row0 = (size_t)bh * T + t0;
+#pragma unroll
+    for (int rt = 0; rt < RT; ++rt)
+      each(S[rt], 16 * (warp + 4 * rt), 0, lane, [&](int r, int c, float &x) { fw<kVW>(sm.s, r, c) = x; });
+    cp_wait<0>();
+    __syncthreads();
+    // ---- phase 1 (warp w, rows 16 w): U = T' V - W S; R = (Q ⊙ e^B) S
+    float u[4][4], rr[4][4];
+    zero(u);
+    zero(rr);
+    wmma(u, 16 * warp, 0, kCh, [&](int m, int kk) { return bfbits(sm.tp + m * kCP + kk); },
+         [&](int kk, int nn) { return bfbits(sm.v + kk * kVP + nn); }, lane);
+    wmma(u, 16 * warp, 0, DK, [&](int m, int kk) { return bfbits(sm.w + m * PH + kk) ^ 0x80000000u; },
+         [&](int kk, int nn) { return tf(fw<kVW>(sm.s, kk, nn)); }, lane);
+    wmma(rr, 16 * warp, 0, DK, [&](int m, int kk) { return bfbits(sm.qt + m * PH + kk); },
+         [&](int kk, int nn) { return tf(fw<kVW>(sm.s, kk, nn)); }, lane);
+    each(u, 16 * warp, 0, lane, [&](int r, int c, float &x) { fw<kVW>(sm.u, r, c) = x; });
+    __syncthreads();
+    if (i + 1 < nch) issue_a(i + 1);
+    // ---- phase 2: O = R + P U; S <- Diag(e^{B_L}) S + (K ⊙ e^{B_L - B})^T U
+    wmma(rr, 16 * warp, 0, kCh, [&](int m, int kk) { return bfbits(sm.p + m * kCP + kk); },
+         [&](int kk, int nn) { return tf(fw<kVW>(sm.u, kk, nn)); }, lane);
+    each(rr, 16 * warp, 0, lane, [&](int r, int c, float &x) {
+      if (r < n) o[(row0 + r) * DV + c0 + c] = __float2bfloat16_rn(x);
+    });
+#pragma unroll
+    for (int rt = 0; rt < RT; ++rt) {
+      const int m0 = 16 * (warp + 4 * rt);
+      each(S[rt], m0, 0, lane, [&](int r, int, float &x) { x *= sm.gl[r]; });
+      wmma(S[rt], m0, 0, kCh, [&](int m, int kk) { return bfbits(sm.kt + kk * PH + m); },
+           [&](int kk, int nn) { return tf(fw<kVW>(sm.u, kk, nn)); }, lane);
+    }
+    __syncthreads();
+    if (i + 1 < nch) issue_b(i + 1);
+  }
+  if (S_final) {
+#pragma unroll
+    for (int rt = 0; rt < RT; ++rt)
+      each(S[rt], 16 * (warp + 4 * rt), 0, lane,
+           [&](int r, int c, float &x) { S_final[((size_t)bh * DK + r) * DV + c0 + c] = x; });
+  }
+}
+
+template <class Smem, class K>
+cudaError_t set_smem(K kernel) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem));
+}
+
+template <int DK, int DV>
+int launch_typed(const ChunkParams &p, uint8_t *ws, cudaStream_t s) {
+  using bf16 = __nv_bfloat16;
+  const int BH = p.B * p.H, nch = (p.T + kCh - 1) / kCh;
+  cudaError_t e = set_smem<KwPreSmem<DK>>(kdw_pre_kernel<DK>);
+  if (e == cudaSuccess) e = set_smem<KwChainSmem<DK>>(kdw_chain_kernel<DK, DV>);
+  if (e == cudaSuccess) {
+    kdw_pre_kernel<DK><<<dim3(nch, BH), 128, sizeof(KwPreSmem<DK>), s>>>(
+        static_cast<const bf16 *>(p.q), static_cast<const bf16 *>(p.k), p.g, p.beta, p.T, ws);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) {
+    kdw_chain_kernel<DK, DV><<<(unsigned)(BH * (DV / kVW)), 128, sizeof(KwChainSmem<DK>), s>>>(
+        static_cast<const bf16 *>(p.v), static_cast<bf16 *>(p.o), p.S0, p.S_final, p.T, ws);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) {
+    set_error("la_chunk_fwd: LA_KDA kernel launch failed: %s", cudaGetErrorString(e));
+    return LA_ERR_CUDA;
+  }
+  return LA_OK;
+}
+
+}  // namespace
+
+size_t kda_wy_workspace_bytes(const ChunkParams &p) {
+  const size_t nch = (size_t)(p.T + kCh - 1) / kCh, BH = (size_t)p.B * p.H;
+  return BH * nch * (p.dk == 128 ? KwOff<128>::bytes : KwOff<64>::bytes);
+}
+
+int launch_kda_wy(const ChunkParams &p, void *workspace, cudaStream_t stream) {
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  if (p.dk == 128 && p.dv == 128) return launch_typed<128, 128>(p, ws, stream);
+  if (p.dk == 128) return launch_typed<128, 64>(p, ws, stream);
+  if (p.dv == 128) return launch_typed<64, 128>(p, ws, stream);
+  return launch_typed<64, 64>(p, ws, stream);
+}
+
+}  // namespace la

@@ -103,10 +103,14 @@ int launch_chunk_noncausal(const ChunkParams &p, void *workspace, cudaStream_t s
 // every (head, chunk) into a workspace of delta_wy_workspace_bytes(p) bytes (one
 // bf16 T' image per chunk), then the state chain on a CTA pair per head.
 size_t delta_wy_workspace_bytes(const ChunkParams &p);
+// Kimi Delta Attention's two-phase path (la_chunk_kda_wy.cu): the key side of
+// every chunk into `workspace` (kda_wy_workspace_bytes), then the state chain.
+size_t kda_wy_workspace_bytes(const ChunkParams &p);
+int launch_kda_wy(const ChunkParams &p, void *workspace, cudaStream_t stream);
 int launch_chunk_delta_wy(const ChunkParams &p, void *workspace, cudaStream_t stream);
 
 // Which chunk-forward kernel a shape goes to (host-side selection).
-enum Variant : int { kVariantSimt = 0, kVariantTc = 1, kVariantMat = 2, kVariantDeltaWy = 3 };
+enum Variant : int { kVariantSimt = 0, kVariantTc = 1, kVariantMat = 2, kVariantDeltaWy = 3, kVariantKdaWy = 4 };
 int select_variant(const ChunkParams &p, int *chunk_out);
 
 }  // namespace la

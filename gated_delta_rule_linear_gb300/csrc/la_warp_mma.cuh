@@ -138,6 +138,14 @@ __device__ __forceinline__ void state_async(float *dst, const float *src, int c0
     cpa16(dst + r * kPw + (c ^ swz16(r)), src + (size_t)r * DV + c0 + c, true);
   }
 }
+// a 64 x DK float32 matrix (row-major, contiguous) into the permuted layout fw<DK>
+template <int DK>
+__device__ __forceinline__ void wide_async(float *dst, const float *src, int tid, int nthr) {
+  for (int i = tid; i < kCh * DK / 4; i += nthr) {
+    const int r = i / (DK / 4), c = (i % (DK / 4)) * 4;
+    cpa16(dst + r * DK + (c ^ swz64(r)), src + 4 * i, true);
+  }
+}
 __device__ __forceinline__ float bf(const __nv_bfloat16 *p) { return __uint_as_float(bfbits(p)); }
 
 }  // namespace wm

@@ -131,3 +131,25 @@ def test_kda_rejects_float32_and_the_materialised_variant(monkeypatch):
     with pytest.raises(la.LAError) as e:
         run_cuda(_inputs(B=1, H=1, T=64))
     assert e.value.code == la.CONSTANTS["LA_ERR_UNSUPPORTED"]
+
+
+@pytest.mark.parametrize("dims", [(128, 128), (64, 64)])
+@pytest.mark.parametrize("T", [1, 65, 300])
+def test_kda_fused_kernel_parity(dims, T, monkeypatch):
+    # the default is the two-phase path; LA_KDA=tc keeps the fused sequential-phase kernel
+    monkeypatch.setenv("LA_KDA", "tc")
+    dk, dv = dims
+    inp = _inputs(B=1, H=2, T=T, dk=dk, dv=dv, seed=41)
+    o, S = run_cuda(inp)
+    o_ref, S_ref = run_oracle(inp)
+    assert_close(f64(o), o_ref, "bf16", f"kda fused T={T} o")
+    assert_close(f64(S), S_ref, "bf16", f"kda fused T={T} S")
+
+
+def test_kda_paths_agree(monkeypatch):
+    inp = _inputs(B=2, H=3, T=777, dk=128, dv=64, seed=42)
+    o_a, S_a = run_cuda(inp)
+    monkeypatch.setenv("LA_KDA", "tc")
+    o_b, S_b = run_cuda(inp)
+    assert_close(f64(o_a), f64(o_b), "bf16", "two-phase vs fused o")
+    assert_close(f64(S_a), f64(S_b), "bf16", "two-phase vs fused S_final")
