@@ -709,6 +709,17 @@ __host__ __device__ inline B2Layout b2_layout(int dk) {
   return L;
 }
 
+// 3-D map over a [BH][T][d] bf16 tensor with 128-row boxes {64, 128, 1}, 128B swizzle
+inline bool make_map128(CUtensorMap *m, const void *base, int d, int T, int BH) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * T};
+  cuuint32_t box[3] = {64u, (cuuint32_t)kC2, 1u};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int DK, int DV, int KIND>
 __global__ void __launch_bounds__(kB2Threads, 2)
 chunk_output128_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, const float *__restrict__ zws,
@@ -958,10 +969,8 @@ int launch_typed(const ChunkParams &p, uint8_t *ws, float *zws, cudaStream_t str
     if (e == cudaSuccess && p.C == kC2) {
       // the 128-token output pass: 128-row boxes, one CTA per (head, chunk, value half)
       CUtensorMap mq2, mk2, mv2, mo2;
-      if (!(make_map(&mq2, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DK, p.T, BH, 64, CU_TENSOR_MAP_SWIZZLE_128B, kC2) &&
-            make_map(&mk2, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DK, p.T, BH, 64, CU_TENSOR_MAP_SWIZZLE_128B, kC2) &&
-            make_map(&mv2, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DV, p.T, BH, 64, CU_TENSOR_MAP_SWIZZLE_128B, kC2) &&
-            make_map(&mo2, p.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DV, p.T, BH, 64, CU_TENSOR_MAP_SWIZZLE_128B, kC2))) {
+      if (!(make_map128(&mq2, p.q, DK, p.T, BH) && make_map128(&mk2, p.k, DK, p.T, BH) &&
+            make_map128(&mv2, p.v, DV, p.T, BH) && make_map128(&mo2, p.o, DV, p.T, BH))) {
         set_error("la_chunk_fwd: cuTensorMapEncodeTiled rejected a tensor map");
         return LA_ERR_CUDA;
       }

@@ -180,12 +180,12 @@ inline bool encode_fn() {
   return g_encode != nullptr;
 }
 
-// 3-D map over a [BH][T][d] row-major tensor, box {box_x, box_y, 1}.
+// 3-D map over a [BH][T][d] row-major tensor, box {box_x, 64, 1}.
 inline bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize, int d, int T,
-              int BH, int box_x, CUtensorMapSwizzle sw, int box_y = kC) {
+              int BH, int box_x, CUtensorMapSwizzle sw) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * esize, (cuuint64_t)d * esize * T};
-  cuuint32_t box[3] = {(cuuint32_t)box_x, (cuuint32_t)box_y, 1};
+  cuuint32_t box[3] = {(cuuint32_t)box_x, (cuuint32_t)kC, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return g_encode(m, dt, 3, const_cast<void *>(base), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
