@@ -37,12 +37,12 @@
  *     LA_ELU1_NORM where W = dv + 1 and column dv holds the normaliser z.
  *   - All pointers are DEVICE pointers owned by the caller. The library never
  *     frees or retains them. Device memory of its own is taken only by the
- *     materialised variant, the two-phase delta-rule variant and the
- *     non-causal form of la_chunk_fwd and by la_chunk_bwd and
- *     la_chunk_bwd_delta: workspaces
- *     allocated and freed on `stream` from a
- *     library-owned stream-ordered pool (one per device) that keeps freed
- *     memory for the next call.
+ *     materialised variant, the two-phase delta-rule variant, the LA_KDA
+ *     path and the non-causal form of la_chunk_fwd, by the bfloat16 path of
+ *     la_chunk_fwd_gdelta, and by la_chunk_bwd and la_chunk_bwd_delta:
+ *     workspaces allocated and freed on `stream` from a library-owned
+ *     stream-ordered pool (one per device) that keeps freed memory for the
+ *     next call.
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream);
  *     nothing synchronises with the host.
  *   - Return value: LA_OK, or an LA_ERR_* code with a message available from
