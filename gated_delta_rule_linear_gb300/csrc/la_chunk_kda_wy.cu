@@ -331,6 +331,10 @@ size_t kda_wy_workspace_bytes(const ChunkParams &p) {
 }
 
 int launch_kda_wy(const ChunkParams &p, void *workspace, cudaStream_t stream) {
+  if ((long long)p.B * p.H > 65535) {  // the pre-pass grid's y dimension
+    set_error("la_chunk_fwd: LA_KDA takes B*H <= 65535 (got %lld)", (long long)p.B * p.H);
+    return LA_ERR_UNSUPPORTED;
+  }
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   if (p.dk == 128 && p.dv == 128) return launch_typed<128, 128>(p, ws, stream);
   if (p.dk == 128) return launch_typed<128, 64>(p, ws, stream);

@@ -105,8 +105,8 @@ typedef struct CUstream_st *la_stream_t;
  * for LA_GLA, with the same range limit. la_chunk_fwd runs it in two phases
  * (every chunk's key side in parallel into a workspace of
  * B*H*ceil(T/64)*(3*64*dk*2 + 2*64*64*2 + dk*4) bytes from the library's
- * pool, then the state chain); LA_KDA=tc or LA_VARIANT=tc selects the fused
- * kernel instead. */
+ * pool, then the state chain; B*H <= 65535, else LA_ERR_UNSUPPORTED);
+ * LA_KDA=tc or LA_VARIANT=tc selects the fused kernel instead. */
 #define LA_KDA           6
 /* Outer-product gate: S_t = (alpha_t beta_t^T) ⊙ S_{t-1} + k_t v_t^T, a
  * key-axis gate alpha_t (row c of S) times a value-axis gate beta_t (column
