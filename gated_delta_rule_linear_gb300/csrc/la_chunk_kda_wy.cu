@@ -133,8 +133,7 @@ __global__ void __launch_bounds__(128) kdw_pre_kernel(const __nv_bfloat16 *__res
     for (int h = 0; h < 2; ++h) {
       float acc[8][4];
       zero(acc);
-      wmma(acc, rbase + 16 * h, 0, DK, [&](int m, int kk) { return bfbits(src + m * PH + kk); },
-           [&](int kk, int nn) { return bfbits(sm.km + nn * PH + kk); }, lane);
+      wmma16(acc, rbase + 16 * h, 0, DK, src, PH, sm.km, PH, lane);
       if (warp < 2)
         each(acc, rbase + 16 * h, 0, lane,
              [&](int r, int s, float &x) { P[r * kCh + s] = __float2bfloat16_rn(s <= r ? x : 0.f); });
@@ -187,8 +186,8 @@ __global__ void __launch_bounds__(128) kdw_pre_kernel(const __nv_bfloat16 *__res
   {
     float acc[DK / 8][4];
     zero(acc);
-    wmma(acc, 16 * warp, 0, kCh, [&](int m, int kk) { return tf(Tf[m * wy::kAp + kk]); },
-         [&](int kk, int nn) { return bfbits(sm.kp + kk * PH + nn); }, lane);
+    wmma_r(acc, 16 * warp, 0, kCh, [&](int m, int kk) { return tf(Tf[m * wy::kAp + kk]); },
+           [&](int kk, int nn) { return bfbits(sm.kp + kk * PH + nn); }, lane);
     bf16 *W = reinterpret_cast<bf16 *>(wc + O::w);
     each(acc, 16 * warp, 0, lane,
          [&](int r, int c, float &x) { W[r * DK + c] = __float2bfloat16_rn(x * __expf(sm.bm[c])); });
@@ -196,11 +195,15 @@ __global__ void __launch_bounds__(128) kdw_pre_kernel(const __nv_bfloat16 *__res
 }
 
 // ============================================================ phase 2
+// bf16 m16n8k16 warp MMAs: S and U enter them as bf16 copies (S^T and U^T, k
+// contiguous), the fp32 state stays in registers; the fragments of v (as B) and
+// of K e^{B_L - B} (as the transposed A of the state update) come from
+// ldmatrix.trans of their token-major tiles.
 template <int DK>
 struct KwChainSmem {
-  float s[DK * kVW], u[kCh * kVW], gl[DK];
+  float gl[DK];
   __nv_bfloat16 tp[kCh * kCP], p[kCh * kCP], w[kCh * Pitch<DK>::h], qt[kCh * Pitch<DK>::h],
-      kt[kCh * Pitch<DK>::h], v[kCh * kVP];
+      kt[kCh * Pitch<DK>::h], v[kCh * kVP], st[kVW * Pitch<DK>::h], ut[kVW * kCP];
 };
 
 template <int DK, int DV>
@@ -250,30 +253,46 @@ __global__ void __launch_bounds__(128) kdw_chain_kernel(const __nv_bfloat16 *__r
   }
   issue_a(0);
   issue_b(0);
+  const int g = lane >> 2, t = lane & 3;
   for (int i = 0; i < nch; ++i) {
     const int t0 = i * kCh, n = min(kCh, T - t0);
     const size_t row0 = (size_t)bh * T + t0;
+    // S^T as bf16 (value column, key channel): the thread's (r, c), (r, c + 1) pairs go to
+    // two rows of S^T; pack neighbouring key rows via a shuffle-free two-element store
 #pragma unroll
-    for (int rt = 0; rt < RT; ++rt)
-      each(S[rt], 16 * (warp + 4 * rt), 0, lane, [&](int r, int c, float &x) { fw<kVW>(sm.s, r, c) = x; });
+    for (int rt = 0; rt < RT; ++rt) {
+      const int m0 = 16 * (warp + 4 * rt);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = 8 * j + 2 * t;
+        sm.st[c * PH + m0 + g] = __float2bfloat16_rn(S[rt][j][0]);
+        sm.st[(c + 1) * PH + m0 + g] = __float2bfloat16_rn(S[rt][j][1]);
+        sm.st[c * PH + m0 + g + 8] = __float2bfloat16_rn(S[rt][j][2]);
+        sm.st[(c + 1) * PH + m0 + g + 8] = __float2bfloat16_rn(S[rt][j][3]);
+      }
+    }
     cp_wait<0>();
     __syncthreads();
     // ---- phase 1 (warp w, rows 16 w): U = T' V - W S; R = (Q ⊙ e^B) S
     float u[4][4], rr[4][4];
     zero(u);
     zero(rr);
-    wmma(u, 16 * warp, 0, kCh, [&](int m, int kk) { return bfbits(sm.tp + m * kCP + kk); },
-         [&](int kk, int nn) { return bfbits(sm.v + kk * kVP + nn); }, lane);
-    wmma(u, 16 * warp, 0, DK, [&](int m, int kk) { return bfbits(sm.w + m * PH + kk) ^ 0x80000000u; },
-         [&](int kk, int nn) { return tf(fw<kVW>(sm.s, kk, nn)); }, lane);
-    wmma(rr, 16 * warp, 0, DK, [&](int m, int kk) { return bfbits(sm.qt + m * PH + kk); },
-         [&](int kk, int nn) { return tf(fw<kVW>(sm.s, kk, nn)); }, lane);
-    each(u, 16 * warp, 0, lane, [&](int r, int c, float &x) { fw<kVW>(sm.u, r, c) = x; });
+    wmma16_bt(u, 16 * warp, 0, kCh, sm.tp, kCP, sm.v, kVP, lane);
+    wmma16<4, true>(u, 16 * warp, 0, DK, sm.w, PH, sm.st, PH, lane);
+    wmma16(rr, 16 * warp, 0, DK, sm.qt, PH, sm.st, PH, lane);
+    // U^T as bf16 for the phase-2 MMAs (value column, token)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = 8 * j + 2 * t, r = 16 * warp + g;
+      sm.ut[c * kCP + r] = __float2bfloat16_rn(u[j][0]);
+      sm.ut[(c + 1) * kCP + r] = __float2bfloat16_rn(u[j][1]);
+      sm.ut[c * kCP + r + 8] = __float2bfloat16_rn(u[j][2]);
+      sm.ut[(c + 1) * kCP + r + 8] = __float2bfloat16_rn(u[j][3]);
+    }
     __syncthreads();
     if (i + 1 < nch) issue_a(i + 1);
     // ---- phase 2: O = R + P U; S <- Diag(e^{B_L}) S + (K ⊙ e^{B_L - B})^T U
-    wmma(rr, 16 * warp, 0, kCh, [&](int m, int kk) { return bfbits(sm.p + m * kCP + kk); },
-         [&](int kk, int nn) { return tf(fw<kVW>(sm.u, kk, nn)); }, lane);
+    wmma16(rr, 16 * warp, 0, kCh, sm.p, kCP, sm.ut, kCP, lane);
     each(rr, 16 * warp, 0, lane, [&](int r, int c, float &x) {
       if (r < n) o[(row0 + r) * DV + c0 + c] = __float2bfloat16_rn(x);
     });
@@ -281,8 +300,7 @@ __global__ void __launch_bounds__(128) kdw_chain_kernel(const __nv_bfloat16 *__r
     for (int rt = 0; rt < RT; ++rt) {
       const int m0 = 16 * (warp + 4 * rt);
       each(S[rt], m0, 0, lane, [&](int r, int, float &x) { x *= sm.gl[r]; });
-      wmma(S[rt], m0, 0, kCh, [&](int m, int kk) { return bfbits(sm.kt + kk * PH + m); },
-           [&](int kk, int nn) { return tf(fw<kVW>(sm.u, kk, nn)); }, lane);
+      wmma16_at(S[rt], m0, 0, kCh, sm.kt, PH, sm.ut, kCP, lane);
     }
     __syncthreads();
     if (i + 1 < nch) issue_b(i + 1);

@@ -70,6 +70,105 @@ __device__ __forceinline__ void wmma(float (&acc)[NT][4], int m0, int n0, int K,
     }
   }
 }
+// wmma with the k loop kept rolled (four steps per iteration): for kernels whose
+// fully unrolled body would not stay in the instruction cache
+template <int NT, class GA, class GB>
+__device__ __forceinline__ void wmma_r(float (&acc)[NT][4], int m0, int n0, int K, GA ga, GB gb, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll 4
+  for (int k0 = 0; k0 < K; k0 += 8) {
+    uint32_t a[4] = {ga(m0 + g, k0 + t), ga(m0 + g + 8, k0 + t), ga(m0 + g, k0 + t + 4),
+                     ga(m0 + g + 8, k0 + t + 4)};
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      uint32_t b[2] = {gb(k0 + t, n0 + 8 * j + g), gb(k0 + t + 4, n0 + 8 * j + g)};
+      mma_16x8x8_tf32(acc[j], a, b);
+    }
+  }
+}
+// ---- bf16 operands: mma.sync m16n8k16 (fp32 accumulate). A is row-major with k
+// contiguous (element (m, k) at pa[m * lda + k]); B is given by columns with k
+// contiguous (element (k, n) at pb[n * ldb + k]); both row pitches in bf16 units,
+// even, with (pitch / 2) % 32 == 4 or 12 or 20 or 28 for conflict-free fragment reads.
+__device__ __forceinline__ void mma_16x8x16_bf16(float *d, const uint32_t *a, const uint32_t *b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+__device__ __forceinline__ uint32_t ld32(const __nv_bfloat16 *p) { return *reinterpret_cast<const uint32_t *>(p); }
+// acc[j] (16 x 8 tiles at rows m0.., columns n0 + 8 j) += A B over k in [0, K), K % 16 == 0;
+// neg flips the sign of A
+template <int NT, bool NEG = false>
+__device__ __forceinline__ void wmma16(float (&acc)[NT][4], int m0, int n0, int K, const __nv_bfloat16 *pa,
+                                       int lda, const __nv_bfloat16 *pb, int ldb, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  const __nv_bfloat16 *a0 = pa + (m0 + g) * lda + 2 * t, *a1 = a0 + 8 * lda;
+#pragma unroll
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    uint32_t a[4] = {ld32(a0 + k0), ld32(a1 + k0), ld32(a0 + k0 + 8), ld32(a1 + k0 + 8)};
+    if (NEG) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) a[e] ^= 0x80008000u;
+    }
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const __nv_bfloat16 *b0 = pb + (n0 + 8 * j + g) * ldb + k0 + 2 * t;
+      uint32_t b[2] = {ld32(b0), ld32(b0 + 8)};
+      mma_16x8x16_bf16(acc[j], a, b);
+    }
+  }
+}
+// The same with B given row-major (element (k, n) at pb[k * ldb + n], 16-byte rows):
+// each B fragment comes from one ldmatrix.trans of two 8 x 8 blocks.
+template <int NT>
+__device__ __forceinline__ void wmma16_bt(float (&acc)[NT][4], int m0, int n0, int K, const __nv_bfloat16 *pa,
+                                          int lda, const __nv_bfloat16 *pb, int ldb, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  const __nv_bfloat16 *a0 = pa + (m0 + g) * lda + 2 * t, *a1 = a0 + 8 * lda;
+  const int lr = (lane & 7) + 8 * ((lane >> 3) & 1);  // the row lanes 0..15 address
+#pragma unroll
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    uint32_t a[4] = {ld32(a0 + k0), ld32(a1 + k0), ld32(a0 + k0 + 8), ld32(a1 + k0 + 8)};
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      uint32_t b[2];
+      asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+                   : "=r"(b[0]), "=r"(b[1])
+                   : "r"(smem_u32(pb + (k0 + lr) * ldb + n0 + 8 * j)));
+      mma_16x8x16_bf16(acc[j], a, b);
+    }
+  }
+}
+// The same with A given transposed (element (m, k) at pa[k * lda + m], 16-byte rows):
+// each A fragment comes from one ldmatrix.trans of four 8 x 8 blocks.
+template <int NT>
+__device__ __forceinline__ void wmma16_at(float (&acc)[NT][4], int m0, int n0, int K, const __nv_bfloat16 *pa,
+                                          int lda, const __nv_bfloat16 *pb, int ldb, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  const int blk = lane >> 3, lr = lane & 7;  // lanes 8i .. 8i + 7 address block i's rows
+  const __nv_bfloat16 *arow = pa + (lr + 8 * (blk >> 1)) * lda + m0 + 8 * (blk & 1);
+#pragma unroll
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    uint32_t a[4];
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+                 : "r"(smem_u32(arow + k0 * lda)));
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const __nv_bfloat16 *b0 = pb + (n0 + 8 * j + g) * ldb + k0 + 2 * t;
+      uint32_t b[2] = {ld32(b0), ld32(b0 + 8)};
+      mma_16x8x16_bf16(acc[j], a, b);
+    }
+  }
+}
+// a float as the high half of a bf16 pair etc.
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
 // f(row, col, value) over the elements of an accumulator set (values may be changed)
 template <int NT, class F>
 __device__ __forceinline__ void each(float (&acc)[NT][4], int m0, int n0, int lane, F f) {
