@@ -166,8 +166,10 @@ __global__ void __launch_bounds__(128) kdw_pre_kernel(const __nv_bfloat16 *__res
     }
     __syncthreads();
   }
-  // ---- T' = T Diag(beta) (zero above the diagonal) in place and to the workspace: thread tid
-  //      owns row tid / 2, columns 32 (tid % 2) .. + 31
+  // ---- T' = T Diag(beta) (zero above the diagonal) as bf16, to the workspace and, for the W
+  //      product, into the Q+ tile (free since the scores): thread tid owns row tid / 2,
+  //      columns 32 (tid % 2) .. + 31
+  bf16 *tpb = sm.qp;
   {
     const int r = tid >> 1, c0 = (tid & 1) * 32;
     bf16 *tp = reinterpret_cast<bf16 *>(wc + O::tp) + r * kCh + c0;
@@ -176,9 +178,9 @@ __global__ void __launch_bounds__(128) kdw_pre_kernel(const __nv_bfloat16 *__res
       const int sc = c0 + e;
       const float x0 = sc <= r ? Tf[r * wy::kAp + sc] * sm.bet[sc] : 0.f;
       const float x1 = sc + 1 <= r ? Tf[r * wy::kAp + sc + 1] * sm.bet[sc + 1] : 0.f;
-      Tf[r * wy::kAp + sc] = x0;
-      Tf[r * wy::kAp + sc + 1] = x1;
-      reinterpret_cast<__nv_bfloat162 *>(tp)[e >> 1] = __floats2bfloat162_rn(x0, x1);
+      const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+      reinterpret_cast<__nv_bfloat162 *>(tp)[e >> 1] = h;
+      *reinterpret_cast<__nv_bfloat162 *>(tpb + r * PH + sc) = h;
     }
   }
   __syncthreads();
@@ -186,8 +188,7 @@ __global__ void __launch_bounds__(128) kdw_pre_kernel(const __nv_bfloat16 *__res
   {
     float acc[DK / 8][4];
     zero(acc);
-    wmma_r(acc, 16 * warp, 0, kCh, [&](int m, int kk) { return tf(Tf[m * wy::kAp + kk]); },
-           [&](int kk, int nn) { return bfbits(sm.kp + kk * PH + nn); }, lane);
+    wmma16_bt(acc, 16 * warp, 0, kCh, tpb, PH, sm.kp, PH, lane);
     bf16 *W = reinterpret_cast<bf16 *>(wc + O::w);
     each(acc, 16 * warp, 0, lane,
          [&](int r, int c, float &x) { W[r * DK + c] = __float2bfloat16_rn(x * __expf(sm.bm[c])); });
