@@ -58,7 +58,7 @@ KERNEL_SOURCES = {
     "backward_gla": [_CS + "la_backward.cu", _CS + "la_chunk_ws.cu"] + _COMMON,
     "decode": [_CS + "la_step.cu"],
     "gdelta": [_CS + "la_chunk_gdelta.cu", _CS + "la_chunk_gdelta_wy.cu", _CS + "la_warp_mma.cuh"],
-    "backward_gdn": [_CS + "la_backward_delta.cu", _CS + "la_wy.cuh", _CS + "la_tc_common.cuh"],
+    "backward_gdn": [_CS + "la_backward_delta.cu", _CS + "la_warp_mma.cuh", _CS + "la_wy.cuh", _CS + "la_tc_common.cuh"],
     "prologue": [_CS + "la_prologue.cu", _CS + "la_sm100.cuh"],
     "prologue_gla": [_CS + "la_prologue.cu", _CS + "la_sm100.cuh"],
 }

@@ -230,6 +230,7 @@ static int check_mode(int mode, const float *g, const float *beta, const char *f
 int la_chunk_fwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
                  void *o, const float *S0, float *S_final, int B, int H, int T, int dk, int dv,
                  int C, int mode, la_stream_t stream) {
+  la::NvtxRange nvtx_range("la_chunk_fwd");
   g_err[0] = '\0';
   const char *fn = "la_chunk_fwd";
   if (!q || !k || !v || !o) {
@@ -363,6 +364,7 @@ int la_chunk_fwd(const void *q, const void *k, const void *v, const float *g, co
 int la_recurrent_step(const void *q, const void *k, const void *v, const float *g,
                       const float *beta, void *o, float *S, int B, int H, int dk, int dv, int mode,
                       la_stream_t stream) {
+  la::NvtxRange nvtx_range("la_recurrent_step");
   g_err[0] = '\0';
   const char *fn = "la_recurrent_step";
   if (!q || !k || !v || !o || !S) {

@@ -257,6 +257,7 @@ extern "C" int la_chunk_bwd(const void *q, const void *k, const void *v, const f
                             const float *dS_final, const float *S0, void *dq_out, void *dk_out, void *dv_out,
                             float *dS0, float *dg_out, int B, int H, int T, int dk, int dv, int C, int mode,
                             la_stream_t stream) {
+  la::NvtxRange nvtx_range("la_chunk_bwd");
   void *dq = dq_out, *dkg = dk_out, *dvg = dv_out;
   const int dk_ = dk, dv_ = dv;
   const char *fn = "la_chunk_bwd";

@@ -711,6 +711,7 @@ extern "C" int la_chunk_bwd_delta(const void *q, const void *k, const void *v, c
                                   const void *dO, const float *dS_final, const float *S0, void *dq_out,
                                   void *dk_out, void *dv_out, float *dbeta_out, float *dg_out, float *dS0,
                                   int B, int H, int T, int dk, int dv, int C, int mode, la_stream_t stream) {
+  la::NvtxRange nvtx_range("la_chunk_bwd_delta");
   const char *fn = "la_chunk_bwd_delta";
   set_error("%s", "");
   if (!q || !k || !v || !dO || !dq_out || !dk_out || !dv_out) {

@@ -278,6 +278,7 @@ using namespace la;
 extern "C" int la_chunk_fwd_gdelta(const void *q, const void *k, const void *v, const void *a, const void *b,
                                    void *o, const float *S0, float *S_final, int B, int H, int T, int dk, int dv,
                                    int C, int mode, la_stream_t stream) {
+  la::NvtxRange nvtx_range("la_chunk_fwd_gdelta");
   const char *fn = "la_chunk_fwd_gdelta";
   set_error("%s", "");
   if (!q || !k || !v || !a || !b || !o) {

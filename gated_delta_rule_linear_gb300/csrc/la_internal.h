@@ -3,6 +3,8 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
+
 #include <cstdint>
 
 #include "../../include/la.h"
@@ -75,6 +77,15 @@ struct StepParams {
 // The library's stream-ordered workspace pool on the current device (keeps
 // freed memory for the next call), or null if it cannot be created.
 cudaMemPool_t library_pool();
+
+// An NVTX range around an entry point's host work and launches (header-only
+// NVTX; a no-op unless a profiler attaches to the process).
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange &) = delete;
+  NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 // Thread-local error message for la_last_error().
 void set_error(const char *fmt, ...);

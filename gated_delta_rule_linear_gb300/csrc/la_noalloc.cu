@@ -41,6 +41,7 @@ using namespace la;
 extern "C" int la_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *g,
                                     const float *beta, void *o, const float *S0, float *S_final, int B,
                                     int H, int T, int dk, int dv, int C, int mode, la_stream_t stream) {
+  la::NvtxRange nvtx_range("la_chunk_fwd_noalloc");
   const char *fn = "la_chunk_fwd_noalloc";
   set_error("%s", "");
   if (!q || !k || !v || !o) {

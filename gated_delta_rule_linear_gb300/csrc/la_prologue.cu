@@ -278,6 +278,7 @@ extern "C" int la_prologue(const void *xq, const void *xk, const void *xv, const
                            int gate_kind, int gate_width, float tau, const float *a_beta, void *q, void *k,
                            void *v, float *g, float *beta, int B, int H, int T, int dk, int dv, int flags,
                            la_stream_t stream) {
+  la::NvtxRange nvtx_range("la_prologue");
   const char *fn = "la_prologue";
   set_error("%s", "");
   if (!xq || !xk || !xv || !q || !k || !v) {
