@@ -92,6 +92,8 @@ void set_error(const char *fmt, ...);
 
 // Device status word of the current device (a __device__ variable).
 unsigned *status_word();
+// multiprocessors of the current device (0 when the query fails)
+int sm_count();
 
 // Launchers: return LA_OK or an LA_ERR_* code (message already set).
 int launch_chunk_simt(const ChunkParams &p, cudaStream_t stream);

@@ -143,7 +143,7 @@ __device__ __forceinline__ void wmma16_bt(float (&acc)[NT][4], int m0, int n0, i
 }
 // The same with A given transposed (element (m, k) at pa[k * lda + m], 16-byte rows):
 // each A fragment comes from one ldmatrix.trans of four 8 x 8 blocks.
-template <int NT>
+template <int NT, bool NEG = false>
 __device__ __forceinline__ void wmma16_at(float (&acc)[NT][4], int m0, int n0, int K, const __nv_bfloat16 *pa,
                                           int lda, const __nv_bfloat16 *pb, int ldb, int lane) {
   const int g = lane >> 2, t = lane & 3;
@@ -155,10 +155,38 @@ __device__ __forceinline__ void wmma16_at(float (&acc)[NT][4], int m0, int n0, i
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
                  : "r"(smem_u32(arow + k0 * lda)));
+    if (NEG) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) a[e] ^= 0x80008000u;
+    }
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
       const __nv_bfloat16 *b0 = pb + (n0 + 8 * j + g) * ldb + k0 + 2 * t;
       uint32_t b[2] = {ld32(b0), ld32(b0 + 8)};
+      mma_16x8x16_bf16(acc[j], a, b);
+    }
+  }
+}
+// The same with both operands through ldmatrix.trans: A given transposed (element
+// (m, k) at pa[k * lda + m]) and B given row-major (element (k, n) at pb[k * ldb + n]).
+template <int NT>
+__device__ __forceinline__ void wmma16_atbt(float (&acc)[NT][4], int m0, int n0, int K, const __nv_bfloat16 *pa,
+                                            int lda, const __nv_bfloat16 *pb, int ldb, int lane) {
+  const int blk = lane >> 3, lr = lane & 7;
+  const __nv_bfloat16 *arow = pa + (lr + 8 * (blk >> 1)) * lda + m0 + 8 * (blk & 1);
+  const int br = (lane & 7) + 8 * ((lane >> 3) & 1);
+#pragma unroll
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    uint32_t a[4];
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+                 : "r"(smem_u32(arow + k0 * lda)));
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      uint32_t b[2];
+      asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+                   : "=r"(b[0]), "=r"(b[1])
+                   : "r"(smem_u32(pb + (k0 + br) * ldb + n0 + 8 * j)));
       mma_16x8x16_bf16(acc[j], a, b);
     }
   }

@@ -143,3 +143,18 @@ def test_gdelta_bf16_paths_agree(monkeypatch):
     o_b, S_b = _gpu(inp)
     assert_close(f64(o_a), f64(o_b), "bf16", "two-phase vs CUDA-core o")
     assert_close(f64(S_a), f64(S_b), "bf16", "two-phase vs CUDA-core S_final")
+
+
+@pytest.mark.parametrize("dims", [(64, 64), (128, 128)])
+def test_gdelta_many_heads_single_buffered_chain(dims):
+    # more chain CTAs (heads x 16-column blocks) than SMs selects the single-buffered
+    # chain (two CTAs an SM); sampled heads against the oracle, ragged tail included
+    dk, dv = dims
+    B, H = 4, 160 * 16 // dv
+    assert B * H * (dv // 16) > torch.cuda.get_device_properties(0).multi_processor_count
+    inp = _inputs("bf16", B=B, H=H, T=321, dk=dk, dv=dv, seed=33)
+    o, S = _gpu(inp)
+    heads = [(0, 0), (B - 1, H - 1), (2, H // 2)]
+    o_ref, S_ref = _ref(inp, heads)
+    assert_close(np.stack([f64(o[b, h]) for b, h in heads])[None], o_ref, "bf16", "gdelta o (many heads)")
+    assert_close(np.stack([f64(S[b, h]) for b, h in heads])[None], S_ref, "bf16", "gdelta S (many heads)")
