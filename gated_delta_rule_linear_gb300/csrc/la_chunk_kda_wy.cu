@@ -4,7 +4,8 @@
 //
 //   S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T,  o_t = S_t^T q_t,
 //
-// bf16 inputs, fp32 state, on tf32 warp MMAs. Per chunk of C = 64 rows with
+// bf16 inputs, fp32 state, on bf16 warp MMAs (16 x 8 x 16, fp32 accumulate;
+// the solve's block levels in tf32). Per chunk of C = 64 rows with
 // the per-channel inclusive prefix B[r][c] of the log-gates, its midpoint row
 // b_m[c] = B[31][c] and its last row B_L[c], the WY/UT form ("Talk Linear
 // Attention" section 6.2) with the decay folded per channel is
@@ -23,9 +24,11 @@
 // operands (bf16, as the fused kernels use them), A and P from one
 // [Q+; K+] K-^T product, T by substitution, T', W;
 // written to a workspace as bf16 operands (with Q ⊙ e^B and K ⊙ e^{B_L - B})
-// and e^{B_L}. Phase 2 (kdw_chain_kernel, per head and 32 value columns -- each value
-// column of S evolves on its own): the chunks in order, S in registers, the
-// next chunk's tiles copied while the current one finishes. A tail chunk is
+// and e^{B_L}. Phase 2 (kdw_chain_kernel, per head and 64 value columns -- each value
+// column of S evolves on its own): the chunks in order, S in registers, eight
+// warps (four row strips x two 32-column halves) sharing one copy of each
+// chunk's images, the next chunk's tiles copied during the whole of the
+// current one (two buffers). A tail chunk is
 // padded with zero rows and zero gates, which leaves every real row's result
 // unchanged.
 #include <cuda_bf16.h>
@@ -41,7 +44,7 @@ namespace {
 using namespace wm;
 
 constexpr int kMid = kCh / 2 - 1;  // the fold's midpoint row
-constexpr int kVW = 32;            // value columns per chain CTA
+constexpr int kVW = 64;            // value columns per chain CTA (two halves of 32)
 constexpr int kVP = kVW + 8;       // row pitch (bf16) of the chain's v tile
 constexpr int kCP = kCh + 8;       // row pitch (bf16) of its C x C tiles
 
@@ -200,15 +203,22 @@ __global__ void __launch_bounds__(128) kdw_pre_kernel(const __nv_bfloat16 *__res
 // contiguous), the fp32 state stays in registers; the fragments of v (as B) and
 // of K e^{B_L - B} (as the transposed A of the state update) come from
 // ldmatrix.trans of their token-major tiles.
+// One chunk's tiles of the chain; two of them, so that chunk i + 1's copies run
+// during all of chunk i.
 template <int DK>
-struct KwChainSmem {
+struct KwTiles {
   float gl[DK];
   __nv_bfloat16 tp[kCh * kCP], p[kCh * kCP], w[kCh * Pitch<DK>::h], qt[kCh * Pitch<DK>::h],
-      kt[kCh * Pitch<DK>::h], v[kCh * kVP], st[kVW * Pitch<DK>::h], ut[kVW * kCP];
+      kt[kCh * Pitch<DK>::h], v[kCh * kVP];
+};
+template <int DK>
+struct KwChainSmem {
+  KwTiles<DK> x[2];
+  __nv_bfloat16 st[kVW * Pitch<DK>::h], ut[kVW * kCP];
 };
 
 template <int DK, int DV>
-__global__ void __launch_bounds__(128) kdw_chain_kernel(const __nv_bfloat16 *__restrict__ v,
+__global__ void __launch_bounds__(256) kdw_chain_kernel(const __nv_bfloat16 *__restrict__ v,
                                                         __nv_bfloat16 *__restrict__ o, const float *__restrict__ S0,
                                                         float *__restrict__ S_final, int T,
                                                         const uint8_t *__restrict__ ws) {
@@ -218,99 +228,104 @@ __global__ void __launch_bounds__(128) kdw_chain_kernel(const __nv_bfloat16 *__r
   extern __shared__ __align__(16) uint8_t smem_raw[];
   KwChainSmem<DK> &sm = *reinterpret_cast<KwChainSmem<DK> *>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rh = warp & 3, n0 = (warp >> 2) * 32;  // the warp's row strip and column half
   const int bh = blockIdx.x / NCB, c0 = (blockIdx.x % NCB) * kVW;
   const int nch = (T + kCh - 1) / kCh;
-  // a chunk's tiles in two groups: T', W, Q e^B and v are read in phase 1 only (the next
-  // chunk's copies start once phase 1 is done), P, K e^{B_L - B} and e^{B_L} in phase 2
-  auto issue_a = [&](int i) {
+  // one chunk's tiles, one commit group
+  auto issue = [&](int i, KwTiles<DK> &x) {
     const uint8_t *wc = ws + ((size_t)bh * nch + i) * O::bytes;
     const int t0 = i * kCh, n = min(kCh, T - t0);
-    rows_async<kCh, kCP>(sm.tp, reinterpret_cast<const bf16 *>(wc + O::tp), kCh, tid, 128);
-    rows_async<DK, PH>(sm.w, reinterpret_cast<const bf16 *>(wc + O::w), kCh, tid, 128);
-    rows_async<DK, PH>(sm.qt, reinterpret_cast<const bf16 *>(wc + O::qt), kCh, tid, 128);
+    rows_async<kCh, kCP>(x.tp, reinterpret_cast<const bf16 *>(wc + O::tp), kCh, tid, 256);
+    rows_async<DK, PH>(x.w, reinterpret_cast<const bf16 *>(wc + O::w), kCh, tid, 256);
+    rows_async<DK, PH>(x.qt, reinterpret_cast<const bf16 *>(wc + O::qt), kCh, tid, 256);
+    rows_async<kCh, kCP>(x.p, reinterpret_cast<const bf16 *>(wc + O::p), kCh, tid, 256);
+    rows_async<DK, PH>(x.kt, reinterpret_cast<const bf16 *>(wc + O::kt), kCh, tid, 256);
+    for (int e = tid; e < DK / 4; e += 256) cpa16(x.gl + 4 * e, wc + O::gl + 16 * e, true);
     const bf16 *vs = v + ((size_t)bh * T + t0) * DV + c0;
-    for (int x = tid; x < kCh * (kVW / 8); x += 128) {
-      const int r = x / (kVW / 8), c = (x % (kVW / 8)) * 8;
+    for (int e = tid; e < kCh * (kVW / 8); e += 256) {
+      const int r = e / (kVW / 8), c = (e % (kVW / 8)) * 8;
       const bool ok = r < n;
-      cpa16(sm.v + r * kVP + c, vs + (ok ? (size_t)r * DV + c : 0), ok);
+      cpa16(x.v + r * kVP + c, vs + (ok ? (size_t)r * DV + c : 0), ok);
     }
     cp_commit();
   };
-  auto issue_b = [&](int i) {
-    const uint8_t *wc = ws + ((size_t)bh * nch + i) * O::bytes;
-    rows_async<kCh, kCP>(sm.p, reinterpret_cast<const bf16 *>(wc + O::p), kCh, tid, 128);
-    rows_async<DK, PH>(sm.kt, reinterpret_cast<const bf16 *>(wc + O::kt), kCh, tid, 128);
-    for (int x = tid; x < DK / 4; x += 128) cpa16(sm.gl + 4 * x, wc + O::gl + 16 * x, true);
-    cp_commit();
-  };
-  // S[:, c0 .. c0 + 32) in registers: warp w holds row tiles w + 4 rt, four 8-column tiles
+  // S[:, c0 + n0 .. + 32) in registers: row tiles rh + 4 rt, four 8-column tiles
   float S[RT][4][4];
 #pragma unroll
   for (int rt = 0; rt < RT; ++rt) {
     zero(S[rt]);
     if (S0)
-      each(S[rt], 16 * (warp + 4 * rt), 0, lane,
+      each(S[rt], 16 * (rh + 4 * rt), n0, lane,
            [&](int r, int c, float &x) { x = __ldg(S0 + ((size_t)bh * DK + r) * DV + c0 + c); });
   }
-  issue_a(0);
-  issue_b(0);
+  issue(0, sm.x[0]);
   const int g = lane >> 2, t = lane & 3;
   for (int i = 0; i < nch; ++i) {
     const int t0 = i * kCh, n = min(kCh, T - t0);
     const size_t row0 = (size_t)bh * T + t0;
-    // S^T as bf16 (value column, key channel): the thread's (r, c), (r, c + 1) pairs go to
-    // two rows of S^T; pack neighbouring key rows via a shuffle-free two-element store
+    KwTiles<DK> &x = sm.x[i & 1];
+    const bool more = i + 1 < nch;
+    // the buffer chunk i - 1 used is free (the barrier that ended it)
+    if (more) issue(i + 1, sm.x[(i + 1) & 1]);
+    // S^T as bf16 (value column, key channel)
 #pragma unroll
     for (int rt = 0; rt < RT; ++rt) {
-      const int m0 = 16 * (warp + 4 * rt);
+      const int m0 = 16 * (rh + 4 * rt);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int c = 8 * j + 2 * t;
+        const int c = n0 + 8 * j + 2 * t;
         sm.st[c * PH + m0 + g] = __float2bfloat16_rn(S[rt][j][0]);
         sm.st[(c + 1) * PH + m0 + g] = __float2bfloat16_rn(S[rt][j][1]);
         sm.st[c * PH + m0 + g + 8] = __float2bfloat16_rn(S[rt][j][2]);
         sm.st[(c + 1) * PH + m0 + g + 8] = __float2bfloat16_rn(S[rt][j][3]);
       }
     }
-    cp_wait<0>();
+    if (more)
+      cp_wait<1>();
+    else
+      cp_wait<0>();
     __syncthreads();
-    // ---- phase 1 (warp w, rows 16 w): U = T' V - W S; R = (Q ⊙ e^B) S
+    // ---- phase 1 (rows 16 rh, columns n0 ..): U = T' V - W S; R = (Q ⊙ e^B) S
     float u[4][4], rr[4][4];
     zero(u);
     zero(rr);
-    wmma16_bt(u, 16 * warp, 0, kCh, sm.tp, kCP, sm.v, kVP, lane);
-    wmma16<4, true>(u, 16 * warp, 0, DK, sm.w, PH, sm.st, PH, lane);
-    wmma16(rr, 16 * warp, 0, DK, sm.qt, PH, sm.st, PH, lane);
+    wmma16_bt(u, 16 * rh, n0, kCh, x.tp, kCP, x.v, kVP, lane);
+    wmma16<4, true>(u, 16 * rh, n0, DK, x.w, PH, sm.st, PH, lane);
+    wmma16(rr, 16 * rh, n0, DK, x.qt, PH, sm.st, PH, lane);
     // U^T as bf16 for the phase-2 MMAs (value column, token)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int c = 8 * j + 2 * t, r = 16 * warp + g;
+      const int c = n0 + 8 * j + 2 * t, r = 16 * rh + g;
       sm.ut[c * kCP + r] = __float2bfloat16_rn(u[j][0]);
       sm.ut[(c + 1) * kCP + r] = __float2bfloat16_rn(u[j][1]);
       sm.ut[c * kCP + r + 8] = __float2bfloat16_rn(u[j][2]);
       sm.ut[(c + 1) * kCP + r + 8] = __float2bfloat16_rn(u[j][3]);
     }
     __syncthreads();
-    if (i + 1 < nch) issue_a(i + 1);
     // ---- phase 2: O = R + P U; S <- Diag(e^{B_L}) S + (K ⊙ e^{B_L - B})^T U
-    wmma16(rr, 16 * warp, 0, kCh, sm.p, kCP, sm.ut, kCP, lane);
-    each(rr, 16 * warp, 0, lane, [&](int r, int c, float &x) {
-      if (r < n) o[(row0 + r) * DV + c0 + c] = __float2bfloat16_rn(x);
-    });
+    wmma16(rr, 16 * rh, n0, kCh, x.p, kCP, sm.ut, kCP, lane);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = 16 * rh + g, c = c0 + n0 + 8 * j + 2 * t;
+      if (r < n)
+        *reinterpret_cast<__nv_bfloat162 *>(o + (row0 + r) * DV + c) = __floats2bfloat162_rn(rr[j][0], rr[j][1]);
+      if (r + 8 < n)
+        *reinterpret_cast<__nv_bfloat162 *>(o + (row0 + r + 8) * DV + c) =
+            __floats2bfloat162_rn(rr[j][2], rr[j][3]);
+    }
 #pragma unroll
     for (int rt = 0; rt < RT; ++rt) {
-      const int m0 = 16 * (warp + 4 * rt);
-      each(S[rt], m0, 0, lane, [&](int r, int, float &x) { x *= sm.gl[r]; });
-      wmma16_at(S[rt], m0, 0, kCh, sm.kt, PH, sm.ut, kCP, lane);
+      const int m0 = 16 * (rh + 4 * rt);
+      each(S[rt], m0, n0, lane, [&](int r, int, float &y) { y *= x.gl[r]; });
+      wmma16_at(S[rt], m0, n0, kCh, x.kt, PH, sm.ut, kCP, lane);
     }
     __syncthreads();
-    if (i + 1 < nch) issue_b(i + 1);
   }
   if (S_final) {
 #pragma unroll
     for (int rt = 0; rt < RT; ++rt)
-      each(S[rt], 16 * (warp + 4 * rt), 0, lane,
-           [&](int r, int c, float &x) { S_final[((size_t)bh * DK + r) * DV + c0 + c] = x; });
+      each(S[rt], 16 * (rh + 4 * rt), n0, lane,
+           [&](int r, int c, float &y) { S_final[((size_t)bh * DK + r) * DV + c0 + c] = y; });
   }
 }
 
@@ -331,7 +346,7 @@ int launch_typed(const ChunkParams &p, uint8_t *ws, cudaStream_t s) {
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) {
-    kdw_chain_kernel<DK, DV><<<(unsigned)(BH * (DV / kVW)), 128, sizeof(KwChainSmem<DK>), s>>>(
+    kdw_chain_kernel<DK, DV><<<(unsigned)(BH * (DV / kVW)), 256, sizeof(KwChainSmem<DK>), s>>>(
         static_cast<const bf16 *>(p.v), static_cast<bf16 *>(p.o), p.S0, p.S_final, p.T, ws);
     e = cudaGetLastError();
   }
