@@ -59,41 +59,46 @@ struct KwOff {
 };
 
 // ============================================================ phase 1
-// One CTA per chunk, 128 threads, ~88 KB of shared memory (two CTAs per SM):
-// a thread per key channel forms the channel's prefix in registers and the
-// folded rows; the products run on the bf16 operand tiles; T comes from 16 x 16
-// diagonal blocks and three block levels on tf32 warp MMAs (la_wy.cuh).
+// One CTA per chunk, 128 threads, three operand tiles of shared memory (~53 KB
+// at dk = 128: four CTAs per SM): a thread per key channel forms the channel's
+// prefix in registers and folds Q and K in place (Q+, K+) and into K-; the
+// products run on the bf16 operand tiles; T comes from 16 x 16 diagonal blocks
+// and three block levels on tf32 warp MMAs (la_wy.cuh). Once the products are
+// taken, A (held in registers across the barrier) replaces K-, T replaces Q+,
+// and T' as bf16 replaces A.
 template <int DK>
 struct KwPreSmem {
   union {
-    struct {
-      __nv_bfloat16 q[kCh * Pitch<DK>::h], k[kCh * Pitch<DK>::h];
-    } in;  // the chunk's rows, until the fold is done
-    struct {
-      float af[kCh * wy::kAp], tf[kCh * wy::kAp];  // A, then T and T' = T Diag(beta)
-    } s;
-  } u;
-  __nv_bfloat16 qp[kCh * Pitch<DK>::h], kp[kCh * Pitch<DK>::h], km[kCh * Pitch<DK>::h];
+    __nv_bfloat16 qp[kCh * Pitch<DK>::h];  // Q, folded in place into Q+
+    float tf[kCh * wy::kAp];               // then T
+  } r1;
+  __nv_bfloat16 kp[kCh * Pitch<DK>::h];  // K, folded in place into K+
+  union {
+    __nv_bfloat16 km[kCh * Pitch<DK>::h];  // K-
+    float af[kCh * wy::kAp];               // then A
+    __nv_bfloat16 tpb[kCh * kCP];          // then T' (bf16), the W product's A operand
+  } r3;
   float bet[kCh], bm[DK];
 };
 
 template <int DK>
-__global__ void __launch_bounds__(128) kdw_pre_kernel(const __nv_bfloat16 *__restrict__ q,
-                                                      const __nv_bfloat16 *__restrict__ k,
-                                                      const float *__restrict__ g, const float *__restrict__ beta,
-                                                      int T, uint8_t *__restrict__ ws) {
+__global__ void __launch_bounds__(128, 4) kdw_pre_kernel(const __nv_bfloat16 *__restrict__ q,
+                                                         const __nv_bfloat16 *__restrict__ k,
+                                                         const float *__restrict__ g, const float *__restrict__ beta,
+                                                         int T, uint8_t *__restrict__ ws) {
   constexpr int PH = Pitch<DK>::h;
   using O = KwOff<DK>;
   using bf16 = __nv_bfloat16;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   KwPreSmem<DK> &sm = *reinterpret_cast<KwPreSmem<DK> *>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gq = lane >> 2, tq = lane & 3;
   const int i = blockIdx.x, bh = blockIdx.y, nch = gridDim.x;
   const int t0 = i * kCh, n = min(kCh, T - t0);
   const size_t row0 = (size_t)bh * T + t0;
   uint8_t *wc = ws + ((size_t)bh * nch + i) * O::bytes;
-  rows_async<DK, PH>(sm.u.in.q, q + row0 * DK, n, tid, 128);
-  rows_async<DK, PH>(sm.u.in.k, k + row0 * DK, n, tid, 128);
+  rows_async<DK, PH>(sm.r1.qp, q + row0 * DK, n, tid, 128);
+  rows_async<DK, PH>(sm.kp, k + row0 * DK, n, tid, 128);
   cp_commit();
   if (tid < kCh) sm.bet[tid] = tid < n ? (beta ? __ldg(beta + row0 + tid) : 1.f) : 0.f;
   // ---- channel c = tid: the prefix B[.][c] in registers (zero gates past the end)
@@ -108,7 +113,7 @@ __global__ void __launch_bounds__(128) kdw_pre_kernel(const __nv_bfloat16 *__res
   }
   cp_wait<0>();
   __syncthreads();
-  // ---- folded rows: Q+, K+, K- (tiles), Q e^B and K e^{B_L - B} (workspace), e^{B_L}
+  // ---- folded rows: Q+, K+ (in place), K- (tiles), Q e^B and K e^{B_L - B} (workspace), e^{B_L}
   if (tid < DK) {
     const int c = tid;
     const float bmid = bc[kMid], bl = bc[kCh - 1];
@@ -117,39 +122,51 @@ __global__ void __launch_bounds__(128) kdw_pre_kernel(const __nv_bfloat16 *__res
     bf16 *qt = reinterpret_cast<bf16 *>(wc + O::qt), *kt = reinterpret_cast<bf16 *>(wc + O::kt);
 #pragma unroll
     for (int r = 0; r < kCh; ++r) {
-      const float qx = bf(sm.u.in.q + r * PH + c), kx = bf(sm.u.in.k + r * PH + c);
+      const float qx = bf(sm.r1.qp + r * PH + c), kx = bf(sm.kp + r * PH + c);
       const float d = bc[r] - bmid, ep = __expf(d), em = __expf(-d);
-      sm.qp[r * PH + c] = __float2bfloat16_rn(qx * ep);
+      sm.r1.qp[r * PH + c] = __float2bfloat16_rn(qx * ep);
       sm.kp[r * PH + c] = __float2bfloat16_rn(kx * ep);
-      sm.km[r * PH + c] = __float2bfloat16_rn(kx * em);
+      sm.r3.km[r * PH + c] = __float2bfloat16_rn(kx * em);
       qt[r * DK + c] = __float2bfloat16_rn(qx * __expf(bc[r]));
       kt[r * DK + c] = __float2bfloat16_rn(kx * __expf(bl - bc[r]));
     }
   }
   __syncthreads();
-  // ---- [Q+; K+] K-^T: warps 0, 1 the rows of Q+ (P), warps 2, 3 the rows of K+ (A)
+  // ---- [Q+; K+] K-^T: warps 0, 1 the rows of Q+ (P, stored at once), warps 2, 3 the
+  //      rows of K+ (A, held until every warp is done with K-)
+  const int rbase = (warp & 1) * 32;
+  float acc[2][8][4];
   {
-    const bf16 *src = warp < 2 ? sm.qp : sm.kp;
-    bf16 *P = reinterpret_cast<bf16 *>(wc + O::p);
-    const int rbase = (warp & 1) * 32;
+    const bf16 *src = warp < 2 ? sm.r1.qp : sm.kp;
+    __nv_bfloat162 *P = reinterpret_cast<__nv_bfloat162 *>(wc + O::p);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      float acc[8][4];
-      zero(acc);
-      wmma16(acc, rbase + 16 * h, 0, DK, src, PH, sm.km, PH, lane);
-      if (warp < 2)
-        each(acc, rbase + 16 * h, 0, lane,
-             [&](int r, int s, float &x) { P[r * kCh + s] = __float2bfloat16_rn(s <= r ? x : 0.f); });
-      else  // rounded to tf32 for the block MMAs of the solve
-        each(acc, rbase + 16 * h, 0, lane, [&](int r, int s, float &x) {
-          sm.u.s.af[r * wy::kAp + s] = s < r ? wy::round_tf32(sm.bet[r] * x) : 0.f;
-        });
+      zero(acc[h]);
+      wmma16(acc[h], rbase + 16 * h, 0, DK, src, PH, sm.r3.km, PH, lane);
+      if (warp < 2) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = rbase + 16 * h + gq, sc = 8 * j + 2 * tq;
+          const float *x = acc[h][j];
+          P[(r * kCh + sc) >> 1] = __floats2bfloat162_rn(sc <= r ? x[0] : 0.f, sc + 1 <= r ? x[1] : 0.f);
+          P[((r + 8) * kCh + sc) >> 1] =
+              __floats2bfloat162_rn(sc <= r + 8 ? x[2] : 0.f, sc + 1 <= r + 8 ? x[3] : 0.f);
+        }
+      }
     }
+  }
+  __syncthreads();
+  if (warp >= 2) {  // rounded to tf32 for the block MMAs of the solve
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      each(acc[h], rbase + 16 * h, 0, lane, [&](int r, int s, float &x) {
+        sm.r3.af[r * wy::kAp + s] = s < r ? wy::round_tf32(sm.bet[r] * x) : 0.f;
+      });
   }
   __syncthreads();
   // ---- T = (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution, then the
   //      off-diagonal blocks in three levels, T_ij = -T_ii sum_{j<=k<i} A_ik T_kj
-  float *Af = sm.u.s.af, *Tf = sm.u.s.tf;
+  float *Af = sm.r3.af, *Tf = sm.r1.tf;
   if (tid < kCh) wy::diag_inverse_16(Af, Tf, tid >> 4, tid & 15);
   __syncthreads();
 #pragma unroll 1
@@ -170,31 +187,40 @@ __global__ void __launch_bounds__(128) kdw_pre_kernel(const __nv_bfloat16 *__res
     __syncthreads();
   }
   // ---- T' = T Diag(beta) (zero above the diagonal) as bf16, to the workspace and, for the W
-  //      product, into the Q+ tile (free since the scores): thread tid owns row tid / 2,
+  //      product, in place of A (free since the last level): thread tid owns row tid / 2,
   //      columns 32 (tid % 2) .. + 31
-  bf16 *tpb = sm.qp;
+  bf16 *tpb = sm.r3.tpb;
   {
     const int r = tid >> 1, c0 = (tid & 1) * 32;
+    float x[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int sc = c0 + e;
+      x[e] = sc <= r ? Tf[r * wy::kAp + sc] * sm.bet[sc] : 0.f;
+    }
+    __syncthreads();  // every thread has read its row of T before T' overwrites A
     bf16 *tp = reinterpret_cast<bf16 *>(wc + O::tp) + r * kCh + c0;
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
-      const int sc = c0 + e;
-      const float x0 = sc <= r ? Tf[r * wy::kAp + sc] * sm.bet[sc] : 0.f;
-      const float x1 = sc + 1 <= r ? Tf[r * wy::kAp + sc + 1] * sm.bet[sc + 1] : 0.f;
-      const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+      const __nv_bfloat162 h = __floats2bfloat162_rn(x[e], x[e + 1]);
       reinterpret_cast<__nv_bfloat162 *>(tp)[e >> 1] = h;
-      *reinterpret_cast<__nv_bfloat162 *>(tpb + r * PH + sc) = h;
+      *reinterpret_cast<__nv_bfloat162 *>(tpb + r * kCP + c0 + e) = h;
     }
   }
   __syncthreads();
   // ---- W = T' (K+ ⊙ e^{b_m}) = (T' K+) e^{b_m} per channel: warp w, rows 16 w
   {
-    float acc[DK / 8][4];
-    zero(acc);
-    wmma16_bt(acc, 16 * warp, 0, kCh, tpb, PH, sm.kp, PH, lane);
-    bf16 *W = reinterpret_cast<bf16 *>(wc + O::w);
-    each(acc, 16 * warp, 0, lane,
-         [&](int r, int c, float &x) { W[r * DK + c] = __float2bfloat16_rn(x * __expf(sm.bm[c])); });
+    float wacc[DK / 8][4];
+    zero(wacc);
+    wmma16_bt(wacc, 16 * warp, 0, kCh, tpb, kCP, sm.kp, PH, lane);
+    __nv_bfloat162 *W = reinterpret_cast<__nv_bfloat162 *>(wc + O::w);
+#pragma unroll
+    for (int j = 0; j < DK / 8; ++j) {
+      const int r = 16 * warp + gq, c = 8 * j + 2 * tq;
+      const float e0 = __expf(sm.bm[c]), e1 = __expf(sm.bm[c + 1]);
+      W[(r * DK + c) >> 1] = __floats2bfloat162_rn(wacc[j][0] * e0, wacc[j][1] * e1);
+      W[((r + 8) * DK + c) >> 1] = __floats2bfloat162_rn(wacc[j][2] * e0, wacc[j][3] * e1);
+    }
   }
 }
 
