@@ -1096,7 +1096,7 @@ def bench_gdelta(args, rank, world, local_rank):
     # the arithmetic intensity (~100 FLOP/byte at d = 64) sits below the bf16 ridge: an HBM roofline
     roof = {"bound": "hbm", "achieved": round(alg / t_launch / 1e9, 1), "peak": hbm_peak, "unit": "GB/s",
             "frac": round(alg / t_launch / 1e9 / hbm_peak, 4), "traffic": recorded_traffic(wl.name),
-            "peak_source": peak_src, "algorithmic_bytes": alg, "kernel": "gdw_pre_kernel + gdw_chain_kernel (tf32 warp MMAs)"
+            "peak_source": peak_src, "algorithmic_bytes": alg, "kernel": "gdw_pre_kernel + gdw_chain_kernel (bf16 warp MMAs)"
             if wl.dtype == "bf16" else "chunk_gdelta_kernel (CUDA cores, fp32)",
             "launch_ms_mean": round(statistics.mean(launch_ms), 4)}
     e2e = None
