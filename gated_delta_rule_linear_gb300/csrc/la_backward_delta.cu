@@ -104,7 +104,8 @@ template <int DK>
 __global__ void __launch_bounds__(128) bd_pre_kernel(const __nv_bfloat16 *__restrict__ q,
                                                      const __nv_bfloat16 *__restrict__ k,
                                                      const float *__restrict__ g, const float *__restrict__ beta,
-                                                     int T, float *__restrict__ Tw, float *__restrict__ Pw) {
+                                                     int T, float *__restrict__ Tw, float *__restrict__ Pw,
+                                                     __nv_bfloat16 *__restrict__ Tb, __nv_bfloat16 *__restrict__ Pb) {
   constexpr int PH = Pitch<DK>::h;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   PreSmem<DK> &sm = *reinterpret_cast<PreSmem<DK> *>(smem_raw);
@@ -130,7 +131,9 @@ __global__ void __launch_bounds__(128) bd_pre_kernel(const __nv_bfloat16 *__rest
          [&](int kk, int nn) { return bfbits(sm.k + nn * PH + kk); }, lane);
     if (warp < 2) {
       each(acc[h], rbase + 16 * h, 0, lane, [&](int r, int s, float &v) {
-        Pw[cbase + r * kCh + s] = s <= r ? __expf(sm.s.b[r] - sm.s.b[s]) * v : 0.f;
+        const float x = s <= r ? __expf(sm.s.b[r] - sm.s.b[s]) * v : 0.f;
+        Pw[cbase + r * kCh + s] = x;
+        Pb[cbase + r * kCh + s] = __float2bfloat16_rn(x);
       });
     } else {
       each(acc[h], rbase + 16 * h, 0, lane, [&](int r, int s, float &v) {
@@ -152,212 +155,269 @@ __global__ void __launch_bounds__(128) bd_pre_kernel(const __nv_bfloat16 *__rest
       tc[r] = r < j ? 0.f : (x[0] + x[1]) + (x[2] + x[3]);
     }
 #pragma unroll
-    for (int r = 0; r < kCh; ++r) Tw[cbase + r * kCh + j] = tc[r];
+    for (int r = 0; r < kCh; ++r) {
+      Tw[cbase + r * kCh + j] = tc[r];
+      Tb[cbase + r * kCh + j] = __float2bfloat16_rn(tc[r]);
+    }
   }
 }
 
-// ============================================================ state chain
-// Double-buffered: the next chunk's k, v and T land while this chunk computes.
+// ============================================================ state chains
+// Both chains run per (b, h) and 64 value columns on eight warps (warp w: token
+// rows 16 (w % 4) of the chunk products, value columns 32 (w / 4) .. + 31), the
+// state (or its gradient) in fp32 registers with a bf16 copy of its transpose
+// as an MMA operand; bf16 m16n8k16 warp MMAs, the token-major operands through
+// ldmatrix.trans; two tile buffers, so that the next chunk's copies run during
+// the whole current one.
+constexpr int kBW = 64;        // value columns per chain CTA
+constexpr int kBP = kBW + 8;   // row pitch (bf16) of the chains' [64][64] tiles
+
+// a [64][64] bf16 image (dense rows) into a tile of pitch kBP
+__device__ __forceinline__ void img_async(__nv_bfloat16 *dst, const __nv_bfloat16 *src, int tid) {
+  for (int e = tid; e < kCh * 8; e += 256) cpa16(dst + (e >> 3) * kBP + (e & 7) * 8, src + e * 8, true);
+}
+// value columns [c0, c0 + 64) of a [T][DV] bf16 tensor from the chunk's first token (n valid rows)
+template <int DV>
+__device__ __forceinline__ void vcols_async(__nv_bfloat16 *dst, const __nv_bfloat16 *src, int c0, int n, int tid) {
+  for (int e = tid; e < kCh * 8; e += 256) {
+    const int r = e >> 3, c = (e & 7) * 8;
+    const bool ok = r < n;
+    cpa16(dst + r * kBP + c, src + (ok ? (size_t)r * DV + c0 + c : 0), ok);
+  }
+}
+// the thread's share of a state tile set (rows 16 (rh + 4 rt), columns n0 ..): fp32 to
+// the image (row-major [DK][DV]) and its bf16 transpose (value column, key channel)
+template <int DK, int DV, int RT>
+__device__ __forceinline__ void state_out(const float (&X)[RT][4][4], float *img, __nv_bfloat16 *xt, int rh,
+                                          int n0, int c0, int lane) {
+  constexpr int PH = Pitch<DK>::h;
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int rt = 0; rt < RT; ++rt) {
+    const int m0 = 16 * (rh + 4 * rt);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = n0 + 8 * j + 2 * t, r = m0 + g;
+      *reinterpret_cast<float2 *>(img + (size_t)r * DV + c0 + c) = make_float2(X[rt][j][0], X[rt][j][1]);
+      *reinterpret_cast<float2 *>(img + (size_t)(r + 8) * DV + c0 + c) = make_float2(X[rt][j][2], X[rt][j][3]);
+      xt[c * PH + r] = __float2bfloat16_rn(X[rt][j][0]);
+      xt[(c + 1) * PH + r] = __float2bfloat16_rn(X[rt][j][1]);
+      xt[c * PH + r + 8] = __float2bfloat16_rn(X[rt][j][2]);
+      xt[(c + 1) * PH + r + 8] = __float2bfloat16_rn(X[rt][j][3]);
+    }
+  }
+}
+// rows 16 rh, columns n0 .. n0 + 31 of a product, scaled per row, as bf16 into a [64][kBP] tile
+template <class F>
+__device__ __forceinline__ void tile_out(const float (&a)[4][4], __nv_bfloat16 *dst, int rh, int n0, int lane, F f) {
+  const int g = lane >> 2, t = lane & 3, r = 16 * rh + g;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int c = n0 + 8 * j + 2 * t;
+    *reinterpret_cast<__nv_bfloat162 *>(dst + r * kBP + c) =
+        __floats2bfloat162_rn(f(r, c, a[j][0]), f(r, c + 1, a[j][1]));
+    *reinterpret_cast<__nv_bfloat162 *>(dst + (r + 8) * kBP + c) =
+        __floats2bfloat162_rn(f(r + 8, c, a[j][2]), f(r + 8, c + 1, a[j][3]));
+  }
+}
+
+// ---- forward state chain: S entering each chunk to the workspace
 template <int DK>
-struct FwdBuf {
-  __nv_bfloat16 k[kCh * Pitch<DK>::h], v[kCh * kPh];
-  float t[kCh * kPf];
+struct FwdTiles {
+  __nv_bfloat16 k[kCh * Pitch<DK>::h], v[kCh * kBP], t[kCh * kBP];
 };
 template <int DK>
 struct FwdSmem {
-  FwdBuf<DK> buf[2];
-  float s[DK * kPw], z[kCh * kPw], u[kCh * kPw];
+  FwdTiles<DK> x[2];
+  __nv_bfloat16 st[kBW * Pitch<DK>::h], z[kCh * kBP], u[kCh * kBP];
   Scal sc[2];
 };
 
 template <int DK, int DV>
-__global__ void __launch_bounds__(128) bd_fwd_kernel(const __nv_bfloat16 *__restrict__ k,
+__global__ void __launch_bounds__(256) bd_fwd_kernel(const __nv_bfloat16 *__restrict__ k,
                                                      const __nv_bfloat16 *__restrict__ v,
                                                      const float *__restrict__ g, const float *__restrict__ beta,
                                                      const float *__restrict__ S0, int T,
-                                                     const float *__restrict__ Tw, float *__restrict__ Sin) {
-  constexpr int PH = Pitch<DK>::h, NCB = DV / kCW, RT = DK / 64;
+                                                     const __nv_bfloat16 *__restrict__ Tb, float *__restrict__ Sin) {
+  constexpr int PH = Pitch<DK>::h, NCB = DV / kBW, RT = DK / 64;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   FwdSmem<DK> &sm = *reinterpret_cast<FwdSmem<DK> *>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x / NCB, c0 = (blockIdx.x % NCB) * kCW;
+  const int rh = warp & 3, n0 = (warp >> 2) * 32;
+  const int bh = blockIdx.x / NCB, c0 = (blockIdx.x % NCB) * kBW;
   const int nch = (T + kCh - 1) / kCh;
-  auto issue = [&](int i, FwdBuf<DK> &b) {
+  auto issue = [&](int i, FwdTiles<DK> &x) {
     const int t0 = i * kCh, n = min(kCh, T - t0);
     const size_t row0 = (size_t)bh * T + t0;
-    rows_async<DK, PH>(b.k, k + row0 * DK, n, tid, 128);
-    cols_async<DV>(b.v, v + row0 * DV, c0, n, tid, 128);
-    cc_async(b.t, Tw + ((size_t)bh * nch + i) * kCh * kCh, tid, 128);
+    rows_async<DK, PH>(x.k, k + row0 * DK, n, tid, 256);
+    vcols_async<DV>(x.v, v + row0 * DV, c0, n, tid);
+    img_async(x.t, Tb + ((size_t)bh * nch + i) * kCh * kCh, tid);
     cp_commit();
   };
   auto gates = [&](int i) { return gate_loads(g, beta, (size_t)bh * T + i * kCh, min(kCh, T - i * kCh), lane); };
-  // S[:, c0 .. c0 + 16) in registers: warp w holds row tiles w + 4 rt
-  float S[RT][2][4];
+  float S[RT][4][4];
 #pragma unroll
   for (int rt = 0; rt < RT; ++rt) {
     zero(S[rt]);
     if (S0)
-      each(S[rt], 16 * (warp + 4 * rt), 0, lane,
+      each(S[rt], 16 * (rh + 4 * rt), n0, lane,
            [&](int r, int c, float &x) { x = __ldg(S0 + ((size_t)bh * DK + r) * DV + c0 + c); });
   }
-  issue(0, sm.buf[0]);
+  issue(0, sm.x[0]);
   if (warp == 0) gate_scan(sm.sc[0], gates(0), lane);
   for (int i = 0; i < nch; ++i) {
-    FwdBuf<DK> &b = sm.buf[i & 1];
+    const FwdTiles<DK> &x = sm.x[i & 1];
     const Scal &sc = sm.sc[i & 1];
+    const bool more = i + 1 < nch;
     Gates nxt{};
-    if (i + 1 < nch) {
-      issue(i + 1, sm.buf[(i + 1) & 1]);
+    if (more) {
+      issue(i + 1, sm.x[(i + 1) & 1]);
       if (warp == 0) nxt = gates(i + 1);
-      cp_wait<1>();
-    } else {
-      cp_wait<0>();
     }
-    float *sout = Sin + ((size_t)bh * nch + i) * DK * DV;
-#pragma unroll
-    for (int rt = 0; rt < RT; ++rt)
-      each(S[rt], 16 * (warp + 4 * rt), 0, lane, [&](int r, int c, float &x) {
-        sout[(size_t)r * DV + c0 + c] = x;
-        w16(sm.s, r, c) = x;
-      });
+    state_out<DK, DV>(S, Sin + ((size_t)bh * nch + i) * DK * DV, sm.st, rh, n0, c0, lane);
+    if (more)
+      cp_wait<1>();
+    else
+      cp_wait<0>();
     __syncthreads();
-    // Z' = Diag(beta) (V - Diag(gamma) K S): warp w, rows 16 w
+    // Z' = Diag(beta) (V - Diag(gamma) K S)
     {
-      float a[2][4];
+      float a[4][4];
       zero(a);
-      wmma(a, 16 * warp, 0, DK, [&](int m, int kk) { return bfbits(b.k + m * PH + kk); },
-           [&](int kk, int nn) { return tf(w16(sm.s, kk, nn)); }, lane);
-      each(a, 16 * warp, 0, lane, [&](int r, int c, float &x) {
-        w16(sm.z, r, c) = sc.bet[r] * (bf(b.v + r * kPh + c) - sc.gam[r] * x);
-      });
+      wmma16(a, 16 * rh, n0, DK, x.k, PH, sm.st, PH, lane);
+      tile_out(a, sm.z, rh, n0, lane,
+               [&](int r, int c, float y) { return sc.bet[r] * (bf(x.v + r * kBP + c) - sc.gam[r] * y); });
     }
     __syncthreads();
     // U' = Diag(gL / gamma) T Z'
     {
-      float a[2][4];
+      float a[4][4];
       zero(a);
-      wmma(a, 16 * warp, 0, kCh, [&](int m, int kk) { return tf(cc(b.t, m, kk)); },
-           [&](int kk, int nn) { return tf(w16(sm.z, kk, nn)); }, lane);
-      each(a, 16 * warp, 0, lane, [&](int r, int c, float &x) { w16(sm.u, r, c) = sc.glr[r] * x; });
+      wmma16_bt(a, 16 * rh, n0, kCh, x.t, kBP, sm.z, kBP, lane);
+      tile_out(a, sm.u, rh, n0, lane, [&](int r, int, float y) { return sc.glr[r] * y; });
     }
     __syncthreads();
     // S <- gL S + K^T U'
     const float gL = sc.gam[kCh - 1];
 #pragma unroll
     for (int rt = 0; rt < RT; ++rt) {
-      each(S[rt], 0, 0, lane, [&](int, int, float &x) { x *= gL; });
-      wmma(S[rt], 16 * (warp + 4 * rt), 0, kCh, [&](int m, int kk) { return bfbits(b.k + kk * PH + m); },
-           [&](int kk, int nn) { return tf(w16(sm.u, kk, nn)); }, lane);
+      each(S[rt], 0, 0, lane, [&](int, int, float &y) { y *= gL; });
+      wmma16_atbt(S[rt], 16 * (rh + 4 * rt), n0, kCh, x.k, PH, sm.u, kBP, lane);
     }
-    if (warp == 0 && i + 1 < nch) gate_scan(sm.sc[(i + 1) & 1], nxt, lane);
+    if (warp == 0 && more) gate_scan(sm.sc[(i + 1) & 1], nxt, lane);
     __syncthreads();
   }
 }
 
-// ============================================================ gradient chain
-// The next chunk's T and P are fetched once this chunk's last use of them is
-// past (the solve), its q, k, dO at the chunk's end.
+// ---- reverse chain of E = dL/dS at each chunk's end; dS0
+template <int DK>
+struct BwdTiles {
+  __nv_bfloat16 q[kCh * Pitch<DK>::h], k[kCh * Pitch<DK>::h], o[kCh * kBP], t[kCh * kBP], p[kCh * kBP];
+};
 template <int DK>
 struct BwdSmem {
-  __nv_bfloat16 q[kCh * Pitch<DK>::h], k[kCh * Pitch<DK>::h], o[kCh * kPh];
-  float t[kCh * kPf], p[kCh * kPf], e[DK * kPw], du[kCh * kPw], y[kCh * kPw];
+  BwdTiles<DK> x[2];
+  __nv_bfloat16 et[kBW * Pitch<DK>::h], og[kCh * kBP], du[kCh * kBP], y[kCh * kBP];
   Scal sc[2];
 };
 
 template <int DK, int DV>
-__global__ void __launch_bounds__(128) bd_bwd_kernel(const __nv_bfloat16 *__restrict__ q,
+__global__ void __launch_bounds__(256) bd_bwd_kernel(const __nv_bfloat16 *__restrict__ q,
                                                      const __nv_bfloat16 *__restrict__ k,
                                                      const __nv_bfloat16 *__restrict__ dO,
                                                      const float *__restrict__ g, const float *__restrict__ beta,
                                                      const float *__restrict__ dS, int T,
-                                                     const float *__restrict__ Tw, const float *__restrict__ Pw,
-                                                     float *__restrict__ Eout, float *__restrict__ dS0) {
-  constexpr int PH = Pitch<DK>::h, NCB = DV / kCW, RT = DK / 64;
+                                                     const __nv_bfloat16 *__restrict__ Tb,
+                                                     const __nv_bfloat16 *__restrict__ Pb, float *__restrict__ Eout,
+                                                     float *__restrict__ dS0) {
+  constexpr int PH = Pitch<DK>::h, NCB = DV / kBW, RT = DK / 64;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   BwdSmem<DK> &sm = *reinterpret_cast<BwdSmem<DK> *>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x / NCB, c0 = (blockIdx.x % NCB) * kCW;
+  const int rh = warp & 3, n0 = (warp >> 2) * 32;
+  const int bh = blockIdx.x / NCB, c0 = (blockIdx.x % NCB) * kBW;
   const int nch = (T + kCh - 1) / kCh;
-  auto issue_tp = [&](int i) {
-    cc_async(sm.t, Tw + ((size_t)bh * nch + i) * kCh * kCh, tid, 128);
-    cc_async(sm.p, Pw + ((size_t)bh * nch + i) * kCh * kCh, tid, 128);
-    cp_commit();
-  };
-  auto issue_qko = [&](int i) {
+  auto issue = [&](int i, BwdTiles<DK> &x) {
     const int t0 = i * kCh, n = min(kCh, T - t0);
-    const size_t row0 = (size_t)bh * T + t0;
-    rows_async<DK, PH>(sm.q, q + row0 * DK, n, tid, 128);
-    rows_async<DK, PH>(sm.k, k + row0 * DK, n, tid, 128);
-    cols_async<DV>(sm.o, dO + row0 * DV, c0, n, tid, 128);
+    const size_t row0 = (size_t)bh * T + t0, cb = ((size_t)bh * nch + i) * kCh * kCh;
+    rows_async<DK, PH>(x.q, q + row0 * DK, n, tid, 256);
+    rows_async<DK, PH>(x.k, k + row0 * DK, n, tid, 256);
+    vcols_async<DV>(x.o, dO + row0 * DV, c0, n, tid);
+    img_async(x.t, Tb + cb, tid);
+    img_async(x.p, Pb + cb, tid);
     cp_commit();
   };
   auto gates = [&](int i) { return gate_loads(g, beta, (size_t)bh * T + i * kCh, min(kCh, T - i * kCh), lane); };
-  float E[RT][2][4];
+  float E[RT][4][4];
 #pragma unroll
   for (int rt = 0; rt < RT; ++rt) {
     zero(E[rt]);
     if (dS)
-      each(E[rt], 16 * (warp + 4 * rt), 0, lane,
+      each(E[rt], 16 * (rh + 4 * rt), n0, lane,
            [&](int r, int c, float &x) { x = __ldg(dS + ((size_t)bh * DK + r) * DV + c0 + c); });
   }
-  issue_tp(nch - 1);
-  issue_qko(nch - 1);
+  issue(nch - 1, sm.x[(nch - 1) & 1]);
   if (warp == 0) gate_scan(sm.sc[(nch - 1) & 1], gates(nch - 1), lane);
   for (int i = nch - 1; i >= 0; --i) {
+    const BwdTiles<DK> &x = sm.x[i & 1];
     const Scal &sc = sm.sc[i & 1];
+    const bool more = i > 0;
     Gates nxt{};
-    if (warp == 0 && i > 0) nxt = gates(i - 1);
-    cp_wait<0>();
-    float *eout = Eout + ((size_t)bh * nch + i) * DK * DV;
-#pragma unroll
-    for (int rt = 0; rt < RT; ++rt)
-      each(E[rt], 16 * (warp + 4 * rt), 0, lane, [&](int r, int c, float &x) {
-        eout[(size_t)r * DV + c0 + c] = x;
-        w16(sm.e, r, c) = x;
-      });
+    if (more) {
+      issue(i - 1, sm.x[(i - 1) & 1]);
+      if (warp == 0) nxt = gates(i - 1);
+    }
+    state_out<DK, DV>(E, Eout + ((size_t)bh * nch + i) * DK * DV, sm.et, rh, n0, c0, lane);
+    if (more)
+      cp_wait<1>();
+    else
+      cp_wait<0>();
     __syncthreads();
+    // Diag(gamma) dO for the state update (thread: a row, eight columns)
+    {
+      const int r = tid >> 2, cq = (tid & 3) * 16;
+      const float gm = sc.gam[r];
+#pragma unroll
+      for (int e = 0; e < 16; e += 2) {
+        const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(x.o + r * kBP + cq + e);
+        *reinterpret_cast<__nv_bfloat162 *>(sm.og + r * kBP + cq + e) =
+            __floats2bfloat162_rn(gm * __low2float(h), gm * __high2float(h));
+      }
+    }
     // dU = Diag(gL / gamma) K E + P^T dO
     {
-      float a[2][4];
+      float a[4][4];
       zero(a);
-      wmma(a, 16 * warp, 0, DK, [&](int m, int kk) { return bfbits(sm.k + m * PH + kk); },
-           [&](int kk, int nn) { return tf(w16(sm.e, kk, nn)); }, lane);
-      each(a, 16 * warp, 0, lane, [&](int r, int, float &x) { x *= sc.glr[r]; });
-      wmma(a, 16 * warp, 0, kCh, [&](int m, int kk) { return tf(cc(sm.p, kk, m)); },
-           [&](int kk, int nn) { return bfbits(sm.o + kk * kPh + nn); }, lane);
-      each(a, 16 * warp, 0, lane, [&](int r, int c, float &x) { w16(sm.du, r, c) = x; });
+      wmma16(a, 16 * rh, n0, DK, x.k, PH, sm.et, PH, lane);
+      each(a, 16 * rh, n0, lane, [&](int r, int, float &y) { y *= sc.glr[r]; });
+      wmma16_atbt(a, 16 * rh, n0, kCh, x.p, kBP, x.o, kBP, lane);
+      tile_out(a, sm.du, rh, n0, lane, [&](int, int, float y) { return y; });
     }
     __syncthreads();
     // -Diag(gamma) dZ = -Diag(gamma beta) T^T dU
     {
-      float a[2][4];
+      float a[4][4];
       zero(a);
-      wmma(a, 16 * warp, 0, kCh, [&](int m, int kk) { return tf(cc(sm.t, kk, m)); },
-           [&](int kk, int nn) { return tf(w16(sm.du, kk, nn)); }, lane);
-      each(a, 16 * warp, 0, lane,
-           [&](int r, int c, float &x) { w16(sm.y, r, c) = -sc.gam[r] * sc.bet[r] * x; });
+      wmma16_atbt(a, 16 * rh, n0, kCh, x.t, kBP, sm.du, kBP, lane);
+      tile_out(a, sm.y, rh, n0, lane, [&](int r, int, float y) { return -sc.gam[r] * sc.bet[r] * y; });
     }
     __syncthreads();
-    if (i > 0) issue_tp(i - 1);  // T and P of this chunk are no longer read
     // E <- gL E + Q^T Diag(gamma) dO - K^T Diag(gamma) dZ
     const float gL = sc.gam[kCh - 1];
 #pragma unroll
     for (int rt = 0; rt < RT; ++rt) {
-      const int m0 = 16 * (warp + 4 * rt);
-      each(E[rt], 0, 0, lane, [&](int, int, float &x) { x *= gL; });
-      wmma(E[rt], m0, 0, kCh, [&](int m, int kk) { return bfbits(sm.q + kk * PH + m); },
-           [&](int kk, int nn) { return tf(sc.gam[kk] * bf(sm.o + kk * kPh + nn)); }, lane);
-      wmma(E[rt], m0, 0, kCh, [&](int m, int kk) { return bfbits(sm.k + kk * PH + m); },
-           [&](int kk, int nn) { return tf(w16(sm.y, kk, nn)); }, lane);
+      const int m0 = 16 * (rh + 4 * rt);
+      each(E[rt], 0, 0, lane, [&](int, int, float &y) { y *= gL; });
+      wmma16_atbt(E[rt], m0, n0, kCh, x.q, PH, sm.og, kBP, lane);
+      wmma16_atbt(E[rt], m0, n0, kCh, x.k, PH, sm.y, kBP, lane);
     }
-    if (warp == 0 && i > 0) gate_scan(sm.sc[(i - 1) & 1], nxt, lane);
+    if (warp == 0 && more) gate_scan(sm.sc[(i - 1) & 1], nxt, lane);
     __syncthreads();
-    if (i > 0) issue_qko(i - 1);
   }
   if (dS0) {
 #pragma unroll
     for (int rt = 0; rt < RT; ++rt)
-      each(E[rt], 16 * (warp + 4 * rt), 0, lane,
+      each(E[rt], 16 * (rh + 4 * rt), n0, lane,
            [&](int r, int c, float &x) { dS0[((size_t)bh * DK + r) * DV + c0 + c] = x; });
   }
 }
@@ -665,21 +725,22 @@ int launch_typed(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bflo
   const int nch = (T + kCh - 1) / kCh;
   const size_t ncc = (size_t)BH * nch * kCh * kCh, nss = (size_t)BH * nch * DK * DV;
   float *Tw = reinterpret_cast<float *>(ws), *Pw = Tw + ncc, *Sin = Pw + ncc, *Eout = Sin + nss;
+  __nv_bfloat16 *Tb = reinterpret_cast<__nv_bfloat16 *>(Eout + nss), *Pb = Tb + ncc;
   cudaError_t e = set_smem<PreSmem<DK>>(bd_pre_kernel<DK>);
   if (e == cudaSuccess) e = set_smem<FwdSmem<DK>>(bd_fwd_kernel<DK, DV>);
   if (e == cudaSuccess) e = set_smem<BwdSmem<DK>>(bd_bwd_kernel<DK, DV>);
   if (e == cudaSuccess) e = set_smem<GradSmem<DK>>(bd_grad_kernel<DK, DV>);
   if (e == cudaSuccess) {
-    bd_pre_kernel<DK><<<dim3(nch, BH), 128, sizeof(PreSmem<DK>), s>>>(q, k, g, beta, T, Tw, Pw);
+    bd_pre_kernel<DK><<<dim3(nch, BH), 128, sizeof(PreSmem<DK>), s>>>(q, k, g, beta, T, Tw, Pw, Tb, Pb);
     e = cudaGetLastError();
   }
-  const unsigned nchain = (unsigned)(BH * (DV / kCW));
+  const unsigned nchain = (unsigned)(BH * (DV / kBW));
   if (e == cudaSuccess) {
-    bd_fwd_kernel<DK, DV><<<nchain, 128, sizeof(FwdSmem<DK>), s>>>(k, v, g, beta, S0, T, Tw, Sin);
+    bd_fwd_kernel<DK, DV><<<nchain, 256, sizeof(FwdSmem<DK>), s>>>(k, v, g, beta, S0, T, Tb, Sin);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) {
-    bd_bwd_kernel<DK, DV><<<nchain, 128, sizeof(BwdSmem<DK>), s>>>(q, k, dO, g, beta, dS, T, Tw, Pw, Eout, dS0);
+    bd_bwd_kernel<DK, DV><<<nchain, 256, sizeof(BwdSmem<DK>), s>>>(q, k, dO, g, beta, dS, T, Tb, Pb, Eout, dS0);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) {
@@ -700,7 +761,8 @@ bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 size_t delta_bwd_workspace_bytes(int BH, int T, int dk, int dv) {
   const size_t nch = (size_t)(T + kCh - 1) / kCh;
-  return (size_t)BH * nch * (2 * kCh * kCh + 2 * (size_t)dk * dv) * sizeof(float);
+  // float32 T, P, S and E images, then bfloat16 copies of T and P for the chains
+  return (size_t)BH * nch * ((2 * kCh * kCh + 2 * (size_t)dk * dv) * sizeof(float) + 2 * kCh * kCh * 2);
 }
 
 }  // namespace la
