@@ -146,6 +146,40 @@ def algorithmic_bytes(wl, has_s0: bool) -> float:
     return float(B * H * (T * per_tok + state))
 
 
+L2_BYTES = 129e6
+FLUSH_NOTE = "inputs smaller than L2: a 256 MB buffer written between timed steps, outside the timed intervals"
+
+
+def l2_flusher(working_set_bytes: float, dev):
+    """A device buffer twice the L2 size, written between timed steps when a
+    step's working set would otherwise stay in L2 from the step before; None
+    when the working set is larger than L2."""
+    if working_set_bytes > L2_BYTES:
+        return None
+    return torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+
+def time_steps(step, stream, steps: int, flush):
+    """Device time of `steps` calls of step() on `stream` (CUDA events): the
+    whole bracket when no flush is needed, else the sum of the per-step
+    intervals with the L2 flush written between them. Returns (total_ms,
+    per-step ms)."""
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(steps):
+        if flush is not None:
+            flush.fill_(i & 0xff)
+        ev[2 * i].record(stream)
+        step()
+        ev[2 * i + 1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    per = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(steps)]
+    total = t_start.elapsed_time(t_end) if flush is None else sum(per)
+    return total, per
+
+
 def max_over_ranks(x: float, dist, device) -> float:
     """The largest of x over all ranks (the job is as slow as its slowest
     replica); x itself with a single process."""
@@ -378,26 +412,16 @@ def main():
     if rc != 0:
         raise RuntimeError(f"device status after warm-up: {la.la_last_error()}")
 
+    flush = l2_flusher(algorithmic_bytes(wl, d["S0"] is not None), dev)
     clocks = ClockSampler(local_rank)
     clocks.start()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        ev[2 * i].record(stream)
-        step()
-        ev[2 * i + 1].record(stream)
-    t_end.record(stream)
-    torch.cuda.synchronize()
+    total_ms, launch_ms = time_steps(step, stream, args.steps, flush)
     if dist:
         dist.barrier()
     clk = clocks.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    launch_ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
     total_ms = max_over_ranks(total_ms, dist, dev)
     ms_per_step = total_ms / args.steps
     tokens_per_step = B * T
@@ -446,8 +470,7 @@ def main():
             "config": {"workload": wl.name, "mode": wl.mode + ("+noncausal" if is_noncausal(wl) else ""), "B": B, "H": H, "T": T, "dk": dk,
                        "dv": dv, "C": wl.C, "global_batch": B * world, "seq_len": T,
                        "parallelism": "replicas" if world > 1 else "single",
-                       "l2": "inputs larger than L2 (no flush)" if alg_bytes > 129e6 else
-                             "inputs smaller than L2"},
+                       "l2": "inputs larger than L2 (no flush)" if flush is None else FLUSH_NOTE},
             "tflops": round(tflops, 2),
             "roofline": roof,
             "cpu_baseline": cpu,
@@ -678,25 +701,16 @@ def bench_prologue(args, rank, world, local_rank):
     for _ in range(args.warmup):
         step(d)
     torch.cuda.synchronize()
+    flush = l2_flusher(prologue_bytes(wl), dev)
     clocks = ClockSampler(local_rank)
     clocks.start()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        ev[2 * i].record(stream)
-        step(d)
-        ev[2 * i + 1].record(stream)
-    t_end.record(stream)
-    torch.cuda.synchronize()
+    total_ms, launch_ms = time_steps(lambda: step(d), stream, args.steps, flush)
     if dist:
         dist.barrier()
     clk = clocks.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    launch_ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
     total_ms = max_over_ranks(total_ms, dist, dev)
     value = replica_throughput(B * T * args.steps, world, total_ms)
     alg = prologue_bytes(wl)
@@ -753,7 +767,7 @@ def bench_prologue(args, rank, world, local_rank):
                        "gate": wl.gate_kind, "gate_width": wl.gate_width, "l2norm_qk": [wl.l2q, wl.l2k],
                        "global_batch": B * world, "seq_len": T,
                        "parallelism": "replicas" if world > 1 else "single",
-                       "l2": "inputs larger than L2 (no flush)" if alg > 129e6 else "inputs smaller than L2"},
+                       "l2": "inputs larger than L2 (no flush)" if flush is None else FLUSH_NOTE},
             "roofline": roof, "cpu_baseline": cpu, "clocks": clk, "e2e": e2e,
             "gpu_launches": args.steps,
         }), flush=True)
@@ -891,25 +905,16 @@ def bench_backward(args, rank, world, local_rank):
     torch.cuda.synchronize()
     if la.la_stream_status(sh) != 0:
         raise RuntimeError(la.la_last_error())
+    flush = l2_flusher(backward_bytes(wl), dev)
     clocks = ClockSampler(local_rank)
     clocks.start()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        ev[2 * i].record(stream)
-        step(d, outs)
-        ev[2 * i + 1].record(stream)
-    t_end.record(stream)
-    torch.cuda.synchronize()
+    total_ms, launch_ms = time_steps(lambda: step(d, outs), stream, args.steps, flush)
     if dist:
         dist.barrier()
     clk = clocks.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    launch_ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
     total_ms = max_over_ranks(total_ms, dist, dev)
     value = replica_throughput(B * T * args.steps, world, total_ms)
     flop = 3 * B * H * T * flops_per_token_head(wl.mode, dk, dv)
@@ -959,7 +964,7 @@ def bench_backward(args, rank, world, local_rank):
         cpu = {"value": round(v_cpu, 2), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
                "seconds": round(dt, 2)}
     if rank == 0:
-        cfg["l2"] = "inputs larger than L2 (no flush)" if alg > 129e6 else "inputs smaller than L2"
+        cfg["l2"] = "inputs larger than L2 (no flush)" if flush is None else FLUSH_NOTE
         print(json.dumps({
             "metric": BWD_METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
@@ -1068,25 +1073,17 @@ def bench_gdelta(args, rank, world, local_rank):
     for _ in range(args.warmup):
         step(d, outs)
     torch.cuda.synchronize()
+    flush = l2_flusher(float(B * H * (T * (2 if wl.dtype == "bf16" else 4) * (4 * dk + 2 * dv) + 4 * dk * dv * (2 if inp["S0"] is not None else 1))), dev)
     clocks = ClockSampler(local_rank)
     clocks.start()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        ev[2 * i].record(stream)
-        step(d, outs)
-        ev[2 * i + 1].record(stream)
-    t_end.record(stream)
-    torch.cuda.synchronize()
+    total_ms, launch_ms = time_steps(lambda: step(d, outs), stream, args.steps, flush)
     if dist:
         dist.barrier()
     clk = clocks.stop()
-    total_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
-    launch_ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
+    total_ms = max_over_ranks(total_ms, dist, dev)
     value = replica_throughput(B * T * args.steps, world, total_ms)
     flop = B * H * T * gdelta_flops_per_token_head(dk, dv)
     e = 2 if wl.dtype == "bf16" else 4
@@ -1134,7 +1131,7 @@ def bench_gdelta(args, rank, world, local_rank):
         cpu = {"value": round(v_cpu, 2), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
                "seconds": round(dt, 2)}
     if rank == 0:
-        cfg["l2"] = "inputs larger than L2 (no flush)" if alg > 129e6 else "inputs smaller than L2"
+        cfg["l2"] = "inputs larger than L2 (no flush)" if flush is None else FLUSH_NOTE
         print(json.dumps({
             "metric": GD_METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
@@ -1220,26 +1217,17 @@ def bench_decode(args, rank, world, local_rank):
     for _ in range(args.warmup):
         step(d, o)
     torch.cuda.synchronize()
+    flush = l2_flusher(decode_bytes(wl), dev)
     clocks = ClockSampler(local_rank)
     clocks.start()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     steps = max(args.steps, 50)  # a step is ~20 us: enough of them to time
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(steps):
-        ev[2 * i].record(stream)
-        step(d, o)
-        ev[2 * i + 1].record(stream)
-    t_end.record(stream)
-    torch.cuda.synchronize()
+    total_ms, launch_ms = time_steps(lambda: step(d, o), stream, steps, flush)
     if dist:
         dist.barrier()
     clk = clocks.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    launch_ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(steps)]
     total_ms = max_over_ranks(total_ms, dist, dev)
     value = replica_throughput(B * steps, world, total_ms)
     alg = decode_bytes(wl)
@@ -1281,8 +1269,8 @@ def bench_decode(args, rank, world, local_rank):
         cpu = {"value": round(v_cpu, 2), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
                "seconds": round(dt, 2)}
     if rank == 0:
-        cfg["l2"] = ("state larger than L2 (no flush)" if alg > 129e6 else
-                     "state smaller than L2: successive steps may hit L2")
+        cfg["l2"] = ("state larger than L2 (no flush)" if flush is None else
+                     "state smaller than L2: a 256 MB buffer written between timed steps, outside the timed intervals")
         print(json.dumps({
             "metric": DEC_METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": steps,
             "warmup": args.warmup, "ms_per_step": round(total_ms / steps, 4), "higher_is_better": True,
