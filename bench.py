@@ -59,6 +59,7 @@ KERNEL_SOURCES = {
     "decode": [_CS + "la_step.cu"],
     "gdelta": [_CS + "la_chunk_gdelta.cu", _CS + "la_chunk_gdelta_wy.cu", _CS + "la_warp_mma.cuh"],
     "backward_gdn": [_CS + "la_backward_delta.cu", _CS + "la_warp_mma.cuh", _CS + "la_wy.cuh", _CS + "la_tc_common.cuh"],
+    "backward_kda": [_CS + "la_backward_delta.cu", _CS + "la_warp_mma.cuh", _CS + "la_wy.cuh", _CS + "la_tc_common.cuh"],
     "prologue": [_CS + "la_prologue.cu", _CS + "la_sm100.cuh"],
     "prologue_gla": [_CS + "la_prologue.cu", _CS + "la_sm100.cuh"],
 }
@@ -777,7 +778,7 @@ def bench_prologue(args, rank, world, local_rank):
 
 # ---------------------------------------------------------------- backward
 
-BWD_METRIC = "tokens/sec of the chunk backward (dq, dk, dv, dS0) at 1 GB300; % of roofline"
+BWD_METRIC = "tokens/sec of the chunk backward (dq, dk, dv, dS0; dg, dbeta where the mode has them) at 1 GB300; % of roofline"
 
 
 def backward_inputs(wl):
@@ -802,6 +803,9 @@ def backward_bytes(wl) -> float:
     elif wl.mode == "gdn":  # read g and beta, write dg and dbeta; also read S0
         per_tok += 16
         return float(wl.B * wl.H * (wl.T * per_tok + 3 * 4 * wl.dk * wl.dv))
+    elif wl.mode == "kda":  # read the per-channel g and beta, write dg and dbeta; also read S0
+        per_tok += 8 * wl.dk + 8
+        return float(wl.B * wl.H * (wl.T * per_tok + 3 * 4 * wl.dk * wl.dv))
     return float(wl.B * wl.H * (wl.T * per_tok + 2 * 4 * wl.dk * wl.dv))
 
 
@@ -814,8 +818,8 @@ def time_backward_oracle(wl, inp, target_s: float = 10.0):
     while done < BH and (time.perf_counter() - t0) < target_s:
         b, h = done // wl.H, done % wl.H
         sl = lambda t: None if t is None else f64(t[b:b + 1, h:h + 1])
-        if wl.mode == "gdn":  # one full-length head per iteration (the token recurrence, reversed)
-            backward_delta(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["dO"]), "gdn", g=sl(inp["g"]),
+        if wl.mode in ("gdn", "kda"):  # one full-length head per iteration (the token recurrence, reversed)
+            backward_delta(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["dO"]), wl.mode, g=sl(inp["g"]),
                            beta=sl(inp["beta"]), S0=sl(inp["S0"]), dS=sl(inp["dS"]))
             done += 1
             continue
@@ -874,7 +878,7 @@ def bench_backward(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     inp = backward_inputs(wl)
-    delta = wl.mode == "gdn"
+    delta = wl.mode in ("gdn", "kda")
     names = [n for n in ("q", "k", "v", "g", "dO", "dS") + (("beta", "S0") if delta else ()) if inp[n] is not None]
     d = {n: inp[n].to(dev) for n in names}
     outs = {"dq": torch.empty_like(d["q"]), "dk": torch.empty_like(d["k"]), "dv": torch.empty_like(d["v"]),
@@ -883,7 +887,7 @@ def bench_backward(args, rank, world, local_rank):
         outs["dg"] = torch.empty(B, H, T, dtype=torch.float32, device=dev)
     if delta:
         outs["dbeta"] = torch.empty(B, H, T, dtype=torch.float32, device=dev)
-    elif wl.mode == "gla":
+    if wl.mode in ("gla", "kda"):
         outs["dg"] = torch.empty(B, H, T, dk, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
@@ -924,7 +928,8 @@ def bench_backward(args, rank, world, local_rank):
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
             "frac": round(achieved / hbm_peak, 4), "traffic": recorded_traffic(wl.name), "peak_source": peak_src,
             "algorithmic_bytes": alg, "kernel": "bd_pre_kernel + bd_fwd_kernel + bd_bwd_kernel + bd_grad_kernel"
-            if delta else "3 x chunk_ws_kernel (dq causal; dk and dv reversed runs)"
+            if wl.mode == "gdn" else "bk_pre_kernel + bd_fwd_kernel + bd_bwd_kernel + bk_grad_kernel (per-channel gates)"
+            if wl.mode == "kda" else "3 x chunk_ws_kernel (dq causal; dk and dv reversed runs)"
             + (" + forward for S_final + dg_tile_kernel + dg_carry_kernel" if wl.mode == "scalar" else
                " + forward for S_final + dgc_tile_kernel + dgc_carry_kernel (dq, dk: outer-product-gate passes)"
                if wl.mode == "gla" else ""),
@@ -973,7 +978,7 @@ def bench_backward(args, rank, world, local_rank):
             "tflops": round(world * flop * args.steps / (total_ms / 1e3) / 1e12, 2), "roofline": roof,
             "cpu_baseline": cpu, "clocks": clk, "e2e": e2e,
             # state prep, 3 passes, dS0 scaling (+ the forward for S_final and the two dg launches)
-            "gpu_launches": args.steps * {"scalar": 8, "gla": 8}.get(wl.mode, 5),
+            "gpu_launches": args.steps * {"scalar": 8, "gla": 8, "gdn": 4, "kda": 4}.get(wl.mode, 5),
         }), flush=True)
     if dist:
         dist.destroy_process_group()

@@ -278,22 +278,24 @@ def chunk_bwd(q, k, v, dO, mode, g=None, S0=None, dS_final=None, with_dS0=True, 
 
 
 def chunk_bwd_delta(q, k, v, dO, g=None, beta=None, S0=None, dS_final=None, with_dS0=True, with_dg=True,
-                    with_dbeta=True, C=0, stream=None):
-    """Gated DeltaNet backward (la_chunk_bwd_delta). q, k [B,H,T,dk], v, dO
-    [B,H,T,dv] bf16 CUDA tensors; g, beta [B,H,T] fp32 or None; S0, dS_final
-    [B,H,dk,dv] fp32 or None. Returns dq, dk, dv, dbeta, dg, dS0 (None where
-    not requested; dg None without g)."""
+                    with_dbeta=True, C=0, stream=None, mode="gdn"):
+    """Delta-rule backward (la_chunk_bwd_delta), mode "gdn" (Gated DeltaNet) or
+    "kda" (Kimi Delta Attention). q, k [B,H,T,dk], v, dO [B,H,T,dv] bf16 CUDA
+    tensors; beta [B,H,T] fp32 or None; g [B,H,T] (gdn, or None) or
+    [B,H,T,dk] (kda, required) fp32; S0, dS_final [B,H,dk,dv] fp32 or None.
+    Returns dq, dk, dv, dbeta, dg, dS0 (None where not requested; dg None
+    without g; dg has g's shape)."""
     import torch
     for name, t in (("q", q), ("k", k), ("v", v), ("dO", dO), ("g", g), ("beta", beta), ("S0", S0),
                     ("dS_final", dS_final)):
         _check(t, name)
     B, H, T, dk = q.shape
     dv = v.shape[-1]
-    mid = _mode_id("gdn", q.dtype)
+    mid = _mode_id(mode, q.dtype)
     dq, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     f32 = dict(dtype=torch.float32, device=q.device)
     dbeta = torch.empty((B, H, T), **f32) if with_dbeta else None
-    dg = torch.empty((B, H, T), **f32) if (with_dg and g is not None) else None
+    dg = torch.empty(tuple(g.shape), **f32) if (with_dg and g is not None) else None
     dS0 = torch.empty((B, H, dk, dv), **f32) if with_dS0 else None
     rc = la_chunk_bwd_delta(q, k, v, g, beta, dO, dS_final, S0, dq, dk_, dv_, dbeta, dg, dS0, B, H, T, dk, dv,
                             C, mid, _stream_handle(stream))

@@ -221,35 +221,53 @@ __device__ __forceinline__ void tile_out(const float (&a)[4][4], __nv_bfloat16 *
   }
 }
 
-// ---- forward state chain: S entering each chunk to the workspace
-template <int DK>
+// ---- forward state chain: S entering each chunk to the workspace. KDA = true
+// (Kimi Delta Attention): k is the pre-pass's image of K e^B (so the gates of
+// the Gated DeltaNet form are absent: g = NULL), k2 its image of K e^{B_L - B}
+// for the state update, and the decay e^{B_L} acts per key channel.
+template <int DK, bool KDA>
 struct FwdTiles {
   __nv_bfloat16 k[kCh * Pitch<DK>::h], v[kCh * kBP], t[kCh * kBP];
+  __nv_bfloat16 k2[KDA ? kCh * Pitch<DK>::h : 8];
+  float gl[KDA ? DK : 4];
 };
-template <int DK>
+template <int DK, bool KDA>
 struct FwdSmem {
-  FwdTiles<DK> x[2];
+  FwdTiles<DK, KDA> x[2];
   __nv_bfloat16 st[kBW * Pitch<DK>::h], z[kCh * kBP], u[kCh * kBP];
   Scal sc[2];
 };
 
-template <int DK, int DV>
+// the per-chunk images of the KDA pre-pass: [BH][nch][64][DK] bf16 and [BH][nch][DK] e^{B_L}
+struct KdaImages {
+  const __nv_bfloat16 *kh, *kt, *qh;
+  const float *gl;
+};
+
+template <int DK, int DV, bool KDA>
 __global__ void __launch_bounds__(256) bd_fwd_kernel(const __nv_bfloat16 *__restrict__ k,
                                                      const __nv_bfloat16 *__restrict__ v,
                                                      const float *__restrict__ g, const float *__restrict__ beta,
                                                      const float *__restrict__ S0, int T,
-                                                     const __nv_bfloat16 *__restrict__ Tb, float *__restrict__ Sin) {
+                                                     const __nv_bfloat16 *__restrict__ Tb, float *__restrict__ Sin,
+                                                     KdaImages img) {
   constexpr int PH = Pitch<DK>::h, NCB = DV / kBW, RT = DK / 64;
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  FwdSmem<DK> &sm = *reinterpret_cast<FwdSmem<DK> *>(smem_raw);
+  FwdSmem<DK, KDA> &sm = *reinterpret_cast<FwdSmem<DK, KDA> *>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rh = warp & 3, n0 = (warp >> 2) * 32;
   const int bh = blockIdx.x / NCB, c0 = (blockIdx.x % NCB) * kBW;
   const int nch = (T + kCh - 1) / kCh;
-  auto issue = [&](int i, FwdTiles<DK> &x) {
+  auto issue = [&](int i, FwdTiles<DK, KDA> &x) {
     const int t0 = i * kCh, n = min(kCh, T - t0);
-    const size_t row0 = (size_t)bh * T + t0;
-    rows_async<DK, PH>(x.k, k + row0 * DK, n, tid, 256);
+    const size_t row0 = (size_t)bh * T + t0, ci = (size_t)bh * nch + i;
+    if constexpr (KDA) {
+      rows_async<DK, PH>(x.k, img.kh + ci * kCh * DK, kCh, tid, 256);
+      rows_async<DK, PH>(x.k2, img.kt + ci * kCh * DK, kCh, tid, 256);
+      for (int e = tid; e < DK / 4; e += 256) cpa16(x.gl + 4 * e, img.gl + ci * DK + 4 * e, true);
+    } else {
+      rows_async<DK, PH>(x.k, k + row0 * DK, n, tid, 256);
+    }
     vcols_async<DV>(x.v, v + row0 * DV, c0, n, tid);
     img_async(x.t, Tb + ((size_t)bh * nch + i) * kCh * kCh, tid);
     cp_commit();
@@ -266,7 +284,7 @@ __global__ void __launch_bounds__(256) bd_fwd_kernel(const __nv_bfloat16 *__rest
   issue(0, sm.x[0]);
   if (warp == 0) gate_scan(sm.sc[0], gates(0), lane);
   for (int i = 0; i < nch; ++i) {
-    const FwdTiles<DK> &x = sm.x[i & 1];
+    const FwdTiles<DK, KDA> &x = sm.x[i & 1];
     const Scal &sc = sm.sc[i & 1];
     const bool more = i + 1 < nch;
     Gates nxt{};
@@ -297,31 +315,41 @@ __global__ void __launch_bounds__(256) bd_fwd_kernel(const __nv_bfloat16 *__rest
       tile_out(a, sm.u, rh, n0, lane, [&](int r, int, float y) { return sc.glr[r] * y; });
     }
     __syncthreads();
-    // S <- gL S + K^T U'
+    // S <- gL S + K^T U' (KDA: Diag(e^{B_L}) S + (K e^{B_L - B})^T U')
     const float gL = sc.gam[kCh - 1];
 #pragma unroll
     for (int rt = 0; rt < RT; ++rt) {
-      each(S[rt], 0, 0, lane, [&](int, int, float &y) { y *= gL; });
-      wmma16_atbt(S[rt], 16 * (rh + 4 * rt), n0, kCh, x.k, PH, sm.u, kBP, lane);
+      const int m0 = 16 * (rh + 4 * rt);
+      if constexpr (KDA) {
+        each(S[rt], m0, n0, lane, [&](int r, int, float &y) { y *= x.gl[r]; });
+        wmma16_atbt(S[rt], m0, n0, kCh, x.k2, PH, sm.u, kBP, lane);
+      } else {
+        each(S[rt], 0, 0, lane, [&](int, int, float &y) { y *= gL; });
+        wmma16_atbt(S[rt], m0, n0, kCh, x.k, PH, sm.u, kBP, lane);
+      }
     }
     if (warp == 0 && more) gate_scan(sm.sc[(i + 1) & 1], nxt, lane);
     __syncthreads();
   }
 }
 
-// ---- reverse chain of E = dL/dS at each chunk's end; dS0
-template <int DK>
+// ---- reverse chain of E = dL/dS at each chunk's end; dS0. KDA = true: q is the
+// image of Q e^B, k that of K e^{B_L - B} (read by dU), k2 that of K e^B (the
+// state-gradient update), the decay e^{B_L} per key channel, g = NULL.
+template <int DK, bool KDA>
 struct BwdTiles {
   __nv_bfloat16 q[kCh * Pitch<DK>::h], k[kCh * Pitch<DK>::h], o[kCh * kBP], t[kCh * kBP], p[kCh * kBP];
+  __nv_bfloat16 k2[KDA ? kCh * Pitch<DK>::h : 8];
+  float gl[KDA ? DK : 4];
 };
-template <int DK>
+template <int DK, bool KDA>
 struct BwdSmem {
-  BwdTiles<DK> x[2];
+  BwdTiles<DK, KDA> x[2];
   __nv_bfloat16 et[kBW * Pitch<DK>::h], og[kCh * kBP], du[kCh * kBP], y[kCh * kBP];
   Scal sc[2];
 };
 
-template <int DK, int DV>
+template <int DK, int DV, bool KDA>
 __global__ void __launch_bounds__(256) bd_bwd_kernel(const __nv_bfloat16 *__restrict__ q,
                                                      const __nv_bfloat16 *__restrict__ k,
                                                      const __nv_bfloat16 *__restrict__ dO,
@@ -329,19 +357,26 @@ __global__ void __launch_bounds__(256) bd_bwd_kernel(const __nv_bfloat16 *__rest
                                                      const float *__restrict__ dS, int T,
                                                      const __nv_bfloat16 *__restrict__ Tb,
                                                      const __nv_bfloat16 *__restrict__ Pb, float *__restrict__ Eout,
-                                                     float *__restrict__ dS0) {
+                                                     float *__restrict__ dS0, KdaImages img) {
   constexpr int PH = Pitch<DK>::h, NCB = DV / kBW, RT = DK / 64;
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  BwdSmem<DK> &sm = *reinterpret_cast<BwdSmem<DK> *>(smem_raw);
+  BwdSmem<DK, KDA> &sm = *reinterpret_cast<BwdSmem<DK, KDA> *>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rh = warp & 3, n0 = (warp >> 2) * 32;
   const int bh = blockIdx.x / NCB, c0 = (blockIdx.x % NCB) * kBW;
   const int nch = (T + kCh - 1) / kCh;
-  auto issue = [&](int i, BwdTiles<DK> &x) {
+  auto issue = [&](int i, BwdTiles<DK, KDA> &x) {
     const int t0 = i * kCh, n = min(kCh, T - t0);
-    const size_t row0 = (size_t)bh * T + t0, cb = ((size_t)bh * nch + i) * kCh * kCh;
-    rows_async<DK, PH>(x.q, q + row0 * DK, n, tid, 256);
-    rows_async<DK, PH>(x.k, k + row0 * DK, n, tid, 256);
+    const size_t row0 = (size_t)bh * T + t0, ci = (size_t)bh * nch + i, cb = ci * kCh * kCh;
+    if constexpr (KDA) {
+      rows_async<DK, PH>(x.q, img.qh + ci * kCh * DK, kCh, tid, 256);
+      rows_async<DK, PH>(x.k, img.kt + ci * kCh * DK, kCh, tid, 256);
+      rows_async<DK, PH>(x.k2, img.kh + ci * kCh * DK, kCh, tid, 256);
+      for (int e = tid; e < DK / 4; e += 256) cpa16(x.gl + 4 * e, img.gl + ci * DK + 4 * e, true);
+    } else {
+      rows_async<DK, PH>(x.q, q + row0 * DK, n, tid, 256);
+      rows_async<DK, PH>(x.k, k + row0 * DK, n, tid, 256);
+    }
     vcols_async<DV>(x.o, dO + row0 * DV, c0, n, tid);
     img_async(x.t, Tb + cb, tid);
     img_async(x.p, Pb + cb, tid);
@@ -359,7 +394,7 @@ __global__ void __launch_bounds__(256) bd_bwd_kernel(const __nv_bfloat16 *__rest
   issue(nch - 1, sm.x[(nch - 1) & 1]);
   if (warp == 0) gate_scan(sm.sc[(nch - 1) & 1], gates(nch - 1), lane);
   for (int i = nch - 1; i >= 0; --i) {
-    const BwdTiles<DK> &x = sm.x[i & 1];
+    const BwdTiles<DK, KDA> &x = sm.x[i & 1];
     const Scal &sc = sm.sc[i & 1];
     const bool more = i > 0;
     Gates nxt{};
@@ -403,13 +438,17 @@ __global__ void __launch_bounds__(256) bd_bwd_kernel(const __nv_bfloat16 *__rest
     }
     __syncthreads();
     // E <- gL E + Q^T Diag(gamma) dO - K^T Diag(gamma) dZ
+    //   (KDA: Diag(e^{B_L}) E + (Q e^B)^T dO - (K e^B)^T dZ)
     const float gL = sc.gam[kCh - 1];
 #pragma unroll
     for (int rt = 0; rt < RT; ++rt) {
       const int m0 = 16 * (rh + 4 * rt);
-      each(E[rt], 0, 0, lane, [&](int, int, float &y) { y *= gL; });
+      if constexpr (KDA)
+        each(E[rt], m0, n0, lane, [&](int r, int, float &y) { y *= x.gl[r]; });
+      else
+        each(E[rt], 0, 0, lane, [&](int, int, float &y) { y *= gL; });
       wmma16_atbt(E[rt], m0, n0, kCh, x.q, PH, sm.og, kBP, lane);
-      wmma16_atbt(E[rt], m0, n0, kCh, x.k, PH, sm.y, kBP, lane);
+      wmma16_atbt(E[rt], m0, n0, kCh, KDA ? x.k2 : x.k, PH, sm.y, kBP, lane);
     }
     if (warp == 0 && more) gate_scan(sm.sc[(i - 1) & 1], nxt, lane);
     __syncthreads();
@@ -712,6 +751,400 @@ __global__ void __launch_bounds__(256, 1) bd_grad_kernel(
   }
 }
 
+// ============================================================ Kimi Delta Attention
+// The same four passes with the per-key-channel gate. Per chunk, with B[r][c]
+// the inclusive prefix of the chunk's log-gates, b_m = B[31] (the fold's
+// midpoint), B_L = B[63], EP = e^{B - b_m} and, in the chunk's products,
+// K+ = K EP, K- = K / EP, Q+ = Q EP, K^ = K e^B, K~ = K e^{B_L - B}, Q^ = Q e^B:
+//
+//   L = strict_lower(K+ K-^T),  T = (I + Diag(beta) L)^{-1},  P = lower(Q+ K-^T)
+//   Z = V - K^ S,  U = T Diag(beta) Z,  S_next = Diag(e^{B_L}) S + K~^T U
+//   dU = K~ E + P^T dO,  Y = T^T dU,  dZ = Diag(beta) Y = dV
+//   dA = -strict_lower(Y U^T),  dL = Diag(beta) dA,  dP = lower(dO U^T)
+//   X1 = e^{b_m} (-dZ S^T) + dL K-,  X2 = e^{B_L - b_m} (U E^T) + dL^T K+ + dP^T Q+
+//   dQ = EP (e^{b_m} dO S^T + dP K-),  dK = EP X1 + X2 / EP
+//   dbeta_r = Y_r . Z_r + sum_s dA_rs L_rs
+//   dB = Q dQ + K (EP X1 - X2 / EP), plus, at the last row, the column sums of
+//        K e^{B_L - B} (U E^T) and e^{B_L} <S, E> per key channel
+//   dg = the suffix sum of dB inside the chunk (per key channel)
+//   E_prev = Diag(e^{B_L}) E + Q^T dO - K^T dZ
+//
+// (the chain rule through the exponentials: e^{B_r} enters Q^ and K^ with +,
+// K~ and the column side of L and P with -, the last row also through
+// S_next's decay). The chains are the Gated DeltaNet ones with the folded
+// images; the pre-pass and the gradient kernel form the folds in float32.
+
+// ---- pre-pass: the folds, P and T (float32 and bf16), the chains' images
+template <int DK>
+struct KPreSmem {
+  static constexpr int FP = DK + 4;  // float pitch: conflict-free tf32 fragment reads
+  union {
+    float qp[kCh * FP];  // Q+, then A
+    float a[kCh * kPf];
+  } u;
+  float kp[kCh * FP], km[kCh * FP];
+  float bet[kCh];
+};
+
+template <int DK>
+__global__ void __launch_bounds__(128) bk_pre_kernel(const __nv_bfloat16 *__restrict__ q,
+                                                     const __nv_bfloat16 *__restrict__ k,
+                                                     const float *__restrict__ g, const float *__restrict__ beta,
+                                                     int T, float *__restrict__ Tw, float *__restrict__ Pw,
+                                                     __nv_bfloat16 *__restrict__ Tb, __nv_bfloat16 *__restrict__ Pb,
+                                                     __nv_bfloat16 *__restrict__ kh, __nv_bfloat16 *__restrict__ kt,
+                                                     __nv_bfloat16 *__restrict__ qh, float *__restrict__ gl) {
+  constexpr int FP = KPreSmem<DK>::FP;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  KPreSmem<DK> &sm = *reinterpret_cast<KPreSmem<DK> *>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int i = blockIdx.x, bh = blockIdx.y, nch = gridDim.x;
+  const int t0 = i * kCh, n = min(kCh, T - t0);
+  const size_t row0 = (size_t)bh * T + t0, ci = (size_t)bh * nch + i;
+  if (tid < kCh) sm.bet[tid] = tid < n ? (beta ? __ldg(beta + row0 + tid) : 1.f) : 0.f;
+  // ---- channel c = tid: the prefix in registers, then the folds (zero rows past the end)
+  if (tid < DK) {
+    const int c = tid;
+    float bc[kCh];
+    float acc = 0.f;
+#pragma unroll
+    for (int r = 0; r < kCh; ++r) {
+      acc += r < n ? __ldg(g + (row0 + r) * DK + c) : 0.f;
+      bc[r] = acc;
+    }
+    const float bm = bc[kCh / 2 - 1], bl = bc[kCh - 1];
+    gl[ci * DK + c] = __expf(bl);
+    const size_t ib = ci * kCh * DK;
+#pragma unroll
+    for (int r = 0; r < kCh; ++r) {
+      const bool ok = r < n;
+      const float qx = ok ? __bfloat162float(q[(row0 + r) * DK + c]) : 0.f;
+      const float kx = ok ? __bfloat162float(k[(row0 + r) * DK + c]) : 0.f;
+      const float d = bc[r] - bm, ep = __expf(d), em = __expf(-d);
+      sm.u.qp[r * FP + c] = qx * ep;
+      sm.kp[r * FP + c] = kx * ep;
+      sm.km[r * FP + c] = kx * em;
+      const float eb = __expf(bc[r]);
+      kh[ib + r * DK + c] = __float2bfloat16_rn(kx * eb);
+      qh[ib + r * DK + c] = __float2bfloat16_rn(qx * eb);
+      kt[ib + r * DK + c] = __float2bfloat16_rn(kx * __expf(bl - bc[r]));
+    }
+  }
+  __syncthreads();
+  // ---- [Q+; K+] K-^T: warps 0, 1 the rows of Q+ (P, stored at once), warps 2, 3 the rows of
+  //      K+ (A = Diag(beta) L, held until Q+ is dead)
+  const float *src = warp < 2 ? sm.u.qp : sm.kp;
+  const int rbase = (warp & 1) * 32;
+  float acc[2][8][4];
+  const size_t cbase = ci * kCh * kCh;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    zero(acc[h]);
+    wmma(acc[h], rbase + 16 * h, 0, DK, [&](int m, int kk) { return tf(src[m * FP + kk]); },
+         [&](int kk, int nn) { return tf(sm.km[nn * FP + kk]); }, lane);
+    if (warp < 2)
+      each(acc[h], rbase + 16 * h, 0, lane, [&](int r, int s, float &v) {
+        const float x = s <= r ? v : 0.f;
+        Pw[cbase + r * kCh + s] = x;
+        Pb[cbase + r * kCh + s] = __float2bfloat16_rn(x);
+      });
+  }
+  __syncthreads();
+  if (warp >= 2) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      each(acc[h], rbase + 16 * h, 0, lane,
+           [&](int r, int s, float &v) { cc(sm.u.a, r, s) = s < r ? sm.bet[r] * v : 0.f; });
+  }
+  __syncthreads();
+  // ---- T = (I + A)^{-1}: column j by forward substitution (as for Gated DeltaNet)
+  if (tid < kCh) {
+    const int j = tid;
+    float tc[kCh];
+#pragma unroll
+    for (int r = 0; r < kCh; ++r) {
+      float x[4] = {r == j ? 1.f : 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int s2 = 0; s2 < r; ++s2) x[s2 & 3] = fmaf(-cc(sm.u.a, r, s2), tc[s2], x[s2 & 3]);
+      tc[r] = r < j ? 0.f : (x[0] + x[1]) + (x[2] + x[3]);
+    }
+#pragma unroll
+    for (int r = 0; r < kCh; ++r) {
+      Tw[cbase + r * kCh + j] = tc[r];
+      Tb[cbase + r * kCh + j] = __float2bfloat16_rn(tc[r]);
+    }
+  }
+}
+
+// ---- per-chunk gradients (tf32 warp MMAs, as bd_grad_kernel; the folds applied in
+//      float32 as the operands are read: EP in shared memory, per-channel factors)
+template <int DK>
+struct KGradBlk {
+  float s[DK * kPw], e[DK * kPw];
+  __nv_bfloat16 v[kCh * kPh], o[kCh * kPh];
+};
+template <int DK>
+struct KGradSmem {
+  static constexpr int FP = DK + 4;
+  __nv_bfloat16 q[kCh * Pitch<DK>::h], k[kCh * Pitch<DK>::h];
+  float ep[kCh * FP];  // e^{B - b_m}
+  float t[kCh * kPf], p[kCh * kPf];
+  union {
+    struct {
+      KGradBlk<DK> b[2];
+      float ks[kCh * kPw], ke[kCh * kPw], z[kCh * kPw], u[kCh * kPw], du[kCh * kPw], y[kCh * kPw];
+    } blk;
+    struct {  // after the blocks: dA (then dL), dP, L; then dB
+      float da[kCh * kPf], dp[kCh * kPf], l[kCh * kPf];
+      float db[kCh * FP];
+    } fin;
+  } w;
+  float bet[kCh], dbeta[kCh], ebm[DK], eblm[DK], ebl[DK], se[DK], dbl[DK];
+};
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(256, 1) bk_grad_kernel(
+    const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
+    const __nv_bfloat16 *__restrict__ dO, const float *__restrict__ g, const float *__restrict__ beta, int T,
+    const float *__restrict__ Tw, const float *__restrict__ Pw, const float *__restrict__ Sin,
+    const float *__restrict__ Eout, __nv_bfloat16 *__restrict__ dq, __nv_bfloat16 *__restrict__ dk,
+    __nv_bfloat16 *__restrict__ dv, float *__restrict__ dbeta, float *__restrict__ dg) {
+  constexpr int PH = Pitch<DK>::h, NT = DK / 16, FP = KGradSmem<DK>::FP;
+  constexpr int TPC = 256 / DK, CPT = kCW / TPC;  // <S, E>: threads per key channel, columns per thread
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  KGradSmem<DK> &sm = *reinterpret_cast<KGradSmem<DK> *>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int i = blockIdx.x, bh = blockIdx.y, nch = gridDim.x;
+  const int t0 = i * kCh, n = min(kCh, T - t0);
+  const size_t row0 = (size_t)bh * T + t0;
+  const size_t cbase = ((size_t)bh * nch + i) * kCh * kCh, sbase = ((size_t)bh * nch + i) * DK * DV;
+  auto &W = sm.w.blk;
+  auto issue_blk = [&](int c0, KGradBlk<DK> &b) {
+    state_async<DK, DV>(b.s, Sin + sbase, c0, tid, 256);
+    state_async<DK, DV>(b.e, Eout + sbase, c0, tid, 256);
+    cols_async<DV>(b.v, v + row0 * DV, c0, n, tid, 256);
+    cols_async<DV>(b.o, dO + row0 * DV, c0, n, tid, 256);
+  };
+  rows_async<DK, PH>(sm.q, q + row0 * DK, n, tid, 256);
+  rows_async<DK, PH>(sm.k, k + row0 * DK, n, tid, 256);
+  cc_async(sm.t, Tw + cbase, tid, 256);
+  cc_async(sm.p, Pw + cbase, tid, 256);
+  issue_blk(0, W.b[0]);
+  cp_commit();
+  if (tid < kCh) {
+    sm.bet[tid] = tid < n ? (beta ? __ldg(beta + row0 + tid) : 1.f) : 0.f;
+    sm.dbeta[tid] = 0.f;
+  }
+  if (tid < DK) {  // channel c = tid: EP and the per-channel factors
+    const int c = tid;
+    float bc[kCh];
+    float acc = 0.f;
+#pragma unroll
+    for (int r = 0; r < kCh; ++r) {
+      acc += r < n ? __ldg(g + (row0 + r) * DK + c) : 0.f;
+      bc[r] = acc;
+    }
+    const float bm = bc[kCh / 2 - 1], bl = bc[kCh - 1];
+#pragma unroll
+    for (int r = 0; r < kCh; ++r) sm.ep[r * FP + c] = __expf(bc[r] - bm);
+    sm.ebm[c] = __expf(bm);
+    sm.eblm[c] = __expf(bl - bm);
+    sm.ebl[c] = __expf(bl);
+    sm.dbl[c] = 0.f;
+  }
+  // folded operands read from the raw bf16 tiles
+  auto kf = [&](int r, int c) { return bf(sm.k + r * PH + c); };
+  auto qf = [&](int r, int c) { return bf(sm.q + r * PH + c); };
+  const int mr = 16 * (warp & 3), half = warp >> 2;
+  const int nq = half * (DK / 2), na = half * 32;
+  float aq[NT][4], ak1[NT][4], ak2[NT][4], aa[4][4], ap[4][4];
+  zero(aq);
+  zero(ak1);
+  zero(ak2);
+  zero(aa);
+  zero(ap);
+  float se = 0.f;  // <S, E> over channel tid / TPC, this thread's columns
+  const int nc = 8 * half;
+  for (int c0 = 0, cb = 0; c0 < DV; c0 += kCW, ++cb) {
+    KGradBlk<DK> &B = W.b[cb & 1];
+    if (c0 + kCW < DV) {
+      issue_blk(c0 + kCW, W.b[(cb + 1) & 1]);
+      cp_commit();
+      cp_wait<1>();
+    } else {
+      cp_wait<0>();
+    }
+    __syncthreads();
+    {
+      const int c = tid / TPC, j0 = (tid % TPC) * CPT;
+#pragma unroll
+      for (int j = 0; j < CPT; ++j) se += w16(B.s, c, j0 + j) * w16(B.e, c, j0 + j);
+    }
+    // ---- K^ S and K~ E: one 16 x 8 tile each per warp
+    {
+      float a[1][4], b[1][4];
+      zero(a);
+      zero(b);
+      wmma(a, mr, nc, DK, [&](int m, int kk) { return tf(kf(m, kk) * sm.ep[m * FP + kk] * sm.ebm[kk]); },
+           [&](int kk, int nn) { return tf(w16(B.s, kk, nn)); }, lane);
+      wmma(b, mr, nc, DK, [&](int m, int kk) { return tf(kf(m, kk) * sm.eblm[kk] / sm.ep[m * FP + kk]); },
+           [&](int kk, int nn) { return tf(w16(B.e, kk, nn)); }, lane);
+      each(a, mr, nc, lane, [&](int r, int col, float &x) { w16(W.ks, r, col) = x; });
+      each(b, mr, nc, lane, [&](int r, int col, float &x) { w16(W.ke, r, col) = x; });
+    }
+    __syncthreads();
+    // ---- Z = V - K^ S
+    {
+      const int r = tid >> 2, cq = (tid & 3) * 4;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) w16(W.z, r, cq + e) = bf(B.v + r * kPh + cq + e) - w16(W.ks, r, cq + e);
+    }
+    __syncthreads();
+    // ---- U = T Diag(beta) Z; dU = K~ E + P^T dO
+    {
+      float a[1][4], b[1][4];
+      zero(a);
+      wmma(a, mr, nc, kCh, [&](int m, int kk) { return tf(cc(sm.t, m, kk)); },
+           [&](int kk, int nn) { return tf(sm.bet[kk] * w16(W.z, kk, nn)); }, lane);
+      each(a, mr, nc, lane, [&](int r, int col, float &x) { w16(W.u, r, col) = x; });
+      each(b, mr, nc, lane, [&](int r, int col, float &x) { x = w16(W.ke, r, col); });
+      wmma(b, mr, nc, kCh, [&](int m, int kk) { return tf(cc(sm.p, kk, m)); },
+           [&](int kk, int nn) { return bfbits(B.o + kk * kPh + nn); }, lane);
+      each(b, mr, nc, lane, [&](int r, int col, float &x) { w16(W.du, r, col) = x; });
+    }
+    __syncthreads();
+    // ---- Y = T^T dU; dV = Diag(beta) Y; dbeta += Y . Z
+    {
+      float a[1][4];
+      zero(a);
+      wmma(a, mr, nc, kCh, [&](int m, int kk) { return tf(cc(sm.t, kk, m)); },
+           [&](int kk, int nn) { return tf(w16(W.du, kk, nn)); }, lane);
+      const int gg = lane >> 2;
+      float pb[2] = {0.f, 0.f};
+      each(a, mr, nc, lane, [&](int r, int col, float &y) {
+        const int h = (r - mr - gg) >> 3;
+        w16(W.y, r, col) = y;
+        if (r < n) dv[(row0 + r) * DV + c0 + col] = __float2bfloat16_rn(sm.bet[r] * y);
+        pb[h] += y * w16(W.z, r, col);
+      });
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        pb[h] += __shfl_xor_sync(0xffffffffu, pb[h], 1);
+        pb[h] += __shfl_xor_sync(0xffffffffu, pb[h], 2);
+        if ((lane & 3) == 0) atomicAdd(&sm.dbeta[mr + gg + 8 * h], pb[h]);
+      }
+    }
+    __syncthreads();
+    // ---- dA -= Y U^T, dP += dO U^T; dO S^T, -dZ S^T = -Diag(beta) Y S^T, U E^T (K = 16 each)
+    wmma(aa, mr, na, kCW, [&](int m, int kk) { return tf(-w16(W.y, m, kk)); },
+         [&](int kk, int nn) { return tf(w16(W.u, nn, kk)); }, lane);
+    wmma(ap, mr, na, kCW, [&](int m, int kk) { return bfbits(B.o + m * kPh + kk); },
+         [&](int kk, int nn) { return tf(w16(W.u, nn, kk)); }, lane);
+    wmma(aq, mr, nq, kCW, [&](int m, int kk) { return bfbits(B.o + m * kPh + kk); },
+         [&](int kk, int nn) { return tf(w16(B.s, nn, kk)); }, lane);
+    wmma(ak1, mr, nq, kCW, [&](int m, int kk) { return tf(-sm.bet[m] * w16(W.y, m, kk)); },
+         [&](int kk, int nn) { return tf(w16(B.s, nn, kk)); }, lane);
+    wmma(ak2, mr, nq, kCW, [&](int m, int kk) { return tf(w16(W.u, m, kk)); },
+         [&](int kk, int nn) { return tf(w16(B.e, nn, kk)); }, lane);
+    __syncthreads();
+  }
+  // ---- <S, E> per channel
+#pragma unroll
+  for (int off = 1; off < TPC; off <<= 1) se += __shfl_xor_sync(0xffffffffu, se, off);
+  if (tid % TPC == 0) sm.se[tid / TPC] = se;
+  // ---- dA, dP to shared memory; L = strict_lower(K+ K-^T)
+  auto &Fn = sm.w.fin;
+  each(aa, mr, na, lane, [&](int r, int s2, float &x) { cc(Fn.da, r, s2) = x; });
+  each(ap, mr, na, lane, [&](int r, int s2, float &x) { cc(Fn.dp, r, s2) = x; });
+  {
+    float a[4][4];
+    zero(a);
+    wmma(a, mr, na, DK, [&](int m, int kk) { return tf(kf(m, kk) * sm.ep[m * FP + kk]); },
+         [&](int kk, int nn) { return tf(kf(nn, kk) / sm.ep[nn * FP + kk]); }, lane);
+    each(a, mr, na, lane, [&](int r, int s2, float &x) { cc(Fn.l, r, s2) = s2 < r ? x : 0.f; });
+  }
+  __syncthreads();
+  // ---- dL = Diag(beta) dA (strict lower), dP masked (lower); dbeta += sum_s dA L
+  {
+    const int r = tid >> 2;
+    float betp = 0.f;
+    for (int jj = 0; jj < kCh / 4; ++jj) {
+      const int s2 = (tid & 3) + 4 * jj;
+      const float a = s2 < r ? cc(Fn.da, r, s2) : 0.f;
+      betp += a * cc(Fn.l, r, s2);
+      cc(Fn.da, r, s2) = sm.bet[r] * a;
+      cc(Fn.dp, r, s2) = s2 <= r ? cc(Fn.dp, r, s2) : 0.f;
+    }
+    betp += __shfl_xor_sync(0xffffffffu, betp, 1);
+    betp += __shfl_xor_sync(0xffffffffu, betp, 2);
+    if ((tid & 3) == 0) sm.dbeta[r] += betp;
+  }
+  __syncthreads();
+  // ---- dQ/EP = e^{b_m} dO S^T + dP K-;  X1 = -e^{b_m} dZ S^T + dL K-;
+  //      X2 = e^{B_L - b_m} U E^T (its K~-weighted column sums to dB's last row) + dL^T K+ + dP^T Q+
+  each(aq, mr, nq, lane, [&](int, int c, float &x) { x *= sm.ebm[c]; });
+  each(ak1, mr, nq, lane, [&](int, int c, float &x) { x *= sm.ebm[c]; });
+  each(ak2, mr, nq, lane, [&](int, int c, float &x) { x *= sm.eblm[c]; });
+  {
+    // column sums over this warp's 16 rows of K (e^{B_L - B} U E^T) = K X2 / EP, per channel
+    float cs[NT][2];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) cs[j][0] = cs[j][1] = 0.f;
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = mr + g + 8 * (e >> 1), c = nq + 8 * j + 2 * t + (e & 1);
+        cs[j][e & 1] += kf(r, c) * ak2[j][e] / sm.ep[r * FP + c];
+      }
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float x = cs[j][h];
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+        if (g == 0) atomicAdd(&sm.dbl[nq + 8 * j + 2 * t + h], x);
+      }
+  }
+  auto kmin = [&](int s2, int c) { return tf(kf(s2, c) / sm.ep[s2 * FP + c]); };
+  auto kplus = [&](int s2, int c) { return tf(kf(s2, c) * sm.ep[s2 * FP + c]); };
+  auto qplus = [&](int s2, int c) { return tf(qf(s2, c) * sm.ep[s2 * FP + c]); };
+  wmma(aq, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.dp, m, kk)); }, kmin, lane);
+  wmma(ak1, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.da, m, kk)); }, kmin, lane);
+  wmma(ak2, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.da, kk, m)); }, kplus, lane);
+  wmma(ak2, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.dp, kk, m)); }, qplus, lane);
+  // ---- dQ, dK; dB = Q dQ + K (EP X1 - X2 / EP) to shared memory
+  {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = mr + g + 8 * (e >> 1), c = nq + 8 * j + 2 * t + (e & 1);
+        const float epv = sm.ep[r * FP + c];
+        const float dqv = epv * aq[j][e], x1 = epv * ak1[j][e], x2 = ak2[j][e] / epv;
+        if (r < n) {
+          dq[(row0 + r) * DK + c] = __float2bfloat16_rn(dqv);
+          dk[(row0 + r) * DK + c] = __float2bfloat16_rn(x1 + x2);
+        }
+        Fn.db[r * FP + c] = qf(r, c) * dqv + kf(r, c) * (x1 - x2);
+      }
+  }
+  __syncthreads();
+  // ---- dg: the suffix sum of dB per channel, the last row with its extra terms
+  if (tid < DK) {
+    const int c = tid;
+    float run = sm.dbl[c] + sm.ebl[c] * sm.se[c];
+    for (int r = kCh - 1; r >= 0; --r) {
+      run += Fn.db[r * FP + c];
+      if (dg && r < n) dg[(row0 + r) * DK + c] = run;
+    }
+  }
+  if (dbeta && tid < n) dbeta[row0 + tid] = sm.dbeta[tid];
+}
+
 template <class Smem, class K>
 cudaError_t set_smem(K kernel) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem));
@@ -727,8 +1160,8 @@ int launch_typed(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bflo
   float *Tw = reinterpret_cast<float *>(ws), *Pw = Tw + ncc, *Sin = Pw + ncc, *Eout = Sin + nss;
   __nv_bfloat16 *Tb = reinterpret_cast<__nv_bfloat16 *>(Eout + nss), *Pb = Tb + ncc;
   cudaError_t e = set_smem<PreSmem<DK>>(bd_pre_kernel<DK>);
-  if (e == cudaSuccess) e = set_smem<FwdSmem<DK>>(bd_fwd_kernel<DK, DV>);
-  if (e == cudaSuccess) e = set_smem<BwdSmem<DK>>(bd_bwd_kernel<DK, DV>);
+  if (e == cudaSuccess) e = set_smem<FwdSmem<DK, false>>(bd_fwd_kernel<DK, DV, false>);
+  if (e == cudaSuccess) e = set_smem<BwdSmem<DK, false>>(bd_bwd_kernel<DK, DV, false>);
   if (e == cudaSuccess) e = set_smem<GradSmem<DK>>(bd_grad_kernel<DK, DV>);
   if (e == cudaSuccess) {
     bd_pre_kernel<DK><<<dim3(nch, BH), 128, sizeof(PreSmem<DK>), s>>>(q, k, g, beta, T, Tw, Pw, Tb, Pb);
@@ -736,11 +1169,13 @@ int launch_typed(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bflo
   }
   const unsigned nchain = (unsigned)(BH * (DV / kBW));
   if (e == cudaSuccess) {
-    bd_fwd_kernel<DK, DV><<<nchain, 256, sizeof(FwdSmem<DK>), s>>>(k, v, g, beta, S0, T, Tb, Sin);
+    bd_fwd_kernel<DK, DV, false><<<nchain, 256, sizeof(FwdSmem<DK, false>), s>>>(k, v, g, beta, S0, T, Tb, Sin,
+                                                                                KdaImages{});
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) {
-    bd_bwd_kernel<DK, DV><<<nchain, 256, sizeof(BwdSmem<DK>), s>>>(q, k, dO, g, beta, dS, T, Tb, Pb, Eout, dS0);
+    bd_bwd_kernel<DK, DV, false><<<nchain, 256, sizeof(BwdSmem<DK, false>), s>>>(q, k, dO, g, beta, dS, T, Tb, Pb,
+                                                                                Eout, dS0, KdaImages{});
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) {
@@ -755,9 +1190,61 @@ int launch_typed(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bflo
   return LA_OK;
 }
 
+// Kimi Delta Attention: workspace per chunk -- T and P in float32 and bf16, the
+// folded bf16 images K e^B, K e^{B_L - B}, Q e^B, e^{B_L}, and the S and E images
+template <int DK, int DV>
+int launch_kda(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const __nv_bfloat16 *dO,
+               const float *g, const float *beta, const float *S0, const float *dS, __nv_bfloat16 *dq,
+               __nv_bfloat16 *dk, __nv_bfloat16 *dv, float *dbeta, float *dg, float *dS0, int BH, int T, uint8_t *ws,
+               cudaStream_t s) {
+  using bf = __nv_bfloat16;
+  const int nch = (T + kCh - 1) / kCh;
+  const size_t ncc = (size_t)BH * nch * kCh * kCh, nss = (size_t)BH * nch * DK * DV, nim = (size_t)BH * nch * kCh * DK;
+  float *Tw = reinterpret_cast<float *>(ws), *Pw = Tw + ncc, *Sin = Pw + ncc, *Eout = Sin + nss, *gl = Eout + nss;
+  bf *Tb = reinterpret_cast<bf *>(gl + (size_t)BH * nch * DK), *Pb = Tb + ncc, *kh = Pb + ncc, *kt = kh + nim,
+     *qh = kt + nim;
+  const KdaImages img{kh, kt, qh, gl};
+  cudaError_t e = set_smem<KPreSmem<DK>>(bk_pre_kernel<DK>);
+  if (e == cudaSuccess) e = set_smem<FwdSmem<DK, true>>(bd_fwd_kernel<DK, DV, true>);
+  if (e == cudaSuccess) e = set_smem<BwdSmem<DK, true>>(bd_bwd_kernel<DK, DV, true>);
+  if (e == cudaSuccess) e = set_smem<KGradSmem<DK>>(bk_grad_kernel<DK, DV>);
+  if (e == cudaSuccess) {
+    bk_pre_kernel<DK><<<dim3(nch, BH), 128, sizeof(KPreSmem<DK>), s>>>(q, k, g, beta, T, Tw, Pw, Tb, Pb, kh, kt, qh,
+                                                                      gl);
+    e = cudaGetLastError();
+  }
+  const unsigned nchain = (unsigned)(BH * (DV / kBW));
+  if (e == cudaSuccess) {  // the chains take the gates through the images (g = NULL)
+    bd_fwd_kernel<DK, DV, true><<<nchain, 256, sizeof(FwdSmem<DK, true>), s>>>(nullptr, v, nullptr, beta, S0, T, Tb,
+                                                                               Sin, img);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) {
+    bd_bwd_kernel<DK, DV, true><<<nchain, 256, sizeof(BwdSmem<DK, true>), s>>>(nullptr, nullptr, dO, nullptr, beta, dS,
+                                                                               T, Tb, Pb, Eout, dS0, img);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) {
+    bk_grad_kernel<DK, DV><<<dim3(nch, BH), 256, sizeof(KGradSmem<DK>), s>>>(q, k, v, dO, g, beta, T, Tw, Pw, Sin,
+                                                                            Eout, dq, dk, dv, dbeta, dg);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) {
+    set_error("la_chunk_bwd_delta: kernel launch failed: %s", cudaGetErrorString(e));
+    return LA_ERR_CUDA;
+  }
+  return LA_OK;
+}
+
 bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+size_t kda_bwd_workspace_bytes(int BH, int T, int dk, int dv) {
+  const size_t nch = (size_t)(T + kCh - 1) / kCh;
+  return (size_t)BH * nch *
+         ((2 * kCh * kCh + 2 * (size_t)dk * dv + dk) * sizeof(float) + (2 * kCh * kCh + 3 * (size_t)kCh * dk) * 2);
+}
 
 size_t delta_bwd_workspace_bytes(int BH, int T, int dk, int dv) {
   const size_t nch = (size_t)(T + kCh - 1) / kCh;
@@ -793,9 +1280,14 @@ extern "C" int la_chunk_bwd_delta(const void *q, const void *k, const void *v, c
     set_error("%s: unknown mode 0x%x", fn, mode);
     return LA_ERR_INVALID_ARG;
   }
-  if (kind != LA_GDN || (mode & LA_F32)) {
-    set_error("%s: covers LA_GDN with bfloat16 inputs (got mode 0x%x)", fn, mode);
+  if ((kind != LA_GDN && kind != LA_KDA) || (mode & LA_F32)) {
+    set_error("%s: covers LA_GDN and LA_KDA with bfloat16 inputs (got mode 0x%x)", fn, mode);
     return LA_ERR_UNSUPPORTED;
+  }
+  const bool kda = kind == LA_KDA;
+  if (kda && !g) {
+    set_error("%s: LA_KDA needs the per-channel log-gates g", fn);
+    return LA_ERR_INVALID_ARG;
   }
   if (dg_out && !g) {
     set_error("%s: dg needs the log-gates g (NULL g means alpha = 1, which has no gradient)", fn);
@@ -818,7 +1310,7 @@ extern "C" int la_chunk_bwd_delta(const void *q, const void *k, const void *v, c
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int BH = B * H;
-  const size_t bytes = delta_bwd_workspace_bytes(BH, T, dk, dv);
+  const size_t bytes = kda ? kda_bwd_workspace_bytes(BH, T, dk, dv) : delta_bwd_workspace_bytes(BH, T, dk, dv);
   cudaMemPool_t pool = library_pool();
   if (!pool) {
     set_error("%s: could not create the workspace pool: %s", fn, cudaGetErrorString(cudaGetLastError()));
@@ -835,7 +1327,20 @@ extern "C" int la_chunk_bwd_delta(const void *q, const void *k, const void *v, c
        ob = static_cast<const bf *>(dO);
   auto dqb = static_cast<bf *>(dq_out), dkb = static_cast<bf *>(dk_out), dvb = static_cast<bf *>(dv_out);
   int rc;
-  if (dk == 128 && dv == 128)
+  if (kda) {
+    if (dk == 128 && dv == 128)
+      rc = launch_kda<128, 128>(qb, kb, vb, ob, g, beta, S0, dS_final, dqb, dkb, dvb, dbeta_out, dg_out, dS0, BH, T,
+                                ws, s);
+    else if (dk == 128)
+      rc = launch_kda<128, 64>(qb, kb, vb, ob, g, beta, S0, dS_final, dqb, dkb, dvb, dbeta_out, dg_out, dS0, BH, T,
+                               ws, s);
+    else if (dv == 128)
+      rc = launch_kda<64, 128>(qb, kb, vb, ob, g, beta, S0, dS_final, dqb, dkb, dvb, dbeta_out, dg_out, dS0, BH, T,
+                               ws, s);
+    else
+      rc = launch_kda<64, 64>(qb, kb, vb, ob, g, beta, S0, dS_final, dqb, dkb, dvb, dbeta_out, dg_out, dS0, BH, T,
+                              ws, s);
+  } else if (dk == 128 && dv == 128)
     rc = launch_typed<128, 128>(qb, kb, vb, ob, g, beta, S0, dS_final, dqb, dkb, dvb, dbeta_out, dg_out, dS0, BH, T,
                                 ws, s);
   else if (dk == 128)

@@ -262,7 +262,9 @@ def _bwd_delta(**kw):
     (dict(T=0), "LA_ERR_INVALID_ARG"),
     (dict(B=65536), "LA_ERR_INVALID_ARG"),
     (dict(dk=96), "LA_ERR_UNSUPPORTED"),
-    (dict(mode=la.LA_KDA), "LA_ERR_UNSUPPORTED"),         # the delta rule with per-channel gates: not built
+    (dict(mode=la.LA_KDA, g=None, dg_out=None), "LA_ERR_INVALID_ARG"),  # KDA needs its per-channel gates
+    (dict(mode=la.LA_KDA | la.LA_F32), "LA_ERR_UNSUPPORTED"),
+    (dict(mode=la.LA_KDA, C=128), "LA_ERR_UNSUPPORTED"),
     (dict(mode=la.LA_RETNET), "LA_ERR_UNSUPPORTED"),      # la_chunk_bwd covers the unit-write modes
     (dict(mode=la.LA_GDN | la.LA_F32), "LA_ERR_UNSUPPORTED"),
     (dict(mode=9), "LA_ERR_INVALID_ARG"),

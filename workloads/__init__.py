@@ -102,6 +102,10 @@ WORKLOADS = {
     # q/k/v/gate/beta recipe, dO and dS_final as for the backward workload.
     "backward_gdn": Workload("backward_gdn", "gdn", 4, 16, 16384, 128, 128, "bf16", 64, seed=15,
                              l2norm_qk=True, s0=True, extra={"backward": True}),
+    # Backward of Kimi Delta Attention (dq, dk, dv, dbeta, the per-channel dg, dS0):
+    # the kda shape and q/k/gate/beta recipe, dO and dS_final as for the backward workload.
+    "backward_kda": Workload("backward_kda", "kda", 4, 16, 16384, 128, 128, "bf16", 64, seed=16,
+                             l2norm_qk=True, s0=True, extra={"backward": True}),
     # Outer-product gate alpha_t beta_t^T (a next row): the GLA shape and q/k/v
     # recipe with GLA-distributed log-gates on both the key and the value axis.
     "outer": Workload("outer", "outer", 8, 16, 8192, 128, 128, "bf16", 64, seed=11,
