@@ -303,39 +303,47 @@ int la_chunk_bwd(const void *q, const void *k, const void *v, const float *g, co
 
 /*
  * la_chunk_bwd_delta -- the backward pass of la_chunk_fwd for LA_GDN (Gated
- * DeltaNet, bfloat16): given dO = dL/do and dS_final = dL/dS_final, the
- * gradients of L through the recurrence
+ * DeltaNet) and LA_KDA (Kimi Delta Attention), bfloat16: given dO = dL/do and
+ * dS_final = dL/dS_final, the gradients of L through the recurrence
  *
- *   R_t = alpha_t S_{t-1},  r_t = v_t - R_t^T k_t,  S_t = R_t + beta_t k_t r_t^T,
+ *   R_t = Diag(alpha_t) S_{t-1},  r_t = v_t - R_t^T k_t,  S_t = R_t + beta_t k_t r_t^T,
  *   o_t = S_t^T q_t
  *
- * ("LLM attention optimisation" page, Gated DeltaNet section; "Talk Linear
- * Attention" section 6.2), i.e. with Gh_t = dL/dS_t (later tokens and o_t):
+ * (alpha_t a scalar for LA_GDN, one value per key channel for LA_KDA; "LLM
+ * attention optimisation" page, Gated DeltaNet and Kimi Delta Attention
+ * sections; "Talk Linear Attention" section 6.2), i.e. with Gh_t = dL/dS_t
+ * (later tokens and o_t):
  *
  *   dq_t = S_t dO_t,  dv_t = beta_t Gh_t^T k_t,  dbeta_t = (Gh_t^T k_t) . r_t,
  *   dk_t = beta_t (Gh_t r_t - R_t Gh_t^T k_t),
- *   dg_t = <(I - beta_t k_t k_t^T) Gh_t, R_t>,  dS0 = dL/dS_{-1}.
+ *   dg_t = <(I - beta_t k_t k_t^T) Gh_t, R_t> (LA_KDA: the row sums, one per key
+ *          channel),  dS0 = dL/dS_{-1}.
  *
  * Chunkwise (C = 64) through the WY form of the forward: the chunk states and
  * the state gradients at the chunk boundaries are recomputed by two serial
- * passes ("Talk Linear Attention" section 4.1.2), then every chunk's
- * gradients are computed in parallel; float32 arithmetic on tf32 warp MMAs.
+ * passes ("Talk Linear Attention" section 4.1.2; bf16 warp MMAs, fp32 states),
+ * then every chunk's gradients are computed in parallel (tf32 warp MMAs,
+ * float32 arithmetic). LA_KDA folds the per-channel gate into the keys and
+ * queries around each chunk's midpoint row, as its forward does.
  *
- *   q, k, v, g, beta, S0  as passed to la_chunk_fwd for LA_GDN (g NULL: alpha
- *            = 1; beta NULL: beta = 1; S0 NULL: zero); bfloat16 q, k, v
+ *   q, k, v, g, beta, S0  as passed to la_chunk_fwd for the mode (LA_GDN: g
+ *            NULL means alpha = 1; LA_KDA: g [B][H][T][dk] required; beta NULL:
+ *            beta = 1; S0 NULL: zero); bfloat16 q, k, v
  *   dO       [B][H][T][dv] bfloat16; dS_final float32 [B][H][dk][dv] or NULL (zero)
  *   dq_out, dk_out [B][H][T][dk]; dv_out [B][H][T][dv]: bfloat16 outputs
  *   dbeta_out float32 [B][H][T] or NULL (not written; with beta NULL it is the
  *            gradient at beta = 1)
- *   dg_out   float32 [B][H][T] or NULL; needs g (LA_ERR_INVALID_ARG otherwise)
+ *   dg_out   float32, g's shape, or NULL; needs g (LA_ERR_INVALID_ARG otherwise)
  *   dS0      float32 [B][H][dk][dv] or NULL
- *   mode     LA_GDN (anything else: LA_ERR_UNSUPPORTED for a known mode or
- *            LA_F32, LA_ERR_INVALID_ARG for an unknown one); C = 0 or 64
+ *   mode     LA_GDN or LA_KDA (another known mode or LA_F32: LA_ERR_UNSUPPORTED;
+ *            an unknown one: LA_ERR_INVALID_ARG); C = 0 or 64
  *   16-byte alignment for every pointer; B*H <= 65535.
- * Workspace from the library's pool: B*H*ceil(T/64)*(2*64*64 + 2*dk*dv)*4
- * bytes (the triangular inverses and masked scores of every chunk, and the
- * states and state gradients at the chunk boundaries). Four kernels on
- * `stream`; errors as la_chunk_fwd.
+ * Workspace from the library's pool, per (b, h) and chunk of 64 tokens:
+ * LA_GDN (2*64*64 + 2*dk*dv)*4 + 2*64*64*2 bytes (the triangular inverses and
+ * masked scores in float32 and bf16, the states and state gradients at the
+ * chunk boundaries); LA_KDA (2*64*64 + 2*dk*dv + dk)*4 + (2*64*64 + 3*64*dk)*2
+ * bytes (the same plus the folded key and query images and e^{B_L}). Four
+ * kernels on `stream`; errors as la_chunk_fwd.
  */
 int la_chunk_bwd_delta(const void *q, const void *k, const void *v, const float *g, const float *beta,
                        const void *dO, const float *dS_final, const float *S0, void *dq_out, void *dk_out,
