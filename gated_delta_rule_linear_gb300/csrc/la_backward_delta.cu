@@ -812,7 +812,7 @@ __global__ void __launch_bounds__(128) bk_pre_kernel(const __nv_bfloat16 *__rest
       acc += r < n ? __ldg(g + (row0 + r) * DK + c) : 0.f;
       bc[r] = acc;
     }
-    const float bm = bc[kCh / 2 - 1], bl = bc[kCh - 1];
+    const float bm = bc[kCh / 2 - 1], bl = bc[kCh - 1], ebm = __expf(bm), eblm = __expf(bl - bm);
     gl[ci * DK + c] = __expf(bl);
     const size_t ib = ci * kCh * DK;
 #pragma unroll
@@ -824,10 +824,10 @@ __global__ void __launch_bounds__(128) bk_pre_kernel(const __nv_bfloat16 *__rest
       sm.u.qp[r * FP + c] = qx * ep;
       sm.kp[r * FP + c] = kx * ep;
       sm.km[r * FP + c] = kx * em;
-      const float eb = __expf(bc[r]);
+      const float eb = ep * ebm;  // e^B and e^{B_L - B} for the chains' bf16 images
       kh[ib + r * DK + c] = __float2bfloat16_rn(kx * eb);
       qh[ib + r * DK + c] = __float2bfloat16_rn(qx * eb);
-      kt[ib + r * DK + c] = __float2bfloat16_rn(kx * __expf(bl - bc[r]));
+      kt[ib + r * DK + c] = __float2bfloat16_rn(kx * (em * eblm));
     }
   }
   __syncthreads();
@@ -887,7 +887,7 @@ template <int DK>
 struct KGradSmem {
   static constexpr int FP = DK + 4;
   __nv_bfloat16 q[kCh * Pitch<DK>::h], k[kCh * Pitch<DK>::h];
-  float ep[kCh * FP];  // e^{B - b_m}
+  float ep[kCh * FP], em[kCh * FP];  // e^{B - b_m} and e^{b_m - B}
   float t[kCh * kPf], p[kCh * kPf];
   union {
     struct {
@@ -946,7 +946,10 @@ __global__ void __launch_bounds__(256, 1) bk_grad_kernel(
     }
     const float bm = bc[kCh / 2 - 1], bl = bc[kCh - 1];
 #pragma unroll
-    for (int r = 0; r < kCh; ++r) sm.ep[r * FP + c] = __expf(bc[r] - bm);
+    for (int r = 0; r < kCh; ++r) {
+      sm.ep[r * FP + c] = __expf(bc[r] - bm);
+      sm.em[r * FP + c] = __expf(bm - bc[r]);
+    }
     sm.ebm[c] = __expf(bm);
     sm.eblm[c] = __expf(bl - bm);
     sm.ebl[c] = __expf(bl);
@@ -985,9 +988,9 @@ __global__ void __launch_bounds__(256, 1) bk_grad_kernel(
       float a[1][4], b[1][4];
       zero(a);
       zero(b);
-      wmma(a, mr, nc, DK, [&](int m, int kk) { return tf(kf(m, kk) * sm.ep[m * FP + kk] * sm.ebm[kk]); },
+      wmma_r(a, mr, nc, DK, [&](int m, int kk) { return tf(kf(m, kk) * sm.ep[m * FP + kk] * sm.ebm[kk]); },
            [&](int kk, int nn) { return tf(w16(B.s, kk, nn)); }, lane);
-      wmma(b, mr, nc, DK, [&](int m, int kk) { return tf(kf(m, kk) * sm.eblm[kk] / sm.ep[m * FP + kk]); },
+      wmma_r(b, mr, nc, DK, [&](int m, int kk) { return tf(kf(m, kk) * sm.eblm[kk] * sm.em[m * FP + kk]); },
            [&](int kk, int nn) { return tf(w16(B.e, kk, nn)); }, lane);
       each(a, mr, nc, lane, [&](int r, int col, float &x) { w16(W.ks, r, col) = x; });
       each(b, mr, nc, lane, [&](int r, int col, float &x) { w16(W.ke, r, col) = x; });
@@ -1059,8 +1062,8 @@ __global__ void __launch_bounds__(256, 1) bk_grad_kernel(
   {
     float a[4][4];
     zero(a);
-    wmma(a, mr, na, DK, [&](int m, int kk) { return tf(kf(m, kk) * sm.ep[m * FP + kk]); },
-         [&](int kk, int nn) { return tf(kf(nn, kk) / sm.ep[nn * FP + kk]); }, lane);
+    wmma_r(a, mr, na, DK, [&](int m, int kk) { return tf(kf(m, kk) * sm.ep[m * FP + kk]); },
+           [&](int kk, int nn) { return tf(kf(nn, kk) * sm.em[nn * FP + kk]); }, lane);
     each(a, mr, na, lane, [&](int r, int s2, float &x) { cc(Fn.l, r, s2) = s2 < r ? x : 0.f; });
   }
   __syncthreads();
@@ -1096,7 +1099,7 @@ __global__ void __launch_bounds__(256, 1) bk_grad_kernel(
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int r = mr + g + 8 * (e >> 1), c = nq + 8 * j + 2 * t + (e & 1);
-        cs[j][e & 1] += kf(r, c) * ak2[j][e] / sm.ep[r * FP + c];
+        cs[j][e & 1] += kf(r, c) * ak2[j][e] * sm.em[r * FP + c];
       }
 #pragma unroll
     for (int j = 0; j < NT; ++j)
@@ -1108,13 +1111,13 @@ __global__ void __launch_bounds__(256, 1) bk_grad_kernel(
         if (g == 0) atomicAdd(&sm.dbl[nq + 8 * j + 2 * t + h], x);
       }
   }
-  auto kmin = [&](int s2, int c) { return tf(kf(s2, c) / sm.ep[s2 * FP + c]); };
+  auto kmin = [&](int s2, int c) { return tf(kf(s2, c) * sm.em[s2 * FP + c]); };
   auto kplus = [&](int s2, int c) { return tf(kf(s2, c) * sm.ep[s2 * FP + c]); };
   auto qplus = [&](int s2, int c) { return tf(qf(s2, c) * sm.ep[s2 * FP + c]); };
-  wmma(aq, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.dp, m, kk)); }, kmin, lane);
-  wmma(ak1, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.da, m, kk)); }, kmin, lane);
-  wmma(ak2, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.da, kk, m)); }, kplus, lane);
-  wmma(ak2, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.dp, kk, m)); }, qplus, lane);
+  wmma_r(aq, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.dp, m, kk)); }, kmin, lane);
+  wmma_r(ak1, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.da, m, kk)); }, kmin, lane);
+  wmma_r(ak2, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.da, kk, m)); }, kplus, lane);
+  wmma_r(ak2, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.dp, kk, m)); }, qplus, lane);
   // ---- dQ, dK; dB = Q dQ + K (EP X1 - X2 / EP) to shared memory
   {
     const int g = lane >> 2, t = lane & 3;
@@ -1124,7 +1127,7 @@ __global__ void __launch_bounds__(256, 1) bk_grad_kernel(
       for (int e = 0; e < 4; ++e) {
         const int r = mr + g + 8 * (e >> 1), c = nq + 8 * j + 2 * t + (e & 1);
         const float epv = sm.ep[r * FP + c];
-        const float dqv = epv * aq[j][e], x1 = epv * ak1[j][e], x2 = ak2[j][e] / epv;
+        const float dqv = epv * aq[j][e], x1 = epv * ak1[j][e], x2 = ak2[j][e] * sm.em[r * FP + c];
         if (r < n) {
           dq[(row0 + r) * DK + c] = __float2bfloat16_rn(dqv);
           dk[(row0 + r) * DK + c] = __float2bfloat16_rn(x1 + x2);
