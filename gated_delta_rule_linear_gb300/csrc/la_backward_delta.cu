@@ -988,9 +988,9 @@ __global__ void __launch_bounds__(256, 1) bk_grad_kernel(
       float a[1][4], b[1][4];
       zero(a);
       zero(b);
-      wmma_r(a, mr, nc, DK, [&](int m, int kk) { return tf(kf(m, kk) * sm.ep[m * FP + kk] * sm.ebm[kk]); },
+      wmma(a, mr, nc, DK, [&](int m, int kk) { return tf(kf(m, kk) * sm.ep[m * FP + kk] * sm.ebm[kk]); },
            [&](int kk, int nn) { return tf(w16(B.s, kk, nn)); }, lane);
-      wmma_r(b, mr, nc, DK, [&](int m, int kk) { return tf(kf(m, kk) * sm.eblm[kk] * sm.em[m * FP + kk]); },
+      wmma(b, mr, nc, DK, [&](int m, int kk) { return tf(kf(m, kk) * sm.eblm[kk] * sm.em[m * FP + kk]); },
            [&](int kk, int nn) { return tf(w16(B.e, kk, nn)); }, lane);
       each(a, mr, nc, lane, [&](int r, int col, float &x) { w16(W.ks, r, col) = x; });
       each(b, mr, nc, lane, [&](int r, int col, float &x) { w16(W.ke, r, col) = x; });
@@ -1062,7 +1062,7 @@ __global__ void __launch_bounds__(256, 1) bk_grad_kernel(
   {
     float a[4][4];
     zero(a);
-    wmma_r(a, mr, na, DK, [&](int m, int kk) { return tf(kf(m, kk) * sm.ep[m * FP + kk]); },
+    wmma(a, mr, na, DK, [&](int m, int kk) { return tf(kf(m, kk) * sm.ep[m * FP + kk]); },
            [&](int kk, int nn) { return tf(kf(nn, kk) * sm.em[nn * FP + kk]); }, lane);
     each(a, mr, na, lane, [&](int r, int s2, float &x) { cc(Fn.l, r, s2) = s2 < r ? x : 0.f; });
   }
@@ -1114,10 +1114,10 @@ __global__ void __launch_bounds__(256, 1) bk_grad_kernel(
   auto kmin = [&](int s2, int c) { return tf(kf(s2, c) * sm.em[s2 * FP + c]); };
   auto kplus = [&](int s2, int c) { return tf(kf(s2, c) * sm.ep[s2 * FP + c]); };
   auto qplus = [&](int s2, int c) { return tf(qf(s2, c) * sm.ep[s2 * FP + c]); };
-  wmma_r(aq, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.dp, m, kk)); }, kmin, lane);
-  wmma_r(ak1, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.da, m, kk)); }, kmin, lane);
-  wmma_r(ak2, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.da, kk, m)); }, kplus, lane);
-  wmma_r(ak2, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.dp, kk, m)); }, qplus, lane);
+  wmma(aq, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.dp, m, kk)); }, kmin, lane);
+  wmma(ak1, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.da, m, kk)); }, kmin, lane);
+  wmma(ak2, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.da, kk, m)); }, kplus, lane);
+  wmma(ak2, mr, nq, kCh, [&](int m, int kk) { return tf(cc(Fn.dp, kk, m)); }, qplus, lane);
   // ---- dQ, dK; dB = Q dQ + K (EP X1 - X2 / EP) to shared memory
   {
     const int g = lane >> 2, t = lane & 3;
