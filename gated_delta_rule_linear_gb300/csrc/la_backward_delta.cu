@@ -462,12 +462,36 @@ __global__ void __launch_bounds__(256) bd_bwd_kernel(const __nv_bfloat16 *__rest
 }
 
 // ============================================================ gradients
-// One CTA per chunk; the value axis in blocks of 16 columns, double-buffered:
-// the next block's S, E (float32) and v, dO columns land while this one computes.
+// One CTA per chunk; the value axis in blocks of kGW = 32 columns (warp w: token
+// rows 16 (w % 4), block columns 16 (w / 4) .. + 15 of the block products),
+// double-buffered: the next block's S, E (float32) and v, dO columns land while
+// this one computes.
+constexpr int kGW = 32;       // value columns per gradient block
+constexpr int kGP = kGW + 8;  // row pitch (bf16) of the block's v and dO tiles: 80-byte rows
+// element (r, c) of a float32 x 32 tile (16-byte groups XOR-permuted by row)
+__device__ __forceinline__ float &w32(float *p, int r, int c) { return fw<kGW>(p, r, c); }
+// the D x 32 columns [c0, c0 + 32) of a [D][DV] float32 matrix into a w32 tile
+template <int D, int DV>
+__device__ __forceinline__ void state32_async(float *dst, const float *src, int c0, int tid) {
+  for (int i = tid; i < D * 8; i += 256) {
+    const int r = i >> 3, c = (i & 7) * 4;
+    cpa16(dst + r * kGW + (c ^ swz64(r)), src + (size_t)r * DV + c0 + c, true);
+  }
+}
+// the 64 x 32 columns [c0, c0 + 32) of a [T][DV] bf16 tensor (n valid rows), pitch kGP
+template <int DV>
+__device__ __forceinline__ void cols32_async(__nv_bfloat16 *dst, const __nv_bfloat16 *src, int c0, int n, int tid) {
+  for (int i = tid; i < kCh * 4; i += 256) {
+    const int r = i >> 2, c = (i & 3) * 8;
+    const bool ok = r < n;
+    cpa16(dst + r * kGP + c, src + (ok ? (size_t)r * DV + c0 + c : 0), ok);
+  }
+}
+
 template <int DK>
 struct GradBlk {
-  float s[DK * kPw], e[DK * kPw];
-  __nv_bfloat16 v[kCh * kPh], o[kCh * kPh];
+  float s[DK * kGW], e[DK * kGW];
+  __nv_bfloat16 v[kCh * kGP], o[kCh * kGP];
 };
 template <int DK>
 struct GradSmem {
@@ -476,8 +500,8 @@ struct GradSmem {
   union {
     struct {
       GradBlk<DK> b[2];
-      float ks[kCh * kPw], qs[kCh * kPw], ke[kCh * kPw], z[kCh * kPw], u[kCh * kPw], du[kCh * kPw],
-          y[kCh * kPw];
+      float ks[kCh * kGW], qs[kCh * kGW], ke[kCh * kGW], z[kCh * kGW], u[kCh * kGW], du[kCh * kGW],
+          y[kCh * kGW];
     } blk;
     struct {  // after the blocks: dA (then F), dP (then H), L
       float da[kCh * kPf], dp[kCh * kPf], l[kCh * kPf];
@@ -487,25 +511,22 @@ struct GradSmem {
   float db[kCh], dbeta[kCh], kd[kCh], red[8];
 };
 
-// acc_a += A B1, acc_b += A B2 with one A fragment per k step
-template <class GA, class GB1, class GB2>
-__device__ __forceinline__ void wmma2(float (&acc_a)[1][4], float (&acc_b)[1][4], int m0, int n0, int K, GA ga,
+// acc_a += A B1, acc_b += A B2 with one A fragment per k step (NT 16 x 8 tiles each)
+template <int NT, class GA, class GB1, class GB2>
+__device__ __forceinline__ void wmma2(float (&acc_a)[NT][4], float (&acc_b)[NT][4], int m0, int n0, int K, GA ga,
                                       GB1 gb1, GB2 gb2, int lane) {
   const int g = lane >> 2, t = lane & 3;
-  float alt_a[4] = {0.f, 0.f, 0.f, 0.f}, alt_b[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int k0 = 0; k0 < K; k0 += 8) {
     uint32_t a[4] = {ga(m0 + g, k0 + t), ga(m0 + g + 8, k0 + t), ga(m0 + g, k0 + t + 4),
                      ga(m0 + g + 8, k0 + t + 4)};
-    uint32_t b1[2] = {gb1(k0 + t, n0 + g), gb1(k0 + t + 4, n0 + g)};
-    uint32_t b2[2] = {gb2(k0 + t, n0 + g), gb2(k0 + t + 4, n0 + g)};
-    mma_16x8x8_tf32((k0 & 8) ? alt_a : acc_a[0], a, b1);
-    mma_16x8x8_tf32((k0 & 8) ? alt_b : acc_b[0], a, b2);
-  }
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    acc_a[0][e] += alt_a[e];
-    acc_b[0][e] += alt_b[e];
+    for (int j = 0; j < NT; ++j) {
+      uint32_t b1[2] = {gb1(k0 + t, n0 + 8 * j + g), gb1(k0 + t + 4, n0 + 8 * j + g)};
+      uint32_t b2[2] = {gb2(k0 + t, n0 + 8 * j + g), gb2(k0 + t + 4, n0 + 8 * j + g)};
+      mma_16x8x8_tf32(acc_a[j], a, b1);
+      mma_16x8x8_tf32(acc_b[j], a, b2);
+    }
   }
 }
 
@@ -526,10 +547,10 @@ __global__ void __launch_bounds__(256, 1) bd_grad_kernel(
   const size_t cbase = ((size_t)bh * nch + i) * kCh * kCh, sbase = ((size_t)bh * nch + i) * DK * DV;
   auto& W = sm.w.blk;
   auto issue_blk = [&](int c0, GradBlk<DK> &b) {
-    state_async<DK, DV>(b.s, Sin + sbase, c0, tid, 256);
-    state_async<DK, DV>(b.e, Eout + sbase, c0, tid, 256);
-    cols_async<DV>(b.v, v + row0 * DV, c0, n, tid, 256);
-    cols_async<DV>(b.o, dO + row0 * DV, c0, n, tid, 256);
+    state32_async<DK, DV>(b.s, Sin + sbase, c0, tid);
+    state32_async<DK, DV>(b.e, Eout + sbase, c0, tid);
+    cols32_async<DV>(b.v, v + row0 * DV, c0, n, tid);
+    cols32_async<DV>(b.o, dO + row0 * DV, c0, n, tid);
   };
   rows_async<DK, PH>(sm.q, q + row0 * DK, n, tid, 256);
   rows_async<DK, PH>(sm.k, k + row0 * DK, n, tid, 256);
@@ -552,43 +573,43 @@ __global__ void __launch_bounds__(256, 1) bd_grad_kernel(
   zero(aa);
   zero(ap);
   float se = 0.f;  // <S, E> over this thread's share
-  const int nc = 8 * half;  // x 16 tiles: warp w owns rows 16 (w & 3), columns 8 (w >> 2) .. + 8
-  for (int c0 = 0, cb = 0; c0 < DV; c0 += kCW, ++cb) {
+  const int nc = 16 * half;  // block products: warp w owns rows 16 (w & 3), columns 16 (w >> 2) .. + 16
+  for (int c0 = 0, cb = 0; c0 < DV; c0 += kGW, ++cb) {
     GradBlk<DK> &B = W.b[cb & 1];
-    if (c0 + kCW < DV) {
-      issue_blk(c0 + kCW, W.b[(cb + 1) & 1]);
+    if (c0 + kGW < DV) {
+      issue_blk(c0 + kGW, W.b[(cb + 1) & 1]);
       cp_commit();
       cp_wait<1>();
     } else {
       cp_wait<0>();
     }
     __syncthreads();
-    for (int x = tid; x < DK * kCW; x += 256) se += w16(B.s, (x >> 4), (x & 15)) * w16(B.e, (x >> 4), (x & 15));
-    // ---- K S and Diag(gL / gamma) K E (one A fragment), Q S: one 16 x 8 tile each per warp
+    for (int x = tid; x < DK * kGW; x += 256) se += w32(B.s, x >> 5, x & 31) * w32(B.e, x >> 5, x & 31);
+    // ---- K S and Diag(gL / gamma) K E (one A fragment), Q S: two 16 x 8 tiles each per warp
     {
-      float a[1][4], b[1][4], c[1][4];
+      float a[2][4], b[2][4], c[2][4];
       zero(a);
       zero(b);
       zero(c);
       wmma2(a, c, mr, nc, DK, [&](int m, int kk) { return bfbits(sm.k + m * PH + kk); },
-            [&](int kk, int nn) { return tf(w16(B.s, kk, nn)); },
-            [&](int kk, int nn) { return tf(w16(B.e, kk, nn)); }, lane);
+            [&](int kk, int nn) { return tf(w32(B.s, kk, nn)); },
+            [&](int kk, int nn) { return tf(w32(B.e, kk, nn)); }, lane);
       wmma(b, mr, nc, DK, [&](int m, int kk) { return bfbits(sm.q + m * PH + kk); },
-           [&](int kk, int nn) { return tf(w16(B.s, kk, nn)); }, lane);
-      each(a, mr, nc, lane, [&](int r, int col, float &x) { w16(W.ks, r, col) = x; });
-      each(b, mr, nc, lane, [&](int r, int col, float &x) { w16(W.qs, r, col) = x; });
-      each(c, mr, nc, lane, [&](int r, int col, float &x) { w16(W.ke, r, col) = sm.sc.glr[r] * x; });
+           [&](int kk, int nn) { return tf(w32(B.s, kk, nn)); }, lane);
+      each(a, mr, nc, lane, [&](int r, int col, float &x) { w32(W.ks, r, col) = x; });
+      each(b, mr, nc, lane, [&](int r, int col, float &x) { w32(W.qs, r, col) = x; });
+      each(c, mr, nc, lane, [&](int r, int col, float &x) { w32(W.ke, r, col) = sm.sc.glr[r] * x; });
     }
     __syncthreads();
-    // ---- Z = V - Diag(gamma) K S; db += gamma dO . (Q S)
+    // ---- Z = V - Diag(gamma) K S; db += gamma dO . (Q S)  (thread: a row, eight columns)
     {
-      const int r = tid >> 2, cq = (tid & 3) * 4;
+      const int r = tid >> 2, cq = (tid & 3) * 8;
       float part = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
+      for (int e = 0; e < 8; ++e) {
         const int c = cq + e;
-        w16(W.z, r, c) = bf(B.v + r * kPh + c) - sm.sc.gam[r] * w16(W.ks, r, c);
-        part += bf(B.o + r * kPh + c) * w16(W.qs, r, c);
+        w32(W.z, r, c) = bf(B.v + r * kGP + c) - sm.sc.gam[r] * w32(W.ks, r, c);
+        part += bf(B.o + r * kGP + c) * w32(W.qs, r, c);
       }
       part += __shfl_xor_sync(0xffffffffu, part, 1);
       part += __shfl_xor_sync(0xffffffffu, part, 2);
@@ -597,33 +618,33 @@ __global__ void __launch_bounds__(256, 1) bd_grad_kernel(
     __syncthreads();
     // ---- U = T Diag(beta) Z; dU = Diag(gL / gamma) K E + P^T dO
     {
-      float a[1][4], b[1][4];
+      float a[2][4], b[2][4];
       zero(a);
       wmma(a, mr, nc, kCh, [&](int m, int kk) { return tf(cc(sm.t, m, kk)); },
-           [&](int kk, int nn) { return tf(sm.sc.bet[kk] * w16(W.z, kk, nn)); }, lane);
-      each(a, mr, nc, lane, [&](int r, int col, float &x) { w16(W.u, r, col) = x; });
-      each(b, mr, nc, lane, [&](int r, int col, float &x) { x = w16(W.ke, r, col); });
+           [&](int kk, int nn) { return tf(sm.sc.bet[kk] * w32(W.z, kk, nn)); }, lane);
+      each(a, mr, nc, lane, [&](int r, int col, float &x) { w32(W.u, r, col) = x; });
+      each(b, mr, nc, lane, [&](int r, int col, float &x) { x = w32(W.ke, r, col); });
       wmma(b, mr, nc, kCh, [&](int m, int kk) { return tf(cc(sm.p, kk, m)); },
-           [&](int kk, int nn) { return bfbits(B.o + kk * kPh + nn); }, lane);
-      each(b, mr, nc, lane, [&](int r, int col, float &x) { w16(W.du, r, col) = x; });
+           [&](int kk, int nn) { return bfbits(B.o + kk * kGP + nn); }, lane);
+      each(b, mr, nc, lane, [&](int r, int col, float &x) { w32(W.du, r, col) = x; });
     }
     __syncthreads();
     // ---- Y = T^T dU; dV = Diag(beta) Y; dbeta += Y . Z; db -= gamma dZ . (K S); kd += U . (Kt E)
     {
-      float a[1][4];
+      float a[2][4];
       zero(a);
       wmma(a, mr, nc, kCh, [&](int m, int kk) { return tf(cc(sm.t, kk, m)); },
-           [&](int kk, int nn) { return tf(w16(W.du, kk, nn)); }, lane);
+           [&](int kk, int nn) { return tf(w32(W.du, kk, nn)); }, lane);
       const int gg = lane >> 2;
       float pb[2] = {0.f, 0.f}, pd[2] = {0.f, 0.f}, pk[2] = {0.f, 0.f};
       each(a, mr, nc, lane, [&](int r, int col, float &y) {
         const int h = (r - mr - gg) >> 3;  // 0: row g, 1: row g + 8
-        w16(W.y, r, col) = y;
+        w32(W.y, r, col) = y;
         const float dz = sm.sc.bet[r] * y;
         if (r < n) dv[(row0 + r) * DV + c0 + col] = __float2bfloat16_rn(dz);
-        pb[h] += y * w16(W.z, r, col);
-        pd[h] += dz * w16(W.ks, r, col);
-        pk[h] += w16(W.u, r, col) * w16(W.ke, r, col);
+        pb[h] += y * w32(W.z, r, col);
+        pd[h] += dz * w32(W.ks, r, col);
+        pk[h] += w32(W.u, r, col) * w32(W.ke, r, col);
       });
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -643,17 +664,17 @@ __global__ void __launch_bounds__(256, 1) bd_grad_kernel(
     }
     __syncthreads();
     // ---- dA -= Y U^T, dP += dO U^T, dQ += Diag(gamma) dO S^T,
-    //      dK += -Diag(gamma beta) Y S^T + Diag(gL / gamma) U E^T (K = 16 each)
-    wmma(aa, mr, na, kCW, [&](int m, int kk) { return tf(-w16(W.y, m, kk)); },
-         [&](int kk, int nn) { return tf(w16(W.u, nn, kk)); }, lane);
-    wmma(ap, mr, na, kCW, [&](int m, int kk) { return bfbits(B.o + m * kPh + kk); },
-         [&](int kk, int nn) { return tf(w16(W.u, nn, kk)); }, lane);
-    wmma(aq, mr, nq, kCW, [&](int m, int kk) { return tf(sm.sc.gam[m] * bf(B.o + m * kPh + kk)); },
-         [&](int kk, int nn) { return tf(w16(B.s, nn, kk)); }, lane);
-    wmma(ak, mr, nq, kCW, [&](int m, int kk) { return tf(-sm.sc.gam[m] * sm.sc.bet[m] * w16(W.y, m, kk)); },
-         [&](int kk, int nn) { return tf(w16(B.s, nn, kk)); }, lane);
-    wmma(ak, mr, nq, kCW, [&](int m, int kk) { return tf(sm.sc.glr[m] * w16(W.u, m, kk)); },
-         [&](int kk, int nn) { return tf(w16(B.e, nn, kk)); }, lane);
+    //      dK += -Diag(gamma beta) Y S^T + Diag(gL / gamma) U E^T (K = 32 each)
+    wmma(aa, mr, na, kGW, [&](int m, int kk) { return tf(-w32(W.y, m, kk)); },
+         [&](int kk, int nn) { return tf(w32(W.u, nn, kk)); }, lane);
+    wmma(ap, mr, na, kGW, [&](int m, int kk) { return bfbits(B.o + m * kGP + kk); },
+         [&](int kk, int nn) { return tf(w32(W.u, nn, kk)); }, lane);
+    wmma(aq, mr, nq, kGW, [&](int m, int kk) { return tf(sm.sc.gam[m] * bf(B.o + m * kGP + kk)); },
+         [&](int kk, int nn) { return tf(w32(B.s, nn, kk)); }, lane);
+    wmma(ak, mr, nq, kGW, [&](int m, int kk) { return tf(-sm.sc.gam[m] * sm.sc.bet[m] * w32(W.y, m, kk)); },
+         [&](int kk, int nn) { return tf(w32(B.s, nn, kk)); }, lane);
+    wmma(ak, mr, nq, kGW, [&](int m, int kk) { return tf(sm.sc.glr[m] * w32(W.u, m, kk)); },
+         [&](int kk, int nn) { return tf(w32(B.e, nn, kk)); }, lane);
     __syncthreads();
   }
   // ---- <S, E> over the block
