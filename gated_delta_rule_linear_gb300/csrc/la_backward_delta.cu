@@ -795,88 +795,98 @@ __global__ void __launch_bounds__(256, 1) bd_grad_kernel(
 // S_next's decay). The chains are the Gated DeltaNet ones with the folded
 // images; the pre-pass and the gradient kernel form the folds in float32.
 
-// ---- pre-pass: the folds, P and T (float32 and bf16), the chains' images
+// ---- pre-pass: the folds, P and T (float32 and bf16), the chains' images.
+// 256 threads: RG groups of threads per key channel, each folding RPG rows (the
+// prefix from the groups' gate sums), so that more loads are in flight per SM.
 template <int DK>
 struct KPreSmem {
   static constexpr int FP = DK + 4;  // float pitch: conflict-free tf32 fragment reads
+  static constexpr int RG = 256 / DK, RPG = kCh / RG;
   union {
     float qp[kCh * FP];  // Q+, then A
     float a[kCh * kPf];
   } u;
   float kp[kCh * FP], km[kCh * FP];
-  float bet[kCh];
+  float bet[kCh], gsum[RG * DK];
 };
 
 template <int DK>
-__global__ void __launch_bounds__(128) bk_pre_kernel(const __nv_bfloat16 *__restrict__ q,
-                                                     const __nv_bfloat16 *__restrict__ k,
-                                                     const float *__restrict__ g, const float *__restrict__ beta,
-                                                     int T, float *__restrict__ Tw, float *__restrict__ Pw,
-                                                     __nv_bfloat16 *__restrict__ Tb, __nv_bfloat16 *__restrict__ Pb,
-                                                     __nv_bfloat16 *__restrict__ kh, __nv_bfloat16 *__restrict__ kt,
-                                                     __nv_bfloat16 *__restrict__ qh, float *__restrict__ gl) {
-  constexpr int FP = KPreSmem<DK>::FP;
+__global__ void __launch_bounds__(256, 2) bk_pre_kernel(const __nv_bfloat16 *__restrict__ q,
+                                                        const __nv_bfloat16 *__restrict__ k,
+                                                        const float *__restrict__ g, const float *__restrict__ beta,
+                                                        int T, float *__restrict__ Tw, float *__restrict__ Pw,
+                                                        __nv_bfloat16 *__restrict__ Tb, __nv_bfloat16 *__restrict__ Pb,
+                                                        __nv_bfloat16 *__restrict__ kh, __nv_bfloat16 *__restrict__ kt,
+                                                        __nv_bfloat16 *__restrict__ qh, float *__restrict__ gl) {
+  using Sm = KPreSmem<DK>;
+  constexpr int FP = Sm::FP, RG = Sm::RG, RPG = Sm::RPG;
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  KPreSmem<DK> &sm = *reinterpret_cast<KPreSmem<DK> *>(smem_raw);
+  Sm &sm = *reinterpret_cast<Sm *>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int i = blockIdx.x, bh = blockIdx.y, nch = gridDim.x;
   const int t0 = i * kCh, n = min(kCh, T - t0);
   const size_t row0 = (size_t)bh * T + t0, ci = (size_t)bh * nch + i;
   if (tid < kCh) sm.bet[tid] = tid < n ? (beta ? __ldg(beta + row0 + tid) : 1.f) : 0.f;
-  // ---- channel c = tid: the prefix in registers, then the folds (zero rows past the end)
-  if (tid < DK) {
-    const int c = tid;
-    float bc[kCh];
+  // ---- channel c, rows r0 .. r0 + RPG - 1: the local prefix in registers (zero gates past the end)
+  const int c = tid % DK, grp = tid / DK, r0 = grp * RPG;
+  float bc[RPG];
+  {
     float acc = 0.f;
 #pragma unroll
-    for (int r = 0; r < kCh; ++r) {
-      acc += r < n ? __ldg(g + (row0 + r) * DK + c) : 0.f;
+    for (int r = 0; r < RPG; ++r) {
+      acc += r0 + r < n ? __ldg(g + (row0 + r0 + r) * DK + c) : 0.f;
       bc[r] = acc;
     }
-    const float bm = bc[kCh / 2 - 1], bl = bc[kCh - 1], ebm = __expf(bm), eblm = __expf(bl - bm);
-    gl[ci * DK + c] = __expf(bl);
+    sm.gsum[grp * DK + c] = acc;
+  }
+  __syncthreads();
+  {
+    float off = 0.f, bm = 0.f, bl = 0.f;
+#pragma unroll
+    for (int j = 0; j < RG; ++j) {
+      const float x = sm.gsum[j * DK + c];
+      off += j < grp ? x : 0.f;
+      bm += j * RPG < kCh / 2 ? x : 0.f;  // B at row 31: the groups of rows 0 .. 31
+      bl += x;
+    }
+    const float ebm = __expf(bm), eblm = __expf(bl - bm);
+    if (grp == 0) gl[ci * DK + c] = __expf(bl);
     const size_t ib = ci * kCh * DK;
 #pragma unroll
-    for (int r = 0; r < kCh; ++r) {
-      const bool ok = r < n;
-      const float qx = ok ? __bfloat162float(q[(row0 + r) * DK + c]) : 0.f;
-      const float kx = ok ? __bfloat162float(k[(row0 + r) * DK + c]) : 0.f;
-      const float d = bc[r] - bm, ep = __expf(d), em = __expf(-d);
-      sm.u.qp[r * FP + c] = qx * ep;
-      sm.kp[r * FP + c] = kx * ep;
-      sm.km[r * FP + c] = kx * em;
+    for (int r = 0; r < RPG; ++r) {
+      const int R = r0 + r;
+      const bool ok = R < n;
+      const float qx = ok ? __bfloat162float(q[(row0 + R) * DK + c]) : 0.f;
+      const float kx = ok ? __bfloat162float(k[(row0 + R) * DK + c]) : 0.f;
+      const float d = off + bc[r] - bm, ep = __expf(d), em = __expf(-d);
+      sm.u.qp[R * FP + c] = qx * ep;
+      sm.kp[R * FP + c] = kx * ep;
+      sm.km[R * FP + c] = kx * em;
       const float eb = ep * ebm;  // e^B and e^{B_L - B} for the chains' bf16 images
-      kh[ib + r * DK + c] = __float2bfloat16_rn(kx * eb);
-      qh[ib + r * DK + c] = __float2bfloat16_rn(qx * eb);
-      kt[ib + r * DK + c] = __float2bfloat16_rn(kx * (em * eblm));
+      kh[ib + R * DK + c] = __float2bfloat16_rn(kx * eb);
+      qh[ib + R * DK + c] = __float2bfloat16_rn(qx * eb);
+      kt[ib + R * DK + c] = __float2bfloat16_rn(kx * (em * eblm));
     }
   }
   __syncthreads();
-  // ---- [Q+; K+] K-^T: warps 0, 1 the rows of Q+ (P, stored at once), warps 2, 3 the rows of
-  //      K+ (A = Diag(beta) L, held until Q+ is dead)
-  const float *src = warp < 2 ? sm.u.qp : sm.kp;
-  const int rbase = (warp & 1) * 32;
-  float acc[2][8][4];
+  // ---- [Q+; K+] K-^T: warps 0..3 the rows of Q+ (P, stored at once), warps 4..7 the rows of
+  //      K+ (A = Diag(beta) L, held until Q+ is dead); warp w: rows 16 (w % 4)
+  const float *src = warp < 4 ? sm.u.qp : sm.kp;
+  const int m0 = 16 * (warp & 3);
+  float acc[8][4];
   const size_t cbase = ci * kCh * kCh;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    zero(acc[h]);
-    wmma(acc[h], rbase + 16 * h, 0, DK, [&](int m, int kk) { return tf(src[m * FP + kk]); },
-         [&](int kk, int nn) { return tf(sm.km[nn * FP + kk]); }, lane);
-    if (warp < 2)
-      each(acc[h], rbase + 16 * h, 0, lane, [&](int r, int s, float &v) {
-        const float x = s <= r ? v : 0.f;
-        Pw[cbase + r * kCh + s] = x;
-        Pb[cbase + r * kCh + s] = __float2bfloat16_rn(x);
-      });
-  }
+  zero(acc);
+  wmma(acc, m0, 0, DK, [&](int m, int kk) { return tf(src[m * FP + kk]); },
+       [&](int kk, int nn) { return tf(sm.km[nn * FP + kk]); }, lane);
+  if (warp < 4)
+    each(acc, m0, 0, lane, [&](int r, int s2, float &x) {
+      const float y = s2 <= r ? x : 0.f;
+      Pw[cbase + r * kCh + s2] = y;
+      Pb[cbase + r * kCh + s2] = __float2bfloat16_rn(y);
+    });
   __syncthreads();
-  if (warp >= 2) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-      each(acc[h], rbase + 16 * h, 0, lane,
-           [&](int r, int s, float &v) { cc(sm.u.a, r, s) = s < r ? sm.bet[r] * v : 0.f; });
-  }
+  if (warp >= 4)
+    each(acc, m0, 0, lane, [&](int r, int s2, float &x) { cc(sm.u.a, r, s2) = s2 < r ? sm.bet[r] * x : 0.f; });
   __syncthreads();
   // ---- T = (I + A)^{-1}: column j by forward substitution (as for Gated DeltaNet)
   if (tid < kCh) {
@@ -1233,7 +1243,7 @@ int launch_kda(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat
   if (e == cudaSuccess) e = set_smem<BwdSmem<DK, true>>(bd_bwd_kernel<DK, DV, true>);
   if (e == cudaSuccess) e = set_smem<KGradSmem<DK>>(bk_grad_kernel<DK, DV>);
   if (e == cudaSuccess) {
-    bk_pre_kernel<DK><<<dim3(nch, BH), 128, sizeof(KPreSmem<DK>), s>>>(q, k, g, beta, T, Tw, Pw, Tb, Pb, kh, kt, qh,
+    bk_pre_kernel<DK><<<dim3(nch, BH), 256, sizeof(KPreSmem<DK>), s>>>(q, k, g, beta, T, Tw, Pw, Tb, Pb, kh, kt, qh,
                                                                       gl);
     e = cudaGetLastError();
   }
