@@ -106,7 +106,7 @@ int select_variant(const ChunkParams &p, int *chunk_out) {
   if (p.f32) return (want == kVariantTc || want == kVariantMat) ? -2 : kVariantSimt;
   if (p.kind == kKda) {
     // the two-phase path (every chunk's key side in parallel, then the state chain per
-    // head and 32 value columns; la_chunk_kda_wy.cu), measured faster on GB300 than the
+    // head and 64 value columns; la_chunk_kda_wy.cu), measured faster on GB300 than the
     // fused sequential-phase kernel, which LA_VARIANT=tc or LA_KDA=tc selects
     if (want == kVariantMat || want == kVariantSimt) {
       set_error("la_chunk_fwd: LA_KDA runs on its two-phase path or the fused tensor-core kernel");

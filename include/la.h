@@ -367,11 +367,11 @@ int la_chunk_bwd_delta(const void *q, const void *k, const void *v, const float 
  *   S0, S_final  float32 [B][H][dk][dv] or NULL (zero / not written),
  *            16-byte aligned; S_final may alias S0
  *   C        0 or 64
- * Chunkwise (C = 64). bfloat16: two phases on tf32 warp MMAs -- every
- * chunk's key side in parallel (T = (I + L_ab)^{-1}, T A, T L_ak and the two
- * masked score matrices) into a workspace of B*H*ceil(T/64)*(64*dk + 3*64*64)*4
- * bytes from the library's pool, then the state chain per head and 16 value
- * columns; B*H <= 65535. float32 (LA_F32), or bfloat16 with the environment
+ * Chunkwise (C = 64). bfloat16: two phases on bf16 warp MMAs (fp32
+ * accumulate) -- every chunk's key side in parallel (T = (I + L_ab)^{-1}, T A,
+ * T L_ak and the two masked score matrices) into bf16 images, a workspace of
+ * B*H*ceil(T/64)*(64*dk + 3*64*64)*2 bytes from the library's pool, then the
+ * state chain per head and 16 value columns; B*H <= 65535. float32 (LA_F32), or bfloat16 with the environment
  * variable LA_GDELTA=simt: one pass on the CUDA cores in float32, no
  * workspace. Errors as la_chunk_fwd; asynchronous on `stream`.
  */

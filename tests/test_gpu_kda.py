@@ -1,9 +1,10 @@
 """GPU parity of Kimi Delta Attention (LA_KDA: Gated DeltaNet with a
 per-key-channel gate) against the float64 oracle, through the C ABI.
 
-The chunk forward runs on the sequential-phase tensor-core kernel with one
-stage; the decode step on the step kernel. Same tolerances as every other
-mode (tests/paritylib.py).
+The chunk forward runs on the two-phase path by default (every chunk's key
+side in parallel, then the state chain on bf16 warp MMAs) and on the fused
+tensor-core kernel with LA_KDA=tc; the decode step on the step kernel. Same
+tolerances as every other mode (tests/paritylib.py).
 """
 import numpy as np
 import pytest
