@@ -79,6 +79,7 @@ struct KwPreSmem {
     __nv_bfloat16 tpb[kCh * kCP];          // then T' (bf16), the W product's A operand
   } r3;
   float bet[kCh], bm[DK];
+  float gsum[(128 / (DK / 2)) * DK];  // the fold's row groups' gate sums per key channel
 };
 
 template <int DK>
@@ -101,34 +102,65 @@ __global__ void __launch_bounds__(128, 4) kdw_pre_kernel(const __nv_bfloat16 *__
   rows_async<DK, PH>(sm.kp, k + row0 * DK, n, tid, 128);
   cp_commit();
   if (tid < kCh) sm.bet[tid] = tid < n ? (beta ? __ldg(beta + row0 + tid) : 1.f) : 0.f;
-  // ---- channel c = tid: the prefix B[.][c] in registers (zero gates past the end)
-  float bc[kCh];
-  if (tid < DK) {
-    float acc = 0.f;
+  // ---- the fold: thread tid owns the key-channel pair (2 cp, 2 cp + 1) and RPG consecutive
+  //      rows; the prefix B[.][c] of its rows in registers, then the row groups' sums
+  constexpr int NP = DK / 2, RG = 128 / NP, RPG = kCh / RG;
+  const int cp = tid % NP, grp = tid / NP, r0 = grp * RPG, c = 2 * cp;
+  float2 bc[RPG];
+  {
+    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int r = 0; r < kCh; ++r) {
-      acc += r < n ? __ldg(g + (row0 + r) * DK + tid) : 0.f;
+    for (int r = 0; r < RPG; ++r) {
+      const float2 x = r0 + r < n ? __ldg(reinterpret_cast<const float2 *>(g + (row0 + r0 + r) * DK + c))
+                                  : make_float2(0.f, 0.f);
+      acc.x += x.x;
+      acc.y += x.y;
       bc[r] = acc;
     }
+    sm.gsum[grp * DK + c] = acc.x;
+    sm.gsum[grp * DK + c + 1] = acc.y;
   }
   cp_wait<0>();
   __syncthreads();
   // ---- folded rows: Q+, K+ (in place), K- (tiles), Q e^B and K e^{B_L - B} (workspace), e^{B_L}
-  if (tid < DK) {
-    const int c = tid;
-    const float bmid = bc[kMid], bl = bc[kCh - 1];
-    sm.bm[c] = bmid;
-    reinterpret_cast<float *>(wc + O::gl)[c] = __expf(bl);
-    bf16 *qt = reinterpret_cast<bf16 *>(wc + O::qt), *kt = reinterpret_cast<bf16 *>(wc + O::kt);
+  {
+    float2 off = make_float2(0.f, 0.f), bmid = off, bl = off;
 #pragma unroll
-    for (int r = 0; r < kCh; ++r) {
-      const float qx = bf(sm.r1.qp + r * PH + c), kx = bf(sm.kp + r * PH + c);
-      const float d = bc[r] - bmid, ep = __expf(d), em = __expf(-d);
-      sm.r1.qp[r * PH + c] = __float2bfloat16_rn(qx * ep);
-      sm.kp[r * PH + c] = __float2bfloat16_rn(kx * ep);
-      sm.r3.km[r * PH + c] = __float2bfloat16_rn(kx * em);
-      qt[r * DK + c] = __float2bfloat16_rn(qx * __expf(bc[r]));
-      kt[r * DK + c] = __float2bfloat16_rn(kx * __expf(bl - bc[r]));
+    for (int j = 0; j < RG; ++j) {
+      const float x0 = sm.gsum[j * DK + c], x1 = sm.gsum[j * DK + c + 1];
+      if (j < grp) {
+        off.x += x0;
+        off.y += x1;
+      }
+      if (j * RPG <= kMid) {  // the groups of rows 0 .. kMid
+        bmid.x += x0;
+        bmid.y += x1;
+      }
+      bl.x += x0;
+      bl.y += x1;
+    }
+    if (grp == 0) {
+      sm.bm[c] = bmid.x;
+      sm.bm[c + 1] = bmid.y;
+      *reinterpret_cast<float2 *>(wc + O::gl + 4 * c) = make_float2(__expf(bl.x), __expf(bl.y));
+    }
+    const float2 ebm = make_float2(__expf(bmid.x), __expf(bmid.y));
+    const float2 eblm = make_float2(__expf(bl.x - bmid.x), __expf(bl.y - bmid.y));
+    __nv_bfloat162 *qt = reinterpret_cast<__nv_bfloat162 *>(wc + O::qt),
+                   *kt = reinterpret_cast<__nv_bfloat162 *>(wc + O::kt);
+#pragma unroll
+    for (int r = 0; r < RPG; ++r) {
+      const int R = r0 + r;
+      const float2 qx = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(sm.r1.qp + R * PH + c));
+      const float2 kx = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(sm.kp + R * PH + c));
+      const float d0 = off.x + bc[r].x - bmid.x, d1 = off.y + bc[r].y - bmid.y;
+      const float ep0 = __expf(d0), ep1 = __expf(d1), em0 = __expf(-d0), em1 = __expf(-d1);
+      *reinterpret_cast<__nv_bfloat162 *>(sm.r1.qp + R * PH + c) = __floats2bfloat162_rn(qx.x * ep0, qx.y * ep1);
+      *reinterpret_cast<__nv_bfloat162 *>(sm.kp + R * PH + c) = __floats2bfloat162_rn(kx.x * ep0, kx.y * ep1);
+      *reinterpret_cast<__nv_bfloat162 *>(sm.r3.km + R * PH + c) = __floats2bfloat162_rn(kx.x * em0, kx.y * em1);
+      // e^B = EP e^{b_m}, e^{B_L - B} = EM e^{B_L - b_m}
+      qt[(R * DK + c) >> 1] = __floats2bfloat162_rn(qx.x * (ep0 * ebm.x), qx.y * (ep1 * ebm.y));
+      kt[(R * DK + c) >> 1] = __floats2bfloat162_rn(kx.x * (em0 * eblm.x), kx.y * (em1 * eblm.y));
     }
   }
   __syncthreads();
