@@ -796,12 +796,12 @@ __global__ void __launch_bounds__(256, 1) bd_grad_kernel(
 // images; the pre-pass and the gradient kernel form the folds in float32.
 
 // ---- pre-pass: the folds, P and T (float32 and bf16), the chains' images.
-// 256 threads: RG groups of threads per key channel, each folding RPG rows (the
-// prefix from the groups' gate sums), so that more loads are in flight per SM.
+// 256 threads: each folds one key-channel pair over RPG rows (RG row groups, the
+// prefix from the groups' gate sums), with paired bf16 and float loads and stores.
 template <int DK>
 struct KPreSmem {
   static constexpr int FP = DK + 4;  // float pitch: conflict-free tf32 fragment reads
-  static constexpr int RG = 256 / DK, RPG = kCh / RG;
+  static constexpr int RG = 256 / (DK / 2), RPG = kCh / RG;  // thread: a key-channel pair, RPG rows
   union {
     float qp[kCh * FP];  // Q+, then A
     float a[kCh * kPf];
@@ -827,45 +827,62 @@ __global__ void __launch_bounds__(256, 2) bk_pre_kernel(const __nv_bfloat16 *__r
   const int t0 = i * kCh, n = min(kCh, T - t0);
   const size_t row0 = (size_t)bh * T + t0, ci = (size_t)bh * nch + i;
   if (tid < kCh) sm.bet[tid] = tid < n ? (beta ? __ldg(beta + row0 + tid) : 1.f) : 0.f;
-  // ---- channel c, rows r0 .. r0 + RPG - 1: the local prefix in registers (zero gates past the end)
-  const int c = tid % DK, grp = tid / DK, r0 = grp * RPG;
-  float bc[RPG];
+  // ---- channels c, c + 1, rows r0 .. r0 + RPG - 1: the local prefix in registers (zero gates
+  //      past the end)
+  const int c = 2 * (tid % (DK / 2)), grp = tid / (DK / 2), r0 = grp * RPG;
+  float2 bc[RPG];
   {
-    float acc = 0.f;
+    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
     for (int r = 0; r < RPG; ++r) {
-      acc += r0 + r < n ? __ldg(g + (row0 + r0 + r) * DK + c) : 0.f;
+      const float2 x = r0 + r < n ? __ldg(reinterpret_cast<const float2 *>(g + (row0 + r0 + r) * DK + c))
+                                  : make_float2(0.f, 0.f);
+      acc.x += x.x;
+      acc.y += x.y;
       bc[r] = acc;
     }
-    sm.gsum[grp * DK + c] = acc;
+    sm.gsum[grp * DK + c] = acc.x;
+    sm.gsum[grp * DK + c + 1] = acc.y;
   }
   __syncthreads();
   {
-    float off = 0.f, bm = 0.f, bl = 0.f;
+    float2 off = make_float2(0.f, 0.f), bm = off, bl = off;
 #pragma unroll
     for (int j = 0; j < RG; ++j) {
-      const float x = sm.gsum[j * DK + c];
-      off += j < grp ? x : 0.f;
-      bm += j * RPG < kCh / 2 ? x : 0.f;  // B at row 31: the groups of rows 0 .. 31
-      bl += x;
+      const float x0 = sm.gsum[j * DK + c], x1 = sm.gsum[j * DK + c + 1];
+      if (j < grp) {
+        off.x += x0;
+        off.y += x1;
+      }
+      if (j * RPG < kCh / 2) {  // B at row 31: the groups of rows 0 .. 31
+        bm.x += x0;
+        bm.y += x1;
+      }
+      bl.x += x0;
+      bl.y += x1;
     }
-    const float ebm = __expf(bm), eblm = __expf(bl - bm);
-    if (grp == 0) gl[ci * DK + c] = __expf(bl);
+    const float2 ebm = make_float2(__expf(bm.x), __expf(bm.y)), eblm = make_float2(__expf(bl.x - bm.x), __expf(bl.y - bm.y));
+    if (grp == 0) *reinterpret_cast<float2 *>(gl + ci * DK + c) = make_float2(__expf(bl.x), __expf(bl.y));
     const size_t ib = ci * kCh * DK;
+    __nv_bfloat162 *kh2 = reinterpret_cast<__nv_bfloat162 *>(kh + ib), *qh2 = reinterpret_cast<__nv_bfloat162 *>(qh + ib),
+                   *kt2 = reinterpret_cast<__nv_bfloat162 *>(kt + ib);
 #pragma unroll
     for (int r = 0; r < RPG; ++r) {
       const int R = r0 + r;
       const bool ok = R < n;
-      const float qx = ok ? __bfloat162float(q[(row0 + R) * DK + c]) : 0.f;
-      const float kx = ok ? __bfloat162float(k[(row0 + R) * DK + c]) : 0.f;
-      const float d = off + bc[r] - bm, ep = __expf(d), em = __expf(-d);
-      sm.u.qp[R * FP + c] = qx * ep;
-      sm.kp[R * FP + c] = kx * ep;
-      sm.km[R * FP + c] = kx * em;
-      const float eb = ep * ebm;  // e^B and e^{B_L - B} for the chains' bf16 images
-      kh[ib + R * DK + c] = __float2bfloat16_rn(kx * eb);
-      qh[ib + R * DK + c] = __float2bfloat16_rn(qx * eb);
-      kt[ib + R * DK + c] = __float2bfloat16_rn(kx * (em * eblm));
+      const float2 qx = ok ? __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(q + (row0 + R) * DK + c))
+                           : make_float2(0.f, 0.f);
+      const float2 kx = ok ? __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(k + (row0 + R) * DK + c))
+                           : make_float2(0.f, 0.f);
+      const float d0 = off.x + bc[r].x - bm.x, d1 = off.y + bc[r].y - bm.y;
+      const float ep0 = __expf(d0), ep1 = __expf(d1), em0 = __expf(-d0), em1 = __expf(-d1);
+      *reinterpret_cast<float2 *>(sm.u.qp + R * FP + c) = make_float2(qx.x * ep0, qx.y * ep1);
+      *reinterpret_cast<float2 *>(sm.kp + R * FP + c) = make_float2(kx.x * ep0, kx.y * ep1);
+      *reinterpret_cast<float2 *>(sm.km + R * FP + c) = make_float2(kx.x * em0, kx.y * em1);
+      // e^B = EP e^{b_m} and e^{B_L - B} = EM e^{B_L - b_m} for the chains' bf16 images
+      kh2[(R * DK + c) >> 1] = __floats2bfloat162_rn(kx.x * (ep0 * ebm.x), kx.y * (ep1 * ebm.y));
+      qh2[(R * DK + c) >> 1] = __floats2bfloat162_rn(qx.x * (ep0 * ebm.x), qx.y * (ep1 * ebm.y));
+      kt2[(R * DK + c) >> 1] = __floats2bfloat162_rn(kx.x * (em0 * eblm.x), kx.y * (em1 * eblm.y));
     }
   }
   __syncthreads();
