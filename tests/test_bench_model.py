@@ -44,3 +44,26 @@ def test_backward_bytes_count_each_tensor_once():
     wg = workloads.WORKLOADS["backward_gla"]
     # GLA also reads g and writes dg, both float32 per key channel
     assert bench.backward_bytes(wg) / (wg.B * wg.H) == per_head + wg.T * 8 * 128
+
+
+def test_delta_rule_backward_bytes():
+    # Gated DeltaNet: q, k, v, dO read and dq, dk, dv written (bf16); g and beta read, dg and dbeta
+    # written (float32 per token); S0 and dS_final read and dS0 written (float32)
+    wl = workloads.WORKLOADS["backward_gdn"]
+    tok = 2 * (4 * 128 + 3 * 128) + 16
+    assert bench.backward_bytes(wl) == wl.B * wl.H * (wl.T * tok + 3 * 4 * 128 * 128)
+    # Kimi Delta Attention: the gate and its gradient per key channel instead of per token
+    wk = workloads.WORKLOADS["backward_kda"]
+    tok_k = 2 * (4 * 128 + 3 * 128) + 8 * 128 + 8
+    assert bench.backward_bytes(wk) == wk.B * wk.H * (wk.T * tok_k + 3 * 4 * 128 * 128)
+
+
+def test_kernel_sources_cover_every_workload_with_a_traffic_record():
+    # every traffic record names a workload whose kernels' sources are listed, so that
+    # the record's hash can be checked against them
+    import re
+    with open(bench.PROFILE_FILE) as f:
+        names = re.findall(r"^traffic workload=(\S+)", f.read(), flags=re.M)
+    assert names
+    for n in names:
+        assert n in bench.KERNEL_SOURCES, n
