@@ -317,7 +317,12 @@ int la_chunk_fwd(const void *q, const void *k, const void *v, const float *g, co
   if (variant == kVariantMat) {
     // stream-ordered workspace: allocated and released on the caller's stream
     void *ws = nullptr;
-    const size_t bytes = mat_workspace_bytes(p);
+    // linear and elu+1: the parallel state pass while its float32 chunk partials take
+    // at most 2 GiB (LA_MAT_STATE=serial keeps the serial one)
+    const char *ms = getenv("LA_MAT_STATE");
+    const size_t sb = mat_scan_bytes(p);
+    const bool scan = sb > 0 && sb <= (size_t(2) << 30) && !(ms && strcmp(ms, "serial") == 0);
+    const size_t bytes = mat_workspace_bytes(p) + (scan ? mat_scan_bytes(p) : 0);
     cudaMemPool_t pool = workspace_pool();
     if (!pool) {
       set_error("%s: could not create the workspace pool: %s", fn, cudaGetErrorString(cudaGetLastError()));
@@ -328,7 +333,7 @@ int la_chunk_fwd(const void *q, const void *k, const void *v, const float *g, co
       set_error("%s: workspace allocation of %zu bytes failed: %s", fn, bytes, cudaGetErrorString(e));
       return LA_ERR_CUDA;
     }
-    rc = launch_chunk_mat(p, ws, s);
+    rc = launch_chunk_mat(p, ws, s, scan);
     e = cudaFreeAsync(ws, s);
     if (rc == LA_OK && e != cudaSuccess) {
       set_error("%s: workspace release failed: %s", fn, cudaGetErrorString(e));

@@ -932,8 +932,13 @@ chunk_output128_kernel(const ChunkParams p, const uint8_t *__restrict__ ws, cons
 
 // ---------------------------------------------------------------- launch
 
+// the parallel state pass of the modes without decay (defined with the non-causal kernels it reuses)
 template <int DK, int DV, int KIND>
-int launch_typed(const ChunkParams &p, uint8_t *ws, float *zws, cudaStream_t stream) {
+cudaError_t launch_scan_state(const ChunkParams &p, uint8_t *ws, float *zws, const CUtensorMap &mk,
+                              const CUtensorMap &mv, cudaStream_t stream);
+
+template <int DK, int DV, int KIND>
+int launch_typed(const ChunkParams &p, uint8_t *ws, float *zws, bool scan, cudaStream_t stream) {
   const int BH = p.B * p.H, nch = (p.T + kC - 1) / kC;
   const ALayout La = a_layout(KIND, a_stages<KIND>());
   const BLayout Lb = b_layout(DK, KIND);
@@ -959,11 +964,16 @@ int launch_typed(const ChunkParams &p, uint8_t *ws, float *zws, cudaStream_t str
     return LA_ERR_CUDA;
   }
   auto ka = chunk_state_kernel<DK, DV, KIND>;
-  cudaError_t e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sa);
+  cudaError_t e = cudaSuccess;
   const int istride = p.C == kC2 ? 2 : 1;
-  if (e == cudaSuccess) {
-    ka<<<(unsigned)(BH * (DK / kKB)), kAThreads, sa, stream>>>(p, ws, zws, istride, mk, mv, mgA);
-    e = cudaGetLastError();
+  if (scan && (KIND == kLinear || KIND == kElu1)) {
+    e = launch_scan_state<DK, DV, KIND>(p, ws, zws, mk, mv, stream);
+  } else {
+    e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sa);
+    if (e == cudaSuccess) {
+      ka<<<(unsigned)(BH * (DK / kKB)), kAThreads, sa, stream>>>(p, ws, zws, istride, mk, mv, mgA);
+      e = cudaGetLastError();
+    }
   }
   if constexpr (KIND != kGla) {
     if (e == cudaSuccess && p.C == kC2) {
@@ -1003,11 +1013,11 @@ int launch_typed(const ChunkParams &p, uint8_t *ws, float *zws, cudaStream_t str
 }
 
 template <int KIND>
-int launch_kind(const ChunkParams &p, uint8_t *ws, float *zws, cudaStream_t stream) {
-  if (p.dk == 128 && p.dv == 128) return launch_typed<128, 128, KIND>(p, ws, zws, stream);
-  if (p.dk == 128 && p.dv == 64) return launch_typed<128, 64, KIND>(p, ws, zws, stream);
-  if (p.dk == 64 && p.dv == 128) return launch_typed<64, 128, KIND>(p, ws, zws, stream);
-  return launch_typed<64, 64, KIND>(p, ws, zws, stream);
+int launch_kind(const ChunkParams &p, uint8_t *ws, float *zws, bool scan, cudaStream_t stream) {
+  if (p.dk == 128 && p.dv == 128) return launch_typed<128, 128, KIND>(p, ws, zws, scan, stream);
+  if (p.dk == 128 && p.dv == 64) return launch_typed<128, 64, KIND>(p, ws, zws, scan, stream);
+  if (p.dk == 64 && p.dv == 128) return launch_typed<64, 128, KIND>(p, ws, zws, scan, stream);
+  return launch_typed<64, 64, KIND>(p, ws, zws, scan, stream);
 }
 
 // ================================================= non-causal forward
@@ -1236,6 +1246,105 @@ nc_finalize_kernel(const ChunkParams p, int nsplit, const float *__restrict__ pa
     zws[(size_t)bh * DK + tid] = z;
     if (p.S_final) p.S_final[((size_t)bh * DK + tid) * W + DV] = z;
   }
+}
+
+// Parallel state pass of the materialised variant for the modes without decay
+// (linear, elu+1): the state entering chunk i is S0 plus the sum of the earlier
+// chunks' K^T V (z: of their phi(k) sums), so nc_sum_kernel forms every 64-token
+// chunk's partial at once (one split per chunk) and mat_scan_kernel walks a
+// head's chunks for 16 value rows, writing the state at every image boundary as
+// the output pass's bf16 image (the serial state pass's layout: S^T rows, value
+// rows beyond dv zero), z there, and S_final. The partials' loads run
+// kScanDepth chunks ahead of the running sums.
+constexpr int kScanDepth = 4;
+
+template <int DK, int DV, bool ELU>
+__global__ void __launch_bounds__(256)
+mat_scan_kernel(const ChunkParams p, int nch, int istride, const float *__restrict__ part,
+                const float *__restrict__ zpart, uint8_t *__restrict__ ws, float *__restrict__ zws) {
+  constexpr int W = DV + (ELU ? 1 : 0);
+  constexpr int EPT = DK * kFRows / 256;  // running-sum elements per thread
+  __shared__ float tile[DK][kFRows + 1];
+  const int bh = blockIdx.x / (128 / kFRows), v0 = (blockIdx.x % (128 / kFRows)) * kFRows;
+  const int tid = threadIdx.x;
+  const int nimg = (nch + istride - 1) / istride;
+  const bool zthr = ELU && v0 == 0 && tid < DK;  // the thread of key channel tid's z
+  // element e of the thread: key channel (tid + 256 e) / 16, value row v0 + (tid + 256 e) % 16
+  int ce[EPT], ve[EPT];
+  float acc[EPT];
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    const int i = tid + 256 * e;
+    ce[e] = i / kFRows;
+    ve[e] = v0 + i % kFRows;
+    acc[e] = (p.S0 && ve[e] < DV) ? p.S0[((size_t)bh * DK + ce[e]) * W + ve[e]] : 0.f;
+  }
+  float z = (zthr && p.S0) ? p.S0[((size_t)bh * DK + tid) * W + DV] : 0.f;
+  const float *pp = part + (size_t)bh * nch * DV * DK;
+  const float *zp = ELU ? zpart + (size_t)bh * nch * DK : nullptr;
+  // the partials of chunks j .. j + kScanDepth - 1 in flight
+  float buf[kScanDepth][EPT], zbuf[kScanDepth];
+  auto load = [&](int j, float (&dst)[EPT], float &zdst) {
+#pragma unroll
+    for (int e = 0; e < EPT; ++e)
+      dst[e] = (j < nch && ve[e] < DV) ? __ldg(pp + (size_t)j * DV * DK + (size_t)ce[e] * DV + ve[e]) : 0.f;
+    zdst = (zthr && j < nch) ? __ldg(zp + (size_t)j * DK + tid) : 0.f;
+  };
+#pragma unroll
+  for (int d = 0; d < kScanDepth; ++d) load(d, buf[d], zbuf[d]);
+  for (int j0 = 0; j0 < nch; j0 += kScanDepth) {
+#pragma unroll
+    for (int d = 0; d < kScanDepth; ++d) {
+      const int j = j0 + d;
+      if (j >= nch) break;  // uniform across the CTA
+      if (j % istride == 0) {  // the state entering image j / istride
+        const int im_i = j / istride;
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) tile[ce[e]][ve[e] - v0] = acc[e];
+        if (zthr) zws[((size_t)bh * nimg + im_i) * DK + tid] = z;
+        __syncthreads();
+        uint8_t *im = ws + ((size_t)bh * nimg + im_i) * blob_bytes(DK);
+        for (int i = tid; i < kFRows * (DK / 2); i += 256) {
+          const int r = i / (DK / 2), c = 2 * (i % (DK / 2));
+          *reinterpret_cast<__nv_bfloat162 *>(im + (size_t)(c >> 6) * 16384u + sw128_off(v0 + r, c & 63)) =
+              __floats2bfloat162_rn(tile[c][r], tile[c + 1][r]);
+        }
+        __syncthreads();
+      }
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) acc[e] += buf[d][e];
+      z += zbuf[d];
+      load(j + kScanDepth, buf[d], zbuf[d]);
+    }
+  }
+  if (p.S_final) {
+#pragma unroll
+    for (int e = 0; e < EPT; ++e)
+      if (ve[e] < DV) p.S_final[((size_t)bh * DK + ce[e]) * W + ve[e]] = acc[e];
+    if (zthr) p.S_final[((size_t)bh * DK + tid) * W + DV] = z;
+  }
+}
+
+template <int DK, int DV, int KIND>
+cudaError_t launch_scan_state(const ChunkParams &p, uint8_t *ws, float *zws, const CUtensorMap &mk,
+                              const CUtensorMap &mv, cudaStream_t stream) {
+  constexpr bool ELU = KIND == kElu1;
+  const int BH = p.B * p.H, nch = (p.T + kC - 1) / kC, istride = p.C == kC2 ? 2 : 1;
+  float *part = reinterpret_cast<float *>(ws + mat_workspace_bytes(p));  // [B*H][nch][dk][dv], after the images
+  float *zpart = part + (size_t)BH * nch * DV * DK;                   // [B*H][nch][dk] (elu+1)
+  const size_t sn = n_layout(DK, ELU).total + 1024;
+  auto ka = nc_sum_kernel<DK, DV, ELU>;
+  cudaError_t e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sn);
+  if (e == cudaSuccess) {
+    ka<<<(unsigned)((size_t)BH * nch), kNThreads, sn, stream>>>(p, nch, part, zpart, mk, mv);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) {
+    mat_scan_kernel<DK, DV, ELU><<<(unsigned)(BH * (128 / kFRows)), 256, 0, stream>>>(p, nch, istride, part, zpart,
+                                                                                      ws, zws);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 // Output of the non-causal form: persistent CTAs (two per SM) each walk a
@@ -1506,7 +1615,13 @@ size_t mat_workspace_bytes(const ChunkParams &p) {
   return b;
 }
 
-int launch_chunk_mat(const ChunkParams &p, void *workspace, cudaStream_t stream) {
+size_t mat_scan_bytes(const ChunkParams &p) {
+  if (p.kind != kLinear && p.kind != kElu1) return 0;
+  const size_t nch = (size_t)(p.T + kC - 1) / kC, BH = (size_t)p.B * p.H;
+  return BH * nch * (size_t)p.dv * p.dk * sizeof(float) + (p.kind == kElu1 ? BH * nch * p.dk * sizeof(float) : 0);
+}
+
+int launch_chunk_mat(const ChunkParams &p, void *workspace, cudaStream_t stream, bool scan) {
   if (!encode_fn()) {
     set_error("la_chunk_fwd: cuTensorMapEncodeTiled is unavailable");
     return LA_ERR_CUDA;
@@ -1520,11 +1635,11 @@ int launch_chunk_mat(const ChunkParams &p, void *workspace, cudaStream_t stream)
   const size_t nch = (size_t)(p.T + c - 1) / c, BH = (size_t)p.B * p.H;
   float *zws = (p.kind == kElu1) ? reinterpret_cast<float *>(ws + BH * nch * blob_bytes(p.dk)) : nullptr;
   switch (p.kind) {
-    case kLinear: return launch_kind<kLinear>(p, ws, zws, stream);
-    case kElu1: return launch_kind<kElu1>(p, ws, zws, stream);
-    case kRetnet: return launch_kind<kRetnet>(p, ws, zws, stream);
-    case kScalar: return launch_kind<kScalar>(p, ws, zws, stream);
-    case kGla: return launch_kind<kGla>(p, ws, zws, stream);
+    case kLinear: return launch_kind<kLinear>(p, ws, zws, scan, stream);
+    case kElu1: return launch_kind<kElu1>(p, ws, zws, scan, stream);
+    case kRetnet: return launch_kind<kRetnet>(p, ws, zws, false, stream);
+    case kScalar: return launch_kind<kScalar>(p, ws, zws, false, stream);
+    case kGla: return launch_kind<kGla>(p, ws, zws, false, stream);
     default:
       set_error("la_chunk_fwd: the materialised variant covers the unit-write modes only");
       return LA_ERR_UNSUPPORTED;

@@ -103,9 +103,13 @@ int launch_chunk_delta(const ChunkParams &p, cudaStream_t stream);
 int launch_chunk_delta_pair(const ChunkParams &p, cudaStream_t stream);
 int launch_step(const StepParams &p, cudaStream_t stream);
 // Materialised (two-phase) variant: chunk-state pass then a parallel output
-// pass, through a caller-provided workspace of mat_workspace_bytes(p) bytes.
+// pass, through a caller-provided workspace of mat_workspace_bytes(p) bytes;
+// with scan set (linear and elu+1 only; the workspace then has
+// mat_scan_bytes(p) more) the state pass runs as every chunk's partial at once
+// plus a prefix scan instead of one serial walk per head.
 size_t mat_workspace_bytes(const ChunkParams &p);
-int launch_chunk_mat(const ChunkParams &p, void *workspace, cudaStream_t stream);
+size_t mat_scan_bytes(const ChunkParams &p);
+int launch_chunk_mat(const ChunkParams &p, void *workspace, cudaStream_t stream, bool scan = false);
 // Non-causal forward (LA_NONCAUSAL; linear and elu+1, bf16): split-T state
 // reduction, finalize, parallel output pass, through a caller-provided
 // workspace of nc_workspace_bytes(p) bytes.

@@ -1,8 +1,10 @@
 """GPU parity of the materialised (two-phase) variant against the float64 oracle.
 
-The variant writes every chunk's incoming state to a workspace in a serial
-state pass and then computes all chunks' outputs in parallel; it covers the
-unit-write modes (everything but the delta rule). It is selected with
+The variant writes every chunk's incoming state to a workspace in a state
+pass (serial per head; for linear and elu+1 attention every chunk's K^T V at
+once and a prefix scan, unless LA_MAT_STATE=serial) and then computes all
+chunks' outputs in parallel; it covers the unit-write modes (everything but
+the delta rule). It is selected with
 LA_VARIANT=mat and must agree with the oracle to the same tolerance as the
 fused kernel, and with the fused kernel itself.
 """
@@ -206,3 +208,22 @@ def test_c128_full_size_workload_sampled_heads(name):
     assert_close(o_got, o_ref, wl.dtype, f"{name} C=128 o (sampled heads)")
     assert_close(S_got, S_ref, wl.dtype, f"{name} C=128 S_final (sampled heads)")
     assert torch.isfinite(o.float()).all()
+
+
+@pytest.mark.parametrize("mode", ["linear", "elu1"])
+@pytest.mark.parametrize("C", [64, 128])
+@pytest.mark.parametrize("dims", [(128, 128), (64, 64)])
+def test_parallel_state_pass_matches_oracle_and_serial_pass(mode, C, dims, mat, monkeypatch):
+    # linear and elu+1: the parallel state pass (every chunk's partial, then a prefix
+    # scan into the images) against the oracle and the serial walk; S0 given, a tail
+    # chunk, several images per head
+    dk, dv = dims
+    inp = _inputs(mode, "bf16", B=2, H=3, T=777, dk=dk, dv=dv)
+    o, S = run_cuda(inp, C=C)
+    o_ref, S_ref = run_oracle(inp)
+    assert_close(f64(o), o_ref, "bf16", f"{mode} C={C} parallel o")
+    assert_close(f64(S), S_ref, "bf16", f"{mode} C={C} parallel S_final")
+    monkeypatch.setenv("LA_MAT_STATE", "serial")
+    o_s, S_s = run_cuda(inp, C=C)
+    assert_close(f64(o), f64(o_s), "bf16", f"{mode} C={C} parallel vs serial o")
+    assert_close(f64(S), f64(S_s), "bf16", f"{mode} C={C} parallel vs serial S_final")

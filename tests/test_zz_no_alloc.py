@@ -84,9 +84,13 @@ def test_noalloc_matches_materialised_entry_point_on_two_calls(lib, mode, monkey
     cases = []
     for B, H, T, seed in shapes:
         wl, d = _inputs(mode, B, H, T, seed)
+        # the no-alloc entry point walks the chunk states serially; elu+1 and linear
+        # attention otherwise take the parallel state pass, which sums in another order
         monkeypatch.setenv("LA_VARIANT", "mat")
+        monkeypatch.setenv("LA_MAT_STATE", "serial")
         o_ref, S_ref = la.chunk_fwd(d["q"], d["k"], d["v"], wl.mode, g=d["g"], S0=d["S0"])
         monkeypatch.delenv("LA_VARIANT")
+        monkeypatch.delenv("LA_MAT_STATE")
         o = torch.full_like(o_ref, float("nan"))
         S = torch.full_like(S_ref, float("nan"))
         cases.append((B, H, T, wl, d, o_ref, S_ref, o, S))
@@ -108,10 +112,12 @@ def test_noalloc_matches_materialised_entry_point_on_two_calls(lib, mode, monkey
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("mode", ["retnet", "elu1"])
-def test_noalloc_c128_matches_entry_point(lib, mode):
+def test_noalloc_c128_matches_entry_point(lib, mode, monkeypatch):
     stream = torch.cuda.current_stream()
     wl, d = _inputs(mode, 1, 4, 1000, 13)
+    monkeypatch.setenv("LA_MAT_STATE", "serial")  # the no-alloc entry point's state pass
     o_ref, S_ref = la.chunk_fwd(d["q"], d["k"], d["v"], wl.mode, g=d["g"], S0=d["S0"], C=128)
+    monkeypatch.delenv("LA_MAT_STATE")
     o = torch.full_like(o_ref, float("nan"))
     S = torch.full_like(S_ref, float("nan"))
     rc = la.la_chunk_fwd_noalloc(d["q"], d["k"], d["v"], d["g"], None, o, d["S0"], S,
