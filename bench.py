@@ -89,12 +89,24 @@ def is_noncausal(wl) -> bool:
     return bool(wl.extra.get("noncausal"))
 
 
+def parallel_state_pass(wl) -> bool:
+    """Whether the materialised variant's state pass runs as every chunk's partial
+    plus a prefix scan (linear and elu+1, partials up to 2 GiB, unless
+    LA_MAT_STATE=serial): three launches a call instead of two."""
+    part = wl.B * wl.H * ((wl.T + 63) // 64) * wl.dk * (wl.dv * 4 + (4 if wl.mode == "elu1" else 0))
+    return (wl.mode in ("linear", "elu1") and part <= (2 << 30)
+            and os.environ.get("LA_MAT_STATE") != "serial")
+
+
 def kernel_name(wl, variant=None, sm_count=152) -> str:
     """The kernel one la_chunk_fwd launch of this workload runs."""
     if is_noncausal(wl):
         return "nc_sum_kernel+nc_finalize_kernel+nc_out_kernel"
     if uses_materialised(wl, variant, sm_count):
-        return "chunk_state_kernel+" + ("chunk_output128_kernel" if mat_chunk(wl) == 128 else "chunk_output_kernel")
+        out = "chunk_output128_kernel" if mat_chunk(wl) == 128 else "chunk_output_kernel"
+        if parallel_state_pass(wl):
+            return "nc_sum_kernel+mat_scan_kernel+" + out
+        return "chunk_state_kernel+" + out
     if wl.dtype == "f32" or variant == "simt":
         return "chunk_simt_kernel"
     if wl.mode == "kda":
@@ -477,7 +489,8 @@ def main():
             "cpu_baseline": cpu,
             "clocks": clk,
             "e2e": e2e,
-            "gpu_launches": args.steps * (3 if is_noncausal(wl) else (2 if mat else 1)),
+            "gpu_launches": args.steps * (3 if is_noncausal(wl) else
+                                          ((3 if parallel_state_pass(wl) else 2) if mat else 1)),
         }
         print(json.dumps(line), flush=True)
     if dist:
