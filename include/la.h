@@ -157,10 +157,15 @@ typedef struct CUstream_st *la_stream_t;
  * Kernel variants ("Talk Linear Attention" section 4.1.2). Fused: one CTA per
  * head walks the chunks, keeping the state on chip; nothing but q, k, v, o and
  * the states touches memory. Materialised (unit-write modes, bfloat16): a
- * serial pass writes every chunk's incoming state to a workspace of
+ * state pass writes every chunk's incoming state to a workspace of
  * B*H*ceil(T/C)*dk*256 bytes (plus B*H*ceil(T/C)*dk*4 for LA_ELU1_NORM),
  * then all chunks' outputs are computed in parallel; it wins when B*H is too
- * small to fill the GPU. The choice is made per shape: materialised for the
+ * small to fill the GPU. The state pass walks each head's chunks in order,
+ * except for LA_LINEAR and LA_ELU1_NORM, whose chunk states are prefix sums:
+ * there every 64-token chunk's K^T V is formed at once into
+ * B*H*ceil(T/64)*dk*dv*4 more bytes of workspace (plus B*H*ceil(T/64)*dk*4
+ * for LA_ELU1_NORM) and a scan adds them up, while those take at most 2 GiB
+ * (the environment variable LA_MAT_STATE=serial keeps the serial walk). The choice is made per shape: materialised for the
  * unit-write modes when T >= 512 and B*H <= SMs / 2 (GLA: SMs / 4; elu+1:
  * any B*H), fused otherwise; with C = 0 the materialised variant runs C = 128
  * for LA_LINEAR and LA_ELU1_NORM, and for LA_RETNET and LA_SCALAR_GATE when
