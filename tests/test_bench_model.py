@@ -67,3 +67,19 @@ def test_kernel_sources_cover_every_workload_with_a_traffic_record():
     assert names
     for n in names:
         assert n in bench.KERNEL_SOURCES, n
+
+
+def test_kernel_names_follow_the_library_choice(monkeypatch):
+    # the materialised variant of elu+1 (any B*H) takes the parallel state pass unless
+    # LA_MAT_STATE=serial; RetNet's materialised pass stays serial; the delta rule and KDA
+    # name their own kernels
+    elu = workloads.WORKLOADS["elu1"]
+    assert bench.kernel_name(elu) == "nc_sum_kernel+mat_scan_kernel+chunk_output_kernel"
+    monkeypatch.setenv("LA_MAT_STATE", "serial")
+    assert bench.kernel_name(elu) == "chunk_state_kernel+chunk_output_kernel"
+    monkeypatch.delenv("LA_MAT_STATE")
+    assert bench.kernel_name(workloads.WORKLOADS["gdn"]) == "chunk_delta_pair_kernel"
+    assert bench.kernel_name(workloads.WORKLOADS["kda"]) == "kdw_pre_kernel+kdw_chain_kernel"
+    small_retnet = workloads.WORKLOADS["retnet"].with_sizes(B=1, H=8, T=4096)
+    assert bench.kernel_name(small_retnet).startswith("chunk_state_kernel+")
+    assert not bench.parallel_state_pass(small_retnet)
